@@ -1,0 +1,286 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is checked against things other than itself: a worked example
+derived by hand, brute-force enumeration of the allowed-pair rule with
+Python sets, special cases that reduce to a library routine
+(torch scaled_dot_product_attention in float64 with a causal, band or
+explicit mask; numpy stable argsort; numpy bincount/cumsum), and closed
+forms for the pair counts.  Each case is chosen so that a plausible slip in
+the oracle (window off by one, dropped causality, wrong GQA head map, wrong
+scale, transposed projection, wrong tie-break) fails at least one test.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from learned_group_sparse_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def _bf16_bits(x):
+    return synth.bits(torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16))
+
+
+def _rand_bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(torch.bfloat16)
+
+
+def _brute_allowed(ids, window):
+    """Boolean [B, n, n] allowed-pair matrix by enumeration with Python sets."""
+    B, n, _ = ids.shape
+    A = np.zeros((B, n, n), dtype=bool)
+    for b in range(B):
+        sets = [set(int(g) for g in ids[b, i]) for i in range(n)]
+        for i in range(n):
+            for j in range(i + 1):
+                A[b, i, j] = (i - j < window) or bool(sets[i] & sets[j])
+    return A
+
+
+def _sdpa(Q, K, V, mask=None, causal=False):
+    """torch SDPA in float64 on [B, n, H, d] bf16 inputs (GQA by repeat)."""
+    q = Q.double().permute(0, 2, 1, 3)
+    k = K.double().permute(0, 2, 1, 3)
+    v = V.double().permute(0, 2, 1, 3)
+    rep = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(rep, dim=1)
+    v = v.repeat_interleave(rep, dim=1)
+    m = None if mask is None else torch.as_tensor(mask)[:, None, :, :]
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, is_causal=causal)
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+def _lse(Q, K, mask):
+    q = Q.double().permute(0, 2, 1, 3)
+    k = K.double().permute(0, 2, 1, 3)
+    k = k.repeat_interleave(q.shape[1] // k.shape[1], dim=1)
+    s = (q @ k.transpose(-1, -2)) / np.sqrt(q.shape[-1])
+    s = s.masked_fill(~torch.as_tensor(mask)[:, None], float("-inf"))
+    return torch.logsumexp(s, dim=-1).permute(0, 2, 1).numpy()
+
+
+def _qkv(B, n, Hq, Hkv, d, seed):
+    return (_rand_bf16((B, n, Hq, d), seed), _rand_bf16((B, n, Hkv, d), seed + 1),
+            _rand_bf16((B, n, Hkv, d), seed + 2))
+
+
+def _run(Q, K, V, ids, window, rows=None):
+    return oracle.attention(synth.bits(Q), synth.bits(K), synth.bits(V), ids, window, rows=rows)
+
+
+def _rand_ids(B, n, K, topk, seed):
+    rng = np.random.default_rng(seed)
+    ids = np.empty((B, n, topk), np.int32)
+    for b in range(B):
+        for i in range(n):
+            ids[b, i] = rng.choice(K, size=topk, replace=False)
+    return ids
+
+
+# ------------------------------------------------------------ hand example ---
+
+def test_hand_worked_example():
+    ex = json.load(open(os.path.join(GOLDEN, "hand_worked_example.json")))
+    n, d = ex["n"], ex["d"]
+    ids = np.array(ex["ids"], np.int32).reshape(1, n, 1)
+    Q = torch.zeros(1, n, 1, d, dtype=torch.bfloat16)
+    K = _rand_bf16((1, n, 1, d), 3)                 # irrelevant when Q = 0
+    V = torch.tensor(ex["V"], dtype=torch.float32).view(1, n, 1, d).to(torch.bfloat16)
+    O, L = _run(Q, K, V, ids, ex["window"])
+    np.testing.assert_allclose(O[0, :, 0], np.array(ex["O"]), rtol=0, atol=1e-6)
+    np.testing.assert_allclose(L[0, :, 0], np.log(np.array(ex["count"], float)), atol=1e-6)
+    per, tot = oracle.count_pairs(ids, ex["window"])
+    assert per[0].tolist() == ex["count"] and tot == sum(ex["count"])
+    A = _brute_allowed(ids, ex["window"])[0]
+    assert [list(np.nonzero(A[i])[0]) for i in range(n)] == ex["allowed"]
+
+
+# -------------------------------------------------------------- mask pins ---
+
+@pytest.mark.parametrize("n,K,topk,window,seed", [
+    (40, 6, 2, 5, 0), (37, 3, 1, 1, 1), (33, 9, 3, 0, 2), (48, 5, 2, 7, 3), (20, 4, 4, 3, 4)])
+def test_mask_by_one_hot_values(n, K, topk, window, seed):
+    """Q = 0 and V[j] = e_j expose the allowed set: O[i, j] = 1/|A_i| on it."""
+    B = 2
+    ids = _rand_ids(B, n, K, topk, seed)
+    d = 64
+    Q = torch.zeros(B, n, 1, d, dtype=torch.bfloat16)
+    Kt = _rand_bf16((B, n, 1, d), seed)
+    V = torch.zeros(B, n, 1, d)
+    for j in range(n):
+        V[:, j, 0, j] = 1.0
+    O, _ = _run(Q, Kt, V.to(torch.bfloat16), ids, window)
+    A = _brute_allowed(ids, window)
+    expect = A / A.sum(-1, keepdims=True)
+    np.testing.assert_allclose(O[:, :, 0, :n], expect, atol=1e-6)
+    per, tot = oracle.count_pairs(ids, window)
+    assert (per == A.sum(-1)).all() and tot == int(A.sum())
+
+
+# ------------------------------------------ reductions to library routines ---
+
+@pytest.mark.parametrize("case", ["one_group", "topk_eq_K", "window_ge_n"])
+def test_reduces_to_dense_causal(case):
+    B, n, Hq, Hkv, d = 2, 70, 4, 2, 32
+    Q, K, V = _qkv(B, n, Hq, Hkv, d, 11)
+    if case == "one_group":
+        ids, window = np.zeros((B, n, 1), np.int32), 3
+    elif case == "topk_eq_K":
+        ids, window = _rand_ids(B, n, 3, 3, 5), 2
+    else:
+        ids, window = _rand_ids(B, n, 16, 1, 6), n
+    O, L = _run(Q, K, V, ids, window)
+    ref = _sdpa(Q, K, V, causal=True)
+    np.testing.assert_allclose(O, ref, atol=2e-6)
+    causal = np.tril(np.ones((n, n), bool))[None].repeat(B, 0)
+    np.testing.assert_allclose(L, _lse(Q, K, causal), atol=2e-5)
+
+
+@pytest.mark.parametrize("window", [1, 4, 9])
+def test_disjoint_groups_reduce_to_sliding_window(window):
+    B, n, H, d = 1, 64, 3, 16
+    Q, K, V = _qkv(B, n, H, H, d, 21)
+    ids = np.arange(n, dtype=np.int32).reshape(1, n, 1)      # K = n, nobody shares
+    O, _ = _run(Q, K, V, ids, window)
+    band = torch.ones(n, n).tril().bool() & ~torch.ones(n, n).tril(-window).bool()
+    ref = _sdpa(Q, K, V, mask=band[None])
+    np.testing.assert_allclose(O, ref, atol=2e-6)
+
+
+@pytest.mark.parametrize("window", [0, 1])
+def test_no_window_reduces_to_per_group_causal(window):
+    """With no window and top-1 groups, each group is plain causal attention
+    over its own gathered rows."""
+    B, n, H, d, K = 1, 90, 2, 32, 4
+    Q, Kt, V = _qkv(B, n, H, H, d, 31)
+    ids = _rand_ids(B, n, K, 1, 9)
+    O, _ = _run(Q, Kt, V, ids, window)
+    ref = np.zeros_like(O)
+    for g in range(K):
+        rows = np.nonzero(ids[0, :, 0] == g)[0]
+        if len(rows) == 0:
+            continue
+        r = torch.as_tensor(rows)
+        ref[0, rows] = _sdpa(Q[:, r], Kt[:, r], V[:, r], causal=True)[0]
+    np.testing.assert_allclose(O, ref, atol=2e-6)
+
+
+@pytest.mark.parametrize("Hq,Hkv,topk,K,window", [(4, 2, 2, 5, 6), (6, 3, 3, 7, 2), (4, 1, 1, 3, 10)])
+def test_explicit_mask_sdpa(Hq, Hkv, topk, K, window):
+    """Random ids, GQA: equal to SDPA with the brute-force boolean mask; the
+    log-sum-exp equals torch.logsumexp over the masked scores."""
+    B, n, d = 2, 100, 64
+    Q, Kt, V = _qkv(B, n, Hq, Hkv, d, 41)
+    ids = _rand_ids(B, n, K, topk, 13)
+    A = _brute_allowed(ids, window)
+    O, L = _run(Q, Kt, V, ids, window)
+    np.testing.assert_allclose(O, _sdpa(Q, Kt, V, mask=A), atol=2e-6)
+    np.testing.assert_allclose(L, _lse(Q, Kt, A), atol=2e-5)
+
+
+def test_rows_subset_matches_full():
+    B, n, H, d = 2, 80, 2, 32
+    Q, K, V = _qkv(B, n, H, H, d, 51)
+    ids = _rand_ids(B, n, 6, 2, 17)
+    O, L = _run(Q, K, V, ids, 5)
+    rows = np.array([0, 79, 80, 123, 159, 4], np.int64)
+    Os, Ls = _run(Q, K, V, ids, 5, rows=rows)
+    np.testing.assert_array_equal(Os, O.reshape(B * n, H, d)[rows])
+    np.testing.assert_array_equal(Ls, L.reshape(B * n, H)[rows])
+
+
+def test_rows_sum_to_one():
+    B, n, H, d = 1, 64, 2, 16
+    Q, K, _ = _qkv(B, n, H, H, d, 61)
+    V = torch.ones(B, n, H, d, dtype=torch.bfloat16)
+    O, _ = _run(Q, K, V, _rand_ids(B, n, 4, 2, 19), 3)
+    np.testing.assert_allclose(O, 1.0, atol=1e-6)
+
+
+# ------------------------------------------------------------- count pins ---
+
+def test_count_closed_forms():
+    n = 200
+    i = np.arange(n)
+    per, tot = oracle.count_pairs(np.zeros((1, n, 1), np.int32), 7)
+    assert (per[0] == i + 1).all() and tot == n * (n + 1) // 2
+    per, _ = oracle.count_pairs(np.arange(n, dtype=np.int32).reshape(1, n, 1), 7)
+    assert (per[0] == np.minimum(7, i + 1)).all()
+    per, _ = oracle.count_pairs(np.arange(n, dtype=np.int32).reshape(1, n, 1), 0)
+    assert (per[0] == 1).all()          # only the token itself (its own group)
+
+
+# ------------------------------------------------------------ assign pins ---
+
+def test_assign_closed_form_identity_projection():
+    """hidden = d_g, W_g = I, C = I: the scores are x itself, so the top-k is
+    the k largest entries of x, ties to the lower index."""
+    x = np.array([[0.5, 2.0, -1.0, 2.0, 3.0], [1.0, 1.0, 1.0, 1.0, 1.0],
+                  [-4.0, -3.0, -2.0, -1.0, -0.5]], np.float32)
+    ids, margin, scores = oracle.assign(_bf16_bits(x), np.eye(5, dtype=np.float32),
+                                        np.eye(5, dtype=np.float32), 2)
+    assert ids.tolist() == [[4, 1], [0, 1], [4, 3]]
+    np.testing.assert_array_equal(scores, x)
+    np.testing.assert_allclose(margin, [0.0, 0.0, 0.5])
+
+
+def test_assign_duplicate_centroid_tie_goes_to_lower_id():
+    rng = np.random.default_rng(3)
+    C = rng.standard_normal((6, 8)).astype(np.float32)
+    C[4] = C[1]
+    X = _bf16_bits(rng.standard_normal((50, 8)))
+    ids, margin, scores = oracle.assign(X, np.eye(8, dtype=np.float32), C, 6)
+    for t in range(50):
+        order = list(ids[t])
+        assert order.index(1) < order.index(4)
+
+
+def test_assign_matches_numpy_argsort():
+    rng = np.random.default_rng(5)
+    hidden, dg, K, topk = 96, 24, 20, 3
+    X = _rand_bf16((2, 30, hidden), 77)
+    Wg = (rng.standard_normal((hidden, dg)) / np.sqrt(hidden)).astype(np.float32)
+    C = rng.standard_normal((K, dg)).astype(np.float32)
+    ids, margin, scores = oracle.assign(synth.bits(X), Wg, C, topk)
+    s = (X.double().numpy() @ Wg.astype(np.float64)) @ C.astype(np.float64).T
+    np.testing.assert_allclose(scores, s, rtol=1e-6, atol=1e-6)
+    order = np.argsort(-scores, axis=-1, kind="stable")[..., :topk]
+    np.testing.assert_array_equal(ids, order)
+    srt = -np.sort(-scores, axis=-1)[..., :topk + 1]
+    np.testing.assert_allclose(margin, np.min(srt[..., :-1] - srt[..., 1:], axis=-1))
+
+
+def test_assign_ranking_invariant_to_positive_scale():
+    rng = np.random.default_rng(8)
+    X = _rand_bf16((40, 32), 99)
+    Wg = rng.standard_normal((32, 16)).astype(np.float32)
+    C = rng.standard_normal((10, 16)).astype(np.float32)
+    a, _, _ = oracle.assign(synth.bits(X), Wg, C, 4)
+    b, _, _ = oracle.assign(synth.bits(X), Wg * 2, C * 0.5, 4)
+    np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------ bucket pins ---
+
+@pytest.mark.parametrize("B,n,K,topk", [(2, 257, 7, 2), (1, 33, 40, 1), (3, 100, 4, 4)])
+def test_bucket_matches_numpy(B, n, K, topk):
+    ids = _rand_ids(B, n, K, topk, 23)
+    off, pos, inv = oracle.bucket(ids, K)
+    for b in range(B):
+        cnt = np.bincount(ids[b].ravel(), minlength=K)
+        np.testing.assert_array_equal(off[b], np.concatenate([[0], np.cumsum(cnt)]))
+        for g in range(K):
+            members = np.nonzero((ids[b] == g).any(-1))[0]
+            np.testing.assert_array_equal(pos[b, off[b, g]:off[b, g + 1]], members)
+        flat_tok = np.repeat(np.arange(n), topk)
+        np.testing.assert_array_equal(pos[b][inv[b].ravel()], flat_tok)
+        grp = np.searchsorted(off[b], inv[b].ravel(), side="right") - 1
+        np.testing.assert_array_equal(grp, ids[b].ravel())
