@@ -1,0 +1,225 @@
+/*
+ * focus.h -- C ABI of the Focus attention inference path on GB300 (sm_103a).
+ *
+ * Focus (arXiv 2604.03260, "Why Attend to Everything? Focus is the Key")
+ * restricts causal attention to the token pairs (i, j), j <= i, that lie in a
+ * local window (i - j < window) or share at least one of their top-k learned
+ * centroid groups.  Sources, web summaries of the paper:
+ *   gist.science/zh, technical summary 2.1.1 (token grouping), 2.1.2 (gated
+ *   attention: local window or shared group), 2.1.3 (inference: hard top-k
+ *   groups, within-group causal attention plus cross-group local attention);
+ *   gist.science/nl, Technische samenvatting, Kerncomponenten 1, 3, 4.
+ *
+ * Conventions shared by every entry point
+ *   - Data pointers are DEVICE pointers to caller-owned memory unless a
+ *     function says otherwise; all must be 16-byte aligned.  The library never
+ *     allocates, frees or synchronises; it only enqueues work on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).
+ *   - bf16 tensors are passed as `const void *` (IEEE bfloat16, row-major).
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     non-zero status means nothing was enqueued, except FOCUS_ERR_CUDA, which
+ *     reports a launch error (work enqueued before it may still run).
+ *   - Device-side waits inside the kernels are bounded.  A wait that runs out
+ *     makes the kernel finish early and records FOCUS_ERR_TIMEOUT in a device
+ *     status word, read with focus_get_device_status().
+ *   - Index types are int32: B * n * topk must stay below 2^31.
+ */
+#ifndef FOCUS_GB300_H
+#define FOCUS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int focus_status_t;
+#define FOCUS_OK                 0
+#define FOCUS_ERR_INVALID_ARG    1   /* null/misaligned pointer, bad size   */
+#define FOCUS_ERR_UNSUPPORTED    2   /* valid but outside supported shapes  */
+#define FOCUS_ERR_WORKSPACE      3   /* workspace smaller than required     */
+#define FOCUS_ERR_CUDA           4   /* a CUDA runtime/launch error         */
+#define FOCUS_ERR_TIMEOUT        5   /* a bounded device wait ran out       */
+
+/* Human-readable name of a status code (static storage). */
+const char *focus_status_string(focus_status_t status);
+
+/* Library version string, e.g. "focus-gb300 0.1.0 sm_103a". */
+const char *focus_version(void);
+
+/*
+ * focus_assign -- centroid scoring and hard top-k group membership.
+ * gist.science/zh 2.1.1: hidden states are projected into centroid space and
+ * scored against every centroid; 2.1.3 and gist.science/nl Kerncomponent 4:
+ * at inference a token belongs to its k highest-scoring groups.
+ *
+ *   z_i = x_i W_g (d_g values), s_{i,c} = z_i . C_c, ids_i = the topk
+ *   largest s_{i,.} in descending order, equal scores -> lower id first.
+ *
+ *   X      [B, n, hidden]  bf16        hidden states
+ *   Wg     [hidden, d_g]   fp32        projection into centroid space
+ *   C      [K, d_g]        fp32        centroids of this layer
+ *   ids    [B, n, topk]    int32 out   group ids by descending score
+ *   margin [B, n]          fp32 out    nullable: smallest gap between
+ *                          consecutive scores among the top min(topk+1, K)
+ *                          (+inf when K == 1); a small margin flags a
+ *                          near-tie whose order depends on rounding.
+ * Arithmetic: fp32 with fp32 accumulation.
+ * Supported: hidden % 8 == 0, 1 <= d_g <= 256, 1 <= K <= 1024,
+ *            1 <= topk <= min(K, 8).
+ */
+focus_status_t focus_assign(const void *X, const float *Wg, const float *C,
+                            int B, int n, int hidden, int d_g, int K, int topk,
+                            int32_t *ids, float *margin, void *stream);
+
+/*
+ * focus_bucket -- per-group member lists (histogram, exclusive scan, stable
+ * scatter).  Implied by running "within-group causal attention"
+ * (gist.science/zh 2.1.3) over each group's members as one dense problem.
+ *
+ *   ids     [B, n, topk]  int32 in   (values in [0, K); the topk ids of a
+ *                                     token must be distinct)
+ *   offsets [B, K+1]      int32 out  offsets[b][g] = number of memberships
+ *                                     of groups < g in batch b
+ *   pos     [B, n*topk]   int32 out  pos[b][offsets[b][g] + r] = r-th
+ *                                     smallest token of group g
+ *   inv     [B, n, topk]  int32 out  index in pos[b] of (i, ids[b][i][s])
+ *   ws, ws_bytes: device workspace of at least
+ *                 focus_bucket_workspace_size(B, n, K, topk) bytes.
+ * Result is exact integer data (deterministic).
+ * Supported: 1 <= K <= 1024, 1 <= topk <= 8.
+ */
+size_t focus_bucket_workspace_size(int B, int n, int K, int topk);
+focus_status_t focus_bucket(const int32_t *ids, int B, int n, int K, int topk,
+                            int32_t *offsets, int32_t *pos, int32_t *inv,
+                            void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * focus_attention_fwd -- exact softmax attention over the allowed pairs
+ * (gist.science/nl Kerncomponent 3: exact softmax within the allowed pairs;
+ * gist.science/zh 2.1.2-2.1.3: local window or shared group, causal).
+ *
+ *   A_i = { j <= i : i - j < window  or  ids_i and ids_j share a group }
+ *   O_i = sum_{j in A_i} softmax_j(scale * q_i . k_j) v_j
+ *   lse_i = ln sum_{j in A_i} exp(scale * q_i . k_j)
+ *
+ * Executed as three tcgen05/TMEM kernels: a causal attention over every
+ * group's gathered members (a pair shared through several groups is counted
+ * only in the lowest shared group), a sliding-window attention that skips
+ * pairs sharing a group, and a log-sum-exp merge of the partial results.
+ *
+ *   Q      [B, n, Hq, d]   bf16      K, V [B, n, Hkv, d] bf16
+ *          query head h reads kv head h / (Hq / Hkv)
+ *   window w >= 0 (0: group pairs only; the token itself is always allowed)
+ *   scale  softmax scale; <= 0 selects 1/sqrt(d)
+ *   ids, offsets, pos, inv: as produced by focus_assign / focus_bucket
+ *   O      [B, n, Hq, d]   bf16 out
+ *   lse    [B, Hq, n]      fp32 out, nullable (natural log)
+ *   ws, ws_bytes: device workspace of at least
+ *          focus_attention_workspace_size(B, n, Hq, Hkv, d, K, topk) bytes.
+ * Arithmetic: bf16 operands, fp32 accumulation and softmax, probabilities
+ * rounded to bf16 for the P.V product, partial outputs kept in bf16.
+ * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= K <= 1024, 1 <= topk <= 8,
+ *            B * K <= 4096.
+ */
+size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d,
+                                      int K, int topk);
+focus_status_t focus_attention_fwd(const void *Q, const void *K, const void *V,
+                                   int B, int n, int Hq, int Hkv, int d,
+                                   int window, float scale,
+                                   const int32_t *ids, const int32_t *offsets,
+                                   const int32_t *pos, const int32_t *inv,
+                                   int num_groups, int topk,
+                                   void *O, float *lse,
+                                   void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * focus_prefill -- the whole path in one call: focus_assign, focus_bucket and
+ * focus_attention_fwd on one stream.  With io_on_host != 0, X, Wg, C, Q, K, V
+ * are HOST pointers (page-locked for asynchronous copies), O and lse are host
+ * pointers, and the copies in and out are enqueued on `stream` around the
+ * kernels (the caller synchronises before reading O).  With io_on_host == 0
+ * every pointer is a device pointer.  ids_out (nullable, device) receives the
+ * group ids.  Workspace: focus_prefill_workspace_size(...) device bytes.
+ */
+size_t focus_prefill_workspace_size(int B, int n, int hidden, int Hq, int Hkv,
+                                    int d, int d_g, int K, int topk,
+                                    int io_on_host);
+focus_status_t focus_prefill(const void *X, const float *Wg, const float *C,
+                             const void *Q, const void *K, const void *V,
+                             int B, int n, int hidden, int Hq, int Hkv, int d,
+                             int d_g, int num_groups, int topk, int window,
+                             float scale, void *O, float *lse, int32_t *ids_out,
+                             void *ws, size_t ws_bytes, int io_on_host,
+                             void *stream);
+
+/*
+ * focus_dense_causal_fwd -- plain causal attention (every j <= i) with the
+ * same tcgen05 mainloop; the baseline the sparse path is compared with.
+ *   Q [B, n, Hq, d], K/V [B, n, Hkv, d] bf16; O [B, n, Hq, d] bf16;
+ *   lse [B, Hq, n] fp32 nullable.  Supported: d in {64, 128}.
+ */
+focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *V,
+                                      int B, int n, int Hq, int Hkv, int d,
+                                      float scale, void *O, float *lse,
+                                      void *stream);
+
+/*
+ * focus_count_pairs -- |A_i| for every query (the work the method does), for
+ * effective-FLOP accounting and the "every pair counted once" check.
+ *   per_query [B, n] int64 out, nullable
+ *   totals    [2]    int64 out (device): totals[0] = sum_i |A_i|,
+ *                    totals[1] = number of pairs that share a group
+ *                    (the pairs the group kernel scores; the rest are
+ *                    window pairs scored by the window kernel).
+ */
+focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets,
+                                 const int32_t *pos, const int32_t *inv,
+                                 int B, int n, int num_groups, int topk,
+                                 int window, int64_t *per_query,
+                                 int64_t *totals, void *stream);
+
+/*
+ * Debug variant of focus_attention_fwd: identical result, and each scored
+ * pair adds 1 to pair_count[b*n + i] (int32, device, caller-zeroed) for query
+ * head 0, so the caller can check that every allowed pair was scored exactly
+ * once (pair_count == |A_i|).
+ */
+focus_status_t focus_attention_fwd_counted(const void *Q, const void *K, const void *V,
+                                           int B, int n, int Hq, int Hkv, int d,
+                                           int window, float scale,
+                                           const int32_t *ids, const int32_t *offsets,
+                                           const int32_t *pos, const int32_t *inv,
+                                           int num_groups, int topk,
+                                           void *O, float *lse,
+                                           void *ws, size_t ws_bytes,
+                                           int32_t *pair_count, void *stream);
+
+/*
+ * Reads (and with reset != 0 clears) the device status word of the current
+ * device: FOCUS_OK or FOCUS_ERR_TIMEOUT.  Synchronises the device.
+ */
+focus_status_t focus_get_device_status(int reset);
+
+/* Number of kernels the last successful call on this host thread enqueued. */
+int focus_last_launch_count(void);
+
+/*
+ * Per-kernel timing for measurement.  While enabled (per host thread), each
+ * kernel the library launches is bracketed by two CUDA events recorded on
+ * its stream.  focus_profile_read() waits for those events, writes up to
+ * max_entries rows (kernel name into names[i * name_stride], NUL-terminated;
+ * summed milliseconds into total_ms[i]; launch count into launches[i]; any
+ * output pointer may be NULL), clears the record and returns the number of
+ * rows, or -1 on a CUDA error.  All pointers are host pointers.
+ */
+void focus_profile_enable(int enable);
+int focus_profile_read(char *names, int name_stride, double *total_ms, int *launches,
+                       int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOCUS_GB300_H */

@@ -1,0 +1,535 @@
+// C ABI of the Focus attention inference path (declared in include/focus.h):
+// host-side validation, workspace layout, TMA descriptors, and the order of
+// the kernel launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/focus.h"
+#include "focus_internal.h"
+
+namespace focus {
+
+namespace {
+
+thread_local int g_last_launches = 0;
+
+// Device status word: set by a kernel whose bounded wait ran out.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_addr[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
+
+cudaError_t status_ptr(int **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return e;
+        g_status_addr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_addr[dev];
+    return cudaSuccess;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [B, rows, H, d] bf16 -> a 4-D map with 64 x 1 x 128 x 1 boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int B, int64_t rows, int H, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
+                                   (cuuint64_t)rows * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct AttnWs {
+    size_t qp, kp, vp, opart, lpart, owin, lwin, tiles, ntiles, total;
+};
+
+int64_t max_tiles(int B, int n, int K, int topk)
+{
+    const int64_t nk = (int64_t)n * topk;
+    return (int64_t)B * ((nk + 127) / 128 + K);
+}
+
+AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
+{
+    const size_t nk = (size_t)n * topk;
+    AttnWs w;
+    size_t off = 0;
+    w.qp = off;    off += align256((size_t)B * nk * Hq * d * 2);
+    w.kp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
+    w.vp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
+    w.opart = off; off += align256((size_t)B * nk * Hq * d * 2);
+    w.lpart = off; off += align256((size_t)B * nk * Hq * 4);
+    w.owin = off;  off += align256((size_t)B * n * Hq * d * 2);
+    w.lwin = off;  off += align256((size_t)B * n * Hq * 4);
+    w.tiles = off; off += align256((size_t)max_tiles(B, n, K, topk) * 8);
+    w.ntiles = off; off += 256;
+    w.total = off;
+    return w;
+}
+
+struct PrefillWs {
+    size_t ids, offsets, pos, inv, bucket, attn, x, wg, c, q, k, v, o, lse, total;
+};
+
+PrefillWs prefill_ws(int B, int n, int hidden, int Hq, int Hkv, int d, int dg, int K, int topk,
+                     bool host)
+{
+    const size_t nk = (size_t)n * topk;
+    PrefillWs w;
+    size_t off = 0;
+    w.ids = off;     off += align256((size_t)B * nk * 4);
+    w.offsets = off; off += align256((size_t)B * (K + 1) * 4);
+    w.pos = off;     off += align256((size_t)B * nk * 4);
+    w.inv = off;     off += align256((size_t)B * nk * 4);
+    w.bucket = off;  off += align256(bucket_ws_bytes(B, n, K, topk));
+    w.attn = off;    off += align256(attn_ws(B, n, Hq, Hkv, d, K, topk).total);
+    w.x = w.wg = w.c = w.q = w.k = w.v = w.o = w.lse = 0;
+    if (host) {
+        w.x = off;   off += align256((size_t)B * n * hidden * 2);
+        w.wg = off;  off += align256((size_t)hidden * dg * 4);
+        w.c = off;   off += align256((size_t)K * dg * 4);
+        w.q = off;   off += align256((size_t)B * n * Hq * d * 2);
+        w.k = off;   off += align256((size_t)B * n * Hkv * d * 2);
+        w.v = off;   off += align256((size_t)B * n * Hkv * d * 2);
+        w.o = off;   off += align256((size_t)B * n * Hq * d * 2);
+        w.lse = off; off += align256((size_t)B * Hq * n * 4);
+    }
+    w.total = off;
+    return w;
+}
+
+focus_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+
+// ------------------------------------------------------------ validation
+focus_status_t check_assign(const void *X, const float *Wg, const float *C, int B, int n,
+                            int hidden, int dg, int K, int topk, const int32_t *ids,
+                            const float *margin)
+{
+    if (!X || !Wg || !C || !ids) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(C) || !aligned16(ids) ||
+        (margin && !aligned16(margin)))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 0 || hidden < 1 || dg < 1 || K < 1 || topk < 1 || topk > K)
+        return FOCUS_ERR_INVALID_ARG;
+    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
+    if (hidden % 8 != 0 || dg > 256 || K > 1024 || topk > 8) return FOCUS_ERR_UNSUPPORTED;
+    return FOCUS_OK;
+}
+
+focus_status_t check_bucket(const int32_t *ids, int B, int n, int K, int topk,
+                            const int32_t *offsets, const int32_t *pos, const int32_t *inv)
+{
+    if (!ids || !offsets || !pos || !inv) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(ids) || !aligned16(offsets) || !aligned16(pos) || !aligned16(inv))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 0 || K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
+    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
+    if (K > 1024 || topk > 8 || B > 65535) return FOCUS_ERR_UNSUPPORTED;
+    return FOCUS_OK;
+}
+
+focus_status_t check_attn_shapes(int B, int n, int Hq, int Hkv, int d, int window)
+{
+    if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || window < 0) return FOCUS_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FOCUS_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FOCUS_ERR_UNSUPPORTED;
+    if (B > 65535 || Hq > 65535) return FOCUS_ERR_UNSUPPORTED;
+    return FOCUS_OK;
+}
+
+focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int B, int n, int Hq,
+                              int Hkv, int d, int window, float scale, const int32_t *ids,
+                              const int32_t *offsets, const int32_t *pos, const int32_t *inv,
+                              int K, int topk, void *O, float *lse, void *ws, size_t ws_bytes,
+                              int32_t *pair_count, cudaStream_t s, int *launches)
+{
+    if (!Q || !Kt || !V || !ids || !offsets || !pos || !inv || !O || !ws)
+        return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(Kt) || !aligned16(V) || !aligned16(O) || !aligned16(ws) ||
+        !aligned16(ids) || !aligned16(offsets) || !aligned16(pos) || !aligned16(inv) ||
+        (lse && !aligned16(lse)) || (pair_count && !aligned16(pair_count)))
+        return FOCUS_ERR_INVALID_ARG;
+    focus_status_t st = check_attn_shapes(B, n, Hq, Hkv, d, window);
+    if (st) return st;
+    if (K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
+    if (K > 1024 || topk > 8 || (int64_t)B * K > 4096) return FOCUS_ERR_UNSUPPORTED;
+    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
+    const AttnWs w = attn_ws(B, n, Hq, Hkv, d, K, topk);
+    if (ws_bytes < w.total) return FOCUS_ERR_WORKSPACE;
+    const int64_t grid_group = max_tiles(B, n, K, topk) * Hq;
+    const int64_t nqt = (n + 127) / 128;
+    const int64_t grid_win = (int64_t)B * nqt * Hq;
+    if (grid_group >= ((int64_t)1 << 31) || grid_win >= ((int64_t)1 << 31))
+        return FOCUS_ERR_UNSUPPORTED;
+
+    int *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    auto *Qp = reinterpret_cast<__nv_bfloat16 *>(base + w.qp);
+    auto *Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
+    auto *Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
+    auto *Opart = reinterpret_cast<__nv_bfloat16 *>(base + w.opart);
+    auto *Lpart = reinterpret_cast<float *>(base + w.lpart);
+    auto *Owin = reinterpret_cast<__nv_bfloat16 *>(base + w.owin);
+    auto *Lwin = reinterpret_cast<float *>(base + w.lwin);
+    auto *tiles = reinterpret_cast<int2 *>(base + w.tiles);
+    auto *ntiles = reinterpret_cast<int *>(base + w.ntiles);
+    const int64_t nk = (int64_t)n * topk;
+
+    CUtensorMap mq, mk, mv, wq, wk, wv;
+    if (!make_map(&mq, Qp, B, nk, Hq, d) || !make_map(&mk, Kp, B, nk, Hkv, d) ||
+        !make_map(&mv, Vp, B, nk, Hkv, d) || !make_map(&wq, Q, B, n, Hq, d) ||
+        !make_map(&wk, Kt, B, n, Hkv, d) || !make_map(&wv, V, B, n, Hkv, d))
+        return FOCUS_ERR_CUDA;
+
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    AttnLaunch p;
+    memset(&p, 0, sizeof p);
+    p.B = B;
+    p.n = n;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.window = window;
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.K = K;
+    p.topk = topk;
+    p.ids = ids;
+    p.offsets = offsets;
+    p.pos = pos;
+    p.tiles = tiles;
+    p.ntiles = ntiles;
+    p.status = status;
+    p.pair_count = pair_count;
+
+    if ((e = launch_plan(offsets, B, K, tiles, ntiles, s, launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
+    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Q),
+                           static_cast<const __nv_bfloat16 *>(Kt),
+                           static_cast<const __nv_bfloat16 *>(V), pos, B, n, topk, Hq, Hkv, d,
+                           Qp, Kp, Vp, s, launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
+
+    p.tmQ = &mq;
+    p.tmK = &mk;
+    p.tmV = &mv;
+    p.rows = (int)nk;
+    p.grid = grid_group;
+    p.out = Opart;
+    p.lse = Lpart;
+    if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+
+    p.tmQ = &wq;
+    p.tmK = &wk;
+    p.tmV = &wv;
+    p.rows = n;
+    p.grid = grid_win;
+    p.out = Owin;
+    p.lse = Lwin;
+    if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+
+    if ((e = launch_merge(Owin, Lwin, Opart, Lpart, inv, B, n, topk, Hq, d,
+                          static_cast<__nv_bfloat16 *>(O), lse, s, launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
+    return FOCUS_OK;
+}
+
+}  // namespace
+
+}  // namespace focus
+
+using namespace focus;
+
+extern "C" {
+
+const char *focus_status_string(focus_status_t status)
+{
+    switch (status) {
+    case FOCUS_OK: return "FOCUS_OK";
+    case FOCUS_ERR_INVALID_ARG: return "FOCUS_ERR_INVALID_ARG";
+    case FOCUS_ERR_UNSUPPORTED: return "FOCUS_ERR_UNSUPPORTED";
+    case FOCUS_ERR_WORKSPACE: return "FOCUS_ERR_WORKSPACE";
+    case FOCUS_ERR_CUDA: return "FOCUS_ERR_CUDA";
+    case FOCUS_ERR_TIMEOUT: return "FOCUS_ERR_TIMEOUT";
+    default: return "FOCUS_ERR_UNKNOWN";
+    }
+}
+
+const char *focus_version(void) { return "focus-gb300 0.1.0 sm_103a"; }
+
+int focus_last_launch_count(void) { return g_last_launches; }
+
+focus_status_t focus_assign(const void *X, const float *Wg, const float *C, int B, int n,
+                            int hidden, int d_g, int K, int topk, int32_t *ids, float *margin,
+                            void *stream)
+{
+    focus_status_t st = check_assign(X, Wg, C, B, n, hidden, d_g, K, topk, ids, margin);
+    if (st) return st;
+    int launches = 0;
+    AssignLaunch p{static_cast<const __nv_bfloat16 *>(X), Wg, C, (int64_t)B * n, hidden, d_g, K,
+                   topk, ids, margin};
+    cudaError_t e = launch_assign(p, static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+size_t focus_bucket_workspace_size(int B, int n, int K, int topk)
+{
+    if (B < 1 || n < 0 || K < 1 || topk < 1) return 0;
+    return bucket_ws_bytes(B, n, K, topk);
+}
+
+focus_status_t focus_bucket(const int32_t *ids, int B, int n, int K, int topk, int32_t *offsets,
+                            int32_t *pos, int32_t *inv, void *ws, size_t ws_bytes, void *stream)
+{
+    focus_status_t st = check_bucket(ids, B, n, K, topk, offsets, pos, inv);
+    if (st) return st;
+    if (!ws || !aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
+    if (ws_bytes < bucket_ws_bytes(B, n, K, topk)) return FOCUS_ERR_WORKSPACE;
+    int launches = 0;
+    cudaError_t e = launch_bucket(ids, B, n, K, topk, offsets, pos, inv, ws,
+                                  static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d, int K, int topk)
+{
+    if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || d < 1 || K < 1 || topk < 1) return 0;
+    return attn_ws(B, n, Hq, Hkv, d, K, topk).total;
+}
+
+focus_status_t focus_attention_fwd(const void *Q, const void *K, const void *V, int B, int n,
+                                   int Hq, int Hkv, int d, int window, float scale,
+                                   const int32_t *ids, const int32_t *offsets, const int32_t *pos,
+                                   const int32_t *inv, int num_groups, int topk, void *O,
+                                   float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    int launches = 0;
+    focus_status_t st = attention_impl(Q, K, V, B, n, Hq, Hkv, d, window, scale, ids, offsets,
+                                       pos, inv, num_groups, topk, O, lse, ws, ws_bytes, nullptr,
+                                       static_cast<cudaStream_t>(stream), &launches);
+    if (st == FOCUS_OK) g_last_launches = launches;
+    return st;
+}
+
+focus_status_t focus_attention_fwd_counted(const void *Q, const void *K, const void *V, int B,
+                                           int n, int Hq, int Hkv, int d, int window, float scale,
+                                           const int32_t *ids, const int32_t *offsets,
+                                           const int32_t *pos, const int32_t *inv,
+                                           int num_groups, int topk, void *O, float *lse,
+                                           void *ws, size_t ws_bytes, int32_t *pair_count,
+                                           void *stream)
+{
+    if (!pair_count) return FOCUS_ERR_INVALID_ARG;
+    int launches = 0;
+    focus_status_t st = attention_impl(Q, K, V, B, n, Hq, Hkv, d, window, scale, ids, offsets,
+                                       pos, inv, num_groups, topk, O, lse, ws, ws_bytes,
+                                       pair_count, static_cast<cudaStream_t>(stream), &launches);
+    if (st == FOCUS_OK) g_last_launches = launches;
+    return st;
+}
+
+size_t focus_prefill_workspace_size(int B, int n, int hidden, int Hq, int Hkv, int d, int d_g,
+                                    int K, int topk, int io_on_host)
+{
+    if (B < 1 || n < 1 || hidden < 1 || Hq < 1 || Hkv < 1 || d < 1 || d_g < 1 || K < 1 ||
+        topk < 1)
+        return 0;
+    return prefill_ws(B, n, hidden, Hq, Hkv, d, d_g, K, topk, io_on_host != 0).total;
+}
+
+focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, const void *Q,
+                             const void *K, const void *V, int B, int n, int hidden, int Hq,
+                             int Hkv, int d, int d_g, int num_groups, int topk, int window,
+                             float scale, void *O, float *lse, int32_t *ids_out, void *ws,
+                             size_t ws_bytes, int io_on_host, void *stream)
+{
+    if (!X || !Wg || !C || !Q || !K || !V || !O || !ws) return FOCUS_ERR_INVALID_ARG;
+    focus_status_t st = check_attn_shapes(B, n, Hq, Hkv, d, window);
+    if (st) return st;
+    const bool host = io_on_host != 0;
+    const PrefillWs w = prefill_ws(B, n, hidden, Hq, Hkv, d, d_g, num_groups, topk, host);
+    if (!aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
+    if (ws_bytes < w.total) return FOCUS_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    int32_t *ids = ids_out ? ids_out : reinterpret_cast<int32_t *>(base + w.ids);
+    int32_t *offsets = reinterpret_cast<int32_t *>(base + w.offsets);
+    int32_t *pos = reinterpret_cast<int32_t *>(base + w.pos);
+    int32_t *inv = reinterpret_cast<int32_t *>(base + w.inv);
+    const void *dX = X, *dQ = Q, *dK = K, *dV = V;
+    const float *dWg = Wg, *dC = C;
+    void *dO = O;
+    float *dL = lse;
+    // host-side validation of the device-side steps before anything is enqueued
+    st = check_assign(host ? base + w.x : X, host ? reinterpret_cast<float *>(base + w.wg) : Wg,
+                      host ? reinterpret_cast<float *>(base + w.c) : C, B, n, hidden, d_g,
+                      num_groups, topk, ids, nullptr);
+    if (st) return st;
+    if (num_groups > 1024 || topk > 8 || (int64_t)B * num_groups > 4096)
+        return FOCUS_ERR_UNSUPPORTED;
+    if (!host && (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+                  (lse && !aligned16(lse))))
+        return FOCUS_ERR_INVALID_ARG;
+    int launches = 0;
+    cudaError_t e = cudaSuccess;
+    if (host) {
+        const size_t xb = (size_t)B * n * hidden * 2, qb = (size_t)B * n * Hq * d * 2,
+                     kb = (size_t)B * n * Hkv * d * 2;
+        dX = base + w.x;
+        dWg = reinterpret_cast<const float *>(base + w.wg);
+        dC = reinterpret_cast<const float *>(base + w.c);
+        dQ = base + w.q;
+        dK = base + w.k;
+        dV = base + w.v;
+        dO = base + w.o;
+        dL = lse ? reinterpret_cast<float *>(base + w.lse) : nullptr;
+        if ((e = cudaMemcpyAsync(base + w.x, X, xb, cudaMemcpyHostToDevice, s)) ||
+            (e = cudaMemcpyAsync(base + w.wg, Wg, (size_t)hidden * d_g * 4, cudaMemcpyHostToDevice, s)) ||
+            (e = cudaMemcpyAsync(base + w.c, C, (size_t)num_groups * d_g * 4, cudaMemcpyHostToDevice, s)) ||
+            (e = cudaMemcpyAsync(base + w.q, Q, qb, cudaMemcpyHostToDevice, s)) ||
+            (e = cudaMemcpyAsync(base + w.k, K, kb, cudaMemcpyHostToDevice, s)) ||
+            (e = cudaMemcpyAsync(base + w.v, V, kb, cudaMemcpyHostToDevice, s)))
+            return FOCUS_ERR_CUDA;
+    }
+    AssignLaunch ap{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden, d_g,
+                    num_groups, topk, ids, nullptr};
+    if ((e = launch_assign(ap, s, &launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if ((e = launch_bucket(ids, B, n, num_groups, topk, offsets, pos, inv, base + w.bucket, s,
+                           &launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
+    const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
+    st = attention_impl(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
+                        num_groups, topk, dO, dL, base + w.attn, aw.total, nullptr, s,
+                        &launches);
+    if (st) return st;
+    if (host) {
+        if ((e = cudaMemcpyAsync(O, dO, (size_t)B * n * Hq * d * 2, cudaMemcpyDeviceToHost, s)))
+            return FOCUS_ERR_CUDA;
+        if (lse && (e = cudaMemcpyAsync(lse, dL, (size_t)B * Hq * n * 4, cudaMemcpyDeviceToHost, s)))
+            return FOCUS_ERR_CUDA;
+    }
+    g_last_launches = launches;
+    return FOCUS_OK;
+}
+
+focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *V, int B, int n,
+                                      int Hq, int Hkv, int d, float scale, void *O, float *lse,
+                                      void *stream)
+{
+    if (!Q || !K || !V || !O) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+        (lse && !aligned16(lse)))
+        return FOCUS_ERR_INVALID_ARG;
+    focus_status_t st = check_attn_shapes(B, n, Hq, Hkv, d, 0);
+    if (st) return st;
+    const int64_t grid = (int64_t)B * ((n + 127) / 128) * Hq;
+    if (grid >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
+    int *status = nullptr;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, Q, B, n, Hq, d) || !make_map(&mk, K, B, n, Hkv, d) ||
+        !make_map(&mv, V, B, n, Hkv, d))
+        return FOCUS_ERR_CUDA;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    AttnLaunch p;
+    memset(&p, 0, sizeof p);
+    p.tmQ = &mq;
+    p.tmK = &mk;
+    p.tmV = &mv;
+    p.B = B;
+    p.n = n;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.rows = n;
+    p.window = n;
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.K = 1;
+    p.topk = 1;
+    p.grid = grid;
+    p.out = static_cast<__nv_bfloat16 *>(O);
+    p.lse = lse;
+    p.status = status;
+    int launches = 0;
+    cudaError_t e = launch_attn_dense(p, static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
+                                 const int32_t *inv, int B, int n, int num_groups, int topk,
+                                 int window, int64_t *per_query, int64_t *totals, void *stream)
+{
+    focus_status_t st = check_bucket(ids, B, n, num_groups, topk, offsets, pos, inv);
+    if (st) return st;
+    if (!totals || window < 0) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(totals) || (per_query && !aligned16(per_query))) return FOCUS_ERR_INVALID_ARG;
+    int launches = 0;
+    cudaError_t e = launch_count_pairs(ids, offsets, pos, inv, B, n, num_groups, topk, window,
+                                       per_query, totals, static_cast<cudaStream_t>(stream),
+                                       &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+focus_status_t focus_get_device_status(int reset)
+{
+    int *p = nullptr;
+    if (status_ptr(&p) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FOCUS_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (reset) {
+        const int z = 0;
+        if (cudaMemcpy(p, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FOCUS_ERR_CUDA;
+    }
+    return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,381 @@
+// Group bucketing and the data movement around the group attention kernel.
+//
+// Bucketing turns the hard top-k memberships (gist.science/zh technical
+// summary 2.1.3) into per-group member lists so that "within-group causal
+// attention" can run over each group as one dense problem:
+//   1. bucket_count    per chunk of 4096 (token, slot) entries, a histogram
+//                      of group ids in shared memory;
+//   2. bucket_scan     per group, an exclusive scan of the chunk counts;
+//   3. bucket_offsets  per batch, an exclusive scan of the group sizes;
+//   4. bucket_scatter  per chunk, a stable scatter: each warp walks its slice
+//                      of the chunk in order and ranks equal ids inside a
+//                      32-entry step with __match_any_sync.
+// The plan kernel orders the group kernel's tiles by decreasing cost, and the
+// gather kernel copies Q/K/V rows into group order.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "focus_internal.h"
+
+namespace focus {
+
+namespace {
+
+constexpr int kScatterWarps = 8;
+constexpr int kWarpSlice = kBucketChunk / kScatterWarps;   // 512 entries per warp
+
+__global__ void bucket_count(const int32_t *__restrict__ ids, int64_t nk, int K, int nchunks,
+                             int32_t *__restrict__ counts)
+{
+    extern __shared__ int hist[];
+    const int chunk = blockIdx.x, b = blockIdx.y;
+    for (int g = threadIdx.x; g < K; g += blockDim.x) hist[g] = 0;
+    __syncthreads();
+    const int64_t e0 = (int64_t)chunk * kBucketChunk;
+    const int64_t e1 = min(e0 + kBucketChunk, nk);
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+        const int g = ids[(int64_t)b * nk + e];
+        if ((unsigned)g < (unsigned)K) atomicAdd(&hist[g], 1);   // out-of-range ids are dropped
+    }
+    __syncthreads();
+    int32_t *out = counts + ((int64_t)b * nchunks + chunk) * K;
+    for (int g = threadIdx.x; g < K; g += blockDim.x) out[g] = hist[g];
+}
+
+// blockDim (32, 32): x = group within a tile of 32 groups, y = slice of chunks.
+__global__ void bucket_scan(int32_t *__restrict__ counts, int K, int nchunks,
+                            int32_t *__restrict__ totals)
+{
+    __shared__ int part[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y, b = blockIdx.y;
+    const int g = blockIdx.x * 32 + tx;
+    const int per = (nchunks + 31) / 32;
+    const int c0 = min(ty * per, nchunks), c1 = min(c0 + per, nchunks);
+    int32_t *col = counts + (int64_t)b * nchunks * K + g;
+    int sum = 0;
+    if (g < K)
+        for (int c = c0; c < c1; ++c) sum += col[(int64_t)c * K];
+    part[ty][tx] = sum;
+    __syncthreads();
+    int run = 0;
+    for (int y = 0; y < ty; ++y) run += part[y][tx];
+    if (g < K) {
+        for (int c = c0; c < c1; ++c) {
+            const int v = col[(int64_t)c * K];
+            col[(int64_t)c * K] = run;
+            run += v;
+        }
+        if (ty == 31) totals[(int64_t)b * K + g] = run;
+    }
+}
+
+// One block of 1024 threads per batch: exclusive scan of K <= 1024 sizes.
+__global__ void bucket_offsets(const int32_t *__restrict__ totals, int K,
+                               int32_t *__restrict__ offsets)
+{
+    __shared__ int warp_sum[32];
+    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int v = t < K ? totals[(int64_t)b * K + t] : 0;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = warp_sum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        warp_sum[lane] = s;
+    }
+    __syncthreads();
+    const int incl = x + (w > 0 ? warp_sum[w - 1] : 0);
+    int32_t *off = offsets + (int64_t)b * (K + 1);
+    if (t < K) off[t] = incl - v;
+    if (t == K - 1) off[K] = incl;
+}
+
+__global__ void __launch_bounds__(256) bucket_scatter(const int32_t *__restrict__ ids,
+                                                      int64_t nk, int K, int topk, int nchunks,
+                                                      const int32_t *__restrict__ chunk_base,
+                                                      const int32_t *__restrict__ offsets,
+                                                      int32_t *__restrict__ pos,
+                                                      int32_t *__restrict__ inv)
+{
+    extern __shared__ int hist[];   // [kScatterWarps][K]
+    const int chunk = blockIdx.x, b = blockIdx.y;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kScatterWarps * K; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int64_t e0 = (int64_t)chunk * kBucketChunk;
+    const int64_t s0 = min(e0 + (int64_t)w * kWarpSlice, nk);
+    const int64_t s1 = min(s0 + kWarpSlice, nk);
+    const int32_t *idb = ids + (int64_t)b * nk;
+    for (int64_t e = s0 + lane; e < s1; e += 32) {
+        const int g = idb[e];
+        if ((unsigned)g < (unsigned)K) atomicAdd(&hist[w * K + g], 1);
+    }
+    __syncthreads();
+    const int32_t *cb = chunk_base + ((int64_t)b * nchunks + chunk) * K;
+    const int32_t *ob = offsets + (int64_t)b * (K + 1);
+    for (int g = threadIdx.x; g < K; g += blockDim.x) {
+        int run = ob[g] + cb[g];
+        for (int x = 0; x < kScatterWarps; ++x) {
+            const int t = hist[x * K + g];
+            hist[x * K + g] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+    int32_t *pb = pos + (int64_t)b * nk;
+    int32_t *ib = inv + (int64_t)b * nk;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int64_t base = s0; base < s1; base += 32) {
+        const int64_t e = base + lane;
+        int g = e < s1 ? idb[e] : -1;
+        const bool active = (unsigned)g < (unsigned)K;
+        if (!active) {
+            g = -1 - lane;            // unique, matches no other lane
+            if (e < s1) ib[e] = -1;   // an out-of-range id gets no list entry
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, g);
+        const int rank = __popc(peers & lt);
+        if (active) {
+            const int r = hist[w * K + g] + rank;
+            pb[r] = (int32_t)(e / topk);
+            ib[e] = r;
+        }
+        __syncwarp();
+        if (active && lane == __ffs(peers) - 1) hist[w * K + g] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------------ plan
+// Tiles of group g: T_g = ceil(size_g / 128); tile t of a group costs t + 1
+// key tiles.  Emits every (group, t) ordered by decreasing t, groups sorted
+// by decreasing T_g inside a layer.  One block of 1024 threads; B*K <= 4096.
+constexpr int kPlanMax = 4096;
+
+__device__ __forceinline__ int layer_count(const int *keyT, int G, int t)
+{
+    // number of sorted (descending) entries with T > t
+    int lo = 0, hi = G;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (keyT[mid] > t) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int B,
+                                                    int K, int2 *__restrict__ tiles,
+                                                    int *__restrict__ ntiles)
+{
+    __shared__ int keyT[kPlanMax];
+    __shared__ int keyG[kPlanMax];
+    __shared__ long long pref[kPlanMax + 1];
+    __shared__ long long wsum[32];
+    const int G = B * K;
+    int Gp = 1;
+    while (Gp < G) Gp <<= 1;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < Gp; i += 1024) {
+        if (i < G) {
+            const int b = i / K, g = i - b * K;
+            const int size = offsets[b * (K + 1) + g + 1] - offsets[b * (K + 1) + g];
+            keyT[i] = (size + 127) / 128;
+            keyG[i] = i;
+        } else {
+            keyT[i] = -1;
+            keyG[i] = 0x7fffffff;
+        }
+    }
+    __syncthreads();
+    // bitonic sort: T descending, group index ascending
+    for (int k = 2; k <= Gp; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < Gp; i += 1024) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const bool desc_block = (i & k) == 0;
+                    const int ti = keyT[i], tp = keyT[p], gi = keyG[i], gp = keyG[p];
+                    // "first" = should come earlier in the final order
+                    const bool p_first = tp > ti || (tp == ti && gp < gi);
+                    if (p_first == desc_block) {
+                        keyT[i] = tp;
+                        keyT[p] = ti;
+                        keyG[i] = gp;
+                        keyG[p] = gi;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // inclusive prefix sums of T over the sorted order (4 entries per thread)
+    long long local[4];
+    long long run = 0;
+    for (int q = 0; q < 4; ++q) {
+        const int i = tid * 4 + q;
+        run += (i < G && keyT[i] > 0) ? keyT[i] : 0;
+        local[q] = run;
+    }
+    long long x = run;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        long long s = wsum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        wsum[lane] = s;
+    }
+    __syncthreads();
+    const long long before = x - run + (w > 0 ? wsum[w - 1] : 0);
+    for (int q = 0; q < 4; ++q) {
+        const int i = tid * 4 + q;
+        if (i < kPlanMax) pref[i + 1] = before + local[q];
+    }
+    if (tid == 0) pref[0] = 0;
+    __syncthreads();
+    const long long total = pref[G];
+    const int Tmax = G > 0 ? max(keyT[0], 0) : 0;
+    if (tid == 0) *ntiles = (int)total;
+    // S(t) = tiles in layers above t = pref[c(t)] - c(t) * (t + 1)
+    for (long long p = tid; p < total; p += 1024) {
+        int lo = 0, hi = Tmax - 1;   // smallest t with S(t) <= p
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const int c = layer_count(keyT, G, mid);
+            const long long S = pref[c] - (long long)c * (mid + 1);
+            if (S <= p) hi = mid;
+            else lo = mid + 1;
+        }
+        const int c = layer_count(keyT, G, lo);
+        const long long S = pref[c] - (long long)c * (lo + 1);
+        const int rank = (int)(p - S);
+        tiles[p] = make_int2(keyG[rank], lo);
+    }
+}
+
+// ---------------------------------------------------------------- gather
+__global__ void __launch_bounds__(256) gather_kernel(
+    const uint4 *__restrict__ Q, const uint4 *__restrict__ K, const uint4 *__restrict__ V,
+    const int32_t *__restrict__ pos, int B, int n, int64_t nk, int qunits, int kvunits,
+    uint4 *__restrict__ Qp, uint4 *__restrict__ Kp, uint4 *__restrict__ Vp)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t total = (int64_t)B * nk;
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < total;
+         row += warps) {
+        const int64_t b = row / nk;
+        const int64_t src = b * n + pos[row];
+        const uint4 *q = Q + src * qunits;
+        uint4 *qd = Qp + row * qunits;
+        for (int u = lane; u < qunits; u += 32) qd[u] = q[u];
+        const uint4 *k = K + src * kvunits;
+        const uint4 *v = V + src * kvunits;
+        uint4 *kd = Kp + row * kvunits;
+        uint4 *vd = Vp + row * kvunits;
+        for (int u = lane; u < kvunits; u += 32) {
+            kd[u] = k[u];
+            vd[u] = v[u];
+        }
+    }
+}
+
+}  // namespace
+
+size_t bucket_ws_bytes(int B, int n, int K, int topk)
+{
+    const int64_t nk = (int64_t)n * topk;
+    const int64_t nchunks = (nk + kBucketChunk - 1) / kBucketChunk;
+    return sizeof(int32_t) * ((size_t)B * (size_t)(nchunks > 0 ? nchunks : 1) * K + (size_t)B * K) +
+           256;
+}
+
+cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int32_t *offsets,
+                          int32_t *pos, int32_t *inv, void *ws, cudaStream_t s, int *launches)
+{
+    const int64_t nk = (int64_t)n * topk;
+    const int nchunks = (int)((nk + kBucketChunk - 1) / kBucketChunk);
+    int32_t *counts = static_cast<int32_t *>(ws);
+    int32_t *totals = counts + (size_t)B * (size_t)(nchunks > 0 ? nchunks : 1) * K;
+    cudaError_t e;
+    if (nchunks > 0) {
+        prof_begin("bucket_count", s);
+        bucket_count<<<dim3(nchunks, B), 256, K * sizeof(int), s>>>(ids, nk, K, nchunks, counts);
+        prof_end(s);
+        prof_begin("bucket_scan", s);
+        bucket_scan<<<dim3((K + 31) / 32, B), dim3(32, 32), 0, s>>>(counts, K, nchunks, totals);
+        prof_end(s);
+        *launches += 2;
+    } else {
+        e = cudaMemsetAsync(totals, 0, sizeof(int32_t) * (size_t)B * K, s);
+        if (e != cudaSuccess) return e;
+    }
+    prof_begin("bucket_offsets", s);
+    bucket_offsets<<<B, 1024, 0, s>>>(totals, K, offsets);
+    prof_end(s);
+    *launches += 1;
+    if (nchunks > 0) {
+        const size_t smem = sizeof(int) * (size_t)kScatterWarps * K;
+        e = cudaFuncSetAttribute(bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        prof_begin("bucket_scatter", s);
+        bucket_scatter<<<dim3(nchunks, B), 256, smem, s>>>(ids, nk, K, topk, nchunks, counts,
+                                                          offsets, pos, inv);
+        prof_end(s);
+        *launches += 1;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *ntiles,
+                        cudaStream_t s, int *launches)
+{
+    prof_begin("plan", s);
+    plan_kernel<<<1, 1024, 0, s>>>(offsets, B, K, tiles, ntiles);
+    prof_end(s);
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                          const __nv_bfloat16 *V, const int32_t *pos, int B, int n, int topk,
+                          int Hq, int Hkv, int d, __nv_bfloat16 *Qp, __nv_bfloat16 *Kp,
+                          __nv_bfloat16 *Vp, cudaStream_t s, int *launches)
+{
+    const int64_t nk = (int64_t)n * topk;
+    const int64_t rows = (int64_t)B * nk;
+    if (rows == 0) return cudaSuccess;
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    prof_begin("gather", s);
+    gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(Q), reinterpret_cast<const uint4 *>(K),
+        reinterpret_cast<const uint4 *>(V), pos, B, n, nk, Hq * d / 8, Hkv * d / 8,
+        reinterpret_cast<uint4 *>(Qp), reinterpret_cast<uint4 *>(Kp), reinterpret_cast<uint4 *>(Vp));
+    prof_end(s);
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+}  // namespace focus

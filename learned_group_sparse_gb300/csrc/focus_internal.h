@@ -1,0 +1,74 @@
+// Internal launch interface between the C-ABI layer (focus_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace focus {
+
+// Per-kernel timing hooks (no-ops unless focus_profile_enable(1) was called
+// on this host thread).
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+struct AssignLaunch {
+    const __nv_bfloat16 *X;
+    const float *Wg;
+    const float *C;
+    int64_t ntok;
+    int hidden, dg, K, topk;
+    int32_t *ids;
+    float *margin;
+};
+cudaError_t launch_assign(const AssignLaunch &p, cudaStream_t s, int *launches);
+
+// ---- bucket: histogram per chunk, scan, offsets, stable scatter
+constexpr int kBucketChunk = 4096;   // (token, slot) entries per chunk
+size_t bucket_ws_bytes(int B, int n, int K, int topk);
+cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int32_t *offsets,
+                          int32_t *pos, int32_t *inv, void *ws, cudaStream_t s, int *launches);
+
+// ---- attention helpers
+// Work list of the group kernel ordered by decreasing cost (tile index).
+cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *ntiles,
+                        cudaStream_t s, int *launches);
+// Qp[b][r] = Q[b][pos[b][r]] (and K, V): rows of H*d bf16.
+cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
+                          const __nv_bfloat16 *V, const int32_t *pos, int B, int n, int topk,
+                          int Hq, int Hkv, int d, __nv_bfloat16 *Qp, __nv_bfloat16 *Kp,
+                          __nv_bfloat16 *Vp, cudaStream_t s, int *launches);
+// O = log-sum-exp merge of the window partial and the topk group partials.
+cudaError_t launch_merge(const __nv_bfloat16 *Owin, const float *Lwin,
+                         const __nv_bfloat16 *Opart, const float *Lpart, const int32_t *inv,
+                         int B, int n, int topk, int Hq, int d, __nv_bfloat16 *O, float *lse,
+                         cudaStream_t s, int *launches);
+cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
+                               const int32_t *inv, int B, int n, int K, int topk, int window,
+                               int64_t *per_query, int64_t *totals, cudaStream_t s,
+                               int *launches);
+
+// ---- tcgen05 attention kernels
+struct AttnLaunch {
+    const CUtensorMap *tmQ, *tmK, *tmV;
+    int B, n, Hq, Hkv, d;
+    int rows;
+    int window;
+    float scale_log2;
+    int K, topk;
+    const int32_t *ids, *offsets, *pos;
+    const int2 *tiles;
+    const int *ntiles;
+    int64_t grid;
+    __nv_bfloat16 *out;
+    float *lse;
+    int *status;
+    int32_t *pair_count;
+};
+cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
+cudaError_t launch_attn_window(const AttnLaunch &p, cudaStream_t s, int *launches);
+cudaError_t launch_attn_dense(const AttnLaunch &p, cudaStream_t s, int *launches);
+
+}  // namespace focus

@@ -69,7 +69,7 @@ def _load():
             lib.oracle_assign.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp]
             lib.oracle_bucket.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
             lib.oracle_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
-                                             vp, i32, vp, i64, vp, vp]
+                                             vp, i32, vp, i64, i32, vp, vp]
             lib.oracle_count_pairs.argtypes = [vp, i32, i32, i32, i32, vp, _I64P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_assign, lib.oracle_bucket, lib.oracle_attention,
@@ -139,13 +139,19 @@ def attention(Q_bits, K_bits, V_bits, ids, window, scale=0.0, rows=None):
 
     Q_bits [B, n, Hq, d], K_bits/V_bits [B, n, Hkv, d] uint16 (bf16 bits);
     ids [B, n, topk] int32.  rows: optional 1-D int64 array of flattened query
-    indices b*n + i.  Returns (O [rows, Hq, d] float32, LSE [rows, Hq]
+    indices b*n + i; then Q_bits may instead hold just those rows,
+    [len(rows), Hq, d].  Returns (O [rows, Hq, d] float32, LSE [rows, Hq]
     float32, natural log); with rows=None the leading shape is [B, n].
     """
     Q, Kt, V = _bits16(Q_bits), _bits16(K_bits), _bits16(V_bits)
-    B, n, Hq, d = Q.shape
-    Hkv = Kt.shape[2]
-    assert Kt.shape == (B, n, Hkv, d) and V.shape == Kt.shape
+    B, n, Hkv, d = Kt.shape
+    q_rows_only = Q.ndim == 3
+    Hq = Q.shape[-2]
+    if q_rows_only:
+        assert rows is not None and Q.shape[0] == len(rows)
+    else:
+        assert Q.shape == (B, n, Hq, d)
+    assert V.shape == Kt.shape
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     topk = ids.shape[-1]
     assert ids.shape == (B, n, topk)
@@ -158,7 +164,7 @@ def attention(Q_bits, K_bits, V_bits, ids, window, scale=0.0, rows=None):
     L = np.empty((nrows, Hq), np.float32)
     rc = _load().oracle_attention(_ptr(Q), _ptr(Kt), _ptr(V), B, n, Hq, Hkv, d, int(window),
                                   float(scale), _ptr(ids), topk, _ptr(rows_arr), nrows,
-                                  _ptr(O), _ptr(L))
+                                  1 if q_rows_only else 0, _ptr(O), _ptr(L))
     if rc:
         raise ValueError("oracle_attention: invalid arguments")
     if rows is None:

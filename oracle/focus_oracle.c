@@ -171,6 +171,8 @@ static int allowed(const int32_t *ids_b, int topk, int window, int64_t i, int64_
  * Q [B, n, Hq, d], Kt/V [B, n, Hkv, d]  bf16 bit patterns
  * ids [B, n, topk]
  * rows: nrows flattened query indices b*n + i (NULL: all B*n rows, in order)
+ * q_rows_only: if non-zero (and rows given), Q holds only the sampled rows,
+ *     [nrows, Hq, d], in the order of `rows`
  * O   [nrows, Hq, d] float out;  LSE [nrows, Hq] float out (natural log),
  *     nullable.  A row with no allowed key cannot occur (j = i is always
  *     allowed because a token shares its own groups).
@@ -179,7 +181,8 @@ static int allowed(const int32_t *ids_b, int topk, int window, int64_t i, int64_
 int oracle_attention(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V,
                      int B, int n, int Hq, int Hkv, int d, int window, float scale,
                      const int32_t *ids, int topk,
-                     const int64_t *rows, int64_t nrows, float *O, float *LSE)
+                     const int64_t *rows, int64_t nrows, int q_rows_only,
+                     float *O, float *LSE)
 {
     if (!Q || !Kt || !V || !ids || !O || B < 1 || n < 1 || Hq < 1 || Hkv < 1 ||
         Hq % Hkv != 0 || d < 1 || window < 0 || topk < 1)
@@ -202,7 +205,8 @@ int oracle_attention(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V,
         double *acc = (double *)malloc(sizeof(double) * (size_t)d);
         for (int h = 0; h < Hq; ++h) {
             int kvh = h / grp;
-            const uint16_t *q = Q + (((int64_t)b * n + i) * Hq + h) * d;
+            const int64_t qrow = (rows && q_rows_only) ? r : (int64_t)b * n + i;
+            const uint16_t *q = Q + (qrow * Hq + h) * d;
             double m = -INFINITY;
             for (int64_t a = 0; a < nj; ++a) {
                 const uint16_t *k = Kt + (((int64_t)b * n + J[a]) * Hkv + kvh) * d;

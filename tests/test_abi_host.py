@@ -1,0 +1,136 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side validation rejects bad arguments before any CUDA call
+(no GPU needed: the fake pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import learned_group_sparse_gb300 as fg
+from learned_group_sparse_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "focus.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+P = ctypes.c_void_p(0x10000)        # aligned, never dereferenced
+P2 = ctypes.c_void_p(0x20000)
+MIS = ctypes.c_void_p(0x10004)      # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fg.library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(focus_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_path_calls():
+    names = _declared()
+    for n in ("focus_assign", "focus_bucket", "focus_attention_fwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert fg.focus_status_string(0) == "FOCUS_OK"
+    assert fg.focus_status_string(3) == "FOCUS_ERR_WORKSPACE"
+    assert "sm_103a" in fg.focus_version()
+
+
+def test_assign_validation(lib):
+    f = lib.focus_assign
+    #            X     Wg    C   B  n  hid dg  K topk ids  margin stream
+    assert f(None, P, P, 1, 8, 64, 16, 8, 2, P, None, None) == INVALID
+    assert f(P, P, P, 1, 8, 64, 16, 8, 9, P, None, None) == INVALID        # topk > K
+    assert f(P, P, P, 1, 8, 64, 16, 8, 0, P, None, None) == INVALID
+    assert f(MIS, P, P, 1, 8, 64, 16, 8, 2, P, None, None) == INVALID
+    assert f(P, P, P, 1, 8, 60, 16, 8, 2, P, None, None) == UNSUPPORTED    # hidden % 8
+    assert f(P, P, P, 1, 8, 64, 300, 8, 2, P, None, None) == UNSUPPORTED   # d_g > 256
+    assert f(P, P, P, 1, 8, 64, 16, 2000, 2, P, None, None) == UNSUPPORTED  # K > 1024
+    assert f(P, P, P, 1, 8, 64, 16, 20, 9, P, None, None) == UNSUPPORTED   # topk > 8
+
+
+def test_bucket_validation(lib):
+    f = lib.focus_bucket
+    need = fg.focus_bucket_workspace_size(2, 5000, 64, 2)
+    assert need > 0
+    assert f(None, 2, 5000, 64, 2, P, P, P, P, need, None) == INVALID
+    assert f(P, 2, 5000, 64, 65, P, P, P, P, need, None) == INVALID          # topk > K
+    assert f(P, 2, 5000, 64, 2, P, P, P, P, need - 1, None) == WORKSPACE
+    assert f(P, 2, 5000, 64, 2, P, P, P, None, need, None) == INVALID
+    assert f(P, 2, 5000, 2048, 2, P, P, P, P, 1 << 40, None) == UNSUPPORTED
+
+
+def test_attention_validation(lib):
+    f = lib.focus_attention_fwd
+    need = fg.focus_attention_workspace_size(1, 1000, 8, 2, 128, 16, 2)
+    assert need > 0
+
+    def call(Q=P, Hq=8, Hkv=2, d=128, window=16, K=16, topk=2, ws=P, nbytes=need, n=1000, B=1):
+        return f(Q, P, P, B, n, Hq, Hkv, d, window, 0.0, P, P, P, P, K, topk, P2, None, ws,
+                 nbytes, None)
+
+    assert call(Q=None) == INVALID
+    assert call(Q=MIS) == INVALID
+    assert call(Hq=8, Hkv=3) == INVALID                  # Hq % Hkv
+    assert call(window=-1) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(topk=17) == INVALID                      # topk > K
+    assert call(K=2000, topk=2) == UNSUPPORTED
+    assert call(nbytes=need - 1) == WORKSPACE
+    assert call(ws=None) == INVALID
+    assert call(n=0) == INVALID
+
+
+def test_attention_workspace_grows_with_problem(lib):
+    a = fg.focus_attention_workspace_size(1, 1024, 8, 8, 64, 16, 1)
+    b = fg.focus_attention_workspace_size(1, 2048, 8, 8, 64, 16, 1)
+    c = fg.focus_attention_workspace_size(1, 2048, 8, 8, 64, 16, 2)
+    assert 0 < a < b < c
+    assert fg.focus_attention_workspace_size(0, 2048, 8, 8, 64, 16, 2) == 0
+
+
+def test_dense_and_count_validation(lib):
+    assert lib.focus_dense_causal_fwd(None, P, P, 1, 64, 2, 2, 64, 0.0, P2, None, None) == INVALID
+    assert lib.focus_dense_causal_fwd(P, P, P, 1, 64, 2, 2, 80, 0.0, P2, None, None) == UNSUPPORTED
+    assert lib.focus_dense_causal_fwd(P, P, P, 1, 64, 3, 2, 64, 0.0, P2, None, None) == INVALID
+    assert lib.focus_count_pairs(P, P, P, P, 1, 64, 8, 2, 4, None, None, None) == INVALID
+    assert lib.focus_count_pairs(P, P, P, P, 1, 64, 8, 2, -1, None, P, None) == INVALID
+
+
+def test_prefill_validation(lib):
+    f = lib.focus_prefill
+    need = fg.focus_prefill_workspace_size(1, 512, 64, 4, 4, 64, 16, 8, 2, 0)
+    need_host = fg.focus_prefill_workspace_size(1, 512, 64, 4, 4, 64, 16, 8, 2, 1)
+    assert need_host > need > 0
+    args = [P, P, P, P, P, P, 1, 512, 64, 4, 4, 64, 16, 8, 2, 16, 0.0, P2, None, None, P]
+    assert f(*args, need - 1, 0, None) == WORKSPACE
+    bad = list(args)
+    bad[11] = 72      # d
+    assert f(*bad, need, 0, None) == UNSUPPORTED
+    bad = list(args)
+    bad[0] = None
+    assert f(*bad, need, 0, None) == INVALID
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle (test infrastructure only)."""
+    pkg = os.path.join(ROOT, "learned_group_sparse_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
