@@ -3,7 +3,8 @@
 
 One step = focus_prefill on device-resident inputs: centroid scoring and
 top-k (focus_assign), group bucketing (focus_bucket) and Focus attention
-(focus_attention_fwd: gather, group-causal kernel, window kernel, merge).
+(focus_attention_fwd: plan, gather, group-causal kernel, window kernel with
+the log-sum-exp merge fused into its epilogue).
 Prints ONE JSON line (rank 0).  Metric: prefill tokens/s; the line also
 carries effective TFLOP/s over the allowed pairs, the roofline of the
 dominant kernel, the speedup over the library's own dense causal kernel,
@@ -233,8 +234,6 @@ def kernel_work(w, share_pairs, total_pairs):
         "attn_dense": (4.0 * d * Hq * B * n * (n + 1) / 2, "flop", "tensor"),
         "assign": (2.0 * B * n * (w.hidden * w.dg + w.dg * w.K), "flop", "alu"),
         "gather": (2.0 * B * nk * (Hq + 2 * Hkv) * d * 2, "byte", "hbm"),
-        "merge": (1.0 * B * n * ((k + 1) * Hq * d * 2 + (k + 1) * Hq * 4 + Hq * d * 2 + k * 4),
-                  "byte", "hbm"),
         "bucket_count": (4.0 * B * nk, "byte", "hbm"),
         "bucket_scatter": (12.0 * B * nk, "byte", "hbm"),
     }
@@ -381,8 +380,8 @@ def main():
                 "frac": ach / peak, "peak_source": f"{peak_src} (burst)",
                 "traffic": traffic_lookup(dom, w.name, src_hash()),
                 "algorithmic_per_launch": work[0], "algorithmic_unit": work[1]}
-    attn_ms = sum(prof.get(k, (0.0, 1))[0] for k in ("attn_group", "attn_window", "merge",
-                                                      "gather", "plan")) / prof_steps
+    attn_ms = sum(prof.get(k, (0.0, 1))[0] for k in ("attn_group", "attn_window", "gather",
+                                                      "plan")) / prof_steps
 
     # ---- the library's own dense causal kernel on the same Q/K/V
     dense = None

@@ -82,7 +82,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnWs {
-    size_t qp, kp, vp, opart, lpart, owin, lwin, tiles, ntiles, total;
+    size_t qp, kp, vp, opart, lpart, tiles, ntiles, total;
 };
 
 int64_t max_tiles(int B, int n, int K, int topk)
@@ -99,10 +99,8 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
     w.qp = off;    off += align256((size_t)B * nk * Hq * d * 2);
     w.kp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
     w.vp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
-    w.opart = off; off += align256((size_t)B * nk * Hq * d * 2);
+    w.opart = off; off += align256((size_t)B * nk * Hq * d * 4);   // fp32 group partials
     w.lpart = off; off += align256((size_t)B * nk * Hq * 4);
-    w.owin = off;  off += align256((size_t)B * n * Hq * d * 2);
-    w.lwin = off;  off += align256((size_t)B * n * Hq * 4);
     w.tiles = off; off += align256((size_t)max_tiles(B, n, K, topk) * 8);
     w.ntiles = off; off += 256;
     w.total = off;
@@ -211,10 +209,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     auto *Qp = reinterpret_cast<__nv_bfloat16 *>(base + w.qp);
     auto *Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
     auto *Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
-    auto *Opart = reinterpret_cast<__nv_bfloat16 *>(base + w.opart);
+    auto *Opart = reinterpret_cast<float *>(base + w.opart);
     auto *Lpart = reinterpret_cast<float *>(base + w.lpart);
-    auto *Owin = reinterpret_cast<__nv_bfloat16 *>(base + w.owin);
-    auto *Lwin = reinterpret_cast<float *>(base + w.lwin);
     auto *tiles = reinterpret_cast<int2 *>(base + w.tiles);
     auto *ntiles = reinterpret_cast<int *>(base + w.ntiles);
     const int64_t nk = (int64_t)n * topk;
@@ -258,22 +254,24 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.tmV = &mv;
     p.rows = (int)nk;
     p.grid = grid_group;
-    p.out = Opart;
-    p.lse = Lpart;
+    p.part_out = Opart;
+    p.part_lse_out = Lpart;
     if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
+    // The window kernel merges the group parts into the final output.
     p.tmQ = &wq;
     p.tmK = &wk;
     p.tmV = &wv;
     p.rows = n;
     p.grid = grid_win;
-    p.out = Owin;
-    p.lse = Lwin;
+    p.part_out = nullptr;
+    p.part_lse_out = nullptr;
+    p.part_o = Opart;
+    p.part_lse = Lpart;
+    p.inv = inv;
+    p.out = static_cast<__nv_bfloat16 *>(O);
+    p.lse = lse;
     if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
-
-    if ((e = launch_merge(Owin, Lwin, Opart, Lpart, inv, B, n, topk, Hq, d,
-                          static_cast<__nv_bfloat16 *>(O), lse, s, launches)) != cudaSuccess)
-        return FOCUS_ERR_CUDA;
     return FOCUS_OK;
 }
 

@@ -18,8 +18,11 @@
 //   kWindow : original token order; keys with i - window < j <= i that share
 //             no group with the query.
 //   kDense  : plain causal attention (the comparison baseline).
-// Partial results (kGroup, kWindow) are normalised outputs plus a base-2
-// log-sum-exp; kDense writes the final output and a natural-log lse.
+// kGroup writes normalised fp32 partial outputs plus a base-2 log-sum-exp per
+// (group member, head).  kWindow merges, in its epilogue, its own part (still
+// in TMEM) with the topk group parts of the row by the exact log-sum-exp rule
+// and writes the final bf16 output and natural-log lse, so the output is
+// rounded to bf16 once.  kDense writes its output directly.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,9 +45,13 @@ struct AttnArgs {
     const int32_t *pos;    // [B, n*topk]
     const int2 *tiles;     // kGroup work list: (b*K + g, tile index in group)
     const int *ntiles;     // kGroup: number of valid entries in tiles
-    __nv_bfloat16 *out;    // kGroup [B, rows, Hq, D]; kWindow/kDense [B, n, Hq, D]
-    float *lse;            // kGroup [B, rows, Hq] / kWindow [B, n, Hq] base 2;
-                           // kDense [B, Hq, n] natural (nullable)
+    __nv_bfloat16 *out;    // kWindow/kDense: final O [B, n, Hq, D]
+    float *lse;            // kWindow/kDense: final lse [B, Hq, n], natural log (nullable)
+    float *part_out;       // kGroup: normalised partial O [B, rows, Hq, D] fp32
+    float *part_lse_out;   // kGroup: partial lse [B, rows, Hq], base 2
+    const float *part_o;   // kWindow: the group partials to merge (= part_out)
+    const float *part_lse; // kWindow: their lse (= part_lse_out)
+    const int32_t *inv;    // kWindow: [B, n, topk] index of (i, ids[i][s]) in group order
     int *status;           // device status word
     int32_t *pair_count;   // nullable: scored pairs per query (head 0)
 };
@@ -469,19 +476,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars[B_PFULL]);
         }
 
-        // ---- epilogue: O / l and the log-sum-exp
+        // ---- epilogue
         if (ok && nkv > 0) {
             ok = mbar_wait(&bars[B_PVDONE], (nkv - 1) & 1, abort_flag, a.status);
             tc_fence_after();
         }
         const bool has = ok && l > 0.f;
-        const float inv_l = has ? 1.f / l : 0.f;
+        const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // this kernel's part
+        // Output scale of the TMEM accumulator (which holds sum p v with
+        // p = 2^(s - m_ref)) and, for kWindow, the merge with the group parts.
+        float fo = has ? 1.f / l : 0.f;
+        float L2 = lse2;
+        int64_t prt[8];
+        float wpart[8];
+        if (MODE == kWindow) {
+            // Exact softmax over the union of the window part and the topk
+            // group parts: L = log2 sum_p 2^{L_p}, O = sum_p 2^{L_p - L} O_p.
+            float m = lse2;
+            const int nk = a.n * a.topk;     // group-order rows per batch
+            for (int s = 0; s < a.topk; ++s) {
+                prt[s] = -1;
+                wpart[s] = -CUDART_INF_F;
+                if (qvalid) {
+                    const int r = a.inv[((int64_t)b * a.n + qi) * a.topk + s];
+                    if ((unsigned)r < (unsigned)nk) {
+                        prt[s] = ((int64_t)b * nk + r) * a.Hq + h;
+                        wpart[s] = a.part_lse[prt[s]];
+                    }
+                }
+                m = fmaxf(m, wpart[s]);
+            }
+            if (m == -CUDART_INF_F) {
+                L2 = -CUDART_INF_F;
+                fo = 0.f;
+                for (int s = 0; s < a.topk; ++s) wpart[s] = 0.f;
+            } else {
+                float sum = exp2f(lse2 - m);
+                for (int s = 0; s < a.topk; ++s) sum += exp2f(wpart[s] - m);
+                L2 = m + log2f(sum);
+                fo = has ? exp2f(m_ref - L2) : 0.f;     // 2^{L_w - L} / l
+                for (int s = 0; s < a.topk; ++s) wpart[s] = exp2f(wpart[s] - L2);
+            }
+        }
         int64_t orow = 0;
         if (MODE == kGroup)
             orow = ((int64_t)b * a.rows + prow) * a.Hq + h;
         else
             orow = ((int64_t)b * a.n + qi) * a.Hq + h;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             float o[32];
@@ -491,24 +532,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = 0.f;
             }
-            if (qvalid) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 v;
-                    v.x = pack_bf16x2(o[q * 8 + 0] * inv_l, o[q * 8 + 1] * inv_l);
-                    v.y = pack_bf16x2(o[q * 8 + 2] * inv_l, o[q * 8 + 3] * inv_l);
-                    v.z = pack_bf16x2(o[q * 8 + 4] * inv_l, o[q * 8 + 5] * inv_l);
-                    v.w = pack_bf16x2(o[q * 8 + 6] * inv_l, o[q * 8 + 7] * inv_l);
-                    dst[c * 4 + q] = v;
+            for (int e = 0; e < 32; ++e) o[e] *= fo;
+            if (!qvalid) continue;
+            if (MODE == kGroup) {
+                float4 *dst = reinterpret_cast<float4 *>(a.part_out + orow * D + c * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                continue;
+            }
+            if (MODE == kWindow) {
+                for (int s = 0; s < a.topk; ++s) {
+                    if (wpart[s] == 0.f) continue;
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(a.part_o + prt[s] * D + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 v = src[q];
+                        o[4 * q] = fmaf(wpart[s], v.x, o[4 * q]);
+                        o[4 * q + 1] = fmaf(wpart[s], v.y, o[4 * q + 1]);
+                        o[4 * q + 2] = fmaf(wpart[s], v.z, o[4 * q + 2]);
+                        o[4 * q + 3] = fmaf(wpart[s], v.w, o[4 * q + 3]);
+                    }
                 }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = pack_bf16x2(o[q * 8 + 0], o[q * 8 + 1]);
+                v.y = pack_bf16x2(o[q * 8 + 2], o[q * 8 + 3]);
+                v.z = pack_bf16x2(o[q * 8 + 4], o[q * 8 + 5]);
+                v.w = pack_bf16x2(o[q * 8 + 6], o[q * 8 + 7]);
+                dst[c * 4 + q] = v;
             }
         }
         if (qvalid) {
-            const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;
-            if (MODE == kDense) {
-                if (a.lse) a.lse[((int64_t)b * a.Hq + h) * a.n + qi] = lse2 * 0.69314718055994531f;
-            } else {
-                a.lse[orow] = lse2;
+            if (MODE == kGroup) {
+                a.part_lse_out[orow] = lse2;
+            } else if (a.lse) {
+                a.lse[((int64_t)b * a.Hq + h) * a.n + qi] = L2 * 0.69314718055994531f;
             }
             if (a.pair_count && h == 0) atomicAdd(&a.pair_count[(int64_t)b * a.n + qi], cnt);
         }

@@ -31,6 +31,11 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.ntiles = p.ntiles;
     a.out = p.out;
     a.lse = p.lse;
+    a.part_out = p.part_out;
+    a.part_lse_out = p.part_lse_out;
+    a.part_o = p.part_o;
+    a.part_lse = p.part_lse;
+    a.inv = p.inv;
     a.status = p.status;
     a.pair_count = p.pair_count;
     prof_begin(MODE == kGroup ? "attn_group" : MODE == kWindow ? "attn_window" : "attn_dense", s);

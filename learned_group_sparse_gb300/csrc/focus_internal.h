@@ -40,11 +40,6 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                           const __nv_bfloat16 *V, const int32_t *pos, int B, int n, int topk,
                           int Hq, int Hkv, int d, __nv_bfloat16 *Qp, __nv_bfloat16 *Kp,
                           __nv_bfloat16 *Vp, cudaStream_t s, int *launches);
-// O = log-sum-exp merge of the window partial and the topk group partials.
-cudaError_t launch_merge(const __nv_bfloat16 *Owin, const float *Lwin,
-                         const __nv_bfloat16 *Opart, const float *Lpart, const int32_t *inv,
-                         int B, int n, int topk, int Hq, int d, __nv_bfloat16 *O, float *lse,
-                         cudaStream_t s, int *launches);
 cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
                                const int32_t *inv, int B, int n, int K, int topk, int window,
                                int64_t *per_query, int64_t *totals, cudaStream_t s,
@@ -64,6 +59,9 @@ struct AttnLaunch {
     int64_t grid;
     __nv_bfloat16 *out;
     float *lse;
+    float *part_out, *part_lse_out;
+    const float *part_o, *part_lse;
+    const int32_t *inv;
     int *status;
     int32_t *pair_count;
 };
