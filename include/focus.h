@@ -96,6 +96,32 @@ focus_status_t focus_bucket(const int32_t *ids, int B, int n, int K, int topk,
                             void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * focus_bucket_static -- focus_bucket without a workspace argument, for
+ * callers that cannot allocate device memory themselves: code that runs
+ * where cudaMalloc is not allowed, such as inside another allocator's
+ * callback, or in an engine that reserves the device's memory up front and
+ * forbids further allocations while it executes.  (The paper has no
+ * counterpart; this is an interface convenience.)
+ *
+ * Same arguments, results and validation as focus_bucket, minus ws/ws_bytes.
+ * The scratch it needs lives in one fixed array of 16 MiB of device memory
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  Problems whose scratch, focus_bucket_workspace_size(B, n,
+ * K, topk), exceeds 16 MiB are rejected with FOCUS_ERR_UNSUPPORTED (that
+ * limit is far above the sizes this library targets: n = 1M, K = 256 needs
+ * about 0.5 MiB).  The call allocates and frees nothing.
+ *
+ * The first call on a device looks up the array's device address (a runtime
+ * query, once per device); make that first call before any stream capture.
+ * All calls share the one array and each call overwrites the parts it uses
+ * before reading them, so calls that overlap on the GPU (on different
+ * streams, or from different host threads at once) race: serialise them.
+ */
+focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int topk,
+                                   int32_t *offsets, int32_t *pos, int32_t *inv,
+                                   void *stream);
+
+/*
  * focus_attention_fwd -- exact softmax attention over the allowed pairs
  * (gist.science/nl Kerncomponent 3: exact softmax within the allowed pairs;
  * gist.science/zh 2.1.2-2.1.3: local window or shared group, causal).

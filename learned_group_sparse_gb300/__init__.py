@@ -67,6 +67,7 @@ def library() -> ctypes.CDLL:
                 "focus_count_pairs": ([vp] * 4 + [i32] * 5 + [vp, vp, vp], i32),
                 "focus_get_device_status": ([i32], i32),
                 "focus_last_launch_count": ([], i32),
+                "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_profile_enable": ([i32], None),
                 "focus_profile_read": ([vp, i32, vp, vp, i32], i32),
             }
@@ -179,6 +180,25 @@ def focus_bucket(ids, num_groups, offsets=None, pos=None, inv=None, ws=None):
     _check("focus_bucket", library().focus_bucket(
         _p(ids), B, n, num_groups, topk, _p(offsets), _p(pos), _p(inv), _p(ws), ws.numel(),
         _stream(ids)))
+    return offsets, pos, inv
+
+
+def focus_bucket_static(ids, num_groups, offsets=None, pos=None, inv=None):
+    """focus_bucket for callers that cannot allocate device memory: the
+    library's own fixed scratch array replaces the workspace (16 MiB limit;
+    calls overlapping on the GPU race).  Output buffers may be passed in so
+    that nothing at all is allocated."""
+    _need(ids, "ids", torch.int32, 3)
+    B, n, topk = ids.shape
+    dev = ids.device
+    if offsets is None:
+        offsets = torch.empty(B, num_groups + 1, dtype=torch.int32, device=dev)
+    if pos is None:
+        pos = torch.empty(B, n * topk, dtype=torch.int32, device=dev)
+    if inv is None:
+        inv = torch.empty(B, n, topk, dtype=torch.int32, device=dev)
+    _check("focus_bucket_static", library().focus_bucket_static(
+        _p(ids), B, n, num_groups, topk, _p(offsets), _p(pos), _p(inv), _stream(ids)))
     return offsets, pos, inv
 
 

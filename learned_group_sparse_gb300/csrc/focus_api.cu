@@ -277,6 +277,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
 
 }  // namespace
 
+void set_last_launches(int launches) { g_last_launches = launches; }
+
 }  // namespace focus
 
 using namespace focus;

@@ -15,6 +15,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "focus_internal.h"
 
 namespace focus {
@@ -379,3 +381,65 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
 }
 
 }  // namespace focus
+
+// ------------------------------------------------ allocation-free variant
+// focus_bucket_static: the same bucketing for callers that cannot allocate
+// device memory at all (see include/focus.h).  Its scratch (the per-chunk
+// counts and the group totals) lives in the file-scope device array below
+// instead of a caller workspace.  Every GPU that loads the library holds the
+// array until the process exits.
+namespace focus {
+
+namespace {
+
+constexpr size_t kStaticScratchInts = (size_t)1 << 22;   // 16 MiB of int32
+__device__ __align__(256) int32_t g_bucket_scratch[kStaticScratchInts];
+
+constexpr int kMaxDevices = 64;
+int32_t *g_scratch_addr[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mu;
+
+// The array's name is only a host-side stand-in in host code: the device
+// address must come from cudaGetSymbolAddress, looked up once per device
+// with that device current.
+cudaError_t scratch_address(int32_t **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_bucket_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace focus
+
+extern "C" int focus_bucket_static(const int32_t *ids, int B, int n, int K, int topk,
+                                   int32_t *offsets, int32_t *pos, int32_t *inv, void *stream)
+{
+    using namespace focus;
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!ids || !offsets || !pos || !inv) return 1;                       // INVALID_ARG
+    if (!al16(ids) || !al16(offsets) || !al16(pos) || !al16(inv)) return 1;
+    if (B < 1 || n < 0 || K < 1 || topk < 1 || topk > K) return 1;
+    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return 2;             // UNSUPPORTED
+    if (K > 1024 || topk > 8 || B > 65535) return 2;
+    if (bucket_ws_bytes(B, n, K, topk) > kStaticScratchInts * sizeof(int32_t)) return 2;
+    int32_t *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return 4;               // CUDA_ERROR
+    int launches = 0;
+    cudaError_t e = launch_bucket(ids, B, n, K, topk, offsets, pos, inv, scratch,
+                                  static_cast<cudaStream_t>(stream), &launches);
+    if (e != cudaSuccess) return 4;
+    set_last_launches(launches);
+    return 0;
+}

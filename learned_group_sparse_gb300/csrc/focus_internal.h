@@ -14,6 +14,9 @@ namespace focus {
 void prof_begin(const char *name, cudaStream_t s);
 void prof_end(cudaStream_t s);
 
+// Records the kernel count that focus_last_launch_count() reports.
+void set_last_launches(int launches);
+
 struct AssignLaunch {
     const __nv_bfloat16 *X;
     const float *Wg;

@@ -1,0 +1,66 @@
+"""focus_bucket_static: the bucketing entry point for callers that cannot
+allocate device memory (for example code running inside another allocator's
+callback, or an engine that has reserved the device's memory and forbids
+cudaMalloc while it runs).  Instead of a caller workspace it uses a fixed
+scratch array inside the library.
+
+Checked through the C ABI against focus_bucket, which takes a workspace: two
+calls in a row with different shapes, so the second call runs on the scratch
+contents the first one left behind.  Bucketing is integer work, so the
+results must be identical.  This file is collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import learned_group_sparse_gb300 as fg
+from learned_group_sparse_gb300 import build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_dev):
+    build.build()
+    fg.library()
+    yield
+    assert fg.focus_get_device_status(reset=True) == 0
+
+
+def _ids(B, n, K, topk, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    r = torch.rand(B * n, K, generator=g, device="cuda")
+    return torch.topk(r, topk, dim=1).indices.to(torch.int32).view(B, n, topk).contiguous()
+
+
+def _static(ids, K):
+    B, n, topk = ids.shape
+    off = torch.full((B, K + 1), -7, dtype=torch.int32, device="cuda")
+    pos = torch.full((B, n * topk), -7, dtype=torch.int32, device="cuda")
+    inv = torch.full((B, n, topk), -7, dtype=torch.int32, device="cuda")
+    lib = fg.library()
+    st = lib.focus_bucket_static(ctypes.c_void_p(ids.data_ptr()), B, n, K, topk,
+                                 ctypes.c_void_p(off.data_ptr()), ctypes.c_void_p(pos.data_ptr()),
+                                 ctypes.c_void_p(inv.data_ptr()),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, fg.focus_status_string(st)
+    return off, pos, inv
+
+
+def test_static_scratch_matches_workspace_path_twice():
+    for B, n, K, topk, seed in ((2, 50000, 256, 2, 1), (1, 30001, 64, 4, 2)):
+        ids = _ids(B, n, K, topk, seed)
+        got = _static(ids, K)
+        want = fg.focus_bucket(ids, K)
+        torch.cuda.synchronize()
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+
+
+def test_static_rejects_problems_beyond_its_scratch():
+    # K = 1024 and 8M (token, slot) entries need ~8 MiB x 4 of chunk counts
+    need = fg.focus_bucket_workspace_size(4, 1 << 20, 1024, 8)
+    assert need > (16 << 20)
+    P = ctypes.c_void_p(0x10000)
+    assert fg.library().focus_bucket_static(P, 4, 1 << 20, 1024, 8, P, P, P, None) == 2
