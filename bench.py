@@ -232,7 +232,7 @@ def kernel_work(w, share_pairs, total_pairs):
         "attn_group": (4.0 * d * Hq * share_pairs, "flop", "tensor"),
         "attn_window": (4.0 * d * Hq * (total_pairs - share_pairs), "flop", "tensor"),
         "attn_dense": (4.0 * d * Hq * B * n * (n + 1) / 2, "flop", "tensor"),
-        "assign": (2.0 * B * n * (w.hidden * w.dg + w.dg * w.K), "flop", "alu"),
+        "assign": (2.0 * B * n * w.hidden + 4.0 * B * n * k, "byte", "hbm"),
         "gather": (2.0 * B * nk * (Hq + 2 * Hkv) * d * 2, "byte", "hbm"),
         "bucket_count": (4.0 * B * nk, "byte", "hbm"),
         "bucket_scatter": (12.0 * B * nk, "byte", "hbm"),

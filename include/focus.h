@@ -65,13 +65,23 @@ const char *focus_version(void);
  *                          consecutive scores among the top min(topk+1, K)
  *                          (+inf when K == 1); a small margin flags a
  *                          near-tie whose order depends on rounding.
- * Arithmetic: fp32 with fp32 accumulation.
+ *   ws, ws_bytes: device workspace of at least
+ *          focus_assign_workspace_size(hidden, d_g, K, topk) bytes (may be
+ *          NULL when that size is 0).
+ * Arithmetic: fp32-accurate scores.  For K <= 256 and hidden % 64 == 0 the
+ * scores are X . (W_g C^T) on the tensor cores, with W_g C^T (fp32) split
+ * into two bf16 parts (X is exact in bf16), fp32 accumulation; otherwise an
+ * fp32 FMA kernel computes (X W_g) C^T.  Rounding differs from an exact
+ * evaluation only below the margin, so ids can differ only where the margin
+ * is tiny.
  * Supported: hidden % 8 == 0, 1 <= d_g <= 256, 1 <= K <= 1024,
  *            1 <= topk <= min(K, 8).
  */
+size_t focus_assign_workspace_size(int hidden, int d_g, int K, int topk);
 focus_status_t focus_assign(const void *X, const float *Wg, const float *C,
                             int B, int n, int hidden, int d_g, int K, int topk,
-                            int32_t *ids, float *margin, void *stream);
+                            int32_t *ids, float *margin,
+                            void *ws, size_t ws_bytes, void *stream);
 
 /*
  * focus_bucket -- per-group member lists (histogram, exclusive scan, stable
@@ -243,6 +253,17 @@ int focus_last_launch_count(void);
 void focus_profile_enable(int enable);
 int focus_profile_read(char *names, int name_stride, double *total_ms, int *launches,
                        int max_entries);
+
+/*
+ * Pipeline wait tracing of the attention kernels (a debugging aid).  For
+ * launches from this host thread, the group / window / dense kernels write,
+ * per persistent CTA, 32 int64 counters of SM cycles into the given DEVICE
+ * buffers (each at least 32 x the number of SMs entries; NULL disables):
+ * time each role spent waiting on each pipeline barrier, the producer's
+ * work-item preparation, the softmax epilogue, and item and tile counts.
+ * Slot meanings are listed with the kernels' trace enum.
+ */
+void focus_trace_attention(long long *group_buf, long long *window_buf, long long *dense_buf);
 
 #ifdef __cplusplus
 }

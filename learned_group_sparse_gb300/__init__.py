@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "FocusError", "library", "library_path",
-    "focus_assign", "focus_bucket", "focus_attention_fwd", "focus_attention_fwd_counted",
+    "focus_assign", "focus_assign_workspace_size", "focus_bucket", "focus_attention_fwd", "focus_attention_fwd_counted",
     "focus_prefill", "focus_dense_causal_fwd", "focus_count_pairs",
     "focus_bucket_workspace_size", "focus_attention_workspace_size",
     "focus_prefill_workspace_size", "focus_get_device_status", "focus_last_launch_count",
@@ -52,7 +52,8 @@ def library() -> ctypes.CDLL:
             sig = {
                 "focus_status_string": ([i32], ctypes.c_char_p),
                 "focus_version": ([], ctypes.c_char_p),
-                "focus_assign": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp], i32),
+                "focus_assign_workspace_size": ([i32] * 4, sz),
+                "focus_assign": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp, sz, vp], i32),
                 "focus_bucket_workspace_size": ([i32, i32, i32, i32], sz),
                 "focus_bucket": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], i32),
                 "focus_attention_workspace_size": ([i32] * 7, sz),
@@ -69,6 +70,7 @@ def library() -> ctypes.CDLL:
                 "focus_last_launch_count": ([], i32),
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_profile_enable": ([i32], None),
+                "focus_trace_attention": ([vp, vp, vp], None),
                 "focus_profile_read": ([vp, i32, vp, vp, i32], i32),
             }
             for name, (args, res) in sig.items():
@@ -142,7 +144,17 @@ def focus_profile_read(max_entries: int = 64) -> dict:
     return out
 
 
-def focus_assign(X, Wg, C, topk, ids=None, margin=None, with_margin=True):
+def focus_trace_attention(group_buf=None, window_buf=None, dense_buf=None) -> None:
+    """Sets (or with None clears) the per-CTA wait-trace buffers, int64 CUDA
+    tensors of >= 32 x SM-count entries, of the group/window/dense kernels."""
+    library().focus_trace_attention(_p(group_buf), _p(window_buf), _p(dense_buf))
+
+
+def focus_assign_workspace_size(hidden, dg, K, topk) -> int:
+    return int(library().focus_assign_workspace_size(hidden, dg, K, topk))
+
+
+def focus_assign(X, Wg, C, topk, ids=None, margin=None, with_margin=True, ws=None):
     """X [B, n, hidden] bf16, Wg [hidden, d_g] fp32, C [K, d_g] fp32 ->
     (ids [B, n, topk] int32, margin [B, n] fp32 or None)."""
     _need(X, "X", torch.bfloat16, 3)
@@ -154,8 +166,12 @@ def focus_assign(X, Wg, C, topk, ids=None, margin=None, with_margin=True):
         ids = torch.empty(B, n, topk, dtype=torch.int32, device=X.device)
     if margin is None and with_margin:
         margin = torch.empty(B, n, dtype=torch.float32, device=X.device)
+    need = focus_assign_workspace_size(hidden, dg, K, topk)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=X.device)
     _check("focus_assign", library().focus_assign(
-        _p(X), _p(Wg), _p(C), B, n, hidden, dg, K, topk, _p(ids), _p(margin), _stream(X)))
+        _p(X), _p(Wg), _p(C), B, n, hidden, dg, K, topk, _p(ids), _p(margin), _p(ws),
+        0 if ws is None else ws.numel(), _stream(X)))
     return ids, margin
 
 

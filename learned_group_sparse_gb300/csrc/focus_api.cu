@@ -78,11 +78,30 @@ bool make_map(CUtensorMap *m, const void *base, int B, int64_t rows, int H, int 
            CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool make_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+namespace {
+
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnWs {
-    size_t qp, kp, vp, opart, lpart, tiles, ntiles, total;
+    size_t qp, kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, total;
 };
 
 int64_t max_tiles(int B, int n, int K, int topk)
@@ -99,8 +118,11 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
     w.qp = off;    off += align256((size_t)B * nk * Hq * d * 2);
     w.kp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
     w.vp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
-    w.opart = off; off += align256((size_t)B * nk * Hq * d * 4);   // fp32 group partials
-    w.lpart = off; off += align256((size_t)B * nk * Hq * 4);
+    w.gidp = off;  off += align256((size_t)B * nk * topk * 4);
+    w.opart = off; off += align256((size_t)B * nk * Hq * d * 2);   // fp16 group partials
+    w.lpart = off; off += align256((size_t)B * nk * Hq * 8);       // {lse, scale}
+    w.owin = off;  off += align256((size_t)B * n * Hq * d * 2);    // fp16 window partials
+    w.lwin = off;  off += align256((size_t)B * n * Hq * 8);
     w.tiles = off; off += align256((size_t)max_tiles(B, n, K, topk) * 8);
     w.ntiles = off; off += 256;
     w.total = off;
@@ -108,7 +130,7 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
 }
 
 struct PrefillWs {
-    size_t ids, offsets, pos, inv, bucket, attn, x, wg, c, q, k, v, o, lse, total;
+    size_t ids, offsets, pos, inv, assign, bucket, attn, x, wg, c, q, k, v, o, lse, total;
 };
 
 PrefillWs prefill_ws(int B, int n, int hidden, int Hq, int Hkv, int d, int dg, int K, int topk,
@@ -121,6 +143,7 @@ PrefillWs prefill_ws(int B, int n, int hidden, int Hq, int Hkv, int d, int dg, i
     w.offsets = off; off += align256((size_t)B * (K + 1) * 4);
     w.pos = off;     off += align256((size_t)B * nk * 4);
     w.inv = off;     off += align256((size_t)B * nk * 4);
+    w.assign = off;  off += align256(assign_ws_bytes(hidden, K));
     w.bucket = off;  off += align256(bucket_ws_bytes(B, n, K, topk));
     w.attn = off;    off += align256(attn_ws(B, n, Hq, Hkv, d, K, topk).total);
     w.x = w.wg = w.c = w.q = w.k = w.v = w.o = w.lse = 0;
@@ -193,6 +216,7 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if (st) return st;
     if (K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
     if (K > 1024 || topk > 8 || (int64_t)B * K > 4096) return FOCUS_ERR_UNSUPPORTED;
+    if (attn_smem_needed(d, K, topk) > kMaxSmemPerBlock) return FOCUS_ERR_UNSUPPORTED;
     if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
     const AttnWs w = attn_ws(B, n, Hq, Hkv, d, K, topk);
     if (ws_bytes < w.total) return FOCUS_ERR_WORKSPACE;
@@ -209,8 +233,11 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     auto *Qp = reinterpret_cast<__nv_bfloat16 *>(base + w.qp);
     auto *Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
     auto *Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
-    auto *Opart = reinterpret_cast<float *>(base + w.opart);
-    auto *Lpart = reinterpret_cast<float *>(base + w.lpart);
+    auto *gidp = reinterpret_cast<int32_t *>(base + w.gidp);
+    auto *Opart = reinterpret_cast<__half *>(base + w.opart);
+    auto *Mpart = reinterpret_cast<float2 *>(base + w.lpart);
+    auto *Owin = reinterpret_cast<__half *>(base + w.owin);
+    auto *Mwin = reinterpret_cast<float2 *>(base + w.lwin);
     auto *tiles = reinterpret_cast<int2 *>(base + w.tiles);
     auto *ntiles = reinterpret_cast<int *>(base + w.ntiles);
     const int64_t nk = (int64_t)n * topk;
@@ -233,7 +260,6 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.scale_log2 = sc * 1.4426950408889634f;
     p.K = K;
     p.topk = topk;
-    p.ids = ids;
     p.offsets = offsets;
     p.pos = pos;
     p.tiles = tiles;
@@ -245,33 +271,33 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
         return FOCUS_ERR_CUDA;
     if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Q),
                            static_cast<const __nv_bfloat16 *>(Kt),
-                           static_cast<const __nv_bfloat16 *>(V), pos, B, n, topk, Hq, Hkv, d,
-                           Qp, Kp, Vp, s, launches)) != cudaSuccess)
+                           static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hq,
+                           Hkv, d, Qp, Kp, Vp, gidp, s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
 
     p.tmQ = &mq;
     p.tmK = &mk;
     p.tmV = &mv;
     p.rows = (int)nk;
+    p.gids = gidp;
     p.grid = grid_group;
-    p.part_out = Opart;
-    p.part_lse_out = Lpart;
+    p.part_out16 = Opart;
+    p.part_meta_out = Mpart;
     if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
-    // The window kernel merges the group parts into the final output.
     p.tmQ = &wq;
     p.tmK = &wk;
     p.tmV = &wv;
     p.rows = n;
+    p.gids = ids;
     p.grid = grid_win;
-    p.part_out = nullptr;
-    p.part_lse_out = nullptr;
-    p.part_o = Opart;
-    p.part_lse = Lpart;
-    p.inv = inv;
-    p.out = static_cast<__nv_bfloat16 *>(O);
-    p.lse = lse;
+    p.win_out16 = Owin;
+    p.win_meta_out = Mwin;
     if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+
+    if ((e = launch_merge(Owin, Mwin, Opart, Mpart, inv, B, n, topk, Hq, d,
+                          static_cast<__nv_bfloat16 *>(O), lse, s, launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
     return FOCUS_OK;
 }
 
@@ -302,16 +328,29 @@ const char *focus_version(void) { return "focus-gb300 0.1.0 sm_103a"; }
 
 int focus_last_launch_count(void) { return g_last_launches; }
 
+size_t focus_assign_workspace_size(int hidden, int d_g, int K, int topk)
+{
+    if (hidden < 1 || d_g < 1 || K < 1 || topk < 1) return 0;
+    return assign_tc_supported(hidden, K, topk) ? assign_ws_bytes(hidden, K) : 0;
+}
+
 focus_status_t focus_assign(const void *X, const float *Wg, const float *C, int B, int n,
                             int hidden, int d_g, int K, int topk, int32_t *ids, float *margin,
-                            void *stream)
+                            void *ws, size_t ws_bytes, void *stream)
 {
     focus_status_t st = check_assign(X, Wg, C, B, n, hidden, d_g, K, topk, ids, margin);
     if (st) return st;
+    const bool tc = assign_tc_supported(hidden, K, topk);
+    if (tc && (!ws || ws_bytes < assign_ws_bytes(hidden, K))) return FOCUS_ERR_WORKSPACE;
+    if (tc && !aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
+    int *status = nullptr;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
     int launches = 0;
     AssignLaunch p{static_cast<const __nv_bfloat16 *>(X), Wg, C, (int64_t)B * n, hidden, d_g, K,
                    topk, ids, margin};
-    cudaError_t e = launch_assign(p, static_cast<cudaStream_t>(stream), &launches);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tc ? launch_assign_tc(p, ws, status, s, &launches)
+                       : launch_assign(p, s, &launches);
     if (e == cudaSuccess) g_last_launches = launches;
     return cuda_status(e);
 }
@@ -438,7 +477,14 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     }
     AssignLaunch ap{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden, d_g,
                     num_groups, topk, ids, nullptr};
-    if ((e = launch_assign(ap, s, &launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (assign_tc_supported(hidden, num_groups, topk)) {
+        int *status = nullptr;
+        if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+        e = launch_assign_tc(ap, base + w.assign, status, s, &launches);
+    } else {
+        e = launch_assign(ap, s, &launches);
+    }
+    if (e != cudaSuccess) return FOCUS_ERR_CUDA;
     if ((e = launch_bucket(ids, B, n, num_groups, topk, offsets, pos, inv, base + w.bucket, s,
                            &launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;

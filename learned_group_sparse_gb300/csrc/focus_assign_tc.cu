@@ -1,0 +1,277 @@
+// Centroid scoring and hard top-k on the tensor cores (Focus, gist.science/zh
+// technical summary 2.1.1 and 2.1.3).
+//
+// The scores s = (X W_g) C^T are formed as s = X M with M = W_g C^T
+// ([hidden, K], fp32, once per call).  X is exactly bf16, so splitting M into
+// two bf16 parts M = M_hi + M_lo (residual below 2^-17 of |M|) and running two
+// tcgen05 bf16 MMAs with fp32 accumulation gives fp32-accurate scores:
+//   S[128 tokens, Kp] (TMEM) = X_tile . M_hi^T + X_tile . M_lo^T.
+// The epilogue keeps each token's top-(k+1) scores in registers (one thread
+// per token = TMEM lane), in descending order with ties to the lower id, and
+// writes the ids and the smallest gap between consecutive kept scores.
+//
+// CTA: warps 0-3 epilogue, warp 4 TMA producer, warp 5 TMEM allocator + MMA.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "focus_internal.h"
+#include "focus_ptx.cuh"
+
+namespace focus {
+
+namespace {
+
+constexpr int kTokens = 128;   // tokens per CTA (MMA M)
+constexpr int kHK = 64;        // hidden per pipeline stage (one 128-byte swizzle row)
+constexpr int kMaxSel = 9;     // top-(k+1), k <= 8
+
+// (score, id) order: larger score first, equal scores -> lower id first.
+__device__ __forceinline__ bool better(float s1, int i1, float s2, int i2)
+{
+    return s1 > s2 || (s1 == s2 && i1 < i2);
+}
+
+// M^T split: mhi[c][h], mlo[c][h] for c < Kp (rows >= K are zero).
+__global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restrict__ Wg,
+                                                          const float *__restrict__ C,
+                                                          int hidden, int dg, int K, int Kp,
+                                                          __nv_bfloat16 *__restrict__ mhi,
+                                                          __nv_bfloat16 *__restrict__ mlo)
+{
+    // block: 32 centroids x 8 hidden rows per pass; C rows staged in shared memory
+    extern __shared__ float csm[];   // [dg][32]
+    const int c0 = blockIdx.y * 32;
+    for (int i = threadIdx.x; i < 32 * dg; i += blockDim.x) {
+        const int c = i / dg, e = i - c * dg;
+        csm[e * 32 + c] = (c0 + c < K) ? C[(int64_t)(c0 + c) * dg + e] : 0.f;
+    }
+    __syncthreads();
+    const int tc = threadIdx.x & 31, th = threadIdx.x >> 5;
+    for (int h = blockIdx.x * 8 + th; h < hidden; h += gridDim.x * 8) {
+        const float *w = Wg + (int64_t)h * dg;
+        float acc = 0.f;
+        for (int e = 0; e < dg; ++e) acc = fmaf(w[e], csm[e * 32 + tc], acc);
+        const int c = c0 + tc;
+        if (c < Kp) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+            mhi[(int64_t)c * hidden + h] = hi;
+            mlo[(int64_t)c * hidden + h] = lo;
+        }
+    }
+}
+
+struct TcArgs {
+    int64_t ntok;
+    int hidden, K, Kp, topk, stages;
+    int32_t *ids;
+    float *margin;
+    int *status;
+};
+
+__device__ __forceinline__ uint32_t tc_stage_bytes(int Kp) { return 128u * kTokens + 2u * 128u * Kp; }
+
+__global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                           const __grid_constant__ CUtensorMap tmHi,
+                                                           const __grid_constant__ CUtensorMap tmLo,
+                                                           const TcArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t stage_bytes = tc_stage_bytes(a.Kp);   // multiple of 1024
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + a.stages * stage_bytes);
+    // bars: full[stages], empty[stages], done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * a.stages + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsteps = a.hidden / kHK;
+    const int64_t t0 = (int64_t)blockIdx.x * kTokens;
+    uint32_t ncols = 32;
+    while ((int)ncols < a.Kp) ncols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&bars[s], 1);
+            mbar_init(&bars[a.stages + s], 1);
+        }
+        mbar_init(&bars[2 * a.stages], 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, ncols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmHi);
+        tma_prefetch_desc(&tmLo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            for (int k = 0; k < nsteps; ++k) {
+                const int st = k % a.stages;
+                if (k >= a.stages &&
+                    !mbar_wait(&bars[a.stages + st], ((k / a.stages) - 1) & 1, abort_flag, a.status))
+                    break;
+                uint8_t *base = sm + st * stage_bytes;
+                mbar_arrive_expect_tx(&bars[st], stage_bytes);
+                tma_load_2d(base, &tmX, &bars[st], k * kHK, (int)t0);
+                tma_load_2d(base + 128 * kTokens, &tmHi, &bars[st], k * kHK, 0);
+                tma_load_2d(base + 128 * kTokens + 128 * a.Kp, &tmLo, &bars[st], k * kHK, 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTokens, a.Kp, false, false);
+            bool ok = true;
+            for (int k = 0; k < nsteps && ok; ++k) {
+                const int st = k % a.stages;
+                ok = mbar_wait(&bars[st], (k / a.stages) & 1, abort_flag, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t xa = smem_u32(sm + st * stage_bytes);
+                const uint32_t hb = xa + 128 * kTokens;
+                const uint32_t lb = hb + 128 * a.Kp;
+#pragma unroll
+                for (int kk = 0; kk < kHK / 16; ++kk) {
+                    const uint64_t ad = sdesc_sw128(xa + kk * 32, 16, 1024);
+                    tc_mma_bf16(tmem, ad, sdesc_sw128(hb + kk * 32, 16, 1024), idesc,
+                                (k > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_bf16(tmem, ad, sdesc_sw128(lb + kk * 32, 16, 1024), idesc, 1u);
+                }
+                tc_commit(&bars[a.stages + st]);
+            }
+            if (ok) tc_commit(&bars[2 * a.stages]);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: thread = token row = TMEM lane
+        const int r = threadIdx.x;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool ok = mbar_wait(&bars[2 * a.stages], 0, abort_flag, a.status);
+        tc_fence_after();
+        const int nsel = min(a.topk + 1, a.K);
+        float bs[kMaxSel];
+        int bi[kMaxSel];
+#pragma unroll
+        for (int j = 0; j < kMaxSel; ++j) {
+            bs[j] = -CUDART_INF_F;
+            bi[j] = 0x7fffffff;
+        }
+        for (int c0 = 0; c0 < a.Kp; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + c0, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                int ci = c0 + e;
+                float cv = v[e];
+                if (cv != cv) cv = -CUDART_INF_F;
+                // ids arrive in increasing order, so a tie never displaces a kept id
+                if (ci >= a.K || !better(cv, ci, bs[kMaxSel - 1], bi[kMaxSel - 1])) continue;
+#pragma unroll
+                for (int j = 0; j < kMaxSel; ++j) {
+                    if (better(cv, ci, bs[j], bi[j])) {
+                        const float ts = bs[j];
+                        const int ti = bi[j];
+                        bs[j] = cv;
+                        bi[j] = ci;
+                        cv = ts;
+                        ci = ti;
+                    }
+                }
+            }
+        }
+        const int64_t tok = t0 + r;
+        if (ok && tok < a.ntok) {
+#pragma unroll
+            for (int j = 0; j < kMaxSel; ++j)
+                if (j < a.topk) a.ids[tok * a.topk + j] = bi[j];
+            if (a.margin) {
+                float gap = CUDART_INF_F;
+#pragma unroll
+                for (int j = 1; j < kMaxSel; ++j)
+                    if (j < nsel) gap = fminf(gap, bs[j - 1] - bs[j]);
+                a.margin[tok] = gap;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
+}  // namespace
+
+int assign_tc_kp(int K) { return (K + 15) / 16 * 16; }
+
+bool assign_tc_supported(int hidden, int K, int topk)
+{
+    return K <= 256 && hidden % kHK == 0 && topk <= 8;
+}
+
+size_t assign_ws_bytes(int hidden, int K)
+{
+    if (K > 256) return 0;
+    return 2 * (size_t)assign_tc_kp(K) * hidden * sizeof(__nv_bfloat16) + 256;
+}
+
+cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaStream_t s,
+                             int *launches)
+{
+    const int Kp = assign_tc_kp(p.K);
+    __nv_bfloat16 *mhi = static_cast<__nv_bfloat16 *>(ws);
+    __nv_bfloat16 *mlo = mhi + (size_t)Kp * p.hidden;
+    {
+        const dim3 grid((unsigned)((p.hidden + 7) / 8), (unsigned)((Kp + 31) / 32));
+        const size_t smem = sizeof(float) * 32 * (size_t)p.dg;
+        cudaError_t e = cudaFuncSetAttribute(assign_prep_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        prof_begin("assign_prep", s);
+        assign_prep_kernel<<<grid, 256, smem, s>>>(p.Wg, p.C, p.hidden, p.dg, p.K, Kp, mhi, mlo);
+        prof_end(s);
+        *launches += 1;
+    }
+    if (p.ntok == 0) return cudaGetLastError();
+    CUtensorMap mx, mh, ml;
+    if (!make_map_2d_bf16(&mx, p.X, (uint64_t)p.hidden, (uint64_t)p.ntok, kHK, kTokens) ||
+        !make_map_2d_bf16(&mh, mhi, (uint64_t)p.hidden, (uint64_t)Kp, kHK, (uint32_t)Kp) ||
+        !make_map_2d_bf16(&ml, mlo, (uint64_t)p.hidden, (uint64_t)Kp, kHK, (uint32_t)Kp))
+        return cudaErrorInvalidValue;
+    TcArgs a;
+    a.ntok = p.ntok;
+    a.hidden = p.hidden;
+    a.K = p.K;
+    a.Kp = Kp;
+    a.topk = p.topk;
+    const uint32_t stage = 128u * kTokens + 2u * 128u * Kp;
+    a.stages = Kp <= 128 ? 4 : 2;
+    a.ids = p.ids;
+    a.margin = p.margin;
+    a.status = status;
+    const size_t smem = (size_t)a.stages * stage + (2 * a.stages + 1) * 8 + 16 + 1024;
+    cudaError_t e = cudaFuncSetAttribute(assign_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (p.ntok + kTokens - 1) / kTokens;
+    prof_begin("assign", s);
+    assign_tc_kernel<<<(unsigned)blocks, 192, smem, s>>>(mx, mh, ml, a);
+    prof_end(s);
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+}  // namespace focus

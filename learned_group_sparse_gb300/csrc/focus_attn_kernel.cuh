@@ -1,11 +1,18 @@
 // Flash-attention mainloop for sm_103a on the 5th-generation tensor cores:
 // TMA loads Q/K/V tiles into 128-byte-swizzled shared memory, one thread
 // issues tcgen05.mma into TMEM accumulators, and a warpgroup runs the online
-// softmax reading S from TMEM and writing P (bf16) back to shared memory.
+// softmax reading S from TMEM and writing P (bf16) back into TMEM over the
+// same columns, where the P.V product reads it as its A operand.  MMAs from
+// one thread execute in issue order, so S of tile t+2 (same columns) is
+// written only after P.V of tile t has read P.
 //
-// One CTA computes one 128-row query tile of one head:
+// Persistent: one CTA per SM walks the work items (128-row query tile x head)
+// item = blockIdx.x, blockIdx.x + gridDim.x, ...  The pipeline (K/V stages,
+// S buffers, barrier phases) runs on across items, so the next item's Q/K/V
+// loads and first Q.K^T overlap the current item's softmax and epilogue.
 //   warps 0-3  softmax + epilogue (thread r owns query row r = TMEM lane r)
-//   warp  4    TMA producer (Q once, K/V double-buffered) + key metadata
+//   warp  4    TMA producer (Q per item, K/V double-buffered) + key-tile
+//              group bitmaps for the masks
 //   warp  5    TMEM allocator and MMA issuer
 // TMEM columns: S double buffer at [0,128) and [128,256), O at [256,256+D).
 //
@@ -18,17 +25,25 @@
 //   kWindow : original token order; keys with i - window < j <= i that share
 //             no group with the query.
 //   kDense  : plain causal attention (the comparison baseline).
-// kGroup writes normalised fp32 partial outputs plus a base-2 log-sum-exp per
-// (group member, head).  kWindow merges, in its epilogue, its own part (still
-// in TMEM) with the topk group parts of the row by the exact log-sum-exp rule
-// and writes the final bf16 output and natural-log lse, so the output is
-// rounded to bf16 once.  kDense writes its output directly.
+// kGroup and kWindow write partial results: the normalised output of every
+// (row, head) in fp16, scaled by a power of two 2^-e that puts its largest
+// entry in [2^14, 2^15) (11-bit precision at any magnitude, no overflow), and
+// {base-2 log-sum-exp, 2^e}.  The merge kernel combines them.  kDense writes
+// its final bf16 output directly.
+//
+// Group masks: for every key tile the producer builds colbits[g][4], the set
+// of the tile's 128 key columns whose token belongs to group g.  A query row
+// excludes the columns in the union of colbits over the groups that must not
+// be shared (all its groups for kWindow; its groups below the tile's group
+// for kGroup): k lookups of 16 bytes instead of a test per column.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "focus_ptx.cuh"
+#include "focus_tmem_wide.cuh"
 
 namespace focus {
 
@@ -40,25 +55,42 @@ struct AttnArgs {
     int window;
     float scale_log2;      // softmax scale * log2(e)
     int K, topk;
-    const int32_t *ids;    // [B, n, topk]
+    const int32_t *gids;   // group ids per Q/K/V row: [B, rows, topk]
     const int32_t *offsets;  // [B, K+1]
-    const int32_t *pos;    // [B, n*topk]
+    const int32_t *pos;    // [B, n*topk] token of each group-order row
     const int2 *tiles;     // kGroup work list: (b*K + g, tile index in group)
     const int *ntiles;     // kGroup: number of valid entries in tiles
-    __nv_bfloat16 *out;    // kWindow/kDense: final O [B, n, Hq, D]
-    float *lse;            // kWindow/kDense: final lse [B, Hq, n], natural log (nullable)
-    float *part_out;       // kGroup: normalised partial O [B, rows, Hq, D] fp32
-    float *part_lse_out;   // kGroup: partial lse [B, rows, Hq], base 2
-    const float *part_o;   // kWindow: the group partials to merge (= part_out)
-    const float *part_lse; // kWindow: their lse (= part_lse_out)
-    const int32_t *inv;    // kWindow: [B, n, topk] index of (i, ids[i][s]) in group order
+    __nv_bfloat16 *out;    // kDense: O [B, n, Hq, D]
+    float *lse;            // kDense: lse [B, Hq, n], natural log (nullable)
+    // partial results: O / l as fp16 scaled by 2^-e, and {lse base 2, 2^e}
+    __half *part_out16;    // kGroup  [B, rows, Hq, D]
+    float2 *part_meta_out; // kGroup  [B, rows, Hq]
+    __half *win_out16;     // kWindow [B, n, Hq, D]
+    float2 *win_meta_out;  // kWindow [B, n, Hq]
     int *status;           // device status word
     int32_t *pair_count;   // nullable: scored pairs per query (head 0)
+    long long *trace;      // nullable: per-CTA wait/phase cycle counters [grid][32]
 };
+
+// Per-CTA trace slots (SM cycles): producer 0-5, MMA issuer 8-14, softmax 16-24.
+enum {
+    TR_P_IEMPTY = 0, TR_P_QEMPTY = 1, TR_P_KEMPTY = 2, TR_P_VEMPTY = 3, TR_P_TOTAL = 4,
+    TR_P_RING = 5, TR_M_PFULL = 8, TR_M_VFULL = 9, TR_M_IFULL = 10, TR_M_QFULL = 11,
+    TR_M_KFULL = 12, TR_M_SEMPTY = 13, TR_M_TOTAL = 14, TR_S_IFULL = 16, TR_S_META = 17,
+    TR_S_SFULL = 18, TR_S_PVDONE = 19, TR_S_PVLAST = 20, TR_S_EPI = 21, TR_S_TOTAL = 22,
+    TR_S_ITEMS = 23, TR_S_TILES = 24, TR_E_TMEM = 25, TR_E_SCALE = 26, TR_E_STORE = 27,
+    TR_T_SLOAD = 28, TR_T_MASK = 29, TR_T_RESCALE = 30, TR_T_P = 31, kTraceSlots = 32
+};
+
+__device__ __forceinline__ void trace_flush(const long long *tr, long long *dst, int lo, int hi)
+{
+    for (int i = lo; i < hi; ++i) dst[i] = tr[i];
+}
 
 constexpr int kThreads = 192;
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // key rows per tile
+constexpr int kMaxTopk = 8;
 
 template <int D>
 struct AttnSmem {
@@ -66,21 +98,51 @@ struct AttnSmem {
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + kTile;               // 2 stages
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 stages
-    static constexpr uint32_t kP = kV + 2 * kTile;           // 128 x 128 bf16
-    static constexpr uint32_t kTok = kP + kBM * kBN * 2;     // int32 [2][128]
-    static constexpr uint32_t kSig = kTok + 2 * kBN * 4;     // uint64 [2][128]
-    static constexpr uint32_t kGid = kSig + 2 * kBN * 8;     // int32 [2][128][8]
-    static constexpr uint32_t kBar = kGid + 2 * kBN * 8 * 4; // 17 mbarriers
-    static constexpr uint32_t kMisc = kBar + 17 * 8;         // tmem slot, abort flag
-    static constexpr uint32_t kBytes = kMisc + 16;
-    static constexpr uint32_t kAlloc = kBytes + 1024;        // slack for 1 KB alignment
+    static constexpr uint32_t kP = kV + 2 * kTile;           // epilogue staging, 128 x D x 2 B
+    static constexpr uint32_t kBar = kP + kBM * D * 2;       // 22 mbarriers
+    static constexpr uint32_t kMisc = kBar + 22 * 8;         // tmem slot, abort flag
+    static constexpr uint32_t kTrace = kMisc + 16;           // int64 [32] trace counters
+    static constexpr uint32_t kColbits = (kTrace + 256 + 127) / 128 * 128;   // uint32 [2][K][4]
+    // then the work-item ring: 2 slots of ring_slot_bytes()
+    __host__ __device__ static constexpr uint32_t colbits_bytes(int K)
+    {
+        return 2u * 16u * (uint32_t)K;
+    }
+    __host__ __device__ static constexpr uint32_t ring_slot_bytes(int mode, int topk)
+    {
+        return (32u + 128u * 4u * (uint32_t)topk + 127u) / 128u * 128u;
+    }
+    // dynamic shared memory of a launch (K groups and topk are 0 for kDense)
+    __host__ __device__ static constexpr uint32_t bytes(int mode, int K, int topk)
+    {
+        return kColbits + colbits_bytes(K) + 2u * ring_slot_bytes(mode, topk) + 1024u;
+    }
 };
 
 // mbarrier slots
 enum {
-    B_QFULL = 0, B_KFULL = 1, B_VFULL = 3, B_KEMPTY = 5, B_VEMPTY = 7, B_SFULL = 9,
-    B_SEMPTY = 11, B_PFULL = 13, B_PVDONE = 14, B_META = 15
+    B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_VEMPTY = 8,
+    B_SFULL = 10, B_SEMPTY = 12, B_PFULL = 14, B_PVDONE = 15, B_META = 16, B_IFULL = 18,
+    B_IEMPTY = 20
 };
+
+// Work-item ring slot: the decoded item (8 ints) followed by the group ids of
+// its 128 query rows, [128][topk].
+struct RingSlot {
+    int *item;
+    int *gid;
+};
+
+template <int D>
+__device__ __forceinline__ RingSlot ring_slot(uint8_t *sm, int mode, int K, int topk, int slot)
+{
+    using L = AttnSmem<D>;
+    uint8_t *base = sm + L::kColbits + L::colbits_bytes(K) + slot * L::ring_slot_bytes(mode, topk);
+    RingSlot r;
+    r.item = reinterpret_cast<int *>(base);
+    r.gid = r.item + 8;
+    return r;
+}
 
 // Bit mask of columns c in [lo, hi] within the 32-column word starting at c0.
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int c0)
@@ -94,6 +156,88 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int c0)
     return upto_b & ~below_a;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+struct WorkItem {
+    int b, h, q0, qend, kv_lo, nkv, g, gend;
+};
+
+// O *= f for this thread's TMEM lane (D columns).  Rarely taken (the row max
+// has to grow by more than 2^8), so it is kept out of line: its registers do
+// not add to those of the softmax loop.
+template <int D>
+__device__ __noinline__ void rescale_o(uint32_t taddr, float f)
+{
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(taddr + c * 32, o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] *= f;
+        tmem_st32(taddr + c * 32, o);
+    }
+    tmem_st_wait();
+}
+
+template <int MODE>
+__device__ __forceinline__ int total_items(const AttnArgs &a)
+{
+    if (MODE == kGroup) return (*a.ntiles) * a.Hq;
+    return a.B * ((a.n + kBM - 1) / kBM) * a.Hq;
+}
+
+// The k-th item of CTA c among G persistent CTAs: rounds of G items, walked
+// forwards in even rounds and backwards in odd ones, so that on a list sorted
+// by decreasing cost every CTA gets a similar total.
+__device__ __forceinline__ int item_of(int k, int c, int G)
+{
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// Work item -> query tile.  Heads vary fastest, so the heads that share a key
+// tile run side by side; items come heaviest first (kGroup: the tile list is
+// ordered by decreasing cost; kDense: the last query tiles first).
+template <int MODE>
+__device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int item)
+{
+    WorkItem w;
+    w.g = 0;
+    w.gend = 0;
+    if (MODE == kGroup) {
+        const int tr = item / a.Hq;
+        w.h = item - tr * a.Hq;
+        const int2 tl = a.tiles[tr];
+        w.b = tl.x / a.K;
+        w.g = tl.x - w.b * a.K;
+        const int gs = a.offsets[w.b * (a.K + 1) + w.g];
+        w.gend = a.offsets[w.b * (a.K + 1) + w.g + 1];
+        w.q0 = gs + kBM * tl.y;
+        w.qend = min(w.q0 + kBM, w.gend);
+        w.kv_lo = gs;
+        w.nkv = tl.y + 1;
+    } else {
+        const int nqt = (a.n + kBM - 1) / kBM;
+        w.h = item % a.Hq;
+        const int rest = item / a.Hq;
+        int qt = rest % nqt;
+        w.b = rest / nqt;
+        if (MODE == kDense) qt = nqt - 1 - qt;
+        w.q0 = kBM * qt;
+        w.qend = min(w.q0 + kBM, a.n);
+        if (MODE == kDense) {
+            w.kv_lo = 0;
+            w.nkv = qt + 1;
+        } else {
+            w.kv_lo = max(0, w.q0 - a.window + 1);
+            w.nkv = a.window > 0 ? (w.qend - w.kv_lo + kBN - 1) / kBN : 0;
+        }
+    }
+    return w;
+}
+
 template <int MODE, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     focus_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -103,39 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = AttnSmem<D>;
     constexpr int kChunks = D / 64;   // 64-column (128-byte) chunks per row
 
-    // ---------------------------------------------------------- work item
-    int h, b, q0, qend, kv_lo, nkv, g = 0, gend = 0;
-    if (MODE == kGroup) {
-        const int tr = blockIdx.x / a.Hq;
-        h = blockIdx.x - tr * a.Hq;
-        if (tr >= *a.ntiles) return;             // whole CTA leaves before any set-up
-        const int2 tl = a.tiles[tr];
-        b = tl.x / a.K;
-        g = tl.x - b * a.K;
-        const int gs = a.offsets[b * (a.K + 1) + g];
-        gend = a.offsets[b * (a.K + 1) + g + 1];
-        q0 = gs + kBM * tl.y;
-        qend = min(q0 + kBM, gend);
-        kv_lo = gs;
-        nkv = tl.y + 1;
-    } else {
-        const int nqt = (a.n + kBM - 1) / kBM;
-        h = blockIdx.x % a.Hq;
-        const int rest = blockIdx.x / a.Hq;
-        int qt = rest % nqt;
-        b = rest / nqt;
-        if (MODE == kDense) qt = nqt - 1 - qt;   // longest rows first
-        q0 = kBM * qt;
-        qend = min(q0 + kBM, a.n);
-        if (MODE == kDense) {
-            kv_lo = 0;
-            nkv = qt + 1;
-        } else {
-            kv_lo = max(0, q0 - a.window + 1);
-            nkv = a.window > 0 ? (qend - kv_lo + kBN - 1) / kBN : 0;
-        }
-    }
-    const int kvh = h / (a.Hq / a.Hkv);
+    const int nitems = total_items<MODE>(a);
+    if ((int)blockIdx.x >= nitems) return;       // whole CTA leaves before any set-up
+    const int kv_per_q = a.Hq / a.Hkv;
 
     // ------------------------------------------------------------ set-up
     extern __shared__ uint8_t smem_raw[];
@@ -144,19 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sQ = sm + L::kQ;
     uint8_t *sK = sm + L::kK;
     uint8_t *sV = sm + L::kV;
-    uint8_t *sP = sm + L::kP;
-    int32_t *mTok = reinterpret_cast<int32_t *>(sm + L::kTok);
-    uint64_t *mSig = reinterpret_cast<uint64_t *>(sm + L::kSig);
-    int32_t *mGid = reinterpret_cast<int32_t *>(sm + L::kGid);
+    uint8_t *sStage = sm + L::kP;       // epilogue staging: one output row per thread
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kMisc + 4);
+    uint32_t *colbits = reinterpret_cast<uint32_t *>(sm + L::kColbits);   // [2][K][4]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[B_QFULL], 1);
+        mbar_init(&bars[B_QEMPTY], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_KFULL + s], 1);
             mbar_init(&bars[B_VFULL + s], 1);
@@ -168,9 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars[B_PFULL], 128);
         mbar_init(&bars[B_PVDONE], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_IFULL + s], 32);           // the producer warp's lanes
+            mbar_init(&bars[B_IEMPTY + s], 128 + 1);     // softmax threads + MMA thread
+        }
+        long long *trz = reinterpret_cast<long long *>(sm + L::kTrace);
+        for (int i = 0; i < kTraceSlots; ++i) trz[i] = 0;
         *abort_flag = 0;
         mbar_fence_init();
     }
+    const int rtopk = (MODE == kDense) ? 0 : a.topk;    // per-row ring data width
     if (warp == 5) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
@@ -186,395 +306,542 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_o = tmem + 256;
 
+    long long *tr = reinterpret_cast<long long *>(sm + L::kTrace);   // zeroed at set-up
+    const long long t_start = clock64();
+
     if (warp == 4) {
         // ------------------------------------------------- TMA producer
-        if (lane == 0 && nkv > 0) {
-            mbar_arrive_expect_tx(&bars[B_QFULL], L::kTile);
-            for (int c = 0; c < kChunks; ++c)
-                tma_load_4d(sQ + c * 16384, &tmQ, &bars[B_QFULL], c * 64, h, q0, b);
-        }
-        int issued = 0;
-        for (int u = 0; u < nkv; ++u) {
-            const int st = u & 1;
-            const int r0 = kv_lo + kBN * u;
-            bool ok = true;
-            if (u >= 2 && lane == 0)
-                ok = mbar_wait(&bars[B_KEMPTY + st], ((u >> 1) - 1) & 1, abort_flag, a.status);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[B_KFULL + st], L::kTile);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_4d(sK + st * L::kTile + c * 16384, &tmK, &bars[B_KFULL + st],
-                                c * 64, kvh, r0, b);
+        const bool trc = a.trace != nullptr && lane == 0;
+        int T = 0, iq = 0;            // key tiles and query tiles issued so far
+        bool ok = true;
+        for (int k = 0, item = blockIdx.x; ok && item < nitems;
+             item = item_of(++k, blockIdx.x, gridDim.x)) {
+            // ---- publish the decoded item and its rows' metadata (ring slot k & 1,
+            // free once item k - 2 is fully consumed)
+            if (k >= 2 && lane == 0)
+                ok = mbar_wait_t(&bars[B_IEMPTY + (k & 1)], ((k >> 1) - 1) & 1, abort_flag,
+                                 a.status, trc, tr[0]);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                ok = false;
+                break;
             }
-            if (u >= 2 && lane == 0)
-                ok = mbar_wait(&bars[B_VEMPTY + st], ((u >> 1) - 1) & 1, abort_flag, a.status);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            if (MODE != kDense) {
-                // key-row metadata for the mask: token index, group signature, ids
-                for (int c = lane; c < kBN; c += 32) {
-                    const int row = r0 + c;
-                    int tok = -1;
-                    if (MODE == kGroup) {
-                        if (row < gend) tok = a.pos[(int64_t)b * a.rows + row];
-                    } else if (row < a.n) {
-                        tok = row;
+            const long long t_ring = trc ? clock64() : 0;
+            const WorkItem w = decode_item<MODE>(a, item);
+            {
+                const RingSlot rs = ring_slot<D>(sm, MODE, a.K, rtopk, k & 1);
+                if (lane == 0) {
+                    rs.item[0] = w.b;
+                    rs.item[1] = w.h;
+                    rs.item[2] = w.q0;
+                    rs.item[3] = w.qend;
+                    rs.item[4] = w.kv_lo;
+                    rs.item[5] = w.nkv;
+                    rs.item[6] = w.g;
+                    rs.item[7] = w.gend;
+                }
+                if (MODE != kDense) {
+                    // the 128 query rows' group ids, [128][topk], coalesced
+                    const int32_t *src = a.gids + ((int64_t)w.b * a.rows + w.q0) * a.topk;
+                    const int nval = (w.qend - w.q0) * a.topk;
+                    for (int i = lane; i < kBM * a.topk; i += 32)
+                        rs.gid[i] = i < nval ? src[i] : -1;
+                }
+                __syncwarp();
+                mbar_arrive(&bars[B_IFULL + (k & 1)]);
+                if (trc) tr[TR_P_RING] += clock64() - t_ring;
+            }
+            if (w.nkv == 0) continue;
+            const int kvh = w.h / kv_per_q;
+            const int kv_end = (MODE == kGroup) ? w.gend : a.n;
+            // Q buffer free once the last Q.K^T of the previous item is done
+            if (iq >= 1 && lane == 0)
+                ok = mbar_wait_t(&bars[B_QEMPTY], (iq - 1) & 1, abort_flag, a.status, trc, tr[1]);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_QFULL], L::kTile);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_4d(sQ + c * 16384, &tmQ, &bars[B_QFULL], c * 64, w.h, w.q0, w.b);
+            }
+            ++iq;
+            for (int u = 0; u < w.nkv; ++u, ++T) {
+                const int st = T & 1;
+                const int r0 = w.kv_lo + kBN * u;
+                // Group ids of this tile's key rows (lane: rows lane + 32 j),
+                // loaded now so that the waits below hide their latency.
+                int kg[4][kMaxTopk];
+                if (MODE != kDense) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = r0 + lane + 32 * j;
+                        const int32_t *gp = a.gids + ((int64_t)w.b * a.rows + row) * a.topk;
+#pragma unroll
+                        for (int s = 0; s < kMaxTopk; ++s)
+                            kg[j][s] = (row < kv_end && s < a.topk) ? gp[s] : -1;
                     }
-                    uint64_t sig = 0;
-                    if (tok >= 0) {
-                        const int32_t *gp = a.ids + ((int64_t)b * a.n + tok) * a.topk;
-                        for (int s = 0; s < a.topk; ++s) {
-                            const int gi = gp[s];
-                            sig |= 1ull << (gi & 63);
-                            mGid[(st * kBN + c) * 8 + s] = gi;
+                }
+                if (T >= 2 && lane == 0)
+                    ok = mbar_wait_t(&bars[B_KEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
+                                     a.status, trc, tr[2]);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[B_KFULL + st], L::kTile);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_4d(sK + st * L::kTile + c * 16384, &tmK, &bars[B_KFULL + st],
+                                    c * 64, kvh, r0, w.b);
+                }
+                // V and the masks of stage st are free once P.V of tile T-2 is
+                // done (its softmax finished reading colbits[st] before P).
+                if (T >= 2 && lane == 0)
+                    ok = mbar_wait_t(&bars[B_VEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
+                                     a.status, trc, tr[3]);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[B_VFULL + st], L::kTile);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
+                                    c * 64, kvh, r0, w.b);
+                }
+                if (MODE != kDense) {
+                    // colbits[st][g][q] bit c: key column 32q + c belongs to group g
+                    uint32_t *cb = colbits + (size_t)st * a.K * 4;
+                    for (int i = lane; i < a.K * 4; i += 32) cb[i] = 0u;
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int s = 0; s < kMaxTopk; ++s) {
+                            const int gi = kg[j][s];
+                            if ((unsigned)gi < (unsigned)a.K)
+                                atomicOr(&cb[gi * 4 + j], 1u << lane);
                         }
                     }
-                    mTok[st * kBN + c] = tok;
-                    mSig[st * kBN + c] = sig;
+                    mbar_arrive(&bars[B_META + st]);
                 }
-                mbar_arrive(&bars[B_META + st]);
+                __syncwarp();
             }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[B_VFULL + st], L::kTile);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
-                                c * 64, kvh, r0, b);
-            }
-            issued = u + 1;
-            __syncwarp();
+        }
+        if (trc) {
+            tr[TR_P_TOTAL] = clock64() - t_start;
+            trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 0, 8);
         }
         // If the CTA gave up early, let the copies already issued land before
         // shared memory is released.
         if (*abort_flag && lane == 0) {
-            const uint64_t tq = global_timer_ns();
-            while (nkv > 0 && !mbar_try_wait(&bars[B_QFULL], 0) &&
-                   global_timer_ns() - tq < 100000000ull) {
+            const uint64_t t0 = global_timer_ns();
+            while (iq > 0 && !mbar_try_wait(&bars[B_QFULL], (iq - 1) & 1) &&
+                   global_timer_ns() - t0 < 100000000ull) {
             }
-            for (int u = max(0, issued - 2); u < issued; ++u) {
-                const int st = u & 1;
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&bars[B_KFULL + st], (u >> 1) & 1) &&
-                       global_timer_ns() - t0 < 100000000ull) {
-                }
-                while (!mbar_try_wait(&bars[B_VFULL + st], (u >> 1) & 1) &&
+            for (int t = max(0, T - 2); t < T + 1; ++t) {
+                const int st = t & 1;
+                while (!mbar_try_wait(&bars[B_KFULL + st], (t >> 1) & 1) &&
                        global_timer_ns() - t0 < 200000000ull) {
+                }
+                while (!mbar_try_wait(&bars[B_VFULL + st], (t >> 1) & 1) &&
+                       global_timer_ns() - t0 < 300000000ull) {
                 }
             }
         }
     } else if (warp == 5) {
         // -------------------------------------------------- MMA issuer
-        if (lane == 0 && nkv > 0) {
+        if (lane == 0) {
+            const bool trc = a.trace != nullptr;
             constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
-            const uint32_t v_base = smem_u32(sV), p_base = smem_u32(sP);
+            const uint32_t v_base = smem_u32(sV);
 
-            auto issue_pv = [&](int v) -> bool {
-                const int st = v & 1;
-                if (!mbar_wait(&bars[B_PFULL], v & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(&bars[B_VFULL + st], (v >> 1) & 1, abort_flag, a.status))
+            // O += P(t) V(t); `first` starts the item's accumulator.
+            auto issue_pv = [&](int t, bool first) -> bool {
+                const int st = t & 1;
+                if (!mbar_wait_t(&bars[B_PFULL], t & 1, abort_flag, a.status, trc, tr[8]))
+                    return false;
+                if (!mbar_wait_t(&bars[B_VFULL + st], (t >> 1) & 1, abort_flag, a.status, trc,
+                                 tr[9]))
                     return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // A = P (K-major): 16 keys = 32 bytes inside a 128-byte row.
-                    const uint64_t ad =
-                        sdesc_sw128(p_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    // A = P in TMEM over this tile's S columns: 16 keys = 8 columns.
+                    const uint32_t at = tmem + st * kBN + kk * 8;
                     // B = V (MN-major): 16 key rows of 128 bytes; the second
                     // 64-column half of D lies 16 KB further (LBO).
                     const uint64_t bd =
                         sdesc_sw128(v_base + st * L::kTile + kk * 2048, 16384, 1024);
-                    tc_mma_bf16(tmem_o, ad, bd, kIdescPV, (v > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_bf16_ts(tmem_o, at, bd, kIdescPV, (!first || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars[B_VEMPTY + st]);
                 tc_commit(&bars[B_PVDONE]);
                 return true;
             };
 
-            bool ok = mbar_wait(&bars[B_QFULL], 0, abort_flag, a.status);
-            for (int u = 0; ok && u < nkv; ++u) {
-                const int st = u & 1;
-                ok = mbar_wait(&bars[B_KFULL + st], (u >> 1) & 1, abort_flag, a.status);
+            int T = 0, iq = 0;
+            bool ok = true;
+            for (int k = 0, item = blockIdx.x; ok && item < nitems;
+             item = item_of(++k, blockIdx.x, gridDim.x)) {
+                ok = mbar_wait_t(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status, trc,
+                                 tr[10]);
                 if (!ok) break;
-                if (u >= 2) {
-                    ok = mbar_wait(&bars[B_SEMPTY + st], ((u >> 1) - 1) & 1, abort_flag,
-                                   a.status);
+                const int *wi = ring_slot<D>(sm, MODE, a.K, rtopk, k & 1).item;
+                WorkItem w;
+                w.nkv = wi[5];
+                mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
+                if (w.nkv == 0) continue;
+                ok = mbar_wait_t(&bars[B_QFULL], iq & 1, abort_flag, a.status, trc, tr[11]);
+                for (int u = 0; ok && u < w.nkv; ++u, ++T) {
+                    const int st = T & 1;
+                    ok = mbar_wait_t(&bars[B_KFULL + st], (T >> 1) & 1, abort_flag, a.status, trc,
+                                     tr[12]);
                     if (!ok) break;
-                }
-                tc_fence_after();
+                    if (T >= 2) {
+                        ok = mbar_wait_t(&bars[B_SEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
+                                         a.status, trc, tr[13]);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(q_base + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(k_base + st * L::kTile + off, 16, 1024);
-                    tc_mma_bf16(tmem + st * kBN, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint64_t ad = sdesc_sw128(q_base + off, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(k_base + st * L::kTile + off, 16, 1024);
+                        tc_mma_bf16(tmem + st * kBN, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&bars[B_SFULL + st]);
+                    tc_commit(&bars[B_KEMPTY + st]);
+                    if (u == w.nkv - 1) tc_commit(&bars[B_QEMPTY]);
+                    if (u >= 1) ok = issue_pv(T - 1, u == 1);
                 }
-                tc_commit(&bars[B_SFULL + st]);
-                tc_commit(&bars[B_KEMPTY + st]);
-                if (u >= 1) ok = issue_pv(u - 1);
+                if (ok) ok = issue_pv(T - 1, w.nkv == 1);
+                ++iq;
             }
-            if (ok) issue_pv(nkv - 1);
+            if (trc) {
+                tr[TR_M_TOTAL] = clock64() - t_start;
+                trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 8, 16);
+            }
         }
         __syncwarp();
     } else {
         // ------------------------------------------- softmax warpgroup
         const int r = threadIdx.x;                       // row in tile, TMEM lane
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const int prow = q0 + r;                         // row in the Q tensor
-        bool qvalid;
-        int qi;                                          // token index of the row
-        uint64_t qsig = 0;
-        int qg[8];
-        int nq = 0;
-        if (MODE == kGroup) {
-            qvalid = prow < qend;
-            qi = qvalid ? a.pos[(int64_t)b * a.rows + prow] : -1;
-            if (qvalid) {
-                const int32_t *gp = a.ids + ((int64_t)b * a.n + qi) * a.topk;
-                for (int s = 0; s < a.topk; ++s) {
-                    const int gi = gp[s];
-                    if (gi < g) {            // groups that would own a shared pair first
-                        qg[nq++] = gi;
-                        qsig |= 1ull << (gi & 63);
-                    }
-                }
-            }
-        } else {
-            qi = prow;
-            qvalid = prow < a.n;
-            if (MODE == kWindow && qvalid) {
-                const int32_t *gp = a.ids + ((int64_t)b * a.n + qi) * a.topk;
-                for (int s = 0; s < a.topk; ++s) {
-                    const int gi = gp[s];
-                    qg[nq++] = gi;
-                    qsig |= 1ull << (gi & 63);
-                }
-            }
-        }
-        const bool sig_exact = a.K <= 64;
-        float m_ref = -CUDART_INF_F;   // reference max (base-2 domain) applied to O and l
-        float l = 0.f;
-        int cnt = 0;
+        const bool trc = a.trace != nullptr && r == 0;
+        int T = 0;
         bool ok = true;
-
-        for (int u = 0; u < nkv; ++u) {
-            const int st = u & 1;
-            const int kvb = kv_lo + kBN * u;             // first key row of the tile
-            if (MODE != kDense) {
-                if (!mbar_wait(&bars[B_META + st], (u >> 1) & 1, abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!mbar_wait(&bars[B_SFULL + st], (u >> 1) & 1, abort_flag, a.status)) {
+        for (int k = 0, item = blockIdx.x; ok && item < nitems;
+             item = item_of(++k, blockIdx.x, gridDim.x)) {
+            // the item and this row's metadata, published by the producer
+            const int slot = k & 1;
+            if (!mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
+                             tr[16])) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            float s[kBN];
+            const RingSlot rs = ring_slot<D>(sm, MODE, a.K, rtopk, slot);
+            WorkItem w;
+            w.b = rs.item[0];
+            w.h = rs.item[1];
+            w.q0 = rs.item[2];
+            w.qend = rs.item[3];
+            w.kv_lo = rs.item[4];
+            w.nkv = rs.item[5];
+            w.g = rs.item[6];
+            w.gend = rs.item[7];
+            const int prow = w.q0 + r;                   // row in the Q tensor
+            const bool qvalid = prow < w.qend;
+            int qi = prow;                               // token index of the row
+            // Groups whose columns this row must not score: every group of the
+            // row (kWindow), or the row's groups below the tile's group (kGroup).
+            int qg[kMaxTopk];          // -1 = unused slot
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_off + st * kBN + c4 * 32, s + c4 * 32);
-            tc_fence_before();
-            mbar_arrive(&bars[B_SEMPTY + st]);
-
-            // ---- which of the 128 keys this row may score
-            uint32_t okb[4];
-#pragma unroll
-            for (int w4 = 0; w4 < 4; ++w4) {
-                uint32_t bits;
-                if (!qvalid) {
-                    bits = 0u;
-                } else if (MODE == kGroup) {
-                    bits = range_bits(0, prow - kvb, 32 * w4);          // causal, packed order
-                } else if (MODE == kWindow) {
-                    bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, 32 * w4);
-                } else {
-                    bits = range_bits(0, qi - kvb, 32 * w4);
+            for (int s = 0; s < kMaxTopk; ++s) {
+                qg[s] = -1;
+                if (MODE != kDense && qvalid && s < a.topk) {
+                    const int gi = rs.gid[r * a.topk + s];
+                    if ((MODE == kWindow || gi < w.g) && (unsigned)gi < (unsigned)a.K)
+                        qg[s] = gi;
                 }
-                if (MODE != kDense && nq > 0) {
-                    uint32_t cand = bits;
-                    while (cand) {
-                        const int cc = __ffs(cand) - 1;
-                        cand &= cand - 1u;
-                        const int c = 32 * w4 + cc;
-                        if (mSig[st * kBN + c] & qsig) {
-                            bool share = sig_exact;
-                            if (!share) {
-                                const int32_t *gj = mGid + (st * kBN + c) * 8;
-                                for (int x = 0; x < nq && !share; ++x)
-                                    for (int y = 0; y < a.topk; ++y)
-                                        if (gj[y] == qg[x]) share = true;
-                            }
-                            if (share) bits &= ~(1u << cc);
-                        }
+            }
+            if (MODE == kGroup && qvalid && a.pair_count)
+                qi = a.pos[(int64_t)w.b * a.rows + prow];
+
+            float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O and l
+            float l = 0.f;
+            int cnt = 0;
+
+            for (int u = 0; u < w.nkv; ++u, ++T) {
+                const int st = T & 1;
+                const int kvb = w.kv_lo + kBN * u;       // first key row of the tile
+                if (MODE != kDense) {
+                    if (!mbar_wait_t(&bars[B_META + st], (T >> 1) & 1, abort_flag, a.status, trc,
+                                     tr[17])) {
+                        ok = false;
+                        break;
                     }
                 }
-                okb[w4] = bits;
-            }
-            if (a.pair_count)
-                cnt += __popc(okb[0]) + __popc(okb[1]) + __popc(okb[2]) + __popc(okb[3]);
-
-            float mx = -CUDART_INF_F;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                const bool on = (okb[c >> 5] >> (c & 31)) & 1u;
-                s[c] = on ? s[c] * a.scale_log2 : -CUDART_INF_F;
-                mx = fmaxf(mx, s[c]);
-            }
-
-            // P(u-1) consumed and O updated by the previous P.V product.
-            if (u >= 1) {
-                if (!mbar_wait(&bars[B_PVDONE], (u - 1) & 1, abort_flag, a.status)) {
+                if (!mbar_wait_t(&bars[B_SFULL + st], (T >> 1) & 1, abort_flag, a.status, trc,
+                                 tr[18])) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                long long tt = trc ? clock64() : 0;
+                float s[kBN];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    tmem_ld32(tmem + lane_off + st * kBN + c4 * 32, s + c4 * 32);
+                if (trc) {
+                    const long long t2 = clock64();
+                    tr[TR_T_SLOAD] += t2 - tt;
+                    tt = t2;
+                }
+                tc_fence_before();
+                mbar_arrive(&bars[B_SEMPTY + st]);
+
+                // ---- which of the 128 keys this row may score
+                uint4 excl = make_uint4(0u, 0u, 0u, 0u);
+                if (MODE != kDense) {
+                    const uint4 *cb =
+                        reinterpret_cast<const uint4 *>(colbits + (size_t)st * a.K * 4);
+#pragma unroll
+                    for (int x = 0; x < kMaxTopk; ++x) {
+                        if (qg[x] >= 0) {
+                            const uint4 v = cb[qg[x]];
+                            excl.x |= v.x;
+                            excl.y |= v.y;
+                            excl.z |= v.z;
+                            excl.w |= v.w;
+                        }
+                    }
+                }
+                const uint32_t exw[4] = {excl.x, excl.y, excl.z, excl.w};
+                uint32_t okb[4];
+#pragma unroll
+                for (int w4 = 0; w4 < 4; ++w4) {
+                    uint32_t bits;
+                    if (!qvalid)
+                        bits = 0u;
+                    else if (MODE == kGroup)
+                        bits = range_bits(0, prow - kvb, 32 * w4);      // causal, group order
+                    else if (MODE == kWindow)
+                        bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, 32 * w4);
+                    else
+                        bits = range_bits(0, qi - kvb, 32 * w4);
+                    okb[w4] = bits & ~exw[w4];
+                }
+                if (a.pair_count)
+                    cnt += __popc(okb[0]) + __popc(okb[1]) + __popc(okb[2]) + __popc(okb[3]);
+
+                // masked raw scores; the row max over 8 independent chains
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const bool on = (okb[c >> 5] >> (c & 31)) & 1u;
+                    s[c] = on ? s[c] : -CUDART_INF_F;
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                 a.scale_log2;   // scale > 0, so max(s) * scale = max(s * scale)
+                if (trc) {
+                    const long long t2 = clock64();
+                    tr[TR_T_MASK] += t2 - tt;
+                    tt = t2;
+                }
+
+                // P of the previous tile consumed and O updated by its P.V.
+                if (u >= 1) {
+                    if (!mbar_wait_t(&bars[B_PVDONE], (T - 1) & 1, abort_flag, a.status, trc,
+                                     tr[19])) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                // Lazy rescaling: keep the reference max unless the row max
+                // grows by more than 2^8.
+                const float m_new = fmaxf(m_ref, mx);
+                const bool grow = (m_ref == -CUDART_INF_F) || (m_new > m_ref + 8.f);
+                const bool resc = grow && l > 0.f;
+                const float new_ref = grow ? m_new : m_ref;
+                if (__any_sync(0xffffffffu, resc)) {
+                    const float f = resc ? exp2f(m_ref - new_ref) : 1.f;
+                    rescale_o<D>(tmem_o + lane_off, f);     // warp-wide (tcgen05 ld/st)
+                    l *= f;
+                }
+                m_ref = new_ref;
+                const float ref = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+                if (trc) {
+                    const long long t2 = clock64();
+                    tr[TR_T_RESCALE] += t2 - tt;
+                    tt = t2;
+                }
+
+                // ---- P = 2^(s * scale - ref) in bf16, written to TMEM over this
+                // tile's S columns (key k in column k / 2), the A operand of P.V
+                const float nref = -ref, sc2 = a.scale_log2;
+                float rs8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = exp2f(fmaf(s[half * 64 + 2 * j], sc2, nref));
+                        const float p1 = exp2f(fmaf(s[half * 64 + 2 * j + 1], sc2, nref));
+                        rs8[j & 7] += p0 + p1;
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32u(tmem + lane_off + st * kBN + half * 32, pk);
+                }
+                tmem_st_wait();
+                l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                if (trc) tr[TR_T_P] += clock64() - tt;
+                tc_fence_before();
+                mbar_arrive(&bars[B_PFULL]);
             }
-            // Lazy rescaling: keep the reference max unless the row max
-            // grows by more than 2^8.
-            const float m_new = fmaxf(m_ref, mx);
-            const bool grow = (m_ref == -CUDART_INF_F) || (m_new > m_ref + 8.f);
-            const bool resc = grow && l > 0.f;
-            const float new_ref = grow ? m_new : m_ref;
-            if (__any_sync(0xffffffffu, resc)) {
-                const float f = resc ? exp2f(m_ref - new_ref) : 1.f;
+            if (!ok) break;
+
+            // ---- epilogue
+            const long long t_epi = trc ? clock64() : 0;
+            if (w.nkv > 0) {
+                ok = mbar_wait_t(&bars[B_PVDONE], (T - 1) & 1, abort_flag, a.status, trc, tr[20]);
+                tc_fence_after();
+                if (!ok) break;
+            }
+            const bool has = l > 0.f;
+            const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // base 2
+            const float inv_l = has ? 1.f / l : 0.f;
+            int64_t orow = 0;
+            if (MODE == kGroup)
+                orow = ((int64_t)w.b * a.rows + prow) * a.Hq + w.h;
+            else
+                orow = ((int64_t)w.b * a.n + qi) * a.Hq + w.h;
+            // Pass 1 (partials only): the row's largest |O| entry, from TMEM.
+            long long te = trc ? clock64() : 0;
+            float amax = 0.f;
+            if (MODE != kDense && w.nkv > 0) {
+                float am8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) am8[i] = 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= f;
-                    tmem_st32(tmem_o + lane_off + c * 32, o);
+                    for (int e = 0; e < 32; ++e) am8[e & 7] = fmaxf(am8[e & 7], fabsf(o[e]));
                 }
-                tmem_st_wait();
-                l *= f;
+                amax = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
+                             fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7]))) *
+                       inv_l;
             }
-            m_ref = new_ref;
-            const float ref = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
-
-            // ---- P = 2^(s - ref) in bf16, 128-byte swizzled, K-major
-            float rs = 0.f;
-            const uint32_t p_row = smem_u32(sP) + r * 128;
+            if (trc) {
+                const long long t2 = clock64();
+                tr[TR_E_TMEM] += t2 - te;
+                te = t2;
+            }
+            // Pack the row into this thread's staging row (16-byte chunk q at slot
+            // q ^ (r mod D/8): conflict-free), then each warp copies its own 32
+            // rows out with whole-row, coalesced 16-byte stores.
+            constexpr int kCh = D / 8;                      // 16-byte chunks per row
+            const uint32_t srow = smem_u32(sStage) + r * (D * 2);
+            // Partials: O / l in fp16 scaled by a power of two so that the largest
+            // entry lies in [2^14, 2^15) (11-bit precision at any magnitude, no
+            // overflow), plus {lse (base 2), 2^e}.  Dense: O / l in bf16.
+            int ex = 0;
+            if (amax > 0.f && amax < CUDART_INF_F) frexpf(amax, &ex);   // amax < 2^ex
+            const float mul = (MODE == kDense) ? inv_l
+                                               : inv_l * __int_as_float((127 + 15 - ex) << 23);
+            const float up = __int_as_float((127 - 15 + ex) << 23);     // 2^(ex - 15)
+            // Pass 2: scale, pack and stage 32 columns at a time.
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                if (w.nkv > 0) {
+                    tmem_ld32(tmem_o + lane_off + c * 32, o);
+                } else {
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    float p[8];
+                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        p[e] = exp2f(s[half * 64 + uu * 8 + e] - ref);
-                        rs += p[e];
-                    }
-                    st_shared_v4(p_row + half * 16384 + ((uu ^ (r & 7)) << 4),
-                                 pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                                 pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int q = c * 4 + qq;
+                    const float *v = o + qq * 8;
+                    if (MODE == kDense)
+                        st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
+                                     pack_bf16x2(v[0] * mul, v[1] * mul),
+                                     pack_bf16x2(v[2] * mul, v[3] * mul),
+                                     pack_bf16x2(v[4] * mul, v[5] * mul),
+                                     pack_bf16x2(v[6] * mul, v[7] * mul));
+                    else
+                        st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
+                                     pack_f16x2(v[0] * mul, v[1] * mul),
+                                     pack_f16x2(v[2] * mul, v[3] * mul),
+                                     pack_f16x2(v[4] * mul, v[5] * mul),
+                                     pack_f16x2(v[6] * mul, v[7] * mul));
                 }
             }
-            l += rs;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars[B_PFULL]);
-        }
-
-        // ---- epilogue
-        if (ok && nkv > 0) {
-            ok = mbar_wait(&bars[B_PVDONE], (nkv - 1) & 1, abort_flag, a.status);
-            tc_fence_after();
-        }
-        const bool has = ok && l > 0.f;
-        const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // this kernel's part
-        // Output scale of the TMEM accumulator (which holds sum p v with
-        // p = 2^(s - m_ref)) and, for kWindow, the merge with the group parts.
-        float fo = has ? 1.f / l : 0.f;
-        float L2 = lse2;
-        int64_t prt[8];
-        float wpart[8];
-        if (MODE == kWindow) {
-            // Exact softmax over the union of the window part and the topk
-            // group parts: L = log2 sum_p 2^{L_p}, O = sum_p 2^{L_p - L} O_p.
-            float m = lse2;
-            const int nk = a.n * a.topk;     // group-order rows per batch
-            for (int s = 0; s < a.topk; ++s) {
-                prt[s] = -1;
-                wpart[s] = -CUDART_INF_F;
-                if (qvalid) {
-                    const int r = a.inv[((int64_t)b * a.n + qi) * a.topk + s];
-                    if ((unsigned)r < (unsigned)nk) {
-                        prt[s] = ((int64_t)b * nk + r) * a.Hq + h;
-                        wpart[s] = a.part_lse[prt[s]];
-                    }
+            if (qvalid) {
+                if (MODE == kDense) {
+                    if (a.lse)
+                        a.lse[((int64_t)w.b * a.Hq + w.h) * a.n + qi] =
+                            lse2 * 0.69314718055994531f;
+                } else {
+                    (MODE == kGroup ? a.part_meta_out : a.win_meta_out)[orow] =
+                        make_float2(lse2, up);
                 }
-                m = fmaxf(m, wpart[s]);
             }
-            if (m == -CUDART_INF_F) {
-                L2 = -CUDART_INF_F;
-                fo = 0.f;
-                for (int s = 0; s < a.topk; ++s) wpart[s] = 0.f;
-            } else {
-                float sum = exp2f(lse2 - m);
-                for (int s = 0; s < a.topk; ++s) sum += exp2f(wpart[s] - m);
-                L2 = m + log2f(sum);
-                fo = has ? exp2f(m_ref - L2) : 0.f;     // 2^{L_w - L} / l
-                for (int s = 0; s < a.topk; ++s) wpart[s] = exp2f(wpart[s] - L2);
+            if (trc) {
+                const long long t2 = clock64();
+                tr[TR_E_SCALE] += t2 - te;
+                te = t2;
             }
-        }
-        int64_t orow = 0;
-        if (MODE == kGroup)
-            orow = ((int64_t)b * a.rows + prow) * a.Hq + h;
-        else
-            orow = ((int64_t)b * a.n + qi) * a.Hq + h;
+            __syncwarp();
+            {
+                constexpr int kRowsPer = 32 / kCh;            // rows per warp instruction
+                const int sub = lane / kCh, q = lane % kCh;
+                uint16_t *obase = (MODE == kDense) ? reinterpret_cast<uint16_t *>(a.out)
+                                  : (MODE == kGroup) ? reinterpret_cast<uint16_t *>(a.part_out16)
+                                                     : reinterpret_cast<uint16_t *>(a.win_out16);
+                const int64_t rstride = (MODE == kGroup) ? (int64_t)a.rows : (int64_t)a.n;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            if (nkv > 0) {
-                tmem_ld32(tmem_o + lane_off + c * 32, o);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= fo;
-            if (!qvalid) continue;
-            if (MODE == kGroup) {
-                float4 *dst = reinterpret_cast<float4 *>(a.part_out + orow * D + c * 32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                continue;
-            }
-            if (MODE == kWindow) {
-                for (int s = 0; s < a.topk; ++s) {
-                    if (wpart[s] == 0.f) continue;
-                    const float4 *src =
-                        reinterpret_cast<const float4 *>(a.part_o + prt[s] * D + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 v = src[q];
-                        o[4 * q] = fmaf(wpart[s], v.x, o[4 * q]);
-                        o[4 * q + 1] = fmaf(wpart[s], v.y, o[4 * q + 1]);
-                        o[4 * q + 2] = fmaf(wpart[s], v.z, o[4 * q + 2]);
-                        o[4 * q + 3] = fmaf(wpart[s], v.w, o[4 * q + 3]);
+                for (int it = 0; it < 32 / kRowsPer; ++it) {
+                    const int j = warp * 32 + it * kRowsPer + sub;    // tile row
+                    const int row = w.q0 + j;
+                    uint4 v;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(smem_u32(sStage) + j * (D * 2) + ((q ^ (j & (kCh - 1))) << 4)));
+                    if (row < w.qend) {
+                        const int64_t orr = ((int64_t)w.b * rstride + row) * a.Hq + w.h;
+                        reinterpret_cast<uint4 *>(obase + orr * D)[q] = v;
                     }
                 }
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 v;
-                v.x = pack_bf16x2(o[q * 8 + 0], o[q * 8 + 1]);
-                v.y = pack_bf16x2(o[q * 8 + 2], o[q * 8 + 3]);
-                v.z = pack_bf16x2(o[q * 8 + 4], o[q * 8 + 5]);
-                v.w = pack_bf16x2(o[q * 8 + 6], o[q * 8 + 7]);
-                dst[c * 4 + q] = v;
+            __syncwarp();
+            if (trc) tr[TR_E_STORE] += clock64() - te;
+            if (qvalid && a.pair_count && w.h == 0)
+                atomicAdd(&a.pair_count[(int64_t)w.b * a.n + qi], cnt);
+            mbar_arrive(&bars[B_IEMPTY + slot]);     // ring slot no longer read
+            if (trc) {
+                tr[TR_S_EPI] += clock64() - t_epi;
+                tr[TR_S_ITEMS] += 1;
+                tr[TR_S_TILES] += w.nkv;
             }
         }
-        if (qvalid) {
-            if (MODE == kGroup) {
-                a.part_lse_out[orow] = lse2;
-            } else if (a.lse) {
-                a.lse[((int64_t)b * a.Hq + h) * a.n + qi] = L2 * 0.69314718055994531f;
-            }
-            if (a.pair_count && h == 0) atomicAdd(&a.pair_count[(int64_t)b * a.n + qi], cnt);
+        if (trc) {
+            tr[TR_S_TOTAL] = clock64() - t_start;
+            trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 16, 32);
         }
     }
 

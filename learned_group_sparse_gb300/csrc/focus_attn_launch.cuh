@@ -6,12 +6,18 @@
 
 namespace focus {
 
+template <int D>
+uint32_t attn_smem_bytes(int mode, int K, int topk)
+{
+    return mode == kDense ? AttnSmem<D>::bytes(kDense, 0, 0) : AttnSmem<D>::bytes(mode, K, topk);
+}
+
 template <int MODE, int D>
 cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
 {
     if (p.grid <= 0) return cudaSuccess;
     auto kern = focus_attn_kernel<MODE, D>;
-    constexpr uint32_t smem = AttnSmem<D>::kAlloc;
+    const uint32_t smem = attn_smem_bytes<D>(MODE, p.K, p.topk);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     AttnArgs a;
@@ -24,22 +30,28 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.scale_log2 = p.scale_log2;
     a.K = p.K;
     a.topk = p.topk;
-    a.ids = p.ids;
+    a.gids = p.gids;
     a.offsets = p.offsets;
     a.pos = p.pos;
     a.tiles = p.tiles;
     a.ntiles = p.ntiles;
     a.out = p.out;
     a.lse = p.lse;
-    a.part_out = p.part_out;
-    a.part_lse_out = p.part_lse_out;
-    a.part_o = p.part_o;
-    a.part_lse = p.part_lse;
-    a.inv = p.inv;
+    a.part_out16 = p.part_out16;
+    a.part_meta_out = p.part_meta_out;
+    a.win_out16 = p.win_out16;
+    a.win_meta_out = p.win_meta_out;
     a.status = p.status;
     a.pair_count = p.pair_count;
+    a.trace = trace_buffer(MODE);
+    // Persistent: at most one CTA per SM; p.grid bounds the number of work items.
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int64_t grid = p.grid < sms ? p.grid : sms;
     prof_begin(MODE == kGroup ? "attn_group" : MODE == kWindow ? "attn_window" : "attn_dense", s);
-    kern<<<(unsigned)p.grid, kThreads, smem, s>>>(*p.tmQ, *p.tmK, *p.tmV, a);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(*p.tmQ, *p.tmK, *p.tmV, a);
     prof_end(s);
     *launches += 1;
     return cudaGetLastError();

@@ -278,8 +278,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 // ---------------------------------------------------------------- gather
 __global__ void __launch_bounds__(256) gather_kernel(
     const uint4 *__restrict__ Q, const uint4 *__restrict__ K, const uint4 *__restrict__ V,
-    const int32_t *__restrict__ pos, int B, int n, int64_t nk, int qunits, int kvunits,
-    uint4 *__restrict__ Qp, uint4 *__restrict__ Kp, uint4 *__restrict__ Vp)
+    const int32_t *__restrict__ pos, const int32_t *__restrict__ ids, int B, int n, int64_t nk,
+    int topk, int qunits, int kvunits, uint4 *__restrict__ Qp, uint4 *__restrict__ Kp,
+    uint4 *__restrict__ Vp, int32_t *__restrict__ gidp)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -288,6 +289,7 @@ __global__ void __launch_bounds__(256) gather_kernel(
          row += warps) {
         const int64_t b = row / nk;
         const int64_t src = b * n + pos[row];
+        if (lane < topk) gidp[row * topk + lane] = ids[src * topk + lane];
         const uint4 *q = Q + src * qunits;
         uint4 *qd = Qp + row * qunits;
         for (int u = lane; u < qunits; u += 32) qd[u] = q[u];
@@ -361,9 +363,10 @@ cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *
 }
 
 cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                          const __nv_bfloat16 *V, const int32_t *pos, int B, int n, int topk,
-                          int Hq, int Hkv, int d, __nv_bfloat16 *Qp, __nv_bfloat16 *Kp,
-                          __nv_bfloat16 *Vp, cudaStream_t s, int *launches)
+                          const __nv_bfloat16 *V, const int32_t *pos, const int32_t *ids,
+                          int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
+                          __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
+                          int *launches)
 {
     const int64_t nk = (int64_t)n * topk;
     const int64_t rows = (int64_t)B * nk;
@@ -373,8 +376,9 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
     prof_begin("gather", s);
     gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<const uint4 *>(Q), reinterpret_cast<const uint4 *>(K),
-        reinterpret_cast<const uint4 *>(V), pos, B, n, nk, Hq * d / 8, Hkv * d / 8,
-        reinterpret_cast<uint4 *>(Qp), reinterpret_cast<uint4 *>(Kp), reinterpret_cast<uint4 *>(Vp));
+        reinterpret_cast<const uint4 *>(V), pos, ids, B, n, nk, topk, Hq * d / 8, Hkv * d / 8,
+        reinterpret_cast<uint4 *>(Qp), reinterpret_cast<uint4 *>(Kp), reinterpret_cast<uint4 *>(Vp),
+        gidp);
     prof_end(s);
     *launches += 1;
     return cudaGetLastError();

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,10 @@ void prof_end(cudaStream_t s);
 // Records the kernel count that focus_last_launch_count() reports.
 void set_last_launches(int launches);
 
+// Wait-time trace buffer of an attention mode (0 group, 1 window, 2 dense)
+// for launches from this host thread, or nullptr (see focus_trace_attention).
+long long *trace_buffer(int mode);
+
 struct AssignLaunch {
     const __nv_bfloat16 *X;
     const float *Wg;
@@ -26,7 +31,18 @@ struct AssignLaunch {
     int32_t *ids;
     float *margin;
 };
+// SIMT fp32 path (any K <= 1024).
 cudaError_t launch_assign(const AssignLaunch &p, cudaStream_t s, int *launches);
+// Tensor-core path (K <= 256, hidden % 64 == 0); ws holds M = W_g C^T split
+// into two bf16 parts (assign_ws_bytes).
+bool assign_tc_supported(int hidden, int K, int topk);
+size_t assign_ws_bytes(int hidden, int K);
+cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaStream_t s,
+                             int *launches);
+// 2-D bf16 tensor map [outer, inner] (inner contiguous), box {box_inner, box_outer},
+// 128-byte swizzle.
+bool make_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer);
 
 // ---- bucket: histogram per chunk, scan, offsets, stable scatter
 constexpr int kBucketChunk = 4096;   // (token, slot) entries per chunk
@@ -38,11 +54,13 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
 // Work list of the group kernel ordered by decreasing cost (tile index).
 cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *ntiles,
                         cudaStream_t s, int *launches);
-// Qp[b][r] = Q[b][pos[b][r]] (and K, V): rows of H*d bf16.
+// Qp[b][r] = Q[b][pos[b][r]] (and K, V): rows of H*d bf16; gidp[b][r] = the
+// group ids of token pos[b][r].
 cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                          const __nv_bfloat16 *V, const int32_t *pos, int B, int n, int topk,
-                          int Hq, int Hkv, int d, __nv_bfloat16 *Qp, __nv_bfloat16 *Kp,
-                          __nv_bfloat16 *Vp, cudaStream_t s, int *launches);
+                          const __nv_bfloat16 *V, const int32_t *pos, const int32_t *ids,
+                          int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
+                          __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
+                          int *launches);
 cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
                                const int32_t *inv, int B, int n, int K, int topk, int window,
                                int64_t *per_query, int64_t *totals, cudaStream_t s,
@@ -56,19 +74,26 @@ struct AttnLaunch {
     int window;
     float scale_log2;
     int K, topk;
-    const int32_t *ids, *offsets, *pos;
+    const int32_t *gids, *offsets, *pos;
     const int2 *tiles;
     const int *ntiles;
     int64_t grid;
     __nv_bfloat16 *out;
     float *lse;
-    float *part_out, *part_lse_out;
-    const float *part_o, *part_lse;
-    const int32_t *inv;
+    __half *part_out16, *win_out16;
+    float2 *part_meta_out, *win_meta_out;
     int *status;
     int32_t *pair_count;
 };
+// O = log-sum-exp merge of the window partial and the topk group partials.
+cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __half *part16,
+                         const float2 *part_meta, const int32_t *inv, int B, int n, int topk,
+                         int Hq, int d, __nv_bfloat16 *O, float *lse, cudaStream_t s,
+                         int *launches);
 cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
+// Shared memory the group and window kernels need for (d, K, topk).
+size_t attn_smem_needed(int d, int K, int topk);
+constexpr size_t kMaxSmemPerBlock = 232448;   // 227 KB opt-in limit of sm_103a
 cudaError_t launch_attn_window(const AttnLaunch &p, cudaStream_t s, int *launches);
 cudaError_t launch_attn_dense(const AttnLaunch &p, cudaStream_t s, int *launches);
 

@@ -39,8 +39,11 @@ struct Profiler {
 };
 
 thread_local Profiler g_prof;
+thread_local long long *g_trace[3] = {nullptr, nullptr, nullptr};
 
 }  // namespace
+
+long long *trace_buffer(int mode) { return (mode >= 0 && mode < 3) ? g_trace[mode] : nullptr; }
 
 void prof_begin(const char *name, cudaStream_t s)
 {
@@ -66,6 +69,13 @@ using namespace focus;
 extern "C" {
 
 void focus_profile_enable(int enable) { g_prof.enabled = enable != 0; }
+
+void focus_trace_attention(long long *group_buf, long long *window_buf, long long *dense_buf)
+{
+    g_trace[0] = group_buf;
+    g_trace[1] = window_buf;
+    g_trace[2] = dense_buf;
+}
 
 int focus_profile_read(char *names, int name_stride, double *total_ms, int *launches,
                        int max_entries)

@@ -52,15 +52,24 @@ def test_status_strings_and_version(lib):
 
 def test_assign_validation(lib):
     f = lib.focus_assign
-    #            X     Wg    C   B  n  hid dg  K topk ids  margin stream
-    assert f(None, P, P, 1, 8, 64, 16, 8, 2, P, None, None) == INVALID
-    assert f(P, P, P, 1, 8, 64, 16, 8, 9, P, None, None) == INVALID        # topk > K
-    assert f(P, P, P, 1, 8, 64, 16, 8, 0, P, None, None) == INVALID
-    assert f(MIS, P, P, 1, 8, 64, 16, 8, 2, P, None, None) == INVALID
-    assert f(P, P, P, 1, 8, 60, 16, 8, 2, P, None, None) == UNSUPPORTED    # hidden % 8
-    assert f(P, P, P, 1, 8, 64, 300, 8, 2, P, None, None) == UNSUPPORTED   # d_g > 256
-    assert f(P, P, P, 1, 8, 64, 16, 2000, 2, P, None, None) == UNSUPPORTED  # K > 1024
-    assert f(P, P, P, 1, 8, 64, 16, 20, 9, P, None, None) == UNSUPPORTED   # topk > 8
+    need = fg.focus_assign_workspace_size(64, 16, 8, 2)
+    assert need > 0
+    assert fg.focus_assign_workspace_size(64, 16, 300, 2) == 0        # K > 256: fp32 kernel
+
+    def call(X=P, hid=64, dg=16, K=8, topk=2, ws=P2, nbytes=need):
+        #        X  Wg C  B  n  hidden dg  K  topk ids margin ws  bytes  stream
+        return f(X, P, P, 1, 8, hid, dg, K, topk, P, None, ws, nbytes, None)
+
+    assert call(X=None) == INVALID
+    assert call(topk=9) == INVALID                      # topk > K
+    assert call(topk=0) == INVALID
+    assert call(X=MIS) == INVALID
+    assert call(hid=60) == UNSUPPORTED                  # hidden % 8
+    assert call(dg=300) == UNSUPPORTED                  # d_g > 256
+    assert call(K=2000) == UNSUPPORTED                  # K > 1024
+    assert call(K=20, topk=9) == UNSUPPORTED            # topk > 8
+    assert call(nbytes=need - 1) == WORKSPACE
+    assert call(ws=None) == WORKSPACE
 
 
 def test_bucket_validation(lib):
