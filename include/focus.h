@@ -155,9 +155,13 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  *   ws, ws_bytes: device workspace of at least
  *          focus_attention_workspace_size(B, n, Hq, Hkv, d, K, topk) bytes.
  * Arithmetic: bf16 operands, fp32 accumulation and softmax, probabilities
- * rounded to bf16 for the P.V product, partial outputs kept in bf16.
+ * rounded to bf16 for the P.V product, partial outputs kept in fp16 with a
+ * power-of-two scale per row (11-bit significand at any magnitude).
  * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= K <= 1024, 1 <= topk <= 8,
- *            B * K <= 4096.
+ *            B * K <= 4096, and the kernel's shared memory within 227 KB:
+ *            for d = 128 that bounds K to 904 (topk 1), 808 (topk 4) or
+ *            680 (topk 8); d = 64 takes any K <= 1024.
+ *            Otherwise FOCUS_ERR_UNSUPPORTED.
  */
 size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d,
                                       int K, int topk);

@@ -10,11 +10,16 @@
 // item = blockIdx.x, blockIdx.x + gridDim.x, ...  The pipeline (K/V stages,
 // S buffers, barrier phases) runs on across items, so the next item's Q/K/V
 // loads and first Q.K^T overlap the current item's softmax and epilogue.
-//   warps 0-3  softmax + epilogue (thread r owns query row r = TMEM lane r)
-//   warp  4    TMA producer (Q per item, K/V double-buffered) + key-tile
+//   warps 0-7  softmax + epilogue: two warpgroups share each query row
+//              (TMEM lane); warpgroup h runs an online softmax of its own over
+//              key columns [64h, 64h + 64) of every tile, with its own
+//              accumulator O_h; the two are merged at the end of the item
+//   warp  8    TMA producer (Q per item, K/V double-buffered) + key-tile
 //              group bitmaps for the masks
-//   warp  5    TMEM allocator and MMA issuer
-// TMEM columns: S double buffer at [0,128) and [128,256), O at [256,256+D).
+//   warp  9    TMEM allocator and MMA issuer: S = Q K^T, then O_h += P_h V_h
+//              for each half as soon as that half's P is written
+// TMEM columns: S double buffer at [0,128) and [128,256) (P_h written over
+// S columns [64h, 64h + 32)), O_0 at [256, 256+D), O_1 at [384, 384+D).
 //
 // Modes (the decomposition of the allowed-pair set of Focus attention,
 // gist.science/zh technical summary 2.1.3: within-group causal attention
@@ -76,7 +81,7 @@ struct AttnArgs {
 enum {
     TR_P_IEMPTY = 0, TR_P_QEMPTY = 1, TR_P_KEMPTY = 2, TR_P_VEMPTY = 3, TR_P_TOTAL = 4,
     TR_P_RING = 5, TR_M_PFULL = 8, TR_M_VFULL = 9, TR_M_IFULL = 10, TR_M_QFULL = 11,
-    TR_M_KFULL = 12, TR_M_SEMPTY = 13, TR_M_TOTAL = 14, TR_S_IFULL = 16, TR_S_META = 17,
+    TR_M_KFULL = 12, TR_M_SEMPTY = 13, TR_M_TOTAL = 14, TR_M_ISSUE = 15, TR_S_IFULL = 16, TR_S_META = 17,
     TR_S_SFULL = 18, TR_S_PVDONE = 19, TR_S_PVLAST = 20, TR_S_EPI = 21, TR_S_TOTAL = 22,
     TR_S_ITEMS = 23, TR_S_TILES = 24, TR_E_TMEM = 25, TR_E_SCALE = 26, TR_E_STORE = 27,
     TR_T_SLOAD = 28, TR_T_MASK = 29, TR_T_RESCALE = 30, TR_T_P = 31, kTraceSlots = 32
@@ -87,7 +92,12 @@ __device__ __forceinline__ void trace_flush(const long long *tr, long long *dst,
     for (int i = lo; i < hi; ++i) dst[i] = tr[i];
 }
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // 2 softmax warpgroups + producer + MMA warp
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
+constexpr uint32_t kOStride = 128;   // TMEM columns from O_0 to O_1
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // key rows per tile
 constexpr int kMaxTopk = 8;
@@ -99,10 +109,11 @@ struct AttnSmem {
     static constexpr uint32_t kK = kQ + kTile;               // 2 stages
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 stages
     static constexpr uint32_t kP = kV + 2 * kTile;           // epilogue staging, 128 x D x 2 B
-    static constexpr uint32_t kBar = kP + kBM * D * 2;       // 22 mbarriers
-    static constexpr uint32_t kMisc = kBar + 22 * 8;         // tmem slot, abort flag
+    static constexpr uint32_t kBar = kP + kBM * D * 2;       // 28 mbarriers
+    static constexpr uint32_t kMisc = kBar + 28 * 8;         // tmem slot, abort flag
     static constexpr uint32_t kTrace = kMisc + 16;           // int64 [32] trace counters
-    static constexpr uint32_t kColbits = (kTrace + 256 + 127) / 128 * 128;   // uint32 [2][K][4]
+    static constexpr uint32_t kXchg = kTrace + 256;          // float [1024]: softmax exchange
+    static constexpr uint32_t kColbits = (kXchg + 4096 + 127) / 128 * 128;   // uint32 [2][K][4]
     // then the work-item ring: 2 slots of ring_slot_bytes()
     __host__ __device__ static constexpr uint32_t colbits_bytes(int K)
     {
@@ -120,10 +131,11 @@ struct AttnSmem {
 };
 
 // mbarrier slots
+// (B_PFULL and B_PVD: [half h][tile parity], index 2h + (tile & 1))
 enum {
     B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_VEMPTY = 8,
-    B_SFULL = 10, B_SEMPTY = 12, B_PFULL = 14, B_PVDONE = 15, B_META = 16, B_IFULL = 18,
-    B_IEMPTY = 20
+    B_SFULL = 10, B_SEMPTY = 12, B_PFULL = 14, B_PVD = 18, B_META = 22, B_IFULL = 24,
+    B_IEMPTY = 26, kNumBars = 28
 };
 
 // Work-item ring slot: the decoded item (8 ints) followed by the group ids of
@@ -165,11 +177,11 @@ struct WorkItem {
     int b, h, q0, qend, kv_lo, nkv, g, gend;
 };
 
-// O *= f for this thread's TMEM lane (D columns).  Rarely taken (the row max
-// has to grow by more than 2^8), so it is kept out of line: its registers do
-// not add to those of the softmax loop.
+// O *= f for this thread's TMEM lane (D columns), 32 columns at a time.
+// Rarely taken (the row max has to grow by more than 2^8); it runs after the
+// tile's scores are dead, so its registers do not add to the softmax loop's.
 template <int D>
-__device__ __noinline__ void rescale_o(uint32_t taddr, float f)
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float f)
 {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
@@ -276,14 +288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_KEMPTY + s], 1);
             mbar_init(&bars[B_VEMPTY + s], 1);
             mbar_init(&bars[B_SFULL + s], 1);
-            mbar_init(&bars[B_SEMPTY + s], 128);
+            mbar_init(&bars[B_SEMPTY + s], kSoftmaxWarps);   // one lane per warp
             mbar_init(&bars[B_META + s], 32);
         }
-        mbar_init(&bars[B_PFULL], 128);
-        mbar_init(&bars[B_PVDONE], 1);
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&bars[B_PFULL + s], kSoftmaxWarps / 2);   // one lane per warp of a half
+            mbar_init(&bars[B_PVD + s], 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_IFULL + s], 32);           // the producer warp's lanes
-            mbar_init(&bars[B_IEMPTY + s], 128 + 1);     // softmax threads + MMA thread
+            mbar_init(&bars[B_IEMPTY + s], kSoftmaxWarps + 1);   // softmax warps + MMA thread
         }
         long long *trz = reinterpret_cast<long long *>(sm + L::kTrace);
         for (int i = 0; i < kTraceSlots; ++i) trz[i] = 0;
@@ -291,11 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_fence_init();
     }
     const int rtopk = (MODE == kDense) ? 0 : a.topk;    // per-row ring data width
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -304,12 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 256;
+    const uint32_t tmem_o = tmem + 256;     // O_0; O_1 at tmem_o + kOStride
 
     long long *tr = reinterpret_cast<long long *>(sm + L::kTrace);   // zeroed at set-up
     const long long t_start = clock64();
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------- TMA producer
         const bool trc = a.trace != nullptr && lane == 0;
         int T = 0, iq = 0;            // key tiles and query tiles issued so far
@@ -450,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // -------------------------------------------------- MMA issuer
         if (lane == 0) {
             const bool trc = a.trace != nullptr;
@@ -459,27 +473,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
             const uint32_t v_base = smem_u32(sV);
 
-            // O += P(t) V(t); `first` starts the item's accumulator.
+            // O_h += P_h(t) V_h(t) for both halves h of the tile's keys, each
+            // as soon as its P is written; `first` starts the item's accumulators.
             auto issue_pv = [&](int t, bool first) -> bool {
                 const int st = t & 1;
-                if (!mbar_wait_t(&bars[B_PFULL], t & 1, abort_flag, a.status, trc, tr[8]))
-                    return false;
                 if (!mbar_wait_t(&bars[B_VFULL + st], (t >> 1) & 1, abort_flag, a.status, trc,
                                  tr[9]))
                     return false;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // A = P in TMEM over this tile's S columns: 16 keys = 8 columns.
-                    const uint32_t at = tmem + st * kBN + kk * 8;
-                    // B = V (MN-major): 16 key rows of 128 bytes; the second
-                    // 64-column half of D lies 16 KB further (LBO).
-                    const uint64_t bd =
-                        sdesc_sw128(v_base + st * L::kTile + kk * 2048, 16384, 1024);
-                    tc_mma_bf16_ts(tmem_o, at, bd, kIdescPV, (!first || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait_t(&bars[B_PFULL + 2 * h + (t & 1)], (t >> 1) & 1, abort_flag,
+                                     a.status, trc, tr[8]))
+                        return false;
+                    tc_fence_after();
+                    const long long ti = trc ? clock64() : 0;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // A = P_h in TMEM over the half's S columns: 16 keys = 8 columns.
+                        const uint32_t at = tmem + st * kBN + 64 * h + kk * 8;
+                        // B = V (MN-major): 16 key rows of 128 bytes; the second
+                        // 64-column half of D lies 16 KB further (LBO).
+                        const uint64_t bd = sdesc_sw128(
+                            v_base + st * L::kTile + (4 * h + kk) * 2048, 16384, 1024);
+                        tc_mma_bf16_ts(tmem_o + h * kOStride, at, bd, kIdescPV,
+                                       (!first || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&bars[B_PVD + 2 * h + (t & 1)]);
+                    if (trc) tr[TR_M_ISSUE] += clock64() - ti;
                 }
                 tc_commit(&bars[B_VEMPTY + st]);
-                tc_commit(&bars[B_PVDONE]);
                 return true;
             };
 
@@ -507,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                     }
                     tc_fence_after();
+                    const long long ti = trc ? clock64() : 0;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -517,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(&bars[B_SFULL + st]);
                     tc_commit(&bars[B_KEMPTY + st]);
                     if (u == w.nkv - 1) tc_commit(&bars[B_QEMPTY]);
+                    if (trc) tr[TR_M_ISSUE] += clock64() - ti;
                     if (u >= 1) ok = issue_pv(T - 1, u == 1);
                 }
                 if (ok) ok = issue_pv(T - 1, w.nkv == 1);
@@ -529,18 +553,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------- softmax warpgroup
-        const int r = threadIdx.x;                       // row in tile, TMEM lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const bool trc = a.trace != nullptr && r == 0;
+        // ------------------------------- softmax: two independent warpgroups
+        // Thread t: query row r = t mod 128 (its TMEM lane).  Warpgroup wg =
+        // t / 128 owns key columns [64 wg, 64 wg + 64) of every S tile and runs
+        // its own online softmax over them (reference max, row sum, and the
+        // accumulator O_wg = sum of P V over its keys).  The warpgroups meet
+        // only at the start and the end of an item, where the two partial
+        // softmaxes of each row are merged exactly.
+        constexpr int kDH = D / 2;                       // output columns per warpgroup
+        constexpr int kCh = D / 8;                       // 16-byte chunks per output row
+        const int wg = warp >> 2;
+        const int r = threadIdx.x & 127;                 // row in tile, TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int cb0 = wg * 64;                         // first key column of this half
+        const uint32_t o_own = tmem_o + lane_off + wg * kOStride;   // O_wg, this lane
+        float *xm = reinterpret_cast<float *>(sm + L::kXchg);   // [2 wg][128] reference max
+        float *xl = xm + 256;                                    // [2 wg][128] row sum
+        float *xa = xl + 256;                                    // [2 wg][128] max |O|
+        int *xc = reinterpret_cast<int *>(xa + 256);             // [2 wg][128] pair count
+        const bool trc = a.trace != nullptr && threadIdx.x == 0;
         int T = 0;
         bool ok = true;
         for (int k = 0, item = blockIdx.x; ok && item < nitems;
              item = item_of(++k, blockIdx.x, gridDim.x)) {
             // the item and this row's metadata, published by the producer
+            // A failed wait is carried in okl to the next 256-thread barrier,
+            // which ends the loops in both warpgroups together.
             const int slot = k & 1;
-            if (!mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
-                             tr[16])) {
+            bool okl = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
+                                   tr[16]);
+            if (!named_bar_and(1, kSoftmaxThreads, okl)) {
                 ok = false;
                 break;
             }
@@ -572,41 +614,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (MODE == kGroup && qvalid && a.pair_count)
                 qi = a.pos[(int64_t)w.b * a.rows + prow];
 
-            float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O and l
-            float l = 0.f;
+            float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O_wg and l
+            float l = 0.f;                 // row sum over this half's keys
             int cnt = 0;
 
             for (int u = 0; u < w.nkv; ++u, ++T) {
                 const int st = T & 1;
                 const int kvb = w.kv_lo + kBN * u;       // first key row of the tile
-                if (MODE != kDense) {
-                    if (!mbar_wait_t(&bars[B_META + st], (T >> 1) & 1, abort_flag, a.status, trc,
-                                     tr[17])) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!mbar_wait_t(&bars[B_SFULL + st], (T >> 1) & 1, abort_flag, a.status, trc,
-                                 tr[18])) {
-                    ok = false;
-                    break;
-                }
+                if (MODE != kDense)
+                    okl = mbar_wait_t(&bars[B_META + st], (T >> 1) & 1, abort_flag, a.status, trc,
+                                      tr[17]);
+                okl = okl && mbar_wait_t(&bars[B_SFULL + st], (T >> 1) & 1, abort_flag, a.status,
+                                         trc, tr[18]);
+                if (!okl) break;                         // on to the end-of-item barrier
                 tc_fence_after();
                 long long tt = trc ? clock64() : 0;
-                float s[kBN];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    tmem_ld32(tmem + lane_off + st * kBN + c4 * 32, s + c4 * 32);
+                float s[64];
+                tmem_ld32(tmem + lane_off + st * kBN + cb0, s);
+                tmem_ld32(tmem + lane_off + st * kBN + cb0 + 32, s + 32);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_SEMPTY + st]);
+                // Keep this half's P.V barriers at most one phase behind: S of
+                // tile T complete means P.V of tile T - 2 complete (the tensor
+                // pipe runs in issue order), so this wait returns at once.
+                if (T >= 2)
+                    okl = mbar_wait_t(&bars[B_PVD + 2 * wg + (T & 1)], ((T - 2) >> 1) & 1,
+                                      abort_flag, a.status, trc, tr[19]);
                 if (trc) {
                     const long long t2 = clock64();
                     tr[TR_T_SLOAD] += t2 - tt;
                     tt = t2;
                 }
-                tc_fence_before();
-                mbar_arrive(&bars[B_SEMPTY + st]);
 
-                // ---- which of the 128 keys this row may score
-                uint4 excl = make_uint4(0u, 0u, 0u, 0u);
+                // ---- which of this half's 64 keys the row may score
+                uint32_t ex0 = 0u, ex1 = 0u;
                 if (MODE != kDense) {
                     const uint4 *cb =
                         reinterpret_cast<const uint4 *>(colbits + (size_t)st * a.K * 4);
@@ -614,43 +656,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < kMaxTopk; ++x) {
                         if (qg[x] >= 0) {
                             const uint4 v = cb[qg[x]];
-                            excl.x |= v.x;
-                            excl.y |= v.y;
-                            excl.z |= v.z;
-                            excl.w |= v.w;
+                            ex0 |= wg ? v.z : v.x;
+                            ex1 |= wg ? v.w : v.y;
                         }
                     }
                 }
-                const uint32_t exw[4] = {excl.x, excl.y, excl.z, excl.w};
-                uint32_t okb[4];
+                uint32_t okb[2];
 #pragma unroll
-                for (int w4 = 0; w4 < 4; ++w4) {
+                for (int j = 0; j < 2; ++j) {
+                    const int c0 = cb0 + 32 * j;
                     uint32_t bits;
                     if (!qvalid)
                         bits = 0u;
                     else if (MODE == kGroup)
-                        bits = range_bits(0, prow - kvb, 32 * w4);      // causal, group order
+                        bits = range_bits(0, prow - kvb, c0);          // causal, group order
                     else if (MODE == kWindow)
-                        bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, 32 * w4);
+                        bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, c0);
                     else
-                        bits = range_bits(0, qi - kvb, 32 * w4);
-                    okb[w4] = bits & ~exw[w4];
+                        bits = range_bits(0, qi - kvb, c0);
+                    okb[j] = bits & ~(j ? ex1 : ex0);
                 }
-                if (a.pair_count)
-                    cnt += __popc(okb[0]) + __popc(okb[1]) + __popc(okb[2]) + __popc(okb[3]);
+                if (a.pair_count) cnt += __popc(okb[0]) + __popc(okb[1]);
 
-                // masked raw scores; the row max over 8 independent chains
+                // masked raw scores; the half-row max over 8 independent chains
+                // (no selects where every key of the warp's rows is allowed)
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = -CUDART_INF_F;
+                if (!__all_sync(0xffffffffu, (okb[0] & okb[1]) == 0xffffffffu)) {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const bool on = (okb[c >> 5] >> (c & 31)) & 1u;
-                    s[c] = on ? s[c] : -CUDART_INF_F;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                    for (int c = 0; c < 64; ++c) {
+                        const bool on = (okb[c >> 5] >> (c & 31)) & 1u;
+                        s[c] = on ? s[c] : -CUDART_INF_F;
+                    }
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+#pragma unroll
+                for (int c = 0; c < 64; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7])) *
                                  a.scale_log2;   // scale > 0, so max(s) * scale = max(s * scale)
                 if (trc) {
                     const long long t2 = clock64();
@@ -658,140 +703,165 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tt = t2;
                 }
 
-                // P of the previous tile consumed and O updated by its P.V.
-                if (u >= 1) {
-                    if (!mbar_wait_t(&bars[B_PVDONE], (T - 1) & 1, abort_flag, a.status, trc,
-                                     tr[19])) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                // Lazy rescaling: keep the reference max unless the row max
-                // grows by more than 2^8.
+                // Lazy rescaling: keep the reference max unless the half-row
+                // max grows by more than 2^8.  Only a rescale touches O_wg, so
+                // only a rescale waits for the previous tile's P.V (after P is
+                // written, so that the wait overlaps the exponentials).
                 const float m_new = fmaxf(m_ref, mx);
                 const bool grow = (m_ref == -CUDART_INF_F) || (m_new > m_ref + 8.f);
-                const bool resc = grow && l > 0.f;
+                const bool resc = grow && m_ref != -CUDART_INF_F;
                 const float new_ref = grow ? m_new : m_ref;
-                if (__any_sync(0xffffffffu, resc)) {
-                    const float f = resc ? exp2f(m_ref - new_ref) : 1.f;
-                    rescale_o<D>(tmem_o + lane_off, f);     // warp-wide (tcgen05 ld/st)
-                    l *= f;
-                }
+                const float f = resc ? exp2f(m_ref - new_ref) : 1.f;
+                const bool any_resc = __any_sync(0xffffffffu, resc);
                 m_ref = new_ref;
                 const float ref = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
-                if (trc) {
-                    const long long t2 = clock64();
-                    tr[TR_T_RESCALE] += t2 - tt;
-                    tt = t2;
-                }
 
-                // ---- P = 2^(s * scale - ref) in bf16, written to TMEM over this
-                // tile's S columns (key k in column k / 2), the A operand of P.V
+                // ---- P = 2^(s * scale - ref) in bf16 into TMEM over this half's
+                // own S columns (key c in column 64 wg + c / 2): the A operand of
+                // this half's P.V
                 const float nref = -ref, sc2 = a.scale_log2;
                 float rs8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+                uint32_t pk[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float p0 = exp2f(fmaf(s[half * 64 + 2 * j], sc2, nref));
-                        const float p1 = exp2f(fmaf(s[half * 64 + 2 * j + 1], sc2, nref));
-                        rs8[j & 7] += p0 + p1;
-                        pk[j] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32u(tmem + lane_off + st * kBN + half * 32, pk);
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = exp2f(fmaf(s[2 * j], sc2, nref));
+                    const float p1 = exp2f(fmaf(s[2 * j + 1], sc2, nref));
+                    rs8[j & 7] += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
                 }
+                tmem_st32u(tmem + lane_off + st * kBN + cb0, pk);
                 tmem_st_wait();
-                l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                if (trc) tr[TR_T_P] += clock64() - tt;
+                l = fmaf(l, f, ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                                   ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                if (trc) {
+                    const long long t2 = clock64();
+                    tr[TR_T_P] += t2 - tt;
+                    tt = t2;
+                }
+                if (any_resc) {
+                    okl = okl && mbar_wait_t(&bars[B_PVD + 2 * wg + ((T - 1) & 1)],
+                                             ((T - 1) >> 1) & 1, abort_flag, a.status, trc,
+                                             tr[19]);
+                    tc_fence_after();
+                    rescale_o<D>(o_own, f);   // warp-wide
+                    if (trc) tr[TR_T_RESCALE] += clock64() - tt;
+                }
                 tc_fence_before();
-                mbar_arrive(&bars[B_PFULL]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_PFULL + 2 * wg + (T & 1)]);
+                if (!okl) break;
             }
-            if (!ok) break;
 
-            // ---- epilogue
+            // ---- epilogue: merge the two halves of each row
             const long long t_epi = trc ? clock64() : 0;
             if (w.nkv > 0) {
-                ok = mbar_wait_t(&bars[B_PVDONE], (T - 1) & 1, abort_flag, a.status, trc, tr[20]);
+                // both halves' last two P.V (this thread reads both accumulators),
+                // in phase order
+                const int last = T - 1;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (last >= 1)
+                        okl = okl && mbar_wait_t(&bars[B_PVD + 2 * h + ((last - 1) & 1)],
+                                                 ((last - 1) >> 1) & 1, abort_flag, a.status, trc,
+                                                 tr[20]);
+                    okl = okl && mbar_wait_t(&bars[B_PVD + 2 * h + (last & 1)], (last >> 1) & 1,
+                                             abort_flag, a.status, trc, tr[20]);
+                }
                 tc_fence_after();
-                if (!ok) break;
             }
-            const bool has = l > 0.f;
-            const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // base 2
-            const float inv_l = has ? 1.f / l : 0.f;
+            xm[wg * 128 + r] = m_ref;
+            xl[wg * 128 + r] = l;
+            xc[wg * 128 + r] = cnt;
+            if (!named_bar_and(1, kSoftmaxThreads, okl)) {
+                ok = false;
+                break;
+            }
+            long long te = trc ? clock64() : 0;
+            const float m0 = xm[r], m1 = xm[128 + r];
+            const float mrow = fmaxf(m0, m1);
+            const float f0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - mrow);
+            const float f1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - mrow);
+            const float lt = f0 * xl[r] + f1 * xl[128 + r];
+            const bool has = lt > 0.f;
+            const float lse2 = has ? mrow + log2f(lt) : -CUDART_INF_F;   // base 2
+            const float inv_l = has ? 1.f / lt : 0.f;
+            const float g0 = f0 * inv_l, g1 = f1 * inv_l;   // weights of O_0 and O_1
+            // this warpgroup's output columns [kDH wg, kDH wg + kDH) of both accumulators
+            const uint32_t oa = tmem_o + lane_off + wg * kDH;
+            // Pass 1: the largest |O| entry of this half row (partials only),
+            // then of the whole row through shared memory.
+            float amax_h = 0.f;
+            if (MODE != kDense && w.nkv > 0) {
+                float am8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) am8[i] = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < kDH / 16; ++c) {
+                    float o0[16], o1[16];
+                    tmem_ld16(oa + c * 16, o0);
+                    tmem_ld16(oa + kOStride + c * 16, o1);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        am8[e & 7] = fmaxf(am8[e & 7], fabsf(fmaf(o0[e], g0, o1[e] * g1)));
+                }
+                amax_h = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
+                               fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7])));
+            }
+            xa[wg * 128 + r] = amax_h;
+            named_bar_sync(1, kSoftmaxThreads);
+            const float amax = fmaxf(xa[r], xa[128 + r]);
+            const int cnt_row = xc[r] + xc[128 + r];
             int64_t orow = 0;
             if (MODE == kGroup)
                 orow = ((int64_t)w.b * a.rows + prow) * a.Hq + w.h;
             else
                 orow = ((int64_t)w.b * a.n + qi) * a.Hq + w.h;
-            // Pass 1 (partials only): the row's largest |O| entry, from TMEM.
-            long long te = trc ? clock64() : 0;
-            float amax = 0.f;
-            if (MODE != kDense && w.nkv > 0) {
-                float am8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) am8[i] = 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_off + c * 32, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) am8[e & 7] = fmaxf(am8[e & 7], fabsf(o[e]));
-                }
-                amax = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
-                             fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7]))) *
-                       inv_l;
-            }
             if (trc) {
                 const long long t2 = clock64();
                 tr[TR_E_TMEM] += t2 - te;
                 te = t2;
             }
-            // Pack the row into this thread's staging row (16-byte chunk q at slot
-            // q ^ (r mod D/8): conflict-free), then each warp copies its own 32
-            // rows out with whole-row, coalesced 16-byte stores.
-            constexpr int kCh = D / 8;                      // 16-byte chunks per row
-            const uint32_t srow = smem_u32(sStage) + r * (D * 2);
-            // Partials: O / l in fp16 scaled by a power of two so that the largest
+            // Partials: O in fp16 scaled by a power of two so that the largest
             // entry lies in [2^14, 2^15) (11-bit precision at any magnitude, no
-            // overflow), plus {lse (base 2), 2^e}.  Dense: O / l in bf16.
+            // overflow), plus {lse (base 2), 2^e}.  Dense: O in bf16.
             int ex = 0;
             if (amax > 0.f && amax < CUDART_INF_F) frexpf(amax, &ex);   // amax < 2^ex
-            const float mul = (MODE == kDense) ? inv_l
-                                               : inv_l * __int_as_float((127 + 15 - ex) << 23);
+            const float mul = (MODE == kDense) ? 1.f : __int_as_float((127 + 15 - ex) << 23);
             const float up = __int_as_float((127 - 15 + ex) << 23);     // 2^(ex - 15)
-            // Pass 2: scale, pack and stage 32 columns at a time.
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
+            const float w0 = g0 * mul, w1 = g1 * mul;
+            // Pass 2: combine, scale, pack and stage this half row, 16 columns at
+            // a time (16-byte chunk q at slot q ^ (r mod D/8): conflict-free).
+            const uint32_t srow = smem_u32(sStage) + r * (D * 2);
+#pragma unroll 1
+            for (int c = 0; c < kDH / 16; ++c) {
+                float o[16];
                 if (w.nkv > 0) {
-                    tmem_ld32(tmem_o + lane_off + c * 32, o);
+                    float o1[16];
+                    tmem_ld16(oa + c * 16, o);
+                    tmem_ld16(oa + kOStride + c * 16, o1);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], w0, o1[e] * w1);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                    for (int e = 0; e < 16; ++e) o[e] = 0.f;
                 }
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int q = c * 4 + qq;
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int q = wg * (kCh / 2) + c * 2 + qq;
                     const float *v = o + qq * 8;
                     if (MODE == kDense)
                         st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
-                                     pack_bf16x2(v[0] * mul, v[1] * mul),
-                                     pack_bf16x2(v[2] * mul, v[3] * mul),
-                                     pack_bf16x2(v[4] * mul, v[5] * mul),
-                                     pack_bf16x2(v[6] * mul, v[7] * mul));
+                                     pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                     pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
                     else
                         st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
-                                     pack_f16x2(v[0] * mul, v[1] * mul),
-                                     pack_f16x2(v[2] * mul, v[3] * mul),
-                                     pack_f16x2(v[4] * mul, v[5] * mul),
-                                     pack_f16x2(v[6] * mul, v[7] * mul));
+                                     pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
+                                     pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
                 }
             }
-            if (qvalid) {
+            if (qvalid && wg == 0) {
                 if (MODE == kDense) {
                     if (a.lse)
                         a.lse[((int64_t)w.b * a.Hq + w.h) * a.n + qi] =
@@ -806,8 +876,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tr[TR_E_SCALE] += t2 - te;
                 te = t2;
             }
-            __syncwarp();
+            named_bar_sync(1, kSoftmaxThreads);          // whole rows staged
             {
+                // warps q and q + 4 copy out the first and second 16 rows of
+                // quadrant q with whole-row, coalesced 16-byte stores
                 constexpr int kRowsPer = 32 / kCh;            // rows per warp instruction
                 const int sub = lane / kCh, q = lane % kCh;
                 uint16_t *obase = (MODE == kDense) ? reinterpret_cast<uint16_t *>(a.out)
@@ -815,8 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      : reinterpret_cast<uint16_t *>(a.win_out16);
                 const int64_t rstride = (MODE == kGroup) ? (int64_t)a.rows : (int64_t)a.n;
 #pragma unroll
-                for (int it = 0; it < 32 / kRowsPer; ++it) {
-                    const int j = warp * 32 + it * kRowsPer + sub;    // tile row
+                for (int it = 0; it < 16 / kRowsPer; ++it) {
+                    const int j = (warp & 3) * 32 + wg * 16 + it * kRowsPer + sub;   // tile row
                     const int row = w.q0 + j;
                     uint4 v;
                     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -828,11 +900,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            __syncwarp();
+            named_bar_sync(1, kSoftmaxThreads);          // staging free for the next item
             if (trc) tr[TR_E_STORE] += clock64() - te;
-            if (qvalid && a.pair_count && w.h == 0)
-                atomicAdd(&a.pair_count[(int64_t)w.b * a.n + qi], cnt);
-            mbar_arrive(&bars[B_IEMPTY + slot]);     // ring slot no longer read
+            if (qvalid && a.pair_count && w.h == 0 && wg == 0)
+                atomicAdd(&a.pair_count[(int64_t)w.b * a.n + qi], cnt_row);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_IEMPTY + slot]);     // ring slot no longer read
             if (trc) {
                 tr[TR_S_EPI] += clock64() - t_epi;
                 tr[TR_S_ITEMS] += 1;
@@ -847,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

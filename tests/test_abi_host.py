@@ -99,6 +99,13 @@ def test_attention_validation(lib):
     assert call(d=96) == UNSUPPORTED
     assert call(topk=17) == INVALID                      # topk > K
     assert call(K=2000, topk=2) == UNSUPPORTED
+    # the shared-memory bound on K for d = 128 (documented per topk)
+    # (supported shapes then stop at the workspace check: nothing launches)
+    assert call(d=128, K=904, topk=1, nbytes=1) == WORKSPACE
+    assert call(d=128, K=905, topk=1, nbytes=1) == UNSUPPORTED
+    assert call(d=128, K=680, topk=8, nbytes=1) == WORKSPACE
+    assert call(d=128, K=681, topk=8, nbytes=1) == UNSUPPORTED
+    assert call(d=64, K=1024, topk=8, nbytes=1) == WORKSPACE
     assert call(nbytes=need - 1) == WORKSPACE
     assert call(ws=None) == INVALID
     assert call(n=0) == INVALID
