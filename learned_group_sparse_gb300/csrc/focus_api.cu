@@ -266,8 +266,12 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.ntiles = ntiles;
     p.status = status;
     p.pair_count = pair_count;
+    // Two query tiles per CTA share the key/value stream: heads 2s, 2s+1 when
+    // they share a key/value head, else consecutive query tiles of one head.
+    p.pair_heads = (Hq / Hkv) % 2 == 0 ? 1 : 0;
 
-    if ((e = launch_plan(offsets, B, K, tiles, ntiles, s, launches)) != cudaSuccess)
+    if ((e = launch_plan(offsets, B, K, !p.pair_heads, tiles, ntiles, s, launches)) !=
+        cudaSuccess)
         return FOCUS_ERR_CUDA;
     if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Q),
                            static_cast<const __nv_bfloat16 *>(Kt),
@@ -537,6 +541,7 @@ focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *
     p.scale_log2 = sc * 1.4426950408889634f;
     p.K = 1;
     p.topk = 1;
+    p.pair_heads = (Hq / Hkv) % 2 == 0 ? 1 : 0;
     p.grid = grid;
     p.out = static_cast<__nv_bfloat16 *>(O);
     p.lse = lse;

@@ -1,25 +1,37 @@
-// Flash-attention mainloop for sm_103a on the 5th-generation tensor cores:
-// TMA loads Q/K/V tiles into 128-byte-swizzled shared memory, one thread
-// issues tcgen05.mma into TMEM accumulators, and a warpgroup runs the online
-// softmax reading S from TMEM and writing P (bf16) back into TMEM over the
-// same columns, where the P.V product reads it as its A operand.  MMAs from
-// one thread execute in issue order, so S of tile t+2 (same columns) is
-// written only after P.V of tile t has read P.
+// Flash-attention mainloop for sm_103a on the 5th-generation tensor cores.
 //
-// Persistent: one CTA per SM walks the work items (128-row query tile x head)
-// item = blockIdx.x, blockIdx.x + gridDim.x, ...  The pipeline (K/V stages,
-// S buffers, barrier phases) runs on across items, so the next item's Q/K/V
-// loads and first Q.K^T overlap the current item's softmax and epilogue.
-//   warps 0-7  softmax + epilogue: two warpgroups share each query row
-//              (TMEM lane); warpgroup h runs an online softmax of its own over
-//              key columns [64h, 64h + 64) of every tile, with its own
-//              accumulator O_h; the two are merged at the end of the item
-//   warp  8    TMA producer (Q per item, K/V double-buffered) + key-tile
-//              group bitmaps for the masks
-//   warp  9    TMEM allocator and MMA issuer: S = Q K^T, then O_h += P_h V_h
-//              for each half as soon as that half's P is written
-// TMEM columns: S double buffer at [0,128) and [128,256) (P_h written over
-// S columns [64h, 64h + 32)), O_0 at [256, 256+D), O_1 at [384, 384+D).
+// One CTA takes two 128-row query tiles, its two "halves" h = 0, 1, against
+// one stream of 128-row key/value tiles, so that every K/V tile that TMA
+// brings into shared memory feeds twice the tensor work: either the same
+// query rows for two heads that share a key/value head (GQA with an even
+// ratio), or two consecutive query tiles of one head.  One thread issues
+// tcgen05.mma into TMEM accumulators,
+//   S_h = Q_h K^T   (both operands in 128-byte-swizzled shared memory)
+//   O_h += P_h V    (P_h in TMEM, V in shared memory)
+// in the order  S_0(j), O_1 += P_1(j-1) V(j-1), S_1(j), O_0 += P_0(j) V(j),
+// so that while one warpgroup turns S_h into P_h the tensor core runs the
+// other half's two products: each half has a full tile of tensor time for
+// its softmax.  The tensor pipe executes in issue order, hence when S_h(j) is
+// complete, O_h += P_h(j-1) V(j-1) is complete as well: the softmax may
+// rescale O_h without a wait, and S_h(j+1), written over the same TMEM
+// columns, comes only after P_h(j) was read.
+//
+// Roles (384 threads, three warpgroups):
+//   warps 0-3  softmax and epilogue of half 0 (thread r: query row r = TMEM lane r)
+//   warps 4-7  softmax and epilogue of half 1
+//   warp  8    TMA producer (Q of each half per item, K/V double-buffered) and
+//              the key-tile group bitmaps for the masks
+//   warp  9    TMEM allocator and MMA issuer
+//   warps 10-11 idle
+// The third warpgroup hands registers to the softmax warpgroups (setmaxnreg),
+// which keep a whole 128-column row of S in registers.
+// TMEM columns: S_0 [0,128), S_1 [128,256) (P_h over the first 64 columns of
+// S_h, two bf16 keys per column), O_0 [256, 256+D), O_1 [384, 384+D).
+//
+// Persistent: one CTA per SM walks the work items item = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  The pipeline (K/V stages, barrier phases) runs
+// on across items, so the next item's loads and first Q.K^T overlap the
+// current item's softmax and epilogue.
 //
 // Modes (the decomposition of the allowed-pair set of Focus attention,
 // gist.science/zh technical summary 2.1.3: within-group causal attention
@@ -60,10 +72,12 @@ struct AttnArgs {
     int window;
     float scale_log2;      // softmax scale * log2(e)
     int K, topk;
+    int pair_heads;        // 1: halves are heads 2s, 2s+1 of one query tile; 0: query
+                           // tiles 2p, 2p+1 of one head
     const int32_t *gids;   // group ids per Q/K/V row: [B, rows, topk]
     const int32_t *offsets;  // [B, K+1]
     const int32_t *pos;    // [B, n*topk] token of each group-order row
-    const int2 *tiles;     // kGroup work list: (b*K + g, tile index in group)
+    const int2 *tiles;     // kGroup work list: (b*K + g, tile or tile-pair index in group)
     const int *ntiles;     // kGroup: number of valid entries in tiles
     __nv_bfloat16 *out;    // kDense: O [B, n, Hq, D]
     float *lse;            // kDense: lse [B, Hq, n], natural log (nullable)
@@ -77,14 +91,15 @@ struct AttnArgs {
     long long *trace;      // nullable: per-CTA wait/phase cycle counters [grid][32]
 };
 
-// Per-CTA trace slots (SM cycles): producer 0-5, MMA issuer 8-14, softmax 16-24.
+// Per-CTA trace slots (SM cycles): producer 0-5, MMA issuer 8-15, softmax of
+// half 0 (its first thread) 16-31.
 enum {
     TR_P_IEMPTY = 0, TR_P_QEMPTY = 1, TR_P_KEMPTY = 2, TR_P_VEMPTY = 3, TR_P_TOTAL = 4,
-    TR_P_RING = 5, TR_M_PFULL = 8, TR_M_VFULL = 9, TR_M_IFULL = 10, TR_M_QFULL = 11,
-    TR_M_KFULL = 12, TR_M_SEMPTY = 13, TR_M_TOTAL = 14, TR_M_ISSUE = 15, TR_S_IFULL = 16, TR_S_META = 17,
-    TR_S_SFULL = 18, TR_S_PVDONE = 19, TR_S_PVLAST = 20, TR_S_EPI = 21, TR_S_TOTAL = 22,
-    TR_S_ITEMS = 23, TR_S_TILES = 24, TR_E_TMEM = 25, TR_E_SCALE = 26, TR_E_STORE = 27,
-    TR_T_SLOAD = 28, TR_T_MASK = 29, TR_T_RESCALE = 30, TR_T_P = 31, kTraceSlots = 32
+    TR_P_RING = 5, TR_M_PFULL = 8, TR_M_LOADS = 9, TR_M_IFULL = 10, TR_M_TOTAL = 14,
+    TR_M_ISSUE = 15, TR_S_IFULL = 16, TR_S_META = 17,
+    TR_S_SFULL = 18, TR_S_ODONE = 20, TR_S_EPI = 21, TR_S_TOTAL = 22, TR_S_ITEMS = 23,
+    TR_S_TILES = 24, TR_E_TMEM = 25, TR_E_SCALE = 26, TR_E_STORE = 27, TR_T_SLOAD = 28,
+    TR_T_MASK = 29, TR_T_RESCALE = 30, TR_T_P = 31, kTraceSlots = 32
 };
 
 __device__ __forceinline__ void trace_flush(const long long *tr, long long *dst, int lo, int hi)
@@ -92,68 +107,114 @@ __device__ __forceinline__ void trace_flush(const long long *tr, long long *dst,
     for (int i = lo; i < hi; ++i) dst[i] = tr[i];
 }
 
-constexpr int kThreads = 320;   // 2 softmax warpgroups + producer + MMA warp
+constexpr int kThreads = 384;   // 2 softmax warpgroups + producer, MMA and 2 idle warps
+// Registers per thread after the split: softmax warpgroups / the third one.
+// 256 * kRegsSoftmax + 128 * kRegsOther must not exceed the launch's
+// kThreads * (registers per thread at launch), which the launcher checks.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 104;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kSoftmaxThreads = 256;
-constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
-constexpr uint32_t kOStride = 128;   // TMEM columns from O_0 to O_1
-constexpr int kBM = 128;   // query rows per tile
-constexpr int kBN = 128;   // key rows per tile
+constexpr int kBM = 128;        // query rows per tile
+constexpr int kBN = 128;        // key rows per tile
 constexpr int kMaxTopk = 8;
+constexpr uint32_t kOStride = 128;        // TMEM columns from O_0 to O_1
+constexpr uint32_t kStageWarp = 2048;     // epilogue staging per softmax warp: 32 rows x 64 B
+
+// mbarrier slots ([half] or [stage] pairs)
+enum {
+    B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_VFULL = 6, B_KEMPTY = 8, B_VEMPTY = 10,
+    B_SFULL = 12, B_PFULL = 14, B_ODONE = 16, B_META = 18, B_IFULL = 20, B_IEMPTY = 22,
+    kNumBars = 24
+};
 
 template <int D>
 struct AttnSmem {
     static constexpr uint32_t kTile = kBM * D * 2;           // one bf16 tile
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kTile;               // 2 stages
+    static constexpr uint32_t kQ = 0;                        // Q_0, Q_1
+    static constexpr uint32_t kK = kQ + 2 * kTile;           // 2 stages
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 stages
-    static constexpr uint32_t kP = kV + 2 * kTile;           // epilogue staging, 128 x D x 2 B
-    static constexpr uint32_t kBar = kP + kBM * D * 2;       // 28 mbarriers
-    static constexpr uint32_t kMisc = kBar + 28 * 8;         // tmem slot, abort flag
+    static constexpr uint32_t kStage = kV + 2 * kTile;       // 8 softmax warps x 2 KB
+    static constexpr uint32_t kBar = kStage + 8 * kStageWarp;
+    static constexpr uint32_t kMisc = kBar + kNumBars * 8;   // tmem slot, abort flag
     static constexpr uint32_t kTrace = kMisc + 16;           // int64 [32] trace counters
-    static constexpr uint32_t kXchg = kTrace + 256;          // float [1024]: softmax exchange
-    static constexpr uint32_t kColbits = (kXchg + 4096 + 127) / 128 * 128;   // uint32 [2][K][4]
+    static constexpr uint32_t kColbits = (kTrace + 256 + 127) / 128 * 128;   // uint32 [2][K][4]
     // then the work-item ring: 2 slots of ring_slot_bytes()
     __host__ __device__ static constexpr uint32_t colbits_bytes(int K)
     {
         return 2u * 16u * (uint32_t)K;
     }
-    __host__ __device__ static constexpr uint32_t ring_slot_bytes(int mode, int topk)
+    __host__ __device__ static constexpr uint32_t ring_slot_bytes(int topk)
     {
-        return (32u + 128u * 4u * (uint32_t)topk + 127u) / 128u * 128u;
+        return (64u + 2u * 128u * 2u * (uint32_t)topk + 127u) / 128u * 128u;
     }
     // dynamic shared memory of a launch (K groups and topk are 0 for kDense)
-    __host__ __device__ static constexpr uint32_t bytes(int mode, int K, int topk)
+    __host__ __device__ static constexpr uint32_t bytes(int K, int topk)
     {
-        return kColbits + colbits_bytes(K) + 2u * ring_slot_bytes(mode, topk) + 1024u;
+        return kColbits + colbits_bytes(K) + 2u * ring_slot_bytes(topk) + 1024u;
     }
 };
 
-// mbarrier slots
-// (B_PFULL and B_PVD: [half h][tile parity], index 2h + (tile & 1))
-enum {
-    B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_VEMPTY = 8,
-    B_SFULL = 10, B_SEMPTY = 12, B_PFULL = 14, B_PVD = 18, B_META = 22, B_IFULL = 24,
-    B_IEMPTY = 26, kNumBars = 28
+// A work item: two halves over one key/value row range.  Half h has query
+// rows [q0[h], qend[h]) of head hd[h] and scores key tiles [ulo[h], uhi[h])
+// of the item's nkv tiles (none when ulo == uhi).
+struct Item {
+    int b, g, gend, kv_lo, nkv;
+    int hd[2], q0[2], qend[2], ulo[2], uhi[2];
 };
 
-// Work-item ring slot: the decoded item (8 ints) followed by the group ids of
-// its 128 query rows, [128][topk].
+// Work-item ring slot: the item (16 ints) followed by the group ids of the
+// 2 x 128 query rows, [2][128][topk] int16 (-1: none).
 struct RingSlot {
     int *item;
-    int *gid;
+    int16_t *gid;
 };
 
 template <int D>
-__device__ __forceinline__ RingSlot ring_slot(uint8_t *sm, int mode, int K, int topk, int slot)
+__device__ __forceinline__ RingSlot ring_slot(uint8_t *sm, int K, int topk, int slot)
 {
     using L = AttnSmem<D>;
-    uint8_t *base = sm + L::kColbits + L::colbits_bytes(K) + slot * L::ring_slot_bytes(mode, topk);
+    uint8_t *base = sm + L::kColbits + L::colbits_bytes(K) + slot * L::ring_slot_bytes(topk);
     RingSlot r;
     r.item = reinterpret_cast<int *>(base);
-    r.gid = r.item + 8;
+    r.gid = reinterpret_cast<int16_t *>(base + 64);
     return r;
+}
+
+__device__ __forceinline__ void put_item(int *p, const Item &w)
+{
+    p[0] = w.b;
+    p[1] = w.g;
+    p[2] = w.gend;
+    p[3] = w.kv_lo;
+    p[4] = w.nkv;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        p[5 + h] = w.hd[h];
+        p[7 + h] = w.q0[h];
+        p[9 + h] = w.qend[h];
+        p[11 + h] = w.ulo[h];
+        p[13 + h] = w.uhi[h];
+    }
+}
+
+__device__ __forceinline__ Item get_item(const int *p)
+{
+    Item w;
+    w.b = p[0];
+    w.g = p[1];
+    w.gend = p[2];
+    w.kv_lo = p[3];
+    w.nkv = p[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        w.hd[h] = p[5 + h];
+        w.q0[h] = p[7 + h];
+        w.qend[h] = p[9 + h];
+        w.ulo[h] = p[11 + h];
+        w.uhi[h] = p[13 + h];
+    }
+    return w;
 }
 
 // Bit mask of columns c in [lo, hi] within the 32-column word starting at c0.
@@ -167,15 +228,6 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int c0)
     const uint32_t below_a = (1u << a) - 1u;
     return upto_b & ~below_a;
 }
-
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-struct WorkItem {
-    int b, h, q0, qend, kv_lo, nkv, g, gend;
-};
 
 // O *= f for this thread's TMEM lane (D columns), 32 columns at a time.
 // Rarely taken (the row max has to grow by more than 2^8); it runs after the
@@ -194,11 +246,19 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f)
     tmem_st_wait();
 }
 
+// Head slots per query tile: heads pair up when they share a key/value head.
+__device__ __forceinline__ int head_slots(const AttnArgs &a)
+{
+    return a.pair_heads ? a.Hq / 2 : a.Hq;
+}
+
 template <int MODE>
 __device__ __forceinline__ int total_items(const AttnArgs &a)
 {
-    if (MODE == kGroup) return (*a.ntiles) * a.Hq;
-    return a.B * ((a.n + kBM - 1) / kBM) * a.Hq;
+    if (MODE == kGroup) return (*a.ntiles) * head_slots(a);
+    const int nqt = (a.n + kBM - 1) / kBM;
+    const int nq = a.pair_heads ? nqt : (nqt + 1) / 2;
+    return a.B * nq * head_slots(a);
 }
 
 // The k-th item of CTA c among G persistent CTAs: rounds of G items, walked
@@ -209,45 +269,94 @@ __device__ __forceinline__ int item_of(int k, int c, int G)
     return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Work item -> query tile.  Heads vary fastest, so the heads that share a key
-// tile run side by side; items come heaviest first (kGroup: the tile list is
-// ordered by decreasing cost; kDense: the last query tiles first).
+// Work item -> two query tiles and their key tiles.  Head slots vary
+// fastest, so items that share key tiles run side by side; items come
+// heaviest first (kGroup: the tile list is ordered by decreasing cost;
+// kDense: the last query tiles first).
 template <int MODE>
-__device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int item)
+__device__ __forceinline__ Item decode_item(const AttnArgs &a, int item)
 {
-    WorkItem w;
+    Item w;
+    const int hsl = head_slots(a);
+    const int hs = item % hsl;
+    const int rest = item / hsl;
+    w.hd[0] = a.pair_heads ? 2 * hs : hs;
+    w.hd[1] = a.pair_heads ? 2 * hs + 1 : hs;
     w.g = 0;
     w.gend = 0;
+    int t0, base, end;     // first half's query tile; the row range tiles index into
     if (MODE == kGroup) {
-        const int tr = item / a.Hq;
-        w.h = item - tr * a.Hq;
-        const int2 tl = a.tiles[tr];
+        const int2 tl = a.tiles[rest];
         w.b = tl.x / a.K;
         w.g = tl.x - w.b * a.K;
-        const int gs = a.offsets[w.b * (a.K + 1) + w.g];
-        w.gend = a.offsets[w.b * (a.K + 1) + w.g + 1];
-        w.q0 = gs + kBM * tl.y;
-        w.qend = min(w.q0 + kBM, w.gend);
-        w.kv_lo = gs;
-        w.nkv = tl.y + 1;
+        base = a.offsets[w.b * (a.K + 1) + w.g];
+        end = a.offsets[w.b * (a.K + 1) + w.g + 1];
+        w.gend = end;
+        t0 = a.pair_heads ? tl.y : 2 * tl.y;
     } else {
         const int nqt = (a.n + kBM - 1) / kBM;
-        w.h = item % a.Hq;
-        const int rest = item / a.Hq;
-        int qt = rest % nqt;
-        w.b = rest / nqt;
-        if (MODE == kDense) qt = nqt - 1 - qt;
-        w.q0 = kBM * qt;
-        w.qend = min(w.q0 + kBM, a.n);
-        if (MODE == kDense) {
-            w.kv_lo = 0;
-            w.nkv = qt + 1;
+        const int nq = a.pair_heads ? nqt : (nqt + 1) / 2;
+        int qp = rest % nq;
+        w.b = rest / nq;
+        if (MODE == kDense) qp = nq - 1 - qp;
+        base = 0;
+        end = a.n;
+        t0 = a.pair_heads ? qp : 2 * qp;
+    }
+    int lo[2], hi[2];      // key rows of each half: [lo, hi)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int t = (a.pair_heads || h == 0) ? t0 : t0 + 1;
+        w.q0[h] = base + kBM * t;
+        w.qend[h] = min(w.q0[h] + kBM, end);
+        if (w.qend[h] < w.q0[h]) w.qend[h] = w.q0[h];
+        if (MODE == kWindow) {
+            lo[h] = max(0, w.q0[h] - a.window + 1);
+            hi[h] = a.window > 0 ? w.qend[h] : lo[h];
         } else {
-            w.kv_lo = max(0, w.q0 - a.window + 1);
-            w.nkv = a.window > 0 ? (w.qend - w.kv_lo + kBN - 1) / kBN : 0;
+            lo[h] = base;
+            hi[h] = w.qend[h];
+        }
+    }
+    w.kv_lo = lo[0];
+    const int kv_hi = max(hi[0], hi[1]);
+    w.nkv = kv_hi > w.kv_lo ? (kv_hi - w.kv_lo + kBN - 1) / kBN : 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (hi[h] > lo[h]) {
+            w.ulo[h] = (lo[h] - w.kv_lo) / kBN;
+            w.uhi[h] = (hi[h] - w.kv_lo + kBN - 1) / kBN;
+        } else {
+            w.ulo[h] = 0;
+            w.uhi[h] = 0;
         }
     }
     return w;
+}
+
+// (x0, x1) * s + c on two fp32 lanes in one instruction.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float x0, float x1, float s, float c)
+{
+    asm("{\n\t.reg .b64 rx, rs, rc, rd;\n\t"
+        "mov.b64 rx, {%2, %3};\n\t"
+        "mov.b64 rs, {%4, %4};\n\t"
+        "mov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, rx, rs, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+// (a0, a1) += (b0, b1) on two fp32 lanes in one instruction.
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
 }
 
 template <int MODE, int D>
@@ -270,41 +379,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sQ = sm + L::kQ;
     uint8_t *sK = sm + L::kK;
     uint8_t *sV = sm + L::kV;
-    uint8_t *sStage = sm + L::kP;       // epilogue staging: one output row per thread
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kMisc + 4);
     uint32_t *colbits = reinterpret_cast<uint32_t *>(sm + L::kColbits);   // [2][K][4]
+    const int rtopk = (MODE == kDense) ? 0 : a.topk;    // per-row ring data width
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[B_QFULL], 1);
-        mbar_init(&bars[B_QEMPTY], 1);
         for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_QFULL + s], 1);
+            mbar_init(&bars[B_QEMPTY + s], 1);
             mbar_init(&bars[B_KFULL + s], 1);
             mbar_init(&bars[B_VFULL + s], 1);
             mbar_init(&bars[B_KEMPTY + s], 1);
             mbar_init(&bars[B_VEMPTY + s], 1);
             mbar_init(&bars[B_SFULL + s], 1);
-            mbar_init(&bars[B_SEMPTY + s], kSoftmaxWarps);   // one lane per warp
-            mbar_init(&bars[B_META + s], 32);
-        }
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&bars[B_PFULL + s], kSoftmaxWarps / 2);   // one lane per warp of a half
-            mbar_init(&bars[B_PVD + s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_IFULL + s], 32);           // the producer warp's lanes
-            mbar_init(&bars[B_IEMPTY + s], kSoftmaxWarps + 1);   // softmax warps + MMA thread
+            mbar_init(&bars[B_PFULL + s], 4);            // one lane per warp of the half
+            mbar_init(&bars[B_ODONE + s], 1);
+            mbar_init(&bars[B_META + s], 32);            // the producer warp's lanes
+            mbar_init(&bars[B_IFULL + s], 32);
+            mbar_init(&bars[B_IEMPTY + s], 9);           // 8 softmax warps + MMA thread
         }
         long long *trz = reinterpret_cast<long long *>(sm + L::kTrace);
         for (int i = 0; i < kTraceSlots; ++i) trz[i] = 0;
         *abort_flag = 0;
         mbar_fence_init();
     }
-    const int rtopk = (MODE == kDense) ? 0 : a.topk;    // per-row ring data width
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
@@ -323,281 +426,303 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long *tr = reinterpret_cast<long long *>(sm + L::kTrace);   // zeroed at set-up
     const long long t_start = clock64();
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------- TMA producer
-        const bool trc = a.trace != nullptr && lane == 0;
-        int T = 0, iq = 0;            // key tiles and query tiles issued so far
-        bool ok = true;
-        for (int k = 0, item = blockIdx.x; ok && item < nitems;
-             item = item_of(++k, blockIdx.x, gridDim.x)) {
-            // ---- publish the decoded item and its rows' metadata (ring slot k & 1,
-            // free once item k - 2 is fully consumed)
-            if (k >= 2 && lane == 0)
-                ok = mbar_wait_t(&bars[B_IEMPTY + (k & 1)], ((k >> 1) - 1) & 1, abort_flag,
-                                 a.status, trc, tr[0]);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                ok = false;
-                break;
-            }
-            const long long t_ring = trc ? clock64() : 0;
-            const WorkItem w = decode_item<MODE>(a, item);
-            {
-                const RingSlot rs = ring_slot<D>(sm, MODE, a.K, rtopk, k & 1);
-                if (lane == 0) {
-                    rs.item[0] = w.b;
-                    rs.item[1] = w.h;
-                    rs.item[2] = w.q0;
-                    rs.item[3] = w.qend;
-                    rs.item[4] = w.kv_lo;
-                    rs.item[5] = w.nkv;
-                    rs.item[6] = w.g;
-                    rs.item[7] = w.gend;
-                }
-                if (MODE != kDense) {
-                    // the 128 query rows' group ids, [128][topk], coalesced
-                    const int32_t *src = a.gids + ((int64_t)w.b * a.rows + w.q0) * a.topk;
-                    const int nval = (w.qend - w.q0) * a.topk;
-                    for (int i = lane; i < kBM * a.topk; i += 32)
-                        rs.gid[i] = i < nval ? src[i] : -1;
-                }
-                __syncwarp();
-                mbar_arrive(&bars[B_IFULL + (k & 1)]);
-                if (trc) tr[TR_P_RING] += clock64() - t_ring;
-            }
-            if (w.nkv == 0) continue;
-            const int kvh = w.h / kv_per_q;
-            const int kv_end = (MODE == kGroup) ? w.gend : a.n;
-            // Q buffer free once the last Q.K^T of the previous item is done
-            if (iq >= 1 && lane == 0)
-                ok = mbar_wait_t(&bars[B_QEMPTY], (iq - 1) & 1, abort_flag, a.status, trc, tr[1]);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[B_QFULL], L::kTile);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_4d(sQ + c * 16384, &tmQ, &bars[B_QFULL], c * 64, w.h, w.q0, w.b);
-            }
-            ++iq;
-            for (int u = 0; u < w.nkv; ++u, ++T) {
-                const int st = T & 1;
-                const int r0 = w.kv_lo + kBN * u;
-                // Group ids of this tile's key rows (lane: rows lane + 32 j),
-                // loaded now so that the waits below hide their latency.
-                int kg[4][kMaxTopk];
-                if (MODE != kDense) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int row = r0 + lane + 32 * j;
-                        const int32_t *gp = a.gids + ((int64_t)w.b * a.rows + row) * a.topk;
-#pragma unroll
-                        for (int s = 0; s < kMaxTopk; ++s)
-                            kg[j][s] = (row < kv_end && s < a.topk) ? gp[s] : -1;
-                    }
-                }
-                if (T >= 2 && lane == 0)
-                    ok = mbar_wait_t(&bars[B_KEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
-                                     a.status, trc, tr[2]);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[B_KFULL + st], L::kTile);
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_4d(sK + st * L::kTile + c * 16384, &tmK, &bars[B_KFULL + st],
-                                    c * 64, kvh, r0, w.b);
-                }
-                // V and the masks of stage st are free once P.V of tile T-2 is
-                // done (its softmax finished reading colbits[st] before P).
-                if (T >= 2 && lane == 0)
-                    ok = mbar_wait_t(&bars[B_VEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
-                                     a.status, trc, tr[3]);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[B_VFULL + st], L::kTile);
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
-                                    c * 64, kvh, r0, w.b);
-                }
-                if (MODE != kDense) {
-                    // colbits[st][g][q] bit c: key column 32q + c belongs to group g
-                    uint32_t *cb = colbits + (size_t)st * a.K * 4;
-                    for (int i = lane; i < a.K * 4; i += 32) cb[i] = 0u;
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                        for (int s = 0; s < kMaxTopk; ++s) {
-                            const int gi = kg[j][s];
-                            if ((unsigned)gi < (unsigned)a.K)
-                                atomicOr(&cb[gi * 4 + j], 1u << lane);
-                        }
-                    }
-                    mbar_arrive(&bars[B_META + st]);
-                }
-                __syncwarp();
-            }
-        }
-        if (trc) {
-            tr[TR_P_TOTAL] = clock64() - t_start;
-            trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 0, 8);
-        }
-        // If the CTA gave up early, let the copies already issued land before
-        // shared memory is released.
-        if (*abort_flag && lane == 0) {
-            const uint64_t t0 = global_timer_ns();
-            while (iq > 0 && !mbar_try_wait(&bars[B_QFULL], (iq - 1) & 1) &&
-                   global_timer_ns() - t0 < 100000000ull) {
-            }
-            for (int t = max(0, T - 2); t < T + 1; ++t) {
-                const int st = t & 1;
-                while (!mbar_try_wait(&bars[B_KFULL + st], (t >> 1) & 1) &&
-                       global_timer_ns() - t0 < 200000000ull) {
-                }
-                while (!mbar_try_wait(&bars[B_VFULL + st], (t >> 1) & 1) &&
-                       global_timer_ns() - t0 < 300000000ull) {
-                }
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // -------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const bool trc = a.trace != nullptr;
-            constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
-            const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK);
-            const uint32_t v_base = smem_u32(sV);
-
-            // O_h += P_h(t) V_h(t) for both halves h of the tile's keys, each
-            // as soon as its P is written; `first` starts the item's accumulators.
-            auto issue_pv = [&](int t, bool first) -> bool {
-                const int st = t & 1;
-                if (!mbar_wait_t(&bars[B_VFULL + st], (t >> 1) & 1, abort_flag, a.status, trc,
-                                 tr[9]))
-                    return false;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_t(&bars[B_PFULL + 2 * h + (t & 1)], (t >> 1) & 1, abort_flag,
-                                     a.status, trc, tr[8]))
-                        return false;
-                    tc_fence_after();
-                    const long long ti = trc ? clock64() : 0;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // A = P_h in TMEM over the half's S columns: 16 keys = 8 columns.
-                        const uint32_t at = tmem + st * kBN + 64 * h + kk * 8;
-                        // B = V (MN-major): 16 key rows of 128 bytes; the second
-                        // 64-column half of D lies 16 KB further (LBO).
-                        const uint64_t bd = sdesc_sw128(
-                            v_base + st * L::kTile + (4 * h + kk) * 2048, 16384, 1024);
-                        tc_mma_bf16_ts(tmem_o + h * kOStride, at, bd, kIdescPV,
-                                       (!first || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&bars[B_PVD + 2 * h + (t & 1)]);
-                    if (trc) tr[TR_M_ISSUE] += clock64() - ti;
-                }
-                tc_commit(&bars[B_VEMPTY + st]);
-                return true;
-            };
-
-            int T = 0, iq = 0;
+    if (warp >= 8) {
+        // third warpgroup: gives registers back, then producer and MMA issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------- TMA producer
+            const bool trc = a.trace != nullptr && lane == 0;
+            int T = 0;                    // key tiles issued so far
+            int iq[2] = {0, 0};           // query tiles loaded per half
             bool ok = true;
             for (int k = 0, item = blockIdx.x; ok && item < nitems;
-             item = item_of(++k, blockIdx.x, gridDim.x)) {
-                ok = mbar_wait_t(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status, trc,
-                                 tr[10]);
-                if (!ok) break;
-                const int *wi = ring_slot<D>(sm, MODE, a.K, rtopk, k & 1).item;
-                WorkItem w;
-                w.nkv = wi[5];
-                mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
-                if (w.nkv == 0) continue;
-                ok = mbar_wait_t(&bars[B_QFULL], iq & 1, abort_flag, a.status, trc, tr[11]);
-                for (int u = 0; ok && u < w.nkv; ++u, ++T) {
-                    const int st = T & 1;
-                    ok = mbar_wait_t(&bars[B_KFULL + st], (T >> 1) & 1, abort_flag, a.status, trc,
-                                     tr[12]);
-                    if (!ok) break;
-                    if (T >= 2) {
-                        ok = mbar_wait_t(&bars[B_SEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
-                                         a.status, trc, tr[13]);
-                        if (!ok) break;
-                    }
-                    tc_fence_after();
-                    const long long ti = trc ? clock64() : 0;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint64_t ad = sdesc_sw128(q_base + off, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(k_base + st * L::kTile + off, 16, 1024);
-                        tc_mma_bf16(tmem + st * kBN, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&bars[B_SFULL + st]);
-                    tc_commit(&bars[B_KEMPTY + st]);
-                    if (u == w.nkv - 1) tc_commit(&bars[B_QEMPTY]);
-                    if (trc) tr[TR_M_ISSUE] += clock64() - ti;
-                    if (u >= 1) ok = issue_pv(T - 1, u == 1);
+                 item = item_of(++k, blockIdx.x, gridDim.x)) {
+                // ---- publish the decoded item and its rows' group ids (ring slot
+                // k & 1, free once item k - 2 is fully consumed)
+                if (k >= 2 && lane == 0)
+                    ok = mbar_wait_t(&bars[B_IEMPTY + (k & 1)], ((k >> 1) - 1) & 1, abort_flag,
+                                     a.status, trc, tr[TR_P_IEMPTY]);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
                 }
-                if (ok) ok = issue_pv(T - 1, w.nkv == 1);
-                ++iq;
+                const long long t_ring = trc ? clock64() : 0;
+                const Item w = decode_item<MODE>(a, item);
+                {
+                    const RingSlot rs = ring_slot<D>(sm, a.K, rtopk, k & 1);
+                    if (lane == 0) put_item(rs.item, w);
+                    if (MODE != kDense) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int32_t *src = a.gids + ((int64_t)w.b * a.rows + w.q0[h]) * a.topk;
+                            const int nval = (w.qend[h] - w.q0[h]) * a.topk;
+                            int16_t *dst = rs.gid + h * kBM * a.topk;
+                            for (int i = lane; i < kBM * a.topk; i += 32)
+                                dst[i] = (int16_t)(i < nval ? src[i] : -1);
+                        }
+                    }
+                    __syncwarp();
+                    mbar_arrive(&bars[B_IFULL + (k & 1)]);
+                    if (trc) tr[TR_P_RING] += clock64() - t_ring;
+                }
+                if (w.nkv == 0) continue;
+                const int kvh = w.hd[0] / kv_per_q;
+                const int kv_end = (MODE == kGroup) ? w.gend : a.n;
+                // Q_h: its buffer is free once the last Q_h.K^T of its previous item is done
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (w.uhi[h] <= w.ulo[h]) continue;
+                    if (iq[h] >= 1 && lane == 0)
+                        ok = mbar_wait_t(&bars[B_QEMPTY + h], (iq[h] - 1) & 1, abort_flag, a.status,
+                                         trc, tr[TR_P_QEMPTY]);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars[B_QFULL + h], L::kTile);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_4d(sQ + h * L::kTile + c * 16384, &tmQ, &bars[B_QFULL + h],
+                                        c * 64, w.hd[h], w.q0[h], w.b);
+                    }
+                    ++iq[h];
+                }
+                if (!ok) break;
+                for (int u = 0; u < w.nkv; ++u, ++T) {
+                    const int st = T & 1;
+                    const int r0 = w.kv_lo + kBN * u;
+                    // Group ids of this tile's key rows (lane: rows lane + 32 j),
+                    // loaded now so that the waits below hide their latency.
+                    int kg[4][kMaxTopk];
+                    if (MODE != kDense) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int row = r0 + lane + 32 * j;
+                            const int32_t *gp = a.gids + ((int64_t)w.b * a.rows + row) * a.topk;
+#pragma unroll
+                            for (int s = 0; s < kMaxTopk; ++s)
+                                kg[j][s] = (row < kv_end && s < a.topk) ? gp[s] : -1;
+                        }
+                    }
+                    if (T >= 2 && lane == 0)
+                        ok = mbar_wait_t(&bars[B_KEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
+                                         a.status, trc, tr[TR_P_KEMPTY]);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars[B_KFULL + st], L::kTile);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_4d(sK + st * L::kTile + c * 16384, &tmK, &bars[B_KFULL + st],
+                                        c * 64, kvh, r0, w.b);
+                    }
+                    // V and the masks of stage st are free once every P.V of tile
+                    // T-2 is done (its softmaxes read colbits[st] before writing P).
+                    if (T >= 2 && lane == 0)
+                        ok = mbar_wait_t(&bars[B_VEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
+                                         a.status, trc, tr[TR_P_VEMPTY]);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars[B_VFULL + st], L::kTile);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
+                                        c * 64, kvh, r0, w.b);
+                    }
+                    if (MODE != kDense) {
+                        // colbits[st][g][q] bit c: key column 32q + c belongs to group g
+                        uint32_t *cb = colbits + (size_t)st * a.K * 4;
+                        for (int i = lane; i < a.K * 4; i += 32) cb[i] = 0u;
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                            for (int s = 0; s < kMaxTopk; ++s) {
+                                const int gi = kg[j][s];
+                                if ((unsigned)gi < (unsigned)a.K)
+                                    atomicOr(&cb[gi * 4 + j], 1u << lane);
+                            }
+                        }
+                        mbar_arrive(&bars[B_META + st]);
+                    }
+                    __syncwarp();
+                }
             }
             if (trc) {
-                tr[TR_M_TOTAL] = clock64() - t_start;
-                trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 8, 16);
+                tr[TR_P_TOTAL] = clock64() - t_start;
+                trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 0, 8);
             }
+            // If the CTA gave up early, let the copies already issued land before
+            // shared memory is released.
+            if (*abort_flag && lane == 0) {
+                const uint64_t t0 = global_timer_ns();
+                for (int h = 0; h < 2; ++h)
+                    while (iq[h] > 0 && !mbar_try_wait(&bars[B_QFULL + h], (iq[h] - 1) & 1) &&
+                           global_timer_ns() - t0 < 100000000ull) {
+                    }
+                for (int t = max(0, T - 2); t < T + 1; ++t) {
+                    const int st = t & 1;
+                    while (!mbar_try_wait(&bars[B_KFULL + st], (t >> 1) & 1) &&
+                           global_timer_ns() - t0 < 200000000ull) {
+                    }
+                    while (!mbar_try_wait(&bars[B_VFULL + st], (t >> 1) & 1) &&
+                           global_timer_ns() - t0 < 300000000ull) {
+                    }
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            // -------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const bool trc = a.trace != nullptr;
+                // trace: waits for the ring, for loads (K, V, Q), for P; time in issue
+                long long c_if = 0, c_ld = 0, c_p = 0, c_is = 0;
+                constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);
+                constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
+                // Low descriptor words of the first Q, K and V tiles.  The start
+                // address is the low field (address / 16), so any other tile or
+                // step inside a tile is one add of a constant.
+                constexpr uint32_t kHiKM = sdesc_hi(1024);     // Q, K: K-major rows
+                constexpr uint32_t kHiMN = sdesc_hi(1024);     // V: MN-major
+                const uint32_t dq0 = sdesc_lo(smem_u32(sQ), 16);
+                const uint32_t dk0 = sdesc_lo(smem_u32(sK), 16);
+                const uint32_t dv0 = sdesc_lo(smem_u32(sV), 16384);
+                constexpr uint32_t kTileD = L::kTile >> 4;
+                int T = 0;                     // key tiles of earlier items
+                int iq[2] = {0, 0};            // Q loads consumed per half
+                int np[2] = {0, 0};            // P.V products issued per half
+                bool ok = true;
+                for (int k = 0, item = blockIdx.x; ok && item < nitems;
+                     item = item_of(++k, blockIdx.x, gridDim.x)) {
+                    ok = mbar_wait_t(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status,
+                                     trc, c_if);
+                    if (!ok) break;
+                    const int *wi = ring_slot<D>(sm, a.K, rtopk, k & 1).item;   // Item fields
+                    const int nkv = wi[4];
+                    const int ulo[2] = {wi[11], wi[12]}, uhi[2] = {wi[13], wi[14]};
+                    mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
+                    if (nkv == 0) continue;
+                    bool qready[2] = {false, false}, first[2] = {true, true};
+                    int kready = -1, vready = -1;   // last tile whose K / V load was waited
+                    // Q_h.K^T of tile u into S_h
+                    auto issue_qk = [&](int h, int u) -> bool {
+                        const int t = T + u, st = t & 1;
+                        if (kready < u) {
+                            if (!mbar_wait_t(&bars[B_KFULL + st], (t >> 1) & 1, abort_flag, a.status,
+                                             trc, c_ld))
+                                return false;
+                            kready = u;
+                        }
+                        if (!qready[h]) {
+                            if (!mbar_wait_t(&bars[B_QFULL + h], iq[h] & 1, abort_flag, a.status, trc,
+                                             c_ld))
+                                return false;
+                            qready[h] = true;
+                        }
+                        tc_fence_after();
+                        const long long ti = trc ? clock64() : 0;
+                        const uint32_t qd = dq0 + h * kTileD, kd = dk0 + st * kTileD;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            // 16 columns = 32 bytes; 64 columns = one 16 KB swizzle block
+                            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                            tc_mma_bf16_lo<kHiKM, kHiKM>(tmem + h * kBN, qd + off, kd + off,
+                                                         kIdescQK, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&bars[B_SFULL + h]);
+                        if (u == uhi[h] - 1) tc_commit(&bars[B_QEMPTY + h]);
+                        if (trc) c_is += clock64() - ti;
+                        return true;
+                    };
+                    // O_h += P_h(u) V(u)
+                    auto issue_pv = [&](int h, int u) -> bool {
+                        const int t = T + u, st = t & 1;
+                        if (vready < u) {
+                            if (!mbar_wait_t(&bars[B_VFULL + st], (t >> 1) & 1, abort_flag, a.status,
+                                             trc, c_ld))
+                                return false;
+                            vready = u;
+                        }
+                        if (!mbar_wait_t(&bars[B_PFULL + h], np[h] & 1, abort_flag, a.status, trc,
+                                         c_p))
+                            return false;
+                        tc_fence_after();
+                        const long long ti = trc ? clock64() : 0;
+                        const uint32_t vd = dv0 + st * kTileD;
+                        const uint32_t acc0 = first[h] ? 0u : 1u;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            // A = P_h in TMEM: 16 keys = 8 columns.  B = V (MN-major):
+                            // 16 key rows of 128 bytes (2 KB); the second 64-column half
+                            // of D lies 16 KB further (LBO).
+                            tc_mma_bf16_ts_lo<kHiMN>(tmem_o + h * kOStride, tmem + h * kBN + kk * 8,
+                                                     vd + ((kk * 2048) >> 4), kIdescPV,
+                                                     kk > 0 ? 1u : acc0);
+                        }
+                        first[h] = false;
+                        ++np[h];
+                        if (u == uhi[h] - 1) tc_commit(&bars[B_ODONE + h]);
+                        if (trc) c_is += clock64() - ti;
+                        return true;
+                    };
+                    auto in = [&](int h, int u) { return u >= ulo[h] && u < uhi[h]; };
+                    for (int u = 0; ok && u <= nkv; ++u) {
+                        if (u < nkv && in(0, u)) ok = issue_qk(0, u);
+                        if (ok && u >= 1) {
+                            if (in(1, u - 1)) ok = issue_pv(1, u - 1);
+                            if (ok) tc_commit(&bars[B_VEMPTY + ((T + u - 1) & 1)]);   // V(u-1) read
+                        }
+                        if (ok && u < nkv) {
+                            if (in(1, u)) ok = issue_qk(1, u);
+                            if (ok) tc_commit(&bars[B_KEMPTY + ((T + u) & 1)]);       // K(u) read
+                        }
+                        if (ok && u < nkv && in(0, u)) ok = issue_pv(0, u);
+                    }
+                    T += nkv;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) iq[h] += (uhi[h] > ulo[h]) ? 1 : 0;
+                }
+                if (trc) {
+                    tr[TR_M_IFULL] = c_if;
+                    tr[TR_M_LOADS] = c_ld;
+                    tr[TR_M_PFULL] = c_p;
+                    tr[TR_M_ISSUE] = c_is;
+                    tr[TR_M_TOTAL] = clock64() - t_start;
+                    trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 8, 16);
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
-        // ------------------------------- softmax: two independent warpgroups
-        // Thread t: query row r = t mod 128 (its TMEM lane).  Warpgroup wg =
-        // t / 128 owns key columns [64 wg, 64 wg + 64) of every S tile and runs
-        // its own online softmax over them (reference max, row sum, and the
-        // accumulator O_wg = sum of P V over its keys).  The warpgroups meet
-        // only at the start and the end of an item, where the two partial
-        // softmaxes of each row are merged exactly.
-        constexpr int kDH = D / 2;                       // output columns per warpgroup
-        constexpr int kCh = D / 8;                       // 16-byte chunks per output row
-        const int wg = warp >> 2;
-        const int r = threadIdx.x & 127;                 // row in tile, TMEM lane
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        // ---------------------------------------- softmax of half hh = warp / 4
+        // Thread t: query row r = t mod 128 of the half (TMEM lane r).
+        const int hh = warp >> 2;
+        const int r = threadIdx.x & 127;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const int cb0 = wg * 64;                         // first key column of this half
-        const uint32_t o_own = tmem_o + lane_off + wg * kOStride;   // O_wg, this lane
-        float *xm = reinterpret_cast<float *>(sm + L::kXchg);   // [2 wg][128] reference max
-        float *xl = xm + 256;                                    // [2 wg][128] row sum
-        float *xa = xl + 256;                                    // [2 wg][128] max |O|
-        int *xc = reinterpret_cast<int *>(xa + 256);             // [2 wg][128] pair count
+        const uint32_t s_col = tmem + lane_off + hh * kBN;        // S_h / P_h of this lane
+        const uint32_t o_col = tmem_o + lane_off + hh * kOStride; // O_h of this lane
+        const uint32_t stage = smem_u32(sm + L::kStage) + warp * kStageWarp;
         const bool trc = a.trace != nullptr && threadIdx.x == 0;
-        int T = 0;
+        int T = 0;          // key tiles of earlier items
+        int ns = 0;         // S_h tiles consumed
+        int nod = 0;        // items of this half with tiles (O_h completions)
         bool ok = true;
         for (int k = 0, item = blockIdx.x; ok && item < nitems;
              item = item_of(++k, blockIdx.x, gridDim.x)) {
-            // the item and this row's metadata, published by the producer
-            // A failed wait is carried in okl to the next 256-thread barrier,
-            // which ends the loops in both warpgroups together.
             const int slot = k & 1;
-            bool okl = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
-                                   tr[16]);
-            if (!named_bar_and(1, kSoftmaxThreads, okl)) {
-                ok = false;
-                break;
-            }
-            const RingSlot rs = ring_slot<D>(sm, MODE, a.K, rtopk, slot);
-            WorkItem w;
-            w.b = rs.item[0];
-            w.h = rs.item[1];
-            w.q0 = rs.item[2];
-            w.qend = rs.item[3];
-            w.kv_lo = rs.item[4];
-            w.nkv = rs.item[5];
-            w.g = rs.item[6];
-            w.gend = rs.item[7];
-            const int prow = w.q0 + r;                   // row in the Q tensor
-            const bool qvalid = prow < w.qend;
+            ok = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
+                             tr[TR_S_IFULL]);
+            if (!ok) break;
+            const RingSlot rs = ring_slot<D>(sm, a.K, rtopk, slot);
+            const int *wi = rs.item;     // the fields of Item, as put_item lays them out
+            const int wb = wi[0], wg = wi[1], kv_lo = wi[3], nkv = wi[4];
+            const int hd = wi[5 + hh], q0 = wi[7 + hh], qend = wi[9 + hh];
+            const int ulo = wi[11 + hh], uhi = wi[13 + hh];
+            const int prow = q0 + r;                     // row in the Q tensor
+            const bool qvalid = prow < qend;
             int qi = prow;                               // token index of the row
             // Groups whose columns this row must not score: every group of the
             // row (kWindow), or the row's groups below the tile's group (kGroup).
@@ -606,49 +731,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kMaxTopk; ++s) {
                 qg[s] = -1;
                 if (MODE != kDense && qvalid && s < a.topk) {
-                    const int gi = rs.gid[r * a.topk + s];
-                    if ((MODE == kWindow || gi < w.g) && (unsigned)gi < (unsigned)a.K)
+                    const int gi = rs.gid[(hh * kBM + r) * a.topk + s];
+                    if ((MODE == kWindow || gi < wg) && (unsigned)gi < (unsigned)a.K)
                         qg[s] = gi;
                 }
             }
             if (MODE == kGroup && qvalid && a.pair_count)
-                qi = a.pos[(int64_t)w.b * a.rows + prow];
+                qi = a.pos[(int64_t)wb * a.rows + prow];
 
-            float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O_wg and l
-            float l = 0.f;                 // row sum over this half's keys
+            float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O_h and l
+            float l = 0.f;                 // row sum
             int cnt = 0;
 
-            for (int u = 0; u < w.nkv; ++u, ++T) {
-                const int st = T & 1;
-                const int kvb = w.kv_lo + kBN * u;       // first key row of the tile
-                if (MODE != kDense)
-                    okl = mbar_wait_t(&bars[B_META + st], (T >> 1) & 1, abort_flag, a.status, trc,
-                                      tr[17]);
-                okl = okl && mbar_wait_t(&bars[B_SFULL + st], (T >> 1) & 1, abort_flag, a.status,
-                                         trc, tr[18]);
-                if (!okl) break;                         // on to the end-of-item barrier
+            for (int u = ulo; u < uhi; ++u) {
+                const int t = T + u, st = t & 1;
+                const int kvb = kv_lo + kBN * u;         // first key row of the tile
+                ok = mbar_wait_t(&bars[B_SFULL + hh], ns & 1, abort_flag, a.status, trc,
+                                 tr[TR_S_SFULL]);
+                ++ns;
+                // (S_h of tile t complete means the producer passed the masks of
+                // tile t-2, so the phase below is at most one ahead)
+                if (ok && MODE != kDense)
+                    ok = mbar_wait_t(&bars[B_META + st], (t >> 1) & 1, abort_flag, a.status,
+                                     trc, tr[TR_S_META]);
+                if (!ok) break;
                 tc_fence_after();
                 long long tt = trc ? clock64() : 0;
-                float s[64];
-                tmem_ld32(tmem + lane_off + st * kBN + cb0, s);
-                tmem_ld32(tmem + lane_off + st * kBN + cb0 + 32, s + 32);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_SEMPTY + st]);
-                // Keep this half's P.V barriers at most one phase behind: S of
-                // tile T complete means P.V of tile T - 2 complete (the tensor
-                // pipe runs in issue order), so this wait returns at once.
-                if (T >= 2)
-                    okl = mbar_wait_t(&bars[B_PVD + 2 * wg + (T & 1)], ((T - 2) >> 1) & 1,
-                                      abort_flag, a.status, trc, tr[19]);
+                float s[128];
+                tmem_ld128(s_col, s);
                 if (trc) {
                     const long long t2 = clock64();
                     tr[TR_T_SLOAD] += t2 - tt;
                     tt = t2;
                 }
 
-                // ---- which of this half's 64 keys the row may score
-                uint32_t ex0 = 0u, ex1 = 0u;
+                // ---- which of the tile's 128 keys the row may score
+                uint32_t ex[4] = {0u, 0u, 0u, 0u};
                 if (MODE != kDense) {
                     const uint4 *cb =
                         reinterpret_cast<const uint4 *>(colbits + (size_t)st * a.K * 4);
@@ -656,44 +774,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < kMaxTopk; ++x) {
                         if (qg[x] >= 0) {
                             const uint4 v = cb[qg[x]];
-                            ex0 |= wg ? v.z : v.x;
-                            ex1 |= wg ? v.w : v.y;
+                            ex[0] |= v.x;
+                            ex[1] |= v.y;
+                            ex[2] |= v.z;
+                            ex[3] |= v.w;
                         }
                     }
                 }
-                uint32_t okb[2];
+                uint32_t okb[4];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = cb0 + 32 * j;
+                for (int j = 0; j < 4; ++j) {
                     uint32_t bits;
                     if (!qvalid)
                         bits = 0u;
                     else if (MODE == kGroup)
-                        bits = range_bits(0, prow - kvb, c0);          // causal, group order
+                        bits = range_bits(0, prow - kvb, 32 * j);          // causal, group order
                     else if (MODE == kWindow)
-                        bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, c0);
+                        bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, 32 * j);
                     else
-                        bits = range_bits(0, qi - kvb, c0);
-                    okb[j] = bits & ~(j ? ex1 : ex0);
+                        bits = range_bits(0, qi - kvb, 32 * j);
+                    okb[j] = bits & ~ex[j];
                 }
-                if (a.pair_count) cnt += __popc(okb[0]) + __popc(okb[1]);
+                if (a.pair_count)
+                    cnt += __popc(okb[0]) + __popc(okb[1]) + __popc(okb[2]) + __popc(okb[3]);
 
-                // masked raw scores; the half-row max over 8 independent chains
-                // (no selects where every key of the warp's rows is allowed)
-                float mx8[8];
+                // masked raw scores (no selects where every key of the warp's
+                // rows is allowed); the row max over 8 independent chains
+                if (!__all_sync(0xffffffffu, (okb[0] & okb[1] & okb[2] & okb[3]) == 0xffffffffu)) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = -CUDART_INF_F;
-                if (!__all_sync(0xffffffffu, (okb[0] & okb[1]) == 0xffffffffu)) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
+                    for (int c = 0; c < 128; ++c) {
                         const bool on = (okb[c >> 5] >> (c & 31)) & 1u;
                         s[c] = on ? s[c] : -CUDART_INF_F;
                     }
                 }
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < 64; c += 16)
+                for (int i = 0; i < 8; ++i) mx8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+                for (int c = 24; c < 120; c += 16)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[120 + i]);
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7])) *
                                  a.scale_log2;   // scale > 0, so max(s) * scale = max(s * scale)
@@ -703,10 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tt = t2;
                 }
 
-                // Lazy rescaling: keep the reference max unless the half-row
-                // max grows by more than 2^8.  Only a rescale touches O_wg, so
-                // only a rescale waits for the previous tile's P.V (after P is
-                // written, so that the wait overlaps the exponentials).
+                // Lazy rescaling: keep the reference max unless the row max
+                // grows by more than 2^8.
                 const float m_new = fmaxf(m_ref, mx);
                 const bool grow = (m_ref == -CUDART_INF_F) || (m_new > m_ref + 8.f);
                 const bool resc = grow && m_ref != -CUDART_INF_F;
@@ -714,24 +834,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float f = resc ? exp2f(m_ref - new_ref) : 1.f;
                 const bool any_resc = __any_sync(0xffffffffu, resc);
                 m_ref = new_ref;
-                const float ref = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+                const float nref = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
 
-                // ---- P = 2^(s * scale - ref) in bf16 into TMEM over this half's
-                // own S columns (key c in column 64 wg + c / 2): the A operand of
-                // this half's P.V
-                const float nref = -ref, sc2 = a.scale_log2;
+                // ---- P = 2^(s * scale - ref) in bf16 into TMEM over the first 64
+                // columns of S_h (keys 2c, 2c+1 in column c): the A operand of P.V
+                const float sc2 = a.scale_log2;
                 float rs8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-                uint32_t pk[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = exp2f(fmaf(s[2 * j], sc2, nref));
-                    const float p1 = exp2f(fmaf(s[2 * j + 1], sc2, nref));
-                    rs8[j & 7] += p0 + p1;
-                    pk[j] = pack_bf16x2(p0, p1);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int c = half * 64 + 2 * j;
+                        float x0, x1;
+                        fma2(x0, x1, s[c], s[c + 1], sc2, nref);
+                        const float p0 = exp2f(x0), p1 = exp2f(x1);
+                        add2(rs8[2 * (j & 3)], rs8[2 * (j & 3) + 1], p0, p1);
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32u(s_col + half * 32, pk);
                 }
-                tmem_st32u(tmem + lane_off + st * kBN + cb0, pk);
                 tmem_st_wait();
                 l = fmaf(l, f, ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
                                    ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
@@ -740,176 +864,135 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tr[TR_T_P] += t2 - tt;
                     tt = t2;
                 }
+                // O_h += P_h(t-1) V(t-1) is complete (it precedes S_h(t) on the
+                // tensor pipe), so a rescale needs no wait.
                 if (any_resc) {
-                    okl = okl && mbar_wait_t(&bars[B_PVD + 2 * wg + ((T - 1) & 1)],
-                                             ((T - 1) >> 1) & 1, abort_flag, a.status, trc,
-                                             tr[19]);
-                    tc_fence_after();
-                    rescale_o<D>(o_own, f);   // warp-wide
+                    rescale_o<D>(o_col, f);   // warp-wide
                     if (trc) tr[TR_T_RESCALE] += clock64() - tt;
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_PFULL + 2 * wg + (T & 1)]);
-                if (!okl) break;
+                if (lane == 0) mbar_arrive(&bars[B_PFULL + hh]);
             }
+            if (!ok) break;
+            T += nkv;
 
-            // ---- epilogue: merge the two halves of each row
+            // ---- epilogue: this half's rows
             const long long t_epi = trc ? clock64() : 0;
-            if (w.nkv > 0) {
-                // both halves' last two P.V (this thread reads both accumulators),
-                // in phase order
-                const int last = T - 1;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (last >= 1)
-                        okl = okl && mbar_wait_t(&bars[B_PVD + 2 * h + ((last - 1) & 1)],
-                                                 ((last - 1) >> 1) & 1, abort_flag, a.status, trc,
-                                                 tr[20]);
-                    okl = okl && mbar_wait_t(&bars[B_PVD + 2 * h + (last & 1)], (last >> 1) & 1,
-                                             abort_flag, a.status, trc, tr[20]);
-                }
+            const bool has_tiles = uhi > ulo;
+            if (has_tiles) {
+                ok = mbar_wait_t(&bars[B_ODONE + hh], nod & 1, abort_flag, a.status, trc,
+                                 tr[TR_S_ODONE]);
+                ++nod;
                 tc_fence_after();
-            }
-            xm[wg * 128 + r] = m_ref;
-            xl[wg * 128 + r] = l;
-            xc[wg * 128 + r] = cnt;
-            if (!named_bar_and(1, kSoftmaxThreads, okl)) {
-                ok = false;
-                break;
+                if (!ok) break;
             }
             long long te = trc ? clock64() : 0;
-            const float m0 = xm[r], m1 = xm[128 + r];
-            const float mrow = fmaxf(m0, m1);
-            const float f0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - mrow);
-            const float f1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - mrow);
-            const float lt = f0 * xl[r] + f1 * xl[128 + r];
-            const bool has = lt > 0.f;
-            const float lse2 = has ? mrow + log2f(lt) : -CUDART_INF_F;   // base 2
-            const float inv_l = has ? 1.f / lt : 0.f;
-            const float g0 = f0 * inv_l, g1 = f1 * inv_l;   // weights of O_0 and O_1
-            // this warpgroup's output columns [kDH wg, kDH wg + kDH) of both accumulators
-            const uint32_t oa = tmem_o + lane_off + wg * kDH;
-            // Pass 1: the largest |O| entry of this half row (partials only),
-            // then of the whole row through shared memory.
-            float amax_h = 0.f;
-            if (MODE != kDense && w.nkv > 0) {
+            const bool has = l > 0.f;
+            const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // base 2
+            const float inv_l = has ? 1.f / l : 0.f;
+            // Pass 1 (partials): the row's largest |O| entry.
+            float amax = 0.f;
+            if (MODE != kDense && has_tiles) {
                 float am8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) am8[i] = 0.f;
 #pragma unroll 1
-                for (int c = 0; c < kDH / 16; ++c) {
-                    float o0[16], o1[16];
-                    tmem_ld16(oa + c * 16, o0);
-                    tmem_ld16(oa + kOStride + c * 16, o1);
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(o_col + c * 32, o);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        am8[e & 7] = fmaxf(am8[e & 7], fabsf(fmaf(o0[e], g0, o1[e] * g1)));
+                    for (int e = 0; e < 32; ++e) am8[e & 7] = fmaxf(am8[e & 7], fabsf(o[e]));
                 }
-                amax_h = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
-                               fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7])));
+                amax = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
+                             fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7]))) *
+                       inv_l;
             }
-            xa[wg * 128 + r] = amax_h;
-            named_bar_sync(1, kSoftmaxThreads);
-            const float amax = fmaxf(xa[r], xa[128 + r]);
-            const int cnt_row = xc[r] + xc[128 + r];
             int64_t orow = 0;
             if (MODE == kGroup)
-                orow = ((int64_t)w.b * a.rows + prow) * a.Hq + w.h;
+                orow = ((int64_t)wb * a.rows + prow) * a.Hq + hd;
             else
-                orow = ((int64_t)w.b * a.n + qi) * a.Hq + w.h;
+                orow = ((int64_t)wb * a.n + qi) * a.Hq + hd;
             if (trc) {
                 const long long t2 = clock64();
                 tr[TR_E_TMEM] += t2 - te;
                 te = t2;
             }
-            // Partials: O in fp16 scaled by a power of two so that the largest
+            // Partials: O / l in fp16 scaled by a power of two so that the largest
             // entry lies in [2^14, 2^15) (11-bit precision at any magnitude, no
-            // overflow), plus {lse (base 2), 2^e}.  Dense: O in bf16.
-            int ex = 0;
-            if (amax > 0.f && amax < CUDART_INF_F) frexpf(amax, &ex);   // amax < 2^ex
-            const float mul = (MODE == kDense) ? 1.f : __int_as_float((127 + 15 - ex) << 23);
-            const float up = __int_as_float((127 - 15 + ex) << 23);     // 2^(ex - 15)
-            const float w0 = g0 * mul, w1 = g1 * mul;
-            // Pass 2: combine, scale, pack and stage this half row, 16 columns at
-            // a time (16-byte chunk q at slot q ^ (r mod D/8): conflict-free).
-            const uint32_t srow = smem_u32(sStage) + r * (D * 2);
-#pragma unroll 1
-            for (int c = 0; c < kDH / 16; ++c) {
-                float o[16];
-                if (w.nkv > 0) {
-                    float o1[16];
-                    tmem_ld16(oa + c * 16, o);
-                    tmem_ld16(oa + kOStride + c * 16, o1);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = fmaf(o[e], w0, o1[e] * w1);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = 0.f;
-                }
-#pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int q = wg * (kCh / 2) + c * 2 + qq;
-                    const float *v = o + qq * 8;
-                    if (MODE == kDense)
-                        st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
-                                     pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                     pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-                    else
-                        st_shared_v4(srow + ((q ^ (r & (kCh - 1))) << 4),
-                                     pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
-                                     pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
-                }
-            }
-            if (qvalid && wg == 0) {
+            // overflow), plus {lse (base 2), 2^e}.  Dense: O / l in bf16.
+            int ex2 = 0;
+            if (amax > 0.f && amax < CUDART_INF_F) frexpf(amax, &ex2);   // amax < 2^ex2
+            const float mul = (MODE == kDense) ? inv_l
+                                               : inv_l * __int_as_float((127 + 15 - ex2) << 23);
+            const float up = __int_as_float((127 - 15 + ex2) << 23);     // 2^(ex2 - 15)
+            if (qvalid) {
                 if (MODE == kDense) {
                     if (a.lse)
-                        a.lse[((int64_t)w.b * a.Hq + w.h) * a.n + qi] =
-                            lse2 * 0.69314718055994531f;
+                        a.lse[((int64_t)wb * a.Hq + hd) * a.n + qi] = lse2 * 0.69314718055994531f;
                 } else {
                     (MODE == kGroup ? a.part_meta_out : a.win_meta_out)[orow] =
                         make_float2(lse2, up);
                 }
             }
-            if (trc) {
-                const long long t2 = clock64();
-                tr[TR_E_SCALE] += t2 - te;
-                te = t2;
-            }
-            named_bar_sync(1, kSoftmaxThreads);          // whole rows staged
-            {
-                // warps q and q + 4 copy out the first and second 16 rows of
-                // quadrant q with whole-row, coalesced 16-byte stores
-                constexpr int kRowsPer = 32 / kCh;            // rows per warp instruction
-                const int sub = lane / kCh, q = lane % kCh;
-                uint16_t *obase = (MODE == kDense) ? reinterpret_cast<uint16_t *>(a.out)
-                                  : (MODE == kGroup) ? reinterpret_cast<uint16_t *>(a.part_out16)
-                                                     : reinterpret_cast<uint16_t *>(a.win_out16);
-                const int64_t rstride = (MODE == kGroup) ? (int64_t)a.rows : (int64_t)a.n;
+            // Pass 2: 32 columns at a time, each warp through its own 2 KB
+            // staging area (row j's 64 bytes, 16-byte chunk q at slot
+            // q ^ ((j >> 1) & 3): conflict-free), then out as 64-byte row
+            // segments.
+            uint16_t *obase = (MODE == kDense) ? reinterpret_cast<uint16_t *>(a.out)
+                              : (MODE == kGroup) ? reinterpret_cast<uint16_t *>(a.part_out16)
+                                                 : reinterpret_cast<uint16_t *>(a.win_out16);
+            const int64_t rstride = (MODE == kGroup) ? (int64_t)a.rows : (int64_t)a.n;
+            const int wrow0 = q0 + (warp & 3) * 32;      // first row of this warp
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                if (has_tiles) {
+                    tmem_ld32(o_col + c * 32, o);
+                } else {
 #pragma unroll
-                for (int it = 0; it < 16 / kRowsPer; ++it) {
-                    const int j = (warp & 3) * 32 + wg * 16 + it * kRowsPer + sub;   // tile row
-                    const int row = w.q0 + j;
+                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float *v = o + q * 8;
+                    const uint32_t dst = stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+                    if (MODE == kDense)
+                        st_shared_v4(dst, pack_bf16x2(v[0] * mul, v[1] * mul),
+                                     pack_bf16x2(v[2] * mul, v[3] * mul),
+                                     pack_bf16x2(v[4] * mul, v[5] * mul),
+                                     pack_bf16x2(v[6] * mul, v[7] * mul));
+                    else
+                        st_shared_v4(dst, pack_f16x2(v[0] * mul, v[1] * mul),
+                                     pack_f16x2(v[2] * mul, v[3] * mul),
+                                     pack_f16x2(v[4] * mul, v[5] * mul),
+                                     pack_f16x2(v[6] * mul, v[7] * mul));
+                }
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int j = it * 8 + (lane >> 2), q = lane & 3;
                     uint4 v;
                     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                 : "r"(smem_u32(sStage) + j * (D * 2) + ((q ^ (j & (kCh - 1))) << 4)));
-                    if (row < w.qend) {
-                        const int64_t orr = ((int64_t)w.b * rstride + row) * a.Hq + w.h;
-                        reinterpret_cast<uint4 *>(obase + orr * D)[q] = v;
+                                 : "r"(stage + j * 64 + ((q ^ ((j >> 1) & 3)) << 4)));
+                    const int row = wrow0 + j;
+                    if (row < qend) {
+                        const int64_t orr = ((int64_t)wb * rstride + row) * a.Hq + hd;
+                        reinterpret_cast<uint4 *>(obase + orr * D + c * 32)[q] = v;
                     }
                 }
+                __syncwarp();
             }
-            named_bar_sync(1, kSoftmaxThreads);          // staging free for the next item
             if (trc) tr[TR_E_STORE] += clock64() - te;
-            if (qvalid && a.pair_count && w.h == 0 && wg == 0)
-                atomicAdd(&a.pair_count[(int64_t)w.b * a.n + qi], cnt_row);
+            if (qvalid && a.pair_count && hd == 0)
+                atomicAdd(&a.pair_count[(int64_t)wb * a.n + qi], cnt);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_IEMPTY + slot]);     // ring slot no longer read
             if (trc) {
                 tr[TR_S_EPI] += clock64() - t_epi;
                 tr[TR_S_ITEMS] += 1;
-                tr[TR_S_TILES] += w.nkv;
+                tr[TR_S_TILES] += uhi - ulo;
             }
         }
         if (trc) {

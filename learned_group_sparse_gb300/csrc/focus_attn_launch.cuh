@@ -9,7 +9,7 @@ namespace focus {
 template <int D>
 uint32_t attn_smem_bytes(int mode, int K, int topk)
 {
-    return mode == kDense ? AttnSmem<D>::bytes(kDense, 0, 0) : AttnSmem<D>::bytes(mode, K, topk);
+    return mode == kDense ? AttnSmem<D>::bytes(0, 0) : AttnSmem<D>::bytes(K, topk);
 }
 
 template <int MODE, int D>
@@ -20,6 +20,12 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     const uint32_t smem = attn_smem_bytes<D>(MODE, p.K, p.topk);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register shares after setmaxnreg must fit in what the
+    // block is launched with, or the increase would wait forever.
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if ((int64_t)fa.numRegs * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
+        return cudaErrorInvalidConfiguration;
     AttnArgs a;
     a.B = p.B;
     a.n = p.n;
@@ -30,6 +36,7 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.scale_log2 = p.scale_log2;
     a.K = p.K;
     a.topk = p.topk;
+    a.pair_heads = p.pair_heads;
     a.gids = p.gids;
     a.offsets = p.offsets;
     a.pos = p.pos;

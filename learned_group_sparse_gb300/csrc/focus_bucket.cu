@@ -159,9 +159,11 @@ __global__ void __launch_bounds__(256) bucket_scatter(const int32_t *__restrict_
 }
 
 // ------------------------------------------------------------------ plan
-// Tiles of group g: T_g = ceil(size_g / 128); tile t of a group costs t + 1
-// key tiles.  Emits every (group, t) ordered by decreasing t, groups sorted
-// by decreasing T_g inside a layer.  One block of 1024 threads; B*K <= 4096.
+// Entries of group g: its T_g = ceil(size_g / 128) query tiles, or with
+// pair_tiles the ceil(T_g / 2) pairs of consecutive tiles; entry t of a group
+// costs t + 1 (tiles) or 2t + 2 (pairs) key tiles.  Emits every (group, t)
+// ordered by decreasing t, groups sorted by decreasing entry count inside a
+// layer.  One block of 1024 threads; B*K <= 4096.
 constexpr int kPlanMax = 4096;
 
 __device__ __forceinline__ int layer_count(const int *keyT, int G, int t)
@@ -177,7 +179,8 @@ __device__ __forceinline__ int layer_count(const int *keyT, int G, int t)
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int B,
-                                                    int K, int2 *__restrict__ tiles,
+                                                    int K, int pair_tiles,
+                                                    int2 *__restrict__ tiles,
                                                     int *__restrict__ ntiles)
 {
     __shared__ int keyT[kPlanMax];
@@ -192,7 +195,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         if (i < G) {
             const int b = i / K, g = i - b * K;
             const int size = offsets[b * (K + 1) + g + 1] - offsets[b * (K + 1) + g];
-            keyT[i] = (size + 127) / 128;
+            const int qt = (size + 127) / 128;             // query tiles of the group
+            keyT[i] = pair_tiles ? (qt + 1) / 2 : qt;      // work entries of the group
             keyG[i] = i;
         } else {
             keyT[i] = -1;
@@ -352,11 +356,11 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *ntiles,
-                        cudaStream_t s, int *launches)
+cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, int2 *tiles,
+                        int *ntiles, cudaStream_t s, int *launches)
 {
     prof_begin("plan", s);
-    plan_kernel<<<1, 1024, 0, s>>>(offsets, B, K, tiles, ntiles);
+    plan_kernel<<<1, 1024, 0, s>>>(offsets, B, K, pair_tiles, tiles, ntiles);
     prof_end(s);
     *launches += 1;
     return cudaGetLastError();

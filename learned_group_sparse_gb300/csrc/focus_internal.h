@@ -51,9 +51,11 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
                           int32_t *pos, int32_t *inv, void *ws, cudaStream_t s, int *launches);
 
 // ---- attention helpers
-// Work list of the group kernel ordered by decreasing cost (tile index).
-cudaError_t launch_plan(const int32_t *offsets, int B, int K, int2 *tiles, int *ntiles,
-                        cudaStream_t s, int *launches);
+// Work list of the group kernel ordered by decreasing cost: entries (b*K + g, t)
+// for the 128-row query tiles t of every group, or, with pair_tiles, for the
+// pairs of consecutive tiles (2t, 2t+1).
+cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, int2 *tiles,
+                        int *ntiles, cudaStream_t s, int *launches);
 // Qp[b][r] = Q[b][pos[b][r]] (and K, V): rows of H*d bf16; gidp[b][r] = the
 // group ids of token pos[b][r].
 cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
@@ -74,6 +76,7 @@ struct AttnLaunch {
     int window;
     float scale_log2;
     int K, topk;
+    int pair_heads;   // the attention kernels pair heads (1) or query tiles (0)
     const int32_t *gids, *offsets, *pos;
     const int2 *tiles;
     const int *ntiles;

@@ -256,6 +256,47 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The two 32-bit words of sdesc_sw128(saddr, lbo, sbo).  The low word holds
+// the start address (/16) and the leading offset, the high word the stride
+// offset and the fixed fields; an MMA loop keeps the high word constant.
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo)
+{
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// tc_mma_bf16 with the descriptors given as low words and constant high words.
+template <uint32_t AHI, uint32_t BHI>
+__device__ __forceinline__ void tc_mma_bf16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 da, {%1, %5};\n\t"
+        "mov.b64 db, {%2, %6};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AHI), "n"(BHI)
+        : "memory");
+}
+
+// tc_mma_bf16_ts with the B descriptor given as low word and constant high word.
+template <uint32_t BHI>
+__device__ __forceinline__ void tc_mma_bf16_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                                  uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(BHI)
+        : "memory");
+}
+
 // Loads 32 consecutive fp32 columns of this thread's TMEM lane and waits.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 {

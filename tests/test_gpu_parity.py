@@ -56,6 +56,8 @@ ATTN_CASES = [
     (1, 1, 2, 2, 64, 4, 2, 16),
     (1, 129, 2, 2, 64, 1024, 8, 7),
     (2, 1500, 4, 2, 128, 64, 2, 256),
+    (1, 1100, 6, 2, 128, 16, 2, 100),     # odd GQA ratio: query tiles pair up
+    (1, 2300, 3, 3, 64, 12, 3, 300),      # odd number of query tiles per head
 ]
 
 
@@ -73,7 +75,8 @@ def test_attention_matches_oracle(case):
 
 
 @pytest.mark.parametrize("B,n,Hq,Hkv,d", [(1, 300, 2, 2, 64), (2, 1000, 8, 2, 128),
-                                         (1, 129, 1, 1, 128), (1, 2048, 4, 4, 64)])
+                                         (1, 129, 1, 1, 128), (1, 2048, 4, 4, 64),
+                                         (1, 700, 3, 1, 128)])
 def test_dense_causal_matches_oracle(B, n, Hq, Hkv, d):
     Q, Kt, V = qkv(B, n, Hq, Hkv, d, seed=3 * n)
     O, L = fg.focus_dense_causal_fwd(Q, Kt, V, with_lse=True)
