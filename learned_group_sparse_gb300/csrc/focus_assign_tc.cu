@@ -3,9 +3,12 @@
 //
 // The scores s = (X W_g) C^T are formed as s = X M with M = W_g C^T
 // ([hidden, K], fp32, once per call).  X is exactly bf16, so splitting M into
-// two bf16 parts M = M_hi + M_lo (residual below 2^-17 of |M|) and running two
-// tcgen05 bf16 MMAs with fp32 accumulation gives fp32-accurate scores:
-//   S[128 tokens, Kp] (TMEM) = X_tile . M_hi^T + X_tile . M_lo^T.
+// two bf16 parts M = M_hi + M_lo (residual below 2^-17 of |M|) and running
+// tcgen05 bf16 MMAs with fp32 accumulation gives fp32-accurate scores.  The
+// two parts are stacked as one B operand [M_hi; M_lo] ([2 Kp, hidden]), so one
+// MMA of N = 2 Kp (two of N = Kp when 2 Kp > 256) yields
+//   S_hi[128 tokens, Kp] = X_tile . M_hi^T and S_lo = X_tile . M_lo^T
+// in TMEM, and the epilogue adds them.
 // The epilogue keeps each token's top-(k+1) scores in registers (one thread
 // per token = TMEM lane), in descending order with ties to the lower id, and
 // writes the ids and the smallest gap between consecutive kept scores.
@@ -32,30 +35,39 @@ __device__ __forceinline__ bool better(float s1, int i1, float s2, int i2)
     return s1 > s2 || (s1 == s2 && i1 < i2);
 }
 
-// M^T split: mhi[c][h], mlo[c][h] for c < Kp (rows >= K are zero).
+// M^T split: mhi[c][h], mlo[c][h] for c < Kp (rows >= K are zero).  Block:
+// 32 centroids x 32 hidden rows, both operands staged in shared memory; each
+// thread accumulates 4 hidden rows of one centroid.
 __global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restrict__ Wg,
                                                           const float *__restrict__ C,
                                                           int hidden, int dg, int K, int Kp,
                                                           __nv_bfloat16 *__restrict__ mhi,
                                                           __nv_bfloat16 *__restrict__ mlo)
 {
-    // block: 32 centroids x 8 hidden rows per pass; C rows staged in shared memory
-    extern __shared__ float csm[];   // [dg][32]
-    const int c0 = blockIdx.y * 32;
+    extern __shared__ float psm[];
+    float *csm = psm;                  // [dg][32]: C rows c0..c0+31, transposed
+    float *wsm = psm + 32 * dg;        // [32][dg + 1]: W_g rows h0..h0+31
+    const int c0 = blockIdx.y * 32, h0 = blockIdx.x * 32;
     for (int i = threadIdx.x; i < 32 * dg; i += blockDim.x) {
-        const int c = i / dg, e = i - c * dg;
-        csm[e * 32 + c] = (c0 + c < K) ? C[(int64_t)(c0 + c) * dg + e] : 0.f;
+        const int r = i / dg, e = i - r * dg;
+        csm[e * 32 + r] = (c0 + r < K) ? C[(int64_t)(c0 + r) * dg + e] : 0.f;
+        wsm[r * (dg + 1) + e] = (h0 + r < hidden) ? Wg[(int64_t)(h0 + r) * dg + e] : 0.f;
     }
     __syncthreads();
     const int tc = threadIdx.x & 31, th = threadIdx.x >> 5;
-    for (int h = blockIdx.x * 8 + th; h < hidden; h += gridDim.x * 8) {
-        const float *w = Wg + (int64_t)h * dg;
-        float acc = 0.f;
-        for (int e = 0; e < dg; ++e) acc = fmaf(w[e], csm[e * 32 + tc], acc);
-        const int c = c0 + tc;
-        if (c < Kp) {
-            const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int e = 0; e < dg; ++e) {
+        const float cv = csm[e * 32 + tc];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(wsm[(th + 8 * j) * (dg + 1) + e], cv, acc[j]);
+    }
+    const int c = c0 + tc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int h = h0 + th + 8 * j;
+        if (c < Kp && h < hidden) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
             mhi[(int64_t)c * hidden + h] = hi;
             mlo[(int64_t)c * hidden + h] = lo;
         }
@@ -73,8 +85,7 @@ struct TcArgs {
 __device__ __forceinline__ uint32_t tc_stage_bytes(int Kp) { return 128u * kTokens + 2u * 128u * Kp; }
 
 __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                           const __grid_constant__ CUtensorMap tmHi,
-                                                           const __grid_constant__ CUtensorMap tmLo,
+                                                           const __grid_constant__ CUtensorMap tmM,
                                                            const TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -89,7 +100,7 @@ __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant
     const int nsteps = a.hidden / kHK;
     const int64_t t0 = (int64_t)blockIdx.x * kTokens;
     uint32_t ncols = 32;
-    while ((int)ncols < a.Kp) ncols <<= 1;
+    while ((int)ncols < 2 * a.Kp) ncols <<= 1;     // S_hi at column 0, S_lo at column Kp
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -106,8 +117,7 @@ __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant
     }
     if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tmX);
-        tma_prefetch_desc(&tmHi);
-        tma_prefetch_desc(&tmLo);
+        tma_prefetch_desc(&tmM);
     }
     tc_fence_before();
     __syncthreads();
@@ -124,14 +134,17 @@ __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant
                 uint8_t *base = sm + st * stage_bytes;
                 mbar_arrive_expect_tx(&bars[st], stage_bytes);
                 tma_load_2d(base, &tmX, &bars[st], k * kHK, (int)t0);
-                tma_load_2d(base + 128 * kTokens, &tmHi, &bars[st], k * kHK, 0);
-                tma_load_2d(base + 128 * kTokens + 128 * a.Kp, &tmLo, &bars[st], k * kHK, 0);
+                // [M_hi; M_lo] rows in boxes of up to 256
+                for (int r0 = 0; r0 < 2 * a.Kp; r0 += 256)
+                    tma_load_2d(base + 128 * kTokens + 128 * r0, &tmM, &bars[st], k * kHK, r0);
             }
         }
         __syncwarp();
     } else if (warp == 5) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTokens, a.Kp, false, false);
+            // one MMA of N = 2 Kp over [M_hi; M_lo], or two of N = Kp
+            const bool one = 2 * a.Kp <= 256;
+            const uint32_t idesc = idesc_bf16_f32(kTokens, one ? 2 * a.Kp : a.Kp, false, false);
             bool ok = true;
             for (int k = 0; k < nsteps && ok; ++k) {
                 const int st = k % a.stages;
@@ -144,9 +157,11 @@ __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < kHK / 16; ++kk) {
                     const uint64_t ad = sdesc_sw128(xa + kk * 32, 16, 1024);
-                    tc_mma_bf16(tmem, ad, sdesc_sw128(hb + kk * 32, 16, 1024), idesc,
-                                (k > 0 || kk > 0) ? 1u : 0u);
-                    tc_mma_bf16(tmem, ad, sdesc_sw128(lb + kk * 32, 16, 1024), idesc, 1u);
+                    const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_bf16(tmem, ad, sdesc_sw128(hb + kk * 32, 16, 1024), idesc, acc);
+                    if (!one)
+                        tc_mma_bf16(tmem + a.Kp, ad, sdesc_sw128(lb + kk * 32, 16, 1024), idesc,
+                                    acc);
                 }
                 tc_commit(&bars[a.stages + st]);
             }
@@ -168,12 +183,13 @@ __global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant
             bi[j] = 0x7fffffff;
         }
         for (int c0 = 0; c0 < a.Kp; c0 += 32) {
-            float v[32];
+            float v[32], vl[32];
             tmem_ld32(tmem + lane_off + c0, v);
+            tmem_ld32(tmem + lane_off + a.Kp + c0, vl);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 int ci = c0 + e;
-                float cv = v[e];
+                float cv = v[e] + vl[e];
                 if (cv != cv) cv = -CUDART_INF_F;
                 // ids arrive in increasing order, so a tie never displaces a kept id
                 if (ci >= a.K || !better(cv, ci, bs[kMaxSel - 1], bi[kMaxSel - 1])) continue;
@@ -232,11 +248,11 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
                              int *launches)
 {
     const int Kp = assign_tc_kp(p.K);
-    __nv_bfloat16 *mhi = static_cast<__nv_bfloat16 *>(ws);
+    __nv_bfloat16 *mhi = static_cast<__nv_bfloat16 *>(ws);   // [M_hi; M_lo]: [2 Kp, hidden]
     __nv_bfloat16 *mlo = mhi + (size_t)Kp * p.hidden;
     {
-        const dim3 grid((unsigned)((p.hidden + 7) / 8), (unsigned)((Kp + 31) / 32));
-        const size_t smem = sizeof(float) * 32 * (size_t)p.dg;
+        const dim3 grid((unsigned)((p.hidden + 31) / 32), (unsigned)((Kp + 31) / 32));
+        const size_t smem = sizeof(float) * ((size_t)32 * p.dg + (size_t)32 * (p.dg + 1));
         cudaError_t e = cudaFuncSetAttribute(assign_prep_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -246,10 +262,10 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
         *launches += 1;
     }
     if (p.ntok == 0) return cudaGetLastError();
-    CUtensorMap mx, mh, ml;
+    CUtensorMap mx, mm;
     if (!make_map_2d_bf16(&mx, p.X, (uint64_t)p.hidden, (uint64_t)p.ntok, kHK, kTokens) ||
-        !make_map_2d_bf16(&mh, mhi, (uint64_t)p.hidden, (uint64_t)Kp, kHK, (uint32_t)Kp) ||
-        !make_map_2d_bf16(&ml, mlo, (uint64_t)p.hidden, (uint64_t)Kp, kHK, (uint32_t)Kp))
+        !make_map_2d_bf16(&mm, mhi, (uint64_t)p.hidden, (uint64_t)(2 * Kp), kHK,
+                          (uint32_t)(2 * Kp <= 256 ? 2 * Kp : 256)))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.ntok = p.ntok;
@@ -268,7 +284,7 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
     if (e != cudaSuccess) return e;
     const int64_t blocks = (p.ntok + kTokens - 1) / kTokens;
     prof_begin("assign", s);
-    assign_tc_kernel<<<(unsigned)blocks, 192, smem, s>>>(mx, mh, ml, a);
+    assign_tc_kernel<<<(unsigned)blocks, 192, smem, s>>>(mx, mm, a);
     prof_end(s);
     *launches += 1;
     return cudaGetLastError();

@@ -452,13 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const RingSlot rs = ring_slot<D>(sm, a.K, rtopk, k & 1);
                     if (lane == 0) put_item(rs.item, w);
                     if (MODE != kDense) {
+                        // (halves over the same rows share the first copy)
+                        const int nh = (w.q0[1] == w.q0[0]) ? 1 : 2;
+                        const int n = kBM * a.topk;
+#pragma unroll 1
+                        for (int h = 0; h < nh; ++h) {
+                            const int q0h = h ? w.q0[1] : w.q0[0], qeh = h ? w.qend[1] : w.qend[0];
+                            const int32_t *src = a.gids + ((int64_t)w.b * a.rows + q0h) * a.topk;
+                            const int nval = (qeh - q0h) * a.topk;
+                            int16_t *dst = rs.gid + h * n;
+#pragma unroll 1
+                            for (int i0 = lane; i0 < n; i0 += 128) {
+                                int v[4];   // four loads in flight per lane
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int32_t *src = a.gids + ((int64_t)w.b * a.rows + w.q0[h]) * a.topk;
-                            const int nval = (w.qend[h] - w.q0[h]) * a.topk;
-                            int16_t *dst = rs.gid + h * kBM * a.topk;
-                            for (int i = lane; i < kBM * a.topk; i += 32)
-                                dst[i] = (int16_t)(i < nval ? src[i] : -1);
+                                for (int j = 0; j < 4; ++j) {
+                                    const int i = i0 + 32 * j;
+                                    v[j] = i < nval ? src[i] : -1;
+                                }
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    if (i0 + 32 * j < n) dst[i0 + 32 * j] = (int16_t)v[j];
+                            }
                         }
                     }
                     __syncwarp();
@@ -721,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int wb = wi[0], wg = wi[1], kv_lo = wi[3], nkv = wi[4];
             const int hd = wi[5 + hh], q0 = wi[7 + hh], qend = wi[9 + hh];
             const int ulo = wi[11 + hh], uhi = wi[13 + hh];
+            const int gh = (q0 == wi[7]) ? 0 : 1;     // ring copy of this half's group ids
             const int prow = q0 + r;                     // row in the Q tensor
             const bool qvalid = prow < qend;
             int qi = prow;                               // token index of the row
@@ -731,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kMaxTopk; ++s) {
                 qg[s] = -1;
                 if (MODE != kDense && qvalid && s < a.topk) {
-                    const int gi = rs.gid[(hh * kBM + r) * a.topk + s];
+                    const int gi = rs.gid[(gh * kBM + r) * a.topk + s];
                     if ((MODE == kWindow || gi < wg) && (unsigned)gi < (unsigned)a.K)
                         qg[s] = gi;
                 }

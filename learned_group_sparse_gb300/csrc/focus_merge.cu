@@ -44,44 +44,57 @@ __global__ void __launch_bounds__(256) merge_kernel(
         const float2 mw = win_meta[tokrow * Hq + h];
         l[0] = mw.x;
         sc[0] = mw.y;
-        for (int s = 0; s < topk; ++s) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
             l[s + 1] = -CUDART_INF_F;
             sc[s + 1] = 0.f;
-            if (rows[s] >= 0) {
+            if (s < topk && rows[s] >= 0) {
                 const float2 mp = part_meta[rows[s] * Hq + h];
                 l[s + 1] = mp.x;
                 sc[s + 1] = mp.y;
             }
         }
         float m = -CUDART_INF_F;
-        for (int p = 0; p < np; ++p) m = fmaxf(m, l[p]);
+#pragma unroll
+        for (int p = 0; p < 9; ++p) m = fmaxf(m, l[p]);
         float L = -CUDART_INF_F;
         if (m != -CUDART_INF_F) {
             float sum = 0.f;
-            for (int p = 0; p < np; ++p) sum += exp2f(l[p] - m);
+#pragma unroll
+            for (int p = 0; p < 9; ++p) sum += exp2f(l[p] - m);   // absent parts add 0
             L = m + log2f(sum);
         }
-        for (int p = 0; p < np; ++p)
-            wts[h * np + p] = (L == -CUDART_INF_F) ? 0.f : exp2f(l[p] - L) * sc[p];
+#pragma unroll
+        for (int p = 0; p < 9; ++p)
+            if (p < np) wts[h * np + p] = (L == -CUDART_INF_F) ? 0.f : exp2f(l[p] - L) * sc[p];
         if (lse) lse[(b * Hq + h) * n + i] = L * 0.69314718055994531f;
     }
     __syncthreads();
     const int units = Hq * d / 8;
     for (int u = threadIdx.x; u < units; u += blockDim.x) {
         const int h = (u * 8) / d;
+        // all parts' 16-byte vectors are loaded before any is used, so that
+        // the loads of a unit are in flight together
+        uint4 raw[9];
+        float wp[9];
+#pragma unroll
+        for (int p = 0; p < 9; ++p) {
+            wp[p] = p < np ? wts[h * np + p] : 0.f;
+            raw[p] = make_uint4(0u, 0u, 0u, 0u);
+            if (wp[p] != 0.f)
+                raw[p] = (p == 0) ? win16[tokrow * units + u] : part16[rows[p - 1] * units + u];
+        }
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int p = 0; p < np; ++p) {
-            const float w = wts[h * np + p];
-            if (w == 0.f) continue;
-            const uint4 raw = (p == 0) ? win16[tokrow * units + u] : part16[rows[p - 1] * units + u];
-            const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int p = 0; p < 9; ++p) {
+            const __half2 *hv = reinterpret_cast<const __half2 *>(&raw[p]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f = __half22float2(hv[e]);
-                acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
-                acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+                acc[2 * e] = fmaf(wp[p], f.x, acc[2 * e]);
+                acc[2 * e + 1] = fmaf(wp[p], f.y, acc[2 * e + 1]);
             }
         }
         uint4 o;
