@@ -3,8 +3,8 @@
 
 One step = focus_prefill on device-resident inputs: centroid scoring and
 top-k (focus_assign), group bucketing (focus_bucket) and Focus attention
-(focus_attention_fwd: plan, gather, group-causal kernel, window kernel with
-the log-sum-exp merge fused into its epilogue).
+(focus_attention_fwd: plan, gather into group order, group-causal kernel,
+window kernel, log-sum-exp merge).
 Prints ONE JSON line (rank 0).  Metric: prefill tokens/s; the line also
 carries effective TFLOP/s over the allowed pairs, the roofline of the
 dominant kernel, the speedup over the library's own dense causal kernel,
@@ -381,7 +381,7 @@ def main():
                 "traffic": traffic_lookup(dom, w.name, src_hash()),
                 "algorithmic_per_launch": work[0], "algorithmic_unit": work[1]}
     attn_ms = sum(prof.get(k, (0.0, 1))[0] for k in ("attn_group", "attn_window", "gather",
-                                                      "plan")) / prof_steps
+                                                      "merge", "plan")) / prof_steps
 
     # ---- the library's own dense causal kernel on the same Q/K/V
     dense = None
