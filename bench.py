@@ -447,11 +447,18 @@ def main():
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
         ids_all, cores = oracle_setup(w, t)
-        nrows = 2048 if ntok >= 2048 else ntok
-        secs, nr = oracle_sample(w, t, sample_rows(w, nrows, 7), ids_all)
+        # a bounded sample of about 10-15 s of CPU work: calibrate, then repeat
+        # seeded row samples (at most all tokens each) until 10 s have run
+        cal_s, cal_n = oracle_sample(w, t, sample_rows(w, 64, 99), ids_all)
+        per = int(max(16, min(ntok, 12.0 * cal_n / cal_s)))
+        secs, nr, reps = 0.0, 0, 0
+        while secs < 10.0 and reps < 8:
+            s_, n_ = oracle_sample(w, t, sample_rows(w, per, 7 + reps), ids_all)
+            secs, nr, reps = secs + s_, nr + n_, reps + 1
         cpu = {"value": nr / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{nr} seeded query rows of {w.name}: their group assignment plus "
-                         f"exact masked softmax over all {w.Hq} heads ({secs:.1f} s wall)"}
+               "sample": f"{reps} x {per} seeded query rows of {w.name}: their group "
+                         f"assignment plus exact masked softmax over all {w.Hq} heads "
+                         f"({secs:.1f} s wall)"}
 
     clk = clocks.summary()
     if rank == 0:
