@@ -84,7 +84,7 @@ struct TcArgs {
 
 __device__ __forceinline__ uint32_t tc_stage_bytes(int Kp) { return 128u * kTokens + 2u * 128u * Kp; }
 
-__global__ void __launch_bounds__(192, 1) assign_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                            const __grid_constant__ CUtensorMap tmM,
                                                            const TcArgs a)
 {
@@ -274,7 +274,11 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
     a.Kp = Kp;
     a.topk = p.topk;
     const uint32_t stage = 128u * kTokens + 2u * 128u * Kp;
-    a.stages = Kp <= 128 ? 4 : 2;
+    // Stages within ~110 KB so that two CTAs share an SM: one streams X while
+    // the other runs its top-k epilogue.
+    a.stages = (int)(113u * 1024u / stage);
+    if (a.stages > 4) a.stages = 4;
+    if (a.stages < 2) a.stages = 2;
     a.ids = p.ids;
     a.margin = p.margin;
     a.status = status;
