@@ -159,8 +159,8 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  * power-of-two scale per row (11-bit significand at any magnitude).
  * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= K <= 1024, 1 <= topk <= 8,
  *            B * K <= 4096, and the kernel's shared memory within 227 KB:
- *            for d = 128 that bounds K to 520 (topk 1), 488 (topk 2),
- *            424 (topk 4) or 296 (topk 8); d = 64 takes any K <= 1024.
+ *            for d = 128 that bounds K to 1000 (topk 2), 936 (topk 4) or
+ *            808 (topk 8); topk 1 and d = 64 take any K <= 1024.
  *            Otherwise FOCUS_ERR_UNSUPPORTED.
  */
 size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d,

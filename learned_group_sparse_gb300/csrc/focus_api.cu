@@ -300,7 +300,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
     if ((e = launch_merge(Owin, Mwin, Opart, Mpart, inv, B, n, topk, Hq, d,
-                          static_cast<__nv_bfloat16 *>(O), lse, s, launches)) != cudaSuccess)
+                          static_cast<__nv_bfloat16 *>(O), lse, status, s, launches)) !=
+        cudaSuccess)
         return FOCUS_ERR_CUDA;
     return FOCUS_OK;
 }

@@ -119,7 +119,6 @@ constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // key rows per tile
 constexpr int kMaxTopk = 8;
 constexpr uint32_t kOStride = 128;        // TMEM columns from O_0 to O_1
-constexpr uint32_t kStageWarp = 2048;     // epilogue staging per softmax warp: 32 rows x 64 B
 
 // mbarrier slots ([half] or [stage] pairs)
 enum {
@@ -134,8 +133,7 @@ struct AttnSmem {
     static constexpr uint32_t kQ = 0;                        // Q_0, Q_1
     static constexpr uint32_t kK = kQ + 2 * kTile;           // 2 stages
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 stages
-    static constexpr uint32_t kStage = kV + 2 * kTile;       // 8 softmax warps x 2 KB
-    static constexpr uint32_t kBar = kStage + 8 * kStageWarp;
+    static constexpr uint32_t kBar = kV + 2 * kTile;
     static constexpr uint32_t kMisc = kBar + kNumBars * 8;   // tmem slot, abort flag
     static constexpr uint32_t kTrace = kMisc + 16;           // int64 [32] trace counters
     static constexpr uint32_t kColbits = (kTrace + 256 + 127) / 128 * 128;   // uint32 [2][K][4]
@@ -718,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_col = tmem + lane_off + hh * kBN;        // S_h / P_h of this lane
         const uint32_t o_col = tmem_o + lane_off + hh * kOStride; // O_h of this lane
-        const uint32_t stage = smem_u32(sm + L::kStage) + warp * kStageWarp;
         const bool trc = a.trace != nullptr && threadIdx.x == 0;
         int T = 0;          // key tiles of earlier items
         int ns = 0;         // S_h tiles consumed
@@ -950,15 +947,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_float2(lse2, up);
                 }
             }
-            // Pass 2: 32 columns at a time, each warp through its own 2 KB
-            // staging area (row j's 64 bytes, 16-byte chunk q at slot
-            // q ^ ((j >> 1) & 3): conflict-free), then out as 64-byte row
-            // segments.
+            // Pass 2: 32 columns at a time straight from registers; each lane
+            // writes its own row.  Partials (workspace rows, 32-byte aligned)
+            // go out as 32-byte stores, whole sectors; the dense output as
+            // 16-byte stores.
             uint16_t *obase = (MODE == kDense) ? reinterpret_cast<uint16_t *>(a.out)
                               : (MODE == kGroup) ? reinterpret_cast<uint16_t *>(a.part_out16)
                                                  : reinterpret_cast<uint16_t *>(a.win_out16);
-            const int64_t rstride = (MODE == kGroup) ? (int64_t)a.rows : (int64_t)a.n;
-            const int wrow0 = q0 + (warp & 3) * 32;      // first row of this warp
+            uint16_t *orow_p = obase + orow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
@@ -968,36 +964,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0.f;
                 }
+                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float *v = o + q * 8;
-                    const uint32_t dst = stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
-                    if (MODE == kDense)
-                        st_shared_v4(dst, pack_bf16x2(v[0] * mul, v[1] * mul),
-                                     pack_bf16x2(v[2] * mul, v[3] * mul),
-                                     pack_bf16x2(v[4] * mul, v[5] * mul),
-                                     pack_bf16x2(v[6] * mul, v[7] * mul));
-                    else
-                        st_shared_v4(dst, pack_f16x2(v[0] * mul, v[1] * mul),
-                                     pack_f16x2(v[2] * mul, v[3] * mul),
-                                     pack_f16x2(v[4] * mul, v[5] * mul),
-                                     pack_f16x2(v[6] * mul, v[7] * mul));
-                }
-                __syncwarp();
+                for (int q = 0; q < 16; ++q)
+                    pk[q] = (MODE == kDense) ? pack_bf16x2(o[2 * q] * mul, o[2 * q + 1] * mul)
+                                             : pack_f16x2(o[2 * q] * mul, o[2 * q + 1] * mul);
+                if (qvalid) {
+                    if (MODE == kDense) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow_p + c * 32);
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int j = it * 8 + (lane >> 2), q = lane & 3;
-                    uint4 v;
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                 : "r"(stage + j * 64 + ((q ^ ((j >> 1) & 3)) << 4)));
-                    const int row = wrow0 + j;
-                    if (row < qend) {
-                        const int64_t orr = ((int64_t)wb * rstride + row) * a.Hq + hd;
-                        reinterpret_cast<uint4 *>(obase + orr * D + c * 32)[q] = v;
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                pk[4 * q + 3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            st_global_v8(orow_p + c * 32 + q * 16, pk + 8 * q);
                     }
                 }
-                __syncwarp();
             }
             if (trc) tr[TR_E_STORE] += clock64() - te;
             if (qvalid && a.pair_count && hd == 0)

@@ -89,10 +89,11 @@ struct AttnLaunch {
     int32_t *pair_count;
 };
 // O = log-sum-exp merge of the window partial and the topk group partials.
+// status: the device status word (bounded waits of the bulk-copy path).
 cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __half *part16,
                          const float2 *part_meta, const int32_t *inv, int B, int n, int topk,
-                         int Hq, int d, __nv_bfloat16 *O, float *lse, cudaStream_t s,
-                         int *launches);
+                         int Hq, int d, __nv_bfloat16 *O, float *lse, int *status,
+                         cudaStream_t s, int *launches);
 cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
 // Shared memory the group and window kernels need for (d, K, topk).
 size_t attn_smem_needed(int d, int K, int topk);

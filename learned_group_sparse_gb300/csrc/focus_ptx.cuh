@@ -204,6 +204,18 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from shared to global memory, tracked
 // in this thread's bulk async-group.
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
@@ -381,6 +393,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
+                 : "memory");
+}
+
+// 32-byte global store of v[0..7] (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7])
                  : "memory");
 }
 

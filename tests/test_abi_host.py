@@ -101,12 +101,11 @@ def test_attention_validation(lib):
     assert call(K=2000, topk=2) == UNSUPPORTED
     # the shared-memory bound on K for d = 128 (documented per topk)
     # (supported shapes then stop at the workspace check: nothing launches)
-    assert call(d=128, K=520, topk=1, nbytes=1) == WORKSPACE
-    assert call(d=128, K=521, topk=1, nbytes=1) == UNSUPPORTED
-    assert call(d=128, K=488, topk=2, nbytes=1) == WORKSPACE
-    assert call(d=128, K=489, topk=2, nbytes=1) == UNSUPPORTED
-    assert call(d=128, K=296, topk=8, nbytes=1) == WORKSPACE
-    assert call(d=128, K=297, topk=8, nbytes=1) == UNSUPPORTED
+    assert call(d=128, K=1024, topk=1, nbytes=1) == WORKSPACE
+    assert call(d=128, K=1000, topk=2, nbytes=1) == WORKSPACE
+    assert call(d=128, K=1001, topk=2, nbytes=1) == UNSUPPORTED
+    assert call(d=128, K=808, topk=8, nbytes=1) == WORKSPACE
+    assert call(d=128, K=809, topk=8, nbytes=1) == UNSUPPORTED
     assert call(d=64, K=1024, topk=8, nbytes=1) == WORKSPACE
     assert call(nbytes=need - 1) == WORKSPACE
     assert call(ws=None) == INVALID
