@@ -3,8 +3,8 @@
 
 One step = focus_prefill on device-resident inputs: centroid scoring and
 top-k (focus_assign), group bucketing (focus_bucket) and Focus attention
-(focus_attention_fwd: plan, gather into group order, group-causal kernel,
-window kernel, log-sum-exp merge).
+(focus_attention_fwd: plan, gather into group order, key-tile group
+bitmaps, group-causal kernel, window kernel, log-sum-exp merge).
 Prints ONE JSON line (rank 0).  Metric: prefill tokens/s; the line also
 carries effective TFLOP/s over the allowed pairs, the roofline of the
 dominant kernel, the speedup over the library's own dense causal kernel,
@@ -236,6 +236,11 @@ def kernel_work(w, share_pairs, total_pairs):
         "gather": (2.0 * B * nk * (Hq + 2 * Hkv) * d * 2, "byte", "hbm"),
         "bucket_count": (4.0 * B * nk, "byte", "hbm"),
         "bucket_scatter": (12.0 * B * nk, "byte", "hbm"),
+        # group ids read (group-order and token-order rows), one [K] uint4
+        # bitmap written per key tile of the group and window kernels
+        "mask_table": (4.0 * B * (nk + n) * k
+                       + 16.0 * w.K * B * ((nk + 127) // 128 + w.K + (n + 127) // 128),
+                       "byte", "hbm"),
     }
 
 
@@ -381,7 +386,7 @@ def main():
                 "traffic": traffic_lookup(dom, w.name, src_hash()),
                 "algorithmic_per_launch": work[0], "algorithmic_unit": work[1]}
     attn_ms = sum(prof.get(k, (0.0, 1))[0] for k in ("attn_group", "attn_window", "gather",
-                                                      "merge", "plan")) / prof_steps
+                                                      "mask_table", "merge", "plan")) / prof_steps
 
     # ---- the library's own dense causal kernel on the same Q/K/V
     dense = None

@@ -158,9 +158,8 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  * rounded to bf16 for the P.V product, partial outputs kept in fp16 with a
  * power-of-two scale per row (11-bit significand at any magnitude).
  * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= K <= 1024, 1 <= topk <= 8,
- *            B * K <= 4096, and the kernel's shared memory within 227 KB:
- *            for d = 128 that bounds K to 1000 (topk 2), 936 (topk 4) or
- *            808 (topk 8); topk 1 and d = 64 take any K <= 1024.
+ *            B * K <= 4096 (the kernels' shared memory holds two key
+ *            tiles' group bitmaps, 32 K bytes, next to the Q/K/V tiles).
  *            Otherwise FOCUS_ERR_UNSUPPORTED.
  */
 size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d,

@@ -101,7 +101,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnWs {
-    size_t qp, kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, total;
+    size_t qp, kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, mtab_g, mtab_w, total;
 };
 
 int64_t max_tiles(int B, int n, int K, int topk)
@@ -125,6 +125,8 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
     w.lwin = off;  off += align256((size_t)B * n * Hq * 8);
     w.tiles = off; off += align256((size_t)max_tiles(B, n, K, topk) * 8);
     w.ntiles = off; off += 256;
+    w.mtab_g = off; off += align256((size_t)B * mask_tiles_group(n, K, topk) * K * 16);
+    w.mtab_w = off; off += align256((size_t)B * mask_tiles_window(n) * K * 16);
     w.total = off;
     return w;
 }
@@ -216,7 +218,7 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if (st) return st;
     if (K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
     if (K > 1024 || topk > 8 || (int64_t)B * K > 4096) return FOCUS_ERR_UNSUPPORTED;
-    if (attn_smem_needed(d, K, topk) > kMaxSmemPerBlock) return FOCUS_ERR_UNSUPPORTED;
+    if (attn_smem_needed(d, K) > kMaxSmemPerBlock) return FOCUS_ERR_UNSUPPORTED;
     if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
     const AttnWs w = attn_ws(B, n, Hq, Hkv, d, K, topk);
     if (ws_bytes < w.total) return FOCUS_ERR_WORKSPACE;
@@ -240,6 +242,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     auto *Mwin = reinterpret_cast<float2 *>(base + w.lwin);
     auto *tiles = reinterpret_cast<int2 *>(base + w.tiles);
     auto *ntiles = reinterpret_cast<int *>(base + w.ntiles);
+    auto *mtab_g = reinterpret_cast<uint4 *>(base + w.mtab_g);
+    auto *mtab_w = reinterpret_cast<uint4 *>(base + w.mtab_w);
     const int64_t nk = (int64_t)n * topk;
 
     CUtensorMap mq, mk, mv, wq, wk, wv;
@@ -278,12 +282,17 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
                            static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hq,
                            Hkv, d, Qp, Kp, Vp, gidp, s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
+    if ((e = launch_mask_tables(offsets, gidp, ids, B, n, K, topk, mtab_g, mtab_w, s,
+                                launches)) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
 
     p.tmQ = &mq;
     p.tmK = &mk;
     p.tmV = &mv;
     p.rows = (int)nk;
     p.gids = gidp;
+    p.masks = mtab_g;
+    p.mask_tiles = mask_tiles_group(n, K, topk);
     p.grid = grid_group;
     p.part_out16 = Opart;
     p.part_meta_out = Mpart;
@@ -294,6 +303,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.tmV = &wv;
     p.rows = n;
     p.gids = ids;
+    p.masks = mtab_w;
+    p.mask_tiles = mask_tiles_window(n);
     p.grid = grid_win;
     p.win_out16 = Owin;
     p.win_meta_out = Mwin;

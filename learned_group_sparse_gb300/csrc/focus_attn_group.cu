@@ -8,12 +8,12 @@ cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches
     return launch_attn_mode<kGroup>(p, s, launches);
 }
 
-size_t attn_smem_needed(int d, int K, int topk)
+size_t attn_smem_needed(int d, int K)
 {
-    const uint32_t g = d == 64 ? attn_smem_bytes<64>(kGroup, K, topk)
-                               : attn_smem_bytes<128>(kGroup, K, topk);
-    const uint32_t w = d == 64 ? attn_smem_bytes<64>(kWindow, K, topk)
-                               : attn_smem_bytes<128>(kWindow, K, topk);
+    const uint32_t g = d == 64 ? attn_smem_bytes<64>(kGroup, K)
+                               : attn_smem_bytes<128>(kGroup, K);
+    const uint32_t w = d == 64 ? attn_smem_bytes<64>(kWindow, K)
+                               : attn_smem_bytes<128>(kWindow, K);
     return g > w ? g : w;
 }
 

@@ -19,8 +19,8 @@
 // Roles (384 threads, three warpgroups):
 //   warps 0-3  softmax and epilogue of half 0 (thread r: query row r = TMEM lane r)
 //   warps 4-7  softmax and epilogue of half 1
-//   warp  8    TMA producer (Q of each half per item, K/V double-buffered) and
-//              the key-tile group bitmaps for the masks
+//   warp  8    producer: publishes each work item, loads Q of each half by TMA,
+//              streams K/V (double-buffered) and each key tile's group bitmaps
 //   warp  9    TMEM allocator and MMA issuer
 //   warps 10-11 idle
 // The third warpgroup hands registers to the softmax warpgroups (setmaxnreg),
@@ -48,8 +48,9 @@
 // {base-2 log-sum-exp, 2^e}.  The merge kernel combines them.  kDense writes
 // its final bf16 output directly.
 //
-// Group masks: for every key tile the producer builds colbits[g][4], the set
-// of the tile's 128 key columns whose token belongs to group g.  A query row
+// Group masks: for every key tile a bulk copy brings colbits[g][4], the set
+// of the tile's 128 key columns whose token belongs to group g, from a table
+// that the mask-table kernel writes before the attention kernels run.  A query row
 // excludes the columns in the union of colbits over the groups that must not
 // be shared (all its groups for kWindow; its groups below the tile's group
 // for kGroup): k lookups of 16 bytes instead of a test per column.
@@ -79,6 +80,10 @@ struct AttnArgs {
     const int32_t *pos;    // [B, n*topk] token of each group-order row
     const int2 *tiles;     // kGroup work list: (b*K + g, tile or tile-pair index in group)
     const int *ntiles;     // kGroup: number of valid entries in tiles
+    const uint4 *masks;    // group bitmaps of the key tiles: [B][mask_tiles][K],
+                           // word j bit c = key 32 j + c of the tile is in the group
+    int64_t mask_tiles;    // slots per batch (group tile u of g: off[g] / 128 + g + u;
+                           // window tile: first key row / 128)
     __nv_bfloat16 *out;    // kDense: O [B, n, Hq, D]
     float *lse;            // kDense: lse [B, Hq, n], natural log (nullable)
     // partial results: O / l as fp16 scaled by 2^-e, and {lse base 2, 2^e}
@@ -137,19 +142,16 @@ struct AttnSmem {
     static constexpr uint32_t kMisc = kBar + kNumBars * 8;   // tmem slot, abort flag
     static constexpr uint32_t kTrace = kMisc + 16;           // int64 [32] trace counters
     static constexpr uint32_t kColbits = (kTrace + 256 + 127) / 128 * 128;   // uint32 [2][K][4]
-    // then the work-item ring: 2 slots of ring_slot_bytes()
+    // then the work-item ring: 2 slots of kRingSlot bytes
+    static constexpr uint32_t kRingSlot = 128;               // an Item (16 ints)
     __host__ __device__ static constexpr uint32_t colbits_bytes(int K)
     {
         return 2u * 16u * (uint32_t)K;
     }
-    __host__ __device__ static constexpr uint32_t ring_slot_bytes(int topk)
+    // dynamic shared memory of a launch (K groups; 0 for kDense)
+    __host__ __device__ static constexpr uint32_t bytes(int K)
     {
-        return (64u + 2u * 128u * 2u * (uint32_t)topk + 127u) / 128u * 128u;
-    }
-    // dynamic shared memory of a launch (K groups and topk are 0 for kDense)
-    __host__ __device__ static constexpr uint32_t bytes(int K, int topk)
-    {
-        return kColbits + colbits_bytes(K) + 2u * ring_slot_bytes(topk) + 1024u;
+        return kColbits + colbits_bytes(K) + 2u * kRingSlot + 1024u;
     }
 };
 
@@ -161,22 +163,12 @@ struct Item {
     int hd[2], q0[2], qend[2], ulo[2], uhi[2];
 };
 
-// Work-item ring slot: the item (16 ints) followed by the group ids of the
-// 2 x 128 query rows, [2][128][topk] int16 (-1: none).
-struct RingSlot {
-    int *item;
-    int16_t *gid;
-};
-
+// Work-item ring slot: the fields of one Item as put_item lays them out.
 template <int D>
-__device__ __forceinline__ RingSlot ring_slot(uint8_t *sm, int K, int topk, int slot)
+__device__ __forceinline__ int *ring_slot(uint8_t *sm, int K, int slot)
 {
     using L = AttnSmem<D>;
-    uint8_t *base = sm + L::kColbits + L::colbits_bytes(K) + slot * L::ring_slot_bytes(topk);
-    RingSlot r;
-    r.item = reinterpret_cast<int *>(base);
-    r.gid = reinterpret_cast<int16_t *>(base + 64);
-    return r;
+    return reinterpret_cast<int *>(sm + L::kColbits + L::colbits_bytes(K) + slot * L::kRingSlot);
 }
 
 __device__ __forceinline__ void put_item(int *p, const Item &w)
@@ -309,7 +301,9 @@ __device__ __forceinline__ Item decode_item(const AttnArgs &a, int item)
         w.qend[h] = min(w.q0[h] + kBM, end);
         if (w.qend[h] < w.q0[h]) w.qend[h] = w.q0[h];
         if (MODE == kWindow) {
-            lo[h] = max(0, w.q0[h] - a.window + 1);
+            // key tiles on multiples of 128 rows (the same tile count as
+            // starting at the band's first key), so that each has a mask slot
+            lo[h] = max(0, w.q0[h] - a.window + 1) / kBN * kBN;
             hi[h] = a.window > 0 ? w.qend[h] : lo[h];
         } else {
             lo[h] = base;
@@ -381,7 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kMisc + 4);
     uint32_t *colbits = reinterpret_cast<uint32_t *>(sm + L::kColbits);   // [2][K][4]
-    const int rtopk = (MODE == kDense) ? 0 : a.topk;    // per-row ring data width
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -397,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_SFULL + s], 1);
             mbar_init(&bars[B_PFULL + s], 4);            // one lane per warp of the half
             mbar_init(&bars[B_ODONE + s], 1);
-            mbar_init(&bars[B_META + s], 32);            // the producer warp's lanes
+            mbar_init(&bars[B_META + s], 1);             // + the mask copy's bytes
             mbar_init(&bars[B_IFULL + s], 32);
             mbar_init(&bars[B_IEMPTY + s], 9);           // 8 softmax warps + MMA thread
         }
@@ -447,39 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long t_ring = trc ? clock64() : 0;
                 const Item w = decode_item<MODE>(a, item);
                 {
-                    const RingSlot rs = ring_slot<D>(sm, a.K, rtopk, k & 1);
-                    if (lane == 0) put_item(rs.item, w);
-                    if (MODE != kDense) {
-                        // (halves over the same rows share the first copy)
-                        const int nh = (w.q0[1] == w.q0[0]) ? 1 : 2;
-                        const int n = kBM * a.topk;
-#pragma unroll 1
-                        for (int h = 0; h < nh; ++h) {
-                            const int q0h = h ? w.q0[1] : w.q0[0], qeh = h ? w.qend[1] : w.qend[0];
-                            const int32_t *src = a.gids + ((int64_t)w.b * a.rows + q0h) * a.topk;
-                            const int nval = (qeh - q0h) * a.topk;
-                            int16_t *dst = rs.gid + h * n;
-#pragma unroll 1
-                            for (int i0 = lane; i0 < n; i0 += 128) {
-                                int v[4];   // four loads in flight per lane
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const int i = i0 + 32 * j;
-                                    v[j] = i < nval ? src[i] : -1;
-                                }
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    if (i0 + 32 * j < n) dst[i0 + 32 * j] = (int16_t)v[j];
-                            }
-                        }
-                    }
+                    if (lane == 0) put_item(ring_slot<D>(sm, a.K, k & 1), w);
                     __syncwarp();
                     mbar_arrive(&bars[B_IFULL + (k & 1)]);
                     if (trc) tr[TR_P_RING] += clock64() - t_ring;
                 }
                 if (w.nkv == 0) continue;
                 const int kvh = w.hd[0] / kv_per_q;
-                const int kv_end = (MODE == kGroup) ? w.gend : a.n;
                 // Q_h: its buffer is free once the last Q_h.K^T of its previous item is done
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -500,22 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++iq[h];
                 }
                 if (!ok) break;
+                // mask slot of tile 0 (see AttnArgs::masks)
+                const int64_t mslot =
+                    (int64_t)w.b * a.mask_tiles + w.kv_lo / kBN + (MODE == kGroup ? w.g : 0);
                 for (int u = 0; u < w.nkv; ++u, ++T) {
                     const int st = T & 1;
                     const int r0 = w.kv_lo + kBN * u;
-                    // Group ids of this tile's key rows (lane: rows lane + 32 j),
-                    // loaded now so that the waits below hide their latency.
-                    int kg[4][kMaxTopk];
-                    if (MODE != kDense) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int row = r0 + lane + 32 * j;
-                            const int32_t *gp = a.gids + ((int64_t)w.b * a.rows + row) * a.topk;
-#pragma unroll
-                            for (int s = 0; s < kMaxTopk; ++s)
-                                kg[j][s] = (row < kv_end && s < a.topk) ? gp[s] : -1;
-                        }
-                    }
                     if (T >= 2 && lane == 0)
                         ok = mbar_wait_t(&bars[B_KEMPTY + st], ((T >> 1) - 1) & 1, abort_flag,
                                          a.status, trc, tr[TR_P_KEMPTY]);
@@ -544,21 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
                                         c * 64, kvh, r0, w.b);
                     }
-                    if (MODE != kDense) {
-                        // colbits[st][g][q] bit c: key column 32q + c belongs to group g
-                        uint32_t *cb = colbits + (size_t)st * a.K * 4;
-                        for (int i = lane; i < a.K * 4; i += 32) cb[i] = 0u;
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                            for (int s = 0; s < kMaxTopk; ++s) {
-                                const int gi = kg[j][s];
-                                if ((unsigned)gi < (unsigned)a.K)
-                                    atomicOr(&cb[gi * 4 + j], 1u << lane);
-                            }
-                        }
-                        mbar_arrive(&bars[B_META + st]);
+                    if (MODE != kDense && lane == 0) {
+                        // colbits[st] <- the tile's group bitmaps
+                        mbar_arrive_expect_tx(&bars[B_META + st], 16u * (uint32_t)a.K);
+                        bulk_load(colbits + (size_t)st * a.K * 4, a.masks + (mslot + u) * a.K,
+                                  16u * (uint32_t)a.K, &bars[B_META + st]);
                     }
                     __syncwarp();
                 }
@@ -582,6 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     while (!mbar_try_wait(&bars[B_VFULL + st], (t >> 1) & 1) &&
                            global_timer_ns() - t0 < 300000000ull) {
+                    }
+                    while (MODE != kDense && !mbar_try_wait(&bars[B_META + st], (t >> 1) & 1) &&
+                           global_timer_ns() - t0 < 400000000ull) {
                     }
                 }
             }
@@ -611,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait_t(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status,
                                      trc, c_if);
                     if (!ok) break;
-                    const int *wi = ring_slot<D>(sm, a.K, rtopk, k & 1).item;   // Item fields
+                    const int *wi = ring_slot<D>(sm, a.K, k & 1);   // Item fields
                     const int nkv = wi[4];
                     const int ulo[2] = {wi[11], wi[12]}, uhi[2] = {wi[13], wi[14]};
                     mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
@@ -727,12 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
                              tr[TR_S_IFULL]);
             if (!ok) break;
-            const RingSlot rs = ring_slot<D>(sm, a.K, rtopk, slot);
-            const int *wi = rs.item;     // the fields of Item, as put_item lays them out
+            const int *wi = ring_slot<D>(sm, a.K, slot);   // the fields of Item
             const int wb = wi[0], wg = wi[1], kv_lo = wi[3], nkv = wi[4];
             const int hd = wi[5 + hh], q0 = wi[7 + hh], qend = wi[9 + hh];
             const int ulo = wi[11 + hh], uhi = wi[13 + hh];
-            const int gh = (q0 == wi[7]) ? 0 : 1;     // ring copy of this half's group ids
             const int prow = q0 + r;                     // row in the Q tensor
             const bool qvalid = prow < qend;
             int qi = prow;                               // token index of the row
@@ -743,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kMaxTopk; ++s) {
                 qg[s] = -1;
                 if (MODE != kDense && qvalid && s < a.topk) {
-                    const int gi = rs.gid[(gh * kBM + r) * a.topk + s];
+                    const int gi = a.gids[((int64_t)wb * a.rows + prow) * a.topk + s];
                     if ((MODE == kWindow || gi < wg) && (unsigned)gi < (unsigned)a.K)
                         qg[s] = gi;
                 }
@@ -761,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_t(&bars[B_SFULL + hh], ns & 1, abort_flag, a.status, trc,
                                  tr[TR_S_SFULL]);
                 ++ns;
-                // (S_h of tile t complete means the producer passed the masks of
-                // tile t-2, so the phase below is at most one ahead)
+                // (S_h of tile t complete means that a softmax finished tile
+                // t-2: the MMA thread issues both P.V of t-2 before either
+                // Q.K^T of t.  So the masks of t-2 have landed and the phase
+                // below is at most one ahead.)
                 if (ok && MODE != kDense)
                     ok = mbar_wait_t(&bars[B_META + st], (t >> 1) & 1, abort_flag, a.status,
                                      trc, tr[TR_S_META]);

@@ -7,9 +7,9 @@
 namespace focus {
 
 template <int D>
-uint32_t attn_smem_bytes(int mode, int K, int topk)
+uint32_t attn_smem_bytes(int mode, int K)
 {
-    return mode == kDense ? AttnSmem<D>::bytes(0, 0) : AttnSmem<D>::bytes(K, topk);
+    return mode == kDense ? AttnSmem<D>::bytes(0) : AttnSmem<D>::bytes(K);
 }
 
 template <int MODE, int D>
@@ -17,7 +17,7 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
 {
     if (p.grid <= 0) return cudaSuccess;
     auto kern = focus_attn_kernel<MODE, D>;
-    const uint32_t smem = attn_smem_bytes<D>(MODE, p.K, p.topk);
+    const uint32_t smem = attn_smem_bytes<D>(MODE, p.K);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // The warpgroups' register shares after setmaxnreg must fit in what the
@@ -42,6 +42,8 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.pos = p.pos;
     a.tiles = p.tiles;
     a.ntiles = p.ntiles;
+    a.masks = p.masks;
+    a.mask_tiles = p.mask_tiles;
     a.out = p.out;
     a.lse = p.lse;
     a.part_out16 = p.part_out16;

@@ -63,6 +63,16 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                           int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
                           __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
                           int *launches);
+// Group bitmaps of every key tile of the group kernel (tab_g, mask_tiles_group
+// slots per batch) and of the window kernel (tab_w, mask_tiles_window slots per
+// batch): [slot][K] uint4, word j bit c = key row 32 j + c of the tile is in
+// the group.  Group tile u of group g is slot floor(off[g] / 128) + g + u;
+// window tile t (rows [128 t, 128 t + 128)) is slot t.
+int64_t mask_tiles_group(int n, int K, int topk);
+int64_t mask_tiles_window(int n);
+cudaError_t launch_mask_tables(const int32_t *offsets, const int32_t *gidp, const int32_t *ids,
+                               int B, int n, int K, int topk, uint4 *tab_g, uint4 *tab_w,
+                               cudaStream_t s, int *launches);
 cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
                                const int32_t *inv, int B, int n, int K, int topk, int window,
                                int64_t *per_query, int64_t *totals, cudaStream_t s,
@@ -80,6 +90,8 @@ struct AttnLaunch {
     const int32_t *gids, *offsets, *pos;
     const int2 *tiles;
     const int *ntiles;
+    const uint4 *masks;      // key-tile group bitmaps of this launch's mode
+    int64_t mask_tiles;      // mask slots per batch
     int64_t grid;
     __nv_bfloat16 *out;
     float *lse;
@@ -95,8 +107,8 @@ cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __ha
                          int Hq, int d, __nv_bfloat16 *O, float *lse, int *status,
                          cudaStream_t s, int *launches);
 cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
-// Shared memory the group and window kernels need for (d, K, topk).
-size_t attn_smem_needed(int d, int K, int topk);
+// Shared memory the group and window kernels need for (d, K).
+size_t attn_smem_needed(int d, int K);
 constexpr size_t kMaxSmemPerBlock = 232448;   // 227 KB opt-in limit of sm_103a
 cudaError_t launch_attn_window(const AttnLaunch &p, cudaStream_t s, int *launches);
 cudaError_t launch_attn_dense(const AttnLaunch &p, cudaStream_t s, int *launches);

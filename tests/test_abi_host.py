@@ -99,14 +99,13 @@ def test_attention_validation(lib):
     assert call(d=96) == UNSUPPORTED
     assert call(topk=17) == INVALID                      # topk > K
     assert call(K=2000, topk=2) == UNSUPPORTED
-    # the shared-memory bound on K for d = 128 (documented per topk)
-    # (supported shapes then stop at the workspace check: nothing launches)
+    # every documented shape fits the kernels' shared memory, up to K = 1024
+    # and topk = 8 at d = 128 (supported shapes then stop at the workspace
+    # check: nothing launches)
     assert call(d=128, K=1024, topk=1, nbytes=1) == WORKSPACE
-    assert call(d=128, K=1000, topk=2, nbytes=1) == WORKSPACE
-    assert call(d=128, K=1001, topk=2, nbytes=1) == UNSUPPORTED
-    assert call(d=128, K=808, topk=8, nbytes=1) == WORKSPACE
-    assert call(d=128, K=809, topk=8, nbytes=1) == UNSUPPORTED
+    assert call(d=128, K=1024, topk=8, nbytes=1) == WORKSPACE
     assert call(d=64, K=1024, topk=8, nbytes=1) == WORKSPACE
+    assert call(d=128, K=1025, topk=8, nbytes=1) == UNSUPPORTED
     assert call(nbytes=need - 1) == WORKSPACE
     assert call(ws=None) == INVALID
     assert call(n=0) == INVALID
