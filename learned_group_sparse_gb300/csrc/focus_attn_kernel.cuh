@@ -706,30 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = ulo; u < uhi; ++u) {
                 const int t = T + u, st = t & 1;
                 const int kvb = kv_lo + kBN * u;         // first key row of the tile
-                ok = mbar_wait_t(&bars[B_SFULL + hh], ns & 1, abort_flag, a.status, trc,
-                                 tr[TR_S_SFULL]);
-                ++ns;
-                // (S_h of tile t complete means that a softmax finished tile
-                // t-2: the MMA thread issues both P.V of t-2 before either
-                // Q.K^T of t.  So the masks of t-2 have landed and the phase
-                // below is at most one ahead.)
-                if (ok && MODE != kDense)
-                    ok = mbar_wait_t(&bars[B_META + st], (t >> 1) & 1, abort_flag, a.status,
-                                     trc, tr[TR_S_META]);
-                if (!ok) break;
-                tc_fence_after();
-                long long tt = trc ? clock64() : 0;
-                float s[128];
-                tmem_ld128(s_col, s);
-                if (trc) {
-                    const long long t2 = clock64();
-                    tr[TR_T_SLOAD] += t2 - tt;
-                    tt = t2;
-                }
-
-                // ---- which of the tile's 128 keys the row may score
+                // ---- the keys of the tile that share an excluded group with the
+                // row: the union of the masks of the row's excluded groups
                 uint32_t ex[4] = {0u, 0u, 0u, 0u};
-                if (MODE != kDense) {
+                auto fetch_ex = [&]() -> bool {
+                    if (!mbar_wait_t(&bars[B_META + st], (t >> 1) & 1, abort_flag, a.status, trc,
+                                     tr[TR_S_META]))
+                        return false;
                     const uint4 *cb =
                         reinterpret_cast<const uint4 *>(colbits + (size_t)st * a.K * 4);
 #pragma unroll
@@ -742,7 +725,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ex[3] |= v.w;
                         }
                     }
+                    return true;
+                };
+                // Once this half has scored tiles t-2 and t-1 of the item, the
+                // masks of t-2 have landed (it waited for them), so the phase of
+                // t is at most one ahead: fetch the masks before S_h, their
+                // latency hidden behind the wait.  For the first two tiles S_h of
+                // tile t gives that order instead: the MMA thread issues both
+                // P.V of t-2 before either Q.K^T of t, so a softmax has finished
+                // t-2 by the time S_h(t) is complete.
+                const bool early = MODE != kDense && u >= ulo + 2;
+                ok = !early || fetch_ex();
+                if (ok)
+                    ok = mbar_wait_t(&bars[B_SFULL + hh], ns & 1, abort_flag, a.status, trc,
+                                     tr[TR_S_SFULL]);
+                ++ns;
+                if (ok && MODE != kDense && !early) ok = fetch_ex();
+                if (!ok) break;
+                tc_fence_after();
+                long long tt = trc ? clock64() : 0;
+                float s[128];
+                tmem_ld128(s_col, s);
+                if (trc) {
+                    const long long t2 = clock64();
+                    tr[TR_T_SLOAD] += t2 - tt;
+                    tt = t2;
                 }
+
                 uint32_t okb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
