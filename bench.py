@@ -233,7 +233,9 @@ def kernel_work(w, share_pairs, total_pairs):
         "attn_window": (4.0 * d * Hq * (total_pairs - share_pairs), "flop", "tensor"),
         "attn_dense": (4.0 * d * Hq * B * n * (n + 1) / 2, "flop", "tensor"),
         "assign": (2.0 * B * n * w.hidden + 4.0 * B * n * k, "byte", "hbm"),
-        "gather": (2.0 * B * nk * (Hq + 2 * Hkv) * d * 2, "byte", "hbm"),
+        # K and V rows into group order (read + write); the group kernel
+        # copies its Q rows from Q itself
+        "gather": (2.0 * B * nk * (2 * Hkv) * d * 2, "byte", "hbm"),
         "bucket_count": (4.0 * B * nk, "byte", "hbm"),
         "bucket_scatter": (12.0 * B * nk, "byte", "hbm"),
         # group ids read (group-order and token-order rows), one [K] uint4

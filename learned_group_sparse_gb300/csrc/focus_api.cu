@@ -101,7 +101,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnWs {
-    size_t qp, kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, mtab_g, mtab_w, total;
+    size_t kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, mtab_g, mtab_w, total;
 };
 
 int64_t max_tiles(int B, int n, int K, int topk)
@@ -115,7 +115,6 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
     const size_t nk = (size_t)n * topk;
     AttnWs w;
     size_t off = 0;
-    w.qp = off;    off += align256((size_t)B * nk * Hq * d * 2);
     w.kp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
     w.vp = off;    off += align256((size_t)B * nk * Hkv * d * 2);
     w.gidp = off;  off += align256((size_t)B * nk * topk * 4);
@@ -232,7 +231,6 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return FOCUS_ERR_CUDA;
     uint8_t *base = static_cast<uint8_t *>(ws);
-    auto *Qp = reinterpret_cast<__nv_bfloat16 *>(base + w.qp);
     auto *Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
     auto *Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
     auto *gidp = reinterpret_cast<int32_t *>(base + w.gidp);
@@ -246,8 +244,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     auto *mtab_w = reinterpret_cast<uint4 *>(base + w.mtab_w);
     const int64_t nk = (int64_t)n * topk;
 
-    CUtensorMap mq, mk, mv, wq, wk, wv;
-    if (!make_map(&mq, Qp, B, nk, Hq, d) || !make_map(&mk, Kp, B, nk, Hkv, d) ||
+    CUtensorMap mk, mv, wq, wk, wv;
+    if (!make_map(&mk, Kp, B, nk, Hkv, d) ||
         !make_map(&mv, Vp, B, nk, Hkv, d) || !make_map(&wq, Q, B, n, Hq, d) ||
         !make_map(&wk, Kt, B, n, Hkv, d) || !make_map(&wv, V, B, n, Hkv, d))
         return FOCUS_ERR_CUDA;
@@ -280,13 +278,15 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Q),
                            static_cast<const __nv_bfloat16 *>(Kt),
                            static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hq,
-                           Hkv, d, Qp, Kp, Vp, gidp, s, launches)) != cudaSuccess)
+                           Hkv, d, nullptr, Kp, Vp, gidp, s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
     if ((e = launch_mask_tables(offsets, gidp, ids, B, n, K, topk, mtab_g, mtab_w, s,
                                 launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
 
-    p.tmQ = &mq;
+    // the group kernel copies its query rows from Q itself (tmQ unused)
+    p.tmQ = &wq;
+    p.q = static_cast<const __nv_bfloat16 *>(Q);
     p.tmK = &mk;
     p.tmV = &mv;
     p.rows = (int)nk;

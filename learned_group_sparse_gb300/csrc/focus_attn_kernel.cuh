@@ -22,7 +22,8 @@
 //   warp  8    producer: publishes each work item, loads Q of each half by TMA,
 //              streams K/V (double-buffered) and each key tile's group bitmaps
 //   warp  9    TMEM allocator and MMA issuer
-//   warps 10-11 idle
+//   warps 10-11 kGroup: copy the query rows of half 0 / 1 from the original Q
+//              (through pos); otherwise idle
 // The third warpgroup hands registers to the softmax warpgroups (setmaxnreg),
 // which keep a whole 128-column row of S in registers.
 // TMEM columns: S_0 [0,128), S_1 [128,256) (P_h over the first 64 columns of
@@ -80,6 +81,8 @@ struct AttnArgs {
     const int32_t *pos;    // [B, n*topk] token of each group-order row
     const int2 *tiles;     // kGroup work list: (b*K + g, tile or tile-pair index in group)
     const int *ntiles;     // kGroup: number of valid entries in tiles
+    const __nv_bfloat16 *q;  // kGroup: the original Q [B, n, Hq, D]; its rows are
+                             // copied into the query tiles through pos
     const uint4 *masks;    // group bitmaps of the key tiles: [B][mask_tiles][K],
                            // word j bit c = key 32 j + c of the tile is in the group
     int64_t mask_tiles;    // slots per batch (group tile u of g: off[g] / 128 + g + u;
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_QFULL + s], 1);
+            mbar_init(&bars[B_QFULL + s], MODE == kGroup ? 32 : 1);   // Q-loader lanes
             mbar_init(&bars[B_QEMPTY + s], 1);
             mbar_init(&bars[B_KFULL + s], 1);
             mbar_init(&bars[B_VFULL + s], 1);
@@ -392,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_ODONE + s], 1);
             mbar_init(&bars[B_META + s], 1);             // + the mask copy's bytes
             mbar_init(&bars[B_IFULL + s], 32);
-            mbar_init(&bars[B_IEMPTY + s], 9);           // 8 softmax warps + MMA thread
+            // 8 softmax warps + MMA thread (+ the two Q-loader warps of kGroup)
+            mbar_init(&bars[B_IEMPTY + s], MODE == kGroup ? 11 : 9);
         }
         long long *trz = reinterpret_cast<long long *>(sm + L::kTrace);
         for (int i = 0; i < kTraceSlots; ++i) trz[i] = 0;
@@ -447,10 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (w.nkv == 0) continue;
                 const int kvh = w.hd[0] / kv_per_q;
-                // Q_h: its buffer is free once the last Q_h.K^T of its previous item is done
+                // Q_h: its buffer is free once the last Q_h.K^T of its previous
+                // item is done.  (kGroup: the Q-loader warps copy the rows.)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (w.uhi[h] <= w.ulo[h]) continue;
+                    if (MODE == kGroup || w.uhi[h] <= w.ulo[h]) continue;
                     if (iq[h] >= 1 && lane == 0)
                         ok = mbar_wait_t(&bars[B_QEMPTY + h], (iq[h] - 1) & 1, abort_flag, a.status,
                                          trc, tr[TR_P_QEMPTY]);
@@ -656,6 +661,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
+        } else if (MODE == kGroup) {
+            // --------------------------- Q loaders: warp 10 + h fills Q_h
+            // The group's query rows are gathered from the original Q through
+            // pos with 16-byte asynchronous copies (lane: rows lane + 32 i),
+            // laid out as the 128-byte-swizzled K-major tile that a TMA load
+            // would write: 16-byte unit u of row r at (u / 8) * 16 KB + 128 r
+            // + 16 ((u mod 8) xor (r mod 8)).
+            const int h = warp - 10;
+            int iq = 0;    // query tiles loaded
+            bool ok = true;
+            for (int k = 0, item = blockIdx.x; ok && item < nitems;
+                 item = item_of(++k, blockIdx.x, gridDim.x)) {
+                if (lane == 0)
+                    ok = mbar_wait(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                const int *wi = ring_slot<D>(sm, a.K, k & 1);   // Item fields
+                const int wb = wi[0], nkv = wi[4], hd = wi[5 + h], q0 = wi[7 + h];
+                const int qend = wi[9 + h], ulo = wi[11 + h], uhi = wi[13 + h];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
+                if (nkv == 0 || uhi <= ulo) continue;
+                int tok[4];    // token of row lane + 32 i, -1 past the group
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = q0 + lane + 32 * i;
+                    tok[i] = row < qend ? a.pos[(int64_t)wb * a.rows + row] : -1;
+                }
+                if (iq >= 1 && lane == 0)
+                    ok = mbar_wait(&bars[B_QEMPTY + h], (iq - 1) & 1, abort_flag, a.status);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *dq = sQ + h * L::kTile;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i;
+                    const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                        a.q + (((int64_t)wb * a.n + max(tok[i], 0)) * a.Hq + hd) * D);
+                    const uint32_t nb = tok[i] >= 0 ? 16u : 0u;
+#pragma unroll
+                    for (int u = 0; u < D / 8; ++u)
+                        cp_async16(dq + (u >> 3) * 16384 + r * 128 + (((u & 7) ^ (r & 7)) << 4),
+                                   src + u * 16, nb);
+                }
+                cp_async_wait_all();
+                fence_proxy_async_smem();     // the MMAs read Q_h through the async proxy
+                mbar_arrive(&bars[B_QFULL + h]);
+                ++iq;
+            }
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));

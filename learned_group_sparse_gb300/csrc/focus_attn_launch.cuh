@@ -42,6 +42,7 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.pos = p.pos;
     a.tiles = p.tiles;
     a.ntiles = p.ntiles;
+    a.q = p.q;
     a.masks = p.masks;
     a.mask_tiles = p.mask_tiles;
     a.out = p.out;

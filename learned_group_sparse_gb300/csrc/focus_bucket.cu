@@ -294,9 +294,11 @@ __global__ void __launch_bounds__(256) gather_kernel(
         const int64_t b = row / nk;
         const int64_t src = b * n + pos[row];
         if (lane < topk) gidp[row * topk + lane] = ids[src * topk + lane];
-        const uint4 *q = Q + src * qunits;
-        uint4 *qd = Qp + row * qunits;
-        for (int u = lane; u < qunits; u += 32) qd[u] = q[u];
+        if (Qp) {
+            const uint4 *q = Q + src * qunits;
+            uint4 *qd = Qp + row * qunits;
+            for (int u = lane; u < qunits; u += 32) qd[u] = q[u];
+        }
         const uint4 *k = K + src * kvunits;
         const uint4 *v = V + src * kvunits;
         uint4 *kd = Kp + row * kvunits;

@@ -56,8 +56,8 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
 // pairs of consecutive tiles (2t, 2t+1).
 cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, int2 *tiles,
                         int *ntiles, cudaStream_t s, int *launches);
-// Qp[b][r] = Q[b][pos[b][r]] (and K, V): rows of H*d bf16; gidp[b][r] = the
-// group ids of token pos[b][r].
+// Kp[b][r] = K[b][pos[b][r]] (and V, and Q when Qp is not null): rows of
+// H*d bf16; gidp[b][r] = the group ids of token pos[b][r].
 cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
                           const __nv_bfloat16 *V, const int32_t *pos, const int32_t *ids,
                           int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
@@ -90,6 +90,7 @@ struct AttnLaunch {
     const int32_t *gids, *offsets, *pos;
     const int2 *tiles;
     const int *ntiles;
+    const __nv_bfloat16 *q;  // kGroup: the original Q, whose rows the kernel gathers
     const uint4 *masks;      // key-tile group bitmaps of this launch's mode
     int64_t mask_tiles;      // mask slots per batch
     int64_t grid;

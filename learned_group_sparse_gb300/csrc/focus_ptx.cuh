@@ -309,6 +309,21 @@ __device__ __forceinline__ void tc_mma_bf16_ts_lo(uint32_t d_tmem, uint32_t a_tm
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L1; src_bytes < 16
+// zero-fills the rest (src_bytes = 0: sixteen zero bytes, nothing read).
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(sdst)),
+                 "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+
+// Waits for all of this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Loads 32 consecutive fp32 columns of this thread's TMEM lane and waits.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 {
