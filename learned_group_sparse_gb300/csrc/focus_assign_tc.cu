@@ -36,8 +36,9 @@ __device__ __forceinline__ bool better(float s1, int i1, float s2, int i2)
 }
 
 // M^T split: mhi[c][h], mlo[c][h] for c < Kp (rows >= K are zero).  Block:
-// 32 centroids x 32 hidden rows, both operands staged in shared memory; each
-// thread accumulates 4 hidden rows of one centroid.
+// 32 centroids x 32 hidden rows, both operands staged in shared memory; lane
+// l takes hidden row h0 + l and warp w centroids c0 + w + 8 j, so that a
+// warp's stores cover 32 consecutive hidden entries of one centroid row.
 __global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restrict__ Wg,
                                                           const float *__restrict__ C,
                                                           int hidden, int dg, int K, int Kp,
@@ -54,17 +55,17 @@ __global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restric
         wsm[r * (dg + 1) + e] = (h0 + r < hidden) ? Wg[(int64_t)(h0 + r) * dg + e] : 0.f;
     }
     __syncthreads();
-    const int tc = threadIdx.x & 31, th = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int e = 0; e < dg; ++e) {
-        const float cv = csm[e * 32 + tc];
+        const float wv = wsm[lane * (dg + 1) + e];   // (dg + 1): no bank conflicts
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j] = fmaf(wsm[(th + 8 * j) * (dg + 1) + e], cv, acc[j]);
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(wv, csm[e * 32 + w + 8 * j], acc[j]);
     }
-    const int c = c0 + tc;
+    const int h = h0 + lane;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int h = h0 + th + 8 * j;
+        const int c = c0 + w + 8 * j;
         if (c < Kp && h < hidden) {
             const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
             const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
