@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) assign_kernel(const __nv_bfloat16 *__rest
                                                      int32_t *__restrict__ ids,
                                                      float *__restrict__ margin)
 {
+    grid_dep_sync();
     extern __shared__ float4 smem4[];
     float *sm = reinterpret_cast<float *>(smem4);
     // layout (floats): z [kTM][dgp] | work area (max of phase A and phase B)
@@ -238,10 +239,10 @@ cudaError_t launch_assign_nj(const AssignLaunch &p, cudaStream_t s)
     const int64_t blocks = (p.ntok + kTM - 1) / kTM;
     if (blocks == 0) return cudaSuccess;
     prof_begin("assign", s);
-    assign_kernel<NJ><<<(unsigned)blocks, 256, smem, s>>>(p.X, p.Wg, p.C, p.ntok, p.hidden, p.dg,
-                                                          p.K, p.topk, p.ids, p.margin);
+    e = launch_pdl(assign_kernel<NJ>, dim3((unsigned)blocks), dim3(256), smem, s, p.X, p.Wg, p.C,
+                   p.ntok, p.hidden, p.dg, p.K, p.topk, p.ids, p.margin);
     prof_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restric
                                                           __nv_bfloat16 *__restrict__ mhi,
                                                           __nv_bfloat16 *__restrict__ mlo)
 {
+    grid_dep_sync();
     extern __shared__ float psm[];
     float *csm = psm;                  // [dg][32]: C rows c0..c0+31, transposed
     float *wsm = psm + 32 * dg;        // [32][dg + 1]: W_g rows h0..h0+31
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmM,
                                                            const TcArgs a)
 {
+    grid_dep_sync();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -258,8 +260,10 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         prof_begin("assign_prep", s);
-        assign_prep_kernel<<<grid, 256, smem, s>>>(p.Wg, p.C, p.hidden, p.dg, p.K, Kp, mhi, mlo);
+        e = launch_pdl(assign_prep_kernel, grid, dim3(256), smem, s, p.Wg, p.C, p.hidden, p.dg, p.K,
+                       Kp, mhi, mlo);
         prof_end(s);
+        if (e != cudaSuccess) return e;
         *launches += 1;
     }
     if (p.ntok == 0) return cudaGetLastError();
@@ -289,10 +293,10 @@ cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaS
     if (e != cudaSuccess) return e;
     const int64_t blocks = (p.ntok + kTokens - 1) / kTokens;
     prof_begin("assign", s);
-    assign_tc_kernel<<<(unsigned)blocks, 192, smem, s>>>(mx, mm, a);
+    e = launch_pdl(assign_tc_kernel, dim3((unsigned)blocks), dim3(192), smem, s, mx, mm, a);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace focus

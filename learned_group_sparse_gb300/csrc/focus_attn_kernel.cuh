@@ -63,6 +63,7 @@
 
 #include "focus_ptx.cuh"
 #include "focus_tmem_wide.cuh"
+#include "focus_internal.h"
 
 namespace focus {
 
@@ -417,6 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_o = tmem + 256;     // O_0; O_1 at tmem_o + kOStride
+    // (set-up above touches no global memory; launched with launch_pdl)
+    grid_dep_sync();
 
     long long *tr = reinterpret_cast<long long *>(sm + L::kTrace);   // zeroed at set-up
     const long long t_start = clock64();

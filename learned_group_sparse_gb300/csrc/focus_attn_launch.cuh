@@ -61,10 +61,10 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
         return e;
     const int64_t grid = p.grid < sms ? p.grid : sms;
     prof_begin(MODE == kGroup ? "attn_group" : MODE == kWindow ? "attn_window" : "attn_dense", s);
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(*p.tmQ, *p.tmK, *p.tmV, a);
+    e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, *p.tmQ, *p.tmK, *p.tmV, a);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 template <int MODE>

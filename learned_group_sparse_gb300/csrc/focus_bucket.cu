@@ -29,6 +29,7 @@ constexpr int kWarpSlice = kBucketChunk / kScatterWarps;   // 512 entries per wa
 __global__ void bucket_count(const int32_t *__restrict__ ids, int64_t nk, int K, int nchunks,
                              int32_t *__restrict__ counts)
 {
+    grid_dep_sync();
     extern __shared__ int hist[];
     const int chunk = blockIdx.x, b = blockIdx.y;
     for (int g = threadIdx.x; g < K; g += blockDim.x) hist[g] = 0;
@@ -48,6 +49,7 @@ __global__ void bucket_count(const int32_t *__restrict__ ids, int64_t nk, int K,
 __global__ void bucket_scan(int32_t *__restrict__ counts, int K, int nchunks,
                             int32_t *__restrict__ totals)
 {
+    grid_dep_sync();
     __shared__ int part[32][33];
     const int tx = threadIdx.x, ty = threadIdx.y, b = blockIdx.y;
     const int g = blockIdx.x * 32 + tx;
@@ -75,6 +77,7 @@ __global__ void bucket_scan(int32_t *__restrict__ counts, int K, int nchunks,
 __global__ void bucket_offsets(const int32_t *__restrict__ totals, int K,
                                int32_t *__restrict__ offsets)
 {
+    grid_dep_sync();
     __shared__ int warp_sum[32];
     const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int v = t < K ? totals[(int64_t)b * K + t] : 0;
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(256) bucket_scatter(const int32_t *__restrict_
                                                       int32_t *__restrict__ pos,
                                                       int32_t *__restrict__ inv)
 {
+    grid_dep_sync();
     extern __shared__ int hist[];   // [kScatterWarps][K]
     const int chunk = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
                                                     int2 *__restrict__ tiles,
                                                     int *__restrict__ ntiles)
 {
+    grid_dep_sync();
     __shared__ int keyT[kPlanMax];
     __shared__ int keyG[kPlanMax];
     __shared__ long long pref[kPlanMax + 1];
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(256) gather_kernel(
     int topk, int qunits, int kvunits, uint4 *__restrict__ Qp, uint4 *__restrict__ Kp,
     uint4 *__restrict__ Vp, int32_t *__restrict__ gidp)
 {
+    grid_dep_sync();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t total = (int64_t)B * nk;
@@ -328,6 +334,7 @@ __global__ void __launch_bounds__(128) mask_table_kernel(
     const int32_t *__restrict__ ids, int n, int64_t nk, int K, int topk, int64_t ntg,
     int64_t ntw, int64_t nblk_g, uint4 *__restrict__ tab_g, uint4 *__restrict__ tab_w)
 {
+    grid_dep_sync();
     extern __shared__ uint32_t bm[];   // [K][4]
     __shared__ int cnt;
     const int tid = threadIdx.x;
@@ -391,11 +398,12 @@ cudaError_t launch_mask_tables(const int32_t *offsets, const int32_t *gidp, cons
     const int64_t blocks = (int64_t)B * (ntg + ntw);
     if (n == 0 || blocks <= 0) return cudaSuccess;
     prof_begin("mask_table", s);
-    mask_table_kernel<<<(unsigned)blocks, 128, (size_t)K * 16, s>>>(
-        offsets, gidp, ids, n, nk, K, topk, ntg, ntw, (int64_t)B * ntg, tab_g, tab_w);
+    const cudaError_t e =
+        launch_pdl(mask_table_kernel, dim3((unsigned)blocks), dim3(128), (size_t)K * 16, s,
+                   offsets, gidp, ids, n, nk, K, topk, ntg, ntw, (int64_t)B * ntg, tab_g, tab_w);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 size_t bucket_ws_bytes(int B, int n, int K, int topk)
@@ -416,19 +424,24 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
     cudaError_t e;
     if (nchunks > 0) {
         prof_begin("bucket_count", s);
-        bucket_count<<<dim3(nchunks, B), 256, K * sizeof(int), s>>>(ids, nk, K, nchunks, counts);
+        e = launch_pdl(bucket_count, dim3(nchunks, B), dim3(256), K * sizeof(int), s, ids, nk, K,
+                       nchunks, counts);
         prof_end(s);
+        if (e != cudaSuccess) return e;
         prof_begin("bucket_scan", s);
-        bucket_scan<<<dim3((K + 31) / 32, B), dim3(32, 32), 0, s>>>(counts, K, nchunks, totals);
+        e = launch_pdl(bucket_scan, dim3((K + 31) / 32, B), dim3(32, 32), 0, s, counts, K, nchunks,
+                       totals);
         prof_end(s);
+        if (e != cudaSuccess) return e;
         *launches += 2;
     } else {
         e = cudaMemsetAsync(totals, 0, sizeof(int32_t) * (size_t)B * K, s);
         if (e != cudaSuccess) return e;
     }
     prof_begin("bucket_offsets", s);
-    bucket_offsets<<<B, 1024, 0, s>>>(totals, K, offsets);
+    e = launch_pdl(bucket_offsets, dim3(B), dim3(1024), 0, s, totals, K, offsets);
     prof_end(s);
+    if (e != cudaSuccess) return e;
     *launches += 1;
     if (nchunks > 0) {
         const size_t smem = sizeof(int) * (size_t)kScatterWarps * K;
@@ -436,9 +449,10 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
                                  (int)smem);
         if (e != cudaSuccess) return e;
         prof_begin("bucket_scatter", s);
-        bucket_scatter<<<dim3(nchunks, B), 256, smem, s>>>(ids, nk, K, topk, nchunks, counts,
-                                                          offsets, pos, inv);
+        e = launch_pdl(bucket_scatter, dim3(nchunks, B), dim3(256), smem, s, ids, nk, K, topk,
+                       nchunks, counts, offsets, pos, inv);
         prof_end(s);
+        if (e != cudaSuccess) return e;
         *launches += 1;
     }
     return cudaGetLastError();
@@ -448,10 +462,11 @@ cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, in
                         int *ntiles, cudaStream_t s, int *launches)
 {
     prof_begin("plan", s);
-    plan_kernel<<<1, 1024, 0, s>>>(offsets, B, K, pair_tiles, tiles, ntiles);
+    const cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, offsets, B, K,
+                                     pair_tiles, tiles, ntiles);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
@@ -466,14 +481,15 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
     int64_t blocks = (rows + 7) / 8;
     if (blocks > 152 * 32) blocks = 152 * 32;
     prof_begin("gather", s);
-    gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+    const cudaError_t e = launch_pdl(
+        gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
         reinterpret_cast<const uint4 *>(Q), reinterpret_cast<const uint4 *>(K),
         reinterpret_cast<const uint4 *>(V), pos, ids, B, n, nk, topk, Hq * d / 8, Hkv * d / 8,
         reinterpret_cast<uint4 *>(Qp), reinterpret_cast<uint4 *>(Kp), reinterpret_cast<uint4 *>(Vp),
         gidp);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace focus

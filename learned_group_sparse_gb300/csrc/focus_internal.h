@@ -10,6 +10,38 @@
 
 namespace focus {
 
+// Kernel launch with programmatic stream serialization: the grid may be
+// scheduled while the previous kernel on the stream drains.  Every kernel
+// launched this way calls grid_dep_sync() before its first global memory
+// access, so it sees all of that kernel's writes and completes after it,
+// which keeps the stream's order transitive.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+#ifdef __CUDACC__
+// Device side of launch_pdl: let the next grid be scheduled once every CTA of
+// this one has started, then wait until the previous grid has completed and
+// its memory operations are visible.
+__device__ __forceinline__ void grid_dep_sync()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+#endif
+
 // Per-kernel timing hooks (no-ops unless focus_profile_enable(1) was called
 // on this host thread).
 void prof_begin(const char *name, cudaStream_t s);

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) merge_kernel(
     const int32_t *__restrict__ inv, int n, int64_t nk, int topk, int Hq, int d,
     uint4 *__restrict__ O, float *__restrict__ lse)
 {
+    grid_dep_sync();
     extern __shared__ float wts[];   // [Hq][topk + 1]
     __shared__ int64_t rows[8];
     const int64_t tokrow = blockIdx.x;            // b * n + i
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
     const int32_t *__restrict__ inv, int n, int64_t nk, int64_t ntok, int topk, int Hq, int d,
     uint4 *__restrict__ O, float *__restrict__ lse, int *status)
 {
+    grid_dep_sync();
     extern __shared__ __align__(16) uint8_t msm[];
     __shared__ uint64_t bar[2];
     __shared__ int present[2][9];      // part p of the token in buffer b was copied
@@ -301,22 +303,24 @@ cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __ha
         int64_t blocks = (int64_t)sms * (per_sm < 1 ? 1 : per_sm);
         if (blocks > rows) blocks = rows;
         prof_begin("merge", s);
-        merge_bulk_kernel<<<(unsigned)blocks, 256, bulk_smem, s>>>(
-            reinterpret_cast<const uint4 *>(win16), win_meta,
-            reinterpret_cast<const uint4 *>(part16), part_meta, inv, n, (int64_t)n * topk, rows,
-            topk, Hq, d, reinterpret_cast<uint4 *>(O), lse, status);
+        e = launch_pdl(merge_bulk_kernel, dim3((unsigned)blocks), dim3(256), bulk_smem, s,
+                       reinterpret_cast<const uint4 *>(win16), win_meta,
+                       reinterpret_cast<const uint4 *>(part16), part_meta, inv, n,
+                       (int64_t)n * topk, rows, topk, Hq, d, reinterpret_cast<uint4 *>(O), lse,
+                       status);
         prof_end(s);
         *launches += 1;
-        return cudaGetLastError();
+        return e;
     }
     const size_t smem = sizeof(float) * (size_t)Hq * (topk + 1);
     prof_begin("merge", s);
-    merge_kernel<<<(unsigned)rows, 256, smem, s>>>(
+    const cudaError_t e = launch_pdl(
+        merge_kernel, dim3((unsigned)rows), dim3(256), smem, s,
         reinterpret_cast<const uint4 *>(win16), win_meta, reinterpret_cast<const uint4 *>(part16),
         part_meta, inv, n, (int64_t)n * topk, topk, Hq, d, reinterpret_cast<uint4 *>(O), lse);
     prof_end(s);
     *launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace focus
