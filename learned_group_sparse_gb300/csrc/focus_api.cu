@@ -275,10 +275,9 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if ((e = launch_plan(offsets, B, K, !p.pair_heads, tiles, ntiles, s, launches)) !=
         cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Q),
-                           static_cast<const __nv_bfloat16 *>(Kt),
-                           static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hq,
-                           Hkv, d, nullptr, Kp, Vp, gidp, s, launches)) != cudaSuccess)
+    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Kt),
+                           static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hkv, d,
+                           Kp, Vp, gidp, s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
     if ((e = launch_mask_tables(offsets, gidp, ids, B, n, K, topk, mtab_g, mtab_w, s,
                                 launches)) != cudaSuccess)

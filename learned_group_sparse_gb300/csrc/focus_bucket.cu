@@ -10,8 +10,10 @@
 //   4. bucket_scatter  per chunk, a stable scatter: each warp walks its slice
 //                      of the chunk in order and ranks equal ids inside a
 //                      32-entry step with __match_any_sync.
-// The plan kernel orders the group kernel's tiles by decreasing cost, and the
-// gather kernel copies Q/K/V rows into group order.
+// The plan kernel orders the group kernel's tiles by decreasing cost, the
+// gather kernel copies K/V rows into group order (the group kernel copies its
+// Q rows itself), and the mask-table kernel writes every key tile's group
+// bitmaps.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -286,10 +288,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 
 // ---------------------------------------------------------------- gather
 __global__ void __launch_bounds__(256) gather_kernel(
-    const uint4 *__restrict__ Q, const uint4 *__restrict__ K, const uint4 *__restrict__ V,
-    const int32_t *__restrict__ pos, const int32_t *__restrict__ ids, int B, int n, int64_t nk,
-    int topk, int qunits, int kvunits, uint4 *__restrict__ Qp, uint4 *__restrict__ Kp,
-    uint4 *__restrict__ Vp, int32_t *__restrict__ gidp)
+    const uint4 *__restrict__ K, const uint4 *__restrict__ V, const int32_t *__restrict__ pos,
+    const int32_t *__restrict__ ids, int B, int n, int64_t nk, int topk, int kvunits,
+    uint4 *__restrict__ Kp, uint4 *__restrict__ Vp, int32_t *__restrict__ gidp)
 {
     grid_dep_sync();
     const int lane = threadIdx.x & 31;
@@ -300,11 +301,6 @@ __global__ void __launch_bounds__(256) gather_kernel(
         const int64_t b = row / nk;
         const int64_t src = b * n + pos[row];
         if (lane < topk) gidp[row * topk + lane] = ids[src * topk + lane];
-        if (Qp) {
-            const uint4 *q = Q + src * qunits;
-            uint4 *qd = Qp + row * qunits;
-            for (int u = lane; u < qunits; u += 32) qd[u] = q[u];
-        }
         const uint4 *k = K + src * kvunits;
         const uint4 *v = V + src * kvunits;
         uint4 *kd = Kp + row * kvunits;
@@ -469,9 +465,8 @@ cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, in
     return e;
 }
 
-cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                          const __nv_bfloat16 *V, const int32_t *pos, const int32_t *ids,
-                          int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
+cudaError_t launch_gather(const __nv_bfloat16 *K, const __nv_bfloat16 *V, const int32_t *pos,
+                          const int32_t *ids, int B, int n, int topk, int Hkv, int d,
                           __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
                           int *launches)
 {
@@ -481,12 +476,11 @@ cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
     int64_t blocks = (rows + 7) / 8;
     if (blocks > 152 * 32) blocks = 152 * 32;
     prof_begin("gather", s);
-    const cudaError_t e = launch_pdl(
-        gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
-        reinterpret_cast<const uint4 *>(Q), reinterpret_cast<const uint4 *>(K),
-        reinterpret_cast<const uint4 *>(V), pos, ids, B, n, nk, topk, Hq * d / 8, Hkv * d / 8,
-        reinterpret_cast<uint4 *>(Qp), reinterpret_cast<uint4 *>(Kp), reinterpret_cast<uint4 *>(Vp),
-        gidp);
+    const cudaError_t e =
+        launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                   reinterpret_cast<const uint4 *>(K), reinterpret_cast<const uint4 *>(V), pos, ids,
+                   B, n, nk, topk, Hkv * d / 8, reinterpret_cast<uint4 *>(Kp),
+                   reinterpret_cast<uint4 *>(Vp), gidp);
     prof_end(s);
     *launches += 1;
     return e;

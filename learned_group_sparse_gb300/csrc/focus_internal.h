@@ -88,11 +88,10 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
 // pairs of consecutive tiles (2t, 2t+1).
 cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, int2 *tiles,
                         int *ntiles, cudaStream_t s, int *launches);
-// Kp[b][r] = K[b][pos[b][r]] (and V, and Q when Qp is not null): rows of
-// H*d bf16; gidp[b][r] = the group ids of token pos[b][r].
-cudaError_t launch_gather(const __nv_bfloat16 *Q, const __nv_bfloat16 *K,
-                          const __nv_bfloat16 *V, const int32_t *pos, const int32_t *ids,
-                          int B, int n, int topk, int Hq, int Hkv, int d, __nv_bfloat16 *Qp,
+// Kp[b][r] = K[b][pos[b][r]] and Vp likewise: rows of Hkv*d bf16;
+// gidp[b][r] = the group ids of token pos[b][r].
+cudaError_t launch_gather(const __nv_bfloat16 *K, const __nv_bfloat16 *V, const int32_t *pos,
+                          const int32_t *ids, int B, int n, int topk, int Hkv, int d,
                           __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
                           int *launches);
 // Group bitmaps of every key tile of the group kernel (tab_g, mask_tiles_group
