@@ -177,9 +177,12 @@ focus_status_t focus_attention_fwd(const void *Q, const void *K, const void *V,
  * focus_prefill -- the whole path in one call: focus_assign, focus_bucket and
  * focus_attention_fwd on one stream.  With io_on_host != 0, X, Wg, C, Q, K, V
  * are HOST pointers (page-locked for asynchronous copies), O and lse are host
- * pointers, and the copies in and out are enqueued on `stream` around the
- * kernels (the caller synchronises before reading O).  With io_on_host == 0
- * every pointer is a device pointer.  ids_out (nullable, device) receives the
+ * pointers, and the copies in and out are enqueued around the kernels (the
+ * caller synchronises `stream` before reading O).  The copies of K, V and Q
+ * run on a second stream that the library creates once per device, after the
+ * copy of X and beside the assignment; `stream` waits for them before the
+ * attention, and they start only after the work already on `stream`.  With
+ * io_on_host == 0 every pointer is a device pointer.  ids_out (nullable, device) receives the
  * group ids.  Workspace: focus_prefill_workspace_size(...) device bytes.
  */
 size_t focus_prefill_workspace_size(int B, int n, int hidden, int Hq, int Hkv,

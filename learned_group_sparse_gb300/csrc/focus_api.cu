@@ -42,6 +42,26 @@ cudaError_t status_ptr(int **out)
     return cudaSuccess;
 }
 
+// The second stream of focus_prefill's host path (input copies that overlap
+// the assignment), created once per device; never destroyed.
+cudaStream_t g_copy_stream[kMaxDevices] = {nullptr};
+std::mutex g_copy_mu;
+
+cudaError_t copy_stream(cudaStream_t *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    if (!g_copy_stream[dev]) {
+        e = cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+    }
+    *out = g_copy_stream[dev];
+    return cudaSuccess;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -471,6 +491,17 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
         return FOCUS_ERR_INVALID_ARG;
     int launches = 0;
     cudaError_t e = cudaSuccess;
+    cudaEvent_t ev_x = nullptr, ev_qkv = nullptr;   // host path only
+    // (the events are released when the call returns; waits enqueued on them
+    // stay valid)
+    struct EventGuard {
+        cudaEvent_t *a, *b;
+        ~EventGuard()
+        {
+            if (*a) cudaEventDestroy(*a);
+            if (*b) cudaEventDestroy(*b);
+        }
+    } guard{&ev_x, &ev_qkv};
     if (host) {
         const size_t xb = (size_t)B * n * hidden * 2, qb = (size_t)B * n * Hq * d * 2,
                      kb = (size_t)B * n * Hkv * d * 2;
@@ -482,12 +513,23 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
         dV = base + w.v;
         dO = base + w.o;
         dL = lse ? reinterpret_cast<float *>(base + w.lse) : nullptr;
+        // X, W_g and C on `stream`; then K, V and Q on the copy stream, in
+        // the link's time that the assignment and bucketing run (the link
+        // carries one copy at its full rate, so they follow X rather than
+        // share the link with it).  `stream` waits for them before attention.
+        cudaStream_t cs = nullptr;
+        if ((e = copy_stream(&cs)) != cudaSuccess) return FOCUS_ERR_CUDA;
+        if ((e = cudaEventCreateWithFlags(&ev_x, cudaEventDisableTiming)) ||
+            (e = cudaEventCreateWithFlags(&ev_qkv, cudaEventDisableTiming)))
+            return FOCUS_ERR_CUDA;
         if ((e = cudaMemcpyAsync(base + w.x, X, xb, cudaMemcpyHostToDevice, s)) ||
             (e = cudaMemcpyAsync(base + w.wg, Wg, (size_t)hidden * d_g * 4, cudaMemcpyHostToDevice, s)) ||
             (e = cudaMemcpyAsync(base + w.c, C, (size_t)num_groups * d_g * 4, cudaMemcpyHostToDevice, s)) ||
-            (e = cudaMemcpyAsync(base + w.q, Q, qb, cudaMemcpyHostToDevice, s)) ||
-            (e = cudaMemcpyAsync(base + w.k, K, kb, cudaMemcpyHostToDevice, s)) ||
-            (e = cudaMemcpyAsync(base + w.v, V, kb, cudaMemcpyHostToDevice, s)))
+            (e = cudaEventRecord(ev_x, s)) || (e = cudaStreamWaitEvent(cs, ev_x, 0)) ||
+            (e = cudaMemcpyAsync(base + w.k, K, kb, cudaMemcpyHostToDevice, cs)) ||
+            (e = cudaMemcpyAsync(base + w.v, V, kb, cudaMemcpyHostToDevice, cs)) ||
+            (e = cudaMemcpyAsync(base + w.q, Q, qb, cudaMemcpyHostToDevice, cs)) ||
+            (e = cudaEventRecord(ev_qkv, cs)))
             return FOCUS_ERR_CUDA;
     }
     AssignLaunch ap{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden, d_g,
@@ -503,6 +545,7 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     if ((e = launch_bucket(ids, B, n, num_groups, topk, offsets, pos, inv, base + w.bucket, s,
                            &launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
+    if (host && (e = cudaStreamWaitEvent(s, ev_qkv, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
     const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
     st = attention_impl(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
                         num_groups, topk, dO, dL, base + w.attn, aw.total, nullptr, s,
