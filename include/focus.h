@@ -180,8 +180,9 @@ focus_status_t focus_attention_fwd(const void *Q, const void *K, const void *V,
  * pointers, and the copies in and out are enqueued around the kernels (the
  * caller synchronises `stream` before reading O).  The copies of K, V and Q
  * run on a second stream that the library creates once per device, after the
- * copy of X and beside the assignment; `stream` waits for them before the
- * attention, and they start only after the work already on `stream`.  With
+ * copy of X and beside the assignment; `stream` waits for K and V before the
+ * gather and for Q before the group kernel, and the copies start only after
+ * the work already on `stream`.  With
  * io_on_host == 0 every pointer is a device pointer.  ids_out (nullable, device) receives the
  * group ids.  Workspace: focus_prefill_workspace_size(...) device bytes.
  */

@@ -225,7 +225,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
                               int Hkv, int d, int window, float scale, const int32_t *ids,
                               const int32_t *offsets, const int32_t *pos, const int32_t *inv,
                               int K, int topk, void *O, float *lse, void *ws, size_t ws_bytes,
-                              int32_t *pair_count, cudaStream_t s, int *launches)
+                              int32_t *pair_count, cudaStream_t s, int *launches,
+                              cudaEvent_t q_ready = nullptr)
 {
     if (!Q || !Kt || !V || !ids || !offsets || !pos || !inv || !O || !ws)
         return FOCUS_ERR_INVALID_ARG;
@@ -315,6 +316,8 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.grid = grid_group;
     p.part_out16 = Opart;
     p.part_meta_out = Mpart;
+    // (Q may still be arriving from the host while the gather runs)
+    if (q_ready && (e = cudaStreamWaitEvent(s, q_ready, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
     if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
     p.tmQ = &wq;
@@ -491,17 +494,17 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
         return FOCUS_ERR_INVALID_ARG;
     int launches = 0;
     cudaError_t e = cudaSuccess;
-    cudaEvent_t ev_x = nullptr, ev_qkv = nullptr;   // host path only
+    cudaEvent_t ev_x = nullptr, ev_kv = nullptr, ev_q = nullptr;   // host path only
     // (the events are released when the call returns; waits enqueued on them
     // stay valid)
     struct EventGuard {
-        cudaEvent_t *a, *b;
+        cudaEvent_t *ev[3];
         ~EventGuard()
         {
-            if (*a) cudaEventDestroy(*a);
-            if (*b) cudaEventDestroy(*b);
+            for (cudaEvent_t *e : ev)
+                if (*e) cudaEventDestroy(*e);
         }
-    } guard{&ev_x, &ev_qkv};
+    } guard{{&ev_x, &ev_kv, &ev_q}};
     if (host) {
         const size_t xb = (size_t)B * n * hidden * 2, qb = (size_t)B * n * Hq * d * 2,
                      kb = (size_t)B * n * Hkv * d * 2;
@@ -513,14 +516,16 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
         dV = base + w.v;
         dO = base + w.o;
         dL = lse ? reinterpret_cast<float *>(base + w.lse) : nullptr;
-        // X, W_g and C on `stream`; then K, V and Q on the copy stream, in
-        // the link's time that the assignment and bucketing run (the link
-        // carries one copy at its full rate, so they follow X rather than
-        // share the link with it).  `stream` waits for them before attention.
+        // X, W_g and C on `stream`; then K, V and Q on the copy stream while
+        // the assignment and bucketing run (the link carries one copy at its
+        // full rate, so they follow X rather than share the link with it).
+        // `stream` waits for K and V before the gather and for Q before the
+        // group kernel.
         cudaStream_t cs = nullptr;
         if ((e = copy_stream(&cs)) != cudaSuccess) return FOCUS_ERR_CUDA;
         if ((e = cudaEventCreateWithFlags(&ev_x, cudaEventDisableTiming)) ||
-            (e = cudaEventCreateWithFlags(&ev_qkv, cudaEventDisableTiming)))
+            (e = cudaEventCreateWithFlags(&ev_kv, cudaEventDisableTiming)) ||
+            (e = cudaEventCreateWithFlags(&ev_q, cudaEventDisableTiming)))
             return FOCUS_ERR_CUDA;
         if ((e = cudaMemcpyAsync(base + w.x, X, xb, cudaMemcpyHostToDevice, s)) ||
             (e = cudaMemcpyAsync(base + w.wg, Wg, (size_t)hidden * d_g * 4, cudaMemcpyHostToDevice, s)) ||
@@ -528,8 +533,9 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
             (e = cudaEventRecord(ev_x, s)) || (e = cudaStreamWaitEvent(cs, ev_x, 0)) ||
             (e = cudaMemcpyAsync(base + w.k, K, kb, cudaMemcpyHostToDevice, cs)) ||
             (e = cudaMemcpyAsync(base + w.v, V, kb, cudaMemcpyHostToDevice, cs)) ||
+            (e = cudaEventRecord(ev_kv, cs)) ||
             (e = cudaMemcpyAsync(base + w.q, Q, qb, cudaMemcpyHostToDevice, cs)) ||
-            (e = cudaEventRecord(ev_qkv, cs)))
+            (e = cudaEventRecord(ev_q, cs)))
             return FOCUS_ERR_CUDA;
     }
     AssignLaunch ap{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden, d_g,
@@ -545,11 +551,11 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     if ((e = launch_bucket(ids, B, n, num_groups, topk, offsets, pos, inv, base + w.bucket, s,
                            &launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if (host && (e = cudaStreamWaitEvent(s, ev_qkv, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (host && (e = cudaStreamWaitEvent(s, ev_kv, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
     const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
     st = attention_impl(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
                         num_groups, topk, dO, dL, base + w.attn, aw.total, nullptr, s,
-                        &launches);
+                        &launches, host ? ev_q : nullptr);
     if (st) return st;
     if (host) {
         if ((e = cudaMemcpyAsync(O, dO, (size_t)B * n * Hq * d * 2, cudaMemcpyDeviceToHost, s)))
