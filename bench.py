@@ -64,10 +64,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The sources of the attention kernels (the kernel whose DRAM traffic
+# profiles/traffic.json records): a stored figure stands only while these are
+# byte-identical to what was profiled.
+ATTN_SOURCES = ("focus_attn_kernel.cuh", "focus_attn_launch.cuh", "focus_attn_group.cu",
+                "focus_attn_window.cu", "focus_ptx.cuh", "focus_tmem_wide.cuh",
+                "focus_internal.h")
+
+
 def src_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "learned_group_sparse_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in ATTN_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
