@@ -59,6 +59,7 @@ ATTN_CASES = [
     (1, 1100, 6, 2, 128, 16, 2, 100),     # odd GQA ratio: query tiles pair up
     (1, 2300, 3, 3, 64, 12, 3, 300),      # odd number of query tiles per head
     (1, 600, 2, 2, 128, 1024, 8, 96),     # the largest K and topk at d = 128
+    (4, 300, 2, 2, 64, 1024, 2, 16),      # B * K at its limit (4096), most groups empty
 ]
 
 
