@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) assign_prep_kernel(const float *__restric
     float *csm = psm;                  // [dg][32]: C rows c0..c0+31, transposed
     float *wsm = psm + 32 * dg;        // [32][dg + 1]: W_g rows h0..h0+31
     const int c0 = blockIdx.y * 32, h0 = blockIdx.x * 32;
+#pragma unroll 8   // several loads in flight per thread
     for (int i = threadIdx.x; i < 32 * dg; i += blockDim.x) {
         const int r = i / dg, e = i - r * dg;
         csm[e * 32 + r] = (c0 + r < K) ? C[(int64_t)(c0 + r) * dg + e] : 0.f;

@@ -6,10 +6,11 @@
 //   1. bucket_count    per chunk of 4096 (token, slot) entries, a histogram
 //                      of group ids in shared memory;
 //   2. bucket_scan     per group, an exclusive scan of the chunk counts;
-//   3. bucket_offsets  per batch, an exclusive scan of the group sizes;
-//   4. bucket_scatter  per chunk, a stable scatter: each warp walks its slice
-//                      of the chunk in order and ranks equal ids inside a
-//                      32-entry step with __match_any_sync.
+//   3. bucket_scatter  per chunk, a stable scatter: the block scans the
+//                      group sizes into offsets (chunk 0 stores them), then
+//                      each warp walks its slice of the chunk in order and
+//                      ranks equal ids inside a 32-entry step with
+//                      __match_any_sync.
 // The plan kernel orders the group kernel's tiles by decreasing cost, the
 // gather kernel copies K/V rows into group order (the group kernel copies its
 // Q rows itself), and the mask-table kernel writes every key tile's group
@@ -75,15 +76,20 @@ __global__ void bucket_scan(int32_t *__restrict__ counts, int K, int nchunks,
     }
 }
 
-// One block of 1024 threads per batch: exclusive scan of K <= 1024 sizes.
-__global__ void bucket_offsets(const int32_t *__restrict__ totals, int K,
-                               int32_t *__restrict__ offsets)
+// Exclusive scan of the K <= 1024 group sizes of one batch into soff[0..K]
+// (soff[K] = total), by a block of 256 threads: four sizes per thread.
+__device__ __forceinline__ void scan_sizes(const int32_t *__restrict__ totals, int K, int *soff)
 {
-    grid_dep_sync();
-    __shared__ int warp_sum[32];
-    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const int v = t < K ? totals[(int64_t)b * K + t] : 0;
-    int x = v;
+    __shared__ int warp_sum[8];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int v[4], local = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int g = 4 * t + q;
+        v[q] = g < K ? totals[g] : 0;
+        local += v[q];
+    }
+    int x = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, off);
@@ -91,35 +97,41 @@ __global__ void bucket_offsets(const int32_t *__restrict__ totals, int K,
     }
     if (lane == 31) warp_sum[w] = x;
     __syncthreads();
-    if (w == 0) {
-        int s = warp_sum[lane];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, off);
-            if (lane >= off) s += y;
-        }
-        warp_sum[lane] = s;
+    int before = x - local, total = 0;
+    for (int i = 0; i < 8; ++i) {
+        if (i < w) before += warp_sum[i];
+        total += warp_sum[i];
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int g = 4 * t + q;
+        if (g < K) soff[g] = before;
+        before += v[q];
+    }
+    if (t == 0) soff[K] = total;
     __syncthreads();
-    const int incl = x + (w > 0 ? warp_sum[w - 1] : 0);
-    int32_t *off = offsets + (int64_t)b * (K + 1);
-    if (t < K) off[t] = incl - v;
-    if (t == K - 1) off[K] = incl;
 }
 
 __global__ void __launch_bounds__(256) bucket_scatter(const int32_t *__restrict__ ids,
                                                       int64_t nk, int K, int topk, int nchunks,
                                                       const int32_t *__restrict__ chunk_base,
-                                                      const int32_t *__restrict__ offsets,
+                                                      const int32_t *__restrict__ totals,
+                                                      int32_t *__restrict__ offsets,
                                                       int32_t *__restrict__ pos,
                                                       int32_t *__restrict__ inv)
 {
     grid_dep_sync();
-    extern __shared__ int hist[];   // [kScatterWarps][K]
+    extern __shared__ int hist[];   // [kScatterWarps][K], then the offsets [K + 1]
+    int *soff = hist + kScatterWarps * K;
     const int chunk = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kScatterWarps * K; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
+    // group offsets of this batch (every block scans the sizes; chunk 0
+    // publishes them)
+    scan_sizes(totals + (int64_t)b * K, K, soff);
+    if (chunk == 0)
+        for (int g = threadIdx.x; g <= K; g += blockDim.x)
+            offsets[(int64_t)b * (K + 1) + g] = soff[g];
     const int64_t e0 = (int64_t)chunk * kBucketChunk;
     const int64_t s0 = min(e0 + (int64_t)w * kWarpSlice, nk);
     const int64_t s1 = min(s0 + kWarpSlice, nk);
@@ -130,9 +142,8 @@ __global__ void __launch_bounds__(256) bucket_scatter(const int32_t *__restrict_
     }
     __syncthreads();
     const int32_t *cb = chunk_base + ((int64_t)b * nchunks + chunk) * K;
-    const int32_t *ob = offsets + (int64_t)b * (K + 1);
     for (int g = threadIdx.x; g < K; g += blockDim.x) {
-        int run = ob[g] + cb[g];
+        int run = soff[g] + cb[g];
         for (int x = 0; x < kScatterWarps; ++x) {
             const int t = hist[x * K + g];
             hist[x * K + g] = run;
@@ -418,7 +429,9 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
     int32_t *counts = static_cast<int32_t *>(ws);
     int32_t *totals = counts + (size_t)B * (size_t)(nchunks > 0 ? nchunks : 1) * K;
     cudaError_t e;
-    if (nchunks > 0) {
+    if (nchunks == 0)   // no entries: every group is empty
+        return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)B * (K + 1), s);
+    {
         prof_begin("bucket_count", s);
         e = launch_pdl(bucket_count, dim3(nchunks, B), dim3(256), K * sizeof(int), s, ids, nk, K,
                        nchunks, counts);
@@ -430,23 +443,15 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
         prof_end(s);
         if (e != cudaSuccess) return e;
         *launches += 2;
-    } else {
-        e = cudaMemsetAsync(totals, 0, sizeof(int32_t) * (size_t)B * K, s);
-        if (e != cudaSuccess) return e;
     }
-    prof_begin("bucket_offsets", s);
-    e = launch_pdl(bucket_offsets, dim3(B), dim3(1024), 0, s, totals, K, offsets);
-    prof_end(s);
-    if (e != cudaSuccess) return e;
-    *launches += 1;
-    if (nchunks > 0) {
-        const size_t smem = sizeof(int) * (size_t)kScatterWarps * K;
+    {
+        const size_t smem = sizeof(int) * ((size_t)kScatterWarps * K + K + 1);
         e = cudaFuncSetAttribute(bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         prof_begin("bucket_scatter", s);
         e = launch_pdl(bucket_scatter, dim3(nchunks, B), dim3(256), smem, s, ids, nk, K, topk,
-                       nchunks, counts, offsets, pos, inv);
+                       nchunks, counts, totals, offsets, pos, inv);
         prof_end(s);
         if (e != cudaSuccess) return e;
         *launches += 1;
