@@ -154,6 +154,23 @@ def dist_setup(args):
     return world, rank, local
 
 
+def slowest_rank_ms(ms, pg, device):
+    """The largest of the ranks' timed-region lengths (ms), so that the whole
+    job's time is that of its slowest replica.  pg: torch.distributed or None."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, units_per_step, total_ms):
+    """Units of all replicas per second: each of the `world` ranks processed
+    `steps` steps of `units_per_step` units within the slowest rank's time."""
+    return world * steps * units_per_step / (total_ms * 1e-3)
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_sample(w, t, rows, ids_all_np):
     """Times the oracle on the sampled query rows: assignment of their tokens
@@ -346,11 +363,8 @@ def main():
     clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
-    if pg:
-        tt = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = world * args.steps * ntok / (total_ms * 1e-3)
+    total_ms = slowest_rank_ms(total_ms, pg, dev)
+    value = job_throughput(world, args.steps, ntok, total_ms)
     ms_per_step = total_ms / args.steps
 
     if args.quick:
@@ -448,12 +462,9 @@ def main():
             eh.append((a, b))
         torch.cuda.synchronize()
         e_ms = sum(a.elapsed_time(b) for a, b in eh)
-        if pg:
-            tt = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = slowest_rank_ms(e_ms, pg, dev)
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        e2e = {"value": world * reps * ntok / (e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": job_throughput(world, reps, ntok, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Oh.numel() * 2,
                "ms_per_step": e_ms / reps}
         del wsh
