@@ -88,6 +88,32 @@ def test_dense_causal_matches_oracle(B, n, Hq, Hkv, d):
     check_output(O, Oref, L.permute(0, 2, 1), Lref, label="dense")
 
 
+@pytest.mark.parametrize("B,n,Hq,Hkv,d,K,topk,window", [
+    (1, 1000, 4, 2, 128, 1, 1, 64),     # one group holds every token
+    (2, 777, 4, 1, 64, 8, 2, 5000),     # the window covers every causal pair
+    (1, 1300, 6, 2, 128, 4, 4, 0),      # topk = K: every pair is scored in group 0
+])
+def test_special_cases_reduce_to_dense_causal(B, n, Hq, Hkv, d, K, topk, window):
+    """Where the allowed set is every causal pair, the Focus path (group,
+    window and merge kernels) must give plain causal attention: checked
+    against the library's own dense kernel, an independent mainloop run.
+    Each output is within (1e-2 max-abs, 1e-3 mean-abs) of the exact result
+    (the oracle tests), so the two agree within twice that; each is rounded
+    to bf16 on its own, and one bf16 step at |O| in [2, 4) is already
+    1.6e-2."""
+    Q, Kt, V = qkv(B, n, Hq, Hkv, d, seed=5 * n + K)
+    ids = torch.from_numpy(rand_ids(B, n, K, topk, seed=n + 3 * K)).cuda()
+    off, pos, inv = fg.focus_bucket(ids, K)
+    O, L = fg.focus_attention_fwd(Q, Kt, V, window, ids, off, pos, inv, K)
+    Od, Ld = fg.focus_dense_causal_fwd(Q, Kt, V, with_lse=True)
+    torch.cuda.synchronize()
+    err = (O.float() - Od.float()).abs()
+    assert torch.isfinite(O.float()).all()
+    assert float(err.max()) <= 2e-2 and float(err.mean()) <= 2e-3, \
+        f"K{K} top{topk} w{window}: max-abs {float(err.max()):.3e} mean-abs {float(err.mean()):.3e}"
+    assert float((L - Ld).abs().max()) <= 2 * 2e-3   # twice the lse bound
+
+
 @pytest.mark.parametrize("B,n,K,topk", [(1, 1, 4, 2), (2, 5000, 64, 2), (3, 4097, 7, 3),
                                         (1, 3000, 1024, 8), (1, 9000, 1, 1), (2, 20000, 256, 2)])
 def test_bucket_matches_oracle_exactly(B, n, K, topk):
