@@ -70,7 +70,7 @@ def _load():
             lib.oracle_bucket.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
             lib.oracle_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
                                              vp, i32, vp, i64, i32, vp, vp]
-            lib.oracle_count_pairs.argtypes = [vp, i32, i32, i32, i32, vp, _I64P]
+            lib.oracle_count_pairs.argtypes = [vp, i32, i32, i32, i32, vp, i64, vp, _I64P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_assign, lib.oracle_bucket, lib.oracle_attention,
                       lib.oracle_count_pairs, lib.oracle_num_threads):
@@ -172,14 +172,21 @@ def attention(Q_bits, K_bits, V_bits, ids, window, scale=0.0, rows=None):
     return O, L
 
 
-def count_pairs(ids, window):
-    """Allowed keys per query.  ids [B, n, topk] -> (per_query [B, n] int64, total)."""
+def count_pairs(ids, window, rows=None):
+    """Allowed keys per query.  ids [B, n, topk] -> (per_query [B, n] int64,
+    total).  rows: optional 1-D int64 array of flattened query indices b*n + i;
+    then per_query is [len(rows)] and total sums over those rows only."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     B, n, topk = ids.shape
-    per = np.empty((B, n), np.int64)
+    if rows is None:
+        rows_arr, nrows = None, B * n
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.shape[0]
+    per = np.empty((nrows,), np.int64)
     tot = ctypes.c_int64(0)
-    rc = _load().oracle_count_pairs(_ptr(ids), B, n, topk, int(window), _ptr(per),
-                                    ctypes.byref(tot))
+    rc = _load().oracle_count_pairs(_ptr(ids), B, n, topk, int(window), _ptr(rows_arr), nrows,
+                                    _ptr(per), ctypes.byref(tot))
     if rc:
         raise ValueError("oracle_count_pairs: invalid arguments")
-    return per, int(tot.value)
+    return (per.reshape(B, n) if rows is None else per), int(tot.value)

@@ -238,18 +238,22 @@ int oracle_attention(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V,
 /* -------------------------------------------------------------------------
  * |A_i|: the number of allowed keys of every query row (the work the
  * method does), by direct enumeration of the rule above.
- * per_query [B*n] (nullable), returns the total through *total.
+ * rows: nrows flattened query indices b*n + i (NULL: all B*n rows, in order)
+ * per_query [nrows] (nullable); the sum over those rows goes to *total.
  * ------------------------------------------------------------------------- */
 int oracle_count_pairs(const int32_t *ids, int B, int n, int topk, int window,
+                       const int64_t *rows, int64_t nrows,
                        int64_t *per_query, int64_t *total)
 {
     if (!ids || !total || B < 1 || n < 0 || topk < 1 || window < 0) return 1;
+    if (!rows) nrows = (int64_t)B * n;
     int64_t sum = 0;
     int64_t r;
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : sum)
-    for (r = 0; r < (int64_t)B * n; ++r) {
-        int b = (int)(r / n);
-        int64_t i = r % n;
+    for (r = 0; r < nrows; ++r) {
+        int64_t flat = rows ? rows[r] : r;
+        int b = (int)(flat / n);
+        int64_t i = flat % n;
         const int32_t *ids_b = ids + (int64_t)b * n * topk;
         int64_t c = 0;
         for (int64_t j = 0; j <= i; ++j) c += allowed(ids_b, topk, window, i, j);

@@ -83,5 +83,11 @@ def test_workload(idx):
         rper, rtot = oracle.count_pairs(ids_np, w.window)
         np.testing.assert_array_equal(per.cpu().numpy(), rper)
         assert int(tot[0]) == rtot
+    else:
+        # the sampled rows: both the count kernel and the counted attention
+        # against the oracle's enumeration of the rule
+        rper, _ = oracle.count_pairs(ids_np, w.window, rows=rows)
+        np.testing.assert_array_equal(per.view(-1)[rt].cpu().numpy(), rper)
+        np.testing.assert_array_equal(cnt.view(-1)[rt].long().cpu().numpy(), rper)
     del Q, K, V, O, L
     free_cuda()

@@ -197,6 +197,27 @@ def test_rows_subset_matches_full():
     np.testing.assert_array_equal(Ls, L.reshape(B * n, H)[rows])
 
 
+def test_rows_only_q_matches_full_and_sdpa():
+    """The sampled-Q form (Q holds only the sampled rows, in the order of
+    `rows`): rows from both batches, out of order, agree bit for bit with the
+    full-Q call on those rows, and with SDPA under the brute-force mask."""
+    B, n, Hq, Hkv, d = 2, 90, 4, 2, 32
+    Q, K, V = _qkv(B, n, Hq, Hkv, d, 53)
+    ids = _rand_ids(B, n, 5, 2, 29)
+    window = 6
+    rows = np.array([131, 7, 89, 90, 0, 179, 45, 100], np.int64)
+    Qr = Q.reshape(B * n, Hq, d)[torch.as_tensor(rows)]
+    Os, Ls = _run(Qr, K, V, ids, window, rows=rows)
+    O, L = _run(Q, K, V, ids, window)
+    np.testing.assert_array_equal(Os, O.reshape(B * n, Hq, d)[rows])
+    np.testing.assert_array_equal(Ls, L.reshape(B * n, Hq)[rows])
+    A = _brute_allowed(ids, window)
+    ref = _sdpa(Q, K, V, mask=A).reshape(B * n, Hq, d)[rows]
+    np.testing.assert_allclose(Os, ref, atol=2e-6)
+    lref = _lse(Q, K, A).reshape(B * n, Hq)[rows]
+    np.testing.assert_allclose(Ls, lref, atol=2e-5)
+
+
 def test_rows_sum_to_one():
     B, n, H, d = 1, 64, 2, 16
     Q, K, _ = _qkv(B, n, H, H, d, 61)
@@ -216,6 +237,22 @@ def test_count_closed_forms():
     assert (per[0] == np.minimum(7, i + 1)).all()
     per, _ = oracle.count_pairs(np.arange(n, dtype=np.int32).reshape(1, n, 1), 0)
     assert (per[0] == 1).all()          # only the token itself (its own group)
+
+
+@pytest.mark.parametrize("window", [0, 3, 11])
+def test_count_rows_subset(window):
+    """Counting only sampled rows (both batches, out of order) gives the
+    brute-force set counts of those rows and their sum."""
+    B, n = 2, 70
+    ids = _rand_ids(B, n, 6, 2, 31 + window)
+    rows = np.array([139, 0, 69, 70, 5, 100, 33], np.int64)
+    per, tot = oracle.count_pairs(ids, window, rows=rows)
+    A = _brute_allowed(ids, window).reshape(B * n, n)
+    expect = A[rows].sum(-1)
+    np.testing.assert_array_equal(per, expect)
+    assert tot == int(expect.sum())
+    full, _ = oracle.count_pairs(ids, window)
+    np.testing.assert_array_equal(per, full.reshape(-1)[rows])
 
 
 # ------------------------------------------------------------ assign pins ---
