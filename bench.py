@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "Focus attn prefill tokens/s (1 GB300); effective TFLOP/s vs bf16 peak"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = 1          # B1 n8192 MHA32 d128 K64 top2 w256
+DEFAULT_WORKLOAD = 4          # B1 n1048576 GQA32/8 d128 K256 top2 w1024
 FLUSH_BYTES = 512 << 20       # > L2 (129 MB)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT = 152
@@ -43,8 +43,8 @@ SM_COUNT = 152
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["focus", "reference"], default="focus")
     ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
     ap.add_argument("--no-e2e", action="store_true")
@@ -190,6 +190,11 @@ def oracle_sample(w, t, rows, ids_all_np):
 
 
 def oracle_setup(w, t):
+    """Host copies of the inputs the sampled rows need.  The masks of the
+    sampled rows use seeded synthetic group ids with the structure of the
+    assignment (first id = the token's mixture component): computing the
+    oracle's own ids for every token would cost minutes of CPU at n = 1M,
+    and the values of the ids do not change the oracle's work per row."""
     import oracle
     from learned_group_sparse_gb300 import synth
     oracle.build()
@@ -197,8 +202,8 @@ def oracle_setup(w, t):
     t["Vh"] = synth.bits(t["V"])
     t["Wgh"] = t["Wg"].cpu().numpy()
     t["Ch"] = t["C"].cpu().numpy()
-    ids, _, _ = oracle.assign(synth.bits(t["X"]), t["Wgh"], t["Ch"], w.topk)
-    return ids.reshape(w.B, w.n, w.topk), oracle.num_threads()
+    ids = synth.synthetic_ids(w, t["comp"], t["K"].device).cpu().numpy()
+    return ids, oracle.num_threads()
 
 
 def sample_rows(w, count, seed):
@@ -228,7 +233,8 @@ def run_reference(args, w, world, rank):
     total = sum(secs)
     value = nrows / total
     sample = (f"{per_step} seeded query rows per step of {w.name}: their group assignment "
-              f"plus exact masked softmax over all heads (ids of all tokens precomputed)")
+              f"plus exact masked softmax over all heads (masks from seeded synthetic ids of "
+              f"the assignment's structure)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
@@ -249,18 +255,30 @@ def workload_config(w):
             "inputs": "device-resident (value); pinned host buffers (e2e)"}
 
 
+def assign_order(w):
+    """The tensor-core assignment's order: (X W_g) C^T when there are more
+    centroids than centroid dimensions (rounded up to 64, at most 128), else
+    X (W_g C^T); returns (z_path, padded d_g)."""
+    kp, dgp = (w.K + 15) // 16 * 16, (w.dg + 63) // 64 * 64
+    return (w.K <= 256 and w.hidden % 64 == 0 and dgp <= 128 and kp > dgp), dgp
+
+
 def kernel_work(w, share_pairs, total_pairs):
-    """Algorithmic work of one launch of each kernel: (amount, unit, bound)."""
+    """Algorithmic work of one launch of each kernel: (amount, unit, bound).
+    HBM kernels count compulsory bytes: each input read once, each output
+    written once."""
     B, n, Hq, Hkv, d, k = w.B, w.n, w.Hq, w.Hkv, w.d, w.topk
     nk = n * k
-    return {
+    ntok = B * n
+    z_path, dgp = assign_order(w)
+    work = {
         "attn_group": (4.0 * d * Hq * share_pairs, "flop", "tensor"),
         "attn_window": (4.0 * d * Hq * (total_pairs - share_pairs), "flop", "tensor"),
         "attn_dense": (4.0 * d * Hq * B * n * (n + 1) / 2, "flop", "tensor"),
-        "assign": (2.0 * B * n * w.hidden + 4.0 * B * n * k, "byte", "hbm"),
-        # K and V rows into group order (read + write); the group kernel
-        # copies its Q rows from Q itself
-        "gather": (2.0 * B * nk * (2 * Hkv) * d * 2, "byte", "hbm"),
+        # K and V rows into group order: every source row read once, every
+        # membership's row written once; pos read, group ids copied
+        "gather": (2.0 * ntok * (2 * Hkv) * d + 2.0 * B * nk * (2 * Hkv) * d
+                   + 4.0 * B * nk + 2 * 4.0 * B * nk * k, "byte", "hbm"),
         "bucket_count": (4.0 * B * nk, "byte", "hbm"),
         "bucket_scatter": (12.0 * B * nk, "byte", "hbm"),
         # group ids read (group-order and token-order rows), one [K] uint4
@@ -268,7 +286,18 @@ def kernel_work(w, share_pairs, total_pairs):
         "mask_table": (4.0 * B * (nk + n) * k
                        + 16.0 * w.K * B * ((nk + 127) // 128 + w.K + (n + 127) // 128),
                        "byte", "hbm"),
+        # k + 1 fp16 partials (all heads) with their {lse, scale} read, inv
+        # read, the bf16 output written
+        "merge": (ntok * ((k + 1) * Hq * (2.0 * d + 8) + 4.0 * k + 2.0 * Hq * d), "byte", "hbm"),
     }
+    if z_path:
+        # Z = X W_g: X read, fp16 hi + lo of Z and a scale written per token
+        work["assign"] = (ntok * (2.0 * w.hidden + 4.0 * dgp + 4), "byte", "hbm")
+        # Z C^T and top-k: Z and its scale read, ids written
+        work["assign_score"] = (ntok * (4.0 * dgp + 4 + 4.0 * k), "byte", "hbm")
+    else:
+        work["assign"] = (ntok * (2.0 * w.hidden + 4.0 * k), "byte", "hbm")
+    return work
 
 
 def roofline_entry(name, ms, work, peaks, peak_kind, clock_mhz):
@@ -380,7 +409,8 @@ def main():
     eff_flop = 4.0 * w.d * w.Hq * total_pairs
 
     # ---- per-kernel times (separate pass, events around every launch)
-    prof_steps = min(args.steps, 50)
+    # (about 3 s of steps: 50 at n = 8K, about 17 at n = 1M)
+    prof_steps = max(1, min(args.steps, 50, int(3000.0 / max(ms_per_step, 1e-3))))
     fg.focus_profile_enable(True)
     for _ in range(prof_steps):
         flush.zero_()
@@ -416,8 +446,11 @@ def main():
     dense = None
     if not args.no_dense:
         Od = torch.empty_like(O)
-        reps = max(3, min(50, args.steps // 4))
-        for _ in range(2):
+        # dense causal attention grows as n^2: at n = 1M one call is about 9 s,
+        # so long workloads time a single call (no warm-up call either)
+        est_s = works["attn_dense"][0] / 1.2e15
+        reps = 1 if est_s > 0.5 else max(3, min(50, args.steps // 4))
+        for _ in range(0 if est_s > 0.5 else 2):
             fg.focus_dense_causal_fwd(t["Q"], t["K"], t["V"], O=Od)
         dms = []
         for _ in range(reps):
@@ -430,7 +463,7 @@ def main():
         torch.cuda.synchronize()
         d_ms = statistics.mean(a.elapsed_time(b) for a, b in dms)
         dflop = works["attn_dense"][0]
-        dense = {"ms": d_ms, "tflops": dflop / (d_ms * 1e-3) / 1e12,
+        dense = {"ms": d_ms, "timed_calls": reps, "tflops": dflop / (d_ms * 1e-3) / 1e12,
                  "speedup_of_focus_step": d_ms / ms_per_step,
                  "speedup_of_focus_attention": d_ms / attn_ms if attn_ms else None}
         del Od
@@ -497,6 +530,8 @@ def main():
             "effective_tflops": eff_flop / (ms_per_step * 1e-3) / 1e12,
             "effective_frac_of_bf16_peak": eff_flop / (ms_per_step * 1e-3) / 1e12
             / float(peaks["bf16_tflops"]),
+            "effective_frac_of_bf16_sustained": eff_flop / (ms_per_step * 1e-3) / 1e12
+            / float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])),
             "attention_effective_tflops": eff_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
             "allowed_pairs": total_pairs, "group_pairs": share_pairs,
             "roofline": roof, "kernels": kernels, "dense_causal": dense,

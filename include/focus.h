@@ -66,18 +66,22 @@ const char *focus_version(void);
  *                          (+inf when K == 1); a small margin flags a
  *                          near-tie whose order depends on rounding.
  *   ws, ws_bytes: device workspace of at least
- *          focus_assign_workspace_size(hidden, d_g, K, topk) bytes (may be
- *          NULL when that size is 0).
- * Arithmetic: fp32-accurate scores.  For K <= 256 and hidden % 64 == 0 the
- * scores are X . (W_g C^T) on the tensor cores, with W_g C^T (fp32) split
- * into two bf16 parts (X is exact in bf16), fp32 accumulation; otherwise an
- * fp32 FMA kernel computes (X W_g) C^T.  Rounding differs from an exact
- * evaluation only below the margin, so ids can differ only where the margin
- * is tiny.
+ *          focus_assign_workspace_size(B, n, hidden, d_g, K, topk) bytes (may
+ *          be NULL when that size is 0).
+ * Arithmetic: fp32-accurate scores on the tensor cores where hidden % 64 == 0
+ * and K <= 256 (X is exact in bf16; fp32 factors are split into two bf16 or
+ * fp16 parts; fp32 accumulation), in one of two orders:
+ *   - more centroids than centroid dimensions (K > d_g rounded up to 64,
+ *     d_g <= 128): the pages' order, Z = X W_g, then Z C^T, with each row of
+ *     Z scaled by a power of two and split into two fp16 parts;
+ *   - otherwise X (W_g C^T), with W_g C^T formed once per call.
+ * Other shapes use an fp32 FMA kernel for (X W_g) C^T.  Rounding differs
+ * from an exact evaluation only below the margin, so ids can differ only
+ * where the margin is tiny.
  * Supported: hidden % 8 == 0, 1 <= d_g <= 256, 1 <= K <= 1024,
  *            1 <= topk <= min(K, 8).
  */
-size_t focus_assign_workspace_size(int hidden, int d_g, int K, int topk);
+size_t focus_assign_workspace_size(int B, int n, int hidden, int d_g, int K, int topk);
 focus_status_t focus_assign(const void *X, const float *Wg, const float *C,
                             int B, int n, int hidden, int d_g, int K, int topk,
                             int32_t *ids, float *margin,
@@ -244,6 +248,18 @@ focus_status_t focus_attention_fwd_counted(const void *Q, const void *K, const v
  * device: FOCUS_OK or FOCUS_ERR_TIMEOUT.  Synchronises the device.
  */
 focus_status_t focus_get_device_status(int reset);
+
+/*
+ * Sets the limit of the kernels' bounded device-side waits on the current
+ * device, in nanoseconds of the GPU's global timer (0 restores the default,
+ * 2 s).  A testing aid: a tiny limit makes the waits of the next launches run
+ * out, so that their error path (the kernel finishes early, lets the copies
+ * and tensor-core operations it issued land, and records FOCUS_ERR_TIMEOUT in
+ * the device status word) can be exercised without faulting or hanging the
+ * GPU.  Outputs of launches whose waits ran out are undefined.  Synchronises
+ * the device; not for use while kernels of this library are in flight.
+ */
+focus_status_t focus_set_wait_limit(unsigned long long ns);
 
 /* Number of kernels the last successful call on this host thread enqueued. */
 int focus_last_launch_count(void);

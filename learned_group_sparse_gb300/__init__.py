@@ -21,7 +21,8 @@ __all__ = [
     "focus_assign", "focus_assign_workspace_size", "focus_bucket", "focus_attention_fwd", "focus_attention_fwd_counted",
     "focus_prefill", "focus_dense_causal_fwd", "focus_count_pairs",
     "focus_bucket_workspace_size", "focus_attention_workspace_size",
-    "focus_prefill_workspace_size", "focus_get_device_status", "focus_last_launch_count",
+    "focus_prefill_workspace_size", "focus_get_device_status", "focus_set_wait_limit",
+    "focus_last_launch_count",
     "focus_status_string", "focus_version", "focus_profile_enable", "focus_profile_read",
 ]
 
@@ -52,7 +53,7 @@ def library() -> ctypes.CDLL:
             sig = {
                 "focus_status_string": ([i32], ctypes.c_char_p),
                 "focus_version": ([], ctypes.c_char_p),
-                "focus_assign_workspace_size": ([i32] * 4, sz),
+                "focus_assign_workspace_size": ([i32] * 6, sz),
                 "focus_assign": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp, sz, vp], i32),
                 "focus_bucket_workspace_size": ([i32, i32, i32, i32], sz),
                 "focus_bucket": ([vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], i32),
@@ -67,6 +68,7 @@ def library() -> ctypes.CDLL:
                 "focus_dense_causal_fwd": ([vp, vp, vp] + [i32] * 5 + [f32, vp, vp, vp], i32),
                 "focus_count_pairs": ([vp] * 4 + [i32] * 5 + [vp, vp, vp], i32),
                 "focus_get_device_status": ([i32], i32),
+                "focus_set_wait_limit": ([ctypes.c_ulonglong], i32),
                 "focus_last_launch_count": ([], i32),
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_profile_enable": ([i32], None),
@@ -124,6 +126,12 @@ def focus_get_device_status(reset: bool = False) -> int:
     return int(library().focus_get_device_status(1 if reset else 0))
 
 
+def focus_set_wait_limit(ns: int = 0) -> None:
+    """Limit of the kernels' bounded device-side waits in ns (0: the default,
+    2 s).  A testing aid for the timeout path; synchronises the device."""
+    _check("focus_set_wait_limit", library().focus_set_wait_limit(int(ns)))
+
+
 def focus_profile_enable(enable: bool = True) -> None:
     library().focus_profile_enable(1 if enable else 0)
 
@@ -150,8 +158,8 @@ def focus_trace_attention(group_buf=None, window_buf=None, dense_buf=None) -> No
     library().focus_trace_attention(_p(group_buf), _p(window_buf), _p(dense_buf))
 
 
-def focus_assign_workspace_size(hidden, dg, K, topk) -> int:
-    return int(library().focus_assign_workspace_size(hidden, dg, K, topk))
+def focus_assign_workspace_size(B, n, hidden, dg, K, topk) -> int:
+    return int(library().focus_assign_workspace_size(B, n, hidden, dg, K, topk))
 
 
 def focus_assign(X, Wg, C, topk, ids=None, margin=None, with_margin=True, ws=None):
@@ -166,7 +174,7 @@ def focus_assign(X, Wg, C, topk, ids=None, margin=None, with_margin=True, ws=Non
         ids = torch.empty(B, n, topk, dtype=torch.int32, device=X.device)
     if margin is None and with_margin:
         margin = torch.empty(B, n, dtype=torch.float32, device=X.device)
-    need = focus_assign_workspace_size(hidden, dg, K, topk)
+    need = focus_assign_workspace_size(B, n, hidden, dg, K, topk)
     if ws is None and need:
         ws = torch.empty(need, dtype=torch.uint8, device=X.device)
     _check("focus_assign", library().focus_assign(

@@ -18,8 +18,14 @@ namespace {
 
 thread_local int g_last_launches = 0;
 
-// Device status word: set by a kernel whose bounded wait ran out.
-__device__ int g_device_status = 0;
+// Device status record: code (set by a kernel whose bounded wait ran out),
+// then the wait limit the kernels' bounded waits use (see focus_ptx.cuh).
+struct DeviceStatus {
+    int code;
+    int reserved;
+    unsigned long long wait_limit_ns;
+};
+__device__ DeviceStatus g_device_status = {0, 0, 2000000000ull};
 
 constexpr int kMaxDevices = 64;
 int *g_status_addr[kMaxDevices] = {nullptr};
@@ -36,7 +42,7 @@ cudaError_t status_ptr(int **out)
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_device_status);
         if (e != cudaSuccess) return e;
-        g_status_addr[dev] = static_cast<int *>(p);
+        g_status_addr[dev] = &static_cast<DeviceStatus *>(p)->code;
     }
     *out = g_status_addr[dev];
     return cudaSuccess;
@@ -100,8 +106,8 @@ bool make_map(CUtensorMap *m, const void *base, int B, int64_t rows, int H, int 
 
 }  // namespace
 
-bool make_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-                      uint32_t box_inner, uint32_t box_outer)
+bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, bool f16)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -109,10 +115,10 @@ bool make_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t
     const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 namespace {
@@ -164,7 +170,7 @@ PrefillWs prefill_ws(int B, int n, int hidden, int Hq, int Hkv, int d, int dg, i
     w.offsets = off; off += align256((size_t)B * (K + 1) * 4);
     w.pos = off;     off += align256((size_t)B * nk * 4);
     w.inv = off;     off += align256((size_t)B * nk * 4);
-    w.assign = off;  off += align256(assign_ws_bytes(hidden, K));
+    w.assign = off;  off += align256(assign_ws_bytes((int64_t)B * n, hidden, dg, K, topk));
     w.bucket = off;  off += align256(bucket_ws_bytes(B, n, K, topk));
     w.attn = off;    off += align256(attn_ws(B, n, Hq, Hkv, d, K, topk).total);
     w.x = w.wg = w.c = w.q = w.k = w.v = w.o = w.lse = 0;
@@ -182,7 +188,6 @@ PrefillWs prefill_ws(int B, int n, int hidden, int Hq, int Hkv, int d, int dg, i
     return w;
 }
 
-focus_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
 
 // ------------------------------------------------------------ validation
 focus_status_t check_assign(const void *X, const float *Wg, const float *C, int B, int n,
@@ -200,18 +205,6 @@ focus_status_t check_assign(const void *X, const float *Wg, const float *C, int 
     return FOCUS_OK;
 }
 
-focus_status_t check_bucket(const int32_t *ids, int B, int n, int K, int topk,
-                            const int32_t *offsets, const int32_t *pos, const int32_t *inv)
-{
-    if (!ids || !offsets || !pos || !inv) return FOCUS_ERR_INVALID_ARG;
-    if (!aligned16(ids) || !aligned16(offsets) || !aligned16(pos) || !aligned16(inv))
-        return FOCUS_ERR_INVALID_ARG;
-    if (B < 1 || n < 0 || K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
-    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
-    if (K > 1024 || topk > 8 || B > 65535) return FOCUS_ERR_UNSUPPORTED;
-    return FOCUS_OK;
-}
-
 focus_status_t check_attn_shapes(int B, int n, int Hq, int Hkv, int d, int window)
 {
     if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || window < 0) return FOCUS_ERR_INVALID_ARG;
@@ -221,12 +214,34 @@ focus_status_t check_attn_shapes(int B, int n, int Hq, int Hkv, int d, int windo
     return FOCUS_OK;
 }
 
-focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int B, int n, int Hq,
-                              int Hkv, int d, int window, float scale, const int32_t *ids,
-                              const int32_t *offsets, const int32_t *pos, const int32_t *inv,
-                              int K, int topk, void *O, float *lse, void *ws, size_t ws_bytes,
-                              int32_t *pair_count, cudaStream_t s, int *launches,
-                              cudaEvent_t q_ready = nullptr)
+// Everything focus_attention_fwd needs before its first launch: validated
+// arguments, the workspace carve-up, the TMA maps and the kernels' launch
+// attributes.  attention_prepare enqueues nothing, so an entry point that
+// calls it before its own first copy or launch keeps the "non-zero status
+// means nothing was enqueued" rule; attention_enqueue then only launches.
+struct AttnPrep {
+    const void *Q, *Kt, *V;
+    const int32_t *ids, *offsets, *pos, *inv;
+    void *O;
+    float *lse;
+    int B, n, Hq, Hkv, d, K, topk;
+    int64_t grid_group, grid_win;
+    __nv_bfloat16 *Kp, *Vp;
+    int32_t *gidp;
+    __half *Opart, *Owin;
+    float2 *Mpart, *Mwin;
+    int2 *tiles;
+    int *ntiles;
+    uint4 *mtab_g, *mtab_w;
+    CUtensorMap mk, mv, wq, wk, wv;
+    AttnLaunch p;     // fields shared by the group and window launches
+};
+
+focus_status_t attention_prepare(const void *Q, const void *Kt, const void *V, int B, int n,
+                                 int Hq, int Hkv, int d, int window, float scale,
+                                 const int32_t *ids, const int32_t *offsets, const int32_t *pos,
+                                 const int32_t *inv, int K, int topk, void *O, float *lse,
+                                 void *ws, size_t ws_bytes, int32_t *pair_count, AttnPrep *ap)
 {
     if (!Q || !Kt || !V || !ids || !offsets || !pos || !inv || !O || !ws)
         return FOCUS_ERR_INVALID_ARG;
@@ -242,37 +257,52 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
     const AttnWs w = attn_ws(B, n, Hq, Hkv, d, K, topk);
     if (ws_bytes < w.total) return FOCUS_ERR_WORKSPACE;
-    const int64_t grid_group = max_tiles(B, n, K, topk) * Hq;
+    ap->grid_group = max_tiles(B, n, K, topk) * Hq;
     const int64_t nqt = (n + 127) / 128;
-    const int64_t grid_win = (int64_t)B * nqt * Hq;
-    if (grid_group >= ((int64_t)1 << 31) || grid_win >= ((int64_t)1 << 31))
+    ap->grid_win = (int64_t)B * nqt * Hq;
+    if (ap->grid_group >= ((int64_t)1 << 31) || ap->grid_win >= ((int64_t)1 << 31))
         return FOCUS_ERR_UNSUPPORTED;
 
     int *status = nullptr;
-    cudaError_t e = status_ptr(&status);
-    if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    // the kernels' shared-memory and register limits, checked before any launch
+    if (attn_preflight(d, K) != cudaSuccess) return FOCUS_ERR_CUDA;
     uint8_t *base = static_cast<uint8_t *>(ws);
-    auto *Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
-    auto *Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
-    auto *gidp = reinterpret_cast<int32_t *>(base + w.gidp);
-    auto *Opart = reinterpret_cast<__half *>(base + w.opart);
-    auto *Mpart = reinterpret_cast<float2 *>(base + w.lpart);
-    auto *Owin = reinterpret_cast<__half *>(base + w.owin);
-    auto *Mwin = reinterpret_cast<float2 *>(base + w.lwin);
-    auto *tiles = reinterpret_cast<int2 *>(base + w.tiles);
-    auto *ntiles = reinterpret_cast<int *>(base + w.ntiles);
-    auto *mtab_g = reinterpret_cast<uint4 *>(base + w.mtab_g);
-    auto *mtab_w = reinterpret_cast<uint4 *>(base + w.mtab_w);
+    ap->Q = Q;
+    ap->Kt = Kt;
+    ap->V = V;
+    ap->ids = ids;
+    ap->offsets = offsets;
+    ap->pos = pos;
+    ap->inv = inv;
+    ap->O = O;
+    ap->lse = lse;
+    ap->B = B;
+    ap->n = n;
+    ap->Hq = Hq;
+    ap->Hkv = Hkv;
+    ap->d = d;
+    ap->K = K;
+    ap->topk = topk;
+    ap->Kp = reinterpret_cast<__nv_bfloat16 *>(base + w.kp);
+    ap->Vp = reinterpret_cast<__nv_bfloat16 *>(base + w.vp);
+    ap->gidp = reinterpret_cast<int32_t *>(base + w.gidp);
+    ap->Opart = reinterpret_cast<__half *>(base + w.opart);
+    ap->Mpart = reinterpret_cast<float2 *>(base + w.lpart);
+    ap->Owin = reinterpret_cast<__half *>(base + w.owin);
+    ap->Mwin = reinterpret_cast<float2 *>(base + w.lwin);
+    ap->tiles = reinterpret_cast<int2 *>(base + w.tiles);
+    ap->ntiles = reinterpret_cast<int *>(base + w.ntiles);
+    ap->mtab_g = reinterpret_cast<uint4 *>(base + w.mtab_g);
+    ap->mtab_w = reinterpret_cast<uint4 *>(base + w.mtab_w);
     const int64_t nk = (int64_t)n * topk;
-
-    CUtensorMap mk, mv, wq, wk, wv;
-    if (!make_map(&mk, Kp, B, nk, Hkv, d) ||
-        !make_map(&mv, Vp, B, nk, Hkv, d) || !make_map(&wq, Q, B, n, Hq, d) ||
-        !make_map(&wk, Kt, B, n, Hkv, d) || !make_map(&wv, V, B, n, Hkv, d))
+    if (!make_map(&ap->mk, ap->Kp, B, nk, Hkv, d) || !make_map(&ap->mv, ap->Vp, B, nk, Hkv, d) ||
+        !make_map(&ap->wq, Q, B, n, Hq, d) || !make_map(&ap->wk, Kt, B, n, Hkv, d) ||
+        !make_map(&ap->wv, V, B, n, Hkv, d))
         return FOCUS_ERR_CUDA;
 
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
-    AttnLaunch p;
+    AttnLaunch &p = ap->p;
     memset(&p, 0, sizeof p);
     p.B = B;
     p.n = n;
@@ -285,63 +315,103 @@ focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int 
     p.topk = topk;
     p.offsets = offsets;
     p.pos = pos;
-    p.tiles = tiles;
-    p.ntiles = ntiles;
+    p.tiles = ap->tiles;
+    p.ntiles = ap->ntiles;
     p.status = status;
     p.pair_count = pair_count;
     // Two query tiles per CTA share the key/value stream: heads 2s, 2s+1 when
     // they share a key/value head, else consecutive query tiles of one head.
     p.pair_heads = (Hq / Hkv) % 2 == 0 ? 1 : 0;
+    return FOCUS_OK;
+}
 
-    if ((e = launch_plan(offsets, B, K, !p.pair_heads, tiles, ntiles, s, launches)) !=
+// Launches the prepared attention: plan, gather, mask tables, group kernel,
+// window kernel, merge.  q_ready (nullable): an event the group kernel waits
+// for (Q may still be arriving from the host while the gather runs).
+focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
+                                 cudaEvent_t q_ready = nullptr)
+{
+    AttnLaunch &p = ap.p;
+    const int B = ap.B, n = ap.n, K = ap.K, topk = ap.topk;
+    cudaError_t e;
+    if ((e = launch_plan(ap.offsets, B, K, !p.pair_heads, ap.tiles, ap.ntiles, s, launches)) !=
         cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(Kt),
-                           static_cast<const __nv_bfloat16 *>(V), pos, ids, B, n, topk, Hkv, d,
-                           Kp, Vp, gidp, s, launches)) != cudaSuccess)
+    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(ap.Kt),
+                           static_cast<const __nv_bfloat16 *>(ap.V), ap.pos, ap.ids, B, n, topk,
+                           ap.Hkv, ap.d, ap.Kp, ap.Vp, ap.gidp, s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if ((e = launch_mask_tables(offsets, gidp, ids, B, n, K, topk, mtab_g, mtab_w, s,
-                                launches)) != cudaSuccess)
+    if ((e = launch_mask_tables(ap.offsets, ap.gidp, ap.ids, B, n, K, topk, ap.mtab_g, ap.mtab_w,
+                                s, launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
 
     // the group kernel copies its query rows from Q itself (tmQ unused)
-    p.tmQ = &wq;
-    p.q = static_cast<const __nv_bfloat16 *>(Q);
-    p.tmK = &mk;
-    p.tmV = &mv;
-    p.rows = (int)nk;
-    p.gids = gidp;
-    p.masks = mtab_g;
+    p.tmQ = &ap.wq;
+    p.q = static_cast<const __nv_bfloat16 *>(ap.Q);
+    p.tmK = &ap.mk;
+    p.tmV = &ap.mv;
+    p.rows = (int)((int64_t)n * topk);
+    p.gids = ap.gidp;
+    p.masks = ap.mtab_g;
     p.mask_tiles = mask_tiles_group(n, K, topk);
-    p.grid = grid_group;
-    p.part_out16 = Opart;
-    p.part_meta_out = Mpart;
-    // (Q may still be arriving from the host while the gather runs)
+    p.grid = ap.grid_group;
+    p.part_out16 = ap.Opart;
+    p.part_meta_out = ap.Mpart;
     if (q_ready && (e = cudaStreamWaitEvent(s, q_ready, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
     if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
-    p.tmQ = &wq;
-    p.tmK = &wk;
-    p.tmV = &wv;
+    p.tmQ = &ap.wq;
+    p.tmK = &ap.wk;
+    p.tmV = &ap.wv;
     p.rows = n;
-    p.gids = ids;
-    p.masks = mtab_w;
+    p.gids = ap.ids;
+    p.masks = ap.mtab_w;
     p.mask_tiles = mask_tiles_window(n);
-    p.grid = grid_win;
-    p.win_out16 = Owin;
-    p.win_meta_out = Mwin;
+    p.grid = ap.grid_win;
+    p.win_out16 = ap.Owin;
+    p.win_meta_out = ap.Mwin;
     if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
-    if ((e = launch_merge(Owin, Mwin, Opart, Mpart, inv, B, n, topk, Hq, d,
-                          static_cast<__nv_bfloat16 *>(O), lse, status, s, launches)) !=
+    if ((e = launch_merge(ap.Owin, ap.Mwin, ap.Opart, ap.Mpart, ap.inv, B, n, topk, ap.Hq, ap.d,
+                          static_cast<__nv_bfloat16 *>(ap.O), ap.lse, p.status, s, launches)) !=
         cudaSuccess)
         return FOCUS_ERR_CUDA;
     return FOCUS_OK;
 }
 
+focus_status_t attention_impl(const void *Q, const void *Kt, const void *V, int B, int n, int Hq,
+                              int Hkv, int d, int window, float scale, const int32_t *ids,
+                              const int32_t *offsets, const int32_t *pos, const int32_t *inv,
+                              int K, int topk, void *O, float *lse, void *ws, size_t ws_bytes,
+                              int32_t *pair_count, cudaStream_t s, int *launches)
+{
+    AttnPrep ap;
+    focus_status_t st = attention_prepare(Q, Kt, V, B, n, Hq, Hkv, d, window, scale, ids, offsets,
+                                          pos, inv, K, topk, O, lse, ws, ws_bytes, pair_count, &ap);
+    if (st) return st;
+    return attention_enqueue(ap, s, launches);
+}
+
 }  // namespace
 
 void set_last_launches(int launches) { g_last_launches = launches; }
+
+// Shared with focus_bucket_static (focus_bucket.cu): one validation and one
+// status mapping for both bucketing entry points.
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+
+int check_bucket(const int32_t *ids, int B, int n, int K, int topk,
+                            const int32_t *offsets, const int32_t *pos, const int32_t *inv)
+{
+    if (!ids || !offsets || !pos || !inv) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(ids) || !aligned16(offsets) || !aligned16(pos) || !aligned16(inv))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 0 || K < 1 || topk < 1 || topk > K) return FOCUS_ERR_INVALID_ARG;
+    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
+    if (K > 1024 || topk > 8 || B > 65535) return FOCUS_ERR_UNSUPPORTED;
+    return FOCUS_OK;
+}
+
 
 }  // namespace focus
 
@@ -366,10 +436,10 @@ const char *focus_version(void) { return "focus-gb300 0.1.0 sm_103a"; }
 
 int focus_last_launch_count(void) { return g_last_launches; }
 
-size_t focus_assign_workspace_size(int hidden, int d_g, int K, int topk)
+size_t focus_assign_workspace_size(int B, int n, int hidden, int d_g, int K, int topk)
 {
-    if (hidden < 1 || d_g < 1 || K < 1 || topk < 1) return 0;
-    return assign_tc_supported(hidden, K, topk) ? assign_ws_bytes(hidden, K) : 0;
+    if (B < 1 || n < 0 || hidden < 1 || d_g < 1 || K < 1 || topk < 1) return 0;
+    return assign_ws_bytes((int64_t)B * n, hidden, d_g, K, topk);
 }
 
 focus_status_t focus_assign(const void *X, const float *Wg, const float *C, int B, int n,
@@ -378,17 +448,17 @@ focus_status_t focus_assign(const void *X, const float *Wg, const float *C, int 
 {
     focus_status_t st = check_assign(X, Wg, C, B, n, hidden, d_g, K, topk, ids, margin);
     if (st) return st;
-    const bool tc = assign_tc_supported(hidden, K, topk);
-    if (tc && (!ws || ws_bytes < assign_ws_bytes(hidden, K))) return FOCUS_ERR_WORKSPACE;
-    if (tc && !aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
+    const size_t need = assign_ws_bytes((int64_t)B * n, hidden, d_g, K, topk);
+    if (need && (!ws || ws_bytes < need)) return FOCUS_ERR_WORKSPACE;
+    if (need && !aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
     int *status = nullptr;
     if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
-    int launches = 0;
     AssignLaunch p{static_cast<const __nv_bfloat16 *>(X), Wg, C, (int64_t)B * n, hidden, d_g, K,
                    topk, ids, margin};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = tc ? launch_assign_tc(p, ws, status, s, &launches)
-                       : launch_assign(p, s, &launches);
+    AssignPlan plan;
+    if (assign_prepare(p, ws, status, &plan) != cudaSuccess) return FOCUS_ERR_CUDA;
+    int launches = 0;
+    cudaError_t e = assign_launch(plan, static_cast<cudaStream_t>(stream), &launches);
     if (e == cudaSuccess) g_last_launches = launches;
     return cuda_status(e);
 }
@@ -482,16 +552,38 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     const float *dWg = Wg, *dC = C;
     void *dO = O;
     float *dL = lse;
-    // host-side validation of the device-side steps before anything is enqueued
-    st = check_assign(host ? base + w.x : X, host ? reinterpret_cast<float *>(base + w.wg) : Wg,
-                      host ? reinterpret_cast<float *>(base + w.c) : C, B, n, hidden, d_g,
-                      num_groups, topk, ids, nullptr);
-    if (st) return st;
-    if (num_groups > 1024 || topk > 8 || (int64_t)B * num_groups > 4096)
-        return FOCUS_ERR_UNSUPPORTED;
-    if (!host && (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
-                  (lse && !aligned16(lse))))
+    if (host) {
+        dX = base + w.x;
+        dWg = reinterpret_cast<const float *>(base + w.wg);
+        dC = reinterpret_cast<const float *>(base + w.c);
+        dQ = base + w.q;
+        dK = base + w.k;
+        dV = base + w.v;
+        dO = base + w.o;
+        dL = lse ? reinterpret_cast<float *>(base + w.lse) : nullptr;
+    } else if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+               (lse && !aligned16(lse))) {
         return FOCUS_ERR_INVALID_ARG;
+    }
+    // Every check of every step, before anything is enqueued: the assignment,
+    // the bucketing, and the attention (shapes, shared memory, grid bounds,
+    // TMA maps, kernel attributes).
+    st = check_assign(dX, dWg, dC, B, n, hidden, d_g, num_groups, topk, ids, nullptr);
+    if (st) return st;
+    st = check_bucket(ids, B, n, num_groups, topk, offsets, pos, inv);
+    if (st) return st;
+    AssignLaunch asg{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden,
+                     d_g, num_groups, topk, ids, nullptr};
+    AssignPlan aplan;
+    int *status = nullptr;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (assign_prepare(asg, base + w.assign, status, &aplan) != cudaSuccess) return FOCUS_ERR_CUDA;
+    const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
+    AttnPrep attn;
+    st = attention_prepare(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
+                           num_groups, topk, dO, dL, base + w.attn, aw.total, nullptr, &attn);
+    if (st) return st;
+
     int launches = 0;
     cudaError_t e = cudaSuccess;
     cudaEvent_t ev_x = nullptr, ev_kv = nullptr, ev_q = nullptr;   // host path only
@@ -508,14 +600,6 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     if (host) {
         const size_t xb = (size_t)B * n * hidden * 2, qb = (size_t)B * n * Hq * d * 2,
                      kb = (size_t)B * n * Hkv * d * 2;
-        dX = base + w.x;
-        dWg = reinterpret_cast<const float *>(base + w.wg);
-        dC = reinterpret_cast<const float *>(base + w.c);
-        dQ = base + w.q;
-        dK = base + w.k;
-        dV = base + w.v;
-        dO = base + w.o;
-        dL = lse ? reinterpret_cast<float *>(base + w.lse) : nullptr;
         // X, W_g and C on `stream`; then K, V and Q on the copy stream while
         // the assignment and bucketing run (the link carries one copy at its
         // full rate, so they follow X rather than share the link with it).
@@ -538,24 +622,12 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
             (e = cudaEventRecord(ev_q, cs)))
             return FOCUS_ERR_CUDA;
     }
-    AssignLaunch ap{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden, d_g,
-                    num_groups, topk, ids, nullptr};
-    if (assign_tc_supported(hidden, num_groups, topk)) {
-        int *status = nullptr;
-        if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
-        e = launch_assign_tc(ap, base + w.assign, status, s, &launches);
-    } else {
-        e = launch_assign(ap, s, &launches);
-    }
-    if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+    if ((e = assign_launch(aplan, s, &launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
     if ((e = launch_bucket(ids, B, n, num_groups, topk, offsets, pos, inv, base + w.bucket, s,
                            &launches)) != cudaSuccess)
         return FOCUS_ERR_CUDA;
     if (host && (e = cudaStreamWaitEvent(s, ev_kv, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
-    const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
-    st = attention_impl(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
-                        num_groups, topk, dO, dL, base + w.attn, aw.total, nullptr, s,
-                        &launches, host ? ev_q : nullptr);
+    st = attention_enqueue(attn, s, &launches, host ? ev_q : nullptr);
     if (st) return st;
     if (host) {
         if ((e = cudaMemcpyAsync(O, dO, (size_t)B * n * Hq * d * 2, cudaMemcpyDeviceToHost, s)))
@@ -626,6 +698,17 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
                                        &launches);
     if (e == cudaSuccess) g_last_launches = launches;
     return cuda_status(e);
+}
+
+focus_status_t focus_set_wait_limit(unsigned long long ns)
+{
+    int *p = nullptr;
+    if (status_ptr(&p) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FOCUS_ERR_CUDA;
+    const unsigned long long v = ns ? ns : 2000000000ull;
+    if (cudaMemcpy(p + 2, &v, sizeof v, cudaMemcpyHostToDevice) != cudaSuccess)
+        return FOCUS_ERR_CUDA;
+    return FOCUS_OK;
 }
 
 focus_status_t focus_get_device_status(int reset)

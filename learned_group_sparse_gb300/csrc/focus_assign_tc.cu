@@ -20,6 +20,7 @@
 
 #include "focus_internal.h"
 #include "focus_ptx.cuh"
+#include "focus_topk.cuh"
 
 namespace focus {
 
@@ -27,13 +28,6 @@ namespace {
 
 constexpr int kTokens = 128;   // tokens per CTA (MMA M)
 constexpr int kHK = 64;        // hidden per pipeline stage (one 128-byte swizzle row)
-constexpr int kMaxSel = 9;     // top-(k+1), k <= 8
-
-// (score, id) order: larger score first, equal scores -> lower id first.
-__device__ __forceinline__ bool better(float s1, int i1, float s2, int i2)
-{
-    return s1 > s2 || (s1 == s2 && i1 < i2);
-}
 
 // M^T split: mhi[c][h], mlo[c][h] for c < Kp (rows >= K are zero).  Block:
 // 32 centroids x 32 hidden rows, both operands staged in shared memory; lane
@@ -87,6 +81,43 @@ struct TcArgs {
 
 __device__ __forceinline__ uint32_t tc_stage_bytes(int Kp) { return 128u * kTokens + 2u * 128u * Kp; }
 
+// Epilogue for top-NS lists (NS = min(k + 1, K)): this thread's row of
+// S_hi + S_lo (the warp-collective TMEM loads are executed by all lanes, even
+// after a timeout).
+template <int NS>
+__device__ __forceinline__ void tc_epilogue(const TcArgs &a, uint32_t tmem, bool ok, int64_t t0)
+{
+    const int warp = threadIdx.x >> 5;
+    const int r = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    TopList<NS> L;
+    L.init();
+    // the first chunk (min(32, K) >= NS candidates) fills the list; the rest
+    // arrive with higher ids than every kept one
+#pragma unroll 1
+    for (int c0 = 0; c0 < a.Kp; c0 += 32) {
+        float v[32], vl[32];
+        tmem_ld32(tmem + lane_off + c0, v);
+        tmem_ld32(tmem + lane_off + a.Kp + c0, vl);
+        if (c0 == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (e < a.K) L.offer_first(v[e] + vl[e], e);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (c0 + e < a.K) L.offer_next(v[e] + vl[e], c0 + e);
+        }
+    }
+    const int64_t tok = t0 + r;
+    if (ok && tok < a.ntok) {
+#pragma unroll
+        for (int q = 0; q < NS; ++q)
+            if (q < a.topk) a.ids[tok * a.topk + q] = L.i[q];
+        if (a.margin) a.margin[tok] = L.gap(min(a.topk + 1, a.K));
+    }
+}
+
 __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                            const __grid_constant__ CUtensorMap tmM,
                                                            const TcArgs a)
@@ -97,8 +128,9 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t stage_bytes = tc_stage_bytes(a.Kp);   // multiple of 1024
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + a.stages * stage_bytes);
-    // bars: full[stages], empty[stages], done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * a.stages + 1);
+    // bars: full[stages], empty[stages], done, drain
+    uint64_t *drain = bars + 2 * a.stages + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * a.stages + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsteps = a.hidden / kHK;
@@ -112,6 +144,7 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
             mbar_init(&bars[a.stages + s], 1);
         }
         mbar_init(&bars[2 * a.stages], 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -130,7 +163,8 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
 
     if (warp == 4) {
         if (lane == 0) {
-            for (int k = 0; k < nsteps; ++k) {
+            int k = 0;
+            for (; k < nsteps; ++k) {
                 const int st = k % a.stages;
                 if (k >= a.stages &&
                     !mbar_wait(&bars[a.stages + st], ((k / a.stages) - 1) & 1, abort_flag, a.status))
@@ -141,6 +175,12 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
                 // [M_hi; M_lo] rows in boxes of up to 256
                 for (int r0 = 0; r0 < 2 * a.Kp; r0 += 256)
                     tma_load_2d(base + 128 * kTokens + 128 * r0, &tmM, &bars[st], k * kHK, r0);
+            }
+            if (*abort_flag) {
+                // let the copies of the last issued stages land
+                const uint64_t deadline = global_timer_ns() + 200000000ull;
+                for (int t = k > a.stages ? k - a.stages : 0; t < k; ++t)
+                    mbar_wait_until(&bars[t % a.stages], (t / a.stages) & 1, deadline);
             }
         }
         __syncwarp();
@@ -170,58 +210,25 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
                 tc_commit(&bars[a.stages + st]);
             }
             if (ok) tc_commit(&bars[2 * a.stages]);
+            // every issued MMA completes before TMEM is released
+            tc_commit(drain);
+            mbar_wait_until(drain, 0, global_timer_ns() + 500000000ull);
         }
         __syncwarp();
     } else {
         // epilogue: thread = token row = TMEM lane
-        const int r = threadIdx.x;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const bool ok = mbar_wait(&bars[2 * a.stages], 0, abort_flag, a.status);
         tc_fence_after();
-        const int nsel = min(a.topk + 1, a.K);
-        float bs[kMaxSel];
-        int bi[kMaxSel];
-#pragma unroll
-        for (int j = 0; j < kMaxSel; ++j) {
-            bs[j] = -CUDART_INF_F;
-            bi[j] = 0x7fffffff;
-        }
-        for (int c0 = 0; c0 < a.Kp; c0 += 32) {
-            float v[32], vl[32];
-            tmem_ld32(tmem + lane_off + c0, v);
-            tmem_ld32(tmem + lane_off + a.Kp + c0, vl);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                int ci = c0 + e;
-                float cv = v[e] + vl[e];
-                if (cv != cv) cv = -CUDART_INF_F;
-                // ids arrive in increasing order, so a tie never displaces a kept id
-                if (ci >= a.K || !better(cv, ci, bs[kMaxSel - 1], bi[kMaxSel - 1])) continue;
-#pragma unroll
-                for (int j = 0; j < kMaxSel; ++j) {
-                    if (better(cv, ci, bs[j], bi[j])) {
-                        const float ts = bs[j];
-                        const int ti = bi[j];
-                        bs[j] = cv;
-                        bi[j] = ci;
-                        cv = ts;
-                        ci = ti;
-                    }
-                }
-            }
-        }
-        const int64_t tok = t0 + r;
-        if (ok && tok < a.ntok) {
-#pragma unroll
-            for (int j = 0; j < kMaxSel; ++j)
-                if (j < a.topk) a.ids[tok * a.topk + j] = bi[j];
-            if (a.margin) {
-                float gap = CUDART_INF_F;
-#pragma unroll
-                for (int j = 1; j < kMaxSel; ++j)
-                    if (j < nsel) gap = fminf(gap, bs[j - 1] - bs[j]);
-                a.margin[tok] = gap;
-            }
+        switch (min(a.topk + 1, a.K)) {
+        case 1: tc_epilogue<1>(a, tmem, ok, t0); break;
+        case 2: tc_epilogue<2>(a, tmem, ok, t0); break;
+        case 3: tc_epilogue<3>(a, tmem, ok, t0); break;
+        case 4: tc_epilogue<4>(a, tmem, ok, t0); break;
+        case 5: tc_epilogue<5>(a, tmem, ok, t0); break;
+        case 6: tc_epilogue<6>(a, tmem, ok, t0); break;
+        case 7: tc_epilogue<7>(a, tmem, ok, t0); break;
+        case 8: tc_epilogue<8>(a, tmem, ok, t0); break;
+        default: tc_epilogue<9>(a, tmem, ok, t0); break;
         }
     }
 
@@ -233,71 +240,122 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
     }
 }
 
-}  // namespace
-
 int assign_tc_kp(int K) { return (K + 15) / 16 * 16; }
+
+}  // namespace
 
 bool assign_tc_supported(int hidden, int K, int topk)
 {
     return K <= 256 && hidden % kHK == 0 && topk <= 8;
 }
 
-size_t assign_ws_bytes(int hidden, int K)
+size_t assign_tc_ws_bytes(int hidden, int K)
 {
     if (K > 256) return 0;
     return 2 * (size_t)assign_tc_kp(K) * hidden * sizeof(__nv_bfloat16) + 256;
 }
 
-cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaStream_t s,
-                             int *launches)
+cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan)
 {
     const int Kp = assign_tc_kp(p.K);
-    __nv_bfloat16 *mhi = static_cast<__nv_bfloat16 *>(ws);   // [M_hi; M_lo]: [2 Kp, hidden]
+    plan->path = 1;
+    plan->p = p;
+    plan->status = status;
+    plan->Kp = Kp;
+    plan->mhi = ws;   // [M_hi; M_lo]: [2 Kp, hidden]
+    const uint32_t stage = 128u * kTokens + 2u * 128u * Kp;
+    // Stages within ~110 KB so that two CTAs share an SM: one streams X while
+    // the other runs its top-k epilogue.
+    int st = (int)(113u * 1024u / stage);
+    plan->stages = st > 4 ? 4 : (st < 2 ? 2 : st);
+    plan->smem = (size_t)plan->stages * stage + (2 * plan->stages + 2) * 8 + 16 + 1024;
+    plan->smem2 = sizeof(float) * ((size_t)32 * p.dg + (size_t)32 * (p.dg + 1));
+    plan->grid = (p.ntok + kTokens - 1) / kTokens;
+    if (p.ntok > 0 &&
+        (!make_map_2d(&plan->map[0], p.X, (uint64_t)p.hidden, (uint64_t)p.ntok, kHK, kTokens,
+                      false) ||
+         !make_map_2d(&plan->map[1], plan->mhi, (uint64_t)p.hidden, (uint64_t)(2 * Kp), kHK,
+                      (uint32_t)(2 * Kp <= 256 ? 2 * Kp : 256), false)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(assign_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)plan->smem2);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)plan->smem);
+}
+
+cudaError_t assign_tc_launch(const AssignPlan &plan, cudaStream_t s, int *launches)
+{
+    const AssignLaunch &p = plan.p;
+    const int Kp = plan.Kp;
+    __nv_bfloat16 *mhi = static_cast<__nv_bfloat16 *>(plan.mhi);
     __nv_bfloat16 *mlo = mhi + (size_t)Kp * p.hidden;
     {
         const dim3 grid((unsigned)((p.hidden + 31) / 32), (unsigned)((Kp + 31) / 32));
-        const size_t smem = sizeof(float) * ((size_t)32 * p.dg + (size_t)32 * (p.dg + 1));
-        cudaError_t e = cudaFuncSetAttribute(assign_prep_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
         prof_begin("assign_prep", s);
-        e = launch_pdl(assign_prep_kernel, grid, dim3(256), smem, s, p.Wg, p.C, p.hidden, p.dg, p.K,
-                       Kp, mhi, mlo);
+        cudaError_t e = launch_pdl(assign_prep_kernel, grid, dim3(256), plan.smem2, s, p.Wg, p.C,
+                                   p.hidden, p.dg, p.K, Kp, mhi, mlo);
         prof_end(s);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
-    if (p.ntok == 0) return cudaGetLastError();
-    CUtensorMap mx, mm;
-    if (!make_map_2d_bf16(&mx, p.X, (uint64_t)p.hidden, (uint64_t)p.ntok, kHK, kTokens) ||
-        !make_map_2d_bf16(&mm, mhi, (uint64_t)p.hidden, (uint64_t)(2 * Kp), kHK,
-                          (uint32_t)(2 * Kp <= 256 ? 2 * Kp : 256)))
-        return cudaErrorInvalidValue;
+    if (p.ntok == 0) return cudaSuccess;
     TcArgs a;
     a.ntok = p.ntok;
     a.hidden = p.hidden;
     a.K = p.K;
     a.Kp = Kp;
     a.topk = p.topk;
-    const uint32_t stage = 128u * kTokens + 2u * 128u * Kp;
-    // Stages within ~110 KB so that two CTAs share an SM: one streams X while
-    // the other runs its top-k epilogue.
-    a.stages = (int)(113u * 1024u / stage);
-    if (a.stages > 4) a.stages = 4;
-    if (a.stages < 2) a.stages = 2;
+    a.stages = plan.stages;
     a.ids = p.ids;
     a.margin = p.margin;
-    a.status = status;
-    const size_t smem = (size_t)a.stages * stage + (2 * a.stages + 1) * 8 + 16 + 1024;
-    cudaError_t e = cudaFuncSetAttribute(assign_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int64_t blocks = (p.ntok + kTokens - 1) / kTokens;
+    a.status = plan.status;
     prof_begin("assign", s);
-    e = launch_pdl(assign_tc_kernel, dim3((unsigned)blocks), dim3(192), smem, s, mx, mm, a);
+    cudaError_t e = launch_pdl(assign_tc_kernel, dim3((unsigned)plan.grid), dim3(192), plan.smem,
+                               s, plan.map[0], plan.map[1], a);
     prof_end(s);
     *launches += 1;
     return e;
+}
+
+// ----------------------------------------------------------- path choice
+int assign_path(int hidden, int dg, int K, int topk)
+{
+    if (assign_z_supported(hidden, dg, K, topk)) return 2;
+    if (assign_tc_supported(hidden, K, topk)) return 1;
+    return 0;
+}
+
+size_t assign_ws_bytes(int64_t ntok, int hidden, int dg, int K, int topk)
+{
+    switch (assign_path(hidden, dg, K, topk)) {
+    case 2: return assign_z_ws_bytes(ntok, hidden, dg, K);
+    case 1: return assign_tc_ws_bytes(hidden, K);
+    default: return 0;
+    }
+}
+
+cudaError_t assign_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan)
+{
+    switch (assign_path(p.hidden, p.dg, p.K, p.topk)) {
+    case 2: return assign_z_prepare(p, ws, status, plan);
+    case 1: return assign_tc_prepare(p, ws, status, plan);
+    default:
+        plan->path = 0;
+        plan->p = p;
+        plan->status = status;
+        return cudaSuccess;
+    }
+}
+
+cudaError_t assign_launch(const AssignPlan &plan, cudaStream_t s, int *launches)
+{
+    switch (plan.path) {
+    case 2: return assign_z_launch(plan, s, launches);
+    case 1: return assign_tc_launch(plan, s, launches);
+    default: return launch_assign(plan.p, s, launches);
+    }
 }
 
 }  // namespace focus

@@ -133,7 +133,7 @@ constexpr uint32_t kOStride = 128;        // TMEM columns from O_0 to O_1
 enum {
     B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_VFULL = 6, B_KEMPTY = 8, B_VEMPTY = 10,
     B_SFULL = 12, B_PFULL = 14, B_ODONE = 16, B_META = 18, B_IFULL = 20, B_IEMPTY = 22,
-    kNumBars = 24
+    B_DRAIN = 24, kNumBars = 25
 };
 
 template <int D>
@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 8 softmax warps + MMA thread (+ the two Q-loader warps of kGroup)
             mbar_init(&bars[B_IEMPTY + s], MODE == kGroup ? 11 : 9);
         }
+        mbar_init(&bars[B_DRAIN], 1);
         long long *trz = reinterpret_cast<long long *>(sm + L::kTrace);
         for (int i = 0; i < kTraceSlots; ++i) trz[i] = 0;
         *abort_flag = 0;
@@ -662,6 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tr[TR_M_TOTAL] = clock64() - t_start;
                     trace_flush(tr, a.trace + (int64_t)blockIdx.x * kTraceSlots, 8, 16);
                 }
+                // Every MMA this thread issued completes before TMEM is released
+                // (already so on the normal path; needed when a wait gave up).
+                tc_commit(&bars[B_DRAIN]);
+                mbar_wait_until(&bars[B_DRAIN], 0, global_timer_ns() + 500000000ull);
             }
             __syncwarp();
         } else if (MODE == kGroup) {
@@ -693,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int row = q0 + lane + 32 * i;
                     tok[i] = row < qend ? a.pos[(int64_t)wb * a.rows + row] : -1;
+                    if ((unsigned)tok[i] >= (unsigned)a.n) tok[i] = -1;   // never read past Q
                 }
                 if (iq >= 1 && lane == 0)
                     ok = mbar_wait(&bars[B_QEMPTY + h], (iq - 1) & 1, abort_flag, a.status);
@@ -737,6 +743,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = k & 1;
             ok = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
                              tr[TR_S_IFULL]);
+            // a warp leaves together: its lanes meet warp-collective instructions
+            // (tcgen05.ld/st, votes) next, so one lane's timeout ends them all
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const int *wi = ring_slot<D>(sm, a.K, slot);   // the fields of Item
             const int wb = wi[0], wg = wi[1], kv_lo = wi[3], nkv = wi[4];
@@ -759,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (MODE == kGroup && qvalid && a.pair_count)
                 qi = a.pos[(int64_t)wb * a.rows + prow];
+            const bool count_ok = (unsigned)qi < (unsigned)a.n;
 
             float m_ref = -CUDART_INF_F;   // reference max (base 2) applied to O_h and l
             float l = 0.f;                 // row sum
@@ -802,6 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      tr[TR_S_SFULL]);
                 ++ns;
                 if (ok && MODE != kDense && !early) ok = fetch_ex();
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
                 long long tt = trc ? clock64() : 0;
@@ -917,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  tr[TR_S_ODONE]);
                 ++nod;
                 tc_fence_after();
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             }
             long long te = trc ? clock64() : 0;
@@ -1004,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (trc) tr[TR_E_STORE] += clock64() - te;
-            if (qvalid && a.pair_count && hd == 0)
+            if (qvalid && a.pair_count && hd == 0 && count_ok)
                 atomicAdd(&a.pair_count[(int64_t)wb * a.n + qi], cnt);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_IEMPTY + slot]);     // ring slot no longer read

@@ -12,20 +12,38 @@ uint32_t attn_smem_bytes(int mode, int K)
     return mode == kDense ? AttnSmem<D>::bytes(0) : AttnSmem<D>::bytes(K);
 }
 
+// The launch attributes of one kernel instance for K groups: its dynamic
+// shared memory, and a check that the warpgroups' register shares after
+// setmaxnreg fit in what the block is launched with (otherwise the increase
+// would wait forever).  Enqueues nothing.
+template <int MODE, int D>
+cudaError_t attn_preflight_impl(int K)
+{
+    auto kern = focus_attn_kernel<MODE, D>;
+    const uint32_t smem = attn_smem_bytes<D>(MODE, K);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if ((int64_t)fa.numRegs * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
+        return cudaErrorInvalidConfiguration;
+    return cudaSuccess;
+}
+
+template <int MODE>
+cudaError_t attn_preflight_mode(int d, int K)
+{
+    return d == 64 ? attn_preflight_impl<MODE, 64>(K) : attn_preflight_impl<MODE, 128>(K);
+}
+
 template <int MODE, int D>
 cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
 {
     if (p.grid <= 0) return cudaSuccess;
     auto kern = focus_attn_kernel<MODE, D>;
     const uint32_t smem = attn_smem_bytes<D>(MODE, p.K);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = attn_preflight_impl<MODE, D>(p.K);
     if (e != cudaSuccess) return e;
-    // The warpgroups' register shares after setmaxnreg must fit in what the
-    // block is launched with, or the increase would wait forever.
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if ((int64_t)fa.numRegs * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
-        return cudaErrorInvalidConfiguration;
     AttnArgs a;
     a.B = p.B;
     a.n = p.n;

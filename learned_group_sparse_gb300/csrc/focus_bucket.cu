@@ -310,12 +310,20 @@ __global__ void __launch_bounds__(256) gather_kernel(
     for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < total;
          row += warps) {
         const int64_t b = row / nk;
-        const int64_t src = b * n + pos[row];
+        const int p = pos[row];
+        uint4 *kd = Kp + row * kvunits;
+        uint4 *vd = Vp + row * kvunits;
+        if ((unsigned)p >= (unsigned)n) {
+            // not a token (ids outside [0, K) leave list entries unwritten):
+            // an empty row that no group reads, never an out-of-range load
+            if (lane < topk) gidp[row * topk + lane] = -1;
+            for (int u = lane; u < kvunits; u += 32) kd[u] = vd[u] = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const int64_t src = b * n + p;
         if (lane < topk) gidp[row * topk + lane] = ids[src * topk + lane];
         const uint4 *k = K + src * kvunits;
         const uint4 *v = V + src * kvunits;
-        uint4 *kd = Kp + row * kvunits;
-        uint4 *vd = Vp + row * kvunits;
         for (int u = lane; u < kvunits; u += 32) {
             kd[u] = k[u];
             vd[u] = v[u];
@@ -538,19 +546,17 @@ extern "C" int focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
                                    int32_t *offsets, int32_t *pos, int32_t *inv, void *stream)
 {
     using namespace focus;
-    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!ids || !offsets || !pos || !inv) return 1;                       // INVALID_ARG
-    if (!al16(ids) || !al16(offsets) || !al16(pos) || !al16(inv)) return 1;
-    if (B < 1 || n < 0 || K < 1 || topk < 1 || topk > K) return 1;
-    if ((int64_t)B * n * topk >= ((int64_t)1 << 31)) return 2;             // UNSUPPORTED
-    if (K > 1024 || topk > 8 || B > 65535) return 2;
-    if (bucket_ws_bytes(B, n, K, topk) > kStaticScratchInts * sizeof(int32_t)) return 2;
+    // the same validation and status codes as focus_bucket
+    int st = check_bucket(ids, B, n, K, topk, offsets, pos, inv);
+    if (st) return st;
+    if (bucket_ws_bytes(B, n, K, topk) > kStaticScratchInts * sizeof(int32_t))
+        return 2;   // FOCUS_ERR_UNSUPPORTED: more scratch than the fixed array holds
     int32_t *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess) return 4;               // CUDA_ERROR
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return cuda_status(e);
     int launches = 0;
-    cudaError_t e = launch_bucket(ids, B, n, K, topk, offsets, pos, inv, scratch,
-                                  static_cast<cudaStream_t>(stream), &launches);
-    if (e != cudaSuccess) return 4;
-    set_last_launches(launches);
-    return 0;
+    e = launch_bucket(ids, B, n, K, topk, offsets, pos, inv, scratch,
+                      static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) set_last_launches(launches);
+    return cuda_status(e);
 }

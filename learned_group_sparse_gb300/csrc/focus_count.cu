@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) count_kernel(
             const int gs = offsets[b * (K + 1) + g];
             for (int rr = gs + lane; rr <= r; rr += 32) {
                 const int j = pos[b * nk + rr];
+                if ((unsigned)j >= (unsigned)n) continue;
                 const int32_t *gj = ids + (b * n + j) * topk;
                 bool owned = true;
                 for (int x = 0; x < topk && owned; ++x) {

@@ -65,18 +65,51 @@ struct AssignLaunch {
 };
 // SIMT fp32 path (any K <= 1024).
 cudaError_t launch_assign(const AssignLaunch &p, cudaStream_t s, int *launches);
-// Tensor-core path (K <= 256, hidden % 64 == 0); ws holds M = W_g C^T split
-// into two bf16 parts (assign_ws_bytes).
+// 2-D bf16 (or fp16) tensor map [outer, inner] (inner contiguous), box
+// {box_inner, box_outer}, 128-byte swizzle.
+bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, bool f16);
+
+// A prepared assignment: the path, its TMA maps and launch sizes.
+// assign_prepare validates nothing that focus_assign's host checks cover, and
+// enqueues nothing; assign_launch enqueues the kernels.
+//   path 0: SIMT fp32 kernel, (X W_g) C^T;
+//   path 1: tensor cores, X (W_g C^T) with W_g C^T split into bf16 hi + lo;
+//   path 2: tensor cores in the order (X W_g) C^T, for more centroids than
+//           centroid dimensions (focus_assign_z.cu).
+struct AssignPlan {
+    CUtensorMap map[4];
+    AssignLaunch p;
+    int path;
+    int *status;
+    int Kp, dgp, stages, stages2;
+    size_t smem, smem2;
+    int64_t grid, grid2;
+    void *mhi;                 // path 1: [M_hi; M_lo]
+    void *wt, *ch, *z;         // path 2: W_g^T hi/lo, C hi/lo, Z hi/lo
+    float *zscale;             // path 2: per-token scale of Z
+};
+int assign_path(int hidden, int dg, int K, int topk);
+size_t assign_ws_bytes(int64_t ntok, int hidden, int dg, int K, int topk);
+cudaError_t assign_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
+// the paths' own halves of the above
 bool assign_tc_supported(int hidden, int K, int topk);
-size_t assign_ws_bytes(int hidden, int K);
-cudaError_t launch_assign_tc(const AssignLaunch &p, void *ws, int *status, cudaStream_t s,
-                             int *launches);
-// 2-D bf16 tensor map [outer, inner] (inner contiguous), box {box_inner, box_outer},
-// 128-byte swizzle.
-bool make_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-                      uint32_t box_inner, uint32_t box_outer);
+cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_tc_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
+size_t assign_tc_ws_bytes(int hidden, int K);
+int assign_z_dgp(int dg);
+bool assign_z_supported(int hidden, int dg, int K, int topk);
+size_t assign_z_ws_bytes(int64_t ntok, int hidden, int dg, int K);
+cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_z_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
 
 // ---- bucket: histogram per chunk, scan, offsets, stable scatter
+// Host-side validation of a bucketing call (a focus.h status code; nothing
+// is enqueued) and the status of a CUDA runtime result.
+int check_bucket(const int32_t *ids, int B, int n, int K, int topk, const int32_t *offsets,
+                 const int32_t *pos, const int32_t *inv);
+int cuda_status(cudaError_t e);
 constexpr int kBucketChunk = 4096;   // (token, slot) entries per chunk
 size_t bucket_ws_bytes(int B, int n, int K, int topk);
 cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int32_t *offsets,
@@ -139,6 +172,10 @@ cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __ha
                          int Hq, int d, __nv_bfloat16 *O, float *lse, int *status,
                          cudaStream_t s, int *launches);
 cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
+// Sets the launch attributes of the group and window kernels for (d, K) and
+// checks their register split; enqueues nothing.
+cudaError_t attn_preflight(int d, int K);
+cudaError_t attn_window_preflight(int d, int K);
 // Shared memory the group and window kernels need for (d, K).
 size_t attn_smem_needed(int d, int K);
 constexpr size_t kMaxSmemPerBlock = 232448;   // 227 KB opt-in limit of sm_103a

@@ -211,15 +211,24 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
             }
         }
     };
+    // thread 0: parity of the copies in flight into buffer b (-1: none)
+    int pending[2] = {-1, -1};
     int64_t tok = blockIdx.x;
-    if (threadIdx.x == 0 && tok < ntok) issue(tok, 0);
+    if (threadIdx.x == 0 && tok < ntok) {
+        issue(tok, 0);
+        pending[0] = 0;
+    }
     for (int k = 0; tok < ntok; ++k, tok += gridDim.x) {
         const int b = k & 1;
         const int64_t next = tok + gridDim.x;
-        if (threadIdx.x == 0 && next < ntok) issue(next, b ^ 1);
+        if (threadIdx.x == 0 && next < ntok) {
+            issue(next, b ^ 1);
+            pending[b ^ 1] = ((k + 1) >> 1) & 1;
+        }
         // every thread waits for this token's copies (bounded); the block
         // leaves together if any wait gave up
         if (!__syncthreads_and(mbar_wait(&bar[b], (k >> 1) & 1, &abort_flag, status))) break;
+        pending[b] = -1;
         const uint8_t *base = buf0 + (size_t)b * tokb;
         const float2 *meta = reinterpret_cast<const float2 *>(base + (size_t)np * rowb);
         const int64_t bb = tok / n;
@@ -270,11 +279,9 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
     }
     // A block that gave up lets its copies in flight land before it exits.
     if (abort_flag && threadIdx.x == 0) {
-        const uint64_t t0 = global_timer_ns();
+        const uint64_t deadline = global_timer_ns() + 100000000ull;
         for (int b = 0; b < 2; ++b)
-            while (!mbar_try_wait(&bar[b], 0) && !mbar_try_wait(&bar[b], 1) &&
-                   global_timer_ns() - t0 < 100000000ull) {
-            }
+            if (pending[b] >= 0) mbar_wait_until(&bar[b], (uint32_t)pending[b], deadline);
     }
 }
 

@@ -8,9 +8,20 @@
 
 namespace focus {
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds of %globaltimer, unless
+// the device status record (below) holds another limit.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr int kDeviceTimeout = 5;                   // FOCUS_ERR_TIMEOUT
+
+// The kernels receive `int *status`, the first word of the library's device
+// status record {int code; int reserved; uint64 wait_limit_ns}: a bounded
+// wait that runs out writes FOCUS_ERR_TIMEOUT to code, and reads its limit
+// from wait_limit_ns (focus_set_wait_limit changes it for tests).
+__device__ __forceinline__ uint64_t wait_limit_ns(const int *status)
+{
+    return status ? *reinterpret_cast<const volatile unsigned long long *>(status + 2)
+                  : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -68,25 +79,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// when *abort is set by another thread of the CTA or after kWaitLimitNs; in
-// the latter case it sets *abort and records the timeout in *status.
-// Returns false if it gave up.
+// when *abort is set by another thread of the CTA or after the status
+// record's wait limit; in the latter case it sets *abort and records the
+// timeout in *status.  Returns false if it gave up.  The clock is read every
+// 64 polls, or after every poll under a limit below a millisecond.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint64_t lim = wait_limit_ns(status);
+    const uint32_t every = lim < 1000000ull ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & every) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > lim) {
                 *abort = 1;
                 if (status) atomicExch(status, kDeviceTimeout);
                 return false;
             }
         }
     }
+}
+
+// The quiet wait of an abort path: waits for the phase of `bar` with the given
+// parity until `deadline` (%globaltimer ns), without flags or status; returns
+// whether it completed.  Used to let copies or MMAs already in flight land
+// before a CTA that gave up releases its shared memory or TMEM.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t *bar, uint32_t parity, uint64_t deadline)
+{
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() > deadline) return false;
+    return true;
 }
 
 // mbar_wait that adds the SM cycles spent waiting to `acc` when `on`.
@@ -250,6 +275,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
            | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B (both
+// K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
+{
+    return (1u << 4)                                  // D format: f32
+           | ((uint32_t)(N >> 3) << 17)               // N / 8 (A, B format 0: f16)
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 

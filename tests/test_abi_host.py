@@ -52,9 +52,13 @@ def test_status_strings_and_version(lib):
 
 def test_assign_validation(lib):
     f = lib.focus_assign
-    need = fg.focus_assign_workspace_size(64, 16, 8, 2)
+    need = fg.focus_assign_workspace_size(1, 8, 64, 16, 8, 2)
     assert need > 0
-    assert fg.focus_assign_workspace_size(64, 16, 300, 2) == 0        # K > 256: fp32 kernel
+    assert fg.focus_assign_workspace_size(1, 8, 64, 16, 300, 2) == 0   # K > 256: fp32 kernel
+    # more centroids than centroid dimensions: Z = X W_g is kept per token
+    z1 = fg.focus_assign_workspace_size(1, 1000, 64, 64, 256, 2)
+    z2 = fg.focus_assign_workspace_size(2, 1000, 64, 64, 256, 2)
+    assert z2 - z1 >= 1000 * (2 * 64 * 2 + 4)      # fp16 hi + lo of 64 values, a scale
 
     def call(X=P, hid=64, dg=16, K=8, topk=2, ws=P2, nbytes=need):
         #        X  Wg C  B  n  hidden dg  K  topk ids margin ws  bytes  stream

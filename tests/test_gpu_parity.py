@@ -131,7 +131,14 @@ def test_bucket_matches_oracle_exactly(B, n, K, topk):
                                synth.small(n=300, hidden=512, dg=200, K=40, topk=4, seed=13),
                                synth.small(n=200, hidden=128, dg=16, K=1000, topk=8,
                                            x_kind="normal", seed=14),
-                               synth.small(n=100, hidden=64, dg=32, K=1, topk=1, seed=15)],
+                               synth.small(n=100, hidden=64, dg=32, K=1, topk=1, seed=15),
+                               # more centroids than centroid dimensions: (X W_g) C^T
+                               synth.small(B=2, n=1000, hidden=1024, dg=64, K=100, topk=4,
+                                           seed=16),
+                               synth.small(n=333, hidden=192, dg=20, K=80, topk=3,
+                                           x_kind="normal", seed=17),
+                               synth.small(n=513, hidden=640, dg=128, K=144, topk=8, seed=18),
+                               synth.small(n=1, hidden=256, dg=64, K=128, topk=2, seed=19)],
                          ids=lambda w: w.label)
 def test_assign_matches_oracle(w):
     Wg, C = synth.make_params(w, "cuda")
