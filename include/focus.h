@@ -161,9 +161,11 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  * Arithmetic: bf16 operands, fp32 accumulation and softmax, probabilities
  * rounded to bf16 for the P.V product, partial outputs kept in fp16 with a
  * power-of-two scale per row (11-bit significand at any magnitude).
- * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= K <= 1024, 1 <= topk <= 8,
- *            B * K <= 4096 (the kernels' shared memory holds two key
- *            tiles' group bitmaps, 32 K bytes, next to the Q/K/V tiles).
+ * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= topk <= 8,
+ *            1 <= K <= 1024 (the kernels' shared memory holds the group
+ *            bitmaps of two key tiles, 16 K bytes each, next to the Q/K/V
+ *            tiles), B * K <= 4096 (the work list is sorted by one
+ *            block with every group of every batch in shared memory).
  *            Otherwise FOCUS_ERR_UNSUPPORTED.
  */
 size_t focus_attention_workspace_size(int B, int n, int Hq, int Hkv, int d,
@@ -250,14 +252,16 @@ focus_status_t focus_attention_fwd_counted(const void *Q, const void *K, const v
 focus_status_t focus_get_device_status(int reset);
 
 /*
- * Sets the limit of the kernels' bounded device-side waits on the current
- * device, in nanoseconds of the GPU's global timer (0 restores the default,
- * 2 s).  A testing aid: a tiny limit makes the waits of the next launches run
- * out, so that their error path (the kernel finishes early, lets the copies
- * and tensor-core operations it issued land, and records FOCUS_ERR_TIMEOUT in
- * the device status word) can be exercised without faulting or hanging the
- * GPU.  Outputs of launches whose waits ran out are undefined.  Synchronises
- * the device; not for use while kernels of this library are in flight.
+ * Sets the limit of the bounded device-side waits of the assignment and merge
+ * kernels for the launches this library enqueues after the call (any host
+ * thread, any device), in nanoseconds of the GPU's global timer; 0 restores
+ * the default, 2 s.  (The attention kernels keep the fixed 2 s limit: a run-
+ * time limit in their waits measured 1.6 % slower.)  A testing aid: a tiny
+ * limit makes the waits of the next launches run out, so
+ * that their error path (the kernel finishes early, lets the copies and
+ * tensor-core operations it issued land, and records FOCUS_ERR_TIMEOUT in the
+ * device status word) can be exercised without faulting or hanging the GPU.
+ * Outputs of launches whose waits ran out are undefined.
  */
 focus_status_t focus_set_wait_limit(unsigned long long ns);
 

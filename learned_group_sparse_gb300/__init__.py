@@ -127,8 +127,9 @@ def focus_get_device_status(reset: bool = False) -> int:
 
 
 def focus_set_wait_limit(ns: int = 0) -> None:
-    """Limit of the kernels' bounded device-side waits in ns (0: the default,
-    2 s).  A testing aid for the timeout path; synchronises the device."""
+    """Limit in ns of the bounded device-side waits of the launches that
+    follow (0: the default, 2 s); the attention kernels keep the default.
+    A testing aid for the timeout path."""
     _check("focus_set_wait_limit", library().focus_set_wait_limit(int(ns)))
 
 

@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/focus.h"
@@ -18,14 +19,12 @@ namespace {
 
 thread_local int g_last_launches = 0;
 
-// Device status record: code (set by a kernel whose bounded wait ran out),
-// then the wait limit the kernels' bounded waits use (see focus_ptx.cuh).
-struct DeviceStatus {
-    int code;
-    int reserved;
-    unsigned long long wait_limit_ns;
-};
-__device__ DeviceStatus g_device_status = {0, 0, 2000000000ull};
+// Device status word: set by a kernel whose bounded wait ran out.
+__device__ int g_device_status = 0;
+
+// Limit of the kernels' bounded waits for the launches that follow
+// (focus_set_wait_limit); it travels in each launch's arguments.
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 constexpr int kMaxDevices = 64;
 int *g_status_addr[kMaxDevices] = {nullptr};
@@ -42,10 +41,18 @@ cudaError_t status_ptr(int **out)
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_device_status);
         if (e != cudaSuccess) return e;
-        g_status_addr[dev] = &static_cast<DeviceStatus *>(p)->code;
+        g_status_addr[dev] = static_cast<int *>(p);
     }
     *out = g_status_addr[dev];
     return cudaSuccess;
+}
+
+// The bounded-wait control of a launch on the current device.
+cudaError_t wait_ctl(WaitCtl *out)
+{
+    cudaError_t e = status_ptr(&out->status);
+    out->limit_ns = g_wait_limit_ns.load();
+    return e;
 }
 
 // The second stream of focus_prefill's host path (input copies that overlap
@@ -263,8 +270,8 @@ focus_status_t attention_prepare(const void *Q, const void *Kt, const void *V, i
     if (ap->grid_group >= ((int64_t)1 << 31) || ap->grid_win >= ((int64_t)1 << 31))
         return FOCUS_ERR_UNSUPPORTED;
 
-    int *status = nullptr;
-    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    WaitCtl wc;
+    if (wait_ctl(&wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     // the kernels' shared-memory and register limits, checked before any launch
     if (attn_preflight(d, K) != cudaSuccess) return FOCUS_ERR_CUDA;
     uint8_t *base = static_cast<uint8_t *>(ws);
@@ -317,7 +324,7 @@ focus_status_t attention_prepare(const void *Q, const void *Kt, const void *V, i
     p.pos = pos;
     p.tiles = ap->tiles;
     p.ntiles = ap->ntiles;
-    p.status = status;
+    p.wc = wc;
     p.pair_count = pair_count;
     // Two query tiles per CTA share the key/value stream: heads 2s, 2s+1 when
     // they share a key/value head, else consecutive query tiles of one head.
@@ -373,7 +380,7 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
 
     if ((e = launch_merge(ap.Owin, ap.Mwin, ap.Opart, ap.Mpart, ap.inv, B, n, topk, ap.Hq, ap.d,
-                          static_cast<__nv_bfloat16 *>(ap.O), ap.lse, p.status, s, launches)) !=
+                          static_cast<__nv_bfloat16 *>(ap.O), ap.lse, p.wc, s, launches)) !=
         cudaSuccess)
         return FOCUS_ERR_CUDA;
     return FOCUS_OK;
@@ -451,12 +458,12 @@ focus_status_t focus_assign(const void *X, const float *Wg, const float *C, int 
     const size_t need = assign_ws_bytes((int64_t)B * n, hidden, d_g, K, topk);
     if (need && (!ws || ws_bytes < need)) return FOCUS_ERR_WORKSPACE;
     if (need && !aligned16(ws)) return FOCUS_ERR_INVALID_ARG;
-    int *status = nullptr;
-    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    WaitCtl wc;
+    if (wait_ctl(&wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     AssignLaunch p{static_cast<const __nv_bfloat16 *>(X), Wg, C, (int64_t)B * n, hidden, d_g, K,
                    topk, ids, margin};
     AssignPlan plan;
-    if (assign_prepare(p, ws, status, &plan) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (assign_prepare(p, ws, wc, &plan) != cudaSuccess) return FOCUS_ERR_CUDA;
     int launches = 0;
     cudaError_t e = assign_launch(plan, static_cast<cudaStream_t>(stream), &launches);
     if (e == cudaSuccess) g_last_launches = launches;
@@ -575,9 +582,9 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C, con
     AssignLaunch asg{static_cast<const __nv_bfloat16 *>(dX), dWg, dC, (int64_t)B * n, hidden,
                      d_g, num_groups, topk, ids, nullptr};
     AssignPlan aplan;
-    int *status = nullptr;
-    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
-    if (assign_prepare(asg, base + w.assign, status, &aplan) != cudaSuccess) return FOCUS_ERR_CUDA;
+    WaitCtl wc;
+    if (wait_ctl(&wc) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (assign_prepare(asg, base + w.assign, wc, &aplan) != cudaSuccess) return FOCUS_ERR_CUDA;
     const AttnWs aw = attn_ws(B, n, Hq, Hkv, d, num_groups, topk);
     AttnPrep attn;
     st = attention_prepare(dQ, dK, dV, B, n, Hq, Hkv, d, window, scale, ids, offsets, pos, inv,
@@ -651,8 +658,8 @@ focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *
     if (st) return st;
     const int64_t grid = (int64_t)B * ((n + 127) / 128) * Hq;
     if (grid >= ((int64_t)1 << 31)) return FOCUS_ERR_UNSUPPORTED;
-    int *status = nullptr;
-    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    WaitCtl wc;
+    if (wait_ctl(&wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, Q, B, n, Hq, d) || !make_map(&mk, K, B, n, Hkv, d) ||
         !make_map(&mv, V, B, n, Hkv, d))
@@ -677,7 +684,7 @@ focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *
     p.grid = grid;
     p.out = static_cast<__nv_bfloat16 *>(O);
     p.lse = lse;
-    p.status = status;
+    p.wc = wc;
     int launches = 0;
     cudaError_t e = launch_attn_dense(p, static_cast<cudaStream_t>(stream), &launches);
     if (e == cudaSuccess) g_last_launches = launches;
@@ -702,12 +709,7 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
 
 focus_status_t focus_set_wait_limit(unsigned long long ns)
 {
-    int *p = nullptr;
-    if (status_ptr(&p) != cudaSuccess) return FOCUS_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return FOCUS_ERR_CUDA;
-    const unsigned long long v = ns ? ns : 2000000000ull;
-    if (cudaMemcpy(p + 2, &v, sizeof v, cudaMemcpyHostToDevice) != cudaSuccess)
-        return FOCUS_ERR_CUDA;
+    g_wait_limit_ns.store(ns ? ns : 2000000000ull);
     return FOCUS_OK;
 }
 

@@ -76,7 +76,7 @@ struct TcArgs {
     int hidden, K, Kp, topk, stages;
     int32_t *ids;
     float *margin;
-    int *status;
+    WaitCtl wc;
 };
 
 __device__ __forceinline__ uint32_t tc_stage_bytes(int Kp) { return 128u * kTokens + 2u * 128u * Kp; }
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
             for (; k < nsteps; ++k) {
                 const int st = k % a.stages;
                 if (k >= a.stages &&
-                    !mbar_wait(&bars[a.stages + st], ((k / a.stages) - 1) & 1, abort_flag, a.status))
+                    !mbar_wait(&bars[a.stages + st], ((k / a.stages) - 1) & 1, abort_flag, a.wc))
                     break;
                 uint8_t *base = sm + st * stage_bytes;
                 mbar_arrive_expect_tx(&bars[st], stage_bytes);
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
             bool ok = true;
             for (int k = 0; k < nsteps && ok; ++k) {
                 const int st = k % a.stages;
-                ok = mbar_wait(&bars[st], (k / a.stages) & 1, abort_flag, a.status);
+                ok = mbar_wait(&bars[st], (k / a.stages) & 1, abort_flag, a.wc);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t xa = smem_u32(sm + st * stage_bytes);
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(192, 2) assign_tc_kernel(const __grid_constant
         __syncwarp();
     } else {
         // epilogue: thread = token row = TMEM lane
-        const bool ok = mbar_wait(&bars[2 * a.stages], 0, abort_flag, a.status);
+        const bool ok = mbar_wait(&bars[2 * a.stages], 0, abort_flag, a.wc);
         tc_fence_after();
         switch (min(a.topk + 1, a.K)) {
         case 1: tc_epilogue<1>(a, tmem, ok, t0); break;
@@ -255,12 +255,12 @@ size_t assign_tc_ws_bytes(int hidden, int K)
     return 2 * (size_t)assign_tc_kp(K) * hidden * sizeof(__nv_bfloat16) + 256;
 }
 
-cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan)
+cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan)
 {
     const int Kp = assign_tc_kp(p.K);
     plan->path = 1;
     plan->p = p;
-    plan->status = status;
+    plan->wc = wc;
     plan->Kp = Kp;
     plan->mhi = ws;   // [M_hi; M_lo]: [2 Kp, hidden]
     const uint32_t stage = 128u * kTokens + 2u * 128u * Kp;
@@ -310,7 +310,7 @@ cudaError_t assign_tc_launch(const AssignPlan &plan, cudaStream_t s, int *launch
     a.stages = plan.stages;
     a.ids = p.ids;
     a.margin = p.margin;
-    a.status = plan.status;
+    a.wc = plan.wc;
     prof_begin("assign", s);
     cudaError_t e = launch_pdl(assign_tc_kernel, dim3((unsigned)plan.grid), dim3(192), plan.smem,
                                s, plan.map[0], plan.map[1], a);
@@ -336,15 +336,15 @@ size_t assign_ws_bytes(int64_t ntok, int hidden, int dg, int K, int topk)
     }
 }
 
-cudaError_t assign_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan)
+cudaError_t assign_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan)
 {
     switch (assign_path(p.hidden, p.dg, p.K, p.topk)) {
-    case 2: return assign_z_prepare(p, ws, status, plan);
-    case 1: return assign_tc_prepare(p, ws, status, plan);
+    case 2: return assign_z_prepare(p, ws, wc, plan);
+    case 1: return assign_tc_prepare(p, ws, wc, plan);
     default:
         plan->path = 0;
         plan->p = p;
-        plan->status = status;
+        plan->wc = wc;
         return cudaSuccess;
     }
 }

@@ -94,7 +94,7 @@ struct ZGemmArgs {
     int hidden, dgp, stages;
     __half *Z;        // [ntok][2 dgp]: fp16 hi part, then lo part, of z * 2^-e
     float *zscale;    // [ntok]: 2^e
-    int *status;
+    WaitCtl wc;
 };
 
 // One stage: X rows of the two token tiles [128 x 64] bf16 (16 KB each), then
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(192, 1) assign_z_gemm_kernel(const __grid_cons
                     const int st = (int)(g % S);
                     if (g >= S &&
                         !(ok = mbar_wait(&empty[st], (uint32_t)((g / S) - 1) & 1u, abort_flag,
-                                         a.status)))
+                                         a.wc)))
                         break;
                     uint8_t *base = sm + (size_t)st * SB;
                     mbar_arrive_expect_tx(&full[st], SB);
@@ -190,13 +190,13 @@ __global__ void __launch_bounds__(192, 1) assign_z_gemm_kernel(const __grid_cons
                 const int b = jj & 1;
                 if (jj >= 2 &&
                     !(ok = mbar_wait(&tempty[b], (uint32_t)((jj >> 1) - 1) & 1u, abort_flag,
-                                     a.status)))
+                                     a.wc)))
                     break;
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)(2 * b * dgp);
                 for (int k = 0; k < nsteps; ++k, ++g) {
                     const int st = (int)(g % S);
-                    if (!(ok = mbar_wait(&full[st], (uint32_t)(g / S) & 1u, abort_flag, a.status)))
+                    if (!(ok = mbar_wait(&full[st], (uint32_t)(g / S) & 1u, abort_flag, a.wc)))
                         break;
                     tc_fence_after();
                     const uint32_t xa = smem_u32(sm + (size_t)st * SB);
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(192, 1) assign_z_gemm_kernel(const __grid_cons
             const int b = jj & 1;
             // warp-uniform: tcgen05.ld below is warp-collective
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(&tfull[b], (uint32_t)(jj >> 1) & 1u, abort_flag, a.status)))
+                            mbar_wait(&tfull[b], (uint32_t)(jj >> 1) & 1u, abort_flag, a.wc)))
                 break;
             tc_fence_after();
 #pragma unroll 1
@@ -295,7 +295,7 @@ struct ZScoreArgs {
     const float *zscale;
     int32_t *ids;
     float *margin;
-    int *status;
+    WaitCtl wc;
 };
 
 // Shared memory: C_hi / C_lo as [dgp / 64 chunks][2 Kp rows][128 B], then the
@@ -327,7 +327,7 @@ __device__ __forceinline__ void z_score_epilogue(const ZScoreArgs &a, uint32_t t
     int jj = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++jj) {
         const int b = jj & 1;
-        const bool ok = mbar_wait(&tfull[b], (uint32_t)(jj >> 1) & 1u, abort_flag, a.status);
+        const bool ok = mbar_wait(&tfull[b], (uint32_t)(jj >> 1) & 1u, abort_flag, a.wc);
         // the two warps of the quarter leave together: they meet at a named
         // barrier below, and tcgen05.ld is warp-collective
         if (!named_bar_and(1 + q4, 64, ok)) break;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(320, 1) assign_z_score_kernel(const __grid_con
                     const int st = (int)(g % S);
                     if (g >= S &&
                         !(ok = mbar_wait(&empty[st], (uint32_t)((g / S) - 1) & 1u, abort_flag,
-                                         a.status)))
+                                         a.wc)))
                         break;
                     uint8_t *base = sZ + (size_t)st * kZsStage;
                     mbar_arrive_expect_tx(&full[st], kZsStage);
@@ -468,20 +468,20 @@ __global__ void __launch_bounds__(320, 1) assign_z_score_kernel(const __grid_con
     } else if (warp == kZEpiWarps + 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(kZTok, Kp);
-            bool ok = mbar_wait(cbar, 0, abort_flag, a.status);
+            bool ok = mbar_wait(cbar, 0, abort_flag, a.wc);
             int64_t g = 0;
             int jj = 0;
             for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++jj) {
                 const int b = jj & 1;
                 if (jj >= 2 &&
                     !(ok = mbar_wait(&tempty[b], (uint32_t)((jj >> 1) - 1) & 1u, abort_flag,
-                                     a.status)))
+                                     a.wc)))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * Kp);
                 for (int c = 0; c < nchunk; ++c, ++g) {
                     const int st = (int)(g % S);
-                    if (!(ok = mbar_wait(&full[st], (uint32_t)(g / S) & 1u, abort_flag, a.status)))
+                    if (!(ok = mbar_wait(&full[st], (uint32_t)(g / S) & 1u, abort_flag, a.wc)))
                         break;
                     tc_fence_after();
                     const uint32_t zh = smem_u32(sZ + (size_t)st * kZsStage), zl = zh + 16384;
@@ -555,7 +555,7 @@ size_t assign_z_ws_bytes(int64_t ntok, int hidden, int dg, int K)
            al256((size_t)ntok * 2 * dgp * 2) + al256((size_t)ntok * 4) + 256;
 }
 
-cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan)
+cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan)
 {
     const int Kp = (p.K + 15) / 16 * 16, dgp = assign_z_dgp(p.dg);
     uint8_t *base = static_cast<uint8_t *>(ws);
@@ -566,7 +566,7 @@ cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, int *status, Assig
     plan->zscale = reinterpret_cast<float *>(base + off);
     plan->Kp = Kp;
     plan->dgp = dgp;
-    plan->status = status;
+    plan->wc = wc;
     plan->p = p;
     plan->path = 2;
     int dev = 0, sms = 0;
@@ -631,7 +631,7 @@ cudaError_t assign_z_launch(const AssignPlan &plan, cudaStream_t s, int *launche
     ga.stages = plan.stages;
     ga.Z = static_cast<__half *>(plan.z);
     ga.zscale = plan.zscale;
-    ga.status = plan.status;
+    ga.wc = plan.wc;
     prof_begin("assign", s);
     e = launch_pdl(assign_z_gemm_kernel, dim3((unsigned)plan.grid), dim3(192), plan.smem, s,
                    plan.map[0], plan.map[1], ga);
@@ -648,7 +648,7 @@ cudaError_t assign_z_launch(const AssignPlan &plan, cudaStream_t s, int *launche
     sa.zscale = plan.zscale;
     sa.ids = p.ids;
     sa.margin = p.margin;
-    sa.status = plan.status;
+    sa.wc = plan.wc;
     prof_begin("assign_score", s);
     e = launch_pdl(assign_z_score_kernel, dim3((unsigned)plan.grid2),
                    dim3(32 * (kZEpiWarps + 2)), plan.smem2, s,

@@ -935,19 +935,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool has = l > 0.f;
             const float lse2 = has ? m_ref + log2f(l) : -CUDART_INF_F;   // base 2
             const float inv_l = has ? 1.f / l : 0.f;
-            // Pass 1 (partials): the row's largest |O| entry.
+            // O_h of this row, all D columns in one TMEM load (the tile's score
+            // registers are dead here), then its largest |entry| (partials).
+            float o[D];
+            if (has_tiles) {
+                if constexpr (D == 128) {
+                    tmem_ld128(o_col, o);
+                } else {
+                    tmem_ld32(o_col, o);
+                    tmem_ld32(o_col + 32, o + 32);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < D; ++e) o[e] = 0.f;
+            }
             float amax = 0.f;
-            if (MODE != kDense && has_tiles) {
+            if (MODE != kDense) {
                 float am8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) am8[i] = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(o_col + c * 32, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) am8[e & 7] = fmaxf(am8[e & 7], fabsf(o[e]));
-                }
+                for (int e = 0; e < D; ++e) am8[e & 7] = fmaxf(am8[e & 7], fabsf(o[e]));
                 amax = fmaxf(fmaxf(fmaxf(am8[0], am8[1]), fmaxf(am8[2], am8[3])),
                              fmaxf(fmaxf(am8[4], am8[5]), fmaxf(am8[6], am8[7]))) *
                        inv_l;
@@ -979,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_float2(lse2, up);
                 }
             }
-            // Pass 2: 32 columns at a time straight from registers; each lane
+            // The row straight from registers, 32 columns at a time; each lane
             // writes its own row.  Partials (workspace rows, 32-byte aligned)
             // go out as 32-byte stores, whole sectors; the dense output as
             // 16-byte stores.
@@ -987,20 +995,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                               : (MODE == kGroup) ? reinterpret_cast<uint16_t *>(a.part_out16)
                                                  : reinterpret_cast<uint16_t *>(a.win_out16);
             uint16_t *orow_p = obase + orow * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                if (has_tiles) {
-                    tmem_ld32(o_col + c * 32, o);
-                } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
-                }
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    pk[q] = (MODE == kDense) ? pack_bf16x2(o[2 * q] * mul, o[2 * q + 1] * mul)
-                                             : pack_f16x2(o[2 * q] * mul, o[2 * q + 1] * mul);
+                for (int q = 0; q < 16; ++q) {
+                    const float x0 = o[32 * c + 2 * q] * mul, x1 = o[32 * c + 2 * q + 1] * mul;
+                    pk[q] = (MODE == kDense) ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
+                }
                 if (qvalid) {
                     if (MODE == kDense) {
                         uint4 *dst = reinterpret_cast<uint4 *>(orow_p + c * 32);

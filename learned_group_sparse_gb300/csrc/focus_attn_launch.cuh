@@ -69,7 +69,7 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.part_meta_out = p.part_meta_out;
     a.win_out16 = p.win_out16;
     a.win_meta_out = p.win_meta_out;
-    a.status = p.status;
+    a.status = p.wc.status;   // the attention kernels' waits use the fixed limit
     a.pair_count = p.pair_count;
     a.trace = trace_buffer(MODE);
     // Persistent: at most one CTA per SM; p.grid bounds the number of work items.

@@ -42,6 +42,15 @@ __device__ __forceinline__ void grid_dep_sync()
 }
 #endif
 
+// Control of the kernels' bounded mbarrier waits, passed by value in every
+// launch that waits: the device status word (a wait that runs out writes
+// FOCUS_ERR_TIMEOUT there) and the limit, in ns of %globaltimer (a kernel
+// argument, so reading it costs no memory access).
+struct WaitCtl {
+    int *status;
+    unsigned long long limit_ns;
+};
+
 // Per-kernel timing hooks (no-ops unless focus_profile_enable(1) was called
 // on this host thread).
 void prof_begin(const char *name, cudaStream_t s);
@@ -81,7 +90,7 @@ struct AssignPlan {
     CUtensorMap map[4];
     AssignLaunch p;
     int path;
-    int *status;
+    WaitCtl wc;
     int Kp, dgp, stages, stages2;
     size_t smem, smem2;
     int64_t grid, grid2;
@@ -91,17 +100,17 @@ struct AssignPlan {
 };
 int assign_path(int hidden, int dg, int K, int topk);
 size_t assign_ws_bytes(int64_t ntok, int hidden, int dg, int K, int topk);
-cudaError_t assign_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan);
 cudaError_t assign_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
 // the paths' own halves of the above
 bool assign_tc_supported(int hidden, int K, int topk);
-cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_tc_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan);
 cudaError_t assign_tc_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
 size_t assign_tc_ws_bytes(int hidden, int K);
 int assign_z_dgp(int dg);
 bool assign_z_supported(int hidden, int dg, int K, int topk);
 size_t assign_z_ws_bytes(int64_t ntok, int hidden, int dg, int K);
-cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, int *status, AssignPlan *plan);
+cudaError_t assign_z_prepare(const AssignLaunch &p, void *ws, const WaitCtl &wc, AssignPlan *plan);
 cudaError_t assign_z_launch(const AssignPlan &plan, cudaStream_t s, int *launches);
 
 // ---- bucket: histogram per chunk, scan, offsets, stable scatter
@@ -162,14 +171,14 @@ struct AttnLaunch {
     float *lse;
     __half *part_out16, *win_out16;
     float2 *part_meta_out, *win_meta_out;
-    int *status;
+    WaitCtl wc;
     int32_t *pair_count;
 };
 // O = log-sum-exp merge of the window partial and the topk group partials.
-// status: the device status word (bounded waits of the bulk-copy path).
+// wc: the bounded waits of the bulk-copy path.
 cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __half *part16,
                          const float2 *part_meta, const int32_t *inv, int B, int n, int topk,
-                         int Hq, int d, __nv_bfloat16 *O, float *lse, int *status,
+                         int Hq, int d, __nv_bfloat16 *O, float *lse, const WaitCtl &wc,
                          cudaStream_t s, int *launches);
 cudaError_t launch_attn_group(const AttnLaunch &p, cudaStream_t s, int *launches);
 // Sets the launch attributes of the group and window kernels for (d, K) and

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
     const uint4 *__restrict__ win16, const float2 *__restrict__ win_meta,
     const uint4 *__restrict__ part16, const float2 *__restrict__ part_meta,
     const int32_t *__restrict__ inv, int n, int64_t nk, int64_t ntok, int topk, int Hq, int d,
-    uint4 *__restrict__ O, float *__restrict__ lse, int *status)
+    uint4 *__restrict__ O, float *__restrict__ lse, const WaitCtl wc)
 {
     grid_dep_sync();
     extern __shared__ __align__(16) uint8_t msm[];
@@ -211,24 +211,24 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
             }
         }
     };
-    // thread 0: parity of the copies in flight into buffer b (-1: none)
-    int pending[2] = {-1, -1};
+    // thread 0: parity of the copies in flight into buffer 0 / 1 (-1: none)
+    int pend0 = -1, pend1 = -1;
     int64_t tok = blockIdx.x;
     if (threadIdx.x == 0 && tok < ntok) {
         issue(tok, 0);
-        pending[0] = 0;
+        pend0 = 0;
     }
     for (int k = 0; tok < ntok; ++k, tok += gridDim.x) {
         const int b = k & 1;
         const int64_t next = tok + gridDim.x;
         if (threadIdx.x == 0 && next < ntok) {
             issue(next, b ^ 1);
-            pending[b ^ 1] = ((k + 1) >> 1) & 1;
+            (b ? pend0 : pend1) = ((k + 1) >> 1) & 1;
         }
         // every thread waits for this token's copies (bounded); the block
         // leaves together if any wait gave up
-        if (!__syncthreads_and(mbar_wait(&bar[b], (k >> 1) & 1, &abort_flag, status))) break;
-        pending[b] = -1;
+        if (!__syncthreads_and(mbar_wait(&bar[b], (k >> 1) & 1, &abort_flag, wc))) break;
+        (b ? pend1 : pend0) = -1;
         const uint8_t *base = buf0 + (size_t)b * tokb;
         const float2 *meta = reinterpret_cast<const float2 *>(base + (size_t)np * rowb);
         const int64_t bb = tok / n;
@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
     // A block that gave up lets its copies in flight land before it exits.
     if (abort_flag && threadIdx.x == 0) {
         const uint64_t deadline = global_timer_ns() + 100000000ull;
-        for (int b = 0; b < 2; ++b)
-            if (pending[b] >= 0) mbar_wait_until(&bar[b], (uint32_t)pending[b], deadline);
+        if (pend0 >= 0) mbar_wait_until(&bar[0], (uint32_t)pend0, deadline);
+        if (pend1 >= 0) mbar_wait_until(&bar[1], (uint32_t)pend1, deadline);
     }
 }
 
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(256) merge_bulk_kernel(
 
 cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __half *part16,
                          const float2 *part_meta, const int32_t *inv, int B, int n, int topk,
-                         int Hq, int d, __nv_bfloat16 *O, float *lse, int *status,
+                         int Hq, int d, __nv_bfloat16 *O, float *lse, const WaitCtl &wc,
                          cudaStream_t s, int *launches)
 {
     const int64_t rows = (int64_t)B * n;
@@ -314,7 +314,7 @@ cudaError_t launch_merge(const __half *win16, const float2 *win_meta, const __ha
                        reinterpret_cast<const uint4 *>(win16), win_meta,
                        reinterpret_cast<const uint4 *>(part16), part_meta, inv, n,
                        (int64_t)n * topk, rows, topk, Hq, d, reinterpret_cast<uint4 *>(O), lse,
-                       status);
+                       wc);
         prof_end(s);
         *launches += 1;
         return e;
