@@ -53,6 +53,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed loop only (for profiler launch lists)")
     return ap.parse_args()
@@ -329,6 +330,50 @@ def traffic_lookup(kernel, workload, h):
     return e.get("bytes_per_launch")
 
 
+def bench_decode(fg, torch, w, t, ids, flush, stream, peaks, kind, args):
+    """One decode step per sequence, timed alone: focus_decode_fwd (list
+    append, split attention, merge) for token n - 1 over lists of the first
+    n - 1 tokens; the lists are restored between steps, outside the timing."""
+    B, n = w.B, w.n
+    off1, pos1, _ = fg.focus_bucket(ids[:, :n - 1].contiguous(), w.K)
+    cap = int((off1[:, 1:] - off1[:, :-1]).max()) + 16
+    glen, gpos = fg.focus_decode_lists_init(off1, pos1, w.K, w.topk, cap=cap)
+    glen0 = glen.clone()
+    q = t["Q"][:, n - 1].contiguous()
+    Od = torch.empty_like(q)
+    wsd = torch.empty(fg.focus_decode_workspace_size(B, w.Hq, w.Hkv, w.d), dtype=torch.uint8,
+                      device=q.device)
+    off, pos, inv = fg.focus_bucket(ids, w.K)
+    per, _ = fg.focus_count_pairs(ids, off, pos, inv, w.K, w.window)
+    keys = int(per[:, n - 1].sum())
+    # list entries scanned: the new token's groups' lists (and each entry's ids)
+    gl = glen0.cpu()
+    last = ids[:, n - 1].cpu()
+    scanned = sum(int(gl[b, int(g)]) for b in range(B) for g in last[b])
+    reps = max(10, min(200, args.steps * 5))
+    evs = []
+    for k in range(3 + reps):
+        glen.copy_(glen0)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fg.focus_decode_fwd(q, t["K"], t["V"], ids, n, w.window, glen, gpos, w.K, O=Od,
+                            ws=wsd, with_lse=False)
+        b.record(stream)
+        if k >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    kv_bytes = keys * w.Hkv * w.d * 2 * 2
+    alg = kv_bytes + B * w.Hq * w.d * 2 * 2 + scanned * 4 * (1 + w.topk)
+    ach = alg / (ms * 1e-3) / 1e9
+    return {"ms": ms, "tokens_per_s": B / (ms * 1e-3), "allowed_keys": keys,
+            "list_entries_scanned": scanned, "algorithmic_bytes": alg, "bound": "hbm",
+            "achieved": ach, "unit": "GB/s", "peak": float(peaks["hbm_gbs"]),
+            "frac": ach / float(peaks["hbm_gbs"]), "reps": reps,
+            "what": "one new token per sequence (position n - 1), L2 flushed between steps"}
+
+
 def main():
     args = parse_args()
     from learned_group_sparse_gb300 import synth
@@ -484,6 +529,13 @@ def main():
                  "speedup_of_focus_attention": d_ms / attn_ms if attn_ms else None}
         del Od
 
+    # ---- decode: the workload's last token as the new token of each sequence,
+    # against group lists built from the first n - 1 tokens (HBM-bound: the K
+    # and V rows of its allowed keys)
+    decode = None
+    if not args.no_decode and n >= 2:
+        decode = bench_decode(fg, torch, w, t, ids, flush, stream, peaks, kind, args)
+
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -550,7 +602,7 @@ def main():
             / float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])),
             "attention_effective_tflops": eff_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
             "allowed_pairs": total_pairs, "group_pairs": share_pairs,
-            "roofline": roof, "kernels": kernels, "dense_causal": dense,
+            "roofline": roof, "kernels": kernels, "dense_causal": dense, "decode": decode,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
             "context": "pages: 8.6x over full attention at 1M tokens (H100) and 2x from "

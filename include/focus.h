@@ -41,6 +41,7 @@ typedef int focus_status_t;
 #define FOCUS_ERR_WORKSPACE      3   /* workspace smaller than required     */
 #define FOCUS_ERR_CUDA           4   /* a CUDA runtime/launch error         */
 #define FOCUS_ERR_TIMEOUT        5   /* a bounded device wait ran out       */
+#define FOCUS_ERR_CAPACITY       6   /* a decode group list was full        */
 
 /* Human-readable name of a status code (static storage). */
 const char *focus_status_string(focus_status_t status);
@@ -204,6 +205,55 @@ focus_status_t focus_prefill(const void *X, const float *Wg, const float *C,
                              void *stream);
 
 /*
+ * Decode: one new token per sequence against a key/value cache.  At inference
+ * a token belongs to its k highest-scoring groups (gist.science/nl
+ * Kerncomponent 4; gist.science/zh 2.1.3) and attends with an exact softmax
+ * to the keys in its local window or sharing one of its groups (nl
+ * Kerncomponent 3; zh 2.1.2).  The cache's group memberships are kept as
+ * per-group position lists that only grow:
+ *   glen [B, K]        int32   entries in each group's list
+ *   gpos [B, K, cap]   int32   token positions of group g in ascending order,
+ *                              gpos[b][g][0 .. glen[b][g])
+ *
+ * focus_decode_lists_init -- the lists of the first n tokens, from their
+ * bucketing (offsets [B, K+1], pos [B, n*topk] of focus_bucket).  cap is the
+ * room of every list; a group larger than cap keeps its first cap members
+ * and records FOCUS_ERR_CAPACITY in the device status word.
+ */
+focus_status_t focus_decode_lists_init(const int32_t *offsets, const int32_t *pos, int B, int n,
+                                       int num_groups, int topk, int cap, int32_t *glen,
+                                       int32_t *gpos, void *stream);
+
+/*
+ * focus_decode_fwd -- the new token i = L - 1 of every sequence: appends i to
+ * the lists of its k groups, then computes its attention over
+ *   A_i = { j <= i : i - j < window  or  ids_i and ids_j share a group }
+ * as a split over the keys (window keys, and each shared key once, from the
+ * list of the lowest shared group) with a log-sum-exp merge.
+ *
+ *   q      [B, Hq, d]        bf16   the new token's query
+ *   Kc, Vc [B, Lmax, Hkv, d] bf16   the cache; row L - 1 holds the new token
+ *   ids    [B, Lmax, topk]   int32  group ids of the cached tokens (row
+ *                                   L - 1: the new token's, e.g. from
+ *                                   focus_assign on its hidden state)
+ *   glen, gpos, cap                 the group lists (updated in place); call
+ *                                   once per new token
+ *   O      [B, Hq, d]        bf16 out;  lse [B, Hq] fp32 out, nullable
+ *   ws, ws_bytes: at least focus_decode_workspace_size(B, Hq, Hkv, d) bytes.
+ * Arithmetic: fp32 scores, softmax and accumulation from bf16 inputs, O
+ * rounded to bf16.  A list already holding cap entries is not appended to
+ * and FOCUS_ERR_CAPACITY is recorded in the device status word.
+ * Supported: d in {64, 128}, Hq % Hkv == 0 with Hq / Hkv <= 8,
+ *            1 <= topk <= min(K, 8), K <= 1024, 1 <= L <= Lmax.
+ */
+size_t focus_decode_workspace_size(int B, int Hq, int Hkv, int d);
+focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, const int32_t *ids,
+                                int B, int L, int Lmax, int Hq, int Hkv, int d, int window,
+                                float scale, int num_groups, int topk, int32_t *glen,
+                                int32_t *gpos, int cap, void *O, float *lse, void *ws,
+                                size_t ws_bytes, void *stream);
+
+/*
  * focus_dense_causal_fwd -- plain causal attention (every j <= i) with the
  * same tcgen05 mainloop; the baseline the sparse path is compared with.
  *   Q [B, n, Hq, d], K/V [B, n, Hkv, d] bf16; O [B, n, Hq, d] bf16;
@@ -247,7 +297,8 @@ focus_status_t focus_attention_fwd_counted(const void *Q, const void *K, const v
 
 /*
  * Reads (and with reset != 0 clears) the device status word of the current
- * device: FOCUS_OK or FOCUS_ERR_TIMEOUT.  Synchronises the device.
+ * device: FOCUS_OK, FOCUS_ERR_TIMEOUT or FOCUS_ERR_CAPACITY.  Synchronises
+ * the device.
  */
 focus_status_t focus_get_device_status(int reset);
 

@@ -24,6 +24,7 @@ __all__ = [
     "focus_prefill_workspace_size", "focus_get_device_status", "focus_set_wait_limit",
     "focus_last_launch_count",
     "focus_status_string", "focus_version", "focus_profile_enable", "focus_profile_read",
+    "focus_decode_workspace_size", "focus_decode_lists_init", "focus_decode_fwd",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +33,8 @@ _lock = threading.Lock()
 _lib = None
 
 _STATUS = {0: "FOCUS_OK", 1: "FOCUS_ERR_INVALID_ARG", 2: "FOCUS_ERR_UNSUPPORTED",
-           3: "FOCUS_ERR_WORKSPACE", 4: "FOCUS_ERR_CUDA", 5: "FOCUS_ERR_TIMEOUT"}
+           3: "FOCUS_ERR_WORKSPACE", 4: "FOCUS_ERR_CUDA", 5: "FOCUS_ERR_TIMEOUT",
+           6: "FOCUS_ERR_CAPACITY"}
 
 
 class FocusError(RuntimeError):
@@ -71,6 +73,10 @@ def library() -> ctypes.CDLL:
                 "focus_set_wait_limit": ([ctypes.c_ulonglong], i32),
                 "focus_last_launch_count": ([], i32),
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
+                "focus_decode_workspace_size": ([i32] * 4, sz),
+                "focus_decode_lists_init": ([vp, vp] + [i32] * 5 + [vp, vp, vp], i32),
+                "focus_decode_fwd": ([vp] * 4 + [i32] * 7 + [f32, i32, i32, vp, vp, i32, vp, vp,
+                                     vp, sz, vp], i32),
                 "focus_profile_enable": ([i32], None),
                 "focus_trace_attention": ([vp, vp, vp], None),
                 "focus_profile_read": ([vp, i32, vp, vp, i32], i32),
@@ -303,6 +309,60 @@ def focus_prefill(X, Wg, C, Q, K, V, topk, window, scale=0.0, O=None, lse=None, 
         _p(X), _p(Wg), _p(C), _p(Q), _p(K), _p(V), B, n, hidden, Hq, Hkv, d, dg, Kg, topk,
         int(window), float(scale), _p(O), _p(lse), _p(ids_out), _p(ws), ws.numel(),
         1 if host else 0, s))
+    return O, lse
+
+
+def focus_decode_workspace_size(B, Hq, Hkv, d) -> int:
+    return int(library().focus_decode_workspace_size(B, Hq, Hkv, d))
+
+
+def focus_decode_lists_init(offsets, pos, num_groups, topk, cap, glen=None, gpos=None):
+    """Group lists with room for `cap` members each, from a prefix's bucketing
+    (offsets [B, K+1], pos [B, n*topk] of focus_bucket) -> (glen [B, K],
+    gpos [B, K, cap]) int32."""
+    _need(offsets, "offsets", torch.int32, 2)
+    _need(pos, "pos", torch.int32, 2)
+    B = offsets.shape[0]
+    n = pos.shape[1] // topk
+    dev = offsets.device
+    if glen is None:
+        glen = torch.empty(B, num_groups, dtype=torch.int32, device=dev)
+    if gpos is None:
+        gpos = torch.empty(B, num_groups, cap, dtype=torch.int32, device=dev)
+    # a prefix of no tokens has an empty pos tensor: pass any valid pointer
+    pos_p = _p(pos) if pos.numel() else _p(glen)
+    _check("focus_decode_lists_init", library().focus_decode_lists_init(
+        _p(offsets), pos_p, B, n, num_groups, topk, cap, _p(glen), _p(gpos), _stream(offsets)))
+    return glen, gpos
+
+
+def focus_decode_fwd(q, Kc, Vc, ids, L, window, glen, gpos, num_groups, scale=0.0, O=None,
+                     lse=None, ws=None, with_lse=True):
+    """One new token per sequence (position L - 1 of the cache): appends it to
+    its groups' lists (glen/gpos, in place) and attends over its allowed keys.
+    q [B, Hq, d], Kc/Vc [B, Lmax, Hkv, d] bf16, ids [B, Lmax, topk] int32 ->
+    (O [B, Hq, d] bf16, lse [B, Hq] fp32 or None)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(Kc, "Kc", torch.bfloat16, 4)
+    _need(Vc, "Vc", torch.bfloat16, 4)
+    _need(ids, "ids", torch.int32, 3)
+    _need(glen, "glen", torch.int32, 2)
+    _need(gpos, "gpos", torch.int32, 3)
+    B, Hq, d = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    topk = ids.shape[-1]
+    cap = gpos.shape[-1]
+    if O is None:
+        O = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    need = focus_decode_workspace_size(B, Hq, Hkv, d)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check("focus_decode_fwd", library().focus_decode_fwd(
+        _p(q), _p(Kc), _p(Vc), _p(ids), B, int(L), Lmax, Hq, Hkv, d, int(window), float(scale),
+        num_groups, topk, _p(glen), _p(gpos), cap, _p(O), _p(lse), _p(ws), ws.numel(),
+        _stream(q)))
     return O, lse
 
 

@@ -435,6 +435,7 @@ const char *focus_status_string(focus_status_t status)
     case FOCUS_ERR_WORKSPACE: return "FOCUS_ERR_WORKSPACE";
     case FOCUS_ERR_CUDA: return "FOCUS_ERR_CUDA";
     case FOCUS_ERR_TIMEOUT: return "FOCUS_ERR_TIMEOUT";
+    case FOCUS_ERR_CAPACITY: return "FOCUS_ERR_CAPACITY";
     default: return "FOCUS_ERR_UNKNOWN";
     }
 }
@@ -703,6 +704,84 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
     cudaError_t e = launch_count_pairs(ids, offsets, pos, inv, B, n, num_groups, topk, window,
                                        per_query, totals, static_cast<cudaStream_t>(stream),
                                        &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+size_t focus_decode_workspace_size(int B, int Hq, int Hkv, int d)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0) return 0;
+    return decode_ws_bytes(B, Hq, Hkv, d);
+}
+
+focus_status_t focus_decode_lists_init(const int32_t *offsets, const int32_t *pos, int B, int n,
+                                       int num_groups, int topk, int cap, int32_t *glen,
+                                       int32_t *gpos, void *stream)
+{
+    if (!offsets || !pos || !glen || !gpos) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(offsets) || !aligned16(pos) || !aligned16(glen) || !aligned16(gpos))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 0 || num_groups < 1 || topk < 1 || topk > num_groups || cap < 1)
+        return FOCUS_ERR_INVALID_ARG;
+    if (num_groups > 1024 || topk > 8 || (int64_t)B * n * topk >= ((int64_t)1 << 31) ||
+        (int64_t)B * num_groups > 65535)
+        return FOCUS_ERR_UNSUPPORTED;
+    int *status = nullptr;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    int launches = 0;
+    cudaError_t e = launch_decode_lists_init(offsets, pos, B, n, num_groups, topk, cap, glen,
+                                             gpos, status, static_cast<cudaStream_t>(stream),
+                                             &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, const int32_t *ids,
+                                int B, int L, int Lmax, int Hq, int Hkv, int d, int window,
+                                float scale, int num_groups, int topk, int32_t *glen,
+                                int32_t *gpos, int cap, void *O, float *lse, void *ws,
+                                size_t ws_bytes, void *stream)
+{
+    if (!q || !Kc || !Vc || !ids || !glen || !gpos || !O || !ws) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(ids) ||
+        !aligned16(glen) || !aligned16(gpos) || !aligned16(O) || !aligned16(ws) ||
+        (lse && !aligned16(lse)))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || L > Lmax || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || window < 0 ||
+        num_groups < 1 || topk < 1 || topk > num_groups || cap < 1)
+        return FOCUS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || Hq / Hkv > 8 || num_groups > 1024 || topk > 8 ||
+        B > 65535 || Hkv > 65535 || (int64_t)B * Hq > ((int64_t)1 << 31) - 1)
+        return FOCUS_ERR_UNSUPPORTED;
+    if (ws_bytes < decode_ws_bytes(B, Hq, Hkv, d)) return FOCUS_ERR_WORKSPACE;
+    int *status = nullptr;
+    if (status_ptr(&status) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (decode_preflight(d) != cudaSuccess) return FOCUS_ERR_CUDA;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    DecodeLaunch p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(Kc);
+    p.v = static_cast<const __nv_bfloat16 *>(Vc);
+    p.ids = ids;
+    p.glen = glen;
+    p.gpos = gpos;
+    p.B = B;
+    p.L = L;
+    p.Lmax = Lmax;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.K = num_groups;
+    p.topk = topk;
+    p.cap = cap;
+    p.window = window;
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.lse = lse;
+    p.ws = ws;
+    p.status = status;
+    int launches = 0;
+    cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream), &launches);
     if (e == cudaSuccess) g_last_launches = launches;
     return cuda_status(e);
 }

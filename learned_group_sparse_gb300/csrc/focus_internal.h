@@ -151,6 +151,27 @@ cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const
                                int64_t *per_query, int64_t *totals, cudaStream_t s,
                                int *launches);
 
+// ---- decode: one new token per sequence against per-group position lists
+struct DecodeLaunch {
+    const __nv_bfloat16 *q, *k, *v;
+    const int32_t *ids;
+    int32_t *glen, *gpos;
+    int B, L, Lmax, Hq, Hkv, d, K, topk, cap, window;
+    float scale_log2;
+    __nv_bfloat16 *O;
+    float *lse;
+    void *ws;
+    int *status;   // device status word (a list that would overflow)
+};
+int decode_splits(int B, int Hkv);
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int d);
+size_t decode_smem_bytes(int d);
+cudaError_t decode_preflight(int d);
+cudaError_t launch_decode_lists_init(const int32_t *offsets, const int32_t *pos, int B, int n,
+                                     int K, int topk, int cap, int32_t *glen, int32_t *gpos,
+                                     int *status, cudaStream_t s, int *launches);
+cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches);
+
 // ---- tcgen05 attention kernels
 struct AttnLaunch {
     const CUtensorMap *tmQ, *tmK, *tmV;
