@@ -68,12 +68,11 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# The sources of the attention kernels (the kernel whose DRAM traffic
-# profiles/traffic.json records): a stored figure stands only while these are
-# byte-identical to what was profiled.
+# The sources of the attention kernels' device code (the kernel whose DRAM
+# traffic profiles/traffic.json records): a stored figure stands only while
+# these are byte-identical to what was profiled.
 ATTN_SOURCES = ("focus_attn_kernel.cuh", "focus_attn_launch.cuh", "focus_attn_group.cu",
-                "focus_attn_window.cu", "focus_ptx.cuh", "focus_tmem_wide.cuh",
-                "focus_internal.h")
+                "focus_attn_window.cu", "focus_ptx.cuh", "focus_tmem_wide.cuh")
 
 
 def src_hash():
