@@ -33,7 +33,9 @@ namespace focus {
 
 namespace {
 
-constexpr int kDecC = 64;           // virtual keys per chunk
+constexpr int kDecC = 64;           // kept keys per chunk of K/V rows
+constexpr int kDecSC = 256;         // virtual keys per super-chunk (two per thread)
+constexpr int kDecMaxSplits = 128;  // splits per (batch, kv head), at most one per merge thread
 constexpr int kDecThreads = 128;
 constexpr int kDecMaxGqa = 8;       // query heads per kv head
 constexpr int kDecMaxTopk = 8;
@@ -91,41 +93,67 @@ struct DecArgs {
     float2 *mpart;             // [B, Hkv, P, gqa]: {running max (base 2), sum}
 };
 
-// Shared memory of a decode CTA for head size D: K and V rows of one chunk
-// (16 bytes of padding per row keep a thread's own-row loads free of bank
-// conflicts), the queries in fp32, the chunk's scores and positions.
+// Shared memory of a decode CTA for head size D: two buffers of K and V rows
+// for a chunk of kept keys (16 bytes of padding per row keep a thread's
+// own-row loads free of bank conflicts), the queries in fp32, the chunk's
+// scores, and the positions of a super-chunk's kept keys.
 template <int D>
 struct DecSmem {
-    static constexpr int kRow = D * 2 + 16;                 // bytes per cached row
-    static constexpr int kK = 0;
-    static constexpr int kV = kK + kDecC * kRow;
-    static constexpr int kQ = kV + kDecC * kRow;            // float [gqa][D]
-    static constexpr int kS = kQ + kDecMaxGqa * D * 4;      // float [gqa][kDecC]
-    static constexpr int kPos = kS + kDecMaxGqa * kDecC * 4;   // int [kDecC]
-    static constexpr int kBytes = kPos + kDecC * 4;
+    static constexpr int kRow = D * 2 + 16;                     // bytes per cached row
+    static constexpr int kBuf = 2 * kDecC * kRow;               // K rows, then V rows
+    static constexpr int kQ = 2 * kBuf;                         // float [gqa][D]
+    static constexpr int kS = kQ + kDecMaxGqa * D * 4;          // float [gqa][kDecC]
+    static constexpr int kPos = kS + kDecMaxGqa * kDecC * 4;    // int [kDecSC]
+    static constexpr int kBytes = kPos + kDecSC * 4;
 };
 
+// The position of virtual key vk if this split scores it, else -1: window
+// keys always; a key from the list of g if it lies before the window and g is
+// the lowest group it shares with the new token.
+__device__ __forceinline__ int decode_key(const DecArgs &a, int b, int i, int vk, int nw, int nvirt,
+                                          const int *gi, const int *seg)
+{
+    if (vk < nw) return i - vk;
+    if (vk >= nvirt) return -1;
+    int s = 0;
+    while (s + 1 < a.topk && vk >= seg[s + 1]) ++s;
+    const int g = gi[s];
+    const int jj = a.gpos[((int64_t)b * a.K + g) * a.cap + (vk - seg[s])];
+    if ((unsigned)jj > (unsigned)i || i - jj < a.window) return -1;
+    // the list of the new token's lowest group owns every shared key in it
+    bool lowest = true;
+    for (int y = 0; y < a.topk; ++y) lowest = lowest && gi[y] >= g;
+    if (lowest) return jj;
+    const int32_t *gj = a.ids + ((int64_t)b * a.Lmax + jj) * a.topk;
+    int own = 0x7fffffff;
+    for (int x = 0; x < a.topk; ++x) {
+        const int gx = gj[x];
+        for (int y = 0; y < a.topk; ++y)
+            if (gi[y] == gx && gx < own) own = gx;
+    }
+    return own == g ? jj : -1;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, 4) decode_attn_kernel(const DecArgs a)
+__global__ void __launch_bounds__(kDecThreads, 3) decode_attn_kernel(const DecArgs a)
 {
     grid_dep_sync();
     using L = DecSmem<D>;
     extern __shared__ __align__(16) uint8_t dsm[];
-    uint8_t *sK = dsm + L::kK;
-    uint8_t *sV = dsm + L::kV;
     float *qf = reinterpret_cast<float *>(dsm + L::kQ);
     float *S = reinterpret_cast<float *>(dsm + L::kS);
     int *spos = reinterpret_cast<int *>(dsm + L::kPos);
     __shared__ int gi[kDecMaxTopk];
     __shared__ int seg[kDecMaxTopk + 1];   // virtual-key bounds: window, then each list
     __shared__ float mrun[kDecMaxGqa], lrun[kDecMaxGqa], alpha[kDecMaxGqa];
-    __shared__ int wcnt[kDecThreads / 32];
+    __shared__ int wcnt[2 * (kDecThreads / 32)];
 
     const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gqa = a.Hq / a.Hkv;
     const int i = a.L - 1;
     const int topk = a.topk;
+    constexpr int kUnits = D / 8;   // 16-byte units per row
 
     if (tid < topk) gi[tid] = a.ids[((int64_t)b * a.Lmax + i) * topk + tid];
     if (tid < kDecMaxGqa) {
@@ -153,134 +181,141 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_attn_kernel(const DecAr
 #pragma unroll
     for (int q = 0; q < kDecMaxGqa; ++q) o[q] = 0.f;
 
-    for (int c = p; c * kDecC < nvirt; c += a.P) {
-        // ---- virtual key -> position of an allowed key this split owns, or -1
-        int j = -1;
-        if (tid < kDecC) {
-            const int vk = c * kDecC + tid;
-            if (vk < nw) {
-                j = i - vk;                                     // window key
-            } else if (vk < nvirt) {
-                int s = 0;
-                while (s + 1 < topk && vk >= seg[s + 1]) ++s;
-                const int g = gi[s];
-                const int jj = a.gpos[((int64_t)b * a.K + g) * a.cap + (vk - seg[s])];
-                if ((unsigned)jj <= (unsigned)i && i - jj >= a.window) {
-                    // owned here iff g is the lowest group the two tokens share
-                    const int32_t *gj = a.ids + ((int64_t)b * a.Lmax + jj) * topk;
-                    int own = 0x7fffffff;
-                    for (int x = 0; x < topk; ++x) {
-                        const int gx = gj[x];
-                        for (int y = 0; y < topk; ++y)
-                            if (gi[y] == gx && gx < own) own = gx;
-                    }
-                    if (own == g) j = jj;
-                }
-            }
+    // K and V rows of kept keys [c0, c0 + cnt) into buffer bf (16-byte copies)
+    auto issue = [&](int bf, int c0, int cnt) {
+        uint8_t *kb = dsm + bf * L::kBuf;
+        uint8_t *vb = kb + kDecC * L::kRow;
+        for (int x = tid; x < cnt * kUnits; x += kDecThreads) {
+            const int u = x / kUnits, q8 = x - u * kUnits;
+            const int64_t row = ((int64_t)b * a.Lmax + spos[c0 + u]) * a.Hkv + h;
+            cp_async16(kb + u * L::kRow + q8 * 16, a.k + row * D + q8 * 8, 16);
+            cp_async16(vb + u * L::kRow + q8 * 16, a.v + row * D + q8 * 8, 16);
         }
-        // ---- compact the kept keys into slots 0..nv-1
-        const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
-        if (lane == 0) wcnt[warp] = __popc(bal);
+        cp_async_commit();
+    };
+
+    for (int sc = p; sc * kDecSC < nvirt; sc += a.P) {
+        // ---- the super-chunk's virtual keys (two per thread: both load
+        // chains in flight), compacted into spos[0 .. nv)
+        const int v0 = sc * kDecSC + tid;
+        const int j0 = decode_key(a, b, i, v0, nw, nvirt, gi, seg);
+        const int j1 = decode_key(a, b, i, v0 + kDecThreads, nw, nvirt, gi, seg);
+        const unsigned b0 = __ballot_sync(0xffffffffu, j0 >= 0);
+        const unsigned b1 = __ballot_sync(0xffffffffu, j1 >= 0);
+        if (lane == 0) {
+            wcnt[warp] = __popc(b0);
+            wcnt[kDecThreads / 32 + warp] = __popc(b1);
+        }
         __syncthreads();
-        int before = 0, nv = 0;
+        int before0 = 0, before1 = 0, nv = 0;
 #pragma unroll
-        for (int w = 0; w < kDecThreads / 32; ++w) {
-            if (w < warp) before += wcnt[w];
+        for (int w = 0; w < 2 * (kDecThreads / 32); ++w) {
+            if (w < warp) before0 += wcnt[w];
+            if (w < kDecThreads / 32 + warp) before1 += wcnt[w];
             nv += wcnt[w];
         }
-        if (j >= 0) spos[before + __popc(bal & ((1u << lane) - 1u))] = j;
+        const unsigned below = (1u << lane) - 1u;
+        if (j0 >= 0) spos[before0 + __popc(b0 & below)] = j0;
+        if (j1 >= 0) spos[before1 + __popc(b1 & below)] = j1;
         __syncthreads();
-        if (nv == 0) continue;   // uniform: nothing of this chunk is ours
-        // ---- K and V rows of the kept keys (kv head h) into shared memory
-        constexpr int kUnits = D / 8;   // 16-byte units per row
-        for (int x = tid; x < nv * kUnits; x += kDecThreads) {
-            const int u = x / kUnits, q8 = x - u * kUnits;
-            const int64_t row = ((int64_t)b * a.Lmax + spos[u]) * a.Hkv + h;
-            cp_async16(sK + u * L::kRow + q8 * 16, a.k + row * D + q8 * 8, 16);
-            cp_async16(sV + u * L::kRow + q8 * 16, a.v + row * D + q8 * 8, 16);
-        }
-        cp_async_wait_all();
-        __syncthreads();
-        // ---- scores of key u for every query head (base 2, scale folded into q)
-        if (tid < nv) {
-            const uint4 *kr = reinterpret_cast<const uint4 *>(sK + tid * L::kRow);
-            float acc[kDecMaxGqa];
+        // ---- chunks of kDecC kept keys, the next chunk's copies in flight
+        const int nch = (nv + kDecC - 1) / kDecC;
+        if (nch > 0) issue(0, 0, min(kDecC, nv));
+        for (int k = 0; k < nch; ++k) {
+            const int c0 = k * kDecC, cnt = min(kDecC, nv - c0);
+            if (k + 1 < nch) {
+                issue((k + 1) & 1, c0 + kDecC, min(kDecC, nv - c0 - kDecC));
+                cp_async_wait_group1();
+            } else {
+                cp_async_wait_all();
+            }
+            __syncthreads();
+            const uint8_t *kb = dsm + (k & 1) * L::kBuf;
+            const uint8_t *vb = kb + kDecC * L::kRow;
+            // scores of key u for every query head (base 2, scale folded into q)
+            if (tid < cnt) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(kb + tid * L::kRow);
+                float acc[kDecMaxGqa];
 #pragma unroll
-            for (int q = 0; q < kDecMaxGqa; ++q) acc[q] = 0.f;
+                for (int q = 0; q < kDecMaxGqa; ++q) acc[q] = 0.f;
 #pragma unroll 4
-            for (int q8 = 0; q8 < kUnits; ++q8) {
-                const uint4 raw = kr[q8];
-                const __nv_bfloat162 *kp = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-                float kv[8];
+                for (int q8 = 0; q8 < kUnits; ++q8) {
+                    const uint4 raw = kr[q8];
+                    const __nv_bfloat162 *kp = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                    float kv[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(kp[e]);
-                    kv[2 * e] = f.x;
-                    kv[2 * e + 1] = f.y;
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(kp[e]);
+                        kv[2 * e] = f.x;
+                        kv[2 * e + 1] = f.y;
+                    }
 #pragma unroll
-                for (int q = 0; q < kDecMaxGqa; ++q) {
-                    if (q < gqa) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(qf + q * D + q8 * 8);
-                        const float4 qb =
-                            *reinterpret_cast<const float4 *>(qf + q * D + q8 * 8 + 4);
-                        acc[q] = fmaf(qa.x, kv[0], acc[q]);
-                        acc[q] = fmaf(qa.y, kv[1], acc[q]);
-                        acc[q] = fmaf(qa.z, kv[2], acc[q]);
-                        acc[q] = fmaf(qa.w, kv[3], acc[q]);
-                        acc[q] = fmaf(qb.x, kv[4], acc[q]);
-                        acc[q] = fmaf(qb.y, kv[5], acc[q]);
-                        acc[q] = fmaf(qb.z, kv[6], acc[q]);
-                        acc[q] = fmaf(qb.w, kv[7], acc[q]);
+                    for (int q = 0; q < kDecMaxGqa; ++q) {
+                        if (q < gqa) {
+                            const float4 qa =
+                                *reinterpret_cast<const float4 *>(qf + q * D + q8 * 8);
+                            const float4 qb =
+                                *reinterpret_cast<const float4 *>(qf + q * D + q8 * 8 + 4);
+                            acc[q] = fmaf(qa.x, kv[0], acc[q]);
+                            acc[q] = fmaf(qa.y, kv[1], acc[q]);
+                            acc[q] = fmaf(qa.z, kv[2], acc[q]);
+                            acc[q] = fmaf(qa.w, kv[3], acc[q]);
+                            acc[q] = fmaf(qb.x, kv[4], acc[q]);
+                            acc[q] = fmaf(qb.y, kv[5], acc[q]);
+                            acc[q] = fmaf(qb.z, kv[6], acc[q]);
+                            acc[q] = fmaf(qb.w, kv[7], acc[q]);
+                        }
                     }
                 }
-            }
-#pragma unroll
-            for (int q = 0; q < kDecMaxGqa; ++q)
-                if (q < gqa) S[q * kDecC + tid] = acc[q];
-        }
-        __syncthreads();
-        // ---- online softmax per query head: warp w takes heads w, w + 4, ...
-        for (int q = warp; q < gqa; q += kDecThreads / 32) {
-            float mx = -CUDART_INF_F;
-            for (int u = lane; u < nv; u += 32) mx = fmaxf(mx, S[q * kDecC + u]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float mold = mrun[q];
-            const float mnew = fmaxf(mold, mx);
-            float sum = 0.f;
-            for (int u = lane; u < nv; u += 32) {
-                const float pr = exp2f(S[q * kDecC + u] - mnew);
-                S[q * kDecC + u] = pr;
-                sum += pr;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            __syncwarp();
-            if (lane == 0) {
-                const float al = (mold == -CUDART_INF_F) ? 0.f : exp2f(mold - mnew);
-                alpha[q] = al;
-                lrun[q] = lrun[q] * al + sum;
-                mrun[q] = mnew;
-            }
-        }
-        __syncthreads();
-        // ---- O += P V: thread t owns column t of every head's output
-        if (tid < D) {
-            float acc[kDecMaxGqa];
-#pragma unroll
-            for (int q = 0; q < kDecMaxGqa; ++q) acc[q] = (q < gqa) ? o[q] * alpha[q] : 0.f;
-            for (int u = 0; u < nv; ++u) {
-                const float vv = __bfloat162float(
-                    *reinterpret_cast<const __nv_bfloat16 *>(sV + u * L::kRow + tid * 2));
 #pragma unroll
                 for (int q = 0; q < kDecMaxGqa; ++q)
-                    if (q < gqa) acc[q] = fmaf(S[q * kDecC + u], vv, acc[q]);
+                    if (q < gqa) S[q * kDecC + tid] = acc[q];
             }
+            __syncthreads();
+            // online softmax per query head: warp w takes heads w, w + 4, ...
+            for (int q = warp; q < gqa; q += kDecThreads / 32) {
+                float mx = -CUDART_INF_F;
+                for (int u = lane; u < cnt; u += 32) mx = fmaxf(mx, S[q * kDecC + u]);
 #pragma unroll
-            for (int q = 0; q < kDecMaxGqa; ++q) o[q] = acc[q];
+                for (int off = 16; off > 0; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float mold = mrun[q];
+                const float mnew = fmaxf(mold, mx);
+                float sum = 0.f;
+                for (int u = lane; u < cnt; u += 32) {
+                    const float pr = exp2f(S[q * kDecC + u] - mnew);
+                    S[q * kDecC + u] = pr;
+                    sum += pr;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                __syncwarp();
+                if (lane == 0) {
+                    const float al = (mold == -CUDART_INF_F) ? 0.f : exp2f(mold - mnew);
+                    alpha[q] = al;
+                    lrun[q] = lrun[q] * al + sum;
+                    mrun[q] = mnew;
+                }
+            }
+            __syncthreads();
+            // O += P V: thread t owns column t of every head's output
+            if (tid < D) {
+                float acc[kDecMaxGqa];
+#pragma unroll
+                for (int q = 0; q < kDecMaxGqa; ++q) acc[q] = (q < gqa) ? o[q] * alpha[q] : 0.f;
+                for (int u = 0; u < cnt; ++u) {
+                    const float vv = __bfloat162float(
+                        *reinterpret_cast<const __nv_bfloat16 *>(vb + u * L::kRow + tid * 2));
+#pragma unroll
+                    for (int q = 0; q < kDecMaxGqa; ++q)
+                        if (q < gqa) acc[q] = fmaf(S[q * kDecC + u], vv, acc[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < kDecMaxGqa; ++q) o[q] = acc[q];
+            }
+            __syncthreads();   // buffer k & 1 and the scores are free again
         }
-        __syncthreads();   // the chunk's rows, scores and positions are free again
     }
     // ---- this split's unnormalised result and its {max, sum}
     const int64_t base = (((int64_t)b * a.Hkv + h) * a.P + p) * gqa;
@@ -293,41 +328,77 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_attn_kernel(const DecAr
 }
 
 // O = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p for every query head.
+// The splits' {max, sum} are read in parallel; four groups of D threads then
+// take a quarter of the splits' partial outputs each.
 template <int D>
-__global__ void __launch_bounds__(D) decode_merge_kernel(const float *__restrict__ opart,
-                                                         const float2 *__restrict__ mpart,
-                                                         int Hq, int Hkv, int P,
-                                                         __nv_bfloat16 *__restrict__ O,
-                                                         float *__restrict__ lse)
+__global__ void __launch_bounds__(4 * D) decode_merge_kernel(const float *__restrict__ opart,
+                                                             const float2 *__restrict__ mpart,
+                                                             int Hq, int Hkv, int P,
+                                                             __nv_bfloat16 *__restrict__ O,
+                                                             float *__restrict__ lse)
 {
     grid_dep_sync();
+    __shared__ float wgt[kDecMaxSplits];
+    __shared__ float red[4 * D / 32], part[4][D];
+    __shared__ float Msh, Lsh;
     const int bh = blockIdx.x;               // b * Hq + hq
     const int b = bh / Hq, hq = bh - b * Hq;
     const int gqa = Hq / Hkv, h = hq / gqa, q = hq - h * gqa;
     const int64_t base = ((int64_t)b * Hkv + h) * P;
-    float M = -CUDART_INF_F;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, mpart[(base + p) * gqa + q].x);
-    float lsum = 0.f, acc = 0.f;
-    for (int p = 0; p < P; ++p) {
-        const float2 ml = mpart[(base + p) * gqa + q];
-        if (ml.x == -CUDART_INF_F) continue;
-        const float wgt = exp2f(ml.x - M);
-        lsum += wgt * ml.y;
-        acc += wgt * opart[((base + p) * gqa + q) * D + threadIdx.x];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float2 ml = make_float2(-CUDART_INF_F, 0.f);
+    if (tid < P) ml = mpart[(base + tid) * gqa + q];
+    float mx = ml.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float M = -CUDART_INF_F;
+        for (int w = 0; w < 4 * D / 32; ++w) M = fmaxf(M, red[w]);
+        Msh = M;
     }
-    const float out = lsum > 0.f ? acc / lsum : 0.f;
-    O[(int64_t)bh * D + threadIdx.x] = __float2bfloat16_rn(out);
-    if (lse && threadIdx.x == 0)
-        lse[bh] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994531f : -CUDART_INF_F;
+    __syncthreads();
+    const float M = Msh;
+    const float wv = (tid < P && ml.x != -CUDART_INF_F) ? exp2f(ml.x - M) : 0.f;
+    if (tid < P) wgt[tid] = wv;
+    float ls = wv * ml.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    __syncthreads();
+    if (lane == 0) red[warp] = ls;
+    __syncthreads();
+    if (tid == 0) {
+        float Lt = 0.f;
+        for (int w = 0; w < 4 * D / 32; ++w) Lt += red[w];
+        Lsh = Lt;
+    }
+    // partial outputs: group gq takes splits gq, gq + 4, ...; thread column c
+    const int gq = tid / D, c = tid - gq * D;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int pp = gq; pp < P; pp += 4) {
+        const float w = wgt[pp];
+        if (w != 0.f) acc += w * opart[((base + pp) * gqa + q) * D + c];
+    }
+    part[gq][c] = acc;
+    __syncthreads();
+    if (tid < D) {
+        const float lsum = Lsh;
+        const float tot = part[0][tid] + part[1][tid] + part[2][tid] + part[3][tid];
+        O[(int64_t)bh * D + tid] = __float2bfloat16_rn(lsum > 0.f ? tot / lsum : 0.f);
+        if (lse && tid == 0)
+            lse[bh] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
 }
 
 }  // namespace
 
 int decode_splits(int B, int Hkv)
 {
-    // about four CTAs per SM of 152 over all (batch, kv head) pairs
-    const int want = (4 * 152 + B * Hkv - 1) / (B * Hkv);
-    return want < 1 ? 1 : (want > 128 ? 128 : want);
+    // about three CTAs per SM of 152 over all (batch, kv head) pairs
+    const int want = (3 * 152 + B * Hkv - 1) / (B * Hkv);
+    return want < 1 ? 1 : (want > kDecMaxSplits ? kDecMaxSplits : want);
 }
 
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int d)
@@ -393,10 +464,10 @@ cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches)
     *launches += 1;
     prof_begin("decode_merge", s);
     if (p.d == 64)
-        e = launch_pdl(decode_merge_kernel<64>, dim3((unsigned)(p.B * p.Hq)), dim3(64), 0, s,
+        e = launch_pdl(decode_merge_kernel<64>, dim3((unsigned)(p.B * p.Hq)), dim3(256), 0, s,
                        a.opart, a.mpart, p.Hq, p.Hkv, P, p.O, p.lse);
     else
-        e = launch_pdl(decode_merge_kernel<128>, dim3((unsigned)(p.B * p.Hq)), dim3(128), 0, s,
+        e = launch_pdl(decode_merge_kernel<128>, dim3((unsigned)(p.B * p.Hq)), dim3(512), 0, s,
                        a.opart, a.mpart, p.Hq, p.Hkv, P, p.O, p.lse);
     prof_end(s);
     *launches += 1;

@@ -368,6 +368,18 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Closes the current group of this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most one group of this thread's cp.async copies is pending.
+__device__ __forceinline__ void cp_async_wait_group1()
+{
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
 // Loads 32 consecutive fp32 columns of this thread's TMEM lane and waits.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 {
