@@ -380,6 +380,12 @@ __device__ __forceinline__ void cp_async_wait_group1()
     asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
+// Waits until at most two groups of this thread's cp.async copies are pending.
+__device__ __forceinline__ void cp_async_wait_group2()
+{
+    asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+
 // Loads 32 consecutive fp32 columns of this thread's TMEM lane and waits.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 {
