@@ -6,22 +6,29 @@
 //
 // Group lists: glen[b][g] entries of gpos[b][g][0..cap), token positions in
 // ascending order.  decode_lists_init copies a prefill's bucketing
-// (offsets, pos) into that layout; decode_append puts the new token at the
-// end of its k lists (positions only grow, so the order holds).
+// (offsets, pos) into that layout; after the attention the new token joins
+// the end of its k lists (positions only grow, so the order holds).
 //
 // Attention of the new token i = L - 1 over its allowed set, split without
 // overlap into
-//   window keys  j in [i - w + 1, i]                    (every one allowed), and
+//   window keys  j in [i - w + 1, i]                    (every one allowed;
+//                at w = 0 the token's own key, through its own groups), and
 //   group keys   j in the list of g, i - j >= w, with g = min(G_i n G_j)
 //                (a pair sharing several groups is taken from the lowest).
 // The keys form one virtual sequence: the window, then the k lists.
-// decode_attn_kernel: CTA (p, kv head, batch) takes chunks p, p + P, ... of
-// 64 virtual keys, maps them to positions, drops the group keys that are not
-// its own (window or a lower shared group), copies the K and V rows of the
-// rest into shared memory (16-byte asynchronous copies), and runs an online
-// softmax for the query heads of the kv head in fp32.  decode_merge_kernel
-// combines the P partial results per query head.  HBM-bound: the K and V rows
-// of the allowed keys are the bytes that matter.
+//
+// decode_attn_kernel: CTA (split p, kv-head group, batch) takes an equal
+// slice of the virtual keys, maps it to positions once for all heads of its
+// group (dropping list keys that belong to a lower shared group), and streams
+// the kept keys' K and V rows in stages: one bulk copy per key and tensor
+// carries the rows of all HG heads of the group, which lie side by side in
+// the cache, so HBM sees runs of HG * d * 2 bytes.  A copy warp fills a
+// three-stage ring; eight MMA warps each take one (head, 16-key block) of a
+// stage: S = Q K^T and O += P V as m16n8k16 bf16 MMAs (the query heads of a
+// kv head are the tile's rows, fp32 accumulation) with an online softmax.
+// The warps of a head are merged in the CTA; decode_merge_kernel combines
+// the P splits per query head and then appends the new tokens to the lists.
+// HBM-bound: the K and V rows of the allowed keys are the bytes that matter.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -33,18 +40,24 @@ namespace focus {
 
 namespace {
 
-constexpr int kDecThreads = 128;
-constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kDecCtasPerSm = 2;     // resident decode CTAs per SM (registers)
-constexpr int kDecBlk = 16;          // kept keys per warp block: the k of one P V MMA
-constexpr int kDecStages = 3;        // blocks of a warp in flight: the current and two more
-constexpr int kDecVpt = 4;           // virtual keys per thread in a mapping pass
-constexpr int kDecSC = kDecVpt * kDecThreads;   // virtual keys per mapping pass
-constexpr int kDecMaxSplits = 128;   // splits per (batch, kv head), at most one per merge thread
+constexpr int kDecWarps = 8;                       // MMA warps; one more warp copies
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+constexpr int kDecBlk = 16;          // keys per warp block: the k of one P V MMA
+constexpr int kDecRows = kDecWarps * kDecBlk;      // (key, head) pairs per stage
+constexpr int kDecStages = 3;        // stages in flight: the one in use and two more
+constexpr int kDecVpt = 4;           // virtual keys per MMA thread in a mapping pass
+constexpr int kDecSC = kDecVpt * kDecWarps * 32;   // virtual keys per mapping pass
+constexpr int kDecMaxSplits = 256;   // splits per (batch, kv head), at most one per merge thread
 constexpr int kDecMaxGqa = 8;        // query heads per kv head: rows 0..7 of the MMA tile
 constexpr int kDecMaxTopk = 8;
 constexpr int kDecMaxK = 1024;       // groups: the new token's groups as a bit set in shared memory
 constexpr int kErrCapacity = 6;     // FOCUS_ERR_CAPACITY
+
+// kv heads per CTA: the largest of 8, 4, 2, 1 dividing Hkv
+__host__ __device__ inline int decode_hg(int Hkv)
+{
+    return Hkv % 8 == 0 ? 8 : Hkv % 4 == 0 ? 4 : Hkv % 2 == 0 ? 2 : 1;
+}
 
 __global__ void __launch_bounds__(256) decode_lists_init_kernel(
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ pos, int n, int K, int topk,
@@ -91,27 +104,26 @@ struct DecArgs {
     const int32_t *ids;        // [B, Lmax, topk]
     const int32_t *glen;       // [B, K]
     const int32_t *gpos;       // [B, K, cap]
-    int B, L, Lmax, Hq, Hkv, K, topk, cap, window, P;
+    int B, L, Lmax, Hq, Hkv, K, topk, cap, window, P, HG;
     float scale_log2;
-    float *opart;              // [B, Hkv, P, gqa, D] unnormalised O of each CTA
+    float *opart;              // [B, Hkv, P, gqa, D] unnormalised O of each split
     float2 *mpart;             // [B, Hkv, P, gqa]: {running max (base 2), sum}
     int *status;               // device status word (a wait that ran out)
 };
 
-// Shared memory of a decode CTA for head size D: per warp, kDecStages stages
-// of the K rows and the V rows of a block of kDecBlk kept keys, then the
-// positions of a pass's kept keys.  A row takes 16 bytes more than it holds,
-// so that the eight row addresses of an ldmatrix (same 16-byte unit, eight
-// consecutive rows) fall in eight different bank groups.  After the key loop
-// the stages hold the warps' partial outputs for the CTA merge.
+// Shared memory of a decode CTA for head size D: kDecStages stages, each the
+// K rows then the V rows of KS = kDecRows / HG keys (a key's row holds its HG
+// heads, HG * D * 2 bytes, plus 16 bytes so that the eight row addresses of
+// an ldmatrix, same head and unit of eight consecutive keys, fall in eight
+// different bank groups), then the positions of a pass's kept keys.  The
+// largest stage is that of HG = 1.  After the key loop the stages hold the
+// warps' partial outputs for the CTA merge.
 template <int D>
 struct DecSmem {
-    static constexpr int kRow = D * 2 + 16;                     // bytes per cached row
-    static constexpr int kBlk = kDecBlk * kRow;                 // K (or V) rows of a block
-    static constexpr int kWarp = kDecStages * 2 * kBlk;         // stages of K and V
-    static constexpr int kPos = kDecWarps * kWarp;              // int [kDecSC]
+    static constexpr int kStage = 2 * kDecRows * (D * 2 + 16);
+    static constexpr int kPos = kDecStages * kStage;            // int [kDecSC]
     static constexpr int kBytes = kPos + kDecSC * 4;
-    static_assert(kDecWarps * kDecMaxGqa * D * 4 <= kPos, "partial outputs fit the stages");
+    static_assert(kDecWarps * kDecMaxGqa * (D + 4) * 4 <= kPos, "partial outputs fit the stages");
 };
 
 __device__ __forceinline__ void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -145,12 +157,11 @@ __device__ __forceinline__ void mma_16816(float &c0, float &c1, uint32_t a0, uin
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f));
 }
 
-
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel(const DecArgs a)
+__global__ void __launch_bounds__(kDecThreads, 1) decode_attn_kernel(const DecArgs a)
 {
     using L = DecSmem<D>;
-    constexpr int kUnits = D / 8;    // 16-byte units per row = n-tiles of P V
+    constexpr int kUnits = D / 8;    // 16-byte units per head row = n-tiles of P V
     constexpr int kSteps = D / 16;   // k-steps of Q K^T = n-tile pairs of P V
     extern __shared__ __align__(128) uint8_t dsm[];
     int *spos = reinterpret_cast<int *>(dsm + L::kPos);
@@ -158,12 +169,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
     __shared__ int seg[kDecMaxTopk + 1];   // virtual-key bounds: window, then each list
     __shared__ int wcnt[kDecVpt * kDecWarps];
     __shared__ float wm[kDecWarps][kDecMaxGqa], wl[kDecWarps][kDecMaxGqa];
-    __shared__ __align__(8) uint64_t bars[kDecWarps][kDecStages];   // one per warp stage
+    __shared__ __align__(8) uint64_t full[kDecStages], empty[kDecStages];
     __shared__ int abort_flag;
     __shared__ uint32_t gmask[kDecMaxK / 32];   // the new token's groups
 
-    const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int p = blockIdx.x, hgrp = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool copier = warp == kDecWarps;
+    const int HG = a.HG;
+    const int KS = kDecRows / HG;                 // keys per stage
+    const int rowB = HG * D * 2 + 16;             // bytes per key row of a stage
+    const int hw = warp % HG, sb = warp / HG;     // an MMA warp's head in the group, key block
     const int gqa = a.Hq / a.Hkv;
     const int i = a.L - 1;
     const int topk = a.topk;
@@ -173,9 +189,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
     // of this step are ready, only the lists wait for the previous kernel
     uint32_t qa[kSteps][2];
     {
-        const bool live = qh < gqa;
+        const bool live = !copier && qh < gqa;
         const uint32_t *qr = reinterpret_cast<const uint32_t *>(
-            a.q + ((int64_t)b * a.Hq + h * gqa + (live ? qh : 0)) * D);
+            a.q + ((int64_t)b * a.Hq + (hgrp * HG + hw) * gqa + (live ? qh : 0)) * D);
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             qa[kk][0] = live ? qr[kk * 8 + (lane & 3)] : 0u;
@@ -183,7 +199,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
         }
     }
     if (tid < topk) gi[tid] = a.ids[((int64_t)b * a.Lmax + i) * topk + tid];
-    if (tid < kDecWarps * kDecStages) mbar_init(&bars[tid / kDecStages][tid % kDecStages], 1);
+    if (tid < kDecStages) {
+        mbar_init(&full[tid], 1);
+        mbar_init(&empty[tid], kDecWarps);
+    }
     if (tid == 0) abort_flag = 0;
     for (int x = tid; x < kDecMaxK / 32; x += kDecThreads) gmask[x] = 0u;
     mbar_fence_init();
@@ -215,41 +234,22 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
     float o[kUnits][2];                       // O tiles: rows = query heads, n = dims
 #pragma unroll
     for (int nt = 0; nt < kUnits; ++nt) o[nt][0] = o[nt][1] = 0.f;
-    uint8_t *wbuf = dsm + warp * L::kWarp;
-    uint32_t issued = 0, used = 0;   // blocks this warp has issued / consumed (stage = n % 3)
-
-    // K and V rows of kept keys [16 t, 16 t + 16) into the next stage: one
-    // bulk copy per lane (lanes 0..15 the K rows, 16..31 the V rows).  Rows
-    // past the last kept key repeat the block's first key; their scores are
-    // masked.
-    auto issue = [&](int t, int nv) {
-        const int st = issued % kDecStages;
-        uint64_t *bar = &bars[warp][st];
-        if (lane == 0) mbar_arrive_expect_tx(bar, 2 * kDecBlk * D * 2);
-        __syncwarp();
-        const int u = lane & (kDecBlk - 1);
-        const int idx = t * kDecBlk + u;
-        const int j = spos[idx < nv ? idx : t * kDecBlk];
-        const int64_t row = ((int64_t)b * a.Lmax + j) * a.Hkv + h;
-        const __nv_bfloat16 *src = (lane < kDecBlk ? a.k : a.v) + row * D;
-        uint8_t *dst = wbuf + st * 2 * L::kBlk + (lane < kDecBlk ? 0 : L::kBlk) + u * L::kRow;
-        bulk_load(dst, src, D * 2, bar);
-        ++issued;
-    };
+    uint32_t kg = 0;                          // stages of this CTA so far
+    uint32_t armed = 0;                       // stages the copy warp has started
 
     // split p takes the virtual keys [lo, hi), kDecSC per pass
     const int per = (nvirt + a.P - 1) / a.P;
     const int lo = min(nvirt, p * per), hi = min(nvirt, lo + per);
     for (int vs = lo; vs < hi; vs += kDecSC) {
-        // ---- positions of the pass's virtual keys, kDecVpt per thread, all
-        // loads of a phase in flight together
+        // ---- positions of the pass's virtual keys, kDecVpt per MMA thread,
+        // all loads of a phase in flight together
         int jj[kDecVpt], gs[kDecVpt];
 #pragma unroll
         for (int r = 0; r < kDecVpt; ++r) {
-            const int vk = vs + r * kDecThreads + tid;
+            const int vk = vs + r * (kDecWarps * 32) + tid;
             jj[r] = -1;
             gs[r] = -1;
-            if (vk < hi) {
+            if (!copier && vk < hi) {
                 if (vk < nw) {
                     jj[r] = i - vk;
                 } else {
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
 #pragma unroll
         for (int r = 0; r < kDecVpt; ++r) {
             bal[r] = __ballot_sync(0xffffffffu, jj[r] >= 0);
-            if (lane == 0) wcnt[r * kDecWarps + warp] = __popc(bal[r]);
+            if (lane == 0 && !copier) wcnt[r * kDecWarps + warp] = __popc(bal[r]);
         }
         __syncthreads();
         int run = 0, basev[kDecVpt];
@@ -313,123 +313,168 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_attn_kernel
             if (jj[r] >= 0) spos[basev[r] + __popc(bal[r] & below)] = jj[r];
         __syncthreads();
 
-        // ---- blocks of kDecBlk kept keys: warp w takes blocks w, w + 4, ...
-        // with the copies of its next two blocks in flight during the current one
-        const int nb = (nv + kDecBlk - 1) / kDecBlk;
-        for (int t = warp, k = 0; t < nb && k < kDecStages - 1; t += kDecWarps, ++k) issue(t, nv);
-        for (int t = warp; t < nb; t += kDecWarps) {
-            const int ahead = (kDecStages - 1) * kDecWarps;
-            if (t + ahead < nb) issue(t + ahead, nv);   // into the stage freed last
-            const int st = used % kDecStages;
-            if (!mbar_wait(&bars[warp][st], (used / kDecStages) & 1, &abort_flag, a.status))
-                break;
-            ++used;
-            const uint8_t *kb = wbuf + st * 2 * L::kBlk;
-            const uint8_t *vb = kb + L::kBlk;
-            const int cnt = min(kDecBlk, nv - t * kDecBlk);
-            // S = Q K^T for 16 keys (two n-tiles of 8)
-            float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-            {
-                const int ku = ((lane >> 4) << 3) + (lane & 7);
-#pragma unroll
-                for (int kk = 0; kk < kSteps; ++kk) {
-                    const int x = 2 * kk + ((lane >> 3) & 1);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kb + ku * L::kRow + (x << 4), r0, r1, r2, r3);
-                    mma_16816(s0[0], s0[1], qa[kk][0], qa[kk][1], r0, r1);
-                    mma_16816(s1[0], s1[1], qa[kk][0], qa[kk][1], r2, r3);
+        // ---- stages of KS kept keys
+        const int nst = (nv + KS - 1) / KS;
+        if (copier) {
+            // one bulk copy per (key, tensor): the key's rows of the group's
+            // HG heads; keys past the last kept one repeat the stage's first
+            // (their scores are masked)
+            for (int k = 0; k < nst; ++k, ++kg) {
+                const int st = kg % kDecStages;
+                if (kg >= kDecStages &&
+                    !mbar_wait(&empty[st], ((kg / kDecStages) - 1) & 1, &abort_flag, a.status))
+                    break;
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * KS * HG * D * 2);
+                __syncwarp();
+                uint8_t *sbase = dsm + st * L::kStage;
+                for (int c = lane; c < 2 * KS; c += 32) {
+                    const int which = c >= KS, u = c - which * KS;
+                    const int idx = k * KS + u;
+                    const int j = spos[idx < nv ? idx : k * KS];
+                    const int64_t row = ((int64_t)b * a.Lmax + j) * a.Hkv + hgrp * HG;
+                    bulk_load(sbase + (which * KS + u) * rowB, (which ? a.v : a.k) + row * D,
+                              HG * D * 2, &full[st]);
                 }
+                ++armed;
             }
-            // online softmax for head qh over keys 2c, 2c + 1, 8 + 2c, 9 + 2c
-            const int c2 = 2 * (lane & 3);
-            const float t0 = c2 < cnt ? s0[0] * a.scale_log2 : -CUDART_INF_F;
-            const float t1 = c2 + 1 < cnt ? s0[1] * a.scale_log2 : -CUDART_INF_F;
-            const float t2 = c2 + 8 < cnt ? s1[0] * a.scale_log2 : -CUDART_INF_F;
-            const float t3 = c2 + 9 < cnt ? s1[1] * a.scale_log2 : -CUDART_INF_F;
-            float mx = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mnew = fmaxf(mrun, mx);          // finite: key 0 of a block is kept
-            const float alpha = exp2f(mrun - mnew);      // 0 on the first block
-            const float p0 = exp2f(t0 - mnew), p1 = exp2f(t1 - mnew);
-            const float p2 = exp2f(t2 - mnew), p3 = exp2f(t3 - mnew);
-            lrun = lrun * alpha + ((p0 + p1) + (p2 + p3));
-            mrun = mnew;
+        } else {
+            for (int k = 0; k < nst; ++k, ++kg) {
+                const int st = kg % kDecStages;
+                if (!mbar_wait(&full[st], (kg / kDecStages) & 1, &abort_flag, a.status)) break;
+                const int k0 = k * KS + sb * kDecBlk;   // this warp's first key of the stage
+                const int cnt = min(kDecBlk, nv - k0);
+                if (cnt > 0) {
+                    const uint8_t *kb = dsm + st * L::kStage + (sb * kDecBlk) * rowB + hw * D * 2;
+                    const uint8_t *vb = kb + KS * rowB;
+                    // S = Q K^T for 16 keys (two n-tiles of 8), two chains per tile
+                    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+                    float e0[2] = {0.f, 0.f}, e1[2] = {0.f, 0.f};
+                    {
+                        const int ku = ((lane >> 4) << 3) + (lane & 7);
 #pragma unroll
-            for (int nt = 0; nt < kUnits; ++nt) {
-                o[nt][0] *= alpha;
-                o[nt][1] *= alpha;
-            }
-            // O += P V (P as the A fragment straight from the S tiles)
-            const uint32_t pa0 = pack_bf16x2(p0, p1), pa2 = pack_bf16x2(p2, p3);
-            {
-                const int vu = (((lane >> 3) & 1) << 3) + (lane & 7);
+                        for (int kk = 0; kk < kSteps; ++kk) {
+                            const int x = 2 * kk + ((lane >> 3) & 1);
+                            uint32_t r0, r1, r2, r3;
+                            ldsm_x4(kb + ku * rowB + (x << 4), r0, r1, r2, r3);
+                            if (kk & 1) {
+                                mma_16816(e0[0], e0[1], qa[kk][0], qa[kk][1], r0, r1);
+                                mma_16816(e1[0], e1[1], qa[kk][0], qa[kk][1], r2, r3);
+                            } else {
+                                mma_16816(s0[0], s0[1], qa[kk][0], qa[kk][1], r0, r1);
+                                mma_16816(s1[0], s1[1], qa[kk][0], qa[kk][1], r2, r3);
+                            }
+                        }
+                    }
+                    // online softmax for head qh over keys 2c, 2c + 1, 8 + 2c, 9 + 2c
+                    const int c2 = 2 * (lane & 3);
+                    const float sc = a.scale_log2;
+                    const float t0 = c2 < cnt ? (s0[0] + e0[0]) * sc : -CUDART_INF_F;
+                    const float t1 = c2 + 1 < cnt ? (s0[1] + e0[1]) * sc : -CUDART_INF_F;
+                    const float t2 = c2 + 8 < cnt ? (s1[0] + e1[0]) * sc : -CUDART_INF_F;
+                    const float t3 = c2 + 9 < cnt ? (s1[1] + e1[1]) * sc : -CUDART_INF_F;
+                    float mx = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float mnew = fmaxf(mrun, mx);       // finite: key 0 of a block is kept
+                    const float alpha = exp2f(mrun - mnew);   // 0 on the first block
+                    const float p0 = exp2f(t0 - mnew), p1 = exp2f(t1 - mnew);
+                    const float p2 = exp2f(t2 - mnew), p3 = exp2f(t3 - mnew);
+                    lrun = lrun * alpha + ((p0 + p1) + (p2 + p3));
+                    mrun = mnew;
 #pragma unroll
-                for (int jp = 0; jp < kSteps; ++jp) {
-                    const int x = 2 * jp + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vb + vu * L::kRow + (x << 4), r0, r1, r2, r3);
-                    mma_16816(o[2 * jp][0], o[2 * jp][1], pa0, pa2, r0, r1);
-                    mma_16816(o[2 * jp + 1][0], o[2 * jp + 1][1], pa0, pa2, r2, r3);
+                    for (int nt = 0; nt < kUnits; ++nt) {
+                        o[nt][0] *= alpha;
+                        o[nt][1] *= alpha;
+                    }
+                    // O += P V (P as the A fragment straight from the S tiles)
+                    const uint32_t pa0 = pack_bf16x2(p0, p1), pa2 = pack_bf16x2(p2, p3);
+                    const int vu = (((lane >> 3) & 1) << 3) + (lane & 7);
+#pragma unroll
+                    for (int jp = 0; jp < kSteps; ++jp) {
+                        const int x = 2 * jp + (lane >> 4);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4_t(vb + vu * rowB + (x << 4), r0, r1, r2, r3);
+                        mma_16816(o[2 * jp][0], o[2 * jp][1], pa0, pa2, r0, r1);
+                        mma_16816(o[2 * jp + 1][0], o[2 * jp + 1][1], pa0, pa2, r2, r3);
+                    }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the stage
             }
-            __syncwarp();   // the stage is free for the copies issued next
         }
         __syncthreads();    // spos and wcnt are rewritten by the next pass
         if (abort_flag) break;
     }
     if (abort_flag) {
-        // a wait ran out: let this warp's copies still in flight land, then
-        // leave without a result (the status word holds the timeout)
-        const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
-        for (; used < issued; ++used)
-            mbar_wait_until(&bars[warp][used % kDecStages], (used / kDecStages) & 1, deadline);
+        // a wait ran out: the copy warp lets its copies still in flight land,
+        // then the CTA leaves without a result (the status word holds the timeout)
+        if (copier) {
+            const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+            for (uint32_t u = armed > kDecStages ? armed - kDecStages : 0; u < armed; ++u)
+                mbar_wait_until(&full[u % kDecStages], (u / kDecStages) & 1, deadline);
+        }
         return;
     }
 
-    // ---- merge the four warps, then write this split's unnormalised result
+    // ---- merge the warps of each head, then write this split's unnormalised
+    // result for the group's HG kv heads
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
-    if ((lane & 3) == 0 && qh < gqa) {
+    if (!copier && (lane & 3) == 0 && qh < gqa) {
         wm[warp][qh] = mrun;
         wl[warp][qh] = lrun;
     }
     __syncthreads();
-    float *ob = reinterpret_cast<float *>(dsm);   // [warp][head][D]
-    if (qh < gqa) {
+    // [warp][query head][D + 4]: the padding puts the eight query heads' rows
+    // of a float2 store in different bank groups
+    constexpr int kRowF = D + 4;
+    float *ob = reinterpret_cast<float *>(dsm);
+    if (!copier && qh < gqa) {
         float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w][qh]);
+        for (int w = hw; w < kDecWarps; w += HG) M = fmaxf(M, wm[w][qh]);
         const float wt = mrun == -CUDART_INF_F ? 0.f : exp2f(mrun - M);
-        float *orow = ob + (warp * kDecMaxGqa + qh) * D + 2 * (lane & 3);
+        float *orow = ob + (warp * kDecMaxGqa + qh) * kRowF + 2 * (lane & 3);
 #pragma unroll
         for (int nt = 0; nt < kUnits; ++nt)
             *reinterpret_cast<float2 *>(orow + nt * 8) = make_float2(o[nt][0] * wt, o[nt][1] * wt);
     }
     __syncthreads();
-    const int64_t base = (((int64_t)b * a.Hkv + h) * a.P + p) * gqa;
-    for (int e = tid; e < gqa * D; e += kDecThreads) {
-        const int hq = e / D, d = e - hq * D;
-        float acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) acc += ob[(w * kDecMaxGqa + hq) * D + d];
-        a.opart[(base + hq) * D + d] = acc;
+    const int64_t hbase = (int64_t)b * a.Hkv + hgrp * HG;   // first kv head of the group
+    {
+        // rows r = (head hh, query head qq) of the group, a float4 per thread
+        constexpr int kV = D / 4;
+        constexpr int kRowsPer = kDecThreads / kV;
+        const int c4 = tid % kV;
+        for (int r = tid / kV; r < HG * gqa; r += kRowsPer) {
+            const int hh = r / gqa, qq = r - hh * gqa;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = hh; w < kDecWarps; w += HG) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    ob + (w * kDecMaxGqa + qq) * kRowF + 4 * c4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<float4 *>(a.opart + (((hbase + hh) * a.P + p) * gqa + qq) * D +
+                                        4 * c4) = acc;
+        }
     }
-    if (tid < gqa) {
+    if (tid < HG * gqa) {
+        const int hh = tid / gqa, qq = tid - hh * gqa;
         float M = -CUDART_INF_F, Ls = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w][tid]);
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w)
-            if (wm[w][tid] != -CUDART_INF_F) Ls += wl[w][tid] * exp2f(wm[w][tid] - M);
-        a.mpart[base + tid] = make_float2(M, Ls);
+        for (int w = hh; w < kDecWarps; w += HG) M = fmaxf(M, wm[w][qq]);
+        for (int w = hh; w < kDecWarps; w += HG)
+            if (wm[w][qq] != -CUDART_INF_F) Ls += wl[w][qq] * exp2f(wm[w][qq] - M);
+        a.mpart[((hbase + hh) * a.P + p) * gqa + qq] = make_float2(M, Ls);
     }
 }
 
 // O = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p for every query head.
-// Four groups of D threads take every fourth split; each thread has its
-// column of all of its splits in flight before the weights are known.  After
-// the attention has read the lists, block 0 appends the new tokens to them.
+// Block (query head, 32 columns): warp g takes splits g, g + 8, ... of its
+// 32 columns, all of them in flight before the weights are known; the
+// splits' {max, sum} are read one per thread.  After the attention has read
+// the lists, the grid's last block appends the new tokens to them.
 struct DecAppend {
     const int32_t *ids;
     int B, Lmax, L, K, topk, cap;
@@ -437,18 +482,24 @@ struct DecAppend {
     int *status;
 };
 
+constexpr int kMrgCols = 32;                       // columns per merge block
+constexpr int kMrgWarps = 8;
+constexpr int kMrgThreads = kMrgWarps * 32;
+static_assert(kMrgThreads >= kDecMaxSplits, "one merge thread per split for the weights");
+
 template <int D>
-__global__ void __launch_bounds__(4 * D, 1) decode_merge_kernel(const float *__restrict__ opart,
-                                                             const float2 *__restrict__ mpart,
-                                                             int Hq, int Hkv, int P,
-                                                             __nv_bfloat16 *__restrict__ O,
-                                                             float *__restrict__ lse,
-                                                             const DecAppend ap)
+__global__ void __launch_bounds__(kMrgThreads) decode_merge_kernel(const float *__restrict__ opart,
+                                                                   const float2 *__restrict__ mpart,
+                                                                   int Hq, int Hkv, int P,
+                                                                   __nv_bfloat16 *__restrict__ O,
+                                                                   float *__restrict__ lse,
+                                                                   const DecAppend ap)
 {
-    constexpr int kPer = kDecMaxSplits / 4;   // splits per thread group, at most
+    constexpr int kPer = kDecMaxSplits / kMrgWarps;   // splits per thread, at most
+    constexpr int kChunks = D / kMrgCols;
     grid_dep_sync();
     __shared__ float wgt[kDecMaxSplits];
-    __shared__ float red[4 * D / 32], part[4][D];
+    __shared__ float red[kMrgWarps], part[kMrgWarps][kMrgCols];
     __shared__ float Msh, Lsh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == gridDim.x - 1) {       // the last block appends
@@ -457,16 +508,16 @@ __global__ void __launch_bounds__(4 * D, 1) decode_merge_kernel(const float *__r
                           ap.status);
         return;
     }
-    const int bh = blockIdx.x;               // b * Hq + hq
+    const int bh = blockIdx.x / kChunks;     // b * Hq + hq
+    const int col = (blockIdx.x - bh * kChunks) * kMrgCols + lane;
     const int b = bh / Hq, hq = bh - b * Hq;
     const int gqa = Hq / Hkv, h = hq / gqa, q = hq - h * gqa;
     const int64_t base = ((int64_t)b * Hkv + h) * P;
-    const int gq = tid / D, c = tid - gq * D;
     float ov[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int pp = gq + 4 * k;
-        ov[k] = pp < P ? opart[((base + pp) * gqa + q) * D + c] : 0.f;
+        const int pp = warp + kMrgWarps * k;
+        ov[k] = pp < P ? opart[((base + pp) * gqa + q) * D + col] : 0.f;
     }
     float2 ml = make_float2(-CUDART_INF_F, 0.f);
     if (tid < P) ml = mpart[(base + tid) * gqa + q];
@@ -477,7 +528,7 @@ __global__ void __launch_bounds__(4 * D, 1) decode_merge_kernel(const float *__r
     __syncthreads();
     if (tid == 0) {
         float M = -CUDART_INF_F;
-        for (int w = 0; w < 4 * D / 32; ++w) M = fmaxf(M, red[w]);
+        for (int w = 0; w < kMrgWarps; ++w) M = fmaxf(M, red[w]);
         Msh = M;
     }
     __syncthreads();
@@ -492,22 +543,24 @@ __global__ void __launch_bounds__(4 * D, 1) decode_merge_kernel(const float *__r
     __syncthreads();
     if (tid == 0) {
         float Lt = 0.f;
-        for (int w = 0; w < 4 * D / 32; ++w) Lt += red[w];
+        for (int w = 0; w < kMrgWarps; ++w) Lt += red[w];
         Lsh = Lt;
     }
     float acc = 0.f;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int pp = gq + 4 * k;
+        const int pp = warp + kMrgWarps * k;
         if (pp < P) acc += wgt[pp] * ov[k];
     }
-    part[gq][c] = acc;
+    part[warp][lane] = acc;
     __syncthreads();
-    if (tid < D) {
+    if (tid < kMrgCols) {
         const float lsum = Lsh;
-        const float tot = part[0][tid] + part[1][tid] + part[2][tid] + part[3][tid];
-        O[(int64_t)bh * D + tid] = __float2bfloat16_rn(lsum > 0.f ? tot / lsum : 0.f);
-        if (lse && tid == 0)
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMrgWarps; ++w) tot += part[w][tid];
+        O[(int64_t)bh * D + col] = __float2bfloat16_rn(lsum > 0.f ? tot / lsum : 0.f);
+        if (lse && col == 0)
             lse[bh] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994531f : -CUDART_INF_F;
     }
 }
@@ -516,8 +569,9 @@ __global__ void __launch_bounds__(4 * D, 1) decode_merge_kernel(const float *__r
 
 int decode_splits(int B, int Hkv)
 {
-    // about kDecCtasPerSm CTAs per SM of 152 over all (batch, kv head) pairs
-    const int want = (kDecCtasPerSm * 152 + B * Hkv - 1) / (B * Hkv);
+    // about one CTA per SM of 152 over all (batch, kv-head group) pairs
+    const int ctas = B * (Hkv / decode_hg(Hkv));
+    const int want = (152 + ctas - 1) / ctas;
     return want < 1 ? 1 : (want > kDecMaxSplits ? kDecMaxSplits : want);
 }
 
@@ -544,6 +598,7 @@ cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches)
 {
     cudaError_t e;
     const int P = decode_splits(p.B, p.Hkv);
+    const int HG = decode_hg(p.Hkv);
     const size_t rows = (size_t)p.B * p.Hkv * P * (p.Hq / p.Hkv);
     uint8_t *ws = static_cast<uint8_t *>(p.ws);
     DecArgs a;
@@ -563,11 +618,12 @@ cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches)
     a.cap = p.cap;
     a.window = p.window;
     a.P = P;
+    a.HG = HG;
     a.scale_log2 = p.scale_log2;
     a.opart = reinterpret_cast<float *>(ws);
     a.mpart = reinterpret_cast<float2 *>(ws + ((rows * p.d * 4 + 255) & ~(size_t)255));
     a.status = p.status;
-    const dim3 grid((unsigned)P, (unsigned)p.Hkv, (unsigned)p.B);
+    const dim3 grid((unsigned)P, (unsigned)(p.Hkv / HG), (unsigned)p.B);
     prof_begin("decode_attn", s);
     if (p.d == 64)
         e = launch_pdl(decode_attn_kernel<64>, grid, dim3(kDecThreads), DecSmem<64>::kBytes, s, a);
@@ -589,12 +645,13 @@ cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches)
     ap.gpos = p.gpos;
     ap.status = p.status;
     prof_begin("decode_merge", s);
+    const unsigned mblocks = (unsigned)(p.B * p.Hq * (p.d / kMrgCols) + 1);   // + the append
     if (p.d == 64)
-        e = launch_pdl(decode_merge_kernel<64>, dim3((unsigned)(p.B * p.Hq + 1)), dim3(256), 0, s,
-                       a.opart, a.mpart, p.Hq, p.Hkv, P, p.O, p.lse, ap);
+        e = launch_pdl(decode_merge_kernel<64>, dim3(mblocks), dim3(kMrgThreads), 0, s, a.opart,
+                       a.mpart, p.Hq, p.Hkv, P, p.O, p.lse, ap);
     else
-        e = launch_pdl(decode_merge_kernel<128>, dim3((unsigned)(p.B * p.Hq + 1)), dim3(512), 0, s,
-                       a.opart, a.mpart, p.Hq, p.Hkv, P, p.O, p.lse, ap);
+        e = launch_pdl(decode_merge_kernel<128>, dim3(mblocks), dim3(kMrgThreads), 0, s, a.opart,
+                       a.mpart, p.Hq, p.Hkv, P, p.O, p.lse, ap);
     prof_end(s);
     *launches += 1;
     return e;

@@ -60,8 +60,9 @@ DECODE_CASES = [
     (1, 400, 4, 6, 3, 64, 32, 1, 1000),   # the window covers the whole cache
     (3, 257, 3, 32, 8, 128, 64, 2, 128),  # GQA 4:1
     (1, 0, 5, 4, 2, 128, 4, 2, 2),        # no prefix: every list starts empty
-    (40, 3000, 2, 8, 8, 64, 4, 2, 256),   # B * Hkv = 320: one split, several mapping passes
-    (19, 3000, 2, 16, 8, 128, 8, 3, 64),  # B * Hkv = 152: two splits of several passes each
+    (152, 3000, 2, 2, 1, 64, 4, 2, 256),  # 152 sequences: one split each, several mapping passes
+    (40, 3000, 2, 8, 8, 64, 4, 2, 256),   # four splits of 8 kv heads each
+    (19, 3000, 2, 16, 8, 128, 8, 3, 64),  # eight splits, d = 128
 ]
 
 
