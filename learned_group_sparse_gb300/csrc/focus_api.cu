@@ -780,6 +780,7 @@ focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, c
     p.lse = lse;
     p.ws = ws;
     p.status = status;
+    if (wait_ctl(&p.wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     int launches = 0;
     cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream), &launches);
     if (e == cudaSuccess) g_last_launches = launches;

@@ -108,7 +108,7 @@ struct DecArgs {
     float scale_log2;
     float *opart;              // [B, Hkv, P, gqa, D] unnormalised O of each split
     float2 *mpart;             // [B, Hkv, P, gqa]: {running max (base 2), sum}
-    int *status;               // device status word (a wait that ran out)
+    WaitCtl wc;                // wait limit and device status word (a wait that ran out)
 };
 
 // Shared memory of a decode CTA for head size D: kDecStages stages, each the
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_attn_kernel(const DecAr
             for (int k = 0; k < nst; ++k, ++kg) {
                 const int st = kg % kDecStages;
                 if (kg >= kDecStages &&
-                    !mbar_wait(&empty[st], ((kg / kDecStages) - 1) & 1, &abort_flag, a.status))
+                    !mbar_wait(&empty[st], ((kg / kDecStages) - 1) & 1, &abort_flag, a.wc))
                     break;
                 if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * KS * HG * D * 2);
                 __syncwarp();
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_attn_kernel(const DecAr
         } else {
             for (int k = 0; k < nst; ++k, ++kg) {
                 const int st = kg % kDecStages;
-                if (!mbar_wait(&full[st], (kg / kDecStages) & 1, &abort_flag, a.status)) break;
+                if (!mbar_wait(&full[st], (kg / kDecStages) & 1, &abort_flag, a.wc)) break;
                 const int k0 = k * KS + sb * kDecBlk;   // this warp's first key of the stage
                 const int cnt = min(kDecBlk, nv - k0);
                 if (cnt > 0) {
@@ -622,7 +622,7 @@ cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches)
     a.scale_log2 = p.scale_log2;
     a.opart = reinterpret_cast<float *>(ws);
     a.mpart = reinterpret_cast<float2 *>(ws + ((rows * p.d * 4 + 255) & ~(size_t)255));
-    a.status = p.status;
+    a.wc = p.wc;
     const dim3 grid((unsigned)P, (unsigned)(p.Hkv / HG), (unsigned)p.B);
     prof_begin("decode_attn", s);
     if (p.d == 64)

@@ -162,6 +162,7 @@ struct DecodeLaunch {
     float *lse;
     void *ws;
     int *status;   // device status word (a list that would overflow)
+    WaitCtl wc;    // limit of the attention kernel's waits
 };
 int decode_splits(int B, int Hkv);
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int d);

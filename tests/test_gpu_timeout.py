@@ -58,3 +58,40 @@ def test_wait_timeout_reported_then_recovered(w):
     assert fg.focus_get_device_status(reset=True) == 0
     assert torch.equal(ids, ids_ref)
     assert torch.equal(O, O_ref)
+
+
+def test_decode_wait_timeout_reported_then_recovered():
+    """The decode attention's copy ring (bulk copies into shared memory, waits
+    on full and empty barriers) gives up on the one-nanosecond limit, lets its
+    copies land and reports FOCUS_ERR_TIMEOUT; with the limit back the same
+    step (lists restored) gives its normal result.  Four groups over 200K
+    tokens give every CTA about eighty stages, so that some wait has to wait."""
+    B, n, Hq, Hkv, d, K, topk, window = 1, 200000, 8, 8, 128, 4, 2, 128
+    g = torch.Generator(device="cuda").manual_seed(41)
+    ids = torch.topk(torch.rand(B * n, K, generator=g, device="cuda"), topk, dim=1).indices
+    ids = ids.to(torch.int32).view(B, n, topk).contiguous()
+    Kc = torch.randn(B, n, Hkv, d, generator=g, device="cuda", dtype=torch.bfloat16)
+    Vc = torch.randn(B, n, Hkv, d, generator=g, device="cuda", dtype=torch.bfloat16)
+    q = torch.randn(B, Hq, d, generator=g, device="cuda", dtype=torch.bfloat16)
+    off, pos, _ = fg.focus_bucket(ids[:, :n - 1].contiguous(), K)
+    glen, gpos = fg.focus_decode_lists_init(off, pos, K, topk, cap=n)
+    glen0 = glen.clone()
+
+    def run():
+        glen.copy_(glen0)
+        O, _ = fg.focus_decode_fwd(q, Kc, Vc, ids, n, window, glen, gpos, K)
+        return O
+
+    O_ref = run()
+    torch.cuda.synchronize()
+    assert fg.focus_get_device_status(reset=True) == 0
+    fg.focus_set_wait_limit(1)
+    try:
+        run()
+        st = fg.focus_get_device_status(reset=True)
+    finally:
+        fg.focus_set_wait_limit(0)
+    assert st == TIMEOUT
+    O = run()
+    assert fg.focus_get_device_status(reset=True) == 0
+    assert torch.equal(O, O_ref)
