@@ -35,6 +35,7 @@
 
 #include "focus_internal.h"
 #include "focus_ptx.cuh"
+#include "focus_wait.cuh"
 #include "focus_topk.cuh"
 
 namespace focus {
