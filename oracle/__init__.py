@@ -20,6 +20,9 @@ arrays.  Function-by-function sources:
   a shared group, causal (gist.science/nl Kerncomponenten 3; gist.science/zh
   2.1.2 and 2.1.3).
 * :func:`count_pairs` -- |A_i| by enumeration of the same rule.
+* :func:`sinkhorn` -- Sinkhorn normalisation of the training-time
+  token-group affinities (gist.science/nl Kerncomponenten 2; gist.science/zh
+  2.1.1): rows to mass 1, groups to equal mass n / K.
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 (brute force on tiny inputs, closed forms, special cases that reduce to
@@ -72,8 +75,9 @@ def _load():
                                              vp, i32, vp, i64, i32, vp, vp]
             lib.oracle_count_pairs.argtypes = [vp, i32, i32, i32, i32, vp, i64, vp, _I64P]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_sinkhorn.argtypes = [vp, i32, i32, i32, ctypes.c_double, i32, vp, vp, vp]
             for f in (lib.oracle_assign, lib.oracle_bucket, lib.oracle_attention,
-                      lib.oracle_count_pairs, lib.oracle_num_threads):
+                      lib.oracle_count_pairs, lib.oracle_num_threads, lib.oracle_sinkhorn):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -190,3 +194,19 @@ def count_pairs(ids, window, rows=None):
     if rc:
         raise ValueError("oracle_count_pairs: invalid arguments")
     return (per.reshape(B, n) if rows is None else per), int(tot.value)
+
+
+def sinkhorn(S, tau=1.0, iters=3, want_p=True):
+    """Sinkhorn-Knopp scaling of exp(S / tau), S [B, n, K] float32: `iters`
+    rounds of (rows to mass 1, then groups to mass n / K), from v = 1.
+    Returns (P [B, n, K] or None, log_u [B, n], log_v [B, K]), float64."""
+    S = np.ascontiguousarray(S, dtype=np.float32)
+    B, n, K = S.shape
+    P = np.empty((B, n, K), np.float64) if want_p else None
+    lu = np.empty((B, n), np.float64)
+    lv = np.empty((B, K), np.float64)
+    rc = _load().oracle_sinkhorn(_ptr(S), B, n, K, float(tau), int(iters), _ptr(P), _ptr(lu),
+                                 _ptr(lv))
+    if rc:
+        raise ValueError("oracle_sinkhorn: invalid arguments")
+    return P, lu, lv

@@ -14,6 +14,8 @@
  *   [ZH]  gist.science/zh, technical summary, section 2.1 "core
  *         architecture": 2.1.1 token grouping, 2.1.2 gated attention,
  *         2.1.3 inference optimisation (top-k discretisation).
+ *   [NL]  Kerncomponenten 2 and [ZH] 2.1.1 also name the Sinkhorn
+ *         normalisation of the training-time assignment (oracle_sinkhorn).
  *
  * Arithmetic: every dot product and softmax sum is accumulated in double;
  * scores and outputs are rounded to float once.  bf16 inputs arrive as raw
@@ -261,6 +263,83 @@ int oracle_count_pairs(const int32_t *ids, int B, int n, int topk, int window,
         sum += c;
     }
     *total = sum;
+    return 0;
+}
+
+/*
+ * Sinkhorn normalisation of token-group affinities ([NL] Kerncomponenten 2:
+ * balance forced as a hard structural constraint; [ZH] 2.1.1: Sinkhorn in
+ * place of softmax, so that every group receives an equal mass of tokens).
+ *
+ * The pages name the algorithm but not its parameters; the readings taken:
+ * kernel A_ic = exp(S_ic / tau); target masses a_i = 1 per token (each
+ * token's assignment is a distribution over the K groups) and b_c = n / K
+ * per group (equal mass); `iters` rounds of the Sinkhorn-Knopp scaling,
+ * each a row update then a column update, in the log domain:
+ *     log u_i = log a_i - log sum_c A_ic v_c
+ *     log v_c = log b_c - log sum_i A_ic u_i
+ * starting from v = 1, and P = diag(u) A diag(v).  Every sequence of the
+ * batch is normalised on its own.  Sums are taken as max + log sum exp in
+ * double.
+ *
+ *   S      [B, n, K] float
+ *   P      [B, n, K] double out (nullable)
+ *   log_u  [B, n]    double out (nullable)
+ *   log_v  [B, K]    double out (nullable)
+ */
+int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
+                    double *P, double *log_u, double *log_v)
+{
+    if (B < 1 || n < 1 || K < 1 || !(tau > 0.0) || iters < 1) return 1;
+    double *lu = (double *)malloc(sizeof(double) * (size_t)n);
+    double *lv = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!lu || !lv) {
+        free(lu);
+        free(lv);
+        return 2;
+    }
+    const double log_a = 0.0, log_b = log((double)n / (double)K);
+    for (int b = 0; b < B; ++b) {
+        const float *Sb = S + (size_t)b * n * K;
+        for (int c = 0; c < K; ++c) lv[c] = 0.0;
+        for (int t = 0; t < iters; ++t) {
+            /* rows: u_i = a_i / sum_c A_ic v_c */
+            for (int i = 0; i < n; ++i) {
+                double m = -INFINITY;
+                for (int c = 0; c < K; ++c) {
+                    const double x = (double)Sb[(size_t)i * K + c] / tau + lv[c];
+                    if (x > m) m = x;
+                }
+                double sum = 0.0;
+                for (int c = 0; c < K; ++c)
+                    sum += exp((double)Sb[(size_t)i * K + c] / tau + lv[c] - m);
+                lu[i] = log_a - (m + log(sum));
+            }
+            /* columns: v_c = b_c / sum_i A_ic u_i */
+            for (int c = 0; c < K; ++c) {
+                double m = -INFINITY;
+                for (int i = 0; i < n; ++i) {
+                    const double y = (double)Sb[(size_t)i * K + c] / tau + lu[i];
+                    if (y > m) m = y;
+                }
+                double sum = 0.0;
+                for (int i = 0; i < n; ++i)
+                    sum += exp((double)Sb[(size_t)i * K + c] / tau + lu[i] - m);
+                lv[c] = log_b - (m + log(sum));
+            }
+        }
+        if (P)
+            for (int i = 0; i < n; ++i)
+                for (int c = 0; c < K; ++c)
+                    P[((size_t)b * n + i) * K + c] =
+                        exp((double)Sb[(size_t)i * K + c] / tau + lu[i] + lv[c]);
+        if (log_u)
+            for (int i = 0; i < n; ++i) log_u[(size_t)b * n + i] = lu[i];
+        if (log_v)
+            for (int c = 0; c < K; ++c) log_v[(size_t)b * K + c] = lv[c];
+    }
+    free(lu);
+    free(lv);
     return 0;
 }
 

@@ -321,3 +321,85 @@ def test_bucket_matches_numpy(B, n, K, topk):
         np.testing.assert_array_equal(pos[b][inv[b].ravel()], flat_tok)
         grp = np.searchsorted(off[b], inv[b].ravel(), side="right") - 1
         np.testing.assert_array_equal(grp, ids[b].ravel())
+
+
+# ---------------------------------------------------------------- Sinkhorn
+
+def _rand_affinities(B, n, K, seed, scale=2.0):
+    r = np.random.default_rng(seed)
+    return (scale * r.standard_normal((B, n, K))).astype(np.float32)
+
+
+def test_sinkhorn_hand_worked_example():
+    """One round on a 2 x 2 matrix, worked by hand (tests/golden)."""
+    g = json.load(open(os.path.join(GOLDEN, "sinkhorn_2x2.json")))
+    S = np.array([[[0.0, np.log(2.0)], [np.log(3.0), 0.0]]], np.float32)
+    P, lu, lv = oracle.sinkhorn(S, g["tau"], g["iters"])
+    # S holds ln 2 and ln 3 rounded to float32: agreement to ~1e-7
+    np.testing.assert_allclose(P[0], np.array(g["P"]), atol=2e-7)
+    np.testing.assert_allclose(lu[0], np.array(g["log_u"]), atol=2e-7)
+    np.testing.assert_allclose(lv[0], np.array(g["log_v"]), atol=2e-7)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 7])
+def test_sinkhorn_rank_one_closed_form(iters):
+    """S_ic = alpha_i + beta_c (a rank-one kernel) is balanced by one round:
+    P = 1/K everywhere, whatever alpha and beta."""
+    r = np.random.default_rng(5)
+    n, K = 37, 6
+    S = (r.standard_normal((n, 1)) * 3 + r.standard_normal((1, K)) * 3).astype(np.float32)
+    P, _, _ = oracle.sinkhorn(S[None], 1.0, iters)
+    np.testing.assert_allclose(P[0], 1.0 / K, rtol=1e-5)
+
+
+@pytest.mark.parametrize("n,K", [(50, 4), (7, 13), (300, 64)])
+def test_sinkhorn_marginals(n, K):
+    """After every round the group masses are exactly n / K (the last
+    update); with many rounds the token masses converge to 1."""
+    S = _rand_affinities(2, n, K, seed=n + K)
+    P, _, _ = oracle.sinkhorn(S, 1.0, 1)
+    np.testing.assert_allclose(P.sum(axis=1), n / K, rtol=1e-12)
+    P, _, _ = oracle.sinkhorn(S, 1.0, 400)
+    np.testing.assert_allclose(P.sum(axis=1), n / K, rtol=1e-12)
+    np.testing.assert_allclose(P.sum(axis=2), 1.0, atol=1e-9)
+
+
+def test_sinkhorn_row_shift_and_temperature():
+    """A constant added to a token's row is absorbed by its u (P unchanged at
+    any round count); S / tau at tau = 1 equals S at temperature tau."""
+    S = _rand_affinities(1, 40, 8, seed=3)
+    shift = np.random.default_rng(4).standard_normal((1, 40, 1)).astype(np.float32) * 5
+    P0, _, _ = oracle.sinkhorn(S, 1.0, 3)
+    P1, _, _ = oracle.sinkhorn((S + shift).astype(np.float32), 1.0, 3)
+    np.testing.assert_allclose(P1, P0, rtol=1e-5, atol=1e-9)
+    Pt, _, _ = oracle.sinkhorn(S, 0.5, 3)
+    Ps, _, _ = oracle.sinkhorn((S / 0.5).astype(np.float32), 1.0, 3)
+    np.testing.assert_allclose(Pt, Ps, rtol=1e-12)
+
+
+def test_sinkhorn_permutations_and_batch():
+    """Permuting tokens or groups permutes P alike; each sequence of a batch
+    is normalised on its own."""
+    S = _rand_affinities(2, 30, 5, seed=8)
+    P, lu, lv = oracle.sinkhorn(S, 1.0, 4)
+    pt = np.random.default_rng(1).permutation(30)
+    pg = np.random.default_rng(2).permutation(5)
+    Pp, _, _ = oracle.sinkhorn(np.ascontiguousarray(S[:, pt][:, :, pg]), 1.0, 4)
+    np.testing.assert_allclose(Pp, P[:, pt][:, :, pg], rtol=1e-12)
+    P1, lu1, lv1 = oracle.sinkhorn(S[1:], 1.0, 4)
+    np.testing.assert_allclose(P1[0], P[1], rtol=1e-12)
+    np.testing.assert_allclose(lu1[0], lu[1], rtol=1e-12)
+    np.testing.assert_allclose(lv1[0], lv[1], rtol=1e-12)
+
+
+def test_sinkhorn_matches_multiplicative_scaling():
+    """The log-domain rounds against the plain multiplicative form of the
+    same scaling (u = a / (A v), v = b / (A^T u)) on a well-scaled problem."""
+    S = _rand_affinities(1, 20, 6, seed=11, scale=1.0)
+    P, _, _ = oracle.sinkhorn(S, 1.0, 5)
+    A = np.exp(S[0].astype(np.float64))
+    v = np.ones(6)
+    for _ in range(5):
+        u = 1.0 / (A @ v)
+        v = (20 / 6) / (A.T @ u)
+    np.testing.assert_allclose(P[0], u[:, None] * A * v[None, :], rtol=1e-10)
