@@ -54,6 +54,7 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-sinkhorn", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed loop only (for profiler launch lists)")
     return ap.parse_args()
@@ -373,6 +374,45 @@ def bench_decode(fg, torch, w, t, ids, flush, stream, peaks, kind, args):
             "what": "one new token per sequence (position n - 1), L2 flushed between steps"}
 
 
+SINKHORN_ROUNDS = 3
+
+
+def bench_sinkhorn(fg, torch, w, t, flush, stream, peaks, args):
+    """Sinkhorn normalisation of the workload's token-group affinities
+    ([B, n, K] fp32 with the mixture's structure), SINKHORN_ROUNDS rounds and
+    P written, timed alone with the L2 flushed before each call.  Algorithmic
+    bytes: one read of S per round, one more read of S and one write of P."""
+    from learned_group_sparse_gb300 import synth
+    S = synth.synthetic_affinities(w, t["comp"], device=t["Q"].device)
+    B, n, K = S.shape
+    P = torch.empty_like(S)
+    lu = torch.empty(B, n, dtype=torch.float32, device=S.device)
+    lv = torch.empty(B, K, dtype=torch.float32, device=S.device)
+    ws = torch.empty(fg.focus_sinkhorn_workspace_size(B, n, K), dtype=torch.uint8,
+                     device=S.device)
+    reps = max(5, min(50, args.steps))
+    evs = []
+    for k in range(3 + reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fg.focus_sinkhorn(S, 1.0, SINKHORN_ROUNDS, P=P, log_u=lu, log_v=lv, ws=ws)
+        b.record(stream)
+        if k >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    mat = B * n * K * 4
+    alg = (SINKHORN_ROUNDS + 1) * mat + mat + (B * n + B * K) * 4
+    ach = alg / (ms * 1e-3) / 1e9
+    del S, P
+    return {"ms": ms, "rounds": SINKHORN_ROUNDS, "shape": [B, n, K], "algorithmic_bytes": alg,
+            "bound": "hbm", "achieved": ach, "unit": "GB/s", "peak": float(peaks["hbm_gbs"]),
+            "frac": ach / float(peaks["hbm_gbs"]), "reps": reps,
+            "what": "Sinkhorn rounds over the token-group affinities, P written, L2 flushed "
+                    "between calls"}
+
+
 def main():
     args = parse_args()
     from learned_group_sparse_gb300 import synth
@@ -535,6 +575,11 @@ def main():
     if not args.no_decode and n >= 2:
         decode = bench_decode(fg, torch, w, t, ids, flush, stream, peaks, kind, args)
 
+    # ---- Sinkhorn normalisation of the workload's token-group affinities
+    sinkhorn = None
+    if not args.no_sinkhorn:
+        sinkhorn = bench_sinkhorn(fg, torch, w, t, flush, stream, peaks, args)
+
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -602,6 +647,7 @@ def main():
             "attention_effective_tflops": eff_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
             "allowed_pairs": total_pairs, "group_pairs": share_pairs,
             "roofline": roof, "kernels": kernels, "dense_causal": dense, "decode": decode,
+            "sinkhorn": sinkhorn,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
             "context": "pages: 8.6x over full attention at 1M tokens (H100) and 2x from "

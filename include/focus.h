@@ -254,6 +254,35 @@ focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, c
                                 size_t ws_bytes, void *stream);
 
 /*
+ * focus_sinkhorn -- Sinkhorn normalisation of the training-time token-group
+ * affinities (gist.science/nl Kerncomponenten 2: group balance forced as a
+ * hard structural constraint; gist.science/zh technical summary 2.1.1:
+ * Sinkhorn instead of softmax, every group receiving an equal mass of
+ * tokens).  For each sequence b, the kernel A = exp(S_b / tau) is scaled to
+ * P = diag(u) A diag(v) by `iters` Sinkhorn-Knopp rounds from v = 1, each a
+ * row update u_i = 1 / sum_c A_ic v_c then a column update
+ * v_c = (n / K) / sum_i A_ic u_i: after every round each group's mass is
+ * n / K, and each token's mass tends to 1 as rounds are added.
+ *   S      [B, n, K] fp32 affinities (e.g. z_i . C_c), device
+ *   tau    temperature > 0 (0 selects 1)
+ *   iters  rounds, 1 <= iters <= 100000
+ *   P      [B, n, K] fp32 out, nullable (then only the potentials)
+ *   log_u  [B, n] fp32 out (natural log of u), nullable
+ *   log_v  [B, K] fp32 out (natural log of v), nullable
+ *   ws, ws_bytes: at least focus_sinkhorn_workspace_size(B, n, K) bytes.
+ * Arithmetic: fp32, base-2 log-sum-exp per row; a group mass that
+ * underflows float is taken as the smallest subnormal.  One read of S per
+ * round, plus one read of S and one write of P at the end.
+ * Supported: 1 <= K <= 1024, n >= 1, B >= 1.  Errors: FOCUS_ERR_INVALID_ARG
+ * for null or unaligned (16-byte) pointers or values out of range,
+ * FOCUS_ERR_WORKSPACE for a short workspace; nothing is launched then.
+ */
+size_t focus_sinkhorn_workspace_size(int B, int n, int K);
+focus_status_t focus_sinkhorn(const float *S, int B, int n, int K, float tau, int iters,
+                              float *P, float *log_u, float *log_v, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/*
  * focus_dense_causal_fwd -- plain causal attention (every j <= i) with the
  * same tcgen05 mainloop; the baseline the sparse path is compared with.
  *   Q [B, n, Hq, d], K/V [B, n, Hkv, d] bf16; O [B, n, Hq, d] bf16;

@@ -25,6 +25,7 @@ __all__ = [
     "focus_last_launch_count",
     "focus_status_string", "focus_version", "focus_profile_enable", "focus_profile_read",
     "focus_decode_workspace_size", "focus_decode_lists_init", "focus_decode_fwd",
+    "focus_sinkhorn_workspace_size", "focus_sinkhorn",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +75,8 @@ def library() -> ctypes.CDLL:
                 "focus_last_launch_count": ([], i32),
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_decode_workspace_size": ([i32] * 4, sz),
+                "focus_sinkhorn_workspace_size": ([i32] * 3, sz),
+                "focus_sinkhorn": ([vp, i32, i32, i32, f32, i32, vp, vp, vp, vp, sz, vp], i32),
                 "focus_decode_lists_init": ([vp, vp] + [i32] * 5 + [vp, vp, vp], i32),
                 "focus_decode_fwd": ([vp] * 4 + [i32] * 7 + [f32, i32, i32, vp, vp, i32, vp, vp,
                                      vp, sz, vp], i32),
@@ -310,6 +313,32 @@ def focus_prefill(X, Wg, C, Q, K, V, topk, window, scale=0.0, O=None, lse=None, 
         int(window), float(scale), _p(O), _p(lse), _p(ids_out), _p(ws), ws.numel(),
         1 if host else 0, s))
     return O, lse
+
+
+def focus_sinkhorn_workspace_size(B, n, K) -> int:
+    return int(library().focus_sinkhorn_workspace_size(B, n, K))
+
+
+def focus_sinkhorn(S, tau=1.0, iters=3, P=None, log_u=None, log_v=None, ws=None, want_p=True):
+    """Sinkhorn normalisation of affinities S [B, n, K] fp32 (rows to mass 1,
+    groups to mass n / K, `iters` rounds) -> (P [B, n, K] or None,
+    log_u [B, n], log_v [B, K]), fp32."""
+    _need(S, "S", torch.float32, 3)
+    B, n, K = S.shape
+    dev = S.device
+    if P is None and want_p:
+        P = torch.empty(B, n, K, dtype=torch.float32, device=dev)
+    if log_u is None:
+        log_u = torch.empty(B, n, dtype=torch.float32, device=dev)
+    if log_v is None:
+        log_v = torch.empty(B, K, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(1, focus_sinkhorn_workspace_size(B, n, K)), dtype=torch.uint8,
+                         device=dev)
+    _check("focus_sinkhorn", library().focus_sinkhorn(
+        _p(S), B, n, K, float(tau), int(iters), _p(P), _p(log_u), _p(log_v), _p(ws), ws.numel(),
+        _stream(S)))
+    return P, log_u, log_v
 
 
 def focus_decode_workspace_size(B, Hq, Hkv, d) -> int:

@@ -708,6 +708,33 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
     return cuda_status(e);
 }
 
+size_t focus_sinkhorn_workspace_size(int B, int n, int K)
+{
+    if (B < 1 || n < 1 || K < 1 || K > 1024) return 0;
+    return sinkhorn_ws_bytes(B, n, K);
+}
+
+focus_status_t focus_sinkhorn(const float *S, int B, int n, int K, float tau, int iters,
+                              float *P, float *log_u, float *log_v, void *ws, size_t ws_bytes,
+                              void *stream)
+{
+    if (!S || !ws) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(ws) || (P && !aligned16(P)) || (log_u && !aligned16(log_u)) ||
+        (log_v && !aligned16(log_v)))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 1 || K < 1 || K > 1024 || !(tau >= 0.f) || !(tau < INFINITY) || iters < 1 ||
+        iters > 100000 || (int64_t)B * n > ((int64_t)1 << 40))
+        return FOCUS_ERR_INVALID_ARG;
+    if (ws_bytes < sinkhorn_ws_bytes(B, n, K)) return FOCUS_ERR_WORKSPACE;
+    WaitCtl wc;
+    if (wait_ctl(&wc) != cudaSuccess) return FOCUS_ERR_CUDA;
+    int launches = 0;
+    cudaError_t e = launch_sinkhorn(S, B, n, K, tau > 0.f ? tau : 1.f, iters, P, log_u, log_v,
+                                    ws, wc, static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
 size_t focus_decode_workspace_size(int B, int Hq, int Hkv, int d)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0) return 0;

@@ -173,6 +173,13 @@ cudaError_t launch_decode_lists_init(const int32_t *offsets, const int32_t *pos,
                                      int *status, cudaStream_t s, int *launches);
 cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches);
 
+// ---- Sinkhorn normalisation of token-group affinities
+int sinkhorn_ctas(int B, int n, int K);
+size_t sinkhorn_ws_bytes(int B, int n, int K);
+cudaError_t launch_sinkhorn(const float *S, int B, int n, int K, float tau, int iters, float *P,
+                            float *log_u, float *log_v, void *ws, const WaitCtl &wc,
+                            cudaStream_t s, int *launches);
+
 // ---- tcgen05 attention kernels
 struct AttnLaunch {
     const CUtensorMap *tmQ, *tmK, *tmV;

@@ -159,6 +159,22 @@ def synthetic_ids(w: Workload, comp, device="cpu", gen=None, chunk_rows=1 << 16)
     return out.view(w.B, w.n, w.topk)
 
 
+def synthetic_affinities(w: Workload, comp, boost=4.0, device="cpu", gen=None,
+                         chunk_rows=1 << 16):
+    """Token-group affinities with the mixture's structure, for the Sinkhorn
+    normalisation: N(0, 1) everywhere plus `boost` on the token's own
+    component.  [B, n, K] float32."""
+    g = gen if gen is not None else _gen(device, w.seed + 5)
+    flat = comp.reshape(-1).to(device)
+    out = torch.empty(flat.numel(), w.K, dtype=torch.float32, device=device)
+    for s in range(0, flat.numel(), chunk_rows):
+        e = min(s + chunk_rows, flat.numel())
+        r = torch.randn(e - s, w.K, generator=g, device=device)
+        r.scatter_add_(1, flat[s:e, None], torch.full((e - s, 1), boost, device=device))
+        out[s:e] = r
+    return out.view(w.B, w.n, w.K)
+
+
 def make_all(w: Workload, device="cpu", with_x=True):
     """Every input of one forward pass, drawn in a fixed order."""
     Wg, C = make_params(w, device)

@@ -304,6 +304,7 @@ int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
         for (int c = 0; c < K; ++c) lv[c] = 0.0;
         for (int t = 0; t < iters; ++t) {
             /* rows: u_i = a_i / sum_c A_ic v_c */
+#pragma omp parallel for schedule(static)
             for (int i = 0; i < n; ++i) {
                 double m = -INFINITY;
                 for (int c = 0; c < K; ++c) {
@@ -316,6 +317,7 @@ int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
                 lu[i] = log_a - (m + log(sum));
             }
             /* columns: v_c = b_c / sum_i A_ic u_i */
+#pragma omp parallel for schedule(static)
             for (int c = 0; c < K; ++c) {
                 double m = -INFINITY;
                 for (int i = 0; i < n; ++i) {
@@ -329,6 +331,7 @@ int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
             }
         }
         if (P)
+#pragma omp parallel for schedule(static)
             for (int i = 0; i < n; ++i)
                 for (int c = 0; c < K; ++c)
                     P[((size_t)b * n + i) * K + c] =

@@ -131,6 +131,24 @@ def test_dense_and_count_validation(lib):
     assert lib.focus_count_pairs(P, P, P, P, 1, 64, 8, 2, -1, None, P, None) == INVALID
 
 
+def test_sinkhorn_validation(lib):
+    f = lib.focus_sinkhorn
+    need = fg.focus_sinkhorn_workspace_size(2, 1000, 64)
+    assert need >= 2 * 64 * 4 + 2 * 1000 * 4
+    assert fg.focus_sinkhorn_workspace_size(1, 10, 1025) == 0       # K above 1024
+    assert fg.focus_sinkhorn_workspace_size(1, 0, 8) == 0
+    ok = (P, 2, 1000, 64, 1.0, 3, P2, P2, P2, P2, need, None)
+    for k, bad in ((0, None), (0, MIS), (1, 0), (2, 0), (3, 0), (3, 1025), (4, -1.0),
+                   (4, float("nan")), (5, 0), (6, MIS), (7, MIS), (8, MIS), (9, None),
+                   (9, MIS)):
+        args = list(ok)
+        args[k] = bad
+        assert f(*args) == INVALID, (k, bad)
+    args = list(ok)
+    args[10] = need - 1
+    assert f(*args) == WORKSPACE
+
+
 def test_prefill_validation(lib):
     f = lib.focus_prefill
     need = fg.focus_prefill_workspace_size(1, 512, 64, 4, 4, 64, 16, 8, 2, 0)
