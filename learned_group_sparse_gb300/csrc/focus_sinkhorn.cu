@@ -38,8 +38,9 @@ constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkMaxK = 1024;
 constexpr int kSkBulkWarps = 16;             // warps of the bulk-copy sweep
 constexpr int kSkBulkThreads = kSkBulkWarps * 32;
-constexpr int kSkStages = 4;                 // stages of the bulk-copy sweep
-constexpr int kSkStageBytes = 32 * 1024;     // rows of S per stage: kSkStageBytes / (4 K)
+constexpr int kSkStages = 3;                 // stages of the bulk-copy sweep
+constexpr int kSkStageBytes = 64 * 1024;     // rows of S per stage: kSkStageBytes / (4 K)
+static_assert(kSkBulkWarps * kSkMaxK * 4 <= kSkStageBytes, "warp column masses fit a stage");
 
 struct SkArgs {
     const float *S;          // [B, n, K]
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(kSkThreads) sinkhorn_sweep_kernel(const SkArgs
 // row (32 LPR >= K), so a warp takes 32 / LPR rows at once and a row's max
 // and sum need log2(LPR) shuffles for all of them together; a lane reads
 // 16-byte groups 4 (j + LPR t) of its row (j its place in the row's lanes),
-// eight lanes covering 128 contiguous bytes.
+// eight lanes covering 128 contiguous bytes.  For K a power of two from 32
+// up, a stage is exactly one row per lane group of every warp.
 template <int LPR>
 __global__ void __launch_bounds__(kSkBulkThreads, 1) sinkhorn_sweep_bulk_kernel(const SkArgs a)
 {
@@ -142,7 +144,8 @@ __global__ void __launch_bounds__(kSkBulkThreads, 1) sinkhorn_sweep_bulk_kernel(
     grid_dep_sync();
     extern __shared__ __align__(128) uint8_t skm[];   // kSkStages x kSkStageBytes
     __shared__ __align__(16) float vs[kSkMaxK];
-    __shared__ __align__(16) float cm[kSkBulkWarps][kSkMaxK];
+    // after the last stage, stage 0 holds the warps' column masses
+    float(*cm)[kSkMaxK] = reinterpret_cast<float(*)[kSkMaxK]>(skm);
     __shared__ __align__(8) uint64_t full[kSkStages];
     __shared__ int abort_flag;
     const int b = blockIdx.y;
@@ -266,6 +269,91 @@ __global__ void __launch_bounds__(kSkBulkThreads, 1) sinkhorn_sweep_bulk_kernel(
     }
 }
 
+// P and log u through the same bulk-copy ring (K % 4 == 0): each lane turns
+// its 16-byte groups of a row into P and stores them as 16-byte words.
+template <int LPR>
+__global__ void __launch_bounds__(kSkBulkThreads, 1) sinkhorn_out_bulk_kernel(
+    const SkArgs a, float *__restrict__ P, float *__restrict__ log_u)
+{
+    constexpr int T = 8;
+    constexpr int RPW = 32 / LPR;
+    grid_dep_sync();
+    extern __shared__ __align__(128) uint8_t skm[];
+    __shared__ __align__(16) float vs[kSkMaxK];
+    __shared__ __align__(8) uint64_t full[kSkStages];
+    __shared__ int abort_flag;
+    const int b = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = lane / LPR, j = lane % LPR;
+    const int K = a.K;
+    const int RC = kSkStageBytes / (4 * K);
+    const int nchunks = (a.n + RC - 1) / RC;
+    const int mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / a.ctas + 1 : 0;
+    const float *Sb = a.S + (int64_t)b * a.n * K;
+    if (tid < kSkStages) mbar_init(&full[tid], 1);
+    if (tid == 0) abort_flag = 0;
+    for (int c = tid; c < kSkMaxK; c += kSkBulkThreads)
+        vs[c] = c < K ? a.v2[(int64_t)b * K + c] : 0.f;
+    mbar_fence_init();
+    __syncthreads();
+    auto arm = [&](int k) {
+        const int jc = blockIdx.x + k * a.ctas;
+        const int r0 = jc * RC, cnt = min(RC, a.n - r0);
+        uint64_t *bar = &full[k % kSkStages];
+        mbar_arrive_expect_tx(bar, (uint32_t)(cnt * K * 4));
+        bulk_load(skm + (k % kSkStages) * kSkStageBytes, Sb + (int64_t)r0 * K,
+                  (uint32_t)(cnt * K * 4), bar);
+    };
+    if (tid == 0)
+        for (int k = 0; k < kSkStages && k < mine; ++k) arm(k);
+    float4 vl[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const int c0 = 4 * (j + LPR * t);
+        vl[t] = c0 < K ? *reinterpret_cast<const float4 *>(vs + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    int k = 0;
+    for (; k < mine; ++k) {
+        const int st = k % kSkStages;
+        const bool ok = mbar_wait(&full[st], (uint32_t)(k / kSkStages) & 1u, &abort_flag, a.wc);
+        if (__syncthreads_or(!ok)) break;   // the whole CTA leaves together
+        const int r0 = (blockIdx.x + k * a.ctas) * RC, cnt = min(RC, a.n - r0);
+        const float *stage = reinterpret_cast<const float *>(skm + st * kSkStageBytes);
+        for (int rr0 = warp * RPW; rr0 < cnt; rr0 += kSkBulkWarps * RPW) {
+            const int rr = rr0 + grp;
+            if (rr < cnt) {
+                const int64_t row = (int64_t)b * a.n + r0 + rr;
+                const float u = a.u2[row];
+                if (log_u && j == 0) log_u[row] = u * 0.69314718055994531f;
+                if (P) {
+                    float *out = P + row * K;
+#pragma unroll
+                    for (int t = 0; t < T; ++t) {
+                        const int c0 = 4 * (j + LPR * t);
+                        if (c0 < K) {
+                            const float4 sv = *reinterpret_cast<const float4 *>(stage + rr * K + c0);
+                            float4 pv;
+                            pv.x = exp2f(fmaf(sv.x, a.k2, u + vl[t].x));
+                            pv.y = exp2f(fmaf(sv.y, a.k2, u + vl[t].y));
+                            pv.z = exp2f(fmaf(sv.z, a.k2, u + vl[t].z));
+                            pv.w = exp2f(fmaf(sv.w, a.k2, u + vl[t].w));
+                            __stcs(reinterpret_cast<float4 *>(out + c0), pv);
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();   // every warp is done with the stage
+        if (tid == 0 && k + kSkStages < mine) arm(k + kSkStages);
+    }
+    if (abort_flag && tid == 0) {
+        const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+        const int armed = min(mine, k + kSkStages);
+        for (int q = k; q < armed; ++q)
+            mbar_wait_until(&full[q % kSkStages], (uint32_t)(q / kSkStages) & 1u, deadline);
+    }
+}
+
 // Column update: log2 v_c += log2(n / K) - log2(sum of the CTAs' masses).  A
 // mass that underflows float is taken as the smallest subnormal.  Block
 // (32 columns, sequence b): warp w sums the partials w, w + 8, ...
@@ -364,6 +452,20 @@ cudaError_t sinkhorn_bulk_sweep(const SkArgs &a, cudaStream_t s)
     }
 }
 
+cudaError_t sinkhorn_bulk_out(const SkArgs &a, float *P, float *log_u, cudaStream_t s)
+{
+    const dim3 grid((unsigned)a.ctas, (unsigned)a.B), blk(kSkBulkThreads);
+    const size_t smem = (size_t)kSkStages * kSkStageBytes;
+    switch (sinkhorn_lpr(a.K)) {
+    case 1: return launch_pdl(sinkhorn_out_bulk_kernel<1>, grid, blk, smem, s, a, P, log_u);
+    case 2: return launch_pdl(sinkhorn_out_bulk_kernel<2>, grid, blk, smem, s, a, P, log_u);
+    case 4: return launch_pdl(sinkhorn_out_bulk_kernel<4>, grid, blk, smem, s, a, P, log_u);
+    case 8: return launch_pdl(sinkhorn_out_bulk_kernel<8>, grid, blk, smem, s, a, P, log_u);
+    case 16: return launch_pdl(sinkhorn_out_bulk_kernel<16>, grid, blk, smem, s, a, P, log_u);
+    default: return launch_pdl(sinkhorn_out_bulk_kernel<32>, grid, blk, smem, s, a, P, log_u);
+    }
+}
+
 template <int PER>
 cudaError_t sinkhorn_launch_t(const SkArgs &a, int iters, float *P, float *log_u, float *log_v,
                               cudaStream_t s, int *launches)
@@ -390,8 +492,11 @@ cudaError_t sinkhorn_launch_t(const SkArgs &a, int iters, float *P, float *log_u
         const int rows = (a.n + kSkWarps - 1) / kSkWarps;
         const int octas = min((4 * 152 + a.B - 1) / a.B, rows);
         prof_begin("sinkhorn_out", s);
-        e = launch_pdl(sinkhorn_out_kernel<PER>, dim3((unsigned)octas, (unsigned)a.B),
-                       dim3(kSkThreads), 0, s, a, P, log_u);
+        if (bulk && P)
+            e = sinkhorn_bulk_out(a, P, log_u, s);
+        else
+            e = launch_pdl(sinkhorn_out_kernel<PER>, dim3((unsigned)octas, (unsigned)a.B),
+                           dim3(kSkThreads), 0, s, a, P, log_u);
         prof_end(s);
         *launches += 1;
     }
@@ -408,14 +513,19 @@ cudaError_t sinkhorn_preflight(int K)
     std::call_once(once[idx], [&] {
         const int bytes = kSkStages * kSkStageBytes;
         const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+#define FOCUS_SK_ATTR(L)                                                              \
+    (cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<L>, at, bytes) != cudaSuccess        \
+         ? cudaErrorInvalidValue                                                          \
+         : cudaFuncSetAttribute(sinkhorn_out_bulk_kernel<L>, at, bytes))
         switch (idx) {
-        case 0: err[0] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<1>, at, bytes); break;
-        case 1: err[1] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<2>, at, bytes); break;
-        case 2: err[2] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<4>, at, bytes); break;
-        case 3: err[3] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<8>, at, bytes); break;
-        case 4: err[4] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<16>, at, bytes); break;
-        default: err[5] = cudaFuncSetAttribute(sinkhorn_sweep_bulk_kernel<32>, at, bytes); break;
+        case 0: err[0] = FOCUS_SK_ATTR(1); break;
+        case 1: err[1] = FOCUS_SK_ATTR(2); break;
+        case 2: err[2] = FOCUS_SK_ATTR(4); break;
+        case 3: err[3] = FOCUS_SK_ATTR(8); break;
+        case 4: err[4] = FOCUS_SK_ATTR(16); break;
+        default: err[5] = FOCUS_SK_ATTR(32); break;
         }
+#undef FOCUS_SK_ATTR
     });
     return err[idx];
 }

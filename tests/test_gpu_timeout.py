@@ -95,3 +95,25 @@ def test_decode_wait_timeout_reported_then_recovered():
     O = run()
     assert fg.focus_get_device_status(reset=True) == 0
     assert torch.equal(O, O_ref)
+
+
+def test_sinkhorn_wait_timeout_reported_then_recovered():
+    """The Sinkhorn sweep's bulk-copy ring gives up on the one-nanosecond
+    limit (the whole CTA leaves at its next barrier after letting the copies
+    land) and reports FOCUS_ERR_TIMEOUT; with the limit back the same call
+    gives its normal, bit-identical result."""
+    g = torch.Generator(device="cuda").manual_seed(43)
+    S = 2.0 * torch.randn(1, 200000, 256, generator=g, device="cuda")
+    P_ref, lu_ref, lv_ref = fg.focus_sinkhorn(S, 1.0, 3)
+    torch.cuda.synchronize()
+    assert fg.focus_get_device_status(reset=True) == 0
+    fg.focus_set_wait_limit(1)
+    try:
+        fg.focus_sinkhorn(S, 1.0, 3)
+        st = fg.focus_get_device_status(reset=True)
+    finally:
+        fg.focus_set_wait_limit(0)
+    assert st == TIMEOUT
+    P, lu, lv = fg.focus_sinkhorn(S, 1.0, 3)
+    assert fg.focus_get_device_status(reset=True) == 0
+    assert torch.equal(P, P_ref) and torch.equal(lu, lu_ref) and torch.equal(lv, lv_ref)
