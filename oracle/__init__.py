@@ -20,6 +20,9 @@ arrays.  Function-by-function sources:
   a shared group, causal (gist.science/nl Kerncomponenten 3; gist.science/zh
   2.1.2 and 2.1.3).
 * :func:`count_pairs` -- |A_i| by enumeration of the same rule.
+* :func:`gated_fwd`, :func:`gated_bwd` -- the soft-gated attention of
+  training over all causal pairs and its gradients (gist.science/zh 2.1.2;
+  gist.science/nl Kerncomponent 4).
 * :func:`sinkhorn` -- Sinkhorn normalisation of the training-time
   token-group affinities (gist.science/nl Kerncomponenten 2; gist.science/zh
   2.1.1): rows to mass 1, groups to equal mass n / K.
@@ -76,8 +79,12 @@ def _load():
             lib.oracle_count_pairs.argtypes = [vp, i32, i32, i32, i32, vp, i64, vp, _I64P]
             lib.oracle_num_threads.argtypes = []
             lib.oracle_sinkhorn.argtypes = [vp, i32, i32, i32, ctypes.c_double, i32, vp, vp, vp]
+            f64 = ctypes.c_double
+            lib.oracle_gated_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f64, f64, vp, vp]
+            lib.oracle_gated_bwd.argtypes = [vp] * 5 + [i32] * 7 + [f64, f64] + [vp] * 5
             for f in (lib.oracle_assign, lib.oracle_bucket, lib.oracle_attention,
-                      lib.oracle_count_pairs, lib.oracle_num_threads, lib.oracle_sinkhorn):
+                      lib.oracle_count_pairs, lib.oracle_num_threads, lib.oracle_sinkhorn,
+                      lib.oracle_gated_fwd, lib.oracle_gated_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -210,3 +217,43 @@ def sinkhorn(S, tau=1.0, iters=3, want_p=True):
     if rc:
         raise ValueError("oracle_sinkhorn: invalid arguments")
     return P, lu, lv
+
+
+def _gated_shapes(Q_bits, K_bits, V_bits, G):
+    Q, K, V = _bits16(Q_bits), _bits16(K_bits), _bits16(V_bits)
+    G = np.ascontiguousarray(G, dtype=np.float32)
+    B, n, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    return Q, K, V, G, B, n, Hq, Hkv, d, G.shape[2]
+
+
+def gated_fwd(Q_bits, K_bits, V_bits, G, window, lam, scale=0.0):
+    """Soft-gated causal attention: Q [B, n, Hq, d], K/V [B, n, Hkv, d] as bf16
+    bit patterns, G [B, n, Kg] float32 -> (O [B, n, Hq, d], LSE [B, Hq, n]),
+    float64."""
+    Q, K, V, G, B, n, Hq, Hkv, d, Kg = _gated_shapes(Q_bits, K_bits, V_bits, G)
+    O = np.empty((B, n, Hq, d), np.float64)
+    L = np.empty((B, Hq, n), np.float64)
+    rc = _load().oracle_gated_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), B, n, Hq, Hkv, d, Kg,
+                                  int(window), float(lam), float(scale), _ptr(O), _ptr(L))
+    if rc:
+        raise ValueError("oracle_gated_fwd: invalid arguments")
+    return O, L
+
+
+def gated_bwd(Q_bits, K_bits, V_bits, G, dO, window, lam, scale=0.0):
+    """Gradients of sum(O * dO) for the soft-gated attention -> (dQ, dK, dV,
+    dG, dlambda), float64."""
+    Q, K, V, G, B, n, Hq, Hkv, d, Kg = _gated_shapes(Q_bits, K_bits, V_bits, G)
+    dO = np.ascontiguousarray(dO, dtype=np.float32)
+    dQ = np.empty((B, n, Hq, d), np.float64)
+    dK = np.empty((B, n, Hkv, d), np.float64)
+    dV = np.empty((B, n, Hkv, d), np.float64)
+    dG = np.empty((B, n, Kg), np.float64)
+    dl = ctypes.c_double(0.0)
+    rc = _load().oracle_gated_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), _ptr(dO), B, n, Hq, Hkv,
+                                  d, Kg, int(window), float(lam), float(scale), _ptr(dQ),
+                                  _ptr(dK), _ptr(dV), _ptr(dG), ctypes.byref(dl))
+    if rc:
+        raise ValueError("oracle_gated_bwd: invalid arguments")
+    return dQ, dK, dV, dG, float(dl.value)

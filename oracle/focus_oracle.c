@@ -15,7 +15,8 @@
  *         architecture": 2.1.1 token grouping, 2.1.2 gated attention,
  *         2.1.3 inference optimisation (top-k discretisation).
  *   [NL]  Kerncomponenten 2 and [ZH] 2.1.1 also name the Sinkhorn
- *         normalisation of the training-time assignment (oracle_sinkhorn).
+ *         normalisation of the training-time assignment (oracle_sinkhorn),
+ *         and [ZH] 2.1.2 the soft gate of training (oracle_gated_fwd/bwd).
  *
  * Arithmetic: every dot product and softmax sum is accumulated in double;
  * scores and outputs are rounded to float once.  bf16 inputs arrive as raw
@@ -343,6 +344,163 @@ int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
     }
     free(lu);
     free(lv);
+    return 0;
+}
+
+/*
+ * Soft-gated attention of training ([ZH] 2.1.2 gated attention; [NL]
+ * Kerncomponent 4: during training every pair is computed, with soft
+ * gates).  The page prints the score as
+ *     s_ij = q_i . k_j * (1_local + (1 - 1_local) * sigma(lambda * a_ij))
+ * with a_ij the group affinity of tokens i and j.  Readings taken where the
+ * page leaves it open: 1_local = [i - j < w]; a_ij = g_i . g_j, the dot
+ * product of the two tokens' soft group assignments (rows of G, e.g. the
+ * Sinkhorn-normalised affinities); lambda a scalar; q . k scaled by `scale`
+ * (1/sqrt(d) when <= 0) before the gate; causal softmax over j <= i.
+ *
+ *   Q [B, n, Hq, d], K and V [B, n, Hkv, d] bf16 bits; G [B, n, Kg] float
+ *   O [B, n, Hq, d] double out; LSE [B, Hq, n] double out (natural log)
+ * oracle_gated_bwd takes dO [B, n, Hq, d] float and returns the gradients
+ * of sum(O * dO): dQ [B, n, Hq, d], dK and dV [B, n, Hkv, d], dG [B, n, Kg]
+ * (all double, overwritten) and d lambda.
+ */
+static double gated_score(const uint16_t *q, const uint16_t *k, const float *gi,
+                          const float *gj, int d, int Kg, double sc, double lambda, int local,
+                          double *t_out, double *a_out, double *gate_out)
+{
+    double dot = 0.0;
+    for (int e = 0; e < d; ++e) dot += bf16_bits_to_double(q[e]) * bf16_bits_to_double(k[e]);
+    double a = 0.0;
+    for (int c = 0; c < Kg; ++c) a += (double)gi[c] * (double)gj[c];
+    const double gate = local ? 1.0 : 1.0 / (1.0 + exp(-lambda * a));
+    *t_out = sc * dot;
+    *a_out = a;
+    *gate_out = gate;
+    return sc * dot * gate;
+}
+
+int oracle_gated_fwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, const float *G,
+                     int B, int n, int Hq, int Hkv, int d, int Kg, int window, double lambda,
+                     double scale, double *O, double *LSE)
+{
+    if (!Q || !Kt || !V || !G || !O || B < 1 || n < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+        d < 1 || Kg < 1 || window < 0)
+        return 1;
+    const double sc = scale > 0.0 ? scale : 1.0 / sqrt((double)d);
+    const int grp = Hq / Hkv;
+    int bh;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (bh = 0; bh < B * Hq; ++bh) {
+        const int b = bh / Hq, h = bh % Hq, kvh = h / grp;
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        for (int i = 0; i < n; ++i) {
+            const uint16_t *q = Q + (((size_t)b * n + i) * Hq + h) * d;
+            const float *gi = G + ((size_t)b * n + i) * Kg;
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double t, a, gate;
+                s[j] = gated_score(q, Kt + (((size_t)b * n + j) * Hkv + kvh) * d, gi,
+                                   G + ((size_t)b * n + j) * Kg, d, Kg, sc, lambda,
+                                   i - j < window, &t, &a, &gate);
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            double *o = O + (((size_t)b * n + i) * Hq + h) * d;
+            for (int e = 0; e < d; ++e) o[e] = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                const double p = exp(s[j] - m);
+                l += p;
+                const uint16_t *v = V + (((size_t)b * n + j) * Hkv + kvh) * d;
+                for (int e = 0; e < d; ++e) o[e] += p * bf16_bits_to_double(v[e]);
+            }
+            for (int e = 0; e < d; ++e) o[e] /= l;
+            if (LSE) LSE[((size_t)b * Hq + h) * n + i] = m + log(l);
+        }
+        free(s);
+    }
+    return 0;
+}
+
+int oracle_gated_bwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, const float *G,
+                     const float *dO, int B, int n, int Hq, int Hkv, int d, int Kg, int window,
+                     double lambda, double scale, double *dQ, double *dK, double *dV,
+                     double *dG, double *dlambda)
+{
+    if (!Q || !Kt || !V || !G || !dO || !dQ || !dK || !dV || !dG || !dlambda || B < 1 ||
+        n < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || Kg < 1 || window < 0)
+        return 1;
+    const double sc = scale > 0.0 ? scale : 1.0 / sqrt((double)d);
+    const int grp = Hq / Hkv;
+    memset(dQ, 0, sizeof(double) * (size_t)B * n * Hq * d);
+    memset(dK, 0, sizeof(double) * (size_t)B * n * Hkv * d);
+    memset(dV, 0, sizeof(double) * (size_t)B * n * Hkv * d);
+    memset(dG, 0, sizeof(double) * (size_t)B * n * Kg);
+    double dl = 0.0;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double *t = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a = (double *)malloc(sizeof(double) * (size_t)n);
+    double *gate = (double *)malloc(sizeof(double) * (size_t)n);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            const int kvh = h / grp;
+            for (int i = 0; i < n; ++i) {
+                const uint16_t *q = Q + (((size_t)b * n + i) * Hq + h) * d;
+                const float *gi = G + ((size_t)b * n + i) * Kg;
+                const float *go = dO + (((size_t)b * n + i) * Hq + h) * d;
+                double m = -INFINITY;
+                for (int j = 0; j <= i; ++j) {
+                    s[j] = gated_score(q, Kt + (((size_t)b * n + j) * Hkv + kvh) * d, gi,
+                                       G + ((size_t)b * n + j) * Kg, d, Kg, sc, lambda,
+                                       i - j < window, &t[j], &a[j], &gate[j]);
+                    if (s[j] > m) m = s[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j <= i; ++j) l += exp(s[j] - m);
+                /* P_ij, dP_ij = dO_i . v_j, D_i = sum_j P_ij dP_ij */
+                double D = 0.0;
+                for (int j = 0; j <= i; ++j) {
+                    const uint16_t *v = V + (((size_t)b * n + j) * Hkv + kvh) * d;
+                    double x = 0.0;
+                    for (int e = 0; e < d; ++e) x += (double)go[e] * bf16_bits_to_double(v[e]);
+                    dp[j] = x;
+                    D += exp(s[j] - m) / l * x;
+                }
+                for (int j = 0; j <= i; ++j) {
+                    const double P = exp(s[j] - m) / l;
+                    const double ds = P * (dp[j] - D);     /* d sum(O dO) / d s_ij */
+                    const double dt = ds * gate[j];
+                    const uint16_t *k = Kt + (((size_t)b * n + j) * Hkv + kvh) * d;
+                    double *dq = dQ + (((size_t)b * n + i) * Hq + h) * d;
+                    double *dk = dK + (((size_t)b * n + j) * Hkv + kvh) * d;
+                    double *dv = dV + (((size_t)b * n + j) * Hkv + kvh) * d;
+                    for (int e = 0; e < d; ++e) {
+                        dq[e] += sc * dt * bf16_bits_to_double(k[e]);
+                        dk[e] += sc * dt * bf16_bits_to_double(q[e]);
+                        dv[e] += P * (double)go[e];
+                    }
+                    if (!(i - j < window)) {
+                        const double dgate = ds * t[j];
+                        const double sp = gate[j] * (1.0 - gate[j]);   /* sigma' */
+                        const double da = dgate * lambda * sp;
+                        dl += dgate * a[j] * sp;
+                        const float *gj = G + ((size_t)b * n + j) * Kg;
+                        double *dgi = dG + ((size_t)b * n + i) * Kg;
+                        double *dgj = dG + ((size_t)b * n + j) * Kg;
+                        for (int c = 0; c < Kg; ++c) {
+                            dgi[c] += da * (double)gj[c];
+                            dgj[c] += da * (double)gi[c];
+                        }
+                    }
+                }
+            }
+        }
+    free(s);
+    free(t);
+    free(a);
+    free(gate);
+    free(dp);
+    *dlambda = dl;
     return 0;
 }
 

@@ -403,3 +403,101 @@ def test_sinkhorn_matches_multiplicative_scaling():
         u = 1.0 / (A @ v)
         v = (20 / 6) / (A.T @ u)
     np.testing.assert_allclose(P[0], u[:, None] * A * v[None, :], rtol=1e-10)
+
+
+# ------------------------------------------------- soft-gated attention (training)
+
+def _grid_bf16(shape, seed, step=2.0 ** -7, span=200):
+    """Values m * step with |m| < span: exact in bf16, and so are x +- step."""
+    r = np.random.default_rng(seed)
+    return (r.integers(-span, span, size=shape) * step).astype(np.float32)
+
+
+def _bits_of(x):
+    return synth.bits(torch.from_numpy(x).to(torch.bfloat16))
+
+
+def _sdpa64(Q, K, V, scale):
+    """Causal SDPA in float64 with torch, [B, n, H, d] layout, GQA expanded."""
+    q = torch.from_numpy(Q).double().transpose(1, 2)
+    grp = Q.shape[2] // K.shape[2]
+    k = torch.from_numpy(K).double().repeat_interleave(grp, dim=2).transpose(1, 2)
+    v = torch.from_numpy(V).double().repeat_interleave(grp, dim=2).transpose(1, 2)
+    return q, k, v
+
+
+@pytest.mark.parametrize("window,lam,scale_mul", [
+    (10 ** 6, 3.0, 1.0),    # every pair local: gate 1, plain causal attention
+    (0, 0.0, 0.5),          # no pair local, lambda 0: gate 1/2 everywhere
+])
+def test_gated_reduces_to_causal_sdpa(window, lam, scale_mul):
+    B, n, Hq, Hkv, d, Kg = 2, 23, 4, 2, 16, 5
+    Q = _grid_bf16((B, n, Hq, d), 1)
+    K = _grid_bf16((B, n, Hkv, d), 2)
+    V = _grid_bf16((B, n, Hkv, d), 3)
+    G = np.random.default_rng(4).random((B, n, Kg)).astype(np.float32)
+    dO = np.random.default_rng(5).standard_normal((B, n, Hq, d)).astype(np.float32)
+    O, L = oracle.gated_fwd(_bits_of(Q), _bits_of(K), _bits_of(V), G, window, lam)
+    dQ, dK, dV, dG, dl = oracle.gated_bwd(_bits_of(Q), _bits_of(K), _bits_of(V), G, dO, window,
+                                          lam)
+    q, k, v = _sdpa64(Q, K, V, 1.0)
+    q.requires_grad_(True)
+    k.requires_grad_(True)
+    v.requires_grad_(True)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                         scale=scale_mul / np.sqrt(d))
+    np.testing.assert_allclose(O, o.detach().transpose(1, 2).numpy(), atol=1e-12)
+    (o * torch.from_numpy(dO).double().transpose(1, 2)).sum().backward()
+    grp = Hq // Hkv
+    np.testing.assert_allclose(dQ, q.grad.transpose(1, 2).numpy(), atol=1e-11)
+    dk = k.grad.transpose(1, 2).numpy().reshape(B, n, Hkv, grp, d).sum(3)
+    dv = v.grad.transpose(1, 2).numpy().reshape(B, n, Hkv, grp, d).sum(3)
+    np.testing.assert_allclose(dK, dk, atol=1e-11)
+    np.testing.assert_allclose(dV, dv, atol=1e-11)
+    if window >= n:   # no gate anywhere: nothing flows to G or lambda
+        assert np.abs(dG).max() == 0.0 and dl == 0.0
+
+
+def test_gated_saturated_gate_is_plain_attention():
+    """lambda large with every affinity >= 0.5: sigma(lambda a) rounds to 1 in
+    double, so the result is causal attention whatever the window."""
+    B, n, Hq, Hkv, d, Kg = 1, 17, 2, 2, 8, 4
+    Q, K, V = _grid_bf16((B, n, Hq, d), 6), _grid_bf16((B, n, Hkv, d), 7), _grid_bf16((B, n, Hkv, d), 8)
+    G = np.full((B, n, Kg), 0.5, np.float32)   # a_ij = 1
+    O, _ = oracle.gated_fwd(_bits_of(Q), _bits_of(K), _bits_of(V), G, 3, 80.0)
+    q, k, v = _sdpa64(Q, K, V, 1.0)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                         scale=1 / np.sqrt(d))
+    np.testing.assert_allclose(O, o.transpose(1, 2).numpy(), atol=1e-12)
+
+
+def test_gated_gradients_by_finite_differences():
+    """Central differences of L = sum(O * dO) with steps exact in bf16 (Q, K,
+    V on a 2^-7 grid), in float32 (G) and in double (lambda), against every
+    gradient of the backward, on a case with local and gated pairs."""
+    B, n, Hq, Hkv, d, Kg, window, lam = 1, 9, 2, 1, 4, 3, 3, 2.5
+    h = 2.0 ** -7
+    Q, K, V = _grid_bf16((B, n, Hq, d), 11), _grid_bf16((B, n, Hkv, d), 12), _grid_bf16((B, n, Hkv, d), 13)
+    G = (np.random.default_rng(14).integers(1, 100, size=(B, n, Kg)) * 2.0 ** -7).astype(np.float32)
+    dO = np.random.default_rng(15).standard_normal((B, n, Hq, d)).astype(np.float32)
+
+    def loss(Qx=Q, Kx=K, Vx=V, Gx=G, lx=lam):
+        O, _ = oracle.gated_fwd(_bits_of(Qx), _bits_of(Kx), _bits_of(Vx), Gx, window, lx)
+        return float((O * dO).sum())
+
+    dQ, dK, dV, dG, dl = oracle.gated_bwd(_bits_of(Q), _bits_of(K), _bits_of(V), G, dO, window,
+                                          lam)
+    for name, X, grad in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV), ("G", G, dG)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(*X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = dict(Qx=Q, Kx=K, Vx=V, Gx=G)
+            args_m = dict(Qx=Q, Kx=K, Vx=V, Gx=G)
+            args_p[name + "x"], args_m[name + "x"] = Xp, Xm
+            num[idx] = (loss(**args_p) - loss(**args_m)) / (2 * h)
+        err = np.abs(num - grad).max()
+        assert err <= 2e-3 * max(1.0, np.abs(grad).max()), (name, err)
+    numl = (loss(lx=lam + 1e-5) - loss(lx=lam - 1e-5)) / 2e-5
+    assert abs(numl - dl) <= 1e-6 * max(1.0, abs(dl)), (numl, dl)
