@@ -254,6 +254,44 @@ focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, c
                                 size_t ws_bytes, void *stream);
 
 /*
+ * focus_gated_attention_fwd / _bwd -- the soft-gated attention of training
+ * over every causal pair (gist.science/zh technical summary 2.1.2 "gated
+ * attention"; gist.science/nl Kerncomponent 4: soft gates over all pairs in
+ * training), and its backward.  The page prints the score as
+ *     s_ij = q_i . k_j * (1_local + (1 - 1_local) * sigma(lambda * a_ij));
+ * readings: 1_local = [i - j < window], a_ij = g_i . g_j (the tokens' soft
+ * group assignments, rows of G, e.g. P of focus_sinkhorn), q . k scaled by
+ * `scale` (0 selects 1/sqrt(d)) before the gate, softmax over j <= i.
+ *   Q [B, n, Hq, d], K and V [B, n, Hkv, d] bf16; G [B, n, Kg] fp32
+ *   fwd: O [B, n, Hq, d] bf16 out; lse [B, Hq, n] fp32 out (natural log),
+ *        needed by the backward
+ *   bwd: O, lse from the forward; dO [B, n, Hq, d] bf16 (the gradient of the
+ *        loss by O) -> dQ [B, n, Hq, d], dK and dV [B, n, Hkv, d],
+ *        dG [B, n, Kg] fp32, *dlambda fp32 (one value, device), all overwritten
+ *   ws, ws_bytes: at least focus_gated_workspace_size(B, n, Hq, Kg) bytes.
+ * Arithmetic: tensor-core tiles with fp32 accumulation: Q K^T, P V and the
+ * gradient products in bf16, G G^T and the dG products in fp16; the gate,
+ * softmax and dS in fp32.  The backward recomputes P from lse; every sum has
+ * a fixed order (no atomics), so results repeat bit for bit.
+ * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= Kg <= 128, window >= 0,
+ * n >= 1.  Errors: FOCUS_ERR_INVALID_ARG (null or unaligned pointers, values
+ * out of range), FOCUS_ERR_UNSUPPORTED, FOCUS_ERR_WORKSPACE; nothing is
+ * launched then.
+ */
+size_t focus_gated_workspace_size(int B, int n, int Hq, int Kg);
+focus_status_t focus_gated_attention_fwd(const void *Q, const void *K, const void *V,
+                                         const float *G, int B, int n, int Hq, int Hkv, int d,
+                                         int Kg, int window, float lambda, float scale, void *O,
+                                         float *lse, void *ws, size_t ws_bytes, void *stream);
+focus_status_t focus_gated_attention_bwd(const void *Q, const void *K, const void *V,
+                                         const float *G, const void *O, const float *lse,
+                                         const void *dO, int B, int n, int Hq, int Hkv, int d,
+                                         int Kg, int window, float lambda, float scale,
+                                         float *dQ, float *dK, float *dV, float *dG,
+                                         float *dlambda, void *ws, size_t ws_bytes,
+                                         void *stream);
+
+/*
  * focus_sinkhorn -- Sinkhorn normalisation of the training-time token-group
  * affinities (gist.science/nl Kerncomponenten 2: group balance forced as a
  * hard structural constraint; gist.science/zh technical summary 2.1.1:

@@ -26,6 +26,7 @@ __all__ = [
     "focus_status_string", "focus_version", "focus_profile_enable", "focus_profile_read",
     "focus_decode_workspace_size", "focus_decode_lists_init", "focus_decode_fwd",
     "focus_sinkhorn_workspace_size", "focus_sinkhorn",
+    "focus_gated_workspace_size", "focus_gated_attention_fwd", "focus_gated_attention_bwd",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +77,11 @@ def library() -> ctypes.CDLL:
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_decode_workspace_size": ([i32] * 4, sz),
                 "focus_sinkhorn_workspace_size": ([i32] * 3, sz),
+                "focus_gated_workspace_size": ([i32] * 4, sz),
+                "focus_gated_attention_fwd": ([vp] * 4 + [i32] * 7 + [f32, f32, vp, vp, vp, sz,
+                                              vp], i32),
+                "focus_gated_attention_bwd": ([vp] * 7 + [i32] * 7 + [f32, f32] + [vp] * 6 +
+                                              [sz, vp], i32),
                 "focus_sinkhorn": ([vp, i32, i32, i32, f32, i32, vp, vp, vp, vp, sz, vp], i32),
                 "focus_decode_lists_init": ([vp, vp] + [i32] * 5 + [vp, vp, vp], i32),
                 "focus_decode_fwd": ([vp] * 4 + [i32] * 7 + [f32, i32, i32, vp, vp, i32, vp, vp,
@@ -313,6 +319,64 @@ def focus_prefill(X, Wg, C, Q, K, V, topk, window, scale=0.0, O=None, lse=None, 
         int(window), float(scale), _p(O), _p(lse), _p(ids_out), _p(ws), ws.numel(),
         1 if host else 0, s))
     return O, lse
+
+
+def focus_gated_workspace_size(B, n, Hq, Kg) -> int:
+    return int(library().focus_gated_workspace_size(B, n, Hq, Kg))
+
+
+def _gated_common(Q, K, V, G):
+    _need(Q, "Q", torch.bfloat16, 4)
+    _need(K, "K", torch.bfloat16, 4)
+    _need(V, "V", torch.bfloat16, 4)
+    _need(G, "G", torch.float32, 3)
+    B, n, Hq, d = Q.shape
+    return B, n, Hq, K.shape[2], d, G.shape[2]
+
+
+def focus_gated_attention_fwd(Q, K, V, G, window, lam, scale=0.0, O=None, lse=None, ws=None):
+    """Soft-gated causal attention of training: Q [B, n, Hq, d], K/V
+    [B, n, Hkv, d] bf16, G [B, n, Kg] fp32 soft assignments -> (O bf16,
+    lse [B, Hq, n] fp32)."""
+    B, n, Hq, Hkv, d, Kg = _gated_common(Q, K, V, G)
+    if O is None:
+        O = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty(B, Hq, n, dtype=torch.float32, device=Q.device)
+    if ws is None:
+        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Kg)), dtype=torch.uint8,
+                         device=Q.device)
+    _check("focus_gated_attention_fwd", library().focus_gated_attention_fwd(
+        _p(Q), _p(K), _p(V), _p(G), B, n, Hq, Hkv, d, Kg, int(window), float(lam), float(scale),
+        _p(O), _p(lse), _p(ws), ws.numel(), _stream(Q)))
+    return O, lse
+
+
+def focus_gated_attention_bwd(Q, K, V, G, O, lse, dO, window, lam, scale=0.0, ws=None,
+                              out=None):
+    """Gradients of the soft-gated attention -> (dQ, dK, dV, dG, dlambda),
+    fp32 tensors (dlambda of one element).  out: optional tuple of the five
+    output tensors to fill."""
+    B, n, Hq, Hkv, d, Kg = _gated_common(Q, K, V, G)
+    _need(O, "O", torch.bfloat16, 4)
+    _need(dO, "dO", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    dev = Q.device
+    if out is None:
+        out = (torch.empty(B, n, Hq, d, dtype=torch.float32, device=dev),
+               torch.empty(B, n, Hkv, d, dtype=torch.float32, device=dev),
+               torch.empty(B, n, Hkv, d, dtype=torch.float32, device=dev),
+               torch.empty(B, n, Kg, dtype=torch.float32, device=dev),
+               torch.empty(1, dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Kg)), dtype=torch.uint8,
+                         device=dev)
+    dQ, dK, dV, dG, dl = out
+    _check("focus_gated_attention_bwd", library().focus_gated_attention_bwd(
+        _p(Q), _p(K), _p(V), _p(G), _p(O), _p(lse), _p(dO), B, n, Hq, Hkv, d, Kg, int(window),
+        float(lam), float(scale), _p(dQ), _p(dK), _p(dV), _p(dG), _p(dl), _p(ws), ws.numel(),
+        _stream(Q)))
+    return dQ, dK, dV, dG, dl
 
 
 def focus_sinkhorn_workspace_size(B, n, K) -> int:

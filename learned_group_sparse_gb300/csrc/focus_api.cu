@@ -708,6 +708,104 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
     return cuda_status(e);
 }
 
+size_t focus_gated_workspace_size(int B, int n, int Hq, int Kg)
+{
+    if (B < 1 || n < 1 || Hq < 1 || Kg < 1 || Kg > 128) return 0;
+    return gated_ws_bytes(B, n, Hq, Kg);
+}
+
+static focus_status_t check_gated(const void *Q, const void *K, const void *V, const float *G,
+                                  int B, int n, int Hq, int Hkv, int d, int Kg, int window,
+                                  float lambda, float scale, const void *ws, size_t ws_bytes)
+{
+    if (!Q || !K || !V || !G || !ws) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(G) || !aligned16(ws))
+        return FOCUS_ERR_INVALID_ARG;
+    if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Kg < 1 || window < 0 ||
+        !(fabsf(lambda) < INFINITY) || !(scale >= 0.f) || !(scale < INFINITY))
+        return FOCUS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || Kg > 128 || (int64_t)B * n * Hq * d >= ((int64_t)1 << 40) ||
+        (n + 63) / 64 > 65535 || Hq > 65535 || B > 65535)
+        return FOCUS_ERR_UNSUPPORTED;
+    if (ws_bytes < gated_ws_bytes(B, n, Hq, Kg)) return FOCUS_ERR_WORKSPACE;
+    return FOCUS_OK;
+}
+
+focus_status_t focus_gated_attention_fwd(const void *Q, const void *K, const void *V,
+                                         const float *G, int B, int n, int Hq, int Hkv, int d,
+                                         int Kg, int window, float lambda, float scale, void *O,
+                                         float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    focus_status_t st = check_gated(Q, K, V, G, B, n, Hq, Hkv, d, Kg, window, lambda, scale, ws,
+                                    ws_bytes);
+    if (st) return st;
+    if (!O || !lse || !aligned16(O) || !aligned16(lse)) return FOCUS_ERR_INVALID_ARG;
+    if (gated_preflight(d, Kg) != cudaSuccess) return FOCUS_ERR_CUDA;
+    GatedLaunch p{};
+    p.q = static_cast<const __nv_bfloat16 *>(Q);
+    p.k = static_cast<const __nv_bfloat16 *>(K);
+    p.v = static_cast<const __nv_bfloat16 *>(V);
+    p.G = G;
+    p.out = static_cast<__nv_bfloat16 *>(O);
+    p.lse_out = lse;
+    p.B = B;
+    p.n = n;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.Kg = Kg;
+    p.window = window;
+    p.lambda = lambda;
+    p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    int launches = 0;
+    cudaError_t e = launch_gated_fwd(p, ws, static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
+focus_status_t focus_gated_attention_bwd(const void *Q, const void *K, const void *V,
+                                         const float *G, const void *O, const float *lse,
+                                         const void *dO, int B, int n, int Hq, int Hkv, int d,
+                                         int Kg, int window, float lambda, float scale,
+                                         float *dQ, float *dK, float *dV, float *dG,
+                                         float *dlambda, void *ws, size_t ws_bytes, void *stream)
+{
+    focus_status_t st = check_gated(Q, K, V, G, B, n, Hq, Hkv, d, Kg, window, lambda, scale, ws,
+                                    ws_bytes);
+    if (st) return st;
+    if (!O || !lse || !dO || !dQ || !dK || !dV || !dG || !dlambda) return FOCUS_ERR_INVALID_ARG;
+    if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+        !aligned16(dV) || !aligned16(dG) || ((uintptr_t)dlambda & 3u))
+        return FOCUS_ERR_INVALID_ARG;
+    if (gated_preflight(d, Kg) != cudaSuccess) return FOCUS_ERR_CUDA;
+    GatedLaunch p{};
+    p.q = static_cast<const __nv_bfloat16 *>(Q);
+    p.k = static_cast<const __nv_bfloat16 *>(K);
+    p.v = static_cast<const __nv_bfloat16 *>(V);
+    p.o = static_cast<const __nv_bfloat16 *>(O);
+    p.dO = static_cast<const __nv_bfloat16 *>(dO);
+    p.G = G;
+    p.lse = lse;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.dg = dG;
+    p.dlam = dlambda;
+    p.B = B;
+    p.n = n;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.Kg = Kg;
+    p.window = window;
+    p.lambda = lambda;
+    p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    int launches = 0;
+    cudaError_t e = launch_gated_bwd(p, ws, static_cast<cudaStream_t>(stream), &launches);
+    if (e == cudaSuccess) g_last_launches = launches;
+    return cuda_status(e);
+}
+
 size_t focus_sinkhorn_workspace_size(int B, int n, int K)
 {
     if (B < 1 || n < 1 || K < 1 || K > 1024) return 0;

@@ -1,0 +1,867 @@
+// Soft-gated attention of training and its backward (Focus, gist.science/zh
+// technical summary 2.1.2 "gated attention": the score is
+//     s_ij = q_i . k_j * (1_local + (1 - 1_local) * sigma(lambda * a_ij)),
+// computed for every causal pair while training; gist.science/nl
+// Kerncomponent 4: soft gates over all pairs in training, hard top-k at
+// inference).  Readings: 1_local = [i - j < w]; a_ij = g_i . g_j, the dot
+// product of the tokens' soft group assignments (rows of G); q . k is scaled
+// by `scale` before the gate; causal softmax over j <= i.
+//
+// All kernels tile queries and keys by 64; a warp owns 16 rows of a tile and
+// runs m16n8k16 tensor-core MMAs (`mma.sync`, fp32 accumulation): S = Q K^T
+// in bf16 and A = G_q G_k^T in fp16 (G is converted once to fp16, its
+// columns padded to a multiple of 16 with zeros), then the gate and the
+// online softmax in registers, P V with P in bf16.  The per-pair work is a
+// few tile products over d and K_g, so these are contractions of the
+// classic flash-attention shape with M = 16 rows per warp.
+//
+// Forward: gated_fwd_kernel, CTA (64 queries, query head, batch); O in bf16
+// and the log-sum-exp.  Backward (each kernel recomputes P from the
+// log-sum-exp, so none needs atomics and every sum has a fixed order):
+//   gated_bwd_prep_kernel   D_i = dO_i . O_i per (row, head)
+//   gated_bwd_dq_kernel     CTA (64 queries, batch), every head: dQ, the
+//                           row side of dG (sum_j da_ij g_j) and d lambda
+//   gated_bwd_dkv_kernel    CTA (64 keys, kv head, batch): dK, dV over the
+//                           query heads of the kv head
+//   gated_bwd_dgk_kernel    CTA (64 keys, batch), every head: the column side
+//                           of dG (sum_i da_ij g_i), added to the row side
+// with dS_ij = P_ij (dP_ij - D_i), dP_ij = dO_i . v_j, and for a gated pair
+// d gate_ij = dS_ij t_ij, da_ij = d gate_ij lambda sigma (1 - sigma).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "focus_internal.h"
+#include "focus_ptx.cuh"
+
+namespace focus {
+
+namespace {
+
+constexpr int kGT = 64;               // rows per tile (queries or keys)
+constexpr int kGWarps = 4;            // 16 rows per warp
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kGMaxKs = 8;            // k-steps of 16 over the padded groups: K_g <= 128
+
+struct GatedArgs {
+    const __nv_bfloat16 *q, *k, *v;   // [B, n, Hq | Hkv, D]
+    const __half *g;                  // [B, n, kp] fp16, zero-padded columns
+    const __nv_bfloat16 *o, *dO;      // [B, n, Hq, D]
+    const float *lse;                 // [B, Hq, n] natural log
+    const float *Dd;                  // [B, Hq, n] dO . O
+    __nv_bfloat16 *out;               // O (forward)
+    float *lse_out;                   // forward
+    float *dq, *dk, *dv, *dg;         // [B, n, Hq, D], [B, n, Hkv, D] x 2, [B, n, Kg]
+    float *dlam_part;                 // [B, n / 64 tiles] partial d lambda
+    int B, n, Hq, Hkv, kp, Kg, window;
+    float scale, lambda;
+};
+
+__device__ __forceinline__ void g_ldsm_x4(const void *p, uint32_t *r)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void g_ldsm_x4_t(const void *p, uint32_t *r)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+// c += A B, m16n8k16, bf16 or fp16 inputs, fp32 accumulation
+__device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment of a 16 x 16 block of rows stored [row][col] with `stride` bytes
+// per row, at (row 0, column c0).
+__device__ __forceinline__ void lda(const uint8_t *base, int stride, int c0, int lane,
+                                    uint32_t *a)
+{
+    const int r = lane & 15, c = c0 + ((lane >> 4) << 3);
+    g_ldsm_x4(base + r * stride + c * 2, a);
+}
+
+// B fragments of two n-tiles (rows 0..7 and 8..15 of a [n][k] array, k = c0
+// .. c0 + 15): b[0], b[1] for the first n-tile, b[2], b[3] for the second.
+__device__ __forceinline__ void ldb_nk(const uint8_t *base, int stride, int c0, int lane,
+                                       uint32_t *b)
+{
+    const int r = ((lane >> 4) << 3) + (lane & 7), c = c0 + (((lane >> 3) & 1) << 3);
+    g_ldsm_x4(base + r * stride + c * 2, b);
+}
+
+// B fragments of two n-tiles from a [k][n] array (k rows 0..15, n columns
+// c0 .. c0 + 15): transposed loads.
+__device__ __forceinline__ void ldb_kn(const uint8_t *base, int stride, int c0, int lane,
+                                       uint32_t *b)
+{
+    const int r = (((lane >> 3) & 1) << 3) + (lane & 7), c = c0 + ((lane >> 4) << 3);
+    g_ldsm_x4_t(base + r * stride + c * 2, b);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// rows [r0, r0 + 64) of a [B, n, H, W] (16-bit) tensor, head h, into shared
+// rows of `stride` bytes; rows past n are zero-filled
+__device__ __forceinline__ void load_tile(uint8_t *dst, int stride, const void *src, int b, int n,
+                                          int H, int h, int W, int r0, int tid)
+{
+    const int units = W / 8;   // 16-byte units per row
+    const uint8_t *s8 = static_cast<const uint8_t *>(src);
+    for (int x = tid; x < kGT * units; x += kGThreads) {
+        const int r = x / units, u = x - r * units;
+        const int row = r0 + r;
+        const bool ok = row < n;
+        const int64_t off = ((((int64_t)b * n + (ok ? row : 0)) * H + h) * W + u * 8) * 2;
+        cp_async16(dst + r * stride + u * 16, s8 + off, ok ? 16u : 0u);
+    }
+}
+
+// Shared-memory rows: D bf16 (or kp fp16) values plus 16 bytes, so that the
+// eight row addresses of an ldmatrix fall in eight different bank groups.
+template <int D>
+struct GatedSmem {
+    static constexpr int kRow = D * 2 + 16;
+    static __host__ __device__ int g_row(int kp) { return kp * 2 + 16; }
+    // one stage: K and V tiles, then the G tile
+    static __host__ __device__ int stage(int kp) { return kGT * (2 * kRow + g_row(kp)); }
+};
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+
+// The gate of pair (i, j): 1 inside the window, else sigma(lambda a).
+__device__ __forceinline__ float gate_of(int i, int j, int window, float lambda, float aff)
+{
+    return (i - j < window) ? 1.f : sigmoidf_(lambda * aff);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kGThreads, 2) gated_fwd_kernel(const GatedArgs a)
+{
+    using L = GatedSmem<D>;
+    constexpr int kRow = L::kRow;
+    grid_dep_sync();
+    extern __shared__ __align__(128) uint8_t gsm[];
+    const int gRow = L::g_row(a.kp), stageB = L::stage(a.kp);
+    const int qt = gridDim.x - 1 - blockIdx.x;   // the longest rows first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int kvh = h / (a.Hq / a.Hkv);
+    const int q0 = qt * kGT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nks = a.kp / 16;
+    const float scale2 = a.scale * 1.4426950408889634f;
+
+    auto load_kv = [&](int kt, uint8_t *st) {
+        load_tile(st, kRow, a.k, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
+        load_tile(st + kGT * kRow, kRow, a.v, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
+        load_tile(st + 2 * kGT * kRow, gRow, a.g, b, a.n, 1, 0, a.kp, kt * kGT, tid);
+    };
+    // the query and G tiles pass through stage 1, key tile 0 goes to stage 0
+    uint8_t *s1 = gsm + stageB;
+    load_tile(s1, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
+    load_tile(s1 + kGT * kRow, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
+    load_kv(0, gsm);
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t qa[D / 16][4], ga[kGMaxKs][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) lda(s1 + 16 * warp * kRow, kRow, 16 * kk, lane, qa[kk]);
+#pragma unroll
+    for (int ks = 0; ks < kGMaxKs; ++ks)
+        if (ks < nks) lda(s1 + kGT * kRow + 16 * warp * gRow, gRow, 16 * ks, lane, ga[ks]);
+    __syncthreads();   // stage 1 is free
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.f, 0.f};
+    const int rbase = q0 + 16 * warp + (lane >> 2);
+    const int ntiles = qt + 1;
+    for (int kt = 0; kt < ntiles; ++kt) {
+        uint8_t *st = gsm + (kt & 1) * stageB;
+        if (kt + 1 < ntiles) load_kv(kt + 1, gsm + ((kt + 1) & 1) * stageB);
+        const uint8_t *Kt = st, *Vt = st + kGT * kRow, *Gt = st + 2 * kGT * kRow;
+        float s[8][4], ag[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bb[4];
+                ldb_nk(Kt + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                mma_bf16(s[2 * np], qa[kk], bb[0], bb[1]);
+                mma_bf16(s[2 * np + 1], qa[kk], bb[2], bb[3]);
+            }
+#pragma unroll
+        for (int ks = 0; ks < kGMaxKs; ++ks)
+            if (ks < nks)
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bb[4];
+                    ldb_nk(Gt + 16 * np * gRow, gRow, 16 * ks, lane, bb);
+                    mma_f16(ag[2 * np], ga[ks], bb[0], bb[1]);
+                    mma_f16(ag[2 * np + 1], ga[ks], bb[2], bb[3]);
+                }
+        // logits in base 2 with the gate; causal and length masks
+        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = rbase + ((e >> 1) << 3);
+                const int j = kt * kGT + 8 * nt + 2 * (lane & 3) + (e & 1);
+                const float x = s[nt][e] * scale2 * gate_of(i, j, a.window, a.lambda, ag[nt][e]);
+                s[nt][e] = (j <= i && j < a.n) ? x : -CUDART_INF_F;
+                mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+            }
+        float alpha[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+            const float mnew = fmaxf(mrow[r], mx[r]);   // finite: key 0 is allowed
+            alpha[r] = exp2f(mrow[r] - mnew);
+            mrow[r] = mnew;
+            lrow[r] *= alpha[r];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[nt][e] = exp2f(s[nt][e] - mrow[e >> 1]);
+                lrow[e >> 1] += s[nt][e];
+            }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            o[nt][0] *= alpha[0];
+            o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1];
+            o[nt][3] *= alpha[1];
+        }
+        // O += P V
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
+                                    pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
+                                    pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                    pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                uint32_t bb[4];
+                ldb_kn(Vt + 16 * kk * kRow, kRow, 16 * dp, lane, bb);
+                mma_bf16(o[2 * dp], pa, bb[0], bb[1]);
+                mma_bf16(o[2 * dp + 1], pa, bb[2], bb[3]);
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = rbase + 8 * r;
+        if (i >= a.n) continue;
+        const float inv = 1.f / lrow[r];
+        __nv_bfloat16 *orow = a.out + (((int64_t)b * a.n + i) * a.Hq + h) * D;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt)
+            *reinterpret_cast<__nv_bfloat162 *>(orow + 8 * nt + 2 * (lane & 3)) =
+                __floats2bfloat162_rn(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
+        if ((lane & 3) == 0)
+            a.lse_out[((int64_t)b * a.Hq + h) * a.n + i] =
+                (mrow[r] + log2f(lrow[r])) * 0.69314718055994531f;
+    }
+}
+
+// G [B, n, Kg] fp32 -> [B, n, kp] fp16 with zero columns past Kg.
+__global__ void gated_g16_kernel(const float *__restrict__ G, int64_t rows, int Kg, int kp,
+                                 __half *__restrict__ g16)
+{
+    grid_dep_sync();
+    const int64_t total = rows * kp;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = x / kp;
+        const int c = (int)(x - r * kp);
+        g16[x] = __float2half_rn(c < Kg ? G[r * Kg + c] : 0.f);
+    }
+}
+
+// D[b, h, i] = dO_i . O_i (bf16 inputs, fp32 sum): one warp per (row, head).
+template <int D>
+__global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ Dd)
+{
+    grid_dep_sync();
+    const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= (int64_t)a.B * a.n * a.Hq) return;
+    const int64_t row = w / a.Hq;   // b * n + i
+    const int h = (int)(w - row * a.Hq);
+    const __nv_bfloat16 *o = a.o + w * D, *g = a.dO + w * D;
+    float sum = 0.f;
+#pragma unroll
+    for (int e = lane; e < D; e += 32) sum += __bfloat162float(o[e]) * __bfloat162float(g[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) {
+        const int64_t b = row / a.n, i = row - b * a.n;
+        Dd[(b * a.Hq + h) * a.n + i] = sum;
+    }
+}
+
+enum GMode { kModeDQ = 0, kModeDGQ = 1, kModeDK = 2, kModeDV = 3, kModeDGK = 4 };
+
+// Shared layout of a backward CTA: the tiles of its own rows (queries:
+// Q, dO, G_q; keys: K, V, G_k), then one stage of the other side's tiles,
+// then the other side's log-sum-exp and D (key orientation only).
+template <int D>
+struct GatedBwdSmem {
+    static constexpr int kRow = D * 2 + 16;
+    static __host__ __device__ int side(int kp) { return kGT * (2 * kRow + kp * 2 + 16); }
+    static __host__ __device__ int bytes(int kp) { return 2 * side(kp) + 2 * kGT * 4; }
+};
+
+// Backward with rows = queries (MODE kModeDQ: dQ of one head; kModeDGQ: the
+// row side of dG and d lambda, over every head).  For each key tile up to
+// the diagonal: S = Q K^T, A = G_q G_k^T, P = exp(gated logit - LSE),
+// dP = dO V^T, dS = P (dP - D); then dQ += (dS gate scale) K or
+// dG_q += (dS t lambda sigma') G_k for gated pairs.
+template <int D, int MODE>
+__global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedArgs a)
+{
+    using L = GatedBwdSmem<D>;
+    constexpr int kRow = L::kRow;
+    constexpr int NACC = MODE == kModeDQ ? D / 8 : 2 * kGMaxKs;
+    grid_dep_sync();
+    extern __shared__ __align__(128) uint8_t gsm[];
+    const int gRow = a.kp * 2 + 16;
+    uint8_t *Qs = gsm, *dOs = gsm + kGT * kRow, *Gqs = gsm + 2 * kGT * kRow;
+    uint8_t *Ks = gsm + L::side(a.kp), *Vs = Ks + kGT * kRow, *Gks = Ks + 2 * kGT * kRow;
+    const int qt = gridDim.x - 1 - blockIdx.x;
+    const int b = blockIdx.z;
+    const int h0 = MODE == kModeDQ ? (int)blockIdx.y : 0;
+    const int h1 = MODE == kModeDQ ? h0 + 1 : a.Hq;
+    const int gqa = a.Hq / a.Hkv;
+    const int q0 = qt * kGT;
+    const int nks = a.kp / 16;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rbase = q0 + 16 * warp + (lane >> 2);
+    const float l2e = 1.4426950408889634f;
+
+    float acc[NACC][4];
+#pragma unroll
+    for (int x = 0; x < NACC; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    float dlam = 0.f;
+    load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
+    for (int h = h0; h < h1; ++h) {
+        const int kvh = h / gqa;
+        load_tile(Qs, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
+        load_tile(dOs, kRow, a.dO, b, a.n, a.Hq, h, D, q0, tid);
+        float lse2[2], dd[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = rbase + 8 * r;
+            const int64_t at = ((int64_t)b * a.Hq + h) * a.n + i;
+            lse2[r] = i < a.n ? a.lse[at] * l2e : 0.f;
+            dd[r] = i < a.n ? a.Dd[at] : 0.f;
+        }
+        for (int kt = 0; kt <= qt; ++kt) {
+            load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
+            load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
+            load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, kt * kGT, tid);
+            cp_async_wait_all();
+            __syncthreads();
+            float s[8][4], ag[8][4], dp[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t qa[4], oa[4];
+                lda(Qs + 16 * warp * kRow, kRow, 16 * kk, lane, qa);
+                lda(dOs + 16 * warp * kRow, kRow, 16 * kk, lane, oa);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bb[4];
+                    ldb_nk(Ks + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                    mma_bf16(s[2 * np], qa, bb[0], bb[1]);
+                    mma_bf16(s[2 * np + 1], qa, bb[2], bb[3]);
+                    ldb_nk(Vs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                    mma_bf16(dp[2 * np], oa, bb[0], bb[1]);
+                    mma_bf16(dp[2 * np + 1], oa, bb[2], bb[3]);
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < kGMaxKs; ++ks)
+                if (ks < nks) {
+                    uint32_t ga[4];
+                    lda(Gqs + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t bb[4];
+                        ldb_nk(Gks + 16 * np * gRow, gRow, 16 * ks, lane, bb);
+                        mma_f16(ag[2 * np], ga, bb[0], bb[1]);
+                        mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
+                    }
+                }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = e >> 1;
+                    const int i = rbase + 8 * r;
+                    const int j = kt * kGT + 8 * nt + 2 * (lane & 3) + (e & 1);
+                    const bool valid = j <= i && i < a.n;
+                    const bool local = i - j < a.window;
+                    const float t = s[nt][e] * a.scale;
+                    const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
+                    const float P = valid ? exp2f(t * sg * l2e - lse2[r]) : 0.f;
+                    const float ds = P * (dp[nt][e] - dd[r]);
+                    if (MODE == kModeDQ) {
+                        s[nt][e] = ds * sg * a.scale;
+                    } else {
+                        const float sp = sg * (1.f - sg);
+                        const bool gated = valid && !local;
+                        s[nt][e] = gated ? ds * t * a.lambda * sp : 0.f;
+                        dlam += gated ? ds * t * ag[nt][e] * sp : 0.f;
+                    }
+                }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                if (MODE == kModeDQ) {
+                    const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
+                                            pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
+                                            pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                            pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+                    for (int dq = 0; dq < D / 16; ++dq) {
+                        uint32_t bb[4];
+                        ldb_kn(Ks + 16 * kk * kRow, kRow, 16 * dq, lane, bb);
+                        mma_bf16(acc[2 * dq], pa, bb[0], bb[1]);
+                        mma_bf16(acc[2 * dq + 1], pa, bb[2], bb[3]);
+                    }
+                } else {
+                    const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
+                                            pack_h2(s[2 * kk][2], s[2 * kk][3]),
+                                            pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                            pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+                    for (int c = 0; c < kGMaxKs; ++c)
+                        if (c < nks) {
+                            uint32_t bb[4];
+                            ldb_kn(Gks + 16 * kk * gRow, gRow, 16 * c, lane, bb);
+                            mma_f16(acc[2 * c], pa, bb[0], bb[1]);
+                            mma_f16(acc[2 * c + 1], pa, bb[2], bb[3]);
+                        }
+                }
+            }
+            __syncthreads();   // the key tiles are rewritten next
+        }
+        if (MODE == kModeDQ) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = rbase + 8 * r;
+                if (i >= a.n) continue;
+                float *row = a.dq + (((int64_t)b * a.n + i) * a.Hq + h) * D;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt)
+                    *reinterpret_cast<float2 *>(row + 8 * nt + 2 * (lane & 3)) =
+                        make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+            }
+        }
+        __syncthreads();   // the query tiles are rewritten for the next head
+    }
+    if (MODE == kModeDGQ) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = rbase + 8 * r;
+            if (i >= a.n) continue;
+            float *row = a.dg + ((int64_t)b * a.n + i) * a.Kg;
+#pragma unroll
+            for (int nt = 0; nt < NACC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int c = 8 * nt + 2 * (lane & 3) + e;
+                    if (c < a.Kg) row[c] = acc[nt][2 * r + e];
+                }
+        }
+        // d lambda of the CTA's pairs, in a fixed order
+        __shared__ float red[kGWarps];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
+        if (lane == 0) red[warp] = dlam;
+        __syncthreads();
+        if (tid == 0)
+            a.dlam_part[(int64_t)b * gridDim.x + qt] = (red[0] + red[1]) + (red[2] + red[3]);
+    }
+}
+
+
+// Backward with rows = keys (MODE kModeDV: dV, kModeDK: dK, both over the
+// query heads of one kv head; kModeDGK: the column side of dG over every
+// head, added to the row side already in dg).  For each query tile from the
+// diagonal on: S^T = K Q^T, A^T = G_k G_q^T, P^T from the queries' LSE,
+// dP^T = V dO^T, dS^T = P^T (dP^T - D); then dV += P^T dO,
+// dK += (dS^T gate scale) Q, or dG_k += (dS^T t lambda sigma') G_q.
+template <int D, int MODE>
+__global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedArgs a)
+{
+    using L = GatedBwdSmem<D>;
+    constexpr int kRow = L::kRow;
+    constexpr int NACC = MODE == kModeDGK ? 2 * kGMaxKs : D / 8;
+    grid_dep_sync();
+    extern __shared__ __align__(128) uint8_t gsm[];
+    const int gRow = a.kp * 2 + 16;
+    uint8_t *Ks = gsm, *Vs = gsm + kGT * kRow, *Gks = gsm + 2 * kGT * kRow;
+    uint8_t *Qs = gsm + L::side(a.kp), *dOs = Qs + kGT * kRow, *Gqs = Qs + 2 * kGT * kRow;
+    float *lse2s = reinterpret_cast<float *>(gsm + 2 * L::side(a.kp));
+    float *dds = lse2s + kGT;
+    const int kt = blockIdx.x;   // the first key tiles have the most query tiles
+    const int b = blockIdx.z;
+    const int gqa = a.Hq / a.Hkv;
+    const int h0 = MODE == kModeDGK ? 0 : (int)blockIdx.y * gqa;
+    const int h1 = MODE == kModeDGK ? a.Hq : h0 + gqa;
+    const int k0 = kt * kGT;
+    const int nqt = (a.n + kGT - 1) / kGT;
+    const int nks = a.kp / 16;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rbase = k0 + 16 * warp + (lane >> 2);
+    const float l2e = 1.4426950408889634f;
+
+    float acc[NACC][4];
+#pragma unroll
+    for (int x = 0; x < NACC; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, k0, tid);
+    for (int h = h0; h < h1; ++h) {
+        const int kvh = h / gqa;
+        if (h == h0 || h % gqa == 0) {   // this kv head's K and V rows
+            load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, k0, tid);
+            load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, k0, tid);
+        }
+        for (int qt = kt; qt < nqt; ++qt) {
+            const int q0 = qt * kGT;
+            load_tile(Qs, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
+            load_tile(dOs, kRow, a.dO, b, a.n, a.Hq, h, D, q0, tid);
+            load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
+            if (tid < kGT) {
+                const int i = q0 + tid;
+                const int64_t at = ((int64_t)b * a.Hq + h) * a.n + i;
+                lse2s[tid] = i < a.n ? a.lse[at] * l2e : 0.f;
+                dds[tid] = i < a.n ? a.Dd[at] : 0.f;
+            }
+            cp_async_wait_all();
+            __syncthreads();
+            float s[8][4], ag[8][4], dp[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t ka[4], va[4];
+                lda(Ks + 16 * warp * kRow, kRow, 16 * kk, lane, ka);
+                if (MODE != kModeDV) lda(Vs + 16 * warp * kRow, kRow, 16 * kk, lane, va);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bb[4];
+                    ldb_nk(Qs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                    mma_bf16(s[2 * np], ka, bb[0], bb[1]);
+                    mma_bf16(s[2 * np + 1], ka, bb[2], bb[3]);
+                    if (MODE != kModeDV) {
+                        ldb_nk(dOs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                        mma_bf16(dp[2 * np], va, bb[0], bb[1]);
+                        mma_bf16(dp[2 * np + 1], va, bb[2], bb[3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < kGMaxKs; ++ks)
+                if (ks < nks) {
+                    uint32_t ga[4];
+                    lda(Gks + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t bb[4];
+                        ldb_nk(Gqs + 16 * np * gRow, gRow, 16 * ks, lane, bb);
+                        mma_f16(ag[2 * np], ga, bb[0], bb[1]);
+                        mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
+                    }
+                }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = rbase + 8 * (e >> 1);                 // key
+                    const int cl = 8 * nt + 2 * (lane & 3) + (e & 1);   // query in the tile
+                    const int i = q0 + cl;
+                    const bool valid = j <= i && i < a.n && j < a.n;
+                    const bool local = i - j < a.window;
+                    const float t = s[nt][e] * a.scale;
+                    const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
+                    const float P = valid ? exp2f(t * sg * l2e - lse2s[cl]) : 0.f;
+                    if (MODE == kModeDV) {
+                        s[nt][e] = P;
+                    } else {
+                        const float ds = P * (dp[nt][e] - dds[cl]);
+                        if (MODE == kModeDK)
+                            s[nt][e] = ds * sg * a.scale;
+                        else
+                            s[nt][e] = (valid && !local) ? ds * t * a.lambda * sg * (1.f - sg) : 0.f;
+                    }
+                }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                if (MODE == kModeDGK) {
+                    const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
+                                            pack_h2(s[2 * kk][2], s[2 * kk][3]),
+                                            pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                            pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+                    for (int c = 0; c < kGMaxKs; ++c)
+                        if (c < nks) {
+                            uint32_t bb[4];
+                            ldb_kn(Gqs + 16 * kk * gRow, gRow, 16 * c, lane, bb);
+                            mma_f16(acc[2 * c], pa, bb[0], bb[1]);
+                            mma_f16(acc[2 * c + 1], pa, bb[2], bb[3]);
+                        }
+                } else {
+                    const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
+                                            pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
+                                            pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                            pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+                    const uint8_t *src = MODE == kModeDV ? dOs : Qs;
+#pragma unroll
+                    for (int dq = 0; dq < D / 16; ++dq) {
+                        uint32_t bb[4];
+                        ldb_kn(src + 16 * kk * kRow, kRow, 16 * dq, lane, bb);
+                        mma_bf16(acc[2 * dq], pa, bb[0], bb[1]);
+                        mma_bf16(acc[2 * dq + 1], pa, bb[2], bb[3]);
+                    }
+                }
+            }
+            __syncthreads();   // the query tiles are rewritten next
+        }
+        if (MODE != kModeDGK && h + 1 == h1) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = rbase + 8 * r;
+                if (j >= a.n) continue;
+                float *row = (MODE == kModeDK ? a.dk : a.dv) + (((int64_t)b * a.n + j) * a.Hkv + kvh) * D;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt)
+                    *reinterpret_cast<float2 *>(row + 8 * nt + 2 * (lane & 3)) =
+                        make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+            }
+        }
+    }
+    if (MODE == kModeDGK) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int j = rbase + 8 * r;
+            if (j >= a.n) continue;
+            float *row = a.dg + ((int64_t)b * a.n + j) * a.Kg;
+#pragma unroll
+            for (int nt = 0; nt < NACC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int c = 8 * nt + 2 * (lane & 3) + e;
+                    if (c < a.Kg) row[c] += acc[nt][2 * r + e];
+                }
+        }
+    }
+}
+
+// d lambda = sum of the query-tile partials, in a fixed order (one thread).
+__global__ void gated_dlam_kernel(const float *__restrict__ part, int count, float *__restrict__ out)
+{
+    grid_dep_sync();
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        double s = 0.0;
+        for (int x = 0; x < count; ++x) s += (double)part[x];
+        *out = (float)s;
+    }
+}
+
+}  // namespace
+
+size_t gated_ws_bytes(int B, int n, int Hq, int Kg)
+{
+    const size_t a256 = 255;
+    const int kp = (Kg + 15) / 16 * 16;
+    const int nqt = (n + kGT - 1) / kGT;
+    return (((size_t)B * n * kp * 2 + a256) & ~a256) + (((size_t)B * Hq * n * 4 + a256) & ~a256) +
+           (((size_t)B * nqt * 4 + a256) & ~a256);
+}
+
+namespace {
+
+template <int D>
+cudaError_t gated_preflight_d(int kp)
+{
+    const int fwd = 2 * GatedSmem<D>::stage(kp), bwd = GatedBwdSmem<D>::bytes(kp);
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(gated_fwd_kernel<D>, at, fwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D, kModeDQ>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D, kModeDGQ>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDK>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDV>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDGK>, at, bwd);
+    return e;
+}
+
+GatedArgs gated_args(const GatedLaunch &p, void *ws)
+{
+    const size_t a256 = 255;
+    GatedArgs a{};
+    a.q = p.q;
+    a.k = p.k;
+    a.v = p.v;
+    a.o = p.o;
+    a.dO = p.dO;
+    a.lse = p.lse;
+    a.out = p.out;
+    a.lse_out = p.lse_out;
+    a.dq = p.dq;
+    a.dk = p.dk;
+    a.dv = p.dv;
+    a.dg = p.dg;
+    a.B = p.B;
+    a.n = p.n;
+    a.Hq = p.Hq;
+    a.Hkv = p.Hkv;
+    a.Kg = p.Kg;
+    a.kp = (p.Kg + 15) / 16 * 16;
+    a.window = p.window;
+    a.scale = p.scale;
+    a.lambda = p.lambda;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    a.g = reinterpret_cast<const __half *>(w);
+    w += ((size_t)p.B * p.n * a.kp * 2 + a256) & ~a256;
+    a.Dd = reinterpret_cast<const float *>(w);
+    w += ((size_t)p.B * p.Hq * p.n * 4 + a256) & ~a256;
+    a.dlam_part = reinterpret_cast<float *>(w);
+    return a;
+}
+
+cudaError_t launch_g16(const GatedLaunch &p, const GatedArgs &a, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)p.B * p.n;
+    const int64_t total = rows * a.kp;
+    const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256, 152 * 16);
+    return launch_pdl(gated_g16_kernel, dim3(blocks), dim3(256), 0, s, p.G, rows, p.Kg, a.kp,
+                      const_cast<__half *>(a.g));
+}
+
+template <int D>
+cudaError_t gated_fwd_t(const GatedLaunch &p, const GatedArgs &a, cudaStream_t s, int *launches)
+{
+    const int nqt = (p.n + kGT - 1) / kGT;
+    prof_begin("gated_fwd", s);
+    const cudaError_t e = launch_pdl(gated_fwd_kernel<D>, dim3((unsigned)nqt, (unsigned)p.Hq,
+                                     (unsigned)p.B), dim3(kGThreads),
+                                     (size_t)2 * GatedSmem<D>::stage(a.kp), s, a);
+    prof_end(s);
+    *launches += 1;
+    return e;
+}
+
+template <int D>
+cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *launches)
+{
+    const int nqt = (p.n + kGT - 1) / kGT;
+    const size_t smem = GatedBwdSmem<D>::bytes(a.kp);
+    const dim3 blk(kGThreads);
+    cudaError_t e;
+    const int64_t warps = (int64_t)p.B * p.n * p.Hq;
+    prof_begin("gated_bwd_prep", s);
+    e = launch_pdl(gated_bwd_prep_kernel<D>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256),
+                   0, s, a, const_cast<float *>(a.Dd));
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_bwd_dq", s);
+    e = launch_pdl(gated_bwd_q_kernel<D, kModeDQ>, dim3(nqt, p.Hq, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_bwd_dgq", s);
+    e = launch_pdl(gated_bwd_q_kernel<D, kModeDGQ>, dim3(nqt, 1, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_bwd_dk", s);
+    e = launch_pdl(gated_bwd_k_kernel<D, kModeDK>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_bwd_dv", s);
+    e = launch_pdl(gated_bwd_k_kernel<D, kModeDV>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_bwd_dgk", s);
+    e = launch_pdl(gated_bwd_k_kernel<D, kModeDGK>, dim3(nqt, 1, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    prof_begin("gated_dlam", s);
+    e = launch_pdl(gated_dlam_kernel, dim3(1), dim3(32), 0, s, a.dlam_part, p.B * nqt, p.dlam);
+    prof_end(s);
+    *launches += 7;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t gated_preflight(int d, int Kg)
+{
+    const int kp = (Kg + 15) / 16 * 16;
+    return d == 64 ? gated_preflight_d<64>(kp) : gated_preflight_d<128>(kp);
+}
+
+cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches)
+{
+    const GatedArgs a = gated_args(p, ws);
+    cudaError_t e = launch_g16(p, a, s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    return p.d == 64 ? gated_fwd_t<64>(p, a, s, launches) : gated_fwd_t<128>(p, a, s, launches);
+}
+
+cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches)
+{
+    const GatedArgs a = gated_args(p, ws);
+    cudaError_t e = launch_g16(p, a, s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    return p.d == 64 ? gated_bwd_t<64>(p, a, s, launches) : gated_bwd_t<128>(p, a, s, launches);
+}
+
+}  // namespace focus

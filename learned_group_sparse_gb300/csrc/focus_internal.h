@@ -173,6 +173,20 @@ cudaError_t launch_decode_lists_init(const int32_t *offsets, const int32_t *pos,
                                      int *status, cudaStream_t s, int *launches);
 cudaError_t launch_decode(const DecodeLaunch &p, cudaStream_t s, int *launches);
 
+// ---- soft-gated attention of training and its backward
+struct GatedLaunch {
+    const __nv_bfloat16 *q, *k, *v, *o, *dO;
+    const float *G, *lse;
+    __nv_bfloat16 *out;
+    float *lse_out, *dq, *dk, *dv, *dg, *dlam;
+    int B, n, Hq, Hkv, d, Kg, window;
+    float scale, lambda;
+};
+size_t gated_ws_bytes(int B, int n, int Hq, int Kg);
+cudaError_t gated_preflight(int d, int Kg);
+cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
+cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
+
 // ---- Sinkhorn normalisation of token-group affinities
 int sinkhorn_ctas(int B, int n, int K);
 size_t sinkhorn_ws_bytes(int B, int n, int K);

@@ -149,6 +149,29 @@ def test_sinkhorn_validation(lib):
     assert f(*args) == WORKSPACE
 
 
+def test_gated_validation(lib):
+    need = fg.focus_gated_workspace_size(1, 100, 4, 16)
+    assert need > 0
+    assert fg.focus_gated_workspace_size(1, 100, 4, 129) == 0   # K_g above 128
+    f = lib.focus_gated_attention_fwd
+    ok = (P, P, P, P, 1, 100, 4, 2, 64, 16, 8, 2.0, 0.0, P2, P2, P2, need, None)
+    for k, bad, want in ((0, None, INVALID), (3, MIS, INVALID), (4, 0, INVALID),
+                         (7, 3, INVALID), (8, 96, UNSUPPORTED), (9, 129, UNSUPPORTED),
+                         (10, -1, INVALID), (11, float("inf"), INVALID), (12, -1.0, INVALID),
+                         (13, None, INVALID), (14, MIS, INVALID), (16, need - 1, WORKSPACE)):
+        args = list(ok)
+        args[k] = bad
+        assert f(*args) == want, (k, bad)
+    g = lib.focus_gated_attention_bwd
+    okb = (P, P, P, P, P, P, P, 1, 100, 4, 2, 64, 16, 8, 2.0, 0.0, P2, P2, P2, P2, P2, P2, need,
+           None)
+    for k, bad, want in ((4, None, INVALID), (6, MIS, INVALID), (16, None, INVALID),
+                         (20, None, INVALID), (12, 0, INVALID), (22, need - 1, WORKSPACE)):
+        args = list(okb)
+        args[k] = bad
+        assert g(*args) == want, (k, bad)
+
+
 def test_prefill_validation(lib):
     f = lib.focus_prefill
     need = fg.focus_prefill_workspace_size(1, 512, 64, 4, 4, 64, 16, 8, 2, 0)
