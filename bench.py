@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-sinkhorn", action="store_true")
+    ap.add_argument("--no-gated", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed loop only (for profiler launch lists)")
     return ap.parse_args()
@@ -413,6 +414,58 @@ def bench_sinkhorn(fg, torch, w, t, flush, stream, peaks, args):
                     "between calls"}
 
 
+GATED_LAMBDA = 3.0
+
+
+def bench_gated(fg, torch, flush, stream, peaks, args):
+    """Soft-gated attention of training, forward and backward, on the n = 8K
+    workload's shapes (B 1, n 8192, 32 heads, d 128, K_g 64, window 256):
+    seeded N(0, 1) Q, K, V and dO in bf16, G the softmax of N(0, 4) logits.
+    Work counted per causal pair and head: forward 4 d (Q K^T, P V) + 2 K_g
+    (G G^T); backward 10 d (Q K^T again, dP, dV, dK, dQ) + 6 K_g (G G^T
+    again, both dG sides).  Timed alone, L2 flushed before each call."""
+    from learned_group_sparse_gb300 import synth
+    w = synth.workload(1)
+    B, n, Hq, Hkv, d, Kg, win = w.B, w.n, w.Hq, w.Hkv, w.d, w.K, w.window
+    g = torch.Generator(device="cuda").manual_seed(w.seed + 7)
+    Q = torch.randn(B, n, Hq, d, generator=g, device="cuda").to(torch.bfloat16)
+    K = torch.randn(B, n, Hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+    V = torch.randn(B, n, Hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+    G = torch.softmax(2.0 * torch.randn(B, n, Kg, generator=g, device="cuda"), -1).contiguous()
+    dO = torch.randn(B, n, Hq, d, generator=g, device="cuda").to(torch.bfloat16)
+    ws = torch.empty(fg.focus_gated_workspace_size(B, n, Hq, Kg), dtype=torch.uint8,
+                     device="cuda")
+    O, lse = fg.focus_gated_attention_fwd(Q, K, V, G, win, GATED_LAMBDA, ws=ws)
+    out = fg.focus_gated_attention_bwd(Q, K, V, G, O, lse, dO, win, GATED_LAMBDA, ws=ws)
+    reps = max(3, min(10, args.steps))
+    tf, tb = [], []
+    for k in range(2 + reps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        fg.focus_gated_attention_fwd(Q, K, V, G, win, GATED_LAMBDA, O=O, lse=lse, ws=ws)
+        e[1].record(stream)
+        fg.focus_gated_attention_bwd(Q, K, V, G, O, lse, dO, win, GATED_LAMBDA, ws=ws, out=out)
+        e[2].record(stream)
+        if k >= 2:
+            tf.append(e)
+    torch.cuda.synchronize()
+    fms = statistics.mean(e[0].elapsed_time(e[1]) for e in tf)
+    bms = statistics.mean(e[1].elapsed_time(e[2]) for e in tf)
+    pairs = B * n * (n + 1) / 2
+    ff = (4 * d + 2 * Kg) * Hq * pairs
+    bf = (10 * d + 6 * Kg) * Hq * pairs
+    peak = float(peaks["bf16_tflops"])
+    return {"shape": {"B": B, "n": n, "Hq": Hq, "Hkv": Hkv, "d": d, "Kg": Kg, "window": win,
+                      "lambda": GATED_LAMBDA},
+            "fwd_ms": fms, "bwd_ms": bms, "fwd_tflops": ff / (fms * 1e-3) / 1e12,
+            "bwd_tflops": bf / (bms * 1e-3) / 1e12, "bound": "tensor", "peak": peak,
+            "fwd_frac": ff / (fms * 1e-3) / 1e12 / peak,
+            "bwd_frac": bf / (bms * 1e-3) / 1e12 / peak, "reps": reps,
+            "what": "training forward and backward over every causal pair (mma.sync tiles), "
+                    "L2 flushed before each call"}
+
+
 def main():
     args = parse_args()
     from learned_group_sparse_gb300 import synth
@@ -580,6 +633,11 @@ def main():
     if not args.no_sinkhorn:
         sinkhorn = bench_sinkhorn(fg, torch, w, t, flush, stream, peaks, args)
 
+    # ---- soft-gated attention of training (forward and backward)
+    gated = None
+    if not args.no_gated:
+        gated = bench_gated(fg, torch, flush, stream, peaks, args)
+
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -647,7 +705,7 @@ def main():
             "attention_effective_tflops": eff_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
             "allowed_pairs": total_pairs, "group_pairs": share_pairs,
             "roofline": roof, "kernels": kernels, "dense_causal": dense, "decode": decode,
-            "sinkhorn": sinkhorn,
+            "sinkhorn": sinkhorn, "gated_training": gated,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
             "context": "pages: 8.6x over full attention at 1M tokens (H100) and 2x from "

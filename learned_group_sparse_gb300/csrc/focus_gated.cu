@@ -19,12 +19,13 @@
 // and the log-sum-exp.  Backward (each kernel recomputes P from the
 // log-sum-exp, so none needs atomics and every sum has a fixed order):
 //   gated_bwd_prep_kernel   D_i = dO_i . O_i per (row, head)
-//   gated_bwd_dq_kernel     CTA (64 queries, batch), every head: dQ, the
-//                           row side of dG (sum_j da_ij g_j) and d lambda
-//   gated_bwd_dkv_kernel    CTA (64 keys, kv head, batch): dK, dV over the
-//                           query heads of the kv head
-//   gated_bwd_dgk_kernel    CTA (64 keys, batch), every head: the column side
-//                           of dG (sum_i da_ij g_i), added to the row side
+//   gated_bwd_q_kernel      rows = queries: dQ (CTA: 64 queries, head,
+//                           batch); the row side of dG, sum_j da_ij g_j, and
+//                           d lambda (CTA: 64 queries, 4 heads, batch)
+//   gated_bwd_k_kernel      rows = keys: dK, dV (CTA: 64 keys, kv head,
+//                           batch, over its query heads); the column side of
+//                           dG, sum_i da_ij g_i (CTA: 64 keys, 4 heads, batch)
+//   gated_dg_reduce_kernel  dG = the sum of the per-chunk partials
 // with dS_ij = P_ij (dP_ij - D_i), dP_ij = dO_i . v_j, and for a gated pair
 // d gate_ij = dS_ij t_ij, da_ij = d gate_ij lambda sigma (1 - sigma).
 #include <cuda_bf16.h>
@@ -45,6 +46,7 @@ constexpr int kGT = 64;               // rows per tile (queries or keys)
 constexpr int kGWarps = 4;            // 16 rows per warp
 constexpr int kGThreads = kGWarps * 32;
 constexpr int kGMaxKs = 8;            // k-steps of 16 over the padded groups: K_g <= 128
+constexpr int kGHeadChunk = 4;        // query heads per CTA of the dG kernels (partials per chunk)
 
 struct GatedArgs {
     const __nv_bfloat16 *q, *k, *v;   // [B, n, Hq | Hkv, D]
@@ -55,8 +57,10 @@ struct GatedArgs {
     __nv_bfloat16 *out;               // O (forward)
     float *lse_out;                   // forward
     float *dq, *dk, *dv, *dg;         // [B, n, Hq, D], [B, n, Hkv, D] x 2, [B, n, Kg]
-    float *dlam_part;                 // [B, n / 64 tiles] partial d lambda
+    float *dlam_part;                 // [B, nhc, n / 64] partial d lambda
+    float *dg_part;                   // [2][nhc][B, n, Kg]: row and column sides of dG
     int B, n, Hq, Hkv, kp, Kg, window;
+    int hc, nhc;                      // query heads per dG chunk, chunks
     float scale, lambda;
 };
 
@@ -371,8 +375,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
     uint8_t *Ks = gsm + L::side(a.kp), *Vs = Ks + kGT * kRow, *Gks = Ks + 2 * kGT * kRow;
     const int qt = gridDim.x - 1 - blockIdx.x;
     const int b = blockIdx.z;
-    const int h0 = MODE == kModeDQ ? (int)blockIdx.y : 0;
-    const int h1 = MODE == kModeDQ ? h0 + 1 : a.Hq;
+    const int h0 = MODE == kModeDQ ? (int)blockIdx.y : (int)blockIdx.y * a.hc;
+    const int h1 = MODE == kModeDQ ? h0 + 1 : min(a.Hq, h0 + a.hc);
     const int gqa = a.Hq / a.Hkv;
     const int q0 = qt * kGT;
     const int nks = a.kp / 16;
@@ -509,7 +513,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
         for (int r = 0; r < 2; ++r) {
             const int i = rbase + 8 * r;
             if (i >= a.n) continue;
-            float *row = a.dg + ((int64_t)b * a.n + i) * a.Kg;
+            float *row = a.dg_part +
+                         (((int64_t)blockIdx.y * a.B + b) * a.n + i) * a.Kg;
 #pragma unroll
             for (int nt = 0; nt < NACC; ++nt)
 #pragma unroll
@@ -525,7 +530,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
         if (lane == 0) red[warp] = dlam;
         __syncthreads();
         if (tid == 0)
-            a.dlam_part[(int64_t)b * gridDim.x + qt] = (red[0] + red[1]) + (red[2] + red[3]);
+            a.dlam_part[((int64_t)b * gridDim.y + blockIdx.y) * gridDim.x + qt] =
+                (red[0] + red[1]) + (red[2] + red[3]);
     }
 }
 
@@ -552,8 +558,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
     const int kt = blockIdx.x;   // the first key tiles have the most query tiles
     const int b = blockIdx.z;
     const int gqa = a.Hq / a.Hkv;
-    const int h0 = MODE == kModeDGK ? 0 : (int)blockIdx.y * gqa;
-    const int h1 = MODE == kModeDGK ? a.Hq : h0 + gqa;
+    const int h0 = (int)blockIdx.y * (MODE == kModeDGK ? a.hc : gqa);
+    const int h1 = MODE == kModeDGK ? min(a.Hq, h0 + a.hc) : h0 + gqa;
     const int k0 = kt * kGT;
     const int nqt = (a.n + kGT - 1) / kGT;
     const int nks = a.kp / 16;
@@ -692,15 +698,29 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
         for (int r = 0; r < 2; ++r) {
             const int j = rbase + 8 * r;
             if (j >= a.n) continue;
-            float *row = a.dg + ((int64_t)b * a.n + j) * a.Kg;
+            float *row = a.dg_part +
+                         ((((int64_t)a.nhc + blockIdx.y) * a.B + b) * a.n + j) * a.Kg;
 #pragma unroll
             for (int nt = 0; nt < NACC; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int c = 8 * nt + 2 * (lane & 3) + e;
-                    if (c < a.Kg) row[c] += acc[nt][2 * r + e];
+                    if (c < a.Kg) row[c] = acc[nt][2 * r + e];
                 }
         }
+    }
+}
+
+// dG = the sum over head chunks of both sides' partials, in a fixed order.
+__global__ void gated_dg_reduce_kernel(const GatedArgs a)
+{
+    grid_dep_sync();
+    const int64_t total = (int64_t)a.B * a.n * a.Kg;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int c = 0; c < 2 * a.nhc; ++c) s += a.dg_part[(int64_t)c * total + x];
+        a.dg[x] = s;
     }
 }
 
@@ -722,8 +742,10 @@ size_t gated_ws_bytes(int B, int n, int Hq, int Kg)
     const size_t a256 = 255;
     const int kp = (Kg + 15) / 16 * 16;
     const int nqt = (n + kGT - 1) / kGT;
+    const int nhc = (Hq + kGHeadChunk - 1) / kGHeadChunk;
     return (((size_t)B * n * kp * 2 + a256) & ~a256) + (((size_t)B * Hq * n * 4 + a256) & ~a256) +
-           (((size_t)B * nqt * 4 + a256) & ~a256);
+           (((size_t)B * nhc * nqt * 4 + a256) & ~a256) +
+           (((size_t)2 * nhc * B * n * Kg * 4 + a256) & ~a256);
 }
 
 namespace {
@@ -772,7 +794,12 @@ GatedArgs gated_args(const GatedLaunch &p, void *ws)
     w += ((size_t)p.B * p.n * a.kp * 2 + a256) & ~a256;
     a.Dd = reinterpret_cast<const float *>(w);
     w += ((size_t)p.B * p.Hq * p.n * 4 + a256) & ~a256;
+    a.hc = kGHeadChunk < p.Hq ? kGHeadChunk : p.Hq;
+    a.nhc = (p.Hq + a.hc - 1) / a.hc;
     a.dlam_part = reinterpret_cast<float *>(w);
+    const int nqt = (p.n + kGT - 1) / kGT;
+    w += ((size_t)p.B * ((p.Hq + kGHeadChunk - 1) / kGHeadChunk) * nqt * 4 + a256) & ~a256;
+    a.dg_part = reinterpret_cast<float *>(w);
     return a;
 }
 
@@ -816,7 +843,7 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dgq", s);
-    e = launch_pdl(gated_bwd_q_kernel<D, kModeDGQ>, dim3(nqt, 1, p.B), blk, smem, s, a);
+    e = launch_pdl(gated_bwd_q_kernel<D, kModeDGQ>, dim3(nqt, a.nhc, p.B), blk, smem, s, a);
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dk", s);
@@ -828,13 +855,21 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dgk", s);
-    e = launch_pdl(gated_bwd_k_kernel<D, kModeDGK>, dim3(nqt, 1, p.B), blk, smem, s, a);
+    e = launch_pdl(gated_bwd_k_kernel<D, kModeDGK>, dim3(nqt, a.nhc, p.B), blk, smem, s, a);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    const int64_t dgn = (int64_t)p.B * p.n * p.Kg;
+    prof_begin("gated_dg_reduce", s);
+    e = launch_pdl(gated_dg_reduce_kernel,
+                   dim3((unsigned)std::min<int64_t>((dgn + 255) / 256, 152 * 8)), dim3(256), 0, s,
+                   a);
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_dlam", s);
-    e = launch_pdl(gated_dlam_kernel, dim3(1), dim3(32), 0, s, a.dlam_part, p.B * nqt, p.dlam);
+    e = launch_pdl(gated_dlam_kernel, dim3(1), dim3(32), 0, s, a.dlam_part, p.B * a.nhc * nqt,
+                   p.dlam);
     prof_end(s);
-    *launches += 7;
+    *launches += 8;
     return e;
 }
 
