@@ -156,13 +156,26 @@ struct GatedSmem {
     static __host__ __device__ int stage(int kp) { return kGT * (2 * kRow + g_row(kp)); }
 };
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
-
-// The gate of pair (i, j): 1 inside the window, else sigma(lambda a).
-__device__ __forceinline__ float gate_of(int i, int j, int window, float lambda, float aff)
+// sigma(z) = 1/2 + tanh(z / 2) / 2 with the hardware tanh approximation
+// (relative error about 2^-11: below the fp16 rounding of the G products).
+__device__ __forceinline__ float sigmoidf_(float z)
 {
-    return (i - j < window) ? 1.f : sigmoidf_(lambda * aff);
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
 }
+
+// Where a 64 x 64 tile of queries [q0, q0 + 64) and keys [k0, k0 + 64) lies
+// against the window: every pair inside it, or some pair inside it.
+__device__ __forceinline__ bool tile_all_local(int q0, int k0, int window)
+{
+    return q0 + kGT - 1 - k0 < window;
+}
+__device__ __forceinline__ bool tile_any_local(int q0, int k0, int window)
+{
+    return q0 - (k0 + kGT - 1) < window;
+}
+
 
 template <int D>
 __global__ void __launch_bounds__(kGThreads, 2) gated_fwd_kernel(const GatedArgs a)
@@ -224,16 +237,21 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_fwd_kernel(const GatedArgs
                 mma_bf16(s[2 * np], qa[kk], bb[0], bb[1]);
                 mma_bf16(s[2 * np + 1], qa[kk], bb[2], bb[3]);
             }
+        const int k0 = kt * kGT;
+        const bool all_local = tile_all_local(q0, k0, a.window);
+        const bool any_local = tile_any_local(q0, k0, a.window);
+        const bool masked = kt == qt || k0 + kGT > a.n;   // the diagonal and the ragged end
+        if (!all_local)
 #pragma unroll
-        for (int ks = 0; ks < kGMaxKs; ++ks)
-            if (ks < nks)
+            for (int ks = 0; ks < kGMaxKs; ++ks)
+                if (ks < nks)
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t bb[4];
-                    ldb_nk(Gt + 16 * np * gRow, gRow, 16 * ks, lane, bb);
-                    mma_f16(ag[2 * np], ga[ks], bb[0], bb[1]);
-                    mma_f16(ag[2 * np + 1], ga[ks], bb[2], bb[3]);
-                }
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t bb[4];
+                        ldb_nk(Gt + 16 * np * gRow, gRow, 16 * ks, lane, bb);
+                        mma_f16(ag[2 * np], ga[ks], bb[0], bb[1]);
+                        mma_f16(ag[2 * np + 1], ga[ks], bb[2], bb[3]);
+                    }
         // logits in base 2 with the gate; causal and length masks
         float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
@@ -241,10 +259,16 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_fwd_kernel(const GatedArgs
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = rbase + ((e >> 1) << 3);
-                const int j = kt * kGT + 8 * nt + 2 * (lane & 3) + (e & 1);
-                const float x = s[nt][e] * scale2 * gate_of(i, j, a.window, a.lambda, ag[nt][e]);
-                s[nt][e] = (j <= i && j < a.n) ? x : -CUDART_INF_F;
-                mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+                const int j = k0 + 8 * nt + 2 * (lane & 3) + (e & 1);
+                float g = 1.f;
+                if (!all_local) {
+                    g = sigmoidf_(a.lambda * ag[nt][e]);
+                    if (any_local && i - j < a.window) g = 1.f;
+                }
+                float x = s[nt][e] * scale2 * g;
+                if (masked) x = (j <= i && j < a.n) ? x : -CUDART_INF_F;
+                s[nt][e] = x;
+                mx[e >> 1] = fmaxf(mx[e >> 1], x);
             }
         float alpha[2];
 #pragma unroll
@@ -402,6 +426,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
             dd[r] = i < a.n ? a.Dd[at] : 0.f;
         }
         for (int kt = 0; kt <= qt; ++kt) {
+            const bool all_local = tile_all_local(q0, kt * kGT, a.window);
+            const bool any_local = tile_any_local(q0, kt * kGT, a.window);
+            if (MODE == kModeDGQ && all_local) continue;   // no gated pair: nothing to add
             load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
             load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
             load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, kt * kGT, tid);
@@ -430,7 +457,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
             }
 #pragma unroll
             for (int ks = 0; ks < kGMaxKs; ++ks)
-                if (ks < nks) {
+                if (ks < nks && !all_local) {
                     uint32_t ga[4];
                     lda(Gqs + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
 #pragma unroll
@@ -449,7 +476,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
                     const int i = rbase + 8 * r;
                     const int j = kt * kGT + 8 * nt + 2 * (lane & 3) + (e & 1);
                     const bool valid = j <= i && i < a.n;
-                    const bool local = i - j < a.window;
+                    const bool local = all_local || (any_local && i - j < a.window);
                     const float t = s[nt][e] * a.scale;
                     const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
                     const float P = valid ? exp2f(t * sg * l2e - lse2[r]) : 0.f;
@@ -506,7 +533,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
                         make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
             }
         }
-        __syncthreads();   // the query tiles are rewritten for the next head
+        cp_async_wait_all();   // copies of a head whose tiles were all skipped
+        __syncthreads();       // the query tiles are rewritten for the next head
     }
     if (MODE == kModeDGQ) {
 #pragma unroll
@@ -579,6 +607,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
         }
         for (int qt = kt; qt < nqt; ++qt) {
             const int q0 = qt * kGT;
+            const bool all_local = tile_all_local(q0, k0, a.window);
+            const bool any_local = tile_any_local(q0, k0, a.window);
+            if (MODE == kModeDGK && all_local) continue;   // no gated pair: nothing to add
             load_tile(Qs, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
             load_tile(dOs, kRow, a.dO, b, a.n, a.Hq, h, D, q0, tid);
             load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
@@ -615,7 +646,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
             }
 #pragma unroll
             for (int ks = 0; ks < kGMaxKs; ++ks)
-                if (ks < nks) {
+                if (ks < nks && !all_local) {
                     uint32_t ga[4];
                     lda(Gks + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
 #pragma unroll
@@ -634,7 +665,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
                     const int cl = 8 * nt + 2 * (lane & 3) + (e & 1);   // query in the tile
                     const int i = q0 + cl;
                     const bool valid = j <= i && i < a.n && j < a.n;
-                    const bool local = i - j < a.window;
+                    const bool local = all_local || (any_local && i - j < a.window);
                     const float t = s[nt][e] * a.scale;
                     const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
                     const float P = valid ? exp2f(t * sg * l2e - lse2s[cl]) : 0.f;
@@ -680,6 +711,8 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
             }
             __syncthreads();   // the query tiles are rewritten next
         }
+        cp_async_wait_all();   // copies of a head whose tiles were all skipped
+        __syncthreads();
         if (MODE != kModeDGK && h + 1 == h1) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
