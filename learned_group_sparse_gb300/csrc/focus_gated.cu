@@ -19,10 +19,10 @@
 // and the log-sum-exp.  Backward (each kernel recomputes P from the
 // log-sum-exp, so none needs atomics and every sum has a fixed order):
 //   gated_bwd_prep_kernel   D_i = dO_i . O_i per (row, head)
-//   gated_bwd_q_kernel      rows = queries: dQ (CTA: 64 queries, head,
-//                           batch); the row side of dG, sum_j da_ij g_j, and
-//                           d lambda (CTA: 64 queries, 4 heads, batch)
-//   gated_bwd_k_kernel      rows = keys: dK, dV (CTA: 64 keys, kv head,
+//   gated_bwd_q_kernel      rows = queries (CTA: 64 queries, 4 heads,
+//                           batch): dQ, the row side of dG, sum_j da_ij g_j,
+//                           and d lambda
+//   gated_bwd_k_kernel      rows = keys: dK and dV (CTA: 64 keys, kv head,
 //                           batch, over its query heads); the column side of
 //                           dG, sum_i da_ij g_i (CTA: 64 keys, 4 heads, batch)
 //   gated_dg_reduce_kernel  dG = the sum of the per-chunk partials
@@ -369,7 +369,7 @@ __global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ Dd)
     }
 }
 
-enum GMode { kModeDQ = 0, kModeDGQ = 1, kModeDK = 2, kModeDV = 3, kModeDGK = 4 };
+enum GMode { kModeDQG = 0, kModeDKV = 1, kModeDGK = 2 };
 
 // Shared layout of a backward CTA: the tiles of its own rows (queries:
 // Q, dO, G_q; keys: K, V, G_k), then one stage of the other side's tiles,
@@ -381,17 +381,19 @@ struct GatedBwdSmem {
     static __host__ __device__ int bytes(int kp) { return 2 * side(kp) + 2 * kGT * 4; }
 };
 
-// Backward with rows = queries (MODE kModeDQ: dQ of one head; kModeDGQ: the
-// row side of dG and d lambda, over every head).  For each key tile up to
-// the diagonal: S = Q K^T, A = G_q G_k^T, P = exp(gated logit - LSE),
-// dP = dO V^T, dS = P (dP - D); then dQ += (dS gate scale) K or
-// dG_q += (dS t lambda sigma') G_k for gated pairs.
-template <int D, int MODE>
+// Backward with rows = queries, CTA (64 queries, chunk of hc heads, batch):
+// for every head of the chunk and every key tile up to the diagonal, taken
+// in two halves of 32 keys (so that the tiles' scores fit the registers next
+// to both accumulators): S = Q K^T, A = G_q G_k^T, P = exp(gated logit -
+// LSE), dP = dO V^T, dS = P (dP - D); then dQ += (dS gate scale) K (written
+// per head) and, for gated pairs, dG_q += (dS t lambda sigma') G_k and
+// d lambda += dS t a sigma' (both summed over the chunk's heads).
+template <int D>
 __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedArgs a)
 {
     using L = GatedBwdSmem<D>;
     constexpr int kRow = L::kRow;
-    constexpr int NACC = MODE == kModeDQ ? D / 8 : 2 * kGMaxKs;
+    constexpr int NG = 2 * kGMaxKs;   // n-tiles of the dG accumulator
     grid_dep_sync();
     extern __shared__ __align__(128) uint8_t gsm[];
     const int gRow = a.kp * 2 + 16;
@@ -399,8 +401,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
     uint8_t *Ks = gsm + L::side(a.kp), *Vs = Ks + kGT * kRow, *Gks = Ks + 2 * kGT * kRow;
     const int qt = gridDim.x - 1 - blockIdx.x;
     const int b = blockIdx.z;
-    const int h0 = MODE == kModeDQ ? (int)blockIdx.y : (int)blockIdx.y * a.hc;
-    const int h1 = MODE == kModeDQ ? h0 + 1 : min(a.Hq, h0 + a.hc);
+    const int h0 = (int)blockIdx.y * a.hc, h1 = min(a.Hq, h0 + a.hc);
     const int gqa = a.Hq / a.Hkv;
     const int q0 = qt * kGT;
     const int nks = a.kp / 16;
@@ -408,9 +409,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
     const int rbase = q0 + 16 * warp + (lane >> 2);
     const float l2e = 1.4426950408889634f;
 
-    float acc[NACC][4];
+    float gacc[NG][4];
 #pragma unroll
-    for (int x = 0; x < NACC; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    for (int x = 0; x < NG; ++x) gacc[x][0] = gacc[x][1] = gacc[x][2] = gacc[x][3] = 0.f;
     float dlam = 0.f;
     load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
     for (int h = h0; h < h1; ++h) {
@@ -425,74 +426,78 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
             lse2[r] = i < a.n ? a.lse[at] * l2e : 0.f;
             dd[r] = i < a.n ? a.Dd[at] : 0.f;
         }
+        float qacc[D / 8][4];
+#pragma unroll
+        for (int x = 0; x < D / 8; ++x) qacc[x][0] = qacc[x][1] = qacc[x][2] = qacc[x][3] = 0.f;
         for (int kt = 0; kt <= qt; ++kt) {
-            const bool all_local = tile_all_local(q0, kt * kGT, a.window);
-            const bool any_local = tile_any_local(q0, kt * kGT, a.window);
-            if (MODE == kModeDGQ && all_local) continue;   // no gated pair: nothing to add
-            load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
-            load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
-            load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, kt * kGT, tid);
+            const int k0 = kt * kGT;
+            const bool all_local = tile_all_local(q0, k0, a.window);
+            const bool any_local = tile_any_local(q0, k0, a.window);
+            load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, k0, tid);
+            load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, k0, tid);
+            if (!all_local) load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, k0, tid);
             cp_async_wait_all();
             __syncthreads();
-            float s[8][4], ag[8][4], dp[8][4];
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                const int c0 = 32 * hf;   // first key of the half in the tile
+                float s[4][4], ag[4][4], dp[4][4];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+                for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t qa[4], oa[4];
-                lda(Qs + 16 * warp * kRow, kRow, 16 * kk, lane, qa);
-                lda(dOs + 16 * warp * kRow, kRow, 16 * kk, lane, oa);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t qa[4], oa[4];
+                    lda(Qs + 16 * warp * kRow, kRow, 16 * kk, lane, qa);
+                    lda(dOs + 16 * warp * kRow, kRow, 16 * kk, lane, oa);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t bb[4];
-                    ldb_nk(Ks + 16 * np * kRow, kRow, 16 * kk, lane, bb);
-                    mma_bf16(s[2 * np], qa, bb[0], bb[1]);
-                    mma_bf16(s[2 * np + 1], qa, bb[2], bb[3]);
-                    ldb_nk(Vs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
-                    mma_bf16(dp[2 * np], oa, bb[0], bb[1]);
-                    mma_bf16(dp[2 * np + 1], oa, bb[2], bb[3]);
-                }
-            }
-#pragma unroll
-            for (int ks = 0; ks < kGMaxKs; ++ks)
-                if (ks < nks && !all_local) {
-                    uint32_t ga[4];
-                    lda(Gqs + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
-#pragma unroll
-                    for (int np = 0; np < 4; ++np) {
+                    for (int np = 0; np < 2; ++np) {
                         uint32_t bb[4];
-                        ldb_nk(Gks + 16 * np * gRow, gRow, 16 * ks, lane, bb);
-                        mma_f16(ag[2 * np], ga, bb[0], bb[1]);
-                        mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
+                        ldb_nk(Ks + (c0 + 16 * np) * kRow, kRow, 16 * kk, lane, bb);
+                        mma_bf16(s[2 * np], qa, bb[0], bb[1]);
+                        mma_bf16(s[2 * np + 1], qa, bb[2], bb[3]);
+                        ldb_nk(Vs + (c0 + 16 * np) * kRow, kRow, 16 * kk, lane, bb);
+                        mma_bf16(dp[2 * np], oa, bb[0], bb[1]);
+                        mma_bf16(dp[2 * np + 1], oa, bb[2], bb[3]);
                     }
                 }
+                if (!all_local)
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+                    for (int ks = 0; ks < kGMaxKs; ++ks)
+                        if (ks < nks) {
+                            uint32_t ga[4];
+                            lda(Gqs + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = e >> 1;
-                    const int i = rbase + 8 * r;
-                    const int j = kt * kGT + 8 * nt + 2 * (lane & 3) + (e & 1);
-                    const bool valid = j <= i && i < a.n;
-                    const bool local = all_local || (any_local && i - j < a.window);
-                    const float t = s[nt][e] * a.scale;
-                    const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
-                    const float P = valid ? exp2f(t * sg * l2e - lse2[r]) : 0.f;
-                    const float ds = P * (dp[nt][e] - dd[r]);
-                    if (MODE == kModeDQ) {
-                        s[nt][e] = ds * sg * a.scale;
-                    } else {
+                            for (int np = 0; np < 2; ++np) {
+                                uint32_t bb[4];
+                                ldb_nk(Gks + (c0 + 16 * np) * gRow, gRow, 16 * ks, lane, bb);
+                                mma_f16(ag[2 * np], ga, bb[0], bb[1]);
+                                mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
+                            }
+                        }
+                // dt = dS gate scale into s, da = dS t lambda sigma' into ag
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = e >> 1;
+                        const int i = rbase + 8 * r;
+                        const int j = k0 + c0 + 8 * nt + 2 * (lane & 3) + (e & 1);
+                        const bool valid = j <= i && i < a.n;
+                        const bool local = all_local || (any_local && i - j < a.window);
+                        const float t = s[nt][e] * a.scale;
+                        const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
+                        const float P = valid ? exp2f(t * sg * l2e - lse2[r]) : 0.f;
+                        const float ds = P * (dp[nt][e] - dd[r]);
                         const float sp = sg * (1.f - sg);
                         const bool gated = valid && !local;
-                        s[nt][e] = gated ? ds * t * a.lambda * sp : 0.f;
                         dlam += gated ? ds * t * ag[nt][e] * sp : 0.f;
+                        s[nt][e] = ds * sg * a.scale;
+                        ag[nt][e] = gated ? ds * t * a.lambda * sp : 0.f;
                     }
-                }
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (MODE == kModeDQ) {
+                for (int kk = 0; kk < 2; ++kk) {
                     const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
                                             pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
                                             pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
@@ -500,82 +505,78 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
 #pragma unroll
                     for (int dq = 0; dq < D / 16; ++dq) {
                         uint32_t bb[4];
-                        ldb_kn(Ks + 16 * kk * kRow, kRow, 16 * dq, lane, bb);
-                        mma_bf16(acc[2 * dq], pa, bb[0], bb[1]);
-                        mma_bf16(acc[2 * dq + 1], pa, bb[2], bb[3]);
+                        ldb_kn(Ks + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
+                        mma_bf16(qacc[2 * dq], pa, bb[0], bb[1]);
+                        mma_bf16(qacc[2 * dq + 1], pa, bb[2], bb[3]);
                     }
-                } else {
-                    const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
-                                            pack_h2(s[2 * kk][2], s[2 * kk][3]),
-                                            pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                            pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+                    if (!all_local) {
+                        const uint32_t ha[4] = {pack_h2(ag[2 * kk][0], ag[2 * kk][1]),
+                                                pack_h2(ag[2 * kk][2], ag[2 * kk][3]),
+                                                pack_h2(ag[2 * kk + 1][0], ag[2 * kk + 1][1]),
+                                                pack_h2(ag[2 * kk + 1][2], ag[2 * kk + 1][3])};
 #pragma unroll
-                    for (int c = 0; c < kGMaxKs; ++c)
-                        if (c < nks) {
-                            uint32_t bb[4];
-                            ldb_kn(Gks + 16 * kk * gRow, gRow, 16 * c, lane, bb);
-                            mma_f16(acc[2 * c], pa, bb[0], bb[1]);
-                            mma_f16(acc[2 * c + 1], pa, bb[2], bb[3]);
-                        }
+                        for (int c = 0; c < kGMaxKs; ++c)
+                            if (c < nks) {
+                                uint32_t bb[4];
+                                ldb_kn(Gks + (c0 + 16 * kk) * gRow, gRow, 16 * c, lane, bb);
+                                mma_f16(gacc[2 * c], ha, bb[0], bb[1]);
+                                mma_f16(gacc[2 * c + 1], ha, bb[2], bb[3]);
+                            }
+                    }
                 }
             }
             __syncthreads();   // the key tiles are rewritten next
         }
-        if (MODE == kModeDQ) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int i = rbase + 8 * r;
-                if (i >= a.n) continue;
-                float *row = a.dq + (((int64_t)b * a.n + i) * a.Hq + h) * D;
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt)
-                    *reinterpret_cast<float2 *>(row + 8 * nt + 2 * (lane & 3)) =
-                        make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
-            }
-        }
-        cp_async_wait_all();   // copies of a head whose tiles were all skipped
-        __syncthreads();       // the query tiles are rewritten for the next head
-    }
-    if (MODE == kModeDGQ) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int i = rbase + 8 * r;
             if (i >= a.n) continue;
-            float *row = a.dg_part +
-                         (((int64_t)blockIdx.y * a.B + b) * a.n + i) * a.Kg;
+            float *row = a.dq + (((int64_t)b * a.n + i) * a.Hq + h) * D;
 #pragma unroll
-            for (int nt = 0; nt < NACC; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int c = 8 * nt + 2 * (lane & 3) + e;
-                    if (c < a.Kg) row[c] = acc[nt][2 * r + e];
-                }
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<float2 *>(row + 8 * nt + 2 * (lane & 3)) =
+                    make_float2(qacc[nt][2 * r], qacc[nt][2 * r + 1]);
         }
-        // d lambda of the CTA's pairs, in a fixed order
-        __shared__ float red[kGWarps];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
-        if (lane == 0) red[warp] = dlam;
-        __syncthreads();
-        if (tid == 0)
-            a.dlam_part[((int64_t)b * gridDim.y + blockIdx.y) * gridDim.x + qt] =
-                (red[0] + red[1]) + (red[2] + red[3]);
+        __syncthreads();   // the query tiles are rewritten for the next head
     }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = rbase + 8 * r;
+        if (i >= a.n) continue;
+        float *row = a.dg_part + (((int64_t)blockIdx.y * a.B + b) * a.n + i) * a.Kg;
+#pragma unroll
+        for (int nt = 0; nt < NG; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 8 * nt + 2 * (lane & 3) + e;
+                if (c < a.Kg) row[c] = gacc[nt][2 * r + e];
+            }
+    }
+    // d lambda of the CTA's pairs, in a fixed order
+    __shared__ float red[kGWarps];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
+    if (lane == 0) red[warp] = dlam;
+    __syncthreads();
+    if (tid == 0)
+        a.dlam_part[((int64_t)b * gridDim.y + blockIdx.y) * gridDim.x + qt] =
+            (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-
-// Backward with rows = keys (MODE kModeDV: dV, kModeDK: dK, both over the
-// query heads of one kv head; kModeDGK: the column side of dG over every
-// head, added to the row side already in dg).  For each query tile from the
-// diagonal on: S^T = K Q^T, A^T = G_k G_q^T, P^T from the queries' LSE,
-// dP^T = V dO^T, dS^T = P^T (dP^T - D); then dV += P^T dO,
+// Backward with rows = keys.  MODE kModeDKV: CTA (64 keys, kv head, batch),
+// dK and dV over the query heads of the kv head; kModeDGK: CTA (64 keys,
+// chunk of hc heads, batch), the column side of dG summed over the chunk's
+// heads (a partial per chunk).  For each query tile from the diagonal on, in
+// two halves of 32 queries: S^T = K Q^T, A^T = G_k G_q^T, P^T from the
+// queries' LSE, dP^T = V dO^T, dS^T = P^T (dP^T - D); then dV += P^T dO,
 // dK += (dS^T gate scale) Q, or dG_k += (dS^T t lambda sigma') G_q.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedArgs a)
 {
     using L = GatedBwdSmem<D>;
     constexpr int kRow = L::kRow;
-    constexpr int NACC = MODE == kModeDGK ? 2 * kGMaxKs : D / 8;
+    constexpr int NA = MODE == kModeDGK ? 2 * kGMaxKs : D / 8;   // first accumulator
+    constexpr int NB = MODE == kModeDKV ? D / 8 : 1;              // second (dV)
     grid_dep_sync();
     extern __shared__ __align__(128) uint8_t gsm[];
     const int gRow = a.kp * 2 + 16;
@@ -595,9 +596,11 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
     const int rbase = k0 + 16 * warp + (lane >> 2);
     const float l2e = 1.4426950408889634f;
 
-    float acc[NACC][4];
+    float acc[NA][4], acc2[NB][4];
 #pragma unroll
-    for (int x = 0; x < NACC; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    for (int x = 0; x < NA; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+#pragma unroll
+    for (int x = 0; x < NB; ++x) acc2[x][0] = acc2[x][1] = acc2[x][2] = acc2[x][3] = 0.f;
     load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, k0, tid);
     for (int h = h0; h < h1; ++h) {
         const int kvh = h / gqa;
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
             if (MODE == kModeDGK && all_local) continue;   // no gated pair: nothing to add
             load_tile(Qs, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
             load_tile(dOs, kRow, a.dO, b, a.n, a.Hq, h, D, q0, tid);
-            load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
+            if (!all_local) load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
             if (tid < kGT) {
                 const int i = q0 + tid;
                 const int64_t at = ((int64_t)b * a.Hq + h) * a.n + i;
@@ -621,91 +624,99 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
             }
             cp_async_wait_all();
             __syncthreads();
-            float s[8][4], ag[8][4], dp[8][4];
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                const int c0 = 32 * hf;   // first query of the half in the tile
+                float s[4][4], ag[4][4], dp[4][4];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+                for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = dp[nt][e] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t ka[4], va[4];
-                lda(Ks + 16 * warp * kRow, kRow, 16 * kk, lane, ka);
-                if (MODE != kModeDV) lda(Vs + 16 * warp * kRow, kRow, 16 * kk, lane, va);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t ka[4], va[4];
+                    lda(Ks + 16 * warp * kRow, kRow, 16 * kk, lane, ka);
+                    lda(Vs + 16 * warp * kRow, kRow, 16 * kk, lane, va);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t bb[4];
-                    ldb_nk(Qs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
-                    mma_bf16(s[2 * np], ka, bb[0], bb[1]);
-                    mma_bf16(s[2 * np + 1], ka, bb[2], bb[3]);
-                    if (MODE != kModeDV) {
-                        ldb_nk(dOs + 16 * np * kRow, kRow, 16 * kk, lane, bb);
+                    for (int np = 0; np < 2; ++np) {
+                        uint32_t bb[4];
+                        ldb_nk(Qs + (c0 + 16 * np) * kRow, kRow, 16 * kk, lane, bb);
+                        mma_bf16(s[2 * np], ka, bb[0], bb[1]);
+                        mma_bf16(s[2 * np + 1], ka, bb[2], bb[3]);
+                        ldb_nk(dOs + (c0 + 16 * np) * kRow, kRow, 16 * kk, lane, bb);
                         mma_bf16(dp[2 * np], va, bb[0], bb[1]);
                         mma_bf16(dp[2 * np + 1], va, bb[2], bb[3]);
                     }
                 }
-            }
+                if (!all_local)
 #pragma unroll
-            for (int ks = 0; ks < kGMaxKs; ++ks)
-                if (ks < nks && !all_local) {
-                    uint32_t ga[4];
-                    lda(Gks + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
+                    for (int ks = 0; ks < kGMaxKs; ++ks)
+                        if (ks < nks) {
+                            uint32_t ga[4];
+                            lda(Gks + 16 * warp * gRow, gRow, 16 * ks, lane, ga);
 #pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        uint32_t bb[4];
-                        ldb_nk(Gqs + 16 * np * gRow, gRow, 16 * ks, lane, bb);
-                        mma_f16(ag[2 * np], ga, bb[0], bb[1]);
-                        mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
-                    }
-                }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = rbase + 8 * (e >> 1);                 // key
-                    const int cl = 8 * nt + 2 * (lane & 3) + (e & 1);   // query in the tile
-                    const int i = q0 + cl;
-                    const bool valid = j <= i && i < a.n && j < a.n;
-                    const bool local = all_local || (any_local && i - j < a.window);
-                    const float t = s[nt][e] * a.scale;
-                    const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
-                    const float P = valid ? exp2f(t * sg * l2e - lse2s[cl]) : 0.f;
-                    if (MODE == kModeDV) {
-                        s[nt][e] = P;
-                    } else {
-                        const float ds = P * (dp[nt][e] - dds[cl]);
-                        if (MODE == kModeDK)
-                            s[nt][e] = ds * sg * a.scale;
-                        else
-                            s[nt][e] = (valid && !local) ? ds * t * a.lambda * sg * (1.f - sg) : 0.f;
-                    }
-                }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (MODE == kModeDGK) {
-                    const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
-                                            pack_h2(s[2 * kk][2], s[2 * kk][3]),
-                                            pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                            pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-#pragma unroll
-                    for (int c = 0; c < kGMaxKs; ++c)
-                        if (c < nks) {
-                            uint32_t bb[4];
-                            ldb_kn(Gqs + 16 * kk * gRow, gRow, 16 * c, lane, bb);
-                            mma_f16(acc[2 * c], pa, bb[0], bb[1]);
-                            mma_f16(acc[2 * c + 1], pa, bb[2], bb[3]);
+                            for (int np = 0; np < 2; ++np) {
+                                uint32_t bb[4];
+                                ldb_nk(Gqs + (c0 + 16 * np) * gRow, gRow, 16 * ks, lane, bb);
+                                mma_f16(ag[2 * np], ga, bb[0], bb[1]);
+                                mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
+                            }
                         }
-                } else {
-                    const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
-                                            pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
-                                            pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                            pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-                    const uint8_t *src = MODE == kModeDV ? dOs : Qs;
+                // P^T into dp (kModeDKV), dt into s; da into s (kModeDGK)
 #pragma unroll
-                    for (int dq = 0; dq < D / 16; ++dq) {
-                        uint32_t bb[4];
-                        ldb_kn(src + 16 * kk * kRow, kRow, 16 * dq, lane, bb);
-                        mma_bf16(acc[2 * dq], pa, bb[0], bb[1]);
-                        mma_bf16(acc[2 * dq + 1], pa, bb[2], bb[3]);
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = rbase + 8 * (e >> 1);                      // key
+                        const int cl = c0 + 8 * nt + 2 * (lane & 3) + (e & 1);   // query in the tile
+                        const int i = q0 + cl;
+                        const bool valid = j <= i && i < a.n && j < a.n;
+                        const bool local = all_local || (any_local && i - j < a.window);
+                        const float t = s[nt][e] * a.scale;
+                        const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
+                        const float P = valid ? exp2f(t * sg * l2e - lse2s[cl]) : 0.f;
+                        const float ds = P * (dp[nt][e] - dds[cl]);
+                        if (MODE == kModeDKV) {
+                            s[nt][e] = ds * sg * a.scale;
+                            dp[nt][e] = P;
+                        } else {
+                            s[nt][e] = (valid && !local) ? ds * t * a.lambda * sg * (1.f - sg) : 0.f;
+                        }
+                    }
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    if (MODE == kModeDGK) {
+                        const uint32_t ha[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
+                                                pack_h2(s[2 * kk][2], s[2 * kk][3]),
+                                                pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                                pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+                        for (int c = 0; c < kGMaxKs; ++c)
+                            if (c < nks) {
+                                uint32_t bb[4];
+                                ldb_kn(Gqs + (c0 + 16 * kk) * gRow, gRow, 16 * c, lane, bb);
+                                mma_f16(acc[2 * c], ha, bb[0], bb[1]);
+                                mma_f16(acc[2 * c + 1], ha, bb[2], bb[3]);
+                            }
+                    } else {
+                        const uint32_t ta[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
+                                                pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
+                                                pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                                pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+                        const uint32_t pa[4] = {pack_bf16x2(dp[2 * kk][0], dp[2 * kk][1]),
+                                                pack_bf16x2(dp[2 * kk][2], dp[2 * kk][3]),
+                                                pack_bf16x2(dp[2 * kk + 1][0], dp[2 * kk + 1][1]),
+                                                pack_bf16x2(dp[2 * kk + 1][2], dp[2 * kk + 1][3])};
+#pragma unroll
+                        for (int dq = 0; dq < D / 16; ++dq) {
+                            uint32_t bb[4];
+                            ldb_kn(Qs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
+                            mma_bf16(acc[2 * dq], ta, bb[0], bb[1]);
+                            mma_bf16(acc[2 * dq + 1], ta, bb[2], bb[3]);
+                            ldb_kn(dOs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
+                            mma_bf16(acc2[(2 * dq) % NB], pa, bb[0], bb[1]);
+                            mma_bf16(acc2[(2 * dq + 1) % NB], pa, bb[2], bb[3]);
+                        }
                     }
                 }
             }
@@ -713,20 +724,23 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
         }
         cp_async_wait_all();   // copies of a head whose tiles were all skipped
         __syncthreads();
-        if (MODE != kModeDGK && h + 1 == h1) {
+    }
+    if (MODE == kModeDKV) {
+        const int kvh = h0 / gqa;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int j = rbase + 8 * r;
-                if (j >= a.n) continue;
-                float *row = (MODE == kModeDK ? a.dk : a.dv) + (((int64_t)b * a.n + j) * a.Hkv + kvh) * D;
+        for (int r = 0; r < 2; ++r) {
+            const int j = rbase + 8 * r;
+            if (j >= a.n) continue;
+            const int64_t off = (((int64_t)b * a.n + j) * a.Hkv + kvh) * D + 2 * (lane & 3);
 #pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt)
-                    *reinterpret_cast<float2 *>(row + 8 * nt + 2 * (lane & 3)) =
-                        make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+            for (int nt = 0; nt < D / 8; ++nt) {
+                *reinterpret_cast<float2 *>(a.dk + off + 8 * nt) =
+                    make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+                *reinterpret_cast<float2 *>(a.dv + off + 8 * nt) =
+                    make_float2(acc2[nt % NB][2 * r], acc2[nt % NB][2 * r + 1]);
             }
         }
-    }
-    if (MODE == kModeDGK) {
+    } else {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int j = rbase + 8 * r;
@@ -734,7 +748,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
             float *row = a.dg_part +
                          ((((int64_t)a.nhc + blockIdx.y) * a.B + b) * a.n + j) * a.Kg;
 #pragma unroll
-            for (int nt = 0; nt < NACC; ++nt)
+            for (int nt = 0; nt < NA; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int c = 8 * nt + 2 * (lane & 3) + e;
@@ -789,10 +803,8 @@ cudaError_t gated_preflight_d(int kp)
     const int fwd = 2 * GatedSmem<D>::stage(kp), bwd = GatedBwdSmem<D>::bytes(kp);
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaFuncSetAttribute(gated_fwd_kernel<D>, at, fwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D, kModeDQ>, at, bwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D, kModeDGQ>, at, bwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDK>, at, bwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDV>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDKV>, at, bwd);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDGK>, at, bwd);
     return e;
 }
@@ -872,19 +884,11 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dq", s);
-    e = launch_pdl(gated_bwd_q_kernel<D, kModeDQ>, dim3(nqt, p.Hq, p.B), blk, smem, s, a);
+    e = launch_pdl(gated_bwd_q_kernel<D>, dim3(nqt, a.nhc, p.B), blk, smem, s, a);
     prof_end(s);
     if (e != cudaSuccess) return e;
-    prof_begin("gated_bwd_dgq", s);
-    e = launch_pdl(gated_bwd_q_kernel<D, kModeDGQ>, dim3(nqt, a.nhc, p.B), blk, smem, s, a);
-    prof_end(s);
-    if (e != cudaSuccess) return e;
-    prof_begin("gated_bwd_dk", s);
-    e = launch_pdl(gated_bwd_k_kernel<D, kModeDK>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
-    prof_end(s);
-    if (e != cudaSuccess) return e;
-    prof_begin("gated_bwd_dv", s);
-    e = launch_pdl(gated_bwd_k_kernel<D, kModeDV>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
+    prof_begin("gated_bwd_dkv", s);
+    e = launch_pdl(gated_bwd_k_kernel<D, kModeDKV>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dgk", s);
@@ -902,7 +906,7 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     e = launch_pdl(gated_dlam_kernel, dim3(1), dim3(32), 0, s, a.dlam_part, p.B * a.nhc * nqt,
                    p.dlam);
     prof_end(s);
-    *launches += 8;
+    *launches += 6;
     return e;
 }
 
