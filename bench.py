@@ -550,6 +550,9 @@ def main():
     _, tot = fg.focus_count_pairs(ids, off, pos, inv, w.K, w.window, per_query=False)
     total_pairs, share_pairs = (int(x) for x in tot.cpu().tolist())
     eff_flop = 4.0 * w.d * w.Hq * total_pairs
+    sizes = (off[:, 1:] - off[:, :-1]).flatten().float()
+    group_size = {"max": int(sizes.max()), "median": float(sizes.median()),
+                  "mean": float(sizes.mean()), "min": int(sizes.min())}
 
     # ---- per-kernel times (separate pass, events around every launch)
     # (about 3 s of steps: 50 at n = 8K, about 17 at n = 1M)
@@ -705,7 +708,7 @@ def main():
             "effective_frac_of_bf16_sustained": eff_flop / (ms_per_step * 1e-3) / 1e12
             / float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])),
             "attention_effective_tflops": eff_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
-            "allowed_pairs": total_pairs, "group_pairs": share_pairs,
+            "allowed_pairs": total_pairs, "group_pairs": share_pairs, "group_size": group_size,
             "roofline": roof, "kernels": kernels, "dense_causal": dense, "decode": decode,
             "sinkhorn": sinkhorn, "gated_training": gated,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
