@@ -60,6 +60,7 @@ CASES = [
     (1, 1, 2, 1, 64, 16, 4, 1.0),
     (2, 257, 4, 4, 128, 33, 1, 6.0),
     (1, 700, 4, 2, 64, 16, 200, 2.5),   # tiles wholly inside, across and outside the window
+    (2, 150, 16, 2, 64, 48, 8, 3.0),    # GQA 8:1, two head chunks for dG
 ]
 
 

@@ -63,6 +63,8 @@ CASES = [
     (2, 333, 1, 1.0, 2),        # one group: P = 1
     (1, 2000, 33, 1.0, 60),     # converged: token masses 1 as well
     (400, 20, 16, 1.0, 4),      # more sequences than CTAs per sequence
+    (2, 50000, 33, 0.7, 3),     # the plain-load sweep over many rows
+    (3, 4099, 100, 1.0, 5),     # the bulk sweep with four lanes per row and a ragged last chunk
 ]
 
 
