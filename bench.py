@@ -433,7 +433,7 @@ def bench_gated(fg, torch, flush, stream, peaks, args):
     V = torch.randn(B, n, Hkv, d, generator=g, device="cuda").to(torch.bfloat16)
     G = torch.softmax(2.0 * torch.randn(B, n, Kg, generator=g, device="cuda"), -1).contiguous()
     dO = torch.randn(B, n, Hq, d, generator=g, device="cuda").to(torch.bfloat16)
-    ws = torch.empty(fg.focus_gated_workspace_size(B, n, Hq, Kg), dtype=torch.uint8,
+    ws = torch.empty(fg.focus_gated_workspace_size(B, n, Hq, Hkv, Kg), dtype=torch.uint8,
                      device="cuda")
     O, lse = fg.focus_gated_attention_fwd(Q, K, V, G, win, GATED_LAMBDA, ws=ws)
     out = fg.focus_gated_attention_bwd(Q, K, V, G, O, lse, dO, win, GATED_LAMBDA, ws=ws)

@@ -268,7 +268,7 @@ focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, c
  *   bwd: O, lse from the forward; dO [B, n, Hq, d] bf16 (the gradient of the
  *        loss by O) -> dQ [B, n, Hq, d], dK and dV [B, n, Hkv, d],
  *        dG [B, n, Kg] fp32, *dlambda fp32 (one value, device), all overwritten
- *   ws, ws_bytes: at least focus_gated_workspace_size(B, n, Hq, Kg) bytes.
+ *   ws, ws_bytes: at least focus_gated_workspace_size(B, n, Hq, Hkv, Kg) bytes.
  * Arithmetic: tensor-core tiles with fp32 accumulation: Q K^T, P V and the
  * gradient products in bf16, G G^T and the dG products in fp16; the gate,
  * softmax and dS in fp32.  The backward recomputes P from lse; every sum has
@@ -278,7 +278,7 @@ focus_status_t focus_decode_fwd(const void *q, const void *Kc, const void *Vc, c
  * out of range), FOCUS_ERR_UNSUPPORTED, FOCUS_ERR_WORKSPACE; nothing is
  * launched then.
  */
-size_t focus_gated_workspace_size(int B, int n, int Hq, int Kg);
+size_t focus_gated_workspace_size(int B, int n, int Hq, int Hkv, int Kg);
 focus_status_t focus_gated_attention_fwd(const void *Q, const void *K, const void *V,
                                          const float *G, int B, int n, int Hq, int Hkv, int d,
                                          int Kg, int window, float lambda, float scale, void *O,

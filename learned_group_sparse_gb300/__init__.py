@@ -77,7 +77,7 @@ def library() -> ctypes.CDLL:
                 "focus_bucket_static": ([vp, i32, i32, i32, i32, vp, vp, vp, vp], i32),
                 "focus_decode_workspace_size": ([i32] * 4, sz),
                 "focus_sinkhorn_workspace_size": ([i32] * 3, sz),
-                "focus_gated_workspace_size": ([i32] * 4, sz),
+                "focus_gated_workspace_size": ([i32] * 5, sz),
                 "focus_gated_attention_fwd": ([vp] * 4 + [i32] * 7 + [f32, f32, vp, vp, vp, sz,
                                               vp], i32),
                 "focus_gated_attention_bwd": ([vp] * 7 + [i32] * 7 + [f32, f32] + [vp] * 6 +
@@ -321,8 +321,8 @@ def focus_prefill(X, Wg, C, Q, K, V, topk, window, scale=0.0, O=None, lse=None, 
     return O, lse
 
 
-def focus_gated_workspace_size(B, n, Hq, Kg) -> int:
-    return int(library().focus_gated_workspace_size(B, n, Hq, Kg))
+def focus_gated_workspace_size(B, n, Hq, Hkv, Kg) -> int:
+    return int(library().focus_gated_workspace_size(B, n, Hq, Hkv, Kg))
 
 
 def _gated_common(Q, K, V, G):
@@ -344,7 +344,7 @@ def focus_gated_attention_fwd(Q, K, V, G, window, lam, scale=0.0, O=None, lse=No
     if lse is None:
         lse = torch.empty(B, Hq, n, dtype=torch.float32, device=Q.device)
     if ws is None:
-        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Kg)), dtype=torch.uint8,
+        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Hkv, Kg)), dtype=torch.uint8,
                          device=Q.device)
     _check("focus_gated_attention_fwd", library().focus_gated_attention_fwd(
         _p(Q), _p(K), _p(V), _p(G), B, n, Hq, Hkv, d, Kg, int(window), float(lam), float(scale),
@@ -369,7 +369,7 @@ def focus_gated_attention_bwd(Q, K, V, G, O, lse, dO, window, lam, scale=0.0, ws
                torch.empty(B, n, Kg, dtype=torch.float32, device=dev),
                torch.empty(1, dtype=torch.float32, device=dev))
     if ws is None:
-        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Kg)), dtype=torch.uint8,
+        ws = torch.empty(max(1, focus_gated_workspace_size(B, n, Hq, Hkv, Kg)), dtype=torch.uint8,
                          device=dev)
     dQ, dK, dV, dG, dl = out
     _check("focus_gated_attention_bwd", library().focus_gated_attention_bwd(

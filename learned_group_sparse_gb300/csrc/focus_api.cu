@@ -708,10 +708,10 @@ focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets, con
     return cuda_status(e);
 }
 
-size_t focus_gated_workspace_size(int B, int n, int Hq, int Kg)
+size_t focus_gated_workspace_size(int B, int n, int Hq, int Hkv, int Kg)
 {
-    if (B < 1 || n < 1 || Hq < 1 || Kg < 1 || Kg > 128) return 0;
-    return gated_ws_bytes(B, n, Hq, Kg);
+    if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Kg < 1 || Kg > 128) return 0;
+    return gated_ws_bytes(B, n, Hq, Hkv, Kg);
 }
 
 static focus_status_t check_gated(const void *Q, const void *K, const void *V, const float *G,
@@ -727,7 +727,7 @@ static focus_status_t check_gated(const void *Q, const void *K, const void *V, c
     if ((d != 64 && d != 128) || Kg > 128 || (int64_t)B * n * Hq * d >= ((int64_t)1 << 40) ||
         (n + 63) / 64 > 65535 || Hq > 65535 || B > 65535)
         return FOCUS_ERR_UNSUPPORTED;
-    if (ws_bytes < gated_ws_bytes(B, n, Hq, Kg)) return FOCUS_ERR_WORKSPACE;
+    if (ws_bytes < gated_ws_bytes(B, n, Hq, Hkv, Kg)) return FOCUS_ERR_WORKSPACE;
     return FOCUS_OK;
 }
 

@@ -22,9 +22,9 @@
 //   gated_bwd_q_kernel      rows = queries (CTA: 64 queries, 4 heads,
 //                           batch): dQ, the row side of dG, sum_j da_ij g_j,
 //                           and d lambda
-//   gated_bwd_k_kernel      rows = keys: dK and dV (CTA: 64 keys, kv head,
-//                           batch, over its query heads); the column side of
-//                           dG, sum_i da_ij g_i (CTA: 64 keys, 4 heads, batch)
+//   gated_bwd_k_kernel      rows = keys (CTA: 64 keys, kv head, batch, over
+//                           its query heads): dK, dV and the column side of
+//                           dG, sum_i da_ij g_i
 //   gated_dg_reduce_kernel  dG = the sum of the per-chunk partials
 // with dS_ij = P_ij (dP_ij - D_i), dP_ij = dO_i . v_j, and for a gated pair
 // d gate_ij = dS_ij t_ij, da_ij = d gate_ij lambda sigma (1 - sigma).
@@ -58,7 +58,8 @@ struct GatedArgs {
     float *lse_out;                   // forward
     float *dq, *dk, *dv, *dg;         // [B, n, Hq, D], [B, n, Hkv, D] x 2, [B, n, Kg]
     float *dlam_part;                 // [B, nhc, n / 64] partial d lambda
-    float *dg_part;                   // [2][nhc][B, n, Kg]: row and column sides of dG
+    float *dg_part;                   // [nhc + Hkv][B, n, Kg]: row side per head chunk, column
+                                      // side per kv head
     int B, n, Hq, Hkv, kp, Kg, window;
     int hc, nhc;                      // query heads per dG chunk, chunks
     float scale, lambda;
@@ -369,8 +370,6 @@ __global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ Dd)
     }
 }
 
-enum GMode { kModeDQG = 0, kModeDKV = 1, kModeDGK = 2 };
-
 // Shared layout of a backward CTA: the tiles of its own rows (queries:
 // Q, dO, G_q; keys: K, V, G_k), then one stage of the other side's tiles,
 // then the other side's log-sum-exp and D (key orientation only).
@@ -378,7 +377,11 @@ template <int D>
 struct GatedBwdSmem {
     static constexpr int kRow = D * 2 + 16;
     static __host__ __device__ int side(int kp) { return kGT * (2 * kRow + kp * 2 + 16); }
-    static __host__ __device__ int bytes(int kp) { return 2 * side(kp) + 2 * kGT * 4; }
+    // + the dG_k tile of the key side, [64][kp + 8] floats
+    static __host__ __device__ int bytes(int kp)
+    {
+        return 2 * side(kp) + 2 * kGT * 4 + kGT * (kp + 8) * 4;
+    }
 };
 
 // Backward with rows = queries, CTA (64 queries, chunk of hc heads, batch):
@@ -563,32 +566,33 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_q_kernel(const GatedAr
             (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-// Backward with rows = keys.  MODE kModeDKV: CTA (64 keys, kv head, batch),
-// dK and dV over the query heads of the kv head; kModeDGK: CTA (64 keys,
-// chunk of hc heads, batch), the column side of dG summed over the chunk's
-// heads (a partial per chunk).  For each query tile from the diagonal on, in
-// two halves of 32 queries: S^T = K Q^T, A^T = G_k G_q^T, P^T from the
-// queries' LSE, dP^T = V dO^T, dS^T = P^T (dP^T - D); then dV += P^T dO,
-// dK += (dS^T gate scale) Q, or dG_k += (dS^T t lambda sigma') G_q.
-template <int D, int MODE>
+// Backward with rows = keys, CTA (64 keys, kv head, batch), over the query
+// heads of the kv head: dK, dV and the column side of dG.  For each query
+// tile from the diagonal on, in two halves of 32 queries: S^T = K Q^T,
+// A^T = G_k G_q^T, P^T from the queries' LSE, dP^T = V dO^T,
+// dS^T = P^T (dP^T - D); then dV += P^T dO, dK += (dS^T gate scale) Q and,
+// for gated pairs, dG_k += (dS^T t lambda sigma') G_q.  dK and dV stay in
+// registers; the dG_k products are added into a shared [64][kp] tile (each
+// element owned by one lane), written at the end as this kv head's partial.
+template <int D>
 __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedArgs a)
 {
     using L = GatedBwdSmem<D>;
     constexpr int kRow = L::kRow;
-    constexpr int NA = MODE == kModeDGK ? 2 * kGMaxKs : D / 8;   // first accumulator
-    constexpr int NB = MODE == kModeDKV ? D / 8 : 1;              // second (dV)
     grid_dep_sync();
     extern __shared__ __align__(128) uint8_t gsm[];
     const int gRow = a.kp * 2 + 16;
+    const int gStride = a.kp + 8;   // floats per row of the dG_k tile
     uint8_t *Ks = gsm, *Vs = gsm + kGT * kRow, *Gks = gsm + 2 * kGT * kRow;
     uint8_t *Qs = gsm + L::side(a.kp), *dOs = Qs + kGT * kRow, *Gqs = Qs + 2 * kGT * kRow;
     float *lse2s = reinterpret_cast<float *>(gsm + 2 * L::side(a.kp));
     float *dds = lse2s + kGT;
-    const int kt = blockIdx.x;   // the first key tiles have the most query tiles
+    float *dgs = dds + kGT;         // [64][gStride]
+    const int kt = blockIdx.x;      // the first key tiles have the most query tiles
     const int b = blockIdx.z;
     const int gqa = a.Hq / a.Hkv;
-    const int h0 = (int)blockIdx.y * (MODE == kModeDGK ? a.hc : gqa);
-    const int h1 = MODE == kModeDGK ? min(a.Hq, h0 + a.hc) : h0 + gqa;
+    const int kvh = blockIdx.y;
+    const int h0 = kvh * gqa, h1 = h0 + gqa;
     const int k0 = kt * kGT;
     const int nqt = (a.n + kGT - 1) / kGT;
     const int nks = a.kp / 16;
@@ -596,23 +600,21 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
     const int rbase = k0 + 16 * warp + (lane >> 2);
     const float l2e = 1.4426950408889634f;
 
-    float acc[NA][4], acc2[NB][4];
+    float dk[D / 8][4], dv[D / 8][4];
 #pragma unroll
-    for (int x = 0; x < NA; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-#pragma unroll
-    for (int x = 0; x < NB; ++x) acc2[x][0] = acc2[x][1] = acc2[x][2] = acc2[x][3] = 0.f;
+    for (int x = 0; x < D / 8; ++x) {
+        dk[x][0] = dk[x][1] = dk[x][2] = dk[x][3] = 0.f;
+        dv[x][0] = dv[x][1] = dv[x][2] = dv[x][3] = 0.f;
+    }
+    for (int x = tid; x < kGT * gStride; x += kGThreads) dgs[x] = 0.f;
     load_tile(Gks, gRow, a.g, b, a.n, 1, 0, a.kp, k0, tid);
+    load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, k0, tid);
+    load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, k0, tid);
     for (int h = h0; h < h1; ++h) {
-        const int kvh = h / gqa;
-        if (h == h0 || h % gqa == 0) {   // this kv head's K and V rows
-            load_tile(Ks, kRow, a.k, b, a.n, a.Hkv, kvh, D, k0, tid);
-            load_tile(Vs, kRow, a.v, b, a.n, a.Hkv, kvh, D, k0, tid);
-        }
         for (int qt = kt; qt < nqt; ++qt) {
             const int q0 = qt * kGT;
             const bool all_local = tile_all_local(q0, k0, a.window);
             const bool any_local = tile_any_local(q0, k0, a.window);
-            if (MODE == kModeDGK && all_local) continue;   // no gated pair: nothing to add
             load_tile(Qs, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
             load_tile(dOs, kRow, a.dO, b, a.n, a.Hq, h, D, q0, tid);
             if (!all_local) load_tile(Gqs, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
                                 mma_f16(ag[2 * np + 1], ga, bb[2], bb[3]);
                             }
                         }
-                // P^T into dp (kModeDKV), dt into s; da into s (kModeDGK)
+                // P^T into dp, dt into s, da into ag
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -676,85 +678,86 @@ __global__ void __launch_bounds__(kGThreads, 2) gated_bwd_k_kernel(const GatedAr
                         const float sg = local ? 1.f : sigmoidf_(a.lambda * ag[nt][e]);
                         const float P = valid ? exp2f(t * sg * l2e - lse2s[cl]) : 0.f;
                         const float ds = P * (dp[nt][e] - dds[cl]);
-                        if (MODE == kModeDKV) {
-                            s[nt][e] = ds * sg * a.scale;
-                            dp[nt][e] = P;
-                        } else {
-                            s[nt][e] = (valid && !local) ? ds * t * a.lambda * sg * (1.f - sg) : 0.f;
-                        }
+                        s[nt][e] = ds * sg * a.scale;
+                        dp[nt][e] = P;
+                        ag[nt][e] = (valid && !local) ? ds * t * a.lambda * sg * (1.f - sg) : 0.f;
                     }
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
-                    if (MODE == kModeDGK) {
-                        const uint32_t ha[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]),
-                                                pack_h2(s[2 * kk][2], s[2 * kk][3]),
-                                                pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                                pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+                    const uint32_t ta[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
+                                            pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
+                                            pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                            pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+                    const uint32_t pa[4] = {pack_bf16x2(dp[2 * kk][0], dp[2 * kk][1]),
+                                            pack_bf16x2(dp[2 * kk][2], dp[2 * kk][3]),
+                                            pack_bf16x2(dp[2 * kk + 1][0], dp[2 * kk + 1][1]),
+                                            pack_bf16x2(dp[2 * kk + 1][2], dp[2 * kk + 1][3])};
 #pragma unroll
-                        for (int c = 0; c < kGMaxKs; ++c)
-                            if (c < nks) {
-                                uint32_t bb[4];
-                                ldb_kn(Gqs + (c0 + 16 * kk) * gRow, gRow, 16 * c, lane, bb);
-                                mma_f16(acc[2 * c], ha, bb[0], bb[1]);
-                                mma_f16(acc[2 * c + 1], ha, bb[2], bb[3]);
-                            }
-                    } else {
-                        const uint32_t ta[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
-                                                pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
-                                                pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                                pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-                        const uint32_t pa[4] = {pack_bf16x2(dp[2 * kk][0], dp[2 * kk][1]),
-                                                pack_bf16x2(dp[2 * kk][2], dp[2 * kk][3]),
-                                                pack_bf16x2(dp[2 * kk + 1][0], dp[2 * kk + 1][1]),
-                                                pack_bf16x2(dp[2 * kk + 1][2], dp[2 * kk + 1][3])};
+                    for (int dq = 0; dq < D / 16; ++dq) {
+                        uint32_t bb[4];
+                        ldb_kn(Qs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
+                        mma_bf16(dk[2 * dq], ta, bb[0], bb[1]);
+                        mma_bf16(dk[2 * dq + 1], ta, bb[2], bb[3]);
+                        ldb_kn(dOs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
+                        mma_bf16(dv[2 * dq], pa, bb[0], bb[1]);
+                        mma_bf16(dv[2 * dq + 1], pa, bb[2], bb[3]);
+                    }
+                }
+                if (!all_local) {
+                    // dG_k += da G_q over the half's 32 queries, two n-tiles
+                    // (16 group columns) at a time, added into the shared tile
+                    uint32_t ha[2][4];
 #pragma unroll
-                        for (int dq = 0; dq < D / 16; ++dq) {
+                    for (int kk = 0; kk < 2; ++kk) {
+                        ha[kk][0] = pack_h2(ag[2 * kk][0], ag[2 * kk][1]);
+                        ha[kk][1] = pack_h2(ag[2 * kk][2], ag[2 * kk][3]);
+                        ha[kk][2] = pack_h2(ag[2 * kk + 1][0], ag[2 * kk + 1][1]);
+                        ha[kk][3] = pack_h2(ag[2 * kk + 1][2], ag[2 * kk + 1][3]);
+                    }
+                    for (int c = 0; c < nks; ++c) {
+                        float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
                             uint32_t bb[4];
-                            ldb_kn(Qs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
-                            mma_bf16(acc[2 * dq], ta, bb[0], bb[1]);
-                            mma_bf16(acc[2 * dq + 1], ta, bb[2], bb[3]);
-                            ldb_kn(dOs + (c0 + 16 * kk) * kRow, kRow, 16 * dq, lane, bb);
-                            mma_bf16(acc2[(2 * dq) % NB], pa, bb[0], bb[1]);
-                            mma_bf16(acc2[(2 * dq + 1) % NB], pa, bb[2], bb[3]);
+                            ldb_kn(Gqs + (c0 + 16 * kk) * gRow, gRow, 16 * c, lane, bb);
+                            mma_f16(g0, ha[kk], bb[0], bb[1]);
+                            mma_f16(g1, ha[kk], bb[2], bb[3]);
+                        }
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            float *row = dgs + (16 * warp + (lane >> 2) + 8 * r) * gStride +
+                                         16 * c + 2 * (lane & 3);
+                            float2 *p0 = reinterpret_cast<float2 *>(row);
+                            float2 *p1 = reinterpret_cast<float2 *>(row + 8);
+                            const float2 v0 = *p0, v1 = *p1;
+                            *p0 = make_float2(v0.x + g0[2 * r], v0.y + g0[2 * r + 1]);
+                            *p1 = make_float2(v1.x + g1[2 * r], v1.y + g1[2 * r + 1]);
                         }
                     }
                 }
             }
             __syncthreads();   // the query tiles are rewritten next
         }
-        cp_async_wait_all();   // copies of a head whose tiles were all skipped
-        __syncthreads();
     }
-    if (MODE == kModeDKV) {
-        const int kvh = h0 / gqa;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int j = rbase + 8 * r;
-            if (j >= a.n) continue;
-            const int64_t off = (((int64_t)b * a.n + j) * a.Hkv + kvh) * D + 2 * (lane & 3);
+    for (int r = 0; r < 2; ++r) {
+        const int j = rbase + 8 * r;
+        if (j >= a.n) continue;
+        const int64_t off = (((int64_t)b * a.n + j) * a.Hkv + kvh) * D + 2 * (lane & 3);
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                *reinterpret_cast<float2 *>(a.dk + off + 8 * nt) =
-                    make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
-                *reinterpret_cast<float2 *>(a.dv + off + 8 * nt) =
-                    make_float2(acc2[nt % NB][2 * r], acc2[nt % NB][2 * r + 1]);
-            }
+        for (int nt = 0; nt < D / 8; ++nt) {
+            *reinterpret_cast<float2 *>(a.dk + off + 8 * nt) =
+                make_float2(dk[nt][2 * r], dk[nt][2 * r + 1]);
+            *reinterpret_cast<float2 *>(a.dv + off + 8 * nt) =
+                make_float2(dv[nt][2 * r], dv[nt][2 * r + 1]);
         }
-    } else {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int j = rbase + 8 * r;
-            if (j >= a.n) continue;
-            float *row = a.dg_part +
-                         ((((int64_t)a.nhc + blockIdx.y) * a.B + b) * a.n + j) * a.Kg;
-#pragma unroll
-            for (int nt = 0; nt < NA; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int c = 8 * nt + 2 * (lane & 3) + e;
-                    if (c < a.Kg) row[c] = acc[nt][2 * r + e];
-                }
-        }
+    }
+    // this kv head's partial of the column side of dG (its rows only)
+    __syncthreads();
+    float *part = a.dg_part + ((((int64_t)a.nhc + kvh) * a.B + b) * a.n) * a.Kg;
+    for (int x = tid; x < kGT * a.Kg; x += kGThreads) {
+        const int r = x / a.Kg, c = x - r * a.Kg;
+        if (k0 + r < a.n) part[(int64_t)(k0 + r) * a.Kg + c] = dgs[r * gStride + c];
     }
 }
 
@@ -766,7 +769,7 @@ __global__ void gated_dg_reduce_kernel(const GatedArgs a)
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
         float s = 0.f;
-        for (int c = 0; c < 2 * a.nhc; ++c) s += a.dg_part[(int64_t)c * total + x];
+        for (int c = 0; c < a.nhc + a.Hkv; ++c) s += a.dg_part[(int64_t)c * total + x];
         a.dg[x] = s;
     }
 }
@@ -784,7 +787,7 @@ __global__ void gated_dlam_kernel(const float *__restrict__ part, int count, flo
 
 }  // namespace
 
-size_t gated_ws_bytes(int B, int n, int Hq, int Kg)
+size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg)
 {
     const size_t a256 = 255;
     const int kp = (Kg + 15) / 16 * 16;
@@ -792,7 +795,7 @@ size_t gated_ws_bytes(int B, int n, int Hq, int Kg)
     const int nhc = (Hq + kGHeadChunk - 1) / kGHeadChunk;
     return (((size_t)B * n * kp * 2 + a256) & ~a256) + (((size_t)B * Hq * n * 4 + a256) & ~a256) +
            (((size_t)B * nhc * nqt * 4 + a256) & ~a256) +
-           (((size_t)2 * nhc * B * n * Kg * 4 + a256) & ~a256);
+           (((size_t)(nhc + Hkv) * B * n * Kg * 4 + a256) & ~a256);
 }
 
 namespace {
@@ -804,8 +807,7 @@ cudaError_t gated_preflight_d(int kp)
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaFuncSetAttribute(gated_fwd_kernel<D>, at, fwd);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D>, at, bwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDKV>, at, bwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D, kModeDGK>, at, bwd);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D>, at, bwd);
     return e;
 }
 
@@ -888,11 +890,7 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin("gated_bwd_dkv", s);
-    e = launch_pdl(gated_bwd_k_kernel<D, kModeDKV>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
-    prof_end(s);
-    if (e != cudaSuccess) return e;
-    prof_begin("gated_bwd_dgk", s);
-    e = launch_pdl(gated_bwd_k_kernel<D, kModeDGK>, dim3(nqt, a.nhc, p.B), blk, smem, s, a);
+    e = launch_pdl(gated_bwd_k_kernel<D>, dim3(nqt, p.Hkv, p.B), blk, smem, s, a);
     prof_end(s);
     if (e != cudaSuccess) return e;
     const int64_t dgn = (int64_t)p.B * p.n * p.Kg;
@@ -906,7 +904,7 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *
     e = launch_pdl(gated_dlam_kernel, dim3(1), dim3(32), 0, s, a.dlam_part, p.B * a.nhc * nqt,
                    p.dlam);
     prof_end(s);
-    *launches += 6;
+    *launches += 5;
     return e;
 }
 

@@ -182,7 +182,7 @@ struct GatedLaunch {
     int B, n, Hq, Hkv, d, Kg, window;
     float scale, lambda;
 };
-size_t gated_ws_bytes(int B, int n, int Hq, int Kg);
+size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg);
 cudaError_t gated_preflight(int d, int Kg);
 cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
 cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);

@@ -150,9 +150,10 @@ def test_sinkhorn_validation(lib):
 
 
 def test_gated_validation(lib):
-    need = fg.focus_gated_workspace_size(1, 100, 4, 16)
+    need = fg.focus_gated_workspace_size(1, 100, 4, 2, 16)
     assert need > 0
-    assert fg.focus_gated_workspace_size(1, 100, 4, 129) == 0   # K_g above 128
+    assert fg.focus_gated_workspace_size(1, 100, 4, 2, 129) == 0   # K_g above 128
+    assert fg.focus_gated_workspace_size(1, 100, 4, 3, 16) == 0    # Hq % Hkv != 0
     f = lib.focus_gated_attention_fwd
     ok = (P, P, P, P, 1, 100, 4, 2, 64, 16, 8, 2.0, 0.0, P2, P2, P2, need, None)
     for k, bad, want in ((0, None, INVALID), (3, MIS, INVALID), (4, 0, INVALID),
