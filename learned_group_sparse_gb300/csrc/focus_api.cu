@@ -128,6 +128,22 @@ bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t oute
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_4d(CUtensorMap *m, const void *base, bool f16, int B, int64_t rows, int H, int d,
+                 uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
+                                   (cuuint64_t)rows * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, box_rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -740,8 +756,8 @@ focus_status_t focus_gated_attention_fwd(const void *Q, const void *K, const voi
                                     ws_bytes);
     if (st) return st;
     if (!O || !lse || !aligned16(O) || !aligned16(lse)) return FOCUS_ERR_INVALID_ARG;
-    if (gated_preflight(d, Kg) != cudaSuccess) return FOCUS_ERR_CUDA;
     GatedLaunch p{};
+    if (wait_ctl(&p.wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     p.q = static_cast<const __nv_bfloat16 *>(Q);
     p.k = static_cast<const __nv_bfloat16 *>(K);
     p.v = static_cast<const __nv_bfloat16 *>(V);

@@ -7,17 +7,15 @@
 // product of the tokens' soft group assignments (rows of G); q . k is scaled
 // by `scale` before the gate; causal softmax over j <= i.
 //
-// All kernels tile queries and keys by 64; a warp owns 16 rows of a tile and
-// runs m16n8k16 tensor-core MMAs (`mma.sync`, fp32 accumulation): S = Q K^T
-// in bf16 and A = G_q G_k^T in fp16 (G is converted once to fp16, its
-// columns padded to a multiple of 16 with zeros), then the gate and the
-// online softmax in registers, P V with P in bf16.  The per-pair work is a
-// few tile products over d and K_g, so these are contractions of the
-// classic flash-attention shape with M = 16 rows per warp.
-//
-// Forward: gated_fwd_kernel, CTA (64 queries, query head, batch); O in bf16
-// and the log-sum-exp.  Backward (each kernel recomputes P from the
-// log-sum-exp, so none needs atomics and every sum has a fixed order):
+// The forward runs on the 5th-generation tensor cores (focus_gated_tc.cu):
+// the fp16 copy of G made here (its columns padded to a multiple of 16 with
+// zeros) feeds a second product A = G_q G_k^T beside S = Q K^T in TMEM.
+// The backward kernels here tile queries and keys by 64; a warp owns 16 rows
+// of a tile and runs m16n8k16 tensor-core MMAs (`mma.sync`, fp32
+// accumulation): S = Q K^T in bf16 and A = G_q G_k^T in fp16, the gate and
+// P in registers, then the gradient products.  Each kernel recomputes P
+// from the forward's log-sum-exp, so none needs atomics and every sum has a
+// fixed order:
 //   gated_bwd_prep_kernel   D_i = dO_i . O_i per (row, head)
 //   gated_bwd_q_kernel      rows = queries (CTA: 64 queries, 4 heads,
 //                           batch): dQ, the row side of dG, sum_j da_ij g_j,
@@ -147,16 +145,6 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, int stride, const void *
     }
 }
 
-// Shared-memory rows: D bf16 (or kp fp16) values plus 16 bytes, so that the
-// eight row addresses of an ldmatrix fall in eight different bank groups.
-template <int D>
-struct GatedSmem {
-    static constexpr int kRow = D * 2 + 16;
-    static __host__ __device__ int g_row(int kp) { return kp * 2 + 16; }
-    // one stage: K and V tiles, then the G tile
-    static __host__ __device__ int stage(int kp) { return kGT * (2 * kRow + g_row(kp)); }
-};
-
 // sigma(z) = 1/2 + tanh(z / 2) / 2 with the hardware tanh approximation
 // (relative error about 2^-11: below the fp16 rounding of the G products).
 __device__ __forceinline__ float sigmoidf_(float z)
@@ -177,162 +165,6 @@ __device__ __forceinline__ bool tile_any_local(int q0, int k0, int window)
     return q0 - (k0 + kGT - 1) < window;
 }
 
-
-template <int D>
-__global__ void __launch_bounds__(kGThreads, 2) gated_fwd_kernel(const GatedArgs a)
-{
-    using L = GatedSmem<D>;
-    constexpr int kRow = L::kRow;
-    grid_dep_sync();
-    extern __shared__ __align__(128) uint8_t gsm[];
-    const int gRow = L::g_row(a.kp), stageB = L::stage(a.kp);
-    const int qt = gridDim.x - 1 - blockIdx.x;   // the longest rows first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int kvh = h / (a.Hq / a.Hkv);
-    const int q0 = qt * kGT;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nks = a.kp / 16;
-    const float scale2 = a.scale * 1.4426950408889634f;
-
-    auto load_kv = [&](int kt, uint8_t *st) {
-        load_tile(st, kRow, a.k, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
-        load_tile(st + kGT * kRow, kRow, a.v, b, a.n, a.Hkv, kvh, D, kt * kGT, tid);
-        load_tile(st + 2 * kGT * kRow, gRow, a.g, b, a.n, 1, 0, a.kp, kt * kGT, tid);
-    };
-    // the query and G tiles pass through stage 1, key tile 0 goes to stage 0
-    uint8_t *s1 = gsm + stageB;
-    load_tile(s1, kRow, a.q, b, a.n, a.Hq, h, D, q0, tid);
-    load_tile(s1 + kGT * kRow, gRow, a.g, b, a.n, 1, 0, a.kp, q0, tid);
-    load_kv(0, gsm);
-    cp_async_wait_all();
-    __syncthreads();
-    uint32_t qa[D / 16][4], ga[kGMaxKs][4];
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) lda(s1 + 16 * warp * kRow, kRow, 16 * kk, lane, qa[kk]);
-#pragma unroll
-    for (int ks = 0; ks < kGMaxKs; ++ks)
-        if (ks < nks) lda(s1 + kGT * kRow + 16 * warp * gRow, gRow, 16 * ks, lane, ga[ks]);
-    __syncthreads();   // stage 1 is free
-
-    float o[D / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.f, 0.f};
-    const int rbase = q0 + 16 * warp + (lane >> 2);
-    const int ntiles = qt + 1;
-    for (int kt = 0; kt < ntiles; ++kt) {
-        uint8_t *st = gsm + (kt & 1) * stageB;
-        if (kt + 1 < ntiles) load_kv(kt + 1, gsm + ((kt + 1) & 1) * stageB);
-        const uint8_t *Kt = st, *Vt = st + kGT * kRow, *Gt = st + 2 * kGT * kRow;
-        float s[8][4], ag[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[nt][e] = ag[nt][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bb[4];
-                ldb_nk(Kt + 16 * np * kRow, kRow, 16 * kk, lane, bb);
-                mma_bf16(s[2 * np], qa[kk], bb[0], bb[1]);
-                mma_bf16(s[2 * np + 1], qa[kk], bb[2], bb[3]);
-            }
-        const int k0 = kt * kGT;
-        const bool all_local = tile_all_local(q0, k0, a.window);
-        const bool any_local = tile_any_local(q0, k0, a.window);
-        const bool masked = kt == qt || k0 + kGT > a.n;   // the diagonal and the ragged end
-        if (!all_local)
-#pragma unroll
-            for (int ks = 0; ks < kGMaxKs; ++ks)
-                if (ks < nks)
-#pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        uint32_t bb[4];
-                        ldb_nk(Gt + 16 * np * gRow, gRow, 16 * ks, lane, bb);
-                        mma_f16(ag[2 * np], ga[ks], bb[0], bb[1]);
-                        mma_f16(ag[2 * np + 1], ga[ks], bb[2], bb[3]);
-                    }
-        // logits in base 2 with the gate; causal and length masks
-        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = rbase + ((e >> 1) << 3);
-                const int j = k0 + 8 * nt + 2 * (lane & 3) + (e & 1);
-                float g = 1.f;
-                if (!all_local) {
-                    g = sigmoidf_(a.lambda * ag[nt][e]);
-                    if (any_local && i - j < a.window) g = 1.f;
-                }
-                float x = s[nt][e] * scale2 * g;
-                if (masked) x = (j <= i && j < a.n) ? x : -CUDART_INF_F;
-                s[nt][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-        float alpha[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float mnew = fmaxf(mrow[r], mx[r]);   // finite: key 0 is allowed
-            alpha[r] = exp2f(mrow[r] - mnew);
-            mrow[r] = mnew;
-            lrow[r] *= alpha[r];
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                s[nt][e] = exp2f(s[nt][e] - mrow[e >> 1]);
-                lrow[e >> 1] += s[nt][e];
-            }
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-        }
-        // O += P V
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]),
-                                    pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
-                                    pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                    pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                uint32_t bb[4];
-                ldb_kn(Vt + 16 * kk * kRow, kRow, 16 * dp, lane, bb);
-                mma_bf16(o[2 * dp], pa, bb[0], bb[1]);
-                mma_bf16(o[2 * dp + 1], pa, bb[2], bb[3]);
-            }
-        }
-        cp_async_wait_all();
-        __syncthreads();
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int i = rbase + 8 * r;
-        if (i >= a.n) continue;
-        const float inv = 1.f / lrow[r];
-        __nv_bfloat16 *orow = a.out + (((int64_t)b * a.n + i) * a.Hq + h) * D;
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
-            *reinterpret_cast<__nv_bfloat162 *>(orow + 8 * nt + 2 * (lane & 3)) =
-                __floats2bfloat162_rn(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
-        if ((lane & 3) == 0)
-            a.lse_out[((int64_t)b * a.Hq + h) * a.n + i] =
-                (mrow[r] + log2f(lrow[r])) * 0.69314718055994531f;
-    }
-}
 
 // G [B, n, Kg] fp32 -> [B, n, kp] fp16 with zero columns past Kg.
 __global__ void gated_g16_kernel(const float *__restrict__ G, int64_t rows, int Kg, int kp,
@@ -803,10 +635,9 @@ namespace {
 template <int D>
 cudaError_t gated_preflight_d(int kp)
 {
-    const int fwd = 2 * GatedSmem<D>::stage(kp), bwd = GatedBwdSmem<D>::bytes(kp);
+    const int bwd = GatedBwdSmem<D>::bytes(kp);
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    cudaError_t e = cudaFuncSetAttribute(gated_fwd_kernel<D>, at, fwd);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_q_kernel<D>, at, bwd);
+    cudaError_t e = cudaFuncSetAttribute(gated_bwd_q_kernel<D>, at, bwd);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(gated_bwd_k_kernel<D>, at, bwd);
     return e;
 }
@@ -860,19 +691,6 @@ cudaError_t launch_g16(const GatedLaunch &p, const GatedArgs &a, cudaStream_t s)
 }
 
 template <int D>
-cudaError_t gated_fwd_t(const GatedLaunch &p, const GatedArgs &a, cudaStream_t s, int *launches)
-{
-    const int nqt = (p.n + kGT - 1) / kGT;
-    prof_begin("gated_fwd", s);
-    const cudaError_t e = launch_pdl(gated_fwd_kernel<D>, dim3((unsigned)nqt, (unsigned)p.Hq,
-                                     (unsigned)p.B), dim3(kGThreads),
-                                     (size_t)2 * GatedSmem<D>::stage(a.kp), s, a);
-    prof_end(s);
-    *launches += 1;
-    return e;
-}
-
-template <int D>
 cudaError_t gated_bwd_t(const GatedLaunch &p, GatedArgs a, cudaStream_t s, int *launches)
 {
     const int nqt = (p.n + kGT - 1) / kGT;
@@ -919,10 +737,12 @@ cudaError_t gated_preflight(int d, int Kg)
 cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches)
 {
     const GatedArgs a = gated_args(p, ws);
-    cudaError_t e = launch_g16(p, a, s);
+    GatedTcPlan plan;
+    cudaError_t e = gated_tc_prepare(p, a.g, a.kp, &plan);   // enqueues nothing
     if (e != cudaSuccess) return e;
+    if ((e = launch_g16(p, a, s)) != cudaSuccess) return e;
     *launches += 1;
-    return p.d == 64 ? gated_fwd_t<64>(p, a, s, launches) : gated_fwd_t<128>(p, a, s, launches);
+    return gated_tc_launch(plan, s, launches);
 }
 
 cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches)

@@ -78,6 +78,10 @@ cudaError_t launch_assign(const AssignLaunch &p, cudaStream_t s, int *launches);
 // {box_inner, box_outer}, 128-byte swizzle.
 bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
                  uint32_t box_inner, uint32_t box_outer, bool f16);
+// 4-D bf16 (or fp16) tensor map of a [B, rows, H, d] tensor (d contiguous),
+// boxes of 64 x 1 x box_rows x 1, 128-byte swizzle; reads past an edge give 0.
+bool make_map_4d(CUtensorMap *m, const void *base, bool f16, int B, int64_t rows, int H, int d,
+                 uint32_t box_rows);
 
 // A prepared assignment: the path, its TMA maps and launch sizes.
 // assign_prepare validates nothing that focus_assign's host checks cover, and
@@ -181,8 +185,20 @@ struct GatedLaunch {
     float *lse_out, *dq, *dk, *dv, *dg, *dlam;
     int B, n, Hq, Hkv, d, Kg, window;
     float scale, lambda;
+    WaitCtl wc;   // the forward kernel's bounded waits
 };
 size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg);
+// The tensor-core forward (focus_gated_tc.cu): its launch attributes and TMA
+// maps (gated_tc_prepare enqueues nothing), then the launch.  g16 is the
+// fp16 copy of G, [B, n, kp] with kp = K_g rounded up to 16.
+struct GatedTcPlan {
+    CUtensorMap map[5];   // Q, K, V, Gq (128-row boxes), Gk (64-row boxes)
+    GatedLaunch p;
+    int kp, pair_heads, grid;
+};
+cudaError_t gated_tc_preflight(int d, int Kg);
+cudaError_t gated_tc_prepare(const GatedLaunch &p, const __half *g16, int kp, GatedTcPlan *plan);
+cudaError_t gated_tc_launch(const GatedTcPlan &plan, cudaStream_t s, int *launches);
 cudaError_t gated_preflight(int d, int Kg);
 cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
 cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);

@@ -81,7 +81,7 @@ def _load():
             lib.oracle_sinkhorn.argtypes = [vp, i32, i32, i32, ctypes.c_double, i32, vp, vp, vp]
             f64 = ctypes.c_double
             lib.oracle_gated_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f64, f64, vp, vp]
-            lib.oracle_gated_bwd.argtypes = [vp] * 5 + [i32] * 7 + [f64, f64] + [vp] * 5
+            lib.oracle_gated_bwd.argtypes = [vp] * 5 + [i32] * 7 + [f64, f64] + [vp] * 6
             for f in (lib.oracle_assign, lib.oracle_bucket, lib.oracle_attention,
                       lib.oracle_count_pairs, lib.oracle_num_threads, lib.oracle_sinkhorn,
                       lib.oracle_gated_fwd, lib.oracle_gated_bwd):
@@ -241,9 +241,10 @@ def gated_fwd(Q_bits, K_bits, V_bits, G, window, lam, scale=0.0):
     return O, L
 
 
-def gated_bwd(Q_bits, K_bits, V_bits, G, dO, window, lam, scale=0.0):
+def gated_bwd(Q_bits, K_bits, V_bits, G, dO, window, lam, scale=0.0, with_abs=False):
     """Gradients of sum(O * dO) for the soft-gated attention -> (dQ, dK, dV,
-    dG, dlambda), float64."""
+    dG, dlambda), float64; with_abs appends the sum of the magnitudes of
+    dlambda's per-pair terms."""
     Q, K, V, G, B, n, Hq, Hkv, d, Kg = _gated_shapes(Q_bits, K_bits, V_bits, G)
     dO = np.ascontiguousarray(dO, dtype=np.float32)
     dQ = np.empty((B, n, Hq, d), np.float64)
@@ -251,9 +252,13 @@ def gated_bwd(Q_bits, K_bits, V_bits, G, dO, window, lam, scale=0.0):
     dV = np.empty((B, n, Hkv, d), np.float64)
     dG = np.empty((B, n, Kg), np.float64)
     dl = ctypes.c_double(0.0)
+    dl_abs = ctypes.c_double(0.0)
     rc = _load().oracle_gated_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), _ptr(dO), B, n, Hq, Hkv,
                                   d, Kg, int(window), float(lam), float(scale), _ptr(dQ),
-                                  _ptr(dK), _ptr(dV), _ptr(dG), ctypes.byref(dl))
+                                  _ptr(dK), _ptr(dV), _ptr(dG), ctypes.byref(dl),
+                                  ctypes.byref(dl_abs))
     if rc:
         raise ValueError("oracle_gated_bwd: invalid arguments")
+    if with_abs:
+        return dQ, dK, dV, dG, float(dl.value), float(dl_abs.value)
     return dQ, dK, dV, dG, float(dl.value)

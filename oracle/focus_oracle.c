@@ -362,7 +362,9 @@ int oracle_sinkhorn(const float *S, int B, int n, int K, double tau, int iters,
  *   O [B, n, Hq, d] double out; LSE [B, Hq, n] double out (natural log)
  * oracle_gated_bwd takes dO [B, n, Hq, d] float and returns the gradients
  * of sum(O * dO): dQ [B, n, Hq, d], dK and dV [B, n, Hkv, d], dG [B, n, Kg]
- * (all double, overwritten) and d lambda.
+ * (all double, overwritten) and d lambda; dlambda_abs (nullable) receives
+ * the sum of the magnitudes of d lambda's per-pair terms, the scale against
+ * which a rounded evaluation of that (often cancelling) sum is judged.
  */
 static double gated_score(const uint16_t *q, const uint16_t *k, const float *gi,
                           const float *gj, int d, int Kg, double sc, double lambda, int local,
@@ -424,7 +426,7 @@ int oracle_gated_fwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, c
 int oracle_gated_bwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, const float *G,
                      const float *dO, int B, int n, int Hq, int Hkv, int d, int Kg, int window,
                      double lambda, double scale, double *dQ, double *dK, double *dV,
-                     double *dG, double *dlambda)
+                     double *dG, double *dlambda, double *dlambda_abs)
 {
     if (!Q || !Kt || !V || !G || !dO || !dQ || !dK || !dV || !dG || !dlambda || B < 1 ||
         n < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || Kg < 1 || window < 0)
@@ -435,7 +437,7 @@ int oracle_gated_bwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, c
     memset(dK, 0, sizeof(double) * (size_t)B * n * Hkv * d);
     memset(dV, 0, sizeof(double) * (size_t)B * n * Hkv * d);
     memset(dG, 0, sizeof(double) * (size_t)B * n * Kg);
-    double dl = 0.0;
+    double dl = 0.0, dl_abs = 0.0;
     double *s = (double *)malloc(sizeof(double) * (size_t)n);
     double *t = (double *)malloc(sizeof(double) * (size_t)n);
     double *a = (double *)malloc(sizeof(double) * (size_t)n);
@@ -484,6 +486,7 @@ int oracle_gated_bwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, c
                         const double sp = gate[j] * (1.0 - gate[j]);   /* sigma' */
                         const double da = dgate * lambda * sp;
                         dl += dgate * a[j] * sp;
+                        dl_abs += fabs(dgate * a[j] * sp);
                         const float *gj = G + ((size_t)b * n + j) * Kg;
                         double *dgi = dG + ((size_t)b * n + i) * Kg;
                         double *dgj = dG + ((size_t)b * n + j) * Kg;
@@ -501,6 +504,7 @@ int oracle_gated_bwd(const uint16_t *Q, const uint16_t *Kt, const uint16_t *V, c
     free(gate);
     free(dp);
     *dlambda = dl;
+    if (dlambda_abs) *dlambda_abs = dl_abs;
     return 0;
 }
 
