@@ -462,7 +462,7 @@ def bench_gated(fg, torch, flush, stream, peaks, args):
             "bwd_tflops": bf / (bms * 1e-3) / 1e12, "bound": "tensor", "peak": peak,
             "fwd_frac": ff / (fms * 1e-3) / 1e12 / peak,
             "bwd_frac": bf / (bms * 1e-3) / 1e12 / peak, "reps": reps,
-            "what": "training forward (tcgen05) and backward (mma.sync tiles) over every causal pair, "
+            "what": "training forward and backward (tcgen05) over every causal pair, "
                     "L2 flushed before each call"}
 
 

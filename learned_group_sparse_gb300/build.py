@@ -20,7 +20,8 @@ LIB = os.path.join(OUT_DIR, "libfocus_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Translation units whose arithmetic is exp2 / log2 / reciprocal-heavy use
 # the fast hardware approximations; the assignment keeps IEEE fp32.
-FAST_MATH = {"focus_attn_group.cu", "focus_attn_window.cu", "focus_gated_tc.cu", "focus_merge.cu"}
+FAST_MATH = {"focus_attn_group.cu", "focus_attn_window.cu", "focus_gated_bwd_tc.cu",
+             "focus_gated_tc.cu", "focus_merge.cu"}
 
 
 def _nvcc() -> str:

@@ -793,8 +793,8 @@ focus_status_t focus_gated_attention_bwd(const void *Q, const void *K, const voi
     if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
         !aligned16(dV) || !aligned16(dG) || ((uintptr_t)dlambda & 3u))
         return FOCUS_ERR_INVALID_ARG;
-    if (gated_preflight(d, Kg) != cudaSuccess) return FOCUS_ERR_CUDA;
     GatedLaunch p{};
+    if (wait_ctl(&p.wc) != cudaSuccess) return FOCUS_ERR_CUDA;
     p.q = static_cast<const __nv_bfloat16 *>(Q);
     p.k = static_cast<const __nv_bfloat16 *>(K);
     p.v = static_cast<const __nv_bfloat16 *>(V);

@@ -1,0 +1,824 @@
+// Backward of soft-gated training attention on the 5th-generation tensor
+// cores (Focus, gist.science/zh technical summary 2.1.2 "gated attention":
+// s_ij = q_i . k_j * scale * gate_ij, gate_ij = 1 inside the local window
+// (i - j < w) and sigma(lambda g_i . g_j) elsewhere, causal softmax over
+// every pair while training).
+//
+// With dP_ij = dO_i . v_j, D_i = dO_i . O_i and dS_ij = P_ij (dP_ij - D_i):
+//   dT_ij = dS_ij scale gate_ij:   dQ_i = sum_j dT_ij k_j,   dK_j = sum_i dT_ij q_i
+//   dV_j = sum_i P_ij dO_i
+//   for a gated pair, with t_ij = scale q_i . k_j and a_ij = g_i . g_j:
+//   da_ij = dS_ij t_ij lambda sigma (1 - sigma):   dG_i gets sum_j da_ij g_j + sum_j da_ji g_j
+//   d lambda = sum over gated pairs of dS_ij t_ij a_ij sigma (1 - sigma)
+// Two kernels, one per side, each recomputing P from the forward's
+// log-sum-exp, so that every sum is owned by one CTA (no atomics, a fixed
+// order, bit-identical repeats):
+//   query side (CTA: 128 queries x a chunk of 4 heads): dQ per head, the
+//     chunk's sum_j da_ij g_j (one partial per chunk) and d lambda;
+//   key side (CTA: 128 keys x a kv head, over its query heads): dK, dV and
+//     sum_i da_ij g_i (one partial per kv head).
+// A CTA's own rows are the TMEM lanes; it streams the other side's tiles.
+// Per tile one thread issues three products into TMEM,
+//   S = R1 C1^T (q . k, bf16),  A = RG CG^T (g . g, fp16; skipped when every
+//   pair of the tile is local),  dP = R2 C2^T (dO . v, bf16)
+// with R1, R2, RG the CTA's Q, dO, G_q (query side) or K, V, G_k (key side)
+// and C1, C2, CG the streamed tile's K, V, G_k or Q, dO, G_q.  Two
+// warpgroups, one per half of the tile's columns (a thread per row), read
+// them with one TMEM load, release S for the next tile's products, and write
+// P, dT and da as bf16 / fp16 operand tiles (128-byte-swizzled rows) into
+// shared memory; the thread then issues the gradient products into TMEM
+// accumulators:
+//   query side: dQ += dT C1,  dG_q += da CG
+//   key side:   dV += P^T C2,  dK += dT^T C1,  dG_k += da^T CG
+// The streamed tiles serve K-major (as the B operand of S, A, dP) and
+// MN-major (as the B operand of the gradient products).  Every wait is
+// bounded; a CTA that gives up drains its copies and MMAs before it releases
+// shared memory and TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "focus_internal.h"
+#include "focus_ptx.cuh"
+
+namespace focus {
+
+namespace {
+
+enum { kSideQ = 0, kSideK = 1 };
+constexpr int kBR = 128;            // the CTA's own rows (TMEM lanes)
+constexpr int kBwThreads = 384;     // 8 elementwise warps, the producer, the MMA thread, 2 idle
+constexpr int kBwProducer = 8;
+constexpr int kBwMma = 9;
+// Registers per thread after the split: elementwise warpgroups / the third
+// one.  256 * kBwRegsEw + 128 * kBwRegsOther must not exceed the launch's
+// kBwThreads * (registers per thread at launch), which the preflight checks.
+constexpr int kBwRegsEw = 216;
+constexpr int kBwRegsOther = 72;
+constexpr int kBwStages = 2;
+constexpr int kBwHeadChunk = 4;     // query heads per query-side CTA (one dG partial each)
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum {
+    W_ROWFULL = 0, W_ROWEMPTY = 1, W_CFULL = 2, W_CEMPTY = 4, W_SFULL = 6, W_SFREE = 7,
+    W_PFULL = 8, W_PEMPTY = 9, W_ACCDONE = 10, W_ACCFREE = 11, W_DRAIN = 12, kWBars = 13
+};
+
+// Shared memory and TMEM columns of one CTA.  BC: rows of a streamed tile
+// (64; 32 on the key side for d 128 with K_g > 64, where the accumulators
+// need 384 TMEM columns).
+template <int SIDE, int D, int KPC, int BC>
+struct BwLayout {
+    static constexpr uint32_t kRowT = kBR * D * 2;        // R1 or R2: D/64 chunks of 16 KB
+    static constexpr uint32_t kRowG = kBR * KPC * 128;    // RG: KPC chunks of 16 KB
+    static constexpr uint32_t kColT = BC * D * 2;         // C1 or C2: chunks of BC * 128 bytes
+    static constexpr uint32_t kColG = BC * KPC * 128;     // CG
+    static constexpr uint32_t kStage = 2 * kColT + kColG;
+    static constexpr uint32_t kOutT = kBR * 128;          // an operand tile: 128 rows of 128 bytes
+    static constexpr int kNOut = SIDE == kSideK ? 3 : 2;  // [P,] dT, da
+    static constexpr uint32_t kR1 = 0;
+    static constexpr uint32_t kR2 = kR1 + kRowT;
+    static constexpr uint32_t kRG = kR2 + kRowT;
+    static constexpr uint32_t kC = kRG + kRowG;
+    static constexpr uint32_t kOut = kC + kBwStages * kStage;
+    static constexpr uint32_t kVecB = SIDE == kSideK ? kBwStages * 2 * BC * 4 : 0;
+    static constexpr uint32_t kVec = kOut + kNOut * kOutT;  // key side: [stage][lse2 | D][BC]
+    static constexpr uint32_t kBar = kVec + kVecB;
+    static constexpr uint32_t kMisc = kBar + kWBars * 8;    // TMEM base, abort flag
+    static constexpr uint32_t kRed = kMisc + 16;            // 8 floats
+    static constexpr uint32_t kBytes = kRed + 32 + 1024;    // + alignment slack
+    // TMEM columns
+    static constexpr uint32_t kColS = 0, kColA = BC, kColP = 2 * BC, kAcc = 3 * BC;
+    static constexpr uint32_t kAccG = kAcc + (SIDE == kSideK ? 2 * D : D);
+    static_assert(kAccG + 64 * KPC <= 512, "TMEM columns");
+    static_assert(kBytes <= 232448, "shared memory per CTA");
+};
+
+struct BwArgs {
+    int B, n, Hq, Hkv, nks, Kg, window, hc, nhc, nqt;   // nqt: 128-row query tiles
+    float scale;         // softmax scale
+    float half_scale;    // scale / 2
+    float half_lambda;   // lambda / 2
+    float lambda;
+    const float *lse;    // [B, Hq, n] natural log
+    const float *Dd;     // [B, Hq, n] dO . O
+    float *dq;           // [B, n, Hq, D]
+    float *dk, *dv;      // [B, n, Hkv, D]
+    float *dg_part;      // [nhc + Hkv][B, n, Kg]
+    float *dlam_part;    // [B, nhc, nqt]
+    int *status;
+};
+
+// A streamed tile against the CTA's rows: its first column row c0; whether
+// some pair of it is gated (i - j >= w), every pair is, and whether some
+// pair has j > i.  r0 = the CTA's first row, rend = one past its last valid
+// row (query side).
+struct BwTile {
+    int c0;
+    bool gated, allg, causal;
+};
+
+template <int SIDE, int BC>
+__device__ __forceinline__ BwTile bw_tile(int v, int r0, int rend, int n, int w)
+{
+    BwTile x;
+    if (SIDE == kSideQ) {   // rows = queries [r0, rend), columns = keys [c0, c0 + 64)
+        x.c0 = 64 * v;
+        x.gated = rend - 1 - x.c0 >= w;
+        x.allg = r0 - (x.c0 + 63) >= w;
+        x.causal = x.c0 + 63 > r0;
+    } else {                // rows = keys [r0, r0 + 128), columns = queries [c0, c0 + BC)
+        x.c0 = r0 + BC * v;
+        const int ce = min(x.c0 + BC, n);
+        x.gated = ce - 1 - r0 >= w;
+        x.allg = x.c0 - (r0 + 127) >= w;
+        x.causal = r0 + 127 > x.c0;
+    }
+    return x;
+}
+
+// Instruction descriptor of kind::f16 with fp16 A (K-major) and fp16 B
+// (MN-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N)
+{
+    return idesc_f16_f32(M, N) | (1u << 16);
+}
+
+// Loads 32 consecutive fp32 columns of this thread's TMEM lane at each of
+// 3 addresses (one wait for all): v[32 * l + c] = column c at a_l.
+__device__ __forceinline__ void tmem_ld3x32(uint32_t a0, uint32_t a1, uint32_t a2, float *v)
+{
+    uint32_t r[96];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%96];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%97];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]),
+          "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]),
+          "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]),
+          "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]),
+          "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]),
+          "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 96; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The same with 16 columns at each address: v[16 * l + c].
+__device__ __forceinline__ void tmem_ld3x16(uint32_t a0, uint32_t a1, uint32_t a2, float *v)
+{
+    uint32_t r[48];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%48];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%49];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%50];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 48; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tanh with the hardware approximation (relative error about 2^-11)
+__device__ __forceinline__ float bw_tanh(float x)
+{
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+    return t;
+}
+
+// D[tmem] (+)= A[smem] B[smem] with fp16 A and B: the same instruction as
+// the bf16 form, the operand type is in the instruction descriptor.
+template <uint32_t AHI, uint32_t BHI>
+__device__ __forceinline__ void bw_mma(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    tc_mma_bf16_lo<AHI, BHI>(d_tmem, a_lo, b_lo, idesc, accumulate);
+}
+
+template <int SIDE, int D, int KPC, int BC>
+__global__ void __launch_bounds__(kBwThreads, 1)
+    gated_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1,
+                        const __grid_constant__ CUtensorMap tmR2,
+                        const __grid_constant__ CUtensorMap tmRG,
+                        const __grid_constant__ CUtensorMap tmC1,
+                        const __grid_constant__ CUtensorMap tmC2,
+                        const __grid_constant__ CUtensorMap tmCG, const BwArgs a)
+{
+    using L = BwLayout<SIDE, D, KPC, BC>;
+    constexpr int kChunks = D / 64;
+    constexpr int HC = BC / 2;          // columns per elementwise warpgroup
+    constexpr int NS = kBwStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kMisc + 4);
+    float *red = reinterpret_cast<float *>(sm + L::kRed);
+    float *vec = reinterpret_cast<float *>(sm + L::kVec);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.z;
+    const int kvq = a.Hq / a.Hkv;
+    // the CTA's rows, heads and streamed tiles
+    int r0, rend, h0, nh, ncol, kvh0;
+    if (SIDE == kSideQ) {
+        const int qt = gridDim.x - 1 - blockIdx.x;   // the longest rows first
+        r0 = kBR * qt;
+        rend = min(r0 + kBR, a.n);
+        h0 = blockIdx.y * a.hc;
+        nh = min(a.hc, a.Hq - h0);
+        ncol = (rend + 63) / 64;                    // key tiles [0, rend)
+        kvh0 = 0;
+    } else {
+        r0 = kBR * blockIdx.x;
+        rend = min(r0 + kBR, a.n);
+        kvh0 = blockIdx.y;
+        h0 = kvh0 * kvq;
+        nh = kvq;
+        ncol = (a.n - r0 + BC - 1) / BC;            // query tiles [r0, n)
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[W_ROWFULL], 1);
+        mbar_init(&bars[W_ROWEMPTY], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[W_CFULL + s], 1);
+            mbar_init(&bars[W_CEMPTY + s], 1);
+        }
+        mbar_init(&bars[W_SFULL], 1);
+        mbar_init(&bars[W_SFREE], 8);
+        mbar_init(&bars[W_PFULL], 8);
+        mbar_init(&bars[W_PEMPTY], 1);
+        mbar_init(&bars[W_ACCDONE], 1);
+        mbar_init(&bars[W_ACCFREE], 8);
+        mbar_init(&bars[W_DRAIN], 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == kBwMma) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == kBwProducer && lane == 0) {
+        tma_prefetch_desc(&tmR1);
+        tma_prefetch_desc(&tmR2);
+        tma_prefetch_desc(&tmRG);
+        tma_prefetch_desc(&tmC1);
+        tma_prefetch_desc(&tmC2);
+        tma_prefetch_desc(&tmCG);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // (set-up above touches no global memory; launched with launch_pdl)
+    grid_dep_sync();
+
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwRegsOther));
+        if (warp == kBwProducer) {
+            // --------------------------------------------------------- producer
+            int t = 0;
+            int nrow = 0;   // row-operand loads issued
+            bool ok = true;
+            for (int hi = 0; ok && hi < nh; ++hi) {
+                const int h = h0 + hi;
+                if (SIDE == kSideQ || hi == 0) {
+                    if (hi > 0 && lane == 0)
+                        ok = mbar_wait(&bars[W_ROWEMPTY], (hi - 1) & 1, abort_flag, a.status);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        uint8_t *d1 = sm + L::kR1, *d2 = sm + L::kR2, *dg = sm + L::kRG;
+                        const uint32_t bytes = 2 * L::kRowT + (hi == 0 ? L::kRowG : 0u);
+                        mbar_arrive_expect_tx(&bars[W_ROWFULL], bytes);
+                        const int rh = SIDE == kSideQ ? h : kvh0;   // head of R1 / R2
+                        for (int c = 0; c < kChunks; ++c) {
+                            tma_load_4d(d1 + c * 16384, &tmR1, &bars[W_ROWFULL], c * 64, rh, r0, b);
+                            tma_load_4d(d2 + c * 16384, &tmR2, &bars[W_ROWFULL], c * 64, rh, r0, b);
+                        }
+                        if (hi == 0)
+                            for (int c = 0; c < KPC; ++c)
+                                tma_load_4d(dg + c * 16384, &tmRG, &bars[W_ROWFULL], c * 64, 0,
+                                            r0, b);
+                    }
+                    ++nrow;
+                }
+                for (int v = 0; ok && v < ncol; ++v, ++t) {
+                    const int st = t % NS;
+                    if (t >= NS && lane == 0)
+                        ok = mbar_wait(&bars[W_CEMPTY + st], ((t / NS) - 1) & 1, abort_flag,
+                                       a.status);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const int c0 = SIDE == kSideQ ? 64 * v : r0 + BC * v;
+                    if (SIDE == kSideK) {
+                        // the tile's queries: base-2 log-sum-exp (+inf past n: P = 0) and D
+                        float *vl = vec + st * 2 * BC;
+                        for (int c = lane; c < BC; c += 32) {
+                            const int i = c0 + c;
+                            const int64_t x = ((int64_t)b * a.Hq + h) * a.n + i;
+                            vl[c] = i < a.n ? a.lse[x] * kLog2e : CUDART_INF_F;
+                            vl[BC + c] = i < a.n ? a.Dd[x] : 0.f;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        uint8_t *sc = sm + L::kC + st * L::kStage;
+                        mbar_arrive_expect_tx(&bars[W_CFULL + st], L::kStage);
+                        const int ch = SIDE == kSideQ ? h / kvq : h;   // head of C1 / C2
+                        for (int c = 0; c < kChunks; ++c) {
+                            tma_load_4d(sc + c * (BC * 128), &tmC1, &bars[W_CFULL + st], c * 64,
+                                        ch, c0, b);
+                            tma_load_4d(sc + L::kColT + c * (BC * 128), &tmC2, &bars[W_CFULL + st],
+                                        c * 64, ch, c0, b);
+                        }
+                        for (int c = 0; c < KPC; ++c)
+                            tma_load_4d(sc + 2 * L::kColT + c * (BC * 128), &tmCG,
+                                        &bars[W_CFULL + st], c * 64, 0, c0, b);
+                    }
+                    __syncwarp();
+                }
+            }
+            // A CTA that gave up lets the copies already issued land before
+            // shared memory is released.
+            if (*abort_flag && lane == 0) {
+                const uint64_t t0 = global_timer_ns();
+                if (nrow > 0)
+                    while (!mbar_try_wait(&bars[W_ROWFULL], (nrow - 1) & 1) &&
+                           global_timer_ns() - t0 < 100000000ull) {
+                    }
+                for (int tt = max(0, t - NS); tt <= t; ++tt)
+                    while (!mbar_try_wait(&bars[W_CFULL + tt % NS], (tt / NS) & 1) &&
+                           global_timer_ns() - t0 < 300000000ull) {
+                    }
+            }
+        } else if (warp == kBwMma) {
+            // ----------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t kIdS = idesc_bf16_f32(kBR, BC, false, false);
+                constexpr uint32_t kIdA = idesc_f16_f32(kBR, BC);
+                constexpr uint32_t kIdAcc = idesc_bf16_f32(kBR, D, false, true);
+                constexpr uint32_t kIdG = idesc_f16_f32_bmn(kBR, 64 * KPC);
+                constexpr uint32_t kHi = sdesc_hi(1024);
+                const uint32_t r1 = sdesc_lo(smem_u32(sm + L::kR1), 16);
+                const uint32_t r2 = sdesc_lo(smem_u32(sm + L::kR2), 16);
+                const uint32_t rg = sdesc_lo(smem_u32(sm + L::kRG), 16);
+                // streamed tiles: the leading offset is the MN-major chunk stride
+                // (unused by the K-major products)
+                const uint32_t cb = sdesc_lo(smem_u32(sm + L::kC), BC * 128);
+                const uint32_t ob = sdesc_lo(smem_u32(sm + L::kOut), 16);
+                const uint32_t outP = ob, outT = ob + (SIDE == kSideK ? (L::kOutT >> 4) : 0u);
+                const uint32_t outA = outT + (L::kOutT >> 4);
+                int t = 0;
+                bool ok = true, dg_started = false;
+                int pt = -1, p_hi = 0;                 // the tile whose gradient products are next
+                bool p_gated = false, p_first = false, p_last = false;
+                auto grads = [&](int tt, bool gtd, bool first, bool last, int hi) -> bool {
+                    if (!mbar_wait(&bars[W_PFULL], tt & 1, abort_flag, a.status)) return false;
+                    if (SIDE == kSideQ && first && hi > 0 &&
+                        !mbar_wait(&bars[W_ACCFREE], (hi - 1) & 1, abort_flag, a.status))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t c1 = cb + (tt % NS) * (L::kStage >> 4);
+                    const uint32_t c2 = c1 + (L::kColT >> 4), cg = c2 + (L::kColT >> 4);
+    #pragma unroll
+                    for (int kk = 0; kk < BC / 16; ++kk) {
+                        // A: 32 bytes further along the rows; B: 16 rows of 128 bytes further
+                        const uint32_t ao = kk * 2, bo = kk * 128;
+                        if (SIDE == kSideQ) {
+                            const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
+                            bw_mma<kHi, kHi>(tmem + L::kAcc, outT + ao, c1 + bo, kIdAcc, acc);
+                        } else {
+                            const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
+                            bw_mma<kHi, kHi>(tmem + L::kAcc, outP + ao, c2 + bo, kIdAcc, acc);
+                            bw_mma<kHi, kHi>(tmem + L::kAcc + D, outT + ao, c1 + bo, kIdAcc, acc);
+                        }
+                    }
+                    if (gtd) {
+    #pragma unroll
+                        for (int kk = 0; kk < BC / 16; ++kk)
+                            bw_mma<kHi, kHi>(tmem + L::kAccG, outA + kk * 2, cg + kk * 128, kIdG,
+                                             (kk > 0 || dg_started) ? 1u : 0u);
+                        dg_started = true;
+                    }
+                    tc_commit(&bars[W_PEMPTY]);
+                    tc_commit(&bars[W_CEMPTY + tt % NS]);
+                    if (SIDE == kSideQ && last) tc_commit(&bars[W_ACCDONE]);
+                    return true;
+                };
+                for (int hi = 0; ok && hi < nh; ++hi) {
+                    if (SIDE == kSideQ || hi == 0) {
+                        ok = mbar_wait(&bars[W_ROWFULL], hi & 1, abort_flag, a.status);
+                        if (!ok) break;
+                    }
+                    for (int v = 0; ok && v < ncol; ++v, ++t) {
+                        const BwTile x = bw_tile<SIDE, BC>(v, r0, rend, a.n, a.window);
+                        const int st = t % NS;
+                        ok = mbar_wait(&bars[W_CFULL + st], (t / NS) & 1, abort_flag, a.status);
+                        if (ok && t > 0)
+                            ok = mbar_wait(&bars[W_SFREE], (t - 1) & 1, abort_flag, a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t c1 = cb + st * (L::kStage >> 4);
+                        const uint32_t c2 = c1 + (L::kColT >> 4), cg = c2 + (L::kColT >> 4);
+    #pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t ro = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                            const uint32_t co = ((kk >> 2) * (BC * 128) + (kk & 3) * 32) >> 4;
+                            const uint32_t acc = kk > 0 ? 1u : 0u;
+                            bw_mma<kHi, kHi>(tmem + L::kColS, r1 + ro, c1 + co, kIdS, acc);
+                            bw_mma<kHi, kHi>(tmem + L::kColP, r2 + ro, c2 + co, kIdS, acc);
+                        }
+                        if (x.gated) {
+    #pragma unroll
+                            for (int ks = 0; ks < 4 * KPC; ++ks) {
+                                if (ks >= a.nks) break;
+                                const uint32_t ro = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                                const uint32_t co = ((ks >> 2) * (BC * 128) + (ks & 3) * 32) >> 4;
+                                bw_mma<kHi, kHi>(tmem + L::kColA, rg + ro, cg + co, kIdA,
+                                                 ks > 0 ? 1u : 0u);
+                            }
+                        }
+                        tc_commit(&bars[W_SFULL]);
+                        if (SIDE == kSideQ && v == ncol - 1) tc_commit(&bars[W_ROWEMPTY]);
+                        if (pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
+                        pt = t;
+                        p_gated = x.gated;
+                        p_first = v == 0;
+                        p_last = v == ncol - 1;
+                        p_hi = hi;
+                    }
+                }
+                if (ok && pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
+                if (ok && SIDE == kSideK) tc_commit(&bars[W_ACCDONE]);
+                // every MMA issued completes before TMEM is released
+                tc_commit(&bars[W_DRAIN]);
+                mbar_wait_until(&bars[W_DRAIN], 0, global_timer_ns() + 500000000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwRegsEw));
+        // ------------------------------------- elementwise (warps 0-7)
+        const int wg = warp >> 2;                 // half of the tile's columns
+        const int r = (warp & 3) * 32 + lane;     // own row = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int row = r0 + r;                   // query (query side) or key (key side)
+        const float scale2 = a.scale * kLog2e, half_scale2 = a.half_scale * kLog2e;
+        float dlam = 0.f;
+        bool ok = true;
+        int t = 0;
+        uint8_t *outb = sm + L::kOut;
+        uint8_t *oP = outb, *oT = outb + (SIDE == kSideK ? L::kOutT : 0u), *oA = oT + L::kOutT;
+        for (int hi = 0; ok && hi < nh; ++hi) {
+            const int h = h0 + hi;
+            float lse2_r = CUDART_INF_F, D_r = 0.f;   // query side: this row's
+            if (SIDE == kSideQ && row < a.n) {
+                const int64_t x = ((int64_t)b * a.Hq + h) * a.n + row;
+                lse2_r = a.lse[x] * kLog2e;
+                D_r = a.Dd[x];
+            }
+            for (int v = 0; ok && v < ncol; ++v, ++t) {
+                const BwTile x = bw_tile<SIDE, BC>(v, r0, rend, a.n, a.window);
+                ok = mbar_wait(&bars[W_SFULL], t & 1, abort_flag, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                float f[3 * HC];   // S, A, dP of this row's HC columns
+                const uint32_t cc = wg * HC;
+                if constexpr (HC == 32)
+                    tmem_ld3x32(trow + L::kColS + cc, trow + L::kColA + cc, trow + L::kColP + cc,
+                                f);
+                else
+                    tmem_ld3x16(trow + L::kColS + cc, trow + L::kColA + cc, trow + L::kColP + cc,
+                                f);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[W_SFREE]);   // S, A, dP may be overwritten
+                const float *vl = vec + (t % NS) * 2 * BC + wg * HC;   // key side
+                uint32_t pkP[HC / 2], pkT[HC / 2], pkA[HC / 2];
+#pragma unroll
+                for (int e = 0; e < HC; e += 2) {
+                    float p2[2], t2[2], a2[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int c = wg * HC + e + k;
+                        const int i = SIDE == kSideQ ? row : x.c0 + c;   // query
+                        const int j = SIDE == kSideQ ? x.c0 + c : row;   // key
+                        const float s = f[e + k], av = f[HC + e + k], dp = f[2 * HC + e + k];
+                        const float lse2 = SIDE == kSideQ ? lse2_r : vl[e + k];
+                        const float Dv = SIDE == kSideQ ? D_r : vl[BC + e + k];
+                        // gate of the pair: g2 = scale log2(e) gate, g1 = scale gate
+                        float g2 = scale2, g1 = a.scale, sp = 0.f;
+                        bool gp = false;
+                        if (x.gated) {
+                            gp = x.allg || (i - j >= a.window);
+                            if (gp) {
+                                const float th = bw_tanh(a.half_lambda * av);
+                                g2 = fmaf(half_scale2, th, half_scale2);
+                                g1 = fmaf(a.half_scale, th, a.half_scale);
+                                sp = fmaf(-0.25f * th, th, 0.25f);   // sigma (1 - sigma)
+                            }
+                        }
+                        float p = exp2f(s * g2 - lse2);
+                        if (x.causal && j > i) p = 0.f;
+                        const float ds = p * (dp - Dv);
+                        float da = 0.f;
+                        if (gp) {
+                            const float dgate = ds * s * a.scale;
+                            da = dgate * a.lambda * sp;
+                            if (SIDE == kSideQ) dlam = fmaf(dgate * sp, av, dlam);
+                        }
+                        p2[k] = p;
+                        t2[k] = ds * g1;
+                        a2[k] = da;
+                    }
+                    pkP[e / 2] = pack_bf16x2(p2[0], p2[1]);
+                    pkT[e / 2] = pack_bf16x2(t2[0], t2[1]);
+                    pkA[e / 2] = pack_f16x2(a2[0], a2[1]);
+                }
+                // the operand tiles are free once the previous tile's gradient
+                // products are done
+                if (t > 0) ok = mbar_wait(&bars[W_PEMPTY], (t - 1) & 1, abort_flag, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                // row r, columns [wg HC, wg HC + HC): 16-byte units u of the
+                // 128-byte row at (u xor (r mod 8))
+                const uint32_t rowoff = (uint32_t)r * 128u;
+#pragma unroll
+                for (int q = 0; q < HC / 8; ++q) {
+                    const uint32_t u = (uint32_t)(wg * (HC / 8) + q);
+                    const uint32_t off = rowoff + ((u ^ (uint32_t)(r & 7)) << 4);
+                    if (SIDE == kSideK)
+                        st_shared_v4(smem_u32(oP + off), pkP[4 * q], pkP[4 * q + 1], pkP[4 * q + 2],
+                                     pkP[4 * q + 3]);
+                    st_shared_v4(smem_u32(oT + off), pkT[4 * q], pkT[4 * q + 1], pkT[4 * q + 2],
+                                 pkT[4 * q + 3]);
+                    st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1], pkA[4 * q + 2],
+                                 pkA[4 * q + 3]);
+                }
+                fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[W_PFULL]);
+                if (SIDE == kSideQ && v == ncol - 1) {
+                    // dQ of head h is complete: this row's half of its columns
+                    ok = mbar_wait(&bars[W_ACCDONE], hi & 1, abort_flag, a.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    float *dst = a.dq + (((int64_t)b * a.n + row) * a.Hq + h) * D + wg * (D / 2);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[32];
+                        tmem_ld32(trow + L::kAcc + wg * (D / 2) + 32 * c, o);
+                        if (row < a.n)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                reinterpret_cast<float4 *>(dst + 32 * c)[q] =
+                                    make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[W_ACCFREE]);
+                }
+            }
+        }
+        // ---- the CTA's accumulators
+        if (ok && SIDE == kSideK) {
+            ok = mbar_wait(&bars[W_ACCDONE], 0, abort_flag, a.status);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const bool valid = row < a.n;
+            if (SIDE == kSideK) {
+                // dV and dK: this row's half of the D columns of each
+                const int64_t base = (((int64_t)b * a.n + row) * a.Hkv + kvh0) * D + wg * (D / 2);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    float *dst = (m == 0 ? a.dv : a.dk) + base;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[32];
+                        tmem_ld32(trow + L::kAcc + m * D + wg * (D / 2) + 32 * c, o);
+                        if (valid)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                reinterpret_cast<float4 *>(dst + 32 * c)[q] = make_float4(
+                                    o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                }
+            }
+            // the dG partial: this row's half of the 64 KPC columns (zero when
+            // no pair of the CTA is gated)
+            const bool any_gated = SIDE == kSideQ ? (rend - 1 >= a.window)
+                                                  : (a.n - 1 - r0 >= a.window);
+            const int part = SIDE == kSideQ ? blockIdx.y : a.nhc + kvh0;
+            float *dst = a.dg_part + ((int64_t)part * a.B * a.n + (int64_t)b * a.n + row) * a.Kg;
+#pragma unroll
+            for (int c = 0; c < KPC; ++c) {
+                float o[32];
+                if (any_gated) {
+                    tmem_ld32(trow + L::kAccG + wg * 32 * KPC + 32 * c, o);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) o[q] = 0.f;
+                }
+                const int col0 = wg * 32 * KPC + 32 * c;
+                if (valid)
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (col0 + q < a.Kg) dst[col0 + q] = o[q];
+            }
+        }
+        if (SIDE == kSideQ) {
+            // d lambda: this CTA's partial, the EW warps' sums in a fixed order
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
+            if (lane == 0) red[warp] = dlam;
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 0 && !*abort_flag) {
+                float s = 0.f;
+                for (int w = 0; w < 8; ++w) s += red[w];
+                const int qt = gridDim.x - 1 - blockIdx.x;
+                a.dlam_part[((int64_t)b * a.nhc + blockIdx.y) * a.nqt + qt] = s;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int SIDE, int D, int KPC, int BC>
+cudaError_t bw_preflight_t()
+{
+    auto kern = gated_bwd_tc_kernel<SIDE, D, KPC, BC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)BwLayout<SIDE, D, KPC, BC>::kBytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    // the warpgroups' shares after setmaxnreg must fit in the launch's registers
+    if ((int64_t)fa.numRegs * kBwThreads < 256 * kBwRegsEw + 128 * kBwRegsOther)
+        return cudaErrorInvalidConfiguration;
+    return cudaSuccess;
+}
+
+template <int SIDE, int D, int KPC, int BC>
+cudaError_t bw_launch_t(const GatedBwTcPlan &plan, const BwArgs &a, cudaStream_t s)
+{
+    const int m = SIDE == kSideQ ? 0 : 6;
+    const dim3 grid = SIDE == kSideQ ? dim3((unsigned)a.nqt, (unsigned)a.nhc, (unsigned)a.B)
+                                     : dim3((unsigned)((a.n + kBR - 1) / kBR), (unsigned)a.Hkv,
+                                            (unsigned)a.B);
+    return launch_pdl(gated_bwd_tc_kernel<SIDE, D, KPC, BC>, grid, dim3(kBwThreads),
+                      (size_t)BwLayout<SIDE, D, KPC, BC>::kBytes, s, plan.map[m], plan.map[m + 1],
+                      plan.map[m + 2], plan.map[m + 3], plan.map[m + 4], plan.map[m + 5], a);
+}
+
+// The key side's streamed tile: 32 query rows for d 128 with K_g > 64.
+inline int bw_key_bc(int d, int Kg) { return (d == 128 && Kg > 64) ? 32 : 64; }
+
+}  // namespace
+
+cudaError_t gated_bwd_tc_preflight(int d, int Kg)
+{
+    cudaError_t e;
+    if (d == 64) {
+        if (Kg > 64) {
+            if ((e = bw_preflight_t<kSideQ, 64, 2, 64>()) != cudaSuccess) return e;
+            return bw_preflight_t<kSideK, 64, 2, 64>();
+        }
+        if ((e = bw_preflight_t<kSideQ, 64, 1, 64>()) != cudaSuccess) return e;
+        return bw_preflight_t<kSideK, 64, 1, 64>();
+    }
+    if (Kg > 64) {
+        if ((e = bw_preflight_t<kSideQ, 128, 2, 64>()) != cudaSuccess) return e;
+        return bw_preflight_t<kSideK, 128, 2, 32>();
+    }
+    if ((e = bw_preflight_t<kSideQ, 128, 1, 64>()) != cudaSuccess) return e;
+    return bw_preflight_t<kSideK, 128, 1, 64>();
+}
+
+cudaError_t gated_bwd_tc_prepare(const GatedLaunch &p, const __half *g16, int kp,
+                                 GatedBwTcPlan *plan)
+{
+    cudaError_t e = gated_bwd_tc_preflight(p.d, p.Kg);
+    if (e != cudaSuccess) return e;
+    plan->p = p;
+    plan->kp = kp;
+    const uint32_t kbc = (uint32_t)bw_key_bc(p.d, p.Kg);
+    // query side: rows Q, dO, G_q (128); streamed K, V, G_k (64)
+    // key side: rows K, V, G_k (128); streamed Q, dO, G_q (64, or 32)
+    if (!make_map_4d(&plan->map[0], p.q, false, p.B, p.n, p.Hq, p.d, 128) ||
+        !make_map_4d(&plan->map[1], p.dO, false, p.B, p.n, p.Hq, p.d, 128) ||
+        !make_map_4d(&plan->map[2], g16, true, p.B, p.n, 1, kp, 128) ||
+        !make_map_4d(&plan->map[3], p.k, false, p.B, p.n, p.Hkv, p.d, 64) ||
+        !make_map_4d(&plan->map[4], p.v, false, p.B, p.n, p.Hkv, p.d, 64) ||
+        !make_map_4d(&plan->map[5], g16, true, p.B, p.n, 1, kp, 64) ||
+        !make_map_4d(&plan->map[6], p.k, false, p.B, p.n, p.Hkv, p.d, 128) ||
+        !make_map_4d(&plan->map[7], p.v, false, p.B, p.n, p.Hkv, p.d, 128) ||
+        !make_map_4d(&plan->map[8], g16, true, p.B, p.n, 1, kp, 128) ||
+        !make_map_4d(&plan->map[9], p.q, false, p.B, p.n, p.Hq, p.d, kbc) ||
+        !make_map_4d(&plan->map[10], p.dO, false, p.B, p.n, p.Hq, p.d, kbc) ||
+        !make_map_4d(&plan->map[11], g16, true, p.B, p.n, 1, kp, kbc))
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, float *dlam_part,
+                                float *dg_part, cudaStream_t s, int *launches)
+{
+    const GatedLaunch &p = plan.p;
+    BwArgs a;
+    a.B = p.B;
+    a.n = p.n;
+    a.Hq = p.Hq;
+    a.Hkv = p.Hkv;
+    a.nks = plan.kp / 16;
+    a.Kg = p.Kg;
+    a.window = std::min(p.window, p.n);   // i - j < n for every pair
+    a.hc = std::min(kBwHeadChunk, p.Hq);
+    a.nhc = (p.Hq + a.hc - 1) / a.hc;
+    a.nqt = (p.n + kBR - 1) / kBR;
+    a.scale = p.scale;
+    a.half_scale = 0.5f * p.scale;
+    a.half_lambda = 0.5f * p.lambda;
+    a.lambda = p.lambda;
+    a.lse = p.lse;
+    a.Dd = Dd;
+    a.dq = p.dq;
+    a.dk = p.dk;
+    a.dv = p.dv;
+    a.dg_part = dg_part;
+    a.dlam_part = dlam_part;
+    a.status = p.wc.status;
+    cudaError_t e;
+    const bool two = p.Kg > 64;
+    prof_begin("gated_bwd_dq", s);
+    if (p.d == 64)
+        e = two ? bw_launch_t<kSideQ, 64, 2, 64>(plan, a, s)
+                : bw_launch_t<kSideQ, 64, 1, 64>(plan, a, s);
+    else
+        e = two ? bw_launch_t<kSideQ, 128, 2, 64>(plan, a, s)
+                : bw_launch_t<kSideQ, 128, 1, 64>(plan, a, s);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    prof_begin("gated_bwd_dkv", s);
+    if (p.d == 64)
+        e = two ? bw_launch_t<kSideK, 64, 2, 64>(plan, a, s)
+                : bw_launch_t<kSideK, 64, 1, 64>(plan, a, s);
+    else
+        e = two ? bw_launch_t<kSideK, 128, 2, 32>(plan, a, s)
+                : bw_launch_t<kSideK, 128, 1, 64>(plan, a, s);
+    prof_end(s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    return cudaSuccess;
+}
+
+int gated_bwd_tc_dlam_count(int B, int n, int Hq)
+{
+    const int hc = std::min(kBwHeadChunk, Hq);
+    return B * ((Hq + hc - 1) / hc) * ((n + kBR - 1) / kBR);
+}
+
+}  // namespace focus

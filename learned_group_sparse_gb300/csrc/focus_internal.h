@@ -197,9 +197,22 @@ struct GatedTcPlan {
     int kp, pair_heads, grid;
 };
 cudaError_t gated_tc_preflight(int d, int Kg);
+// The tensor-core backward (focus_gated_bwd_tc.cu): the query-side and
+// key-side kernels' attributes and TMA maps (enqueues nothing), then their
+// launches, given D = dO . O and the partial buffers of d lambda and dG.
+struct GatedBwTcPlan {
+    CUtensorMap map[12];   // query side: Q, dO, G_q, K, V, G_k; key side: K, V, G_k, Q, dO, G_q
+    GatedLaunch p;
+    int kp;
+};
+cudaError_t gated_bwd_tc_preflight(int d, int Kg);
+cudaError_t gated_bwd_tc_prepare(const GatedLaunch &p, const __half *g16, int kp,
+                                 GatedBwTcPlan *plan);
+cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, float *dlam_part,
+                                float *dg_part, cudaStream_t s, int *launches);
+int gated_bwd_tc_dlam_count(int B, int n, int Hq);
 cudaError_t gated_tc_prepare(const GatedLaunch &p, const __half *g16, int kp, GatedTcPlan *plan);
 cudaError_t gated_tc_launch(const GatedTcPlan &plan, cudaStream_t s, int *launches);
-cudaError_t gated_preflight(int d, int Kg);
 cudaError_t launch_gated_fwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
 cudaError_t launch_gated_bwd(const GatedLaunch &p, void *ws, cudaStream_t s, int *launches);
 
