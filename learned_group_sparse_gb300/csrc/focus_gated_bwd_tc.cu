@@ -210,6 +210,127 @@ __device__ __forceinline__ float bw_tanh(float x)
     return t;
 }
 
+__device__ __forceinline__ float bw_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two fp32 lanes per instruction: a * b + c, a * b, a + b.
+__device__ __forceinline__ float2 fma2v(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2v(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2v(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// The elementwise constants, as lane pairs.
+struct EwConst {
+    float2 sc2;   // scale log2(e)
+    float2 sc;    // scale
+    float2 hs2;   // scale log2(e) / 2
+    float2 hs;    // scale / 2
+    float2 hl;    // lambda / 2
+    float2 q1;    // -scale / 4
+    float2 q0;    // scale / 4
+    float2 lam;   // lambda
+};
+
+// One elementwise pass over this row's HC columns of a tile: from S, A, dP
+// (f[0..HC), f[HC..2HC), f[2HC..3HC)) and the columns' or the row's
+// -lse2 and -D (nl, nd), the packed P, dT and (GATED) da.  Column c of the
+// tile is causal iff c <= lim (query side) / c >= lim (key side), and gated
+// iff c <= loc / c >= loc (tested only where the tile needs it).
+template <int SIDE, int HC, bool GATED>
+__device__ __forceinline__ void ew_tile(const float *f, const float *vl, int BC, float2 nl_r,
+                                        float2 nd_r, const EwConst &k, bool allg, bool causal,
+                                        int cb, int lim, int loc, uint32_t *pkP, uint32_t *pkT,
+                                        uint32_t *pkA, float2 &dl2)
+{
+#pragma unroll
+    for (int e = 0; e < HC; e += 2) {
+        const float2 sv = make_float2(f[e], f[e + 1]);
+        const float2 dpv = make_float2(f[2 * HC + e], f[2 * HC + e + 1]);
+        float2 nl = nl_r, nd = nd_r;
+        if (SIDE == kSideK) {
+            nl = *reinterpret_cast<const float2 *>(vl + e);
+            nd = *reinterpret_cast<const float2 *>(vl + BC + e);
+        }
+        float2 g2 = k.sc2, g1 = k.sc, sps = make_float2(0.f, 0.f), av = sps;
+        if constexpr (GATED) {
+            av = make_float2(f[HC + e], f[HC + e + 1]);
+            const float2 z = mul2v(av, k.hl);
+            const float2 th = make_float2(bw_tanh(z.x), bw_tanh(z.y));
+            g2 = fma2v(th, k.hs2, k.hs2);                 // scale log2(e) sigma
+            g1 = fma2v(th, k.hs, k.hs);                   // scale sigma
+            sps = fma2v(mul2v(th, k.q1), th, k.q0);       // scale sigma (1 - sigma)
+            if (!allg) {   // a tile across the window's edge: local pairs keep gate 1
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int c = cb + e + q;
+                    const bool gp = SIDE == kSideQ ? c <= loc : c >= loc;
+                    if (!gp) {
+                        (q ? g2.y : g2.x) = k.sc2.x;
+                        (q ? g1.y : g1.x) = k.sc.x;
+                        (q ? sps.y : sps.x) = 0.f;
+                    }
+                }
+            }
+        }
+        const float2 xx = fma2v(sv, g2, nl);
+        float2 p = make_float2(bw_ex2(xx.x), bw_ex2(xx.y));
+        if (causal) {
+            const int c = cb + e;
+            if (!(SIDE == kSideQ ? c <= lim : c >= lim)) p.x = 0.f;
+            if (!(SIDE == kSideQ ? c + 1 <= lim : c + 1 >= lim)) p.y = 0.f;
+        }
+        const float2 ds = mul2v(p, add2v(dpv, nd));
+        const float2 dt = mul2v(ds, g1);
+        pkP[e / 2] = pack_bf16x2(p.x, p.y);
+        pkT[e / 2] = pack_bf16x2(dt.x, dt.y);
+        if constexpr (GATED) {
+            const float2 u = mul2v(mul2v(ds, sv), sps);   // d gate sigma (1 - sigma)
+            const float2 da = mul2v(u, k.lam);
+            if (SIDE == kSideQ) dl2 = fma2v(u, av, dl2);
+            pkA[e / 2] = pack_f16x2(da.x, da.y);
+        }
+    }
+}
+
 // D[tmem] (+)= A[smem] B[smem] with fp16 A and B: the same instruction as
 // the bf16 form, the operand type is in the instruction descriptor.
 template <uint32_t AHI, uint32_t BHI>
@@ -344,13 +465,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     }
                     const int c0 = SIDE == kSideQ ? 64 * v : r0 + BC * v;
                     if (SIDE == kSideK) {
-                        // the tile's queries: base-2 log-sum-exp (+inf past n: P = 0) and D
+                        // the tile's queries: minus the base-2 log-sum-exp (-inf
+                        // past n: P = 0) and minus D
                         float *vl = vec + st * 2 * BC;
                         for (int c = lane; c < BC; c += 32) {
                             const int i = c0 + c;
                             const int64_t x = ((int64_t)b * a.Hq + h) * a.n + i;
-                            vl[c] = i < a.n ? a.lse[x] * kLog2e : CUDART_INF_F;
-                            vl[BC + c] = i < a.n ? a.Dd[x] : 0.f;
+                            vl[c] = i < a.n ? -a.lse[x] * kLog2e : -CUDART_INF_F;
+                            vl[BC + c] = i < a.n ? -a.Dd[x] : 0.f;
                         }
                     }
                     __syncwarp();
@@ -496,19 +618,29 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         const int r = (warp & 3) * 32 + lane;     // own row = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int row = r0 + r;                   // query (query side) or key (key side)
-        const float scale2 = a.scale * kLog2e, half_scale2 = a.half_scale * kLog2e;
-        float dlam = 0.f;
+        EwConst kc;
+        kc.sc2 = make_float2(a.scale * kLog2e, a.scale * kLog2e);
+        kc.sc = make_float2(a.scale, a.scale);
+        kc.hs2 = make_float2(a.half_scale * kLog2e, a.half_scale * kLog2e);
+        kc.hs = make_float2(a.half_scale, a.half_scale);
+        kc.hl = make_float2(a.half_lambda, a.half_lambda);
+        kc.q1 = make_float2(-0.5f * a.half_scale, -0.5f * a.half_scale);
+        kc.q0 = make_float2(0.5f * a.half_scale, 0.5f * a.half_scale);
+        kc.lam = make_float2(a.lambda, a.lambda);
+        float2 dl2 = make_float2(0.f, 0.f);
         bool ok = true;
         int t = 0;
         uint8_t *outb = sm + L::kOut;
         uint8_t *oP = outb, *oT = outb + (SIDE == kSideK ? L::kOutT : 0u), *oA = oT + L::kOutT;
         for (int hi = 0; ok && hi < nh; ++hi) {
             const int h = h0 + hi;
-            float lse2_r = CUDART_INF_F, D_r = 0.f;   // query side: this row's
+            // query side: minus this row's base-2 log-sum-exp (-inf past n) and D
+            float2 nl_r = make_float2(-CUDART_INF_F, -CUDART_INF_F), nd_r = make_float2(0.f, 0.f);
             if (SIDE == kSideQ && row < a.n) {
                 const int64_t x = ((int64_t)b * a.Hq + h) * a.n + row;
-                lse2_r = a.lse[x] * kLog2e;
-                D_r = a.Dd[x];
+                const float l2 = -a.lse[x] * kLog2e, dd = -a.Dd[x];
+                nl_r = make_float2(l2, l2);
+                nd_r = make_float2(dd, dd);
             }
             for (int v = 0; ok && v < ncol; ++v, ++t) {
                 const BwTile x = bw_tile<SIDE, BC>(v, r0, rend, a.n, a.window);
@@ -529,46 +661,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 if (lane == 0) mbar_arrive(&bars[W_SFREE]);   // S, A, dP may be overwritten
                 const float *vl = vec + (t % NS) * 2 * BC + wg * HC;   // key side
                 uint32_t pkP[HC / 2], pkT[HC / 2], pkA[HC / 2];
-#pragma unroll
-                for (int e = 0; e < HC; e += 2) {
-                    float p2[2], t2[2], a2[2];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int c = wg * HC + e + k;
-                        const int i = SIDE == kSideQ ? row : x.c0 + c;   // query
-                        const int j = SIDE == kSideQ ? x.c0 + c : row;   // key
-                        const float s = f[e + k], av = f[HC + e + k], dp = f[2 * HC + e + k];
-                        const float lse2 = SIDE == kSideQ ? lse2_r : vl[e + k];
-                        const float Dv = SIDE == kSideQ ? D_r : vl[BC + e + k];
-                        // gate of the pair: g2 = scale log2(e) gate, g1 = scale gate
-                        float g2 = scale2, g1 = a.scale, sp = 0.f;
-                        bool gp = false;
-                        if (x.gated) {
-                            gp = x.allg || (i - j >= a.window);
-                            if (gp) {
-                                const float th = bw_tanh(a.half_lambda * av);
-                                g2 = fmaf(half_scale2, th, half_scale2);
-                                g1 = fmaf(a.half_scale, th, a.half_scale);
-                                sp = fmaf(-0.25f * th, th, 0.25f);   // sigma (1 - sigma)
-                            }
-                        }
-                        float p = exp2f(s * g2 - lse2);
-                        if (x.causal && j > i) p = 0.f;
-                        const float ds = p * (dp - Dv);
-                        float da = 0.f;
-                        if (gp) {
-                            const float dgate = ds * s * a.scale;
-                            da = dgate * a.lambda * sp;
-                            if (SIDE == kSideQ) dlam = fmaf(dgate * sp, av, dlam);
-                        }
-                        p2[k] = p;
-                        t2[k] = ds * g1;
-                        a2[k] = da;
-                    }
-                    pkP[e / 2] = pack_bf16x2(p2[0], p2[1]);
-                    pkT[e / 2] = pack_bf16x2(t2[0], t2[1]);
-                    pkA[e / 2] = pack_f16x2(a2[0], a2[1]);
-                }
+                const int dlt = row - x.c0;   // the row against the tile's first column
+                const int loc = SIDE == kSideQ ? dlt - a.window : dlt + a.window;
+                if (x.gated)
+                    ew_tile<SIDE, HC, true>(f, vl, BC, nl_r, nd_r, kc, x.allg, x.causal, wg * HC,
+                                            dlt, loc, pkP, pkT, pkA, dl2);
+                else
+                    ew_tile<SIDE, HC, false>(f, vl, BC, nl_r, nd_r, kc, x.allg, x.causal, wg * HC,
+                                             dlt, loc, pkP, pkT, pkA, dl2);
                 // the operand tiles are free once the previous tile's gradient
                 // products are done
                 if (t > 0) ok = mbar_wait(&bars[W_PEMPTY], (t - 1) & 1, abort_flag, a.status);
@@ -586,8 +686,9 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                      pkP[4 * q + 3]);
                     st_shared_v4(smem_u32(oT + off), pkT[4 * q], pkT[4 * q + 1], pkT[4 * q + 2],
                                  pkT[4 * q + 3]);
-                    st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1], pkA[4 * q + 2],
-                                 pkA[4 * q + 3]);
+                    if (x.gated)   // the dG product runs on gated tiles only
+                        st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1],
+                                     pkA[4 * q + 2], pkA[4 * q + 3]);
                 }
                 fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
                 __syncwarp();
@@ -665,6 +766,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         }
         if (SIDE == kSideQ) {
             // d lambda: this CTA's partial, the EW warps' sums in a fixed order
+            float dlam = dl2.x + dl2.y;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
             if (lane == 0) red[warp] = dlam;
