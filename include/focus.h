@@ -410,6 +410,18 @@ int focus_profile_read(char *names, int name_stride, double *total_ms, int *laun
  */
 void focus_trace_attention(long long *group_buf, long long *window_buf, long long *dense_buf);
 
+/*
+ * Pipeline wait tracing of the gated backward (a debugging aid).  For
+ * launches from this host thread, the query-side and key-side kernels write,
+ * for each CTA whose linear index (x fastest, then y, then z) is below
+ * max_ctas, 32 int64 counters of SM cycles into the given DEVICE buffers
+ * (each at least 32 x max_ctas entries; NULL or max_ctas <= 0 disables):
+ * the producer's, the MMA thread's and the first elementwise thread's time
+ * waiting on each pipeline barrier and in each phase, and the tile count.
+ * Slot meanings are listed with the kernel's trace enum.
+ */
+void focus_trace_gated(long long *query_buf, long long *key_buf, int max_ctas);
+
 #ifdef __cplusplus
 }
 #endif

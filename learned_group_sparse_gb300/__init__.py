@@ -88,6 +88,7 @@ def library() -> ctypes.CDLL:
                                      vp, sz, vp], i32),
                 "focus_profile_enable": ([i32], None),
                 "focus_trace_attention": ([vp, vp, vp], None),
+                "focus_trace_gated": ([vp, vp, i32], None),
                 "focus_profile_read": ([vp, i32, vp, vp, i32], i32),
             }
             for name, (args, res) in sig.items():
@@ -166,6 +167,12 @@ def focus_profile_read(max_entries: int = 64) -> dict:
         nm = names.raw[i * stride:(i + 1) * stride].split(b"\0", 1)[0].decode()
         out[nm] = (float(ms[i]), int(cnt[i]))
     return out
+
+
+def focus_trace_gated(query_buf=None, key_buf=None, max_ctas=0) -> None:
+    """Sets (or with None / 0 clears) the per-CTA wait-trace buffers of the
+    gated backward, int64 CUDA tensors of at least 32 x max_ctas entries."""
+    library().focus_trace_gated(_p(query_buf), _p(key_buf), int(max_ctas))
 
 
 def focus_trace_attention(group_buf=None, window_buf=None, dense_buf=None) -> None:

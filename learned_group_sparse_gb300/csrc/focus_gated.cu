@@ -36,14 +36,15 @@ struct GatedArgs {
     const __half *g;                  // [B, n, kp] fp16, zero-padded columns
     const __nv_bfloat16 *o, *dO;      // [B, n, Hq, D]
     const float *lse;                 // [B, Hq, n] natural log
-    const float *Dd;                  // [B, Hq, n] dO . O
+    const float *rowv;                // [2][B, Hq, npad]: -lse log2(e) (-inf past n) and
+                                      // -dO . O (0 past n), npad = n rounded up to 128
     __nv_bfloat16 *out;               // O (forward)
     float *lse_out;                   // forward
     float *dq, *dk, *dv, *dg;         // [B, n, Hq, D], [B, n, Hkv, D] x 2, [B, n, Kg]
     float *dlam_part;                 // [B, nhc, n / 64] partial d lambda
     float *dg_part;                   // [nhc + Hkv][B, n, Kg]: row side per head chunk, column
                                       // side per kv head
-    int B, n, Hq, Hkv, kp, Kg, window;
+    int B, n, Hq, Hkv, kp, Kg, window, npad;
     int hc, nhc;                      // query heads per dG chunk, chunks
     float scale, lambda;
 };
@@ -62,25 +63,33 @@ __global__ void gated_g16_kernel(const float *__restrict__ G, int64_t rows, int 
     }
 }
 
-// D[b, h, i] = dO_i . O_i (bf16 inputs, fp32 sum): one warp per (row, head).
+// The backward's per-(row, head) values, one warp each: -lse_i log2(e) and
+// -D_i = -dO_i . O_i (bf16 inputs, fp32 sum), in rows padded to npad (-inf
+// and 0 past n) so that a kernel can copy any 64-row run of them whole.
 template <int D>
-__global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ Dd)
+__global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ rowv)
 {
     grid_dep_sync();
     const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (w >= (int64_t)a.B * a.n * a.Hq) return;
-    const int64_t row = w / a.Hq;   // b * n + i
-    const int h = (int)(w - row * a.Hq);
-    const __nv_bfloat16 *o = a.o + w * D, *g = a.dO + w * D;
+    if (w >= (int64_t)a.B * a.npad * a.Hq) return;
+    const int64_t bi = w / a.Hq;     // b * npad + i
+    const int h = (int)(w - bi * a.Hq);
+    const int64_t b = bi / a.npad, i = bi - b * a.npad;
     float sum = 0.f;
+    if (i < a.n) {
+        const int64_t x = ((b * a.n + i) * a.Hq + h) * D;
+        const __nv_bfloat16 *o = a.o + x, *g = a.dO + x;
 #pragma unroll
-    for (int e = lane; e < D; e += 32) sum += __bfloat162float(o[e]) * __bfloat162float(g[e]);
+        for (int e = lane; e < D; e += 32) sum += __bfloat162float(o[e]) * __bfloat162float(g[e]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
     if (lane == 0) {
-        const int64_t b = row / a.n, i = row - b * a.n;
-        Dd[(b * a.Hq + h) * a.n + i] = sum;
+        const int64_t y = (b * a.Hq + h) * a.npad + i;
+        const int64_t plane = (int64_t)a.B * a.Hq * a.npad;
+        rowv[y] = i < a.n ? -a.lse[(b * a.Hq + h) * a.n + i] * 1.4426950408889634f : -CUDART_INF_F;
+        rowv[plane + y] = -sum;
     }
 }
 
@@ -98,7 +107,8 @@ __global__ void gated_dg_reduce_kernel(const GatedArgs a)
 }
 
 // d lambda = sum of the query-tile partials, in a fixed order (one thread).
-__global__ void gated_dlam_kernel(const float *__restrict__ part, int count, float *__restrict__ out)
+__global__ void gated_dlam_kernel(const float *__restrict__ part, int count,
+                                  float *__restrict__ out)
 {
     grid_dep_sync();
     if (threadIdx.x == 0 && blockIdx.x == 0) {
@@ -116,7 +126,9 @@ size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg)
     const int kp = (Kg + 15) / 16 * 16;
     const int nqt = (n + kGT - 1) / kGT;
     const int nhc = (Hq + kGHeadChunk - 1) / kGHeadChunk;
-    return (((size_t)B * n * kp * 2 + a256) & ~a256) + (((size_t)B * Hq * n * 4 + a256) & ~a256) +
+    const size_t npad = ((size_t)n + 127) / 128 * 128;
+    return (((size_t)B * n * kp * 2 + a256) & ~a256) +
+           (((size_t)2 * B * Hq * npad * 4 + a256) & ~a256) +
            (((size_t)B * nhc * nqt * 4 + a256) & ~a256) +
            (((size_t)(nhc + Hkv) * B * n * Kg * 4 + a256) & ~a256);
 }
@@ -151,8 +163,9 @@ GatedArgs gated_args(const GatedLaunch &p, void *ws)
     uint8_t *w = static_cast<uint8_t *>(ws);
     a.g = reinterpret_cast<const __half *>(w);
     w += ((size_t)p.B * p.n * a.kp * 2 + a256) & ~a256;
-    a.Dd = reinterpret_cast<const float *>(w);
-    w += ((size_t)p.B * p.Hq * p.n * 4 + a256) & ~a256;
+    a.npad = (p.n + 127) / 128 * 128;
+    a.rowv = reinterpret_cast<const float *>(w);
+    w += ((size_t)2 * p.B * p.Hq * a.npad * 4 + a256) & ~a256;
     a.hc = kGHeadChunk < p.Hq ? kGHeadChunk : p.Hq;
     a.nhc = (p.Hq + a.hc - 1) / a.hc;
     a.dlam_part = reinterpret_cast<float *>(w);
@@ -176,14 +189,15 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, const GatedArgs &a, const GatedBwT
                         cudaStream_t s, int *launches)
 {
     cudaError_t e;
-    const int64_t warps = (int64_t)p.B * p.n * p.Hq;
+    const int64_t warps = (int64_t)p.B * a.npad * p.Hq;
     prof_begin("gated_bwd_prep", s);
     e = launch_pdl(gated_bwd_prep_kernel<D>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256),
-                   0, s, a, const_cast<float *>(a.Dd));
+                   0, s, a, const_cast<float *>(a.rowv));
     prof_end(s);
     if (e != cudaSuccess) return e;
     *launches += 1;
-    if ((e = gated_bwd_tc_launch(plan, a.Dd, a.dlam_part, a.dg_part, s, launches)) != cudaSuccess)
+    if ((e = gated_bwd_tc_launch(plan, a.rowv, a.npad, a.dlam_part, a.dg_part, s, launches)) !=
+        cudaSuccess)
         return e;
     const int64_t dgn = (int64_t)p.B * p.n * p.Kg;
     prof_begin("gated_dg_reduce", s);

@@ -58,43 +58,50 @@ constexpr int kBwMma = 9;
 // kBwThreads * (registers per thread at launch), which the preflight checks.
 constexpr int kBwRegsEw = 216;
 constexpr int kBwRegsOther = 72;
-constexpr int kBwStages = 2;
 constexpr int kBwHeadChunk = 4;     // query heads per query-side CTA (one dG partial each)
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum {
-    W_ROWFULL = 0, W_ROWEMPTY = 1, W_CFULL = 2, W_CEMPTY = 4, W_SFULL = 6, W_SFREE = 7,
-    W_PFULL = 8, W_PEMPTY = 9, W_ACCDONE = 10, W_ACCFREE = 11, W_DRAIN = 12, kWBars = 13
+    W_ROWFULL = 0, W_ROWEMPTY = 1, W_CFULL = 2, W_CEMPTY = 6, W_SFULL = 10, W_SFREE = 11,
+    W_PFULL = 12, W_PEMPTY = 13, W_ACCDONE = 14, W_ACCFREE = 15, W_DRAIN = 16, kWBars = 17
 };
 
 // Shared memory and TMEM columns of one CTA.  BC: rows of a streamed tile
 // (64; 32 on the key side for d 128 with K_g > 64, where the accumulators
-// need 384 TMEM columns).
+// need 384 TMEM columns).  The query side keeps its operand tiles dT and da
+// in TMEM (bf16 / fp16 pairs, 32 columns each) and streams through three
+// stages where they fit; the key side, whose accumulators fill TMEM, keeps
+// P, dT and da in shared memory and streams through two.
 template <int SIDE, int D, int KPC, int BC>
 struct BwLayout {
     static constexpr uint32_t kRowT = kBR * D * 2;        // R1 or R2: D/64 chunks of 16 KB
     static constexpr uint32_t kRowG = kBR * KPC * 128;    // RG: KPC chunks of 16 KB
     static constexpr uint32_t kColT = BC * D * 2;         // C1 or C2: chunks of BC * 128 bytes
     static constexpr uint32_t kColG = BC * KPC * 128;     // CG
-    static constexpr uint32_t kStage = 2 * kColT + kColG;
+    // key side: -lse2 and -D of the tile's queries (2 BC floats, in 1 KB)
+    static constexpr uint32_t kVecB = SIDE == kSideK ? 1024 : 0;
+    static constexpr uint32_t kStage = 2 * kColT + kColG + kVecB;
     static constexpr uint32_t kOutT = kBR * 128;          // an operand tile: 128 rows of 128 bytes
-    static constexpr int kNOut = SIDE == kSideK ? 3 : 2;  // [P,] dT, da
+    static constexpr int kNOut = SIDE == kSideK ? 3 : 0;  // P, dT, da (key side)
+    static constexpr uint32_t kFixed = 2 * kRowT + kRowG + kNOut * kOutT + 1024 + 1024;
+    static constexpr int NS = (SIDE == kSideQ && kFixed + 3 * kStage <= 232448) ? 3 : 2;
     static constexpr uint32_t kR1 = 0;
     static constexpr uint32_t kR2 = kR1 + kRowT;
     static constexpr uint32_t kRG = kR2 + kRowT;
-    static constexpr uint32_t kC = kRG + kRowG;
-    static constexpr uint32_t kOut = kC + kBwStages * kStage;
-    static constexpr uint32_t kVecB = SIDE == kSideK ? kBwStages * 2 * BC * 4 : 0;
-    static constexpr uint32_t kVec = kOut + kNOut * kOutT;  // key side: [stage][lse2 | D][BC]
-    static constexpr uint32_t kBar = kVec + kVecB;
+    static constexpr uint32_t kOut = kRG + kRowG;
+    static constexpr uint32_t kC = kOut + kNOut * kOutT;  // stages: C1, C2, CG[, vec]
+    static constexpr uint32_t kBar = kC + NS * kStage;
     static constexpr uint32_t kMisc = kBar + kWBars * 8;    // TMEM base, abort flag
     static constexpr uint32_t kRed = kMisc + 16;            // 8 floats
     static constexpr uint32_t kBytes = kRed + 32 + 1024;    // + alignment slack
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColA = BC, kColP = 2 * BC, kAcc = 3 * BC;
     static constexpr uint32_t kAccG = kAcc + (SIDE == kSideK ? 2 * D : D);
-    static_assert(kAccG + 64 * KPC <= 512, "TMEM columns");
+    static constexpr uint32_t kOutTm = kAccG + 64 * KPC;   // query side: dT, then da
+    static constexpr uint32_t kOutAm = kOutTm + BC / 2;
+    static_assert(kAccG + 64 * KPC + (SIDE == kSideQ ? BC : 0) <= 512, "TMEM columns");
     static_assert(kBytes <= 232448, "shared memory per CTA");
+    static_assert(kStage % 1024 == 0, "stage alignment");
 };
 
 struct BwArgs {
@@ -103,13 +110,26 @@ struct BwArgs {
     float half_scale;    // scale / 2
     float half_lambda;   // lambda / 2
     float lambda;
-    const float *lse;    // [B, Hq, n] natural log
-    const float *Dd;     // [B, Hq, n] dO . O
+    const float *nl2;    // [B, Hq, npad] -lse log2(e), -inf past n
+    const float *nD;     // [B, Hq, npad] -dO . O, 0 past n
+    int npad;
     float *dq;           // [B, n, Hq, D]
     float *dk, *dv;      // [B, n, Hkv, D]
     float *dg_part;      // [nhc + Hkv][B, n, Kg]
     float *dlam_part;    // [B, nhc, nqt]
     int *status;
+    long long *trace;    // nullable: [CTA][kBwTrace] SM cycles (CTAs below trace_ctas)
+    int trace_ctas;
+};
+
+// Per-CTA trace slots (SM cycles): the producer's waits, the MMA thread's
+// waits, the first elementwise thread's waits and phases.
+enum {
+    BT_P_ROWEMPTY = 0, BT_P_CEMPTY = 1, BT_P_TOTAL = 3,
+    BT_M_ROWFULL = 8, BT_M_CFULL = 9, BT_M_SFREE = 10, BT_M_PFULL = 11, BT_M_ACCFREE = 12,
+    BT_M_TOTAL = 14,
+    BT_E_SFULL = 16, BT_E_TMEM = 17, BT_E_MATH = 18, BT_E_PEMPTY = 19, BT_E_STORE = 20,
+    BT_E_ACCDONE = 21, BT_E_TOTAL = 23, BT_E_TILES = 24, kBwTrace = 32
 };
 
 // A streamed tile against the CTA's rows: its first column row c0; whether
@@ -200,6 +220,18 @@ __device__ __forceinline__ void tmem_ld3x16(uint32_t a0, uint32_t a1, uint32_t a
         : "memory");
 #pragma unroll
     for (int i = 0; i < 48; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
 }
 
 // tanh with the hardware approximation (relative error about 2^-11)
@@ -352,7 +384,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     using L = BwLayout<SIDE, D, KPC, BC>;
     constexpr int kChunks = D / 64;
     constexpr int HC = BC / 2;          // columns per elementwise warpgroup
-    constexpr int NS = kBwStages;
+    constexpr int NS = L::NS;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -361,12 +393,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kMisc + 4);
     float *red = reinterpret_cast<float *>(sm + L::kRed);
-    float *vec = reinterpret_cast<float *>(sm + L::kVec);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.z;
     const int kvq = a.Hq / a.Hkv;
+    const int64_t cta = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    long long *tr = (a.trace && cta < a.trace_ctas) ? a.trace + cta * kBwTrace : nullptr;
+    const long long t_start = clock64();
     // the CTA's rows, heads and streamed tiles
     int r0, rend, h0, nh, ncol, kvh0;
     if (SIDE == kSideQ) {
@@ -429,11 +463,13 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             int t = 0;
             int nrow = 0;   // row-operand loads issued
             bool ok = true;
+            long long ptr_[4] = {0, 0, 0, 0};   // producer slots
             for (int hi = 0; ok && hi < nh; ++hi) {
                 const int h = h0 + hi;
                 if (SIDE == kSideQ || hi == 0) {
                     if (hi > 0 && lane == 0)
-                        ok = mbar_wait(&bars[W_ROWEMPTY], (hi - 1) & 1, abort_flag, a.status);
+                        ok = mbar_wait_t(&bars[W_ROWEMPTY], (hi - 1) & 1, abort_flag, a.status,
+                                     tr != nullptr, ptr_[BT_P_ROWEMPTY]);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) {
                         ok = false;
                         break;
@@ -457,28 +493,25 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 for (int v = 0; ok && v < ncol; ++v, ++t) {
                     const int st = t % NS;
                     if (t >= NS && lane == 0)
-                        ok = mbar_wait(&bars[W_CEMPTY + st], ((t / NS) - 1) & 1, abort_flag,
-                                       a.status);
+                        ok = mbar_wait_t(&bars[W_CEMPTY + st], ((t / NS) - 1) & 1, abort_flag,
+                                         a.status, tr != nullptr, ptr_[BT_P_CEMPTY]);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) {
                         ok = false;
                         break;
                     }
                     const int c0 = SIDE == kSideQ ? 64 * v : r0 + BC * v;
-                    if (SIDE == kSideK) {
-                        // the tile's queries: minus the base-2 log-sum-exp (-inf
-                        // past n: P = 0) and minus D
-                        float *vl = vec + st * 2 * BC;
-                        for (int c = lane; c < BC; c += 32) {
-                            const int i = c0 + c;
-                            const int64_t x = ((int64_t)b * a.Hq + h) * a.n + i;
-                            vl[c] = i < a.n ? -a.lse[x] * kLog2e : -CUDART_INF_F;
-                            vl[BC + c] = i < a.n ? -a.Dd[x] : 0.f;
-                        }
-                    }
-                    __syncwarp();
                     if (lane == 0) {
                         uint8_t *sc = sm + L::kC + st * L::kStage;
-                        mbar_arrive_expect_tx(&bars[W_CFULL + st], L::kStage);
+                        mbar_arrive_expect_tx(&bars[W_CFULL + st],
+                                              L::kStage - L::kVecB + (SIDE == kSideK ? 8 * BC : 0));
+                        if (SIDE == kSideK) {
+                            // the tile's queries: minus the base-2 log-sum-exp (-inf
+                            // past n: P = 0) and minus D, from rows padded past n
+                            const int64_t x = ((int64_t)b * a.Hq + h) * a.npad + c0;
+                            uint8_t *vd = sc + 2 * L::kColT + L::kColG;
+                            bulk_load(vd, a.nl2 + x, 4 * BC, &bars[W_CFULL + st]);
+                            bulk_load(vd + 4 * BC, a.nD + x, 4 * BC, &bars[W_CFULL + st]);
+                        }
                         const int ch = SIDE == kSideQ ? h / kvq : h;   // head of C1 / C2
                         for (int c = 0; c < kChunks; ++c) {
                             tma_load_4d(sc + c * (BC * 128), &tmC1, &bars[W_CFULL + st], c * 64,
@@ -492,6 +525,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     }
                     __syncwarp();
                 }
+            }
+            if (tr && lane == 0) {
+                ptr_[BT_P_TOTAL] = clock64() - t_start;
+                for (int i = 0; i < 4; ++i) tr[i] = ptr_[i];
             }
             // A CTA that gave up lets the copies already issued land before
             // shared memory is released.
@@ -525,23 +562,30 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 const uint32_t outA = outT + (L::kOutT >> 4);
                 int t = 0;
                 bool ok = true, dg_started = false;
+                const bool trc = tr != nullptr;
+                long long mtr[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // slots 8..15
                 int pt = -1, p_hi = 0;                 // the tile whose gradient products are next
                 bool p_gated = false, p_first = false, p_last = false;
                 auto grads = [&](int tt, bool gtd, bool first, bool last, int hi) -> bool {
-                    if (!mbar_wait(&bars[W_PFULL], tt & 1, abort_flag, a.status)) return false;
+                    if (!mbar_wait_t(&bars[W_PFULL], tt & 1, abort_flag, a.status, trc,
+                                 mtr[BT_M_PFULL - 8]))
+                    return false;
                     if (SIDE == kSideQ && first && hi > 0 &&
-                        !mbar_wait(&bars[W_ACCFREE], (hi - 1) & 1, abort_flag, a.status))
+                        !mbar_wait_t(&bars[W_ACCFREE], (hi - 1) & 1, abort_flag, a.status, trc,
+                                 mtr[BT_M_ACCFREE - 8]))
                         return false;
                     tc_fence_after();
                     const uint32_t c1 = cb + (tt % NS) * (L::kStage >> 4);
                     const uint32_t c2 = c1 + (L::kColT >> 4), cg = c2 + (L::kColT >> 4);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
                         // A: 32 bytes further along the rows; B: 16 rows of 128 bytes further
                         const uint32_t ao = kk * 2, bo = kk * 128;
                         if (SIDE == kSideQ) {
+                            // dT in TMEM: 16 keys = 8 columns per step
                             const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
-                            bw_mma<kHi, kHi>(tmem + L::kAcc, outT + ao, c1 + bo, kIdAcc, acc);
+                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutTm + kk * 8, c1 + bo,
+                                                   kIdAcc, acc);
                         } else {
                             const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
                             bw_mma<kHi, kHi>(tmem + L::kAcc, outP + ao, c2 + bo, kIdAcc, acc);
@@ -549,10 +593,16 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                         }
                     }
                     if (gtd) {
-    #pragma unroll
-                        for (int kk = 0; kk < BC / 16; ++kk)
-                            bw_mma<kHi, kHi>(tmem + L::kAccG, outA + kk * 2, cg + kk * 128, kIdG,
-                                             (kk > 0 || dg_started) ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < BC / 16; ++kk) {
+                            const uint32_t acc = (kk > 0 || dg_started) ? 1u : 0u;
+                            if (SIDE == kSideQ)
+                                tc_mma_bf16_ts_lo<kHi>(tmem + L::kAccG, tmem + L::kOutAm + kk * 8,
+                                                       cg + kk * 128, kIdG, acc);
+                            else
+                                bw_mma<kHi, kHi>(tmem + L::kAccG, outA + kk * 2, cg + kk * 128, kIdG,
+                                                 acc);
+                        }
                         dg_started = true;
                     }
                     tc_commit(&bars[W_PEMPTY]);
@@ -562,20 +612,23 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 };
                 for (int hi = 0; ok && hi < nh; ++hi) {
                     if (SIDE == kSideQ || hi == 0) {
-                        ok = mbar_wait(&bars[W_ROWFULL], hi & 1, abort_flag, a.status);
+                        ok = mbar_wait_t(&bars[W_ROWFULL], hi & 1, abort_flag, a.status, trc,
+                                     mtr[BT_M_ROWFULL - 8]);
                         if (!ok) break;
                     }
                     for (int v = 0; ok && v < ncol; ++v, ++t) {
                         const BwTile x = bw_tile<SIDE, BC>(v, r0, rend, a.n, a.window);
                         const int st = t % NS;
-                        ok = mbar_wait(&bars[W_CFULL + st], (t / NS) & 1, abort_flag, a.status);
+                        ok = mbar_wait_t(&bars[W_CFULL + st], (t / NS) & 1, abort_flag, a.status,
+                                         trc, mtr[BT_M_CFULL - 8]);
                         if (ok && t > 0)
-                            ok = mbar_wait(&bars[W_SFREE], (t - 1) & 1, abort_flag, a.status);
+                            ok = mbar_wait_t(&bars[W_SFREE], (t - 1) & 1, abort_flag, a.status,
+                                             trc, mtr[BT_M_SFREE - 8]);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t c1 = cb + st * (L::kStage >> 4);
                         const uint32_t c2 = c1 + (L::kColT >> 4), cg = c2 + (L::kColT >> 4);
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t ro = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                             const uint32_t co = ((kk >> 2) * (BC * 128) + (kk & 3) * 32) >> 4;
@@ -584,7 +637,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                             bw_mma<kHi, kHi>(tmem + L::kColP, r2 + ro, c2 + co, kIdS, acc);
                         }
                         if (x.gated) {
-    #pragma unroll
+#pragma unroll
                             for (int ks = 0; ks < 4 * KPC; ++ks) {
                                 if (ks >= a.nks) break;
                                 const uint32_t ro = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
@@ -605,6 +658,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 }
                 if (ok && pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
                 if (ok && SIDE == kSideK) tc_commit(&bars[W_ACCDONE]);
+                if (trc) {
+                    mtr[BT_M_TOTAL - 8] = clock64() - t_start;
+                    for (int i = 0; i < 8; ++i) tr[8 + i] = mtr[i];
+                }
                 // every MMA issued completes before TMEM is released
                 tc_commit(&bars[W_DRAIN]);
                 mbar_wait_until(&bars[W_DRAIN], 0, global_timer_ns() + 500000000ull);
@@ -628,6 +685,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         kc.q0 = make_float2(0.5f * a.half_scale, 0.5f * a.half_scale);
         kc.lam = make_float2(a.lambda, a.lambda);
         float2 dl2 = make_float2(0.f, 0.f);
+        const bool etr = tr != nullptr && threadIdx.x == 0;
+        long long etr_[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};   // slots 16..31
         bool ok = true;
         int t = 0;
         uint8_t *outb = sm + L::kOut;
@@ -636,18 +695,20 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             const int h = h0 + hi;
             // query side: minus this row's base-2 log-sum-exp (-inf past n) and D
             float2 nl_r = make_float2(-CUDART_INF_F, -CUDART_INF_F), nd_r = make_float2(0.f, 0.f);
-            if (SIDE == kSideQ && row < a.n) {
-                const int64_t x = ((int64_t)b * a.Hq + h) * a.n + row;
-                const float l2 = -a.lse[x] * kLog2e, dd = -a.Dd[x];
+            if (SIDE == kSideQ) {   // rows below npad: -inf and 0 past n
+                const int64_t x = ((int64_t)b * a.Hq + h) * a.npad + row;
+                const float l2 = a.nl2[x], dd = a.nD[x];
                 nl_r = make_float2(l2, l2);
                 nd_r = make_float2(dd, dd);
             }
             for (int v = 0; ok && v < ncol; ++v, ++t) {
                 const BwTile x = bw_tile<SIDE, BC>(v, r0, rend, a.n, a.window);
-                ok = mbar_wait(&bars[W_SFULL], t & 1, abort_flag, a.status);
+                ok = mbar_wait_t(&bars[W_SFULL], t & 1, abort_flag, a.status, etr,
+                                 etr_[BT_E_SFULL - 16]);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                long long te = etr ? clock64() : 0;
                 float f[3 * HC];   // S, A, dP of this row's HC columns
                 const uint32_t cc = wg * HC;
                 if constexpr (HC == 32)
@@ -659,7 +720,15 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[W_SFREE]);   // S, A, dP may be overwritten
-                const float *vl = vec + (t % NS) * 2 * BC + wg * HC;   // key side
+                if (etr) {
+                    const long long t2 = clock64();
+                    etr_[BT_E_TMEM - 16] += t2 - te;
+                    te = t2;
+                }
+                // key side: the stage's -lse2 and -D, from this warpgroup's columns
+                const float *vl = reinterpret_cast<const float *>(
+                                      sm + L::kC + (t % NS) * L::kStage + 2 * L::kColT + L::kColG) +
+                                  wg * HC;
                 uint32_t pkP[HC / 2], pkT[HC / 2], pkA[HC / 2];
                 const int dlt = row - x.c0;   // the row against the tile's first column
                 const int loc = SIDE == kSideQ ? dlt - a.window : dlt + a.window;
@@ -671,31 +740,50 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                              dlt, loc, pkP, pkT, pkA, dl2);
                 // the operand tiles are free once the previous tile's gradient
                 // products are done
-                if (t > 0) ok = mbar_wait(&bars[W_PEMPTY], (t - 1) & 1, abort_flag, a.status);
+                if (etr) {
+                    const long long t2 = clock64();
+                    etr_[BT_E_MATH - 16] += t2 - te;
+                    te = t2;
+                }
+                if (t > 0)
+                    ok = mbar_wait_t(&bars[W_PEMPTY], (t - 1) & 1, abort_flag, a.status, etr,
+                                     etr_[BT_E_PEMPTY - 16]);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                // row r, columns [wg HC, wg HC + HC): 16-byte units u of the
-                // 128-byte row at (u xor (r mod 8))
-                const uint32_t rowoff = (uint32_t)r * 128u;
+                if constexpr (SIDE == kSideQ) {
+                    // dT and da into TMEM: this row's HC keys as HC / 2 pairs
+                    tmem_st16u(trow + L::kOutTm + wg * (HC / 2), pkT);
+                    if (x.gated) tmem_st16u(trow + L::kOutAm + wg * (HC / 2), pkA);
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    // row r, columns [wg HC, wg HC + HC): 16-byte units u of the
+                    // 128-byte row at (u xor (r mod 8))
+                    const uint32_t rowoff = (uint32_t)r * 128u;
 #pragma unroll
-                for (int q = 0; q < HC / 8; ++q) {
-                    const uint32_t u = (uint32_t)(wg * (HC / 8) + q);
-                    const uint32_t off = rowoff + ((u ^ (uint32_t)(r & 7)) << 4);
-                    if (SIDE == kSideK)
-                        st_shared_v4(smem_u32(oP + off), pkP[4 * q], pkP[4 * q + 1], pkP[4 * q + 2],
-                                     pkP[4 * q + 3]);
-                    st_shared_v4(smem_u32(oT + off), pkT[4 * q], pkT[4 * q + 1], pkT[4 * q + 2],
-                                 pkT[4 * q + 3]);
-                    if (x.gated)   // the dG product runs on gated tiles only
-                        st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1],
-                                     pkA[4 * q + 2], pkA[4 * q + 3]);
+                    for (int q = 0; q < HC / 8; ++q) {
+                        const uint32_t u = (uint32_t)(wg * (HC / 8) + q);
+                        const uint32_t off = rowoff + ((u ^ (uint32_t)(r & 7)) << 4);
+                        st_shared_v4(smem_u32(oP + off), pkP[4 * q], pkP[4 * q + 1],
+                                     pkP[4 * q + 2], pkP[4 * q + 3]);
+                        st_shared_v4(smem_u32(oT + off), pkT[4 * q], pkT[4 * q + 1],
+                                     pkT[4 * q + 2], pkT[4 * q + 3]);
+                        if (x.gated)   // the dG product runs on gated tiles only
+                            st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1],
+                                         pkA[4 * q + 2], pkA[4 * q + 3]);
+                    }
+                    fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
                 }
-                fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[W_PFULL]);
+                if (etr) {
+                    etr_[BT_E_STORE - 16] += clock64() - te;
+                    etr_[BT_E_TILES - 16] += 1;
+                }
                 if (SIDE == kSideQ && v == ncol - 1) {
                     // dQ of head h is complete: this row's half of its columns
-                    ok = mbar_wait(&bars[W_ACCDONE], hi & 1, abort_flag, a.status);
+                    ok = mbar_wait_t(&bars[W_ACCDONE], hi & 1, abort_flag, a.status, etr,
+                                     etr_[BT_E_ACCDONE - 16]);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -718,7 +806,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         }
         // ---- the CTA's accumulators
         if (ok && SIDE == kSideK) {
-            ok = mbar_wait(&bars[W_ACCDONE], 0, abort_flag, a.status);
+            ok = mbar_wait_t(&bars[W_ACCDONE], 0, abort_flag, a.status, etr,
+                             etr_[BT_E_ACCDONE - 16]);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
@@ -763,6 +852,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     for (int q = 0; q < 32; ++q)
                         if (col0 + q < a.Kg) dst[col0 + q] = o[q];
             }
+        }
+        if (etr) {
+            etr_[BT_E_TOTAL - 16] = clock64() - t_start;
+            for (int i = 0; i < 16; ++i) tr[16 + i] = etr_[i];
         }
         if (SIDE == kSideQ) {
             // d lambda: this CTA's partial, the EW warps' sums in a fixed order
@@ -865,8 +958,8 @@ cudaError_t gated_bwd_tc_prepare(const GatedLaunch &p, const __half *g16, int kp
     return cudaSuccess;
 }
 
-cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, float *dlam_part,
-                                float *dg_part, cudaStream_t s, int *launches)
+cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *rowv, int npad,
+                                float *dlam_part, float *dg_part, cudaStream_t s, int *launches)
 {
     const GatedLaunch &p = plan.p;
     BwArgs a;
@@ -884,16 +977,20 @@ cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, floa
     a.half_scale = 0.5f * p.scale;
     a.half_lambda = 0.5f * p.lambda;
     a.lambda = p.lambda;
-    a.lse = p.lse;
-    a.Dd = Dd;
+    a.nl2 = rowv;
+    a.nD = rowv + (size_t)p.B * p.Hq * npad;
+    a.npad = npad;
     a.dq = p.dq;
     a.dk = p.dk;
     a.dv = p.dv;
     a.dg_part = dg_part;
     a.dlam_part = dlam_part;
     a.status = p.wc.status;
+    a.trace = nullptr;
+    a.trace_ctas = 0;
     cudaError_t e;
     const bool two = p.Kg > 64;
+    gated_trace_buffer(0, &a.trace, &a.trace_ctas);
     prof_begin("gated_bwd_dq", s);
     if (p.d == 64)
         e = two ? bw_launch_t<kSideQ, 64, 2, 64>(plan, a, s)
@@ -904,6 +1001,7 @@ cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, floa
     prof_end(s);
     if (e != cudaSuccess) return e;
     *launches += 1;
+    gated_trace_buffer(1, &a.trace, &a.trace_ctas);
     prof_begin("gated_bwd_dkv", s);
     if (p.d == 64)
         e = two ? bw_launch_t<kSideK, 64, 2, 64>(plan, a, s)

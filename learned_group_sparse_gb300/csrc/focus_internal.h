@@ -62,6 +62,9 @@ void set_last_launches(int launches);
 // Wait-time trace buffer of an attention mode (0 group, 1 window, 2 dense)
 // for launches from this host thread, or nullptr (see focus_trace_attention).
 long long *trace_buffer(int mode);
+// Trace buffer of the gated backward's query side (0) or key side (1) for
+// launches from this host thread: nullptr, or the buffer and its CTA count.
+void gated_trace_buffer(int side, long long **buf, int *ctas);
 
 struct AssignLaunch {
     const __nv_bfloat16 *X;
@@ -199,7 +202,8 @@ struct GatedTcPlan {
 cudaError_t gated_tc_preflight(int d, int Kg);
 // The tensor-core backward (focus_gated_bwd_tc.cu): the query-side and
 // key-side kernels' attributes and TMA maps (enqueues nothing), then their
-// launches, given D = dO . O and the partial buffers of d lambda and dG.
+// launches, given -lse log2(e) and -dO . O in rows padded to npad (rowv,
+// [2][B, Hq, npad]) and the partial buffers of d lambda and dG.
 struct GatedBwTcPlan {
     CUtensorMap map[12];   // query side: Q, dO, G_q, K, V, G_k; key side: K, V, G_k, Q, dO, G_q
     GatedLaunch p;
@@ -208,8 +212,8 @@ struct GatedBwTcPlan {
 cudaError_t gated_bwd_tc_preflight(int d, int Kg);
 cudaError_t gated_bwd_tc_prepare(const GatedLaunch &p, const __half *g16, int kp,
                                  GatedBwTcPlan *plan);
-cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *Dd, float *dlam_part,
-                                float *dg_part, cudaStream_t s, int *launches);
+cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *rowv, int npad,
+                                float *dlam_part, float *dg_part, cudaStream_t s, int *launches);
 int gated_bwd_tc_dlam_count(int B, int n, int Hq);
 cudaError_t gated_tc_prepare(const GatedLaunch &p, const __half *g16, int kp, GatedTcPlan *plan);
 cudaError_t gated_tc_launch(const GatedTcPlan &plan, cudaStream_t s, int *launches);

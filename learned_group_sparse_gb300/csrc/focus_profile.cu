@@ -40,10 +40,18 @@ struct Profiler {
 
 thread_local Profiler g_prof;
 thread_local long long *g_trace[3] = {nullptr, nullptr, nullptr};
+thread_local long long *g_gtrace[2] = {nullptr, nullptr};
+thread_local int g_gtrace_ctas = 0;
 
 }  // namespace
 
 long long *trace_buffer(int mode) { return (mode >= 0 && mode < 3) ? g_trace[mode] : nullptr; }
+
+void gated_trace_buffer(int side, long long **buf, int *ctas)
+{
+    *buf = (side == 0 || side == 1) ? g_gtrace[side] : nullptr;
+    *ctas = *buf ? g_gtrace_ctas : 0;
+}
 
 void prof_begin(const char *name, cudaStream_t s)
 {
@@ -75,6 +83,13 @@ void focus_trace_attention(long long *group_buf, long long *window_buf, long lon
     g_trace[0] = group_buf;
     g_trace[1] = window_buf;
     g_trace[2] = dense_buf;
+}
+
+void focus_trace_gated(long long *query_buf, long long *key_buf, int max_ctas)
+{
+    g_gtrace[0] = max_ctas > 0 ? query_buf : nullptr;
+    g_gtrace[1] = max_ctas > 0 ? key_buf : nullptr;
+    g_gtrace_ctas = max_ctas > 0 ? max_ctas : 0;
 }
 
 int focus_profile_read(char *names, int name_stride, double *total_ms, int *launches,
