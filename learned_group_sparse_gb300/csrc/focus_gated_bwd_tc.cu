@@ -22,12 +22,12 @@
 //   S = R1 C1^T (q . k, bf16),  A = RG CG^T (g . g, fp16; skipped when every
 //   pair of the tile is local),  dP = R2 C2^T (dO . v, bf16)
 // with R1, R2, RG the CTA's Q, dO, G_q (query side) or K, V, G_k (key side)
-// and C1, C2, CG the streamed tile's K, V, G_k or Q, dO, G_q.  Two
-// warpgroups, one per half of the tile's columns (a thread per row), read
+// and C1, C2, CG the streamed tile's K, V, G_k or Q, dO, G_q.  Four
+// warpgroups, one per quarter of the tile's columns (a thread per row), read
 // them with one TMEM load, release S for the next tile's products, and write
-// P, dT and da as bf16 / fp16 operand tiles (128-byte-swizzled rows) into
-// shared memory; the thread then issues the gradient products into TMEM
-// accumulators:
+// P, dT and da as bf16 / fp16 operands (the query side into TMEM, the key
+// side as 128-byte-swizzled tiles in shared memory); the thread then issues
+// the gradient products into TMEM accumulators:
 //   query side: dQ += dT C1,  dG_q += da CG
 //   key side:   dV += P^T C2,  dK += dT^T C1,  dG_k += da^T CG
 // The streamed tiles serve K-major (as the B operand of S, A, dP) and
@@ -50,14 +50,17 @@ namespace {
 
 enum { kSideQ = 0, kSideK = 1 };
 constexpr int kBR = 128;            // the CTA's own rows (TMEM lanes)
-constexpr int kBwThreads = 384;     // 8 elementwise warps, the producer, the MMA thread, 2 idle
-constexpr int kBwProducer = 8;
-constexpr int kBwMma = 9;
-// Registers per thread after the split: elementwise warpgroups / the third
-// one.  256 * kBwRegsEw + 128 * kBwRegsOther must not exceed the launch's
-// kBwThreads * (registers per thread at launch), which the preflight checks.
-constexpr int kBwRegsEw = 216;
-constexpr int kBwRegsOther = 72;
+constexpr int kEwGroups = 4;        // elementwise warpgroups: a quarter of a tile's columns each
+constexpr int kEwWarps = 4 * kEwGroups;
+constexpr int kBwThreads = 32 * kEwWarps + 128;   // + the producer, the MMA thread, 2 idle
+constexpr int kBwProducer = kEwWarps;
+constexpr int kBwMma = kEwWarps + 1;
+// Registers per thread after the split: elementwise warpgroups / the last
+// one.  32 kEwWarps * kBwRegsEw + 128 * kBwRegsOther must not exceed the
+// launch's kBwThreads * (registers per thread at launch), which the
+// preflight checks.
+constexpr int kBwRegsEw = 96;
+constexpr int kBwRegsOther = 88;
 constexpr int kBwHeadChunk = 4;     // query heads per query-side CTA (one dG partial each)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -67,11 +70,14 @@ enum {
 };
 
 // Shared memory and TMEM columns of one CTA.  BC: rows of a streamed tile
-// (64; 32 on the key side for d 128 with K_g > 64, where the accumulators
-// need 384 TMEM columns).  The query side keeps its operand tiles dT and da
-// in TMEM (bf16 / fp16 pairs, 32 columns each) and streams through three
-// stages where they fit; the key side, whose accumulators fill TMEM, keeps
-// P, dT and da in shared memory and streams through two.
+// (64; 32 on the key side for d 128 with K_g > 64, whose accumulators dV, dK
+// and dG_k take 2 d + 64 KPC TMEM columns; a 32-row tile halves the work of
+// each MMA against the same reads of the CTA's own 128-row operands, so the
+// 64-row tile is kept wherever TMEM allows).  The operands P, dT and da sit in
+// TMEM (bf16 / fp16 pairs, BC / 2 columns each) where the columns allow,
+// else as 128-byte-swizzled tiles in shared memory (key side with d 128 and
+// K_g > 64); the streamed tiles pass through as many stages (up to four) as
+// shared memory holds.
 template <int SIDE, int D, int KPC, int BC>
 struct BwLayout {
     static constexpr uint32_t kRowT = kBR * D * 2;        // R1 or R2: D/64 chunks of 16 KB
@@ -81,10 +87,22 @@ struct BwLayout {
     // key side: -lse2 and -D of the tile's queries (2 BC floats, in 1 KB)
     static constexpr uint32_t kVecB = SIDE == kSideK ? 1024 : 0;
     static constexpr uint32_t kStage = 2 * kColT + kColG + kVecB;
+    // TMEM columns: S, A, dP, the accumulators, then the operands
+    static constexpr uint32_t kColS = 0, kColA = BC, kColP = 2 * BC, kAcc = 3 * BC;
+    static constexpr uint32_t kAccG = kAcc + (SIDE == kSideK ? 2 * D : D);
+    static constexpr int kNOpd = SIDE == kSideK ? 3 : 2;   // [P,] dT, da
+    static constexpr uint32_t kOutM = kAccG + 64 * KPC;
+    static constexpr bool kTmemOut = kOutM + kNOpd * (BC / 2) <= 512;
+    static constexpr uint32_t kOutPm = kOutM;                                   // key side: P
+    static constexpr uint32_t kOutTm = kOutM + (SIDE == kSideK ? BC / 2 : 0);  // dT
+    static constexpr uint32_t kOutAm = kOutTm + BC / 2;                        // da
+    // shared memory
     static constexpr uint32_t kOutT = kBR * 128;          // an operand tile: 128 rows of 128 bytes
-    static constexpr int kNOut = SIDE == kSideK ? 3 : 0;  // P, dT, da (key side)
-    static constexpr uint32_t kFixed = 2 * kRowT + kRowG + kNOut * kOutT + 1024 + 1024;
-    static constexpr int NS = (SIDE == kSideQ && kFixed + 3 * kStage <= 232448) ? 3 : 2;
+    static constexpr int kNOut = kTmemOut ? 0 : kNOpd;    // operand tiles in shared memory
+    static constexpr uint32_t kFixed = 2 * kRowT + kRowG + kNOut * kOutT + 2048;
+    static constexpr int NS = kFixed + 4 * kStage <= 232448   ? 4
+                              : kFixed + 3 * kStage <= 232448 ? 3
+                                                              : 2;
     static constexpr uint32_t kR1 = 0;
     static constexpr uint32_t kR2 = kR1 + kRowT;
     static constexpr uint32_t kRG = kR2 + kRowT;
@@ -92,14 +110,9 @@ struct BwLayout {
     static constexpr uint32_t kC = kOut + kNOut * kOutT;  // stages: C1, C2, CG[, vec]
     static constexpr uint32_t kBar = kC + NS * kStage;
     static constexpr uint32_t kMisc = kBar + kWBars * 8;    // TMEM base, abort flag
-    static constexpr uint32_t kRed = kMisc + 16;            // 8 floats
-    static constexpr uint32_t kBytes = kRed + 32 + 1024;    // + alignment slack
-    // TMEM columns
-    static constexpr uint32_t kColS = 0, kColA = BC, kColP = 2 * BC, kAcc = 3 * BC;
-    static constexpr uint32_t kAccG = kAcc + (SIDE == kSideK ? 2 * D : D);
-    static constexpr uint32_t kOutTm = kAccG + 64 * KPC;   // query side: dT, then da
-    static constexpr uint32_t kOutAm = kOutTm + BC / 2;
-    static_assert(kAccG + 64 * KPC + (SIDE == kSideQ ? BC : 0) <= 512, "TMEM columns");
+    static constexpr uint32_t kRed = kMisc + 16;            // a float per elementwise warp
+    static constexpr uint32_t kBytes = kRed + 4 * kEwWarps + 1024;   // + alignment slack
+    static_assert(kOutM <= 512 && (kTmemOut || SIDE == kSideK), "TMEM columns");
     static_assert(kBytes <= 232448, "shared memory per CTA");
     static_assert(kStage % 1024 == 0, "stage alignment");
 };
@@ -167,39 +180,8 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N)
     return idesc_f16_f32(M, N) | (1u << 16);
 }
 
-// Loads 32 consecutive fp32 columns of this thread's TMEM lane at each of
-// 3 addresses (one wait for all): v[32 * l + c] = column c at a_l.
-__device__ __forceinline__ void tmem_ld3x32(uint32_t a0, uint32_t a1, uint32_t a2, float *v)
-{
-    uint32_t r[96];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%96];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%97];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
-          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
-          "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]),
-          "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]),
-          "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]),
-          "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]),
-          "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]),
-          "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95])
-        : "r"(a0), "r"(a1), "r"(a2)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 96; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// The same with 16 columns at each address: v[16 * l + c].
+// Loads 16 consecutive fp32 columns of this thread's TMEM lane at each of
+// 3 addresses (one wait for all): v[16 * l + c] = column c at a_l.
 __device__ __forceinline__ void tmem_ld3x16(uint32_t a0, uint32_t a1, uint32_t a2, float *v)
 {
     uint32_t r[48];
@@ -220,6 +202,57 @@ __device__ __forceinline__ void tmem_ld3x16(uint32_t a0, uint32_t a1, uint32_t a
         : "memory");
 #pragma unroll
     for (int i = 0; i < 48; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The same with 8 columns at each address: v[8 * l + c].
+__device__ __forceinline__ void tmem_ld3x8(uint32_t a0, uint32_t a1, uint32_t a2, float *v)
+{
+    uint32_t r[24];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Loads NC (a multiple of 16) consecutive fp32 columns of this thread's TMEM
+// lane and waits.
+template <int NC>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float *v)
+{
+    if constexpr (NC % 32 == 0) {
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) tmem_ld32(taddr + 32 * c, v + 32 * c);
+    } else {
+#pragma unroll
+        for (int c = 0; c < NC / 16; ++c) tmem_ld16(taddr + 16 * c, v + 16 * c);
+    }
+}
+
+// Stores 4 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st4u(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+
+// Stores 8 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7])
+                 : "memory");
 }
 
 // Stores 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
@@ -383,7 +416,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
 {
     using L = BwLayout<SIDE, D, KPC, BC>;
     constexpr int kChunks = D / 64;
-    constexpr int HC = BC / 2;          // columns per elementwise warpgroup
+    constexpr int HC = BC / kEwGroups;  // columns per elementwise warpgroup
     constexpr int NS = L::NS;
 
     extern __shared__ uint8_t smem_raw[];
@@ -428,11 +461,11 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             mbar_init(&bars[W_CEMPTY + s], 1);
         }
         mbar_init(&bars[W_SFULL], 1);
-        mbar_init(&bars[W_SFREE], 8);
-        mbar_init(&bars[W_PFULL], 8);
+        mbar_init(&bars[W_SFREE], kEwWarps);
+        mbar_init(&bars[W_PFULL], kEwWarps);
         mbar_init(&bars[W_PEMPTY], 1);
         mbar_init(&bars[W_ACCDONE], 1);
-        mbar_init(&bars[W_ACCFREE], 8);
+        mbar_init(&bars[W_ACCFREE], kEwWarps);
         mbar_init(&bars[W_DRAIN], 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -456,7 +489,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     // (set-up above touches no global memory; launched with launch_pdl)
     grid_dep_sync();
 
-    if (warp >= 8) {
+    if (warp >= kEwWarps) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwRegsOther));
         if (warp == kBwProducer) {
             // --------------------------------------------------------- producer
@@ -581,11 +614,17 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     for (int kk = 0; kk < BC / 16; ++kk) {
                         // A: 32 bytes further along the rows; B: 16 rows of 128 bytes further
                         const uint32_t ao = kk * 2, bo = kk * 128;
+                        // operands in TMEM: 16 rows of the streamed tile = 8 columns per step
                         if (SIDE == kSideQ) {
-                            // dT in TMEM: 16 keys = 8 columns per step
                             const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
                             tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutTm + kk * 8, c1 + bo,
                                                    kIdAcc, acc);
+                        } else if constexpr (L::kTmemOut) {
+                            const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
+                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutPm + kk * 8, c2 + bo,
+                                                   kIdAcc, acc);
+                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc + D, tmem + L::kOutTm + kk * 8,
+                                                   c1 + bo, kIdAcc, acc);
                         } else {
                             const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
                             bw_mma<kHi, kHi>(tmem + L::kAcc, outP + ao, c2 + bo, kIdAcc, acc);
@@ -596,7 +635,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < BC / 16; ++kk) {
                             const uint32_t acc = (kk > 0 || dg_started) ? 1u : 0u;
-                            if (SIDE == kSideQ)
+                            if (L::kTmemOut)
                                 tc_mma_bf16_ts_lo<kHi>(tmem + L::kAccG, tmem + L::kOutAm + kk * 8,
                                                        cg + kk * 128, kIdG, acc);
                             else
@@ -671,7 +710,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwRegsEw));
         // ------------------------------------- elementwise (warps 0-7)
-        const int wg = warp >> 2;                 // half of the tile's columns
+        const int wg = warp >> 2;                 // quarter of the tile's columns
         const int r = (warp & 3) * 32 + lane;     // own row = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int row = r0 + r;                   // query (query side) or key (key side)
@@ -711,12 +750,11 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 long long te = etr ? clock64() : 0;
                 float f[3 * HC];   // S, A, dP of this row's HC columns
                 const uint32_t cc = wg * HC;
-                if constexpr (HC == 32)
-                    tmem_ld3x32(trow + L::kColS + cc, trow + L::kColA + cc, trow + L::kColP + cc,
-                                f);
-                else
+                if constexpr (HC == 16)
                     tmem_ld3x16(trow + L::kColS + cc, trow + L::kColA + cc, trow + L::kColP + cc,
                                 f);
+                else
+                    tmem_ld3x8(trow + L::kColS + cc, trow + L::kColA + cc, trow + L::kColP + cc, f);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[W_SFREE]);   // S, A, dP may be overwritten
@@ -750,10 +788,19 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                      etr_[BT_E_PEMPTY - 16]);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if constexpr (SIDE == kSideQ) {
-                    // dT and da into TMEM: this row's HC keys as HC / 2 pairs
-                    tmem_st16u(trow + L::kOutTm + wg * (HC / 2), pkT);
-                    if (x.gated) tmem_st16u(trow + L::kOutAm + wg * (HC / 2), pkA);
+                if constexpr (L::kTmemOut) {
+                    // [P,] dT and da into TMEM: this row's HC columns as HC / 2 pairs
+                    static_assert(HC == 8 || HC == 16, "4 or 8 TMEM columns per operand");
+                    const uint32_t tc = trow + wg * (HC / 2);
+                    if constexpr (HC == 16) {
+                        if (SIDE == kSideK) tmem_st8u(tc + L::kOutPm, pkP);
+                        tmem_st8u(tc + L::kOutTm, pkT);
+                        if (x.gated) tmem_st8u(tc + L::kOutAm, pkA);
+                    } else {
+                        if (SIDE == kSideK) tmem_st4u(tc + L::kOutPm, pkP);
+                        tmem_st4u(tc + L::kOutTm, pkT);
+                        if (x.gated) tmem_st4u(tc + L::kOutAm, pkA);
+                    }
                     tmem_st_wait();
                     tc_fence_before();
                 } else {
@@ -781,23 +828,21 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     etr_[BT_E_TILES - 16] += 1;
                 }
                 if (SIDE == kSideQ && v == ncol - 1) {
-                    // dQ of head h is complete: this row's half of its columns
+                    // dQ of head h is complete: this row's quarter of its columns
                     ok = mbar_wait_t(&bars[W_ACCDONE], hi & 1, abort_flag, a.status, etr,
                                      etr_[BT_E_ACCDONE - 16]);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
-                    float *dst = a.dq + (((int64_t)b * a.n + row) * a.Hq + h) * D + wg * (D / 2);
+                    constexpr int QC = D / kEwGroups;
+                    float o[QC];
+                    tmem_ldn<QC>(trow + L::kAcc + wg * QC, o);
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.dq + (((int64_t)b * a.n + row) * a.Hq + h) * D + wg * QC);
+                    if (row < a.n)
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[32];
-                        tmem_ld32(trow + L::kAcc + wg * (D / 2) + 32 * c, o);
-                        if (row < a.n)
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                reinterpret_cast<float4 *>(dst + 32 * c)[q] =
-                                    make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                    }
+                        for (int q = 0; q < QC / 4; ++q)
+                            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[W_ACCFREE]);
@@ -814,44 +859,38 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             tc_fence_after();
             const bool valid = row < a.n;
             if (SIDE == kSideK) {
-                // dV and dK: this row's half of the D columns of each
-                const int64_t base = (((int64_t)b * a.n + row) * a.Hkv + kvh0) * D + wg * (D / 2);
+                // dV and dK: this row's quarter of the D columns of each
+                constexpr int QC = D / kEwGroups;
+                const int64_t base = (((int64_t)b * a.n + row) * a.Hkv + kvh0) * D + wg * QC;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    float *dst = (m == 0 ? a.dv : a.dk) + base;
+                    float o[QC];
+                    tmem_ldn<QC>(trow + L::kAcc + m * D + wg * QC, o);
+                    float4 *dst = reinterpret_cast<float4 *>((m == 0 ? a.dv : a.dk) + base);
+                    if (valid)
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[32];
-                        tmem_ld32(trow + L::kAcc + m * D + wg * (D / 2) + 32 * c, o);
-                        if (valid)
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                reinterpret_cast<float4 *>(dst + 32 * c)[q] = make_float4(
-                                    o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                    }
+                        for (int q = 0; q < QC / 4; ++q)
+                            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                 }
             }
-            // the dG partial: this row's half of the 64 KPC columns (zero when
-            // no pair of the CTA is gated)
+            // the dG partial: this row's quarter of the 64 KPC columns (zero
+            // when no pair of the CTA is gated)
             const bool any_gated = SIDE == kSideQ ? (rend - 1 >= a.window)
                                                   : (a.n - 1 - r0 >= a.window);
             const int part = SIDE == kSideQ ? blockIdx.y : a.nhc + kvh0;
             float *dst = a.dg_part + ((int64_t)part * a.B * a.n + (int64_t)b * a.n + row) * a.Kg;
+            constexpr int GC = 64 * KPC / kEwGroups;
+            float o[GC];
+            if (any_gated) {
+                tmem_ldn<GC>(trow + L::kAccG + wg * GC, o);
+            } else {
 #pragma unroll
-            for (int c = 0; c < KPC; ++c) {
-                float o[32];
-                if (any_gated) {
-                    tmem_ld32(trow + L::kAccG + wg * 32 * KPC + 32 * c, o);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = 0.f;
-                }
-                const int col0 = wg * 32 * KPC + 32 * c;
-                if (valid)
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (col0 + q < a.Kg) dst[col0 + q] = o[q];
+                for (int q = 0; q < GC; ++q) o[q] = 0.f;
             }
+            if (valid)
+#pragma unroll
+                for (int q = 0; q < GC; ++q)
+                    if (wg * GC + q < a.Kg) dst[wg * GC + q] = o[q];
         }
         if (etr) {
             etr_[BT_E_TOTAL - 16] = clock64() - t_start;
@@ -863,10 +902,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, off);
             if (lane == 0) red[warp] = dlam;
-            named_bar_sync(1, 256);
+            named_bar_sync(1, 32 * kEwWarps);
             if (threadIdx.x == 0 && !*abort_flag) {
                 float s = 0.f;
-                for (int w = 0; w < 8; ++w) s += red[w];
+                for (int w = 0; w < kEwWarps; ++w) s += red[w];
                 const int qt = gridDim.x - 1 - blockIdx.x;
                 a.dlam_part[((int64_t)b * a.nhc + blockIdx.y) * a.nqt + qt] = s;
             }
@@ -891,7 +930,7 @@ cudaError_t bw_preflight_t()
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
     // the warpgroups' shares after setmaxnreg must fit in the launch's registers
-    if ((int64_t)fa.numRegs * kBwThreads < 256 * kBwRegsEw + 128 * kBwRegsOther)
+    if ((int64_t)fa.numRegs * kBwThreads < 32 * kEwWarps * kBwRegsEw + 128 * kBwRegsOther)
         return cudaErrorInvalidConfiguration;
     return cudaSuccess;
 }
@@ -908,7 +947,8 @@ cudaError_t bw_launch_t(const GatedBwTcPlan &plan, const BwArgs &a, cudaStream_t
                       plan.map[m + 2], plan.map[m + 3], plan.map[m + 4], plan.map[m + 5], a);
 }
 
-// The key side's streamed tile: 32 query rows for d 128 with K_g > 64.
+// The key side's streamed tile: 64 query rows, 32 for d 128 with K_g > 64
+// (TMEM columns for the accumulators).
 inline int bw_key_bc(int d, int Kg) { return (d == 128 && Kg > 64) ? 32 : 64; }
 
 }  // namespace
