@@ -338,13 +338,13 @@ struct EwConst {
 // One elementwise pass over this row's HC columns of a tile: from S, A, dP
 // (f[0..HC), f[HC..2HC), f[2HC..3HC)) and the columns' or the row's
 // -lse2 and -D (nl, nd), the packed P, dT and (GATED) da.  Column c of the
-// tile is causal iff c <= lim (query side) / c >= lim (key side), and gated
-// iff c <= loc / c >= loc (tested only where the tile needs it).
-template <int SIDE, int HC, bool GATED>
+// tile is causal iff c <= lim (query side) / c >= lim (key side), tested
+// when CAUSAL (a tile across the diagonal), and gated iff c <= loc /
+// c >= loc, tested when EDGE (a gated tile across the window's edge).
+template <int SIDE, int HC, bool GATED, bool EDGE, bool CAUSAL>
 __device__ __forceinline__ void ew_tile(const float *f, const float *vl, int BC, float2 nl_r,
-                                        float2 nd_r, const EwConst &k, bool allg, bool causal,
-                                        int cb, int lim, int loc, uint32_t *pkP, uint32_t *pkT,
-                                        uint32_t *pkA, float2 &dl2)
+                                        float2 nd_r, const EwConst &k, int cb, int lim, int loc,
+                                        uint32_t *pkP, uint32_t *pkT, uint32_t *pkA, float2 &dl2)
 {
 #pragma unroll
     for (int e = 0; e < HC; e += 2) {
@@ -363,7 +363,7 @@ __device__ __forceinline__ void ew_tile(const float *f, const float *vl, int BC,
             g2 = fma2v(th, k.hs2, k.hs2);                 // scale log2(e) sigma
             g1 = fma2v(th, k.hs, k.hs);                   // scale sigma
             sps = fma2v(mul2v(th, k.q1), th, k.q0);       // scale sigma (1 - sigma)
-            if (!allg) {   // a tile across the window's edge: local pairs keep gate 1
+            if constexpr (EDGE) {   // a tile across the window's edge: local pairs keep gate 1
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int c = cb + e + q;
@@ -378,7 +378,7 @@ __device__ __forceinline__ void ew_tile(const float *f, const float *vl, int BC,
         }
         const float2 xx = fma2v(sv, g2, nl);
         float2 p = make_float2(bw_ex2(xx.x), bw_ex2(xx.y));
-        if (causal) {
+        if constexpr (CAUSAL) {
             const int c = cb + e;
             if (!(SIDE == kSideQ ? c <= lim : c >= lim)) p.x = 0.f;
             if (!(SIDE == kSideQ ? c + 1 <= lim : c + 1 >= lim)) p.y = 0.f;
@@ -770,12 +770,21 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 uint32_t pkP[HC / 2], pkT[HC / 2], pkA[HC / 2];
                 const int dlt = row - x.c0;   // the row against the tile's first column
                 const int loc = SIDE == kSideQ ? dlt - a.window : dlt + a.window;
-                if (x.gated)
-                    ew_tile<SIDE, HC, true>(f, vl, BC, nl_r, nd_r, kc, x.allg, x.causal, wg * HC,
-                                            dlt, loc, pkP, pkT, pkA, dl2);
-                else
-                    ew_tile<SIDE, HC, false>(f, vl, BC, nl_r, nd_r, kc, x.allg, x.causal, wg * HC,
-                                             dlt, loc, pkP, pkT, pkA, dl2);
+                // the tile's kind (uniform over the CTA): gated or not, across
+                // the window's edge, across the diagonal
+#define FOCUS_EW(G, E, C)                                                                       \
+    ew_tile<SIDE, HC, G, E, C>(f, vl, BC, nl_r, nd_r, kc, wg * HC, dlt, loc, pkP, pkT, pkA, dl2)
+                if (!x.gated) {
+                    if (x.causal) FOCUS_EW(false, false, true);
+                    else FOCUS_EW(false, false, false);
+                } else if (x.allg) {
+                    if (x.causal) FOCUS_EW(true, false, true);
+                    else FOCUS_EW(true, false, false);
+                } else {
+                    if (x.causal) FOCUS_EW(true, true, true);
+                    else FOCUS_EW(true, true, false);
+                }
+#undef FOCUS_EW
                 // the operand tiles are free once the previous tile's gradient
                 // products are done
                 if (etr) {
