@@ -93,12 +93,17 @@ struct BwLayout {
     static constexpr int kNOpd = SIDE == kSideK ? 3 : 2;   // [P,] dT, da
     static constexpr uint32_t kOutM = kAccG + 64 * KPC;
     static constexpr bool kTmemOut = kOutM + kNOpd * (BC / 2) <= 512;
-    static constexpr uint32_t kOutPm = kOutM;                                   // key side: P
-    static constexpr uint32_t kOutTm = kOutM + (SIDE == kSideK ? BC / 2 : 0);  // dT
-    static constexpr uint32_t kOutAm = kOutTm + BC / 2;                        // da
+    // Otherwise (key side with d 128): P and dT over the columns of A, which
+    // the elementwise pass has read by then (the next tile's A product is
+    // issued after this tile's gradient products), da in shared memory.
+    static constexpr bool kAOut = !kTmemOut;
+    static constexpr uint32_t kOutPm = kTmemOut ? kOutM : kColA;                     // key side: P
+    static constexpr uint32_t kOutTm =
+        kTmemOut ? kOutM + (SIDE == kSideK ? BC / 2 : 0) : kColA + BC / 2;          // dT
+    static constexpr uint32_t kOutAm = kOutTm + BC / 2;                              // da (TMEM)
     // shared memory
     static constexpr uint32_t kOutT = kBR * 128;          // an operand tile: 128 rows of 128 bytes
-    static constexpr int kNOut = kTmemOut ? 0 : kNOpd;    // operand tiles in shared memory
+    static constexpr int kNOut = kTmemOut ? 0 : 1;        // operand tiles in shared memory: da
     static constexpr uint32_t kFixed = 2 * kRowT + kRowG + kNOut * kOutT + 2048;
     static constexpr int NS = kFixed + 4 * kStage <= 232448   ? 4
                               : kFixed + 3 * kStage <= 232448 ? 3
@@ -590,9 +595,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 // streamed tiles: the leading offset is the MN-major chunk stride
                 // (unused by the K-major products)
                 const uint32_t cb = sdesc_lo(smem_u32(sm + L::kC), BC * 128);
-                const uint32_t ob = sdesc_lo(smem_u32(sm + L::kOut), 16);
-                const uint32_t outP = ob, outT = ob + (SIDE == kSideK ? (L::kOutT >> 4) : 0u);
-                const uint32_t outA = outT + (L::kOutT >> 4);
+                const uint32_t outA = sdesc_lo(smem_u32(sm + L::kOut), 16);   // da (kAOut)
                 int t = 0;
                 bool ok = true, dg_started = false;
                 const bool trc = tr != nullptr;
@@ -619,16 +622,12 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                             const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
                             tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutTm + kk * 8, c1 + bo,
                                                    kIdAcc, acc);
-                        } else if constexpr (L::kTmemOut) {
+                        } else {
                             const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
                             tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutPm + kk * 8, c2 + bo,
                                                    kIdAcc, acc);
                             tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc + D, tmem + L::kOutTm + kk * 8,
                                                    c1 + bo, kIdAcc, acc);
-                        } else {
-                            const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
-                            bw_mma<kHi, kHi>(tmem + L::kAcc, outP + ao, c2 + bo, kIdAcc, acc);
-                            bw_mma<kHi, kHi>(tmem + L::kAcc + D, outT + ao, c1 + bo, kIdAcc, acc);
                         }
                     }
                     if (gtd) {
@@ -675,7 +674,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                             bw_mma<kHi, kHi>(tmem + L::kColS, r1 + ro, c1 + co, kIdS, acc);
                             bw_mma<kHi, kHi>(tmem + L::kColP, r2 + ro, c2 + co, kIdS, acc);
                         }
-                        if (x.gated) {
+                        auto issue_a = [&]() {
+                            if (!x.gated) return;
 #pragma unroll
                             for (int ks = 0; ks < 4 * KPC; ++ks) {
                                 if (ks >= a.nks) break;
@@ -684,10 +684,21 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                 bw_mma<kHi, kHi>(tmem + L::kColA, rg + ro, cg + co, kIdA,
                                                  ks > 0 ? 1u : 0u);
                             }
+                        };
+                        if constexpr (L::kAOut) {
+                            // A's columns hold the previous tile's P and dT until its
+                            // gradient products are issued; the tensor pipe runs in
+                            // issue order
+                            if (pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
+                            if (!ok) break;
+                            issue_a();
+                            tc_commit(&bars[W_SFULL]);
+                        } else {
+                            issue_a();
+                            tc_commit(&bars[W_SFULL]);
+                            if (SIDE == kSideQ && v == ncol - 1) tc_commit(&bars[W_ROWEMPTY]);
+                            if (pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
                         }
-                        tc_commit(&bars[W_SFULL]);
-                        if (SIDE == kSideQ && v == ncol - 1) tc_commit(&bars[W_ROWEMPTY]);
-                        if (pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
                         pt = t;
                         p_gated = x.gated;
                         p_first = v == 0;
@@ -728,8 +739,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         long long etr_[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};   // slots 16..31
         bool ok = true;
         int t = 0;
-        uint8_t *outb = sm + L::kOut;
-        uint8_t *oP = outb, *oT = outb + (SIDE == kSideK ? L::kOutT : 0u), *oA = oT + L::kOutT;
+        uint8_t *oA = sm + L::kOut;   // da (kAOut)
         for (int hi = 0; ok && hi < nh; ++hi) {
             const int h = h0 + hi;
             // query side: minus this row's base-2 log-sum-exp (-inf past n) and D
@@ -813,22 +823,30 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     tmem_st_wait();
                     tc_fence_before();
                 } else {
-                    // row r, columns [wg HC, wg HC + HC): 16-byte units u of the
-                    // 128-byte row at (u xor (r mod 8))
-                    const uint32_t rowoff = (uint32_t)r * 128u;
+                    // P and dT over A's columns (read above), da as a tile in shared
+                    // memory: row r, columns [wg HC, wg HC + HC) as 16-byte units u
+                    // of the 128-byte row at (u xor (r mod 8))
+                    const uint32_t tc = trow + wg * (HC / 2);
+                    if constexpr (HC == 16) {
+                        tmem_st8u(tc + L::kOutPm, pkP);
+                        tmem_st8u(tc + L::kOutTm, pkT);
+                    } else {
+                        tmem_st4u(tc + L::kOutPm, pkP);
+                        tmem_st4u(tc + L::kOutTm, pkT);
+                    }
+                    if (x.gated) {   // the dG product runs on gated tiles only
+                        const uint32_t rowoff = (uint32_t)r * 128u;
 #pragma unroll
-                    for (int q = 0; q < HC / 8; ++q) {
-                        const uint32_t u = (uint32_t)(wg * (HC / 8) + q);
-                        const uint32_t off = rowoff + ((u ^ (uint32_t)(r & 7)) << 4);
-                        st_shared_v4(smem_u32(oP + off), pkP[4 * q], pkP[4 * q + 1],
-                                     pkP[4 * q + 2], pkP[4 * q + 3]);
-                        st_shared_v4(smem_u32(oT + off), pkT[4 * q], pkT[4 * q + 1],
-                                     pkT[4 * q + 2], pkT[4 * q + 3]);
-                        if (x.gated)   // the dG product runs on gated tiles only
+                        for (int q = 0; q < HC / 8; ++q) {
+                            const uint32_t u = (uint32_t)(wg * (HC / 8) + q);
+                            const uint32_t off = rowoff + ((u ^ (uint32_t)(r & 7)) << 4);
                             st_shared_v4(smem_u32(oA + off), pkA[4 * q], pkA[4 * q + 1],
                                          pkA[4 * q + 2], pkA[4 * q + 3]);
+                        }
+                        fence_proxy_async_smem();   // the MMA reads the tile through the async proxy
                     }
-                    fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
+                    tmem_st_wait();
+                    tc_fence_before();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[W_PFULL]);
