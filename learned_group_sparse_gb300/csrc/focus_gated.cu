@@ -63,29 +63,39 @@ __global__ void gated_g16_kernel(const float *__restrict__ G, int64_t rows, int 
     }
 }
 
-// The backward's per-(row, head) values, one warp each: -lse_i log2(e) and
+// The backward's per-(row, head) values, D / 8 lanes each (16 bytes of O and
+// of dO per lane): -lse_i log2(e) and
 // -D_i = -dO_i . O_i (bf16 inputs, fp32 sum), in rows padded to npad (-inf
 // and 0 past n) so that a kernel can copy any 64-row run of them whole.
 template <int D>
 __global__ void gated_bwd_prep_kernel(const GatedArgs a, float *__restrict__ rowv)
 {
+    constexpr int LPR = D / 8;   // lanes per (row, head): 16 bytes of O and of dO each
     grid_dep_sync();
-    const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= (int64_t)a.B * a.npad * a.Hq) return;
+    const int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int64_t w = g / LPR;
+    const int sub = (int)(g % LPR);
+    const bool live = w < (int64_t)a.B * a.npad * a.Hq;   // whole groups of LPR lanes
     const int64_t bi = w / a.Hq;     // b * npad + i
     const int h = (int)(w - bi * a.Hq);
     const int64_t b = bi / a.npad, i = bi - b * a.npad;
     float sum = 0.f;
-    if (i < a.n) {
-        const int64_t x = ((b * a.n + i) * a.Hq + h) * D;
-        const __nv_bfloat16 *o = a.o + x, *g = a.dO + x;
+    if (live && i < a.n) {
+        const int64_t x = ((b * a.n + i) * a.Hq + h) * D + sub * 8;
+        const uint4 ov = *reinterpret_cast<const uint4 *>(a.o + x);
+        const uint4 gv = *reinterpret_cast<const uint4 *>(a.dO + x);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-        for (int e = lane; e < D; e += 32) sum += __bfloat162float(o[e]) * __bfloat162float(g[e]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        for (int q = 0; q < 4; ++q) {
+            const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[q]));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[q]));
+            sum = fmaf(of.x, gf.x, sum);
+            sum = fmaf(of.y, gf.y, sum);
+        }
     }
-    if (lane == 0) {
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (live && sub == 0) {
         const int64_t y = (b * a.Hq + h) * a.npad + i;
         const int64_t plane = (int64_t)a.B * a.Hq * a.npad;
         rowv[y] = i < a.n ? -a.lse[(b * a.Hq + h) * a.n + i] * 1.4426950408889634f : -CUDART_INF_F;
@@ -106,16 +116,17 @@ __global__ void gated_dg_reduce_kernel(const GatedArgs a)
     }
 }
 
-// d lambda = sum of the query-tile partials, in a fixed order (one thread).
+// d lambda = sum of the query-tile partials, in a fixed order (one warp).
 __global__ void gated_dlam_kernel(const float *__restrict__ part, int count,
                                   float *__restrict__ out)
 {
     grid_dep_sync();
-    if (threadIdx.x == 0 && blockIdx.x == 0) {
-        double s = 0.0;
-        for (int x = 0; x < count; ++x) s += (double)part[x];
-        *out = (float)s;
-    }
+    // lane l sums partials l, l + 32, ... in double, then a fixed shuffle tree
+    double s = 0.0;
+    for (int x = threadIdx.x; x < count; x += 32) s += (double)part[x];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (threadIdx.x == 0) *out = (float)s;
 }
 
 }  // namespace
@@ -189,9 +200,10 @@ cudaError_t gated_bwd_t(const GatedLaunch &p, const GatedArgs &a, const GatedBwT
                         cudaStream_t s, int *launches)
 {
     cudaError_t e;
-    const int64_t warps = (int64_t)p.B * a.npad * p.Hq;
+    const int64_t warps = (int64_t)p.B * a.npad * p.Hq;   // (row, head) groups
     prof_begin("gated_bwd_prep", s);
-    e = launch_pdl(gated_bwd_prep_kernel<D>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256),
+    e = launch_pdl(gated_bwd_prep_kernel<D>, dim3((unsigned)((warps * (D / 8) + 255) / 256)),
+                   dim3(256),
                    0, s, a, const_cast<float *>(a.rowv));
     prof_end(s);
     if (e != cudaSuccess) return e;
