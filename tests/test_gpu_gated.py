@@ -64,6 +64,8 @@ CASES = [
     (1, 700, 4, 2, 64, 16, 200, 2.5),   # tiles wholly inside, across and outside the window
     (2, 150, 16, 2, 64, 48, 8, 3.0),    # GQA 8:1, two head chunks for dG
     (1, 390, 3, 1, 128, 64, 100, 2.0),  # GQA 3:1 (odd: consecutive query tiles share a CTA)
+    (2, 1100, 4, 2, 128, 64, 128, 2.5), # d 128, K_g 64 as in training: the streams wrap their
+                                        # stage rings many times, two heads per key-side CTA
 ]
 
 
