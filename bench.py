@@ -496,6 +496,16 @@ def main():
     t = synth.make_all(w, dev)
     B, n = w.B, w.n
     ntok = B * n
+    # pinned host copies of the inputs and the output for the end-to-end leg,
+    # allocated up front (the host's copy rate varies between runs: the same
+    # leg read 364 and 543 ms per step at n = 1M in two processes in a row)
+    host = Oh = None
+    if not args.no_e2e:
+        host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True)
+                for k in ("X", "Wg", "C", "Q", "K", "V")}
+        for k, v in host.items():
+            v.copy_(t[k])
+        Oh = torch.empty((B, n, w.Hq, w.d), dtype=torch.bfloat16, pin_memory=True)
     ids = torch.empty(B, n, w.topk, dtype=torch.int32, device=dev)
     O = torch.empty(B, n, w.Hq, w.d, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(fg.focus_prefill_workspace_size(B, n, w.hidden, w.Hq, w.Hkv, w.d, w.dg,
@@ -603,8 +613,6 @@ def main():
     # long at n = 1M, while a fresh process matches this position)
     e2e = None
     if not args.no_e2e:
-        host = {k: t[k].cpu().pin_memory() for k in ("X", "Wg", "C", "Q", "K", "V")}
-        Oh = torch.empty(O.shape, dtype=torch.bfloat16).pin_memory()
         wsh = torch.empty(fg.focus_prefill_workspace_size(B, n, w.hidden, w.Hq, w.Hkv, w.d,
                                                           w.dg, w.K, w.topk, True),
                           dtype=torch.uint8, device=dev)
