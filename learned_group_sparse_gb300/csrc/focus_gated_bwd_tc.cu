@@ -260,18 +260,6 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t *v)
                  : "memory");
 }
 
-// Stores 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
-__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v)
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15])
-        : "memory");
-}
-
 // tanh with the hardware approximation (relative error about 2^-11)
 __device__ __forceinline__ float bw_tanh(float x)
 {
@@ -602,34 +590,40 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 long long mtr[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // slots 8..15
                 int pt = -1, p_hi = 0;                 // the tile whose gradient products are next
                 bool p_gated = false, p_first = false, p_last = false;
-                auto grads = [&](int tt, bool gtd, bool first, bool last, int hi) -> bool {
+                // the gradient products of tile tt: dQ, or dV and dK, first ...
+                auto grads_main = [&](int tt, bool first, int hi) -> bool {
                     if (!mbar_wait_t(&bars[W_PFULL], tt & 1, abort_flag, a.status, trc,
-                                 mtr[BT_M_PFULL - 8]))
-                    return false;
+                                     mtr[BT_M_PFULL - 8]))
+                        return false;
                     if (SIDE == kSideQ && first && hi > 0 &&
                         !mbar_wait_t(&bars[W_ACCFREE], (hi - 1) & 1, abort_flag, a.status, trc,
-                                 mtr[BT_M_ACCFREE - 8]))
+                                     mtr[BT_M_ACCFREE - 8]))
                         return false;
                     tc_fence_after();
                     const uint32_t c1 = cb + (tt % NS) * (L::kStage >> 4);
-                    const uint32_t c2 = c1 + (L::kColT >> 4), cg = c2 + (L::kColT >> 4);
+                    const uint32_t c2 = c1 + (L::kColT >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
-                        // A: 32 bytes further along the rows; B: 16 rows of 128 bytes further
-                        const uint32_t ao = kk * 2, bo = kk * 128;
-                        // operands in TMEM: 16 rows of the streamed tile = 8 columns per step
+                        // operands in TMEM: 16 rows of the streamed tile = 8 columns
+                        // per step; B: 16 rows of 128 bytes further
+                        const uint32_t bo = kk * 128;
                         if (SIDE == kSideQ) {
                             const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
-                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutTm + kk * 8, c1 + bo,
-                                                   kIdAcc, acc);
+                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutTm + kk * 8,
+                                                   c1 + bo, kIdAcc, acc);
                         } else {
                             const uint32_t acc = (kk > 0 || tt > 0) ? 1u : 0u;
-                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutPm + kk * 8, c2 + bo,
-                                                   kIdAcc, acc);
+                            tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc, tmem + L::kOutPm + kk * 8,
+                                                   c2 + bo, kIdAcc, acc);
                             tc_mma_bf16_ts_lo<kHi>(tmem + L::kAcc + D, tmem + L::kOutTm + kk * 8,
                                                    c1 + bo, kIdAcc, acc);
                         }
                     }
+                    return true;
+                };
+                // ... then dG and the releases
+                auto grads_tail = [&](int tt, bool gtd, bool last) {
+                    const uint32_t cg = cb + (tt % NS) * (L::kStage >> 4) + 2 * (L::kColT >> 4);
                     if (gtd) {
 #pragma unroll
                         for (int kk = 0; kk < BC / 16; ++kk) {
@@ -638,14 +632,18 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                 tc_mma_bf16_ts_lo<kHi>(tmem + L::kAccG, tmem + L::kOutAm + kk * 8,
                                                        cg + kk * 128, kIdG, acc);
                             else
-                                bw_mma<kHi, kHi>(tmem + L::kAccG, outA + kk * 2, cg + kk * 128, kIdG,
-                                                 acc);
+                                bw_mma<kHi, kHi>(tmem + L::kAccG, outA + kk * 2, cg + kk * 128,
+                                                 kIdG, acc);
                         }
                         dg_started = true;
                     }
                     tc_commit(&bars[W_PEMPTY]);
                     tc_commit(&bars[W_CEMPTY + tt % NS]);
                     if (SIDE == kSideQ && last) tc_commit(&bars[W_ACCDONE]);
+                };
+                auto grads = [&](int tt, bool gtd, bool first, bool last, int hi) -> bool {
+                    if (!grads_main(tt, first, hi)) return false;
+                    grads_tail(tt, gtd, last);
                     return true;
                 };
                 for (int hi = 0; ok && hi < nh; ++hi) {
@@ -687,12 +685,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                         };
                         if constexpr (L::kAOut) {
                             // A's columns hold the previous tile's P and dT until its
-                            // gradient products are issued; the tensor pipe runs in
-                            // issue order
-                            if (pt >= 0) ok = grads(pt, p_gated, p_first, p_last, p_hi);
+                            // dV and dK products are issued (the tensor pipe runs in
+                            // issue order); its dG product, on da in shared memory,
+                            // follows the signal
+                            if (pt >= 0) ok = grads_main(pt, p_first, p_hi);
                             if (!ok) break;
                             issue_a();
                             tc_commit(&bars[W_SFULL]);
+                            if (pt >= 0) grads_tail(pt, p_gated, p_last);
                         } else {
                             issue_a();
                             tc_commit(&bars[W_SFULL]);
