@@ -29,7 +29,6 @@ namespace focus {
 namespace {
 
 constexpr int kGT = 64;               // d lambda partials: at most one per 64 query rows
-constexpr int kGHeadChunk = 4;        // query heads per query-side CTA (one dG partial each)
 
 struct GatedArgs {
     const __nv_bfloat16 *q, *k, *v;   // [B, n, Hq | Hkv, D]
@@ -136,7 +135,7 @@ size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg)
     const size_t a256 = 255;
     const int kp = (Kg + 15) / 16 * 16;
     const int nqt = (n + kGT - 1) / kGT;
-    const int nhc = (Hq + kGHeadChunk - 1) / kGHeadChunk;
+    const int nhc = (Hq + kGatedHeadChunk - 1) / kGatedHeadChunk;
     const size_t npad = ((size_t)n + 127) / 128 * 128;
     return (((size_t)B * n * kp * 2 + a256) & ~a256) +
            (((size_t)2 * B * Hq * npad * 4 + a256) & ~a256) +
@@ -177,11 +176,11 @@ GatedArgs gated_args(const GatedLaunch &p, void *ws)
     a.npad = (p.n + 127) / 128 * 128;
     a.rowv = reinterpret_cast<const float *>(w);
     w += ((size_t)2 * p.B * p.Hq * a.npad * 4 + a256) & ~a256;
-    a.hc = kGHeadChunk < p.Hq ? kGHeadChunk : p.Hq;
+    a.hc = kGatedHeadChunk < p.Hq ? kGatedHeadChunk : p.Hq;
     a.nhc = (p.Hq + a.hc - 1) / a.hc;
     a.dlam_part = reinterpret_cast<float *>(w);
     const int nqt = (p.n + kGT - 1) / kGT;
-    w += ((size_t)p.B * ((p.Hq + kGHeadChunk - 1) / kGHeadChunk) * nqt * 4 + a256) & ~a256;
+    w += ((size_t)p.B * a.nhc * nqt * 4 + a256) & ~a256;
     a.dg_part = reinterpret_cast<float *>(w);
     return a;
 }

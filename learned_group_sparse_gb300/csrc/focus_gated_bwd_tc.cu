@@ -61,7 +61,6 @@ constexpr int kBwMma = kEwWarps + 1;
 // preflight checks.
 constexpr int kBwRegsEw = 96;
 constexpr int kBwRegsOther = 88;
-constexpr int kBwHeadChunk = 4;     // query heads per query-side CTA (one dG partial each)
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum {
@@ -1037,7 +1036,7 @@ cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *rowv, in
     a.nks = plan.kp / 16;
     a.Kg = p.Kg;
     a.window = std::min(p.window, p.n);   // i - j < n for every pair
-    a.hc = std::min(kBwHeadChunk, p.Hq);
+    a.hc = std::min(kGatedHeadChunk, p.Hq);
     a.nhc = (p.Hq + a.hc - 1) / a.hc;
     a.nqt = (p.n + kBR - 1) / kBR;
     a.scale = p.scale;
@@ -1084,7 +1083,7 @@ cudaError_t gated_bwd_tc_launch(const GatedBwTcPlan &plan, const float *rowv, in
 
 int gated_bwd_tc_dlam_count(int B, int n, int Hq)
 {
-    const int hc = std::min(kBwHeadChunk, Hq);
+    const int hc = std::min(kGatedHeadChunk, Hq);
     return B * ((Hq + hc - 1) / hc) * ((n + kBR - 1) / kBR);
 }
 

@@ -191,6 +191,9 @@ struct GatedLaunch {
     WaitCtl wc;   // the forward kernel's bounded waits
 };
 size_t gated_ws_bytes(int B, int n, int Hq, int Hkv, int Kg);
+// Query heads per query-side CTA of the gated backward: one partial of the
+// row side of dG per chunk, in the workspace that gated_ws_bytes sizes.
+constexpr int kGatedHeadChunk = 4;
 // The tensor-core forward (focus_gated_tc.cu): its launch attributes and TMA
 // maps (gated_tc_prepare enqueues nothing), then the launch.  g16 is the
 // fp16 copy of G, [B, n, kp] with kp = K_g rounded up to 16.
