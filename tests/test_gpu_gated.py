@@ -66,6 +66,8 @@ CASES = [
     (1, 390, 3, 1, 128, 64, 100, 2.0),  # GQA 3:1 (odd: consecutive query tiles share a CTA)
     (2, 1100, 4, 2, 128, 64, 128, 2.5), # d 128, K_g 64 as in training: the streams wrap their
                                         # stage rings many times, two heads per key-side CTA
+    (1, 260, 4, 4, 64, 100, 40, 2.0),   # d 64 with K_g > 64: the key side keeps P and dT over
+                                        # the A product's TMEM columns
 ]
 
 
