@@ -356,16 +356,15 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
 {
     AttnLaunch &p = ap.p;
     const int B = ap.B, n = ap.n, K = ap.K, topk = ap.topk;
-    cudaError_t e;
-    if ((e = launch_plan(ap.offsets, B, K, !p.pair_heads, ap.tiles, ap.ntiles, s, launches)) !=
+    if (launch_plan(ap.offsets, B, K, !p.pair_heads, ap.tiles, ap.ntiles, s, launches) !=
         cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if ((e = launch_gather(static_cast<const __nv_bfloat16 *>(ap.Kt),
-                           static_cast<const __nv_bfloat16 *>(ap.V), ap.pos, ap.ids, B, n, topk,
-                           ap.Hkv, ap.d, ap.Kp, ap.Vp, ap.gidp, s, launches)) != cudaSuccess)
+    if (launch_gather(static_cast<const __nv_bfloat16 *>(ap.Kt),
+                      static_cast<const __nv_bfloat16 *>(ap.V), ap.pos, ap.ids, B, n, topk,
+                      ap.Hkv, ap.d, ap.Kp, ap.Vp, ap.gidp, s, launches) != cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if ((e = launch_mask_tables(ap.offsets, ap.gidp, ap.ids, B, n, K, topk, ap.mtab_g, ap.mtab_w,
-                                s, launches)) != cudaSuccess)
+    if (launch_mask_tables(ap.offsets, ap.gidp, ap.ids, B, n, K, topk, ap.mtab_g, ap.mtab_w, s,
+                           launches) != cudaSuccess)
         return FOCUS_ERR_CUDA;
 
     // the group kernel copies its query rows from Q itself (tmQ unused)
@@ -380,8 +379,8 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.grid = ap.grid_group;
     p.part_out16 = ap.Opart;
     p.part_meta_out = ap.Mpart;
-    if (q_ready && (e = cudaStreamWaitEvent(s, q_ready, 0)) != cudaSuccess) return FOCUS_ERR_CUDA;
-    if ((e = launch_attn_group(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (q_ready && cudaStreamWaitEvent(s, q_ready, 0) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (launch_attn_group(p, s, launches) != cudaSuccess) return FOCUS_ERR_CUDA;
 
     p.tmQ = &ap.wq;
     p.tmK = &ap.wk;
@@ -393,11 +392,10 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.grid = ap.grid_win;
     p.win_out16 = ap.Owin;
     p.win_meta_out = ap.Mwin;
-    if ((e = launch_attn_window(p, s, launches)) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (launch_attn_window(p, s, launches) != cudaSuccess) return FOCUS_ERR_CUDA;
 
-    if ((e = launch_merge(ap.Owin, ap.Mwin, ap.Opart, ap.Mpart, ap.inv, B, n, topk, ap.Hq, ap.d,
-                          static_cast<__nv_bfloat16 *>(ap.O), ap.lse, p.wc, s, launches)) !=
-        cudaSuccess)
+    if (launch_merge(ap.Owin, ap.Mwin, ap.Opart, ap.Mpart, ap.inv, B, n, topk, ap.Hq, ap.d,
+                     static_cast<__nv_bfloat16 *>(ap.O), ap.lse, p.wc, s, launches) != cudaSuccess)
         return FOCUS_ERR_CUDA;
     return FOCUS_OK;
 }
