@@ -145,10 +145,11 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  *   O_i = sum_{j in A_i} softmax_j(scale * q_i . k_j) v_j
  *   lse_i = ln sum_{j in A_i} exp(scale * q_i . k_j)
  *
- * Executed as three tcgen05/TMEM kernels: a causal attention over every
- * group's gathered members (a pair shared through several groups is counted
- * only in the lowest shared group), a sliding-window attention that skips
- * pairs sharing a group, and a log-sum-exp merge of the partial results.
+ * Executed as three tcgen05/TMEM kernels: a sliding-window attention over
+ * every pair with i - j < window, a causal attention over every group's
+ * gathered members that takes the pairs with i - j >= window (a pair shared
+ * through several groups is counted only in the lowest shared group), and a
+ * log-sum-exp merge of the partial results.
  *
  *   Q      [B, n, Hq, d]   bf16      K, V [B, n, Hkv, d] bf16
  *          query head h reads kv head h / (Hq / Hkv)
@@ -336,9 +337,7 @@ focus_status_t focus_dense_causal_fwd(const void *Q, const void *K, const void *
  * effective-FLOP accounting and the "every pair counted once" check.
  *   per_query [B, n] int64 out, nullable
  *   totals    [2]    int64 out (device): totals[0] = sum_i |A_i|,
- *                    totals[1] = number of pairs that share a group
- *                    (the pairs the group kernel scores; the rest are
- *                    window pairs scored by the window kernel).
+ *                    totals[1] = number of pairs that share a group.
  */
 focus_status_t focus_count_pairs(const int32_t *ids, const int32_t *offsets,
                                  const int32_t *pos, const int32_t *inv,

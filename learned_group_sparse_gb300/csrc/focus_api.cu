@@ -150,7 +150,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnWs {
-    size_t kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, mtab_g, mtab_w, total;
+    size_t kp, vp, gidp, opart, lpart, owin, lwin, tiles, ntiles, mtab_g, wlo, total;
 };
 
 int64_t max_tiles(int B, int n, int K, int topk)
@@ -174,7 +174,7 @@ AttnWs attn_ws(int B, int n, int Hq, int Hkv, int d, int K, int topk)
     w.tiles = off; off += align256((size_t)max_tiles(B, n, K, topk) * 8);
     w.ntiles = off; off += 256;
     w.mtab_g = off; off += align256((size_t)B * mask_tiles_group(n, K, topk) * K * 16);
-    w.mtab_w = off; off += align256((size_t)B * mask_tiles_window(n) * K * 16);
+    w.wlo = off;   off += align256((size_t)B * nk * 4);
     w.total = off;
     return w;
 }
@@ -255,7 +255,8 @@ struct AttnPrep {
     float2 *Mpart, *Mwin;
     int2 *tiles;
     int *ntiles;
-    uint4 *mtab_g, *mtab_w;
+    uint4 *mtab_g;
+    int32_t *wlo;
     CUtensorMap mk, mv, wq, wk, wv;
     AttnLaunch p;     // fields shared by the group and window launches
 };
@@ -317,7 +318,7 @@ focus_status_t attention_prepare(const void *Q, const void *Kt, const void *V, i
     ap->tiles = reinterpret_cast<int2 *>(base + w.tiles);
     ap->ntiles = reinterpret_cast<int *>(base + w.ntiles);
     ap->mtab_g = reinterpret_cast<uint4 *>(base + w.mtab_g);
-    ap->mtab_w = reinterpret_cast<uint4 *>(base + w.mtab_w);
+    ap->wlo = reinterpret_cast<int32_t *>(base + w.wlo);
     const int64_t nk = (int64_t)n * topk;
     if (!make_map(&ap->mk, ap->Kp, B, nk, Hkv, d) || !make_map(&ap->mv, ap->Vp, B, nk, Hkv, d) ||
         !make_map(&ap->wq, Q, B, n, Hq, d) || !make_map(&ap->wk, Kt, B, n, Hkv, d) ||
@@ -363,8 +364,8 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
                       static_cast<const __nv_bfloat16 *>(ap.V), ap.pos, ap.ids, B, n, topk,
                       ap.Hkv, ap.d, ap.Kp, ap.Vp, ap.gidp, s, launches) != cudaSuccess)
         return FOCUS_ERR_CUDA;
-    if (launch_mask_tables(ap.offsets, ap.gidp, ap.ids, B, n, K, topk, ap.mtab_g, ap.mtab_w, s,
-                           launches) != cudaSuccess)
+    if (launch_mask_tables(ap.offsets, ap.gidp, ap.ids, ap.pos, ap.inv, B, n, K, topk, p.window,
+                           ap.mtab_g, ap.wlo, s, launches) != cudaSuccess)
         return FOCUS_ERR_CUDA;
 
     // the group kernel copies its query rows from Q itself (tmQ unused)
@@ -376,6 +377,7 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.gids = ap.gidp;
     p.masks = ap.mtab_g;
     p.mask_tiles = mask_tiles_group(n, K, topk);
+    p.wlo = ap.wlo;
     p.grid = ap.grid_group;
     p.part_out16 = ap.Opart;
     p.part_meta_out = ap.Mpart;
@@ -386,9 +388,10 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.tmK = &ap.wk;
     p.tmV = &ap.wv;
     p.rows = n;
-    p.gids = ap.ids;
-    p.masks = ap.mtab_w;
-    p.mask_tiles = mask_tiles_window(n);
+    p.gids = nullptr;      // every pair of the window: no group masks
+    p.masks = nullptr;
+    p.mask_tiles = 0;
+    p.wlo = nullptr;
     p.grid = ap.grid_win;
     p.win_out16 = ap.Owin;
     p.win_meta_out = ap.Mwin;

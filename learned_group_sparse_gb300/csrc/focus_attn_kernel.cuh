@@ -38,10 +38,14 @@
 // gist.science/zh technical summary 2.1.3: within-group causal attention
 // plus cross-group local attention):
 //   kGroup  : query/key rows are one group's gathered members (ascending
-//             token order); causal in that order; a pair whose tokens share
-//             several groups is scored only in the lowest shared group.
-//   kWindow : original token order; keys with i - window < j <= i that share
-//             no group with the query.
+//             token order); causal in that order and outside the window
+//             (i - j >= window); a pair whose tokens share several groups is
+//             scored only in the lowest shared group.
+//   kWindow : original token order; every key with i - window < j <= i.
+// The two modes split the allowed set without overlap: the window pairs all
+// go to kWindow, which then needs no group masks, and kGroup leaves them out
+// with one bound per row (the window holds few of a group's members, so that
+// bound cuts into one or two key tiles of an item).
 //   kDense  : plain causal attention (the comparison baseline).
 // kGroup and kWindow write partial results: the normalised output of every
 // (row, head) in fp16, scaled by a power of two 2^-e that puts its largest
@@ -49,12 +53,11 @@
 // {base-2 log-sum-exp, 2^e}.  The merge kernel combines them.  kDense writes
 // its final bf16 output directly.
 //
-// Group masks: for every key tile a bulk copy brings colbits[g][4], the set
-// of the tile's 128 key columns whose token belongs to group g, from a table
-// that the mask-table kernel writes before the attention kernels run.  A query row
-// excludes the columns in the union of colbits over the groups that must not
-// be shared (all its groups for kWindow; its groups below the tile's group
-// for kGroup): k lookups of 16 bytes instead of a test per column.
+// Group masks (kGroup): for every key tile a bulk copy brings colbits[g][4],
+// the set of the tile's 128 key columns whose token belongs to group g, from a
+// table that the mask-table kernel writes before the attention kernels run.  A
+// query row excludes the columns in the union of colbits over its groups below
+// the tile's group: k lookups of 16 bytes instead of a test per column.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -84,10 +87,11 @@ struct AttnArgs {
     const int *ntiles;     // kGroup: number of valid entries in tiles
     const __nv_bfloat16 *q;  // kGroup: the original Q [B, n, Hq, D]; its rows are
                              // copied into the query tiles through pos
-    const uint4 *masks;    // group bitmaps of the key tiles: [B][mask_tiles][K],
+    const uint4 *masks;    // kGroup: group bitmaps of the key tiles: [B][mask_tiles][K],
                            // word j bit c = key 32 j + c of the tile is in the group
-    int64_t mask_tiles;    // slots per batch (group tile u of g: off[g] / 128 + g + u;
-                           // window tile: first key row / 128)
+    int64_t mask_tiles;    // slots per batch (group tile u of g: off[g] / 128 + g + u)
+    const int32_t *wlo;    // kGroup: [B, rows] the first row of each row's group
+                           // inside its window; keys from there on are kWindow's
     __nv_bfloat16 *out;    // kDense: O [B, n, Hq, D]
     float *lse;            // kDense: lse [B, Hq, n], natural log (nullable)
     // partial results: O / l as fp16 scaled by 2^-e, and {lse base 2, 2^e}
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_4d(sV + st * L::kTile + c * 16384, &tmV, &bars[B_VFULL + st],
                                         c * 64, kvh, r0, w.b);
                     }
-                    if (MODE != kDense && lane == 0) {
+                    if (MODE == kGroup && lane == 0) {
                         // colbits[st] <- the tile's group bitmaps
                         mbar_arrive_expect_tx(&bars[B_META + st], 16u * (uint32_t)a.K);
                         bulk_load(colbits + (size_t)st * a.K * 4, a.masks + (mslot + u) * a.K,
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     while (!mbar_try_wait(&bars[B_VFULL + st], (t >> 1) & 1) &&
                            global_timer_ns() - t0 < 300000000ull) {
                     }
-                    while (MODE != kDense && !mbar_try_wait(&bars[B_META + st], (t >> 1) & 1) &&
+                    while (MODE == kGroup && !mbar_try_wait(&bars[B_META + st], (t >> 1) & 1) &&
                            global_timer_ns() - t0 < 400000000ull) {
                     }
                 }
@@ -754,18 +758,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int prow = q0 + r;                     // row in the Q tensor
             const bool qvalid = prow < qend;
             int qi = prow;                               // token index of the row
-            // Groups whose columns this row must not score: every group of the
-            // row (kWindow), or the row's groups below the tile's group (kGroup).
+            // kGroup: the groups whose columns this row must not score (the
+            // row's groups below the tile's group), and its last key row
+            // outside the window.
             int qg[kMaxTopk];          // -1 = unused slot
 #pragma unroll
             for (int s = 0; s < kMaxTopk; ++s) {
                 qg[s] = -1;
-                if (MODE != kDense && qvalid && s < a.topk) {
+                if (MODE == kGroup && qvalid && s < a.topk) {
                     const int gi = a.gids[((int64_t)wb * a.rows + prow) * a.topk + s];
-                    if ((MODE == kWindow || gi < wg) && (unsigned)gi < (unsigned)a.K)
+                    if (gi < wg && (unsigned)gi < (unsigned)a.K)
                         qg[s] = gi;
                 }
             }
+            const int hib = (MODE == kGroup && qvalid)
+                                ? min(prow, a.wlo[(int64_t)wb * a.rows + prow] - 1)
+                                : prow;
             if (MODE == kGroup && qvalid && a.pair_count)
                 qi = a.pos[(int64_t)wb * a.rows + prow];
             const bool count_ok = (unsigned)qi < (unsigned)a.n;
@@ -805,13 +813,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile t gives that order instead: the MMA thread issues both
                 // P.V of t-2 before either Q.K^T of t, so a softmax has finished
                 // t-2 by the time S_h(t) is complete.
-                const bool early = MODE != kDense && u >= ulo + 2;
+                const bool early = MODE == kGroup && u >= ulo + 2;
                 ok = !early || fetch_ex();
                 if (ok)
                     ok = mbar_wait_t(&bars[B_SFULL + hh], ns & 1, abort_flag, a.status, trc,
                                      tr[TR_S_SFULL]);
                 ++ns;
-                if (ok && MODE != kDense && !early) ok = fetch_ex();
+                if (ok && MODE == kGroup && !early) ok = fetch_ex();
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -831,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!qvalid)
                         bits = 0u;
                     else if (MODE == kGroup)
-                        bits = range_bits(0, prow - kvb, 32 * j);          // causal, group order
+                        bits = range_bits(0, hib - kvb, 32 * j);   // causal, outside the window
                     else if (MODE == kWindow)
                         bits = range_bits(qi - a.window + 1 - kvb, qi - kvb, 32 * j);
                     else

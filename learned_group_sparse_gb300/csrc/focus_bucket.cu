@@ -332,62 +332,100 @@ __global__ void __launch_bounds__(256) gather_kernel(
 }
 
 // ---------------------------------------------------------------- mask tables
-// Group bitmaps of the attention kernels' key tiles, one [K] uint4 entry per
+// Group bitmaps of the group kernel's key tiles, one [K] uint4 entry per
 // tile: word j of entry g has bit c set when key row 32 j + c of the tile
 // belongs to group g.  The softmax excludes a key by OR-ing the entries of
-// the query's excluded groups (the allowed set of the technical summary's
-// section 2.1.2 with each shared pair scored once).
+// the query's groups below the tile's group, so that a pair sharing several
+// groups is scored in the lowest of them (the allowed set of the technical
+// summary's section 2.1.2 with each shared pair scored once).
 //
-// Window tiles: 128 consecutive tokens, slot t = rows [128 t, 128 t + 128).
 // Group tiles: 128 consecutive group-order rows from the start of group g,
 // tile u at slot floor(off[g] / 128) + g + u.  That slot map needs no scan and
 // never overlaps the next group: floor(a + s) - floor(a) + 1 >= ceil(s) for
 // a = off[g] / 128, s = size_g / 128.  Slots past a group's last tile are
 // never read and are left unwritten.
+//
+// Window bounds: the window kernel takes every pair with i - j < w, so the
+// group kernel takes, of the keys sharing a group with query i, only those
+// with i - j >= w.  A group's members are in ascending token order, so for the
+// group-order row r of (i, g) those keys are the rows [off[g], wlo[r]), where
+// wlo[r] is the first row of the group whose token lies inside i's window
+// (r + 1 at w = 0).  Found by a backward galloping search from r: the
+// window holds few of a group's members.
 __global__ void __launch_bounds__(128) mask_table_kernel(
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ gidp,
-    const int32_t *__restrict__ ids, int n, int64_t nk, int K, int topk, int64_t ntg,
-    int64_t ntw, int64_t nblk_g, uint4 *__restrict__ tab_g, uint4 *__restrict__ tab_w)
+    const int32_t *__restrict__ ids, const int32_t *__restrict__ pos,
+    const int32_t *__restrict__ inv, int n, int64_t nk, int K, int topk, int window,
+    int64_t ntg, int64_t nblk_g, uint4 *__restrict__ tab_g, int32_t *__restrict__ wlo)
 {
     grid_dep_sync();
-    extern __shared__ uint32_t bm[];   // [K][4]
-    __shared__ int cnt;
     const int tid = threadIdx.x;
     const int64_t blk = blockIdx.x;
-    int64_t r0, rend;
-    const int32_t *src;
-    uint4 *dst;
-    if (blk < nblk_g) {
-        const int64_t b = blk / ntg, slot = blk - b * ntg;
-        const int32_t *off = offsets + b * (K + 1);
-        // g = the last group whose first slot is <= slot (slots rise with g)
-        if (tid == 0) cnt = 0;
-        __syncthreads();
-        int c = 0;
-        for (int g = tid; g < K; g += 128) c += ((int64_t)(off[g] >> 7) + g <= slot) ? 1 : 0;
-        if (c) atomicAdd(&cnt, c);
-        __syncthreads();
-        const int g = cnt - 1;
-        r0 = off[g] + 128 * (slot - ((off[g] >> 7) + g));
-        rend = off[g + 1];
-        if (r0 >= rend) return;   // not a tile of group g (uniform over the block)
-        src = gidp + b * nk * topk;
-        dst = tab_g + (b * ntg + slot) * K;
-    } else {
+    if (blk >= nblk_g) {
+        // window bounds of the rows of tokens [128 t, 128 t + 128)
         const int64_t wb = blk - nblk_g;
-        const int64_t b = wb / ntw, t = wb - b * ntw;
-        r0 = 128 * t;
-        rend = n;
-        src = ids + b * (int64_t)n * topk;
-        dst = tab_w + wb * K;
+        const int64_t ntw = ((int64_t)n + 127) / 128;
+        const int64_t b = wb / ntw;
+        const int i = (int)(128 * (wb - b * ntw)) + tid;
+        if (i >= n) return;
+        const int32_t *off = offsets + b * (K + 1);
+        const int32_t *pb = pos + b * nk;
+        for (int s = 0; s < topk; ++s) {
+            const int64_t q = (b * n + i) * topk + s;
+            const int g = ids[q];
+            const int r = inv[q];
+            if ((unsigned)g >= (unsigned)K || (int64_t)(unsigned)r >= nk) continue;
+            int t = r + 1;
+            if (window > 0) {
+                // pb[r] = i > i - w: find the first row m in [off[g], r] with
+                // pb[m] > i - w, i.e. lo < m <= hi with pb[lo] <= i - w
+                const int thr = i - window, seg = off[g];
+                int hi = r, lo = seg - 1;
+                for (int64_t step = 1; (int64_t)hi - step >= seg; step <<= 1) {
+                    const int m = (int)(hi - step);
+                    if (pb[m] <= thr) {
+                        lo = m;
+                        break;
+                    }
+                    hi = m;
+                }
+                while (hi - lo > 1) {
+                    const int m = lo + (hi - lo) / 2;
+                    if (pb[m] > thr)
+                        hi = m;
+                    else
+                        lo = m;
+                }
+                t = hi;
+            }
+            wlo[b * nk + r] = t;
+        }
+        return;
     }
+    extern __shared__ uint32_t bm[];   // [K][4]
+    __shared__ int cnt;
+    const int64_t b = blk / ntg, slot = blk - b * ntg;
+    const int32_t *off = offsets + b * (K + 1);
+    // g = the last group whose first slot is <= slot (slots rise with g)
+    if (tid == 0) cnt = 0;
+    __syncthreads();
+    int c = 0;
+    for (int g = tid; g < K; g += 128) c += ((int64_t)(off[g] >> 7) + g <= slot) ? 1 : 0;
+    if (c) atomicAdd(&cnt, c);
+    __syncthreads();
+    const int g = cnt - 1;
+    const int64_t r0 = off[g] + 128 * (slot - ((off[g] >> 7) + g));
+    const int64_t rend = off[g + 1];
+    if (r0 >= rend) return;   // not a tile of group g (uniform over the block)
+    const int32_t *src = gidp + b * nk * topk;
+    uint4 *dst = tab_g + (b * ntg + slot) * K;
     for (int i = tid; i < 4 * K; i += 128) bm[i] = 0u;
     __syncthreads();
     const int64_t row = r0 + tid;
     if (row < rend) {
         for (int s = 0; s < topk; ++s) {
-            const int g = src[row * topk + s];
-            if ((unsigned)g < (unsigned)K) atomicOr(&bm[g * 4 + (tid >> 5)], 1u << (tid & 31));
+            const int gg = src[row * topk + s];
+            if ((unsigned)gg < (unsigned)K) atomicOr(&bm[gg * 4 + (tid >> 5)], 1u << (tid & 31));
         }
     }
     __syncthreads();
@@ -402,20 +440,19 @@ int64_t mask_tiles_group(int n, int K, int topk)
     return ((int64_t)n * topk + 127) / 128 + K;
 }
 
-int64_t mask_tiles_window(int n) { return ((int64_t)n + 127) / 128; }
-
 cudaError_t launch_mask_tables(const int32_t *offsets, const int32_t *gidp, const int32_t *ids,
-                               int B, int n, int K, int topk, uint4 *tab_g, uint4 *tab_w,
-                               cudaStream_t s, int *launches)
+                               const int32_t *pos, const int32_t *inv, int B, int n, int K,
+                               int topk, int window, uint4 *tab_g, int32_t *wlo, cudaStream_t s,
+                               int *launches)
 {
     const int64_t nk = (int64_t)n * topk;
-    const int64_t ntg = mask_tiles_group(n, K, topk), ntw = mask_tiles_window(n);
+    const int64_t ntg = mask_tiles_group(n, K, topk), ntw = ((int64_t)n + 127) / 128;
     const int64_t blocks = (int64_t)B * (ntg + ntw);
     if (n == 0 || blocks <= 0) return cudaSuccess;
     prof_begin("mask_table", s);
-    const cudaError_t e =
-        launch_pdl(mask_table_kernel, dim3((unsigned)blocks), dim3(128), (size_t)K * 16, s,
-                   offsets, gidp, ids, n, nk, K, topk, ntg, ntw, (int64_t)B * ntg, tab_g, tab_w);
+    const cudaError_t e = launch_pdl(mask_table_kernel, dim3((unsigned)blocks), dim3(128),
+                                     (size_t)K * 16, s, offsets, gidp, ids, pos, inv, n, nk, K,
+                                     topk, window, ntg, (int64_t)B * ntg, tab_g, wlo);
     prof_end(s);
     *launches += 1;
     return e;

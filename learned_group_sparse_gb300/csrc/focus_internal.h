@@ -144,15 +144,16 @@ cudaError_t launch_gather(const __nv_bfloat16 *K, const __nv_bfloat16 *V, const 
                           __nv_bfloat16 *Kp, __nv_bfloat16 *Vp, int32_t *gidp, cudaStream_t s,
                           int *launches);
 // Group bitmaps of every key tile of the group kernel (tab_g, mask_tiles_group
-// slots per batch) and of the window kernel (tab_w, mask_tiles_window slots per
-// batch): [slot][K] uint4, word j bit c = key row 32 j + c of the tile is in
-// the group.  Group tile u of group g is slot floor(off[g] / 128) + g + u;
-// window tile t (rows [128 t, 128 t + 128)) is slot t.
+// slots per batch): [slot][K] uint4, word j bit c = key row 32 j + c of the
+// tile is in the group; group tile u of group g is slot floor(off[g] / 128) +
+// g + u.  And the window bound of every group-order row (wlo [B, n*topk]): the
+// first row of its group whose token lies inside the row's window (its own row
+// + 1 at window 0); the group kernel scores the keys before it.
 int64_t mask_tiles_group(int n, int K, int topk);
-int64_t mask_tiles_window(int n);
 cudaError_t launch_mask_tables(const int32_t *offsets, const int32_t *gidp, const int32_t *ids,
-                               int B, int n, int K, int topk, uint4 *tab_g, uint4 *tab_w,
-                               cudaStream_t s, int *launches);
+                               const int32_t *pos, const int32_t *inv, int B, int n, int K,
+                               int topk, int window, uint4 *tab_g, int32_t *wlo, cudaStream_t s,
+                               int *launches);
 cudaError_t launch_count_pairs(const int32_t *ids, const int32_t *offsets, const int32_t *pos,
                                const int32_t *inv, int B, int n, int K, int topk, int window,
                                int64_t *per_query, int64_t *totals, cudaStream_t s,
@@ -243,8 +244,9 @@ struct AttnLaunch {
     const int2 *tiles;
     const int *ntiles;
     const __nv_bfloat16 *q;  // kGroup: the original Q, whose rows the kernel gathers
-    const uint4 *masks;      // key-tile group bitmaps of this launch's mode
+    const uint4 *masks;      // kGroup: key-tile group bitmaps
     int64_t mask_tiles;      // mask slots per batch
+    const int32_t *wlo;      // kGroup: window bound of each group-order row
     int64_t grid;
     __nv_bfloat16 *out;
     float *lse;

@@ -1,9 +1,9 @@
 // Log-sum-exp merge of the partial attention results.
 //
 // The allowed set of query i (gist.science/zh technical summary 2.1.2-2.1.3)
-// is split without overlap into the window keys that share no group with i
-// (window kernel) and the keys sharing a group, each scored in the lowest
-// shared group (group kernel).  The exact softmax over the union
+// is split without overlap into the window keys j > i - w (window kernel) and
+// the keys sharing a group with j <= i - w, each scored in the lowest shared
+// group (group kernel).  The exact softmax over the union
 // (gist.science/nl Kerncomponent 3) is the base-2 log-sum-exp combination of
 // the k + 1 normalised partials:
 //   L = log2 sum_p 2^{L_p},  O = sum_p 2^{L_p - L} O_p.
