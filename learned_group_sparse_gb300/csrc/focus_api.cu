@@ -378,6 +378,7 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.masks = ap.mtab_g;
     p.mask_tiles = mask_tiles_group(n, K, topk);
     p.wlo = ap.wlo;
+    p.work = ap.ntiles + 1;    // zeroed by the plan kernel
     p.grid = ap.grid_group;
     p.part_out16 = ap.Opart;
     p.part_meta_out = ap.Mpart;
@@ -392,6 +393,7 @@ focus_status_t attention_enqueue(AttnPrep &ap, cudaStream_t s, int *launches,
     p.masks = nullptr;
     p.mask_tiles = 0;
     p.wlo = nullptr;
+    p.work = ap.ntiles + 2;    // zeroed by the plan kernel
     p.grid = ap.grid_win;
     p.win_out16 = ap.Owin;
     p.win_meta_out = ap.Mwin;

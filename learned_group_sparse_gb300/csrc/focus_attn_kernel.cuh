@@ -29,10 +29,14 @@
 // TMEM columns: S_0 [0,128), S_1 [128,256) (P_h over the first 64 columns of
 // S_h, two bf16 keys per column), O_0 [256, 256+D), O_1 [384, 384+D).
 //
-// Persistent: one CTA per SM walks the work items item = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  The pipeline (K/V stages, barrier phases) runs
-// on across items, so the next item's loads and first Q.K^T overlap the
-// current item's softmax and epilogue.
+// Persistent: one CTA per SM runs work items one after another.  Its
+// producer takes the next item from a counter (group and window kernels: the
+// list is ordered by decreasing cost, so a CTA that is ahead takes more of the
+// cheap items at its end) or from a fixed share of the list (dense kernel),
+// and publishes it in a two-slot ring that the other roles read, an end mark
+// after the last.  The pipeline (K/V stages, barrier phases) runs on across
+// items, so the next item's loads and first Q.K^T overlap the current item's
+// softmax and epilogue.
 //
 // Modes (the decomposition of the allowed-pair set of Focus attention,
 // gist.science/zh technical summary 2.1.3: within-group causal attention
@@ -99,6 +103,9 @@ struct AttnArgs {
     float2 *part_meta_out; // kGroup  [B, rows, Hq]
     __half *win_out16;     // kWindow [B, n, Hq, D]
     float2 *win_meta_out;  // kWindow [B, n, Hq]
+    int *work;             // nullable: work-item counter, zero before the launch; the
+                           // producers take items from it in list order (null: CTA c
+                           // takes items c, 2G - 1 - c, 2G + c, ... of G CTAs)
     int *status;           // device status word
     int32_t *pair_count;   // nullable: scored pairs per query (head 0)
     long long *trace;      // nullable: per-CTA wait/phase cycle counters [grid][32]
@@ -179,8 +186,11 @@ __device__ __forceinline__ int *ring_slot(uint8_t *sm, int K, int slot)
     return reinterpret_cast<int *>(sm + L::kColbits + L::colbits_bytes(K) + slot * L::kRingSlot);
 }
 
-__device__ __forceinline__ void put_item(int *p, const Item &w)
+// p[15]: the item's index, or -1 for "no more items" (the other fields unset).
+__device__ __forceinline__ void put_item(int *p, const Item &w, int item)
 {
+    p[15] = item;
+    if (item < 0) return;
     p[0] = w.b;
     p[1] = w.g;
     p[2] = w.gend;
@@ -368,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = AttnSmem<D>;
     constexpr int kChunks = D / 64;   // 64-column (128-byte) chunks per row
 
+    // kGroup's work-list length is written by an earlier kernel on the stream
+    if (MODE == kGroup) grid_dep_sync();
     const int nitems = total_items<MODE>(a);
     if ((int)blockIdx.x >= nitems) return;       // whole CTA leaves before any set-up
     const int kv_per_q = a.Hq / a.Hkv;
@@ -438,10 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int T = 0;                    // key tiles issued so far
             int iq[2] = {0, 0};           // query tiles loaded per half
             bool ok = true;
-            for (int k = 0, item = blockIdx.x; ok && item < nitems;
-                 item = item_of(++k, blockIdx.x, gridDim.x)) {
-                // ---- publish the decoded item and its rows' group ids (ring slot
-                // k & 1, free once item k - 2 is fully consumed)
+            for (int k = 0; ok; ++k) {
+                // ---- take the next item and publish it decoded (ring slot k & 1,
+                // free once item k - 2 is fully consumed); past the list's end,
+                // an end mark that stops the other roles
                 if (k >= 2 && lane == 0)
                     ok = mbar_wait_t(&bars[B_IEMPTY + (k & 1)], ((k >> 1) - 1) & 1, abort_flag,
                                      a.status, trc, tr[TR_P_IEMPTY]);
@@ -450,13 +462,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const long long t_ring = trc ? clock64() : 0;
-                const Item w = decode_item<MODE>(a, item);
+                int item = 0;
+                if (lane == 0)
+                    item = a.work ? atomicAdd(a.work, 1) : item_of(k, blockIdx.x, gridDim.x);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                const bool more = item < nitems;
+                Item w;
+                w.nkv = 0;
+                if (more) w = decode_item<MODE>(a, item);
                 {
-                    if (lane == 0) put_item(ring_slot<D>(sm, a.K, k & 1), w);
+                    if (lane == 0) put_item(ring_slot<D>(sm, a.K, k & 1), w, more ? item : -1);
                     __syncwarp();
                     mbar_arrive(&bars[B_IFULL + (k & 1)]);
                     if (trc) tr[TR_P_RING] += clock64() - t_ring;
                 }
+                if (!more) break;
                 if (w.nkv == 0) continue;
                 const int kvh = w.hd[0] / kv_per_q;
                 // Q_h: its buffer is free once the last Q_h.K^T of its previous
@@ -569,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int iq[2] = {0, 0};            // Q loads consumed per half
                 int np[2] = {0, 0};            // P.V products issued per half
                 bool ok = true;
-                for (int k = 0, item = blockIdx.x; ok && item < nitems;
-                     item = item_of(++k, blockIdx.x, gridDim.x)) {
+                for (int k = 0; ok; ++k) {
                     ok = mbar_wait_t(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status,
                                      trc, c_if);
                     if (!ok) break;
                     const int *wi = ring_slot<D>(sm, a.K, k & 1);   // Item fields
+                    if (wi[15] < 0) break;                           // no more items
                     const int nkv = wi[4];
                     const int ulo[2] = {wi[11], wi[12]}, uhi[2] = {wi[13], wi[14]};
                     mbar_arrive(&bars[B_IEMPTY + (k & 1)]);
@@ -683,8 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int h = warp - 10;
             int iq = 0;    // query tiles loaded
             bool ok = true;
-            for (int k = 0, item = blockIdx.x; ok && item < nitems;
-                 item = item_of(++k, blockIdx.x, gridDim.x)) {
+            for (int k = 0; ok; ++k) {
                 if (lane == 0)
                     ok = mbar_wait(&bars[B_IFULL + (k & 1)], (k >> 1) & 1, abort_flag, a.status);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -692,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int *wi = ring_slot<D>(sm, a.K, k & 1);   // Item fields
+                if (wi[15] < 0) break;                           // no more items
                 const int wb = wi[0], nkv = wi[4], hd = wi[5 + h], q0 = wi[7 + h];
                 const int qend = wi[9 + h], ulo = wi[11 + h], uhi = wi[13 + h];
                 __syncwarp();
@@ -742,8 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ns = 0;         // S_h tiles consumed
         int nod = 0;        // items of this half with tiles (O_h completions)
         bool ok = true;
-        for (int k = 0, item = blockIdx.x; ok && item < nitems;
-             item = item_of(++k, blockIdx.x, gridDim.x)) {
+        for (int k = 0; ok; ++k) {
             const int slot = k & 1;
             ok = mbar_wait_t(&bars[B_IFULL + slot], (k >> 1) & 1, abort_flag, a.status, trc,
                              tr[TR_S_IFULL]);
@@ -752,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const int *wi = ring_slot<D>(sm, a.K, slot);   // the fields of Item
+            if (wi[15] < 0) break;                         // no more items
             const int wb = wi[0], wg = wi[1], kv_lo = wi[3], nkv = wi[4];
             const int hd = wi[5 + hh], q0 = wi[7 + hh], qend = wi[9 + hh];
             const int ulo = wi[11 + hh], uhi = wi[13 + hh];

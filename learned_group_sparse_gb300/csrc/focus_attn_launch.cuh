@@ -64,6 +64,7 @@ cudaError_t launch_attn_impl(const AttnLaunch &p, cudaStream_t s, int *launches)
     a.masks = p.masks;
     a.mask_tiles = p.mask_tiles;
     a.wlo = p.wlo;
+    a.work = p.work;
     a.out = p.out;
     a.lse = p.lse;
     a.part_out16 = p.part_out16;

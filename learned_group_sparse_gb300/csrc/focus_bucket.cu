@@ -279,7 +279,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     __syncthreads();
     const long long total = pref[G];
     const int Tmax = G > 0 ? max(keyT[0], 0) : 0;
-    if (tid == 0) *ntiles = (int)total;
+    if (tid == 0) {
+        ntiles[0] = (int)total;
+        ntiles[1] = 0;   // work counters of the group and window kernels
+        ntiles[2] = 0;
+    }
     // S(t) = tiles in layers above t = pref[c(t)] - c(t) * (t + 1)
     for (long long p = tid; p < total; p += 1024) {
         int lo = 0, hi = Tmax - 1;   // smallest t with S(t) <= p

@@ -134,7 +134,9 @@ cudaError_t launch_bucket(const int32_t *ids, int B, int n, int K, int topk, int
 // ---- attention helpers
 // Work list of the group kernel ordered by decreasing cost: entries (b*K + g, t)
 // for the 128-row query tiles t of every group, or, with pair_tiles, for the
-// pairs of consecutive tiles (2t, 2t+1).
+// pairs of consecutive tiles (2t, 2t+1).  ntiles[0] = the list's length;
+// ntiles[1] and ntiles[2] are set to 0: the work counters from which the group
+// and window kernels' CTAs take their items.
 cudaError_t launch_plan(const int32_t *offsets, int B, int K, int pair_tiles, int2 *tiles,
                         int *ntiles, cudaStream_t s, int *launches);
 // Kp[b][r] = K[b][pos[b][r]] and Vp likewise: rows of Hkv*d bf16;
@@ -247,6 +249,7 @@ struct AttnLaunch {
     const uint4 *masks;      // kGroup: key-tile group bitmaps
     int64_t mask_tiles;      // mask slots per batch
     const int32_t *wlo;      // kGroup: window bound of each group-order row
+    int *work;               // nullable: work-item counter, zero before the launch
     int64_t grid;
     __nv_bfloat16 *out;
     float *lse;
