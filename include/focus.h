@@ -164,9 +164,9 @@ focus_status_t focus_bucket_static(const int32_t *ids, int B, int n, int K, int 
  * rounded to bf16 for the P.V product, partial outputs kept in fp16 with a
  * power-of-two scale per row (11-bit significand at any magnitude).
  * Supported: d in {64, 128}, Hq % Hkv == 0, 1 <= topk <= 8,
- *            1 <= K <= 1024 (the kernels' shared memory holds the group
- *            bitmaps of two key tiles, 16 K bytes each, next to the Q/K/V
- *            tiles), B * K <= 4096 (the work list is sorted by one
+ *            1 <= K <= 1024 (the group kernel's shared memory holds the
+ *            group bitmaps of two key tiles, 16 K bytes each, next to the
+ *            Q/K/V tiles), B * K <= 4096 (the work list is sorted by one
  *            block with every group of every batch in shared memory).
  *            Otherwise FOCUS_ERR_UNSUPPORTED.
  */
