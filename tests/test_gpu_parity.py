@@ -60,6 +60,8 @@ ATTN_CASES = [
     (1, 2300, 3, 3, 64, 12, 3, 300),      # odd number of query tiles per head
     (1, 600, 2, 2, 128, 1024, 8, 96),     # the largest K and topk at d = 128
     (4, 300, 2, 2, 64, 1024, 2, 16),      # B * K at its limit (4096), most groups empty
+    (1, 1500, 2, 2, 128, 4, 2, 700),      # a row's window holds ~350 members of its groups:
+                                          # the group kernel's window bound spans key tiles
 ]
 
 
@@ -154,8 +156,13 @@ def test_assign_matches_oracle(w):
     np.testing.assert_allclose(margin.cpu().numpy()[sure], rmargin[sure], atol=5e-5, rtol=1e-4)
 
 
+# (the window kernel takes every pair with i - j < w, the group kernel the
+# shared pairs further back: w = 300 with 6 groups over 700 tokens puts about
+# a hundred members of each group inside a row's window, so the group
+# kernel's window bound masks whole key tiles; w > n leaves it nothing)
 @pytest.mark.parametrize("case", [(1, 700, 6, 2, 40), (2, 1000, 64, 2, 256), (1, 600, 128, 4, 16),
-                                  (1, 300, 5, 5, 3), (1, 260, 9, 1, 0)])
+                                  (1, 300, 5, 5, 3), (1, 260, 9, 1, 0), (1, 700, 6, 2, 300),
+                                  (2, 900, 3, 2, 1000)])
 def test_every_allowed_pair_scored_exactly_once(case):
     B, n, K, topk, window = case
     ids_np = rand_ids(B, n, K, topk, seed=n * 3 + K)
